@@ -1,0 +1,348 @@
+"""Throughput of the gated delta rule on GB300 (tokens/s), one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one forward pass (gdn_fwd, every forward row of the chunked
+recurrence) over one batch of the named workload, inputs already resident in
+device memory; the line also carries the forward+backward throughput of the
+same shape (gdn_fwd followed by gdn_bwd), the end-to-end throughput through
+the C ABI with host buffers (host->device copies of the inputs and the
+device->host read of the outputs inside the timed region), the roofline of
+the dominant kernel, the clocks seen during the timed region and the fp64
+CPU oracle timed on the host cores as a baseline.
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and a device synchronise on both sides; CUDA events on the launching stream.
+The default workload's inputs (272.6 MB) exceed the 129 MB L2, so no flush is
+needed between steps.  Multi-GPU runs (torchrun) are independent replicas, one
+batch per rank (weak scaling, no collective on the data path); rank 0 prints
+the whole-job tokens/s over the max time across ranks.
+
+--impl reference times the fp64 CPU oracle on the same workload and metric: each
+step is a bounded sample of the workload (every head of one batch row).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from linear_attention_recurrence_delta_gb300 import inputs as I  # noqa: E402
+
+DEFAULT_WORKLOAD = "delta_bf16_8x16x4096x64"
+METRIC = "GDN fwd / fwd+bwd tokens/sec at H=16,T=4096,d=64 bf16; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def io_bytes(w, backward=False):
+    """Algorithmic HBM bytes of one forward (or backward) launch over workload w:
+    every input read once, every output written once."""
+    e = 2 if w.dtype == "bf16" else 4
+    tok = w.B * w.T * w.H
+    per_tok = (2 * w.dk + 2 * w.dv) * e + e + (e if w.mode == "delta" else 0)   # v,b,c,o + g (+beta)
+    state = w.B * w.H * w.dk * w.dv * 4
+    fwd = tok * per_tok + state + w.H * w.dk * 4 + (state if w.h0_std > 0 else 0)
+    if not backward:
+        return fwd
+    # backward: reads v,b,c,g,(beta),dO (+A_log, h0, dhT); writes dv,db,dc,dg,(dbeta) (+dA_log, dh0)
+    rd = tok * ((2 * w.dk + 2 * w.dv) * e + e + (e if w.mode == "delta" else 0))
+    wr = tok * ((2 * w.dk + w.dv) * e + e + (e if w.mode == "delta" else 0))
+    return rd + wr + 2 * state + 2 * w.H * w.dk * 4
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, x):
+    """Every head of batch row 0: T tokens' worth of work (units = H)."""
+    sl = lambda a: None if a is None else a[:1]
+    return {k: (sl(v) if k not in ("A_log",) else v) for k, v in x.items()}
+
+
+def time_oracle(w, x, steps, warmup):
+    import oracle
+    xs = oracle_sample(w, x)
+    threads = os.cpu_count() or 1
+    fn = lambda: oracle.gdn_fwd(xs["v"], xs["b"], xs["c"], xs["g"], xs["beta"], xs["A_log"], xs["h0"],
+                                mode=w.mode, threads=threads)
+    for _ in range(warmup):
+        fn()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        fn()
+    dt = (time.perf_counter() - t0) / steps
+    tokens = w.T  # one batch row, all heads
+    return tokens / dt, dt, min(threads, w.H)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = I.WORKLOADS[args.workload]
+    x = I.make_inputs(w)
+    value, dt, cores = time_oracle(w, x, args.steps, args.warmup)
+    sample = f"batch row 0 of {w.name}: all {w.H} heads x {w.T} tokens per step, serial fp64"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "pass": "fwd", "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+                   "mode": w.mode, "io": w.dtype},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-bwd", action="store_true", help="skip the forward+backward measurement")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import numpy as np
+    import torch
+
+    import linear_attention_recurrence_delta_gb300 as gdn
+    from linear_attention_recurrence_delta_gb300 import _build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    _build.build()
+    gdn.load()
+
+    base = I.WORKLOADS[args.workload]
+    w = base.with_(seed=base.seed + 1000 * rank) if world > 1 else base
+    wb = w.with_(backward=True)
+    x = I.make_inputs(wb)
+    s = gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.mode, w.dtype)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dev = lambda a: None if a is None else torch.from_numpy(a).to("cuda", dt)
+    dev32 = lambda a: None if a is None else torch.from_numpy(a).to("cuda", torch.float32)
+    t = {k: dev(x[k]) for k in ("v", "b", "c", "g", "beta", "dO")}
+    A_log, h0 = dev32(x["A_log"]), dev32(x["h0"])
+    o = torch.empty((w.B, w.T, w.H, w.dv), dtype=dt, device="cuda")
+    hT = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+    ws = torch.empty(gdn.gdn_workspace_bytes(s, 1), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        gdn.check(gdn.gdn_fwd(s, t["v"], t["b"], t["c"], t["g"], t["beta"], A_log, h0, o, hT, ws,
+                              stream=stream), "gdn_fwd")
+
+    grads = {
+        "dv": torch.empty_like(t["v"]), "db": torch.empty_like(t["b"]), "dc": torch.empty_like(t["c"]),
+        "dg": torch.empty_like(t["g"]), "dbeta": torch.empty_like(t["beta"]) if t["beta"] is not None else None,
+        "dA_log": torch.empty_like(A_log), "dh0": torch.empty_like(hT),
+    }
+
+    def bwd():
+        gdn.check(gdn.gdn_bwd(s, t["v"], t["b"], t["c"], t["g"], t["beta"], A_log, h0, t["dO"], None,
+                              grads["dv"], grads["db"], grads["dc"], grads["dg"], grads["dbeta"], grads["dA_log"],
+                              grads["dh0"], ws, stream=stream), "gdn_bwd")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        tt = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return float(tt.item())
+
+    def timed(step_fn, K, W):
+        for _ in range(W):
+            step_fn()
+        barrier()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(K):
+            ev[k][0].record(stream)
+            step_fn()
+            ev[k][1].record(stream)
+        end.record(stream)
+        barrier()
+        total_ms = start.elapsed_time(end)
+        per = [a.elapsed_time(b) for a, b in ev]
+        return max_over_ranks(total_ms), statistics.mean(per)
+
+    tokens = w.B * w.T
+    with ClockSampler(local) as clk:
+        total_ms, launch_ms = timed(fwd, args.steps, args.warmup)
+    clocks = clk.summary()
+    ms_per_step = total_ms / args.steps
+    value = world * tokens / (ms_per_step * 1e-3)
+    gdn.check(gdn.gdn_last_device_status(ws), "device status")
+
+    peaks, peak_kind = load_peaks()
+    fwd_bytes = io_bytes(w)
+    achieved = fwd_bytes / (launch_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
+                "kernel": "gdn_fwd (one launch)", "bytes_per_launch": fwd_bytes, "launch_ms": launch_ms}
+    # launches of our kernels per forward step: the forward kernel itself
+    gpu_launches = 1 * args.steps
+
+    # end to end through the C ABI with host buffers
+    hx = {k: (None if v is None else v.cpu().pin_memory()) for k, v in t.items() if k != "dO"}
+    hA = A_log.cpu().pin_memory()
+    ho = torch.empty(o.shape, dtype=dt).pin_memory()
+    hhT = torch.empty(hT.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in hx.values() if v is not None) + hA.numel() * 4
+    d2h = ho.numel() * ho.element_size() + hhT.numel() * 4
+
+    def e2e_step():
+        for k, v in hx.items():
+            if v is not None:
+                t[k].copy_(v, non_blocking=True)
+        A_log.copy_(hA, non_blocking=True)
+        fwd()
+        ho.copy_(o, non_blocking=True)
+        hhT.copy_(hT, non_blocking=True)
+
+    e2e_total, _ = timed(e2e_step, max(3, args.steps // 2), 3)
+    e2e_ms = e2e_total / max(3, args.steps // 2)
+    e2e = {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    fwdbwd = None
+    if not args.no_bwd:
+        def fb():
+            fwd()
+            bwd()
+        kb = max(3, args.steps // 4)
+        fb_total, fb_launch = timed(fb, kb, 3)
+        fb_ms = fb_total / kb
+        fwdbwd = {"value": world * tokens / (fb_ms * 1e-3), "unit": "tokens/s", "ms_per_step": fb_ms,
+                  "bwd_bytes": io_bytes(w, backward=True)}
+        gpu_launches += 3 * kb   # fwd kernel + backward kernel + dA_log reduction
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v_cpu, dt_cpu, cores = time_oracle(w, x, 1, 0)
+        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"batch row 0 of {w.name} (all {w.H} heads x {w.T} tokens), serial fp64 forward, "
+                         f"{dt_cpu:.2f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "pass": "fwd", "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+                       "mode": w.mode, "io": w.dtype, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": f"inputs {fwd_bytes / 1e6:.1f} MB > 129 MB L2, no flush"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "fwd_bwd": fwdbwd, "clocks": clocks,
+            "gpu_launches": gpu_launches,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,133 @@
+/*
+ * gdn.h -- C ABI of libgdn, the GB300 (sm_103a) gated delta rule library.
+ *
+ * The operation (per batch index b and head h, one independent recurrence
+ * over t = 0 .. T-1 on a state h of shape [d_k, d_v], rows indexed by the
+ * key/state index i):
+ *
+ *   "GDN & MLA Mechanism Deep-Dive", Step 4 (Gated delta rule):
+ *     alpha_t[i] = exp(g_t * A[i]),  A[i] = -exp(A_log[h, i])
+ *     GDN_GATED:  h_t = alpha_t (.)rows h_{t-1} + b_t v_t^T
+ *   "HyMo-434M -- documentation portal", card 01 (GDN recurrence, delta rule):
+ *     GDN_DELTA:  h_t = alpha_t (.)rows h_{t-1}
+ *                       + beta_t b_t (v_t - (alpha_t (.)rows h_{t-1})^T b_t)^T
+ *   both modes:  o_t = h_t^T c_t       (the read sees token t's own write)
+ *
+ * "GDN & MLA Mechanism Deep-Dive", Step 5 (Chunked recurrence) is how the
+ * kernels evaluate it: chunks of 64 tokens solved in closed form, with the
+ * state carried serially from chunk to chunk.
+ *
+ * Inputs arrive already transformed: g and beta after their sigmoid (values
+ * in [0, 1]), and in delta mode b already L2-normalised by the caller.  The
+ * library applies no 1/sqrt(d) scale, no output norm and no state clamp
+ * ("Signed-state caveat": HyMo does not bound the state norm).
+ *
+ * Layouts (all contiguous, row-major, element strides implied by the shape):
+ *   v, o, dO, dv              [B, T, H, d_v]   dtype `io`
+ *   b, c, db, dc              [B, T, H, d_k]   dtype `io`
+ *   g, beta, dg, dbeta        [B, T, H]        dtype `io`
+ *   A_log, dA_log             [H, d_k]         float32
+ *   h0, hT, dhT, dh0          [B, H, d_k, d_v] float32
+ *
+ * Ownership: the caller allocates and owns every buffer, including the
+ * workspace; the library allocates no memory, never synchronises inside
+ * gdn_fwd / gdn_bwd, and enqueues all work on the caller's stream.  All data
+ * pointers are device pointers.
+ *
+ * Errors: argument problems are reported synchronously, before anything is
+ * enqueued.  A failed launch returns GDN_ERR_CUDA.  Conditions the kernels
+ * detect on the device (an expired bounded wait) are written to a status
+ * word at the start of the workspace, which gdn_last_device_status reads.
+ *
+ * Limits: B, H >= 1; T >= 0 (with T = 0 the per-token pointers may be NULL:
+ * the forward copies h0, or zeros, to hT; the backward writes dh0 = dhT and
+ * dA_log = 0); 1 <= d_k, d_v <= 64.  With io = GDN_BF16, d_k
+ * and d_v must be multiples of 8 and every bf16 pointer 16-byte aligned;
+ * with io = GDN_F32, every pointer 4-byte aligned.  float32 state and A_log
+ * pointers must be 16-byte aligned.  Outputs must not alias inputs.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                      /* same type as cudaStream_t's target */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef enum {
+    GDN_GATED = 0,   /* h_t = alpha_t h_{t-1} + b_t v_t^T            */
+    GDN_DELTA = 1    /* decay, then erase-and-write with key b_t     */
+} gdn_mode_t;
+
+typedef enum {
+    GDN_F32 = 0,     /* float32 I/O (computed in fp32 on CUDA cores) */
+    GDN_BF16 = 1     /* bfloat16 I/O, fp32 accumulation              */
+} gdn_dtype_t;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_NULL = 1,        /* a required pointer is NULL                  */
+    GDN_ERR_SHAPE = 2,       /* a size is out of range                      */
+    GDN_ERR_ALIGN = 3,       /* a pointer is not aligned as required        */
+    GDN_ERR_MODE = 4,        /* unknown mode/dtype, or beta given/missing   */
+    GDN_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than required     */
+    GDN_ERR_CUDA = 6,        /* a CUDA call or kernel launch failed         */
+    GDN_ERR_TIMEOUT = 7,     /* a bounded device-side wait expired          */
+    GDN_ERR_DEVICE = 8       /* the current device is not an sm_103 GPU     */
+} gdn_status_t;
+
+typedef struct {
+    int B, H, T;     /* batch, heads, tokens                               */
+    int dk, dv;      /* key (state-row) and value (state-column) widths    */
+    int mode;        /* gdn_mode_t                                         */
+    int io;          /* gdn_dtype_t of v, b, c, g, beta, o and the grads   */
+} gdn_shape_t;
+
+/* Bytes of workspace gdn_fwd (backward = 0) or gdn_bwd (backward = 1) needs
+ * for this shape; 0 if the shape is invalid.  Always a multiple of 256 and
+ * at least 256 (the device status word lives in the first bytes). */
+size_t gdn_workspace_bytes(const gdn_shape_t* shape, int backward);
+
+/* Forward pass.  Reads v, b, c, g, beta (NULL iff mode == GDN_GATED), A_log,
+ * h0 (NULL => zero initial state); writes o and hT (NULL => not written).
+ * ws must be device memory of at least gdn_workspace_bytes(shape, 0) bytes,
+ * 256-byte aligned.  Returns GDN_OK once the work is enqueued on `stream`. */
+gdn_status_t gdn_fwd(const gdn_shape_t* shape,
+                     const void* v, const void* b, const void* c,
+                     const void* g, const void* beta, const float* A_log,
+                     const float* h0, void* o, float* hT,
+                     void* ws, size_t ws_bytes, gdn_stream_t stream);
+
+/* Backward pass: gradients of L(o, h_T) given dL/do = dO and dL/dh_T = dhT
+ * (NULL => zero).  Takes the forward's inputs again (the forward is
+ * recomputed inside; nothing from gdn_fwd is kept).  Writes dv, db, dc, dg,
+ * dbeta (NULL iff mode == GDN_GATED) in dtype `io`, dA_log [H, d_k] float32
+ * (overwritten, summed over the batch) and dh0 (NULL => not written).
+ * dg and dbeta are gradients with respect to the post-sigmoid g and beta.
+ * ws must hold at least gdn_workspace_bytes(shape, 1) bytes. */
+gdn_status_t gdn_bwd(const gdn_shape_t* shape,
+                     const void* v, const void* b, const void* c,
+                     const void* g, const void* beta, const float* A_log,
+                     const float* h0, const void* dO, const float* dhT,
+                     void* dv, void* db, void* dc, void* dg, void* dbeta,
+                     float* dA_log, float* dh0,
+                     void* ws, size_t ws_bytes, gdn_stream_t stream);
+
+/* Synchronises `stream` and returns the status the kernels of the last call
+ * that used `ws` left in it (GDN_OK, GDN_ERR_TIMEOUT), or GDN_ERR_CUDA if the
+ * synchronisation itself failed. */
+gdn_status_t gdn_last_device_status(const void* ws, gdn_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* gdn_status_string(gdn_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

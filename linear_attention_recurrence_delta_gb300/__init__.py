@@ -1,0 +1,133 @@
+"""GB300 (sm_103a) gated delta rule: Python binding of libgdn's C ABI.
+
+The functions below carry the C names (``gdn_fwd``, ``gdn_bwd``,
+``gdn_workspace_bytes``, ``gdn_last_device_status``, ``gdn_status_string``)
+and only marshal arguments: torch tensors become device pointers, ``None``
+becomes NULL, and the stream defaults to torch's current stream.  Every step
+of the computation runs in libgdn's CUDA kernels.  There is no fallback: if
+the library is missing or cannot be loaded, the first call raises.
+
+The operation ("GDN & MLA Mechanism Deep-Dive", Step 4 and Step 5; delta rule
+from the card "01 GDN recurrence" of "HyMo-434M -- documentation portal"),
+layouts and limits are documented in ``include/gdn.h``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+GDN_GATED, GDN_DELTA = 0, 1
+GDN_F32, GDN_BF16 = 0, 1
+GDN_OK = 0
+STATUS_NAMES = {
+    0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_ALIGN", 4: "GDN_ERR_MODE",
+    5: "GDN_ERR_WORKSPACE", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_DEVICE",
+}
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}{': ' if what else ''}{gdn_status_string(status)}")
+
+
+class gdn_shape_t(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int), ("dk", ctypes.c_int),
+                ("dv", ctypes.c_int), ("mode", ctypes.c_int), ("io", ctypes.c_int)]
+
+    def __repr__(self):
+        return (f"gdn_shape_t(B={self.B}, H={self.H}, T={self.T}, dk={self.dk}, dv={self.dv}, "
+                f"mode={self.mode}, io={self.io})")
+
+
+def make_shape(B, H, T, dk, dv, mode="gated", io="bf16") -> gdn_shape_t:
+    m = {"gated": GDN_GATED, "delta": GDN_DELTA}.get(mode, mode)
+    d = {"f32": GDN_F32, "bf16": GDN_BF16}.get(io, io)
+    return gdn_shape_t(int(B), int(H), int(T), int(dk), int(dv), int(m), int(d))
+
+
+def load(path: str | None = None):
+    """Load libgdn.so (once).  Raises if it is missing: there is no fallback."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"libgdn.so not built ({p}); run __graft_entry__.build() first")
+            lib = ctypes.CDLL(p)
+            vp, sz, sp = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(gdn_shape_t)
+            lib.gdn_workspace_bytes.argtypes = [sp, ctypes.c_int]
+            lib.gdn_workspace_bytes.restype = sz
+            lib.gdn_fwd.argtypes = [sp] + [vp] * 9 + [vp, sz, vp]
+            lib.gdn_fwd.restype = ctypes.c_int
+            lib.gdn_bwd.argtypes = [sp] + [vp] * 16 + [vp, sz, vp]
+            lib.gdn_bwd.restype = ctypes.c_int
+            lib.gdn_last_device_status.argtypes = [vp, vp]
+            lib.gdn_last_device_status.restype = ctypes.c_int
+            lib.gdn_status_string.argtypes = [ctypes.c_int]
+            lib.gdn_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def gdn_workspace_bytes(shape: gdn_shape_t, backward: int) -> int:
+    return int(load().gdn_workspace_bytes(ctypes.byref(shape), int(backward)))
+
+
+def gdn_fwd(shape, v, b, c, g, beta, A_log, h0, o, hT, ws, ws_bytes=None, stream=None) -> int:
+    """Enqueue the forward; returns the gdn_status_t code (0 = GDN_OK)."""
+    wsb = _nbytes(ws) if ws_bytes is None and ws is not None else (ws_bytes or 0)
+    return int(load().gdn_fwd(ctypes.byref(shape), _ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(beta), _ptr(A_log),
+                              _ptr(h0), _ptr(o), _ptr(hT), _ptr(ws), wsb, _stream(stream)))
+
+
+def gdn_bwd(shape, v, b, c, g, beta, A_log, h0, dO, dhT, dv, db, dc, dg, dbeta, dA_log, dh0, ws,
+            ws_bytes=None, stream=None) -> int:
+    """Enqueue the backward; returns the gdn_status_t code (0 = GDN_OK)."""
+    wsb = _nbytes(ws) if ws_bytes is None and ws is not None else (ws_bytes or 0)
+    return int(load().gdn_bwd(ctypes.byref(shape), _ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(beta), _ptr(A_log),
+                              _ptr(h0), _ptr(dO), _ptr(dhT), _ptr(dv), _ptr(db), _ptr(dc), _ptr(dg), _ptr(dbeta),
+                              _ptr(dA_log), _ptr(dh0), _ptr(ws), wsb, _stream(stream)))
+
+
+def gdn_last_device_status(ws, stream=None) -> int:
+    return int(load().gdn_last_device_status(_ptr(ws), _stream(stream)))
+
+
+def gdn_status_string(status: int) -> str:
+    try:
+        return load().gdn_status_string(int(status)).decode()
+    except RuntimeError:
+        return STATUS_NAMES.get(int(status), f"status {status}")
+
+
+def check(status: int, what: str = "") -> None:
+    if status != GDN_OK:
+        raise GdnError(status, what)

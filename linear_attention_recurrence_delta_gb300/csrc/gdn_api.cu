@@ -1,0 +1,191 @@
+// gdn_api.cu -- the C ABI of libgdn: argument checks, workspace carve-up and
+// dispatch to the kernels.  Nothing here allocates or synchronises, except
+// gdn_last_device_status, whose job is to synchronise and read back.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static bool shape_ok(const gdn_shape_t& s)
+{
+    if (s.B < 1 || s.H < 1 || s.T < 0) return false;
+    if (s.dk < 1 || s.dk > 64 || s.dv < 1 || s.dv > 64) return false;
+    if (s.io == GDN_BF16 && ((s.dk % 8) || (s.dv % 8))) return false;
+    // keep every element offset inside a signed 64-bit range with margin
+    const double elems = (double)s.B * s.T * s.H * 64.0;
+    if (elems > 9.0e15) return false;
+    return true;
+}
+
+WsLayout ws_layout(const gdn_shape_t& s, int backward)
+{
+    WsLayout L;
+    size_t off = 256;  // status word
+    if (backward) {
+        const size_t units = (size_t)s.B * s.H;
+        const size_t nseg = (size_t)((s.T + kSerialSeg - 1) / kSerialSeg);
+        L.ck_off = off;
+        off = round_up(off + units * nseg * kStateSlot, 256);
+        L.scratch_off = off;
+        off = round_up(off + units * kSerialSeg * kStateSlot, 256);
+        L.dalog_off = off;
+        off = round_up(off + units * (size_t)s.dk * 4, 256);
+    }
+    L.total = off;
+    return L;
+}
+
+static int cached_dev_ok[64];  // 0 unknown, 1 ok, 2 not sm_103
+
+static gdn_status_t check_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return GDN_ERR_DEVICE;
+    if (cached_dev_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        cached_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return cached_dev_ok[dev] == 1 ? GDN_OK : GDN_ERR_DEVICE;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+static gdn_status_t check_common(const gdn_shape_t* s, const void* v, const void* b, const void* c,
+                                 const void* g, const void* beta, const float* A_log, const float* h0,
+                                 void* ws, size_t ws_bytes, int backward)
+{
+    if (!s) return GDN_ERR_NULL;
+    if (s->mode != GDN_GATED && s->mode != GDN_DELTA) return GDN_ERR_MODE;
+    if (s->io != GDN_F32 && s->io != GDN_BF16) return GDN_ERR_MODE;
+    if (!shape_ok(*s)) return GDN_ERR_SHAPE;
+    // with T == 0 there are no tokens: the per-token pointers may be NULL
+    const bool tok = s->T > 0;
+    if ((tok && (!v || !b || !c || !g)) || !A_log) return GDN_ERR_NULL;
+    if (!ws) return GDN_ERR_WORKSPACE;
+    if (tok && (s->mode == GDN_DELTA) != (beta != nullptr)) return GDN_ERR_MODE;
+    if (s->mode == GDN_GATED && beta) return GDN_ERR_MODE;
+    const size_t ioa = s->io == GDN_BF16 ? 16 : 4;
+    if (!aligned(v, ioa) || !aligned(b, ioa) || !aligned(c, ioa) || !aligned(g, s->io == GDN_BF16 ? 2 : 4) ||
+        (beta && !aligned(beta, s->io == GDN_BF16 ? 2 : 4)))
+        return GDN_ERR_ALIGN;
+    if (!aligned(A_log, 16) || (h0 && !aligned(h0, 16)) || !aligned(ws, 256)) return GDN_ERR_ALIGN;
+    if (ws_bytes < ws_layout(*s, backward).total) return GDN_ERR_WORKSPACE;
+    return GDN_OK;
+}
+
+static Args make_args(const gdn_shape_t* s)
+{
+    Args a;
+    memset(&a, 0, sizeof(a));
+    a.B = s->B; a.H = s->H; a.T = s->T; a.dk = s->dk; a.dv = s->dv; a.mode = s->mode; a.io = s->io;
+    return a;
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" size_t gdn_workspace_bytes(const gdn_shape_t* shape, int backward)
+{
+    if (!shape || !shape_ok(*shape)) return 0;
+    if ((shape->mode != GDN_GATED && shape->mode != GDN_DELTA) || (shape->io != GDN_F32 && shape->io != GDN_BF16))
+        return 0;
+    return ws_layout(*shape, backward ? 1 : 0).total;
+}
+
+extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape, const void* v, const void* b, const void* c,
+                                const void* g, const void* beta, const float* A_log, const float* h0,
+                                void* o, float* hT, void* ws, size_t ws_bytes, gdn_stream_t stream)
+{
+    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 0);
+    if (r != GDN_OK) return r;
+    if (!o && shape->T > 0) return GDN_ERR_NULL;
+    const size_t ioa = shape->io == GDN_BF16 ? 16 : 4;
+    if (!aligned(o, ioa) || (hT && !aligned(hT, 16))) return GDN_ERR_ALIGN;
+    if ((r = check_device()) != GDN_OK) return r;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return GDN_ERR_CUDA;
+    Args a = make_args(shape);
+    a.v = v; a.b = b; a.c = c; a.g = g; a.beta = beta; a.A_log = A_log; a.h0 = h0; a.o = o; a.hT = hT;
+    a.ws = ws; a.ws_bytes = ws_bytes;
+    const size_t state_bytes = (size_t)a.B * a.H * a.dk * a.dv * sizeof(float);
+    if (a.T == 0) {
+        if (hT) {
+            cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, state_bytes, cudaMemcpyDeviceToDevice, st)
+                               : cudaMemsetAsync(hT, 0, state_bytes, st);
+            if (e != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        return GDN_OK;
+    }
+    bool handled = false;
+    if (a.io == GDN_BF16) {
+        if (launch_fwd_tc(a, st, &handled) != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    if (!handled && launch_serial_fwd(a, st) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape, const void* v, const void* b, const void* c,
+                                const void* g, const void* beta, const float* A_log, const float* h0,
+                                const void* dO, const float* dhT, void* dv, void* db, void* dc, void* dg,
+                                void* dbeta, float* dA_log, float* dh0, void* ws, size_t ws_bytes,
+                                gdn_stream_t stream)
+{
+    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 1);
+    if (r != GDN_OK) return r;
+    const bool tok = shape->T > 0;
+    if ((tok && (!dO || !dv || !db || !dc || !dg)) || !dA_log) return GDN_ERR_NULL;
+    if (tok && (shape->mode == GDN_DELTA) != (dbeta != nullptr)) return GDN_ERR_MODE;
+    if (shape->mode == GDN_GATED && dbeta) return GDN_ERR_MODE;
+    const size_t ioa = shape->io == GDN_BF16 ? 16 : 4;
+    const size_t sca = shape->io == GDN_BF16 ? 2 : 4;
+    if (!aligned(dO, ioa) || !aligned(dv, ioa) || !aligned(db, ioa) || !aligned(dc, ioa) || !aligned(dg, sca) ||
+        (dbeta && !aligned(dbeta, sca)) || !aligned(dA_log, 16) || (dhT && !aligned(dhT, 16)) ||
+        (dh0 && !aligned(dh0, 16)))
+        return GDN_ERR_ALIGN;
+    if ((r = check_device()) != GDN_OK) return r;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return GDN_ERR_CUDA;
+    Args a = make_args(shape);
+    a.v = v; a.b = b; a.c = c; a.g = g; a.beta = beta; a.A_log = A_log; a.h0 = h0;
+    a.dO = dO; a.dhT = dhT; a.dv_ = dv; a.db = db; a.dc = dc; a.dg = dg; a.dbeta = dbeta;
+    a.dA_log = dA_log; a.dh0 = dh0; a.ws = ws; a.ws_bytes = ws_bytes;
+    if (launch_serial_bwd(a, st) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+extern "C" gdn_status_t gdn_last_device_status(const void* ws, gdn_stream_t stream)
+{
+    if (!ws) return GDN_ERR_NULL;
+    uint32_t word[2] = {0, 0};
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaMemcpy(word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+    return word[0] == kDevOk ? GDN_OK : GDN_ERR_TIMEOUT;
+}
+
+extern "C" const char* gdn_status_string(gdn_status_t s)
+{
+    switch (s) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_NULL: return "GDN_ERR_NULL: a required pointer is NULL";
+        case GDN_ERR_SHAPE: return "GDN_ERR_SHAPE: a size is out of range";
+        case GDN_ERR_ALIGN: return "GDN_ERR_ALIGN: a pointer is misaligned";
+        case GDN_ERR_MODE: return "GDN_ERR_MODE: bad mode/dtype or beta presence";
+        case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA call failed";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait expired";
+        case GDN_ERR_DEVICE: return "GDN_ERR_DEVICE: the current device is not sm_103";
+    }
+    return "unknown gdn status";
+}

@@ -22,7 +22,7 @@ float64 arrays are the rounded values, exactly representable in the I/O dtype.
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field, replace
+from dataclasses import dataclass, replace
 
 import numpy as np
 
@@ -117,7 +117,6 @@ class Workload:
     g_mu: float = 0.0          # g = sigmoid(N(g_mu, 1))
     h0_std: float = 0.0        # h0 = h0_std * N(0, 1) (0 => no h0)
     notes: str = ""
-    extra: dict = field(default_factory=dict)
 
     @property
     def tokens(self) -> int:

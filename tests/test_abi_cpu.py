@@ -1,0 +1,109 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function
+include/gdn.h declares, sizes workspaces, and rejects bad arguments before
+touching any device (no compute call is made without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_recurrence_delta_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", txt))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(gdn.LIB_PATH):
+        from linear_attention_recurrence_delta_gb300 import _build
+        _build.build()
+    return gdn.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("gdn_fwd", "gdn_bwd", "gdn_workspace_bytes", "gdn_last_device_status", "gdn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    for code, name in gdn.STATUS_NAMES.items():
+        assert gdn.gdn_status_string(code).startswith(name)
+
+
+def test_workspace_sizes(lib):
+    s = gdn.make_shape(8, 16, 4096, 64, 64, "delta", "bf16")
+    f = gdn.gdn_workspace_bytes(s, 0)
+    b = gdn.gdn_workspace_bytes(s, 1)
+    assert f >= 256 and f % 256 == 0
+    assert b > f and b % 256 == 0
+    assert gdn.gdn_workspace_bytes(gdn.make_shape(1, 1, 0, 8, 8), 1) >= 256
+    for bad in (gdn.make_shape(0, 1, 8, 8, 8), gdn.make_shape(1, 1, 8, 65, 8), gdn.make_shape(1, 1, 8, 8, 0),
+                gdn.make_shape(1, 1, -1, 8, 8), gdn.make_shape(1, 1, 8, 12, 8, "gated", "bf16"),
+                gdn.make_shape(1, 1, 8, 8, 8, 7, "bf16"), gdn.make_shape(1, 1, 8, 8, 8, "gated", 5)):
+        assert gdn.gdn_workspace_bytes(bad, 0) == 0
+
+
+FAKE = 1 << 20   # a 256-byte aligned non-null address; never dereferenced
+
+
+def fwd_args(**kw):
+    a = dict(v=FAKE, b=FAKE, c=FAKE, g=FAKE, beta=None, A_log=FAKE, h0=None, o=FAKE, hT=None, ws=FAKE,
+             ws_bytes=1 << 30)
+    a.update(kw)
+    return a
+
+
+def call_fwd(shape, a):
+    return gdn.gdn_fwd(shape, a["v"], a["b"], a["c"], a["g"], a["beta"], a["A_log"], a["h0"], a["o"], a["hT"],
+                       a["ws"], ws_bytes=a["ws_bytes"], stream=0)
+
+
+def test_fwd_rejects_bad_arguments_before_any_device_work(lib):
+    s = gdn.make_shape(2, 2, 64, 16, 16, "gated", "bf16")
+    assert call_fwd(s, fwd_args(v=None)) == 1                     # NULL input
+    assert call_fwd(s, fwd_args(o=None)) == 1                     # NULL output
+    assert call_fwd(s, fwd_args(ws=None)) == 5                    # no workspace
+    assert call_fwd(s, fwd_args(ws_bytes=16)) == 5                # workspace too small
+    assert call_fwd(s, fwd_args(beta=FAKE)) == 4                  # beta in gated mode
+    sd = gdn.make_shape(2, 2, 64, 16, 16, "delta", "bf16")
+    assert call_fwd(sd, fwd_args()) == 4                          # beta missing in delta mode
+    assert call_fwd(s, fwd_args(v=FAKE + 2)) == 3                 # misaligned bf16 tensor
+    assert call_fwd(s, fwd_args(ws=FAKE + 16)) == 3               # misaligned workspace
+    assert call_fwd(gdn.make_shape(2, 2, 64, 12, 16, "gated", "bf16"), fwd_args()) == 2
+    assert call_fwd(gdn.make_shape(2, 2, 64, 16, 72, "gated", "f32"), fwd_args()) == 2
+    assert call_fwd(gdn.make_shape(0, 2, 64, 16, 16, "gated", "f32"), fwd_args()) == 2
+    assert call_fwd(gdn.make_shape(2, 2, 64, 16, 16, 3, "f32"), fwd_args()) == 4
+
+
+def test_bwd_rejects_bad_arguments_before_any_device_work(lib):
+    s = gdn.make_shape(2, 2, 64, 16, 16, "delta", "f32")
+
+    def call(**kw):
+        a = dict(v=FAKE, b=FAKE, c=FAKE, g=FAKE, beta=FAKE, A_log=FAKE, h0=None, dO=FAKE, dhT=None, dv=FAKE,
+                 db=FAKE, dc=FAKE, dg=FAKE, dbeta=FAKE, dA_log=FAKE, dh0=None, ws=FAKE, ws_bytes=1 << 40)
+        a.update(kw)
+        ws_bytes = a.pop("ws_bytes")
+        return gdn.gdn_bwd(s, *a.values(), ws_bytes=ws_bytes, stream=0)
+
+    assert call(dO=None) == 1
+    assert call(dA_log=None) == 1
+    assert call(dbeta=None) == 4
+    assert call(ws_bytes=256) == 5
+    assert call(dA_log=FAKE + 4) == 3
+    assert call(b=FAKE + 2) == 3
