@@ -118,6 +118,27 @@ gdn_status_t gdn_bwd(const gdn_shape_t* shape,
                      float* dA_log, float* dh0,
                      void* ws, size_t ws_bytes, gdn_stream_t stream);
 
+/* Backward pass that allocates nothing and needs no workspace argument.  The
+ * pages describe no counterpart; this is a convenience of the library.  It is
+ * for callers that cannot call cudaMalloc: latency-critical code that cannot
+ * afford cudaMalloc's implicit device synchronisation, plugins inside a host
+ * framework that owns all device memory and offers them no allocator, and
+ * processes that reserve their memory at start-up and forbid later
+ * allocations.  Arguments, results and errors are those of gdn_bwd; the
+ * workspace is a 32 MiB array inside the library (one per GPU that loads it,
+ * held until the process exits).  Shapes whose gdn_workspace_bytes(shape, 1)
+ * exceeds 32 MiB are rejected with GDN_ERR_WORKSPACE before anything is
+ * enqueued.  All calls on a device share that array: calls that may overlap
+ * on the GPU race and must be ordered by the caller.  The first call on each
+ * device looks up the array's address (cudaGetSymbolAddress) with that device
+ * current; make it before any stream capture on that device. */
+gdn_status_t gdn_bwd_noalloc(const gdn_shape_t* shape,
+                             const void* v, const void* b, const void* c,
+                             const void* g, const void* beta, const float* A_log,
+                             const float* h0, const void* dO, const float* dhT,
+                             void* dv, void* db, void* dc, void* dg, void* dbeta,
+                             float* dA_log, float* dh0, gdn_stream_t stream);
+
 /* Synchronises `stream` and returns the status the kernels of the last call
  * that used `ws` left in it (GDN_OK, GDN_ERR_TIMEOUT), or GDN_ERR_CUDA if the
  * synchronisation itself failed. */

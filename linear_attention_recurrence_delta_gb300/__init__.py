@@ -68,6 +68,8 @@ def load(path: str | None = None):
             lib.gdn_fwd.restype = ctypes.c_int
             lib.gdn_bwd.argtypes = [sp] + [vp] * 16 + [vp, sz, vp]
             lib.gdn_bwd.restype = ctypes.c_int
+            lib.gdn_bwd_noalloc.argtypes = [sp] + [vp] * 16 + [vp]
+            lib.gdn_bwd_noalloc.restype = ctypes.c_int
             lib.gdn_last_device_status.argtypes = [vp, vp]
             lib.gdn_last_device_status.restype = ctypes.c_int
             lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -115,6 +117,15 @@ def gdn_bwd(shape, v, b, c, g, beta, A_log, h0, dO, dhT, dv, db, dc, dg, dbeta, 
     return int(load().gdn_bwd(ctypes.byref(shape), _ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(beta), _ptr(A_log),
                               _ptr(h0), _ptr(dO), _ptr(dhT), _ptr(dv), _ptr(db), _ptr(dc), _ptr(dg), _ptr(dbeta),
                               _ptr(dA_log), _ptr(dh0), _ptr(ws), wsb, _stream(stream)))
+
+
+def gdn_bwd_noalloc(shape, v, b, c, g, beta, A_log, h0, dO, dhT, dv, db, dc, dg, dbeta, dA_log, dh0,
+                    stream=None) -> int:
+    """gdn_bwd without a workspace argument: the library's own fixed 32 MiB
+    device array serves as workspace, so the call allocates nothing."""
+    return int(load().gdn_bwd_noalloc(ctypes.byref(shape), _ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(beta),
+                                      _ptr(A_log), _ptr(h0), _ptr(dO), _ptr(dhT), _ptr(dv), _ptr(db), _ptr(dc),
+                                      _ptr(dg), _ptr(dbeta), _ptr(dA_log), _ptr(dh0), _stream(stream)))
 
 
 def gdn_last_device_status(ws, stream=None) -> int:
