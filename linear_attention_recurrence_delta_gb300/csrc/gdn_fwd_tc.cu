@@ -28,10 +28,10 @@
 //       ~69 (always for A_log <= ln 16 and g <= 1).  A per-chunk check picks
 //       an exact elementwise evaluation of those entries when it is not.
 //
-// Precision: the operands of the dominant products are kept as bf16 hi + lo
-// pairs (x = hi + lo, ~16 significant bits): the L3 level runs as
-// hi*hi + hi*lo + lo*hi, and P, Bhat^T and the state enter the output MMA as
-// both parts.  Everything else is plain bf16; accumulation is fp32 in TMEM and
+// Precision: L1 and L2 operands (factors <= 1) are fp16; the operands of the
+// dominant products are kept as bf16 hi + lo pairs (x = hi + lo, ~16
+// significant bits): the L3 level runs as hi*hi + hi*lo + lo*hi, and P,
+// Bhat^T and the state enter the output MMA as both parts.  Everything else is plain bf16; accumulation is fp32 in TMEM and
 // the state itself is carried in fp32 registers.
 //
 // CTA = one (b, h) pair; warps 0-3 (128 threads, thread r <-> TMEM lane r)
@@ -42,19 +42,16 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include "gdn_internal.h"
-#include "tc_ptx.cuh"
+#include "fwd_tc_common.cuh"
 
 namespace gdn {
 namespace {
 
 using namespace tc;
+using namespace fwdtc;
 
-constexpr int kC = 64;
 constexpr int kStages = 2;
 constexpr int kThreads = 160;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kSafeLog2 = 100.f;   // bound on |A| log2(e) * (sum of 4 g) for the L3 split
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_RING = 0;                       // stage s: V, B, C tiles (8 KB each)
@@ -93,70 +90,6 @@ struct Small {
     float a2max;
 };
 
-struct TcParams {
-    CUtensorMap tm_v, tm_b, tm_c;
-    const __nv_bfloat16* g;
-    const float* A_log;
-    const float* h0;
-    __nv_bfloat16* o;
-    float* hT;
-    uint32_t* status;
-    int B, H, T, dk, dv, nchunks;
-};
-
-__device__ __forceinline__ float bf2f(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
-
-// 8 bf16 of row `row`, chunk q (elements 8q..8q+7) of a swizzled [.][64] tile
-__device__ __forceinline__ void ld_row8(const unsigned char* tile, int row, int q, float (&v)[8])
-{
-    const uint4 u = *reinterpret_cast<const uint4*>(tile + sw128(row, 8 * q));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        v[2 * k] = __uint_as_float(w[k] << 16);
-        v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-    }
-}
-
-__device__ __forceinline__ void st_row8(unsigned char* tile, int row, int q, const float (&v)[8])
-{
-    uint4 u;
-    u.x = pack_bf16(v[0], v[1]);
-    u.y = pack_bf16(v[2], v[3]);
-    u.z = pack_bf16(v[4], v[5]);
-    u.w = pack_bf16(v[6], v[7]);
-    *reinterpret_cast<uint4*>(tile + sw128(row, 8 * q)) = u;
-}
-
-// store hi = bf16(v) and lo = bf16(v - hi): together ~16 significant bits
-__device__ __forceinline__ void st_row8_split(unsigned char* thi, unsigned char* tlo, int row, int q,
-                                              const float (&v)[8])
-{
-    float hi[8], lo[8];
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        hi[k] = __bfloat162float(__float2bfloat16_rn(v[k]));
-        lo[k] = v[k] - hi[k];
-    }
-    st_row8(thi, row, q, hi);
-    st_row8(tlo, row, q, lo);
-}
-
-// x[k] * exp2(A2[8q+k] * dG) for the 8 channels of chunk q
-__device__ __forceinline__ void scale8(const float (&x)[8], const float* A2, int q, float dG, float (&y)[8])
-{
-#pragma unroll
-    for (int k = 0; k < 8; k++) y[k] = x[k] * exp2f(A2[8 * q + k] * dG);
-}
-
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Small& sm, uint32_t* status)
-{
-    if (*(volatile uint32_t*)&sm.abort) return false;
-    if (mbar_wait(bar, parity, nullptr, 1u << 24)) return true;
-    *(volatile uint32_t*)&sm.abort = 1;
-    atomicExch(status, kDevTimeout);
-    return false;
-}
 
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_constant__ TcParams p)
 {
@@ -202,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
         int issued = 0;
         for (int k = 0; k < p.nchunks; k++) {
             const int s = k % kStages;
-            if (k >= kStages && !wait_or_abort(&S.empty[s], ((k / kStages) - 1) & 1, S, p.status)) break;
+            if (k >= kStages && !wait_or_abort(&S.empty[s], ((k / kStages) - 1) & 1, &S.abort, p.status)) break;
             issued = k + 1;
             for (int tt = lane; tt < kC; tt += 32) {
                 const int t = k * kC + tt;
@@ -246,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
 
         for (int k = 0; k < p.nchunks; k++) {
             const int s = k % kStages;
-            if (!wait_or_abort(&S.full[s], (k / kStages) & 1, S, p.status)) break;
+            if (!wait_or_abort(&S.full[s], (k / kStages) & 1, &S.abort, p.status)) break;
             unsigned char* sV = sm + OFF_RING + s * STAGE_BYTES;
             unsigned char* sB = sV + 8192;
             unsigned char* sCt = sV + 16384;
@@ -289,15 +222,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
                     ld_row8(sCt, t, q, cv);
                     ld_row8(sB, t, q, bv);
                     // rows (P side)
-                    if (I > 0) { scale8(cv, S.A2, q, Gt - Gr1, y); st_row8(sm + OFF_A1, t, q, y); }
-                    if (upper) { scale8(cv, S.A2, q, Gt - Gr2, y); st_row8(sm + OFF_A2, t, q, y); }
+                    if (I > 0) { scale8(cv, S.A2, q, Gt - Gr1, y); st_row8_f16(sm + OFF_A1, t, q, y); }
+                    if (upper) { scale8(cv, S.A2, q, Gt - Gr2, y); st_row8_f16(sm + OFF_A2, t, q, y); }
                     scale8(cv, S.A2, q, Gt - Gr3, y); st_row8_split(sm + OFF_A3, sm + OFF_A3L, t, q, y);
                     scale8(cv, S.A2, q, Gt, y); st_row8(sm + OFF_CH1, 64 + t, q, y);
                     // columns (b side): row s = t of the B operands
-                    if (I < 1) { scale8(bv, S.A2, q, S.G[15] - Gt, y); st_row8(sm + OFF_B1a, t, q, y); }
-                    if (I < 2) { scale8(bv, S.A2, q, S.G[31] - Gt, y); st_row8(sm + OFF_B1b, t, q, y); }
-                    if (I < 3) { scale8(bv, S.A2, q, S.G[47] - Gt, y); st_row8(sm + OFF_B1c, t, q, y); }
-                    if (!upper) { scale8(bv, S.A2, q, Gr2 - Gt, y); st_row8(sm + OFF_B2, t, q, y); }
+                    if (I < 1) { scale8(bv, S.A2, q, S.G[15] - Gt, y); st_row8_f16(sm + OFF_B1a, t, q, y); }
+                    if (I < 2) { scale8(bv, S.A2, q, S.G[31] - Gt, y); st_row8_f16(sm + OFF_B1b, t, q, y); }
+                    if (I < 3) { scale8(bv, S.A2, q, S.G[47] - Gt, y); st_row8_f16(sm + OFF_B1c, t, q, y); }
+                    if (!upper) { scale8(bv, S.A2, q, Gr2 - Gt, y); st_row8_f16(sm + OFF_B2, t, q, y); }
                     scale8(bv, S.A2, q, Gr3 - Gt, y); st_row8_split(sm + OFF_B3, sm + OFF_B3L, t, q, y);
                 }
                 // Bhat^T: row i = t (channel), columns s in [32 hc, 32 hc + 32)
@@ -331,10 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
                 for (int I = 1; I <= 3; I++)
                     for (int ks = 0; ks < 4; ks++)
                         mma_bf16(tbase + d1[I - 1], sdesc(a1 + ks * 32, 16, 1024), sdesc(b1[I - 1] + ks * 32, 16, 1024),
-                                 idesc_bf16(128, 16 * I, false, false), ks > 0);
+                                 idesc_f16(128, 16 * I, false, false), ks > 0);
                 for (int ks = 0; ks < 4; ks++)
                     mma_bf16(tbase + TM_D2, sdesc(a2 + ks * 32, 16, 1024),
-                             sdesc(smem_u32(sm + OFF_B2) + ks * 32, 16, 1024), idesc_bf16(128, 64, false, false), ks > 0);
+                             sdesc(smem_u32(sm + OFF_B2) + ks * 32, 16, 1024), idesc_f16(128, 64, false, false), ks > 0);
                 const uint32_t a3l = smem_u32(sm + OFF_A3L);
                 const uint32_t b3 = smem_u32(sm + OFF_B3), b3l = smem_u32(sm + OFF_B3L);
                 const uint32_t l3a[3] = {a3, a3, a3l}, l3b[3] = {b3, b3l, b3};
@@ -344,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
                                  idesc_bf16(128, 64, false, false), (part | ks) > 0);
                 mma_commit(&S.mma);
             }
-            if (!wait_or_abort(&S.mma, mma_phase, S, p.status)) break;
+            if (!wait_or_abort(&S.mma, mma_phase, &S.abort, p.status)) break;
             mma_phase ^= 1;
             tc_fence_after();
 
@@ -355,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
                 float ew[8];   // exact same-8-block entries when the L3 split is unsafe
                 if (unsafe) {
                     const int s0 = 8 * (t >> 3);
-#pragma unroll 1
+#pragma unroll
                     for (int e = 0; e < 8; e++) {
                         float acc = 0.f;
                         const int sc = s0 + e;
@@ -372,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
                         ew[e] = acc;
                     }
                 }
-#pragma unroll 1
+#pragma unroll
                 for (int cg = 0; cg < 4; cg++) {
                     float out[16];
                     if (16 * cg > 32 * warp + 31) {
@@ -381,9 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
                     } else {
                         float v1a[16], v1b[16], v2[16], v3[16];
                         const int Ia = 2 * warp, Ib = 2 * warp + 1;   // row blocks in this warp
-                        const uint32_t d1[4] = {0, TM_D1a, TM_D1b, TM_D1c};
-                        if (Ia >= 1 && cg < Ia) tmem_ld16(tbase + lane_base + d1[Ia] + 16 * cg, v1a);
-                        if (cg < Ib) tmem_ld16(tbase + lane_base + d1[Ib] + 16 * cg, v1b);
+                        // warp 0 holds row blocks 0 and 1, warp 1 holds row blocks 2 and 3
+                        const uint32_t colA = warp == 0 ? 0u : TM_D1b, colB = warp == 0 ? TM_D1a : TM_D1c;
+                        if (Ia >= 1 && cg < Ia) tmem_ld16(tbase + lane_base + colA + 16 * cg, v1a);
+                        if (cg < Ib) tmem_ld16(tbase + lane_base + colB + 16 * cg, v1b);
                         tmem_ld16(tbase + lane_base + TM_D2 + 16 * cg, v2);
                         tmem_ld16(tbase + lane_base + TM_D3 + 16 * cg, v3);
                         tmem_wait_ld();
@@ -394,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
                             if (sc > t) val = 0.f;
                             else if ((sc >> 4) < tb) val = (tb == Ia) ? v1a[c] : v1b[c];
                             else if ((sc >> 3) < (t >> 3)) val = v2[c];
-                            else val = unsafe ? ew[sc & 7] : v3[c];
+                            else val = unsafe ? ew[c & 7] : v3[c];
                             out[c] = val;
                         }
                     }
@@ -424,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
                 mma_commit(&S.empty[s]);
                 mma_commit(&S.mma);
             }
-            if (!wait_or_abort(&S.mma, mma_phase, S, p.status)) break;
+            if (!wait_or_abort(&S.mma, mma_phase, &S.abort, p.status)) break;
             mma_phase ^= 1;
             tc_fence_after();
 
@@ -477,7 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
         }
         if (r < 64 && p.hT && r < dk) {
             float* hrow = p.hT + ((size_t)u * dk + r) * dv;
-            for (int j = 0; j < dv; j++) hrow[j] = Sreg[j];
+#pragma unroll
+            for (int j = 0; j < 64; j++)
+                if (j < dv) hrow[j] = Sreg[j];
         }
     }
     tc_fence_before();
@@ -486,46 +422,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
     if (warp == 0) tmem_dealloc(tbase, TM_COLS);
 }
 
-// ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode()
-{
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = (EncodeTiledFn)ptr;
-    }
-    return fn;
-}
-
-// [B, T, H, d] bf16 -> 4-D map, box = 64 (d) x 1 (H) x 64 (T) x 1 (B), 128B swizzle
-bool make_map(CUtensorMap* m, const void* base, int B, int T, int H, int d)
-{
-    EncodeTiledFn enc = get_encode();
-    if (!enc) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)T * H * d * 2};
-    cuuint32_t box[4] = {64, 1, 64, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
 {
     *handled = false;
-    if (a.io != GDN_BF16 || a.mode != GDN_GATED || a.T <= 0) return cudaSuccess;
+    if (a.io != GDN_BF16 || a.T <= 0) return cudaSuccess;
+    if (a.mode == GDN_DELTA) {
+        *handled = true;
+        return launch_fwd_tc_delta(a, st);
+    }
     TcParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map(&p.tm_v, a.v, a.B, a.T, a.H, a.dv) || !make_map(&p.tm_b, a.b, a.B, a.T, a.H, a.dk) ||

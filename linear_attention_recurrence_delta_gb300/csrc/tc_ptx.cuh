@@ -188,6 +188,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// Instruction descriptor: kind::f16 with fp16 A/B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn, bool neg_a = false)
+{
+    return (1u << 4)                       // D format: f32
+           | ((neg_a ? 1u : 0u) << 13)
+           | ((a_mn ? 1u : 0u) << 15)
+           | ((b_mn ? 1u : 0u) << 16)
+           | ((uint32_t)(N >> 3) << 17)
+           | ((uint32_t)(M >> 4) << 24);   // A, B format fields 0 = f16
+}
+
 // D[tmem] (+)= A[smem] * B[smem], issued by a single thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate)
@@ -214,6 +225,13 @@ __host__ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t col)
 {
     const uint32_t chunk = (col >> 3) ^ (row & 7);
     return row * 128u + chunk * 16u + (col & 7u) * 2u;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
