@@ -138,7 +138,9 @@ def oracle_sample(w, x):
     return {k: (sl(v) if k not in ("A_log",) else v) for k, v in x.items()}
 
 
-def time_oracle(w, x, steps, warmup):
+def time_oracle(w, x, steps, warmup, min_seconds=0.0):
+    """Time the fp64 oracle forward on batch row 0 (all heads, all tokens).
+    Repeats the sample until at least `min_seconds` of wall time per step."""
     import oracle
     xs = oracle_sample(w, x)
     threads = os.cpu_count() or 1
@@ -146,12 +148,18 @@ def time_oracle(w, x, steps, warmup):
                                 mode=w.mode, threads=threads)
     for _ in range(warmup):
         fn()
-    t0 = time.perf_counter()
-    for _ in range(steps):
+    reps = 1
+    if min_seconds > 0:
+        t0 = time.perf_counter()
         fn()
-    dt = (time.perf_counter() - t0) / steps
+        one = max(time.perf_counter() - t0, 1e-6)
+        reps = max(1, int(min_seconds / one + 0.999))
+    t0 = time.perf_counter()
+    for _ in range(steps * reps):
+        fn()
+    dt = (time.perf_counter() - t0) / (steps * reps)
     tokens = w.T  # one batch row, all heads
-    return tokens / dt, dt, min(threads, w.H)
+    return tokens / dt, dt, min(threads, w.H), reps
 
 
 def run_reference(args):
@@ -160,7 +168,7 @@ def run_reference(args):
         return
     w = I.WORKLOADS[args.workload]
     x = I.make_inputs(w)
-    value, dt, cores = time_oracle(w, x, args.steps, args.warmup)
+    value, dt, cores, reps = time_oracle(w, x, args.steps, args.warmup)
     sample = f"batch row 0 of {w.name}: all {w.H} heads x {w.T} tokens per step, serial fp64"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
@@ -323,10 +331,10 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        v_cpu, dt_cpu, cores = time_oracle(w, x, 1, 0)
+        v_cpu, dt_cpu, cores, reps = time_oracle(w, x, 1, 1, min_seconds=1.5)
         cpu = {"value": v_cpu, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"batch row 0 of {w.name} (all {w.H} heads x {w.T} tokens), serial fp64 forward, "
-                         f"{dt_cpu:.2f} s"}
+                         f"repeated {reps}x, {dt_cpu * reps:.2f} s wall on {cores} threads"}
 
     if rank == 0:
         line = {
