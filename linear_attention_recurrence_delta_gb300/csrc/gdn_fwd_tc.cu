@@ -1,43 +1,53 @@
 // gdn_fwd_tc.cu -- chunked forward of the gated delta rule on tcgen05 tensor
-// cores (bf16 I/O, fp32 accumulation and fp32 state).
+// cores, both modes (bf16 I/O, fp32 accumulation, fp32 state).
 //
-// "GDN & MLA Mechanism Deep-Dive", Step 5 (Chunked recurrence): the sequence
-// is cut into chunks of C = 64 tokens; inside a chunk the recurrence is solved
-// in closed form with 64 x 64 matrices, and the state is carried serially from
-// chunk to chunk.  Per (b, h) and chunk, with G_t = sum_{r<=t} g_r (inclusive,
-// restarted per chunk), Gam_t[i] = A[i] G_t, S = state entering the chunk:
+// "GDN & MLA Mechanism Deep-Dive", Step 5 (Chunked recurrence): chunks of
+// C = 64 tokens are solved in closed form with 64 x 64 matrices and the state
+// is carried serially from chunk to chunk.  Per (b, h) and chunk, with
+// G_t = sum_{r<=t} g_r (inclusive, restarted per chunk), Gam_t[i] = A[i] G_t
+// and S the state entering the chunk:
+//   P[t,s] = sum_i c_t[i] b_s[i] exp(Gam_t[i] - Gam_s[i])            (s <= t)
+//   Ctil_t = c_t (.) exp(Gam_t),  Bhat_s = b_s (.) exp(Gam_63 - Gam_s)
+// gated ("GDN & MLA Mechanism Deep-Dive", Step 4):   U = V
+// delta ("HyMo-434M -- documentation portal", card 01): with
+//   M[t,s] = beta_t sum_i b_t[i] b_s[i] exp(Gam_t[i] - Gam_s[i])     (s < t),
+//   Btil_t = b_t (.) exp(Gam_t), the written values solve
+//   (I + M) U = diag(beta) (V - Btil S) = Util - W S
+// and then   O = Ctil S + P U,   S' = exp(Gam_63) (.)rows S + Bhat^T U.
 //
-//   P[t,s] = sum_i c_t[i] b_s[i] exp(Gam_t[i] - Gam_s[i])       (s <= t)
-//   O      = Ctil S + P V,           Ctil_t = c_t (.) exp(Gam_t)
-//   S'     = exp(Gam_63) (.)rows S + Bhat^T V,
-//            Bhat_s = b_s (.) exp(Gam_63 - Gam_s)
+// Decay split.  exp(Gam_t - Gam_s) is factored into a row and a column factor
+// around a reference point r between s and t, so no factor overflows (|A| up
+// to 16 over a chunk reaches exp(+-1024)); secondary chunking after Yang et al.
+// 2023 (Gated Linear Attention):
+//   L1  different 16-blocks: r = last token before the row block, one MMA per
+//       row block (N = 16, 32, 48); factors <= 1;
+//   L2  same 16-block, row in the upper and column in the lower 8-half:
+//       r = last token of the lower half; factors <= 1;
+//   L3  same 8-block: r = the block's 4th token; factors up to
+//       exp(|A| * (sum of 4 g)).
+// Every factor is an "anchor" exp(A (G_t - G_r8(t))) (its inverse for
+// columns) times a per-(8-block, reference) constant <= 1, so a chunk costs
+// two exponentials per (token, channel) plus the shared constants.  A
+// per-chunk check (|A| log2(e) * span <= 100) guarantees finite anchors; when
+// it fails every factor is evaluated directly and the L3 entries elementwise
+// in fp32.
 //
-// Both products of the last two lines run as one M = 128 MMA:
-//   [dS ; O] = [[Bhat^T, 0], [P, Ctil]] x [V ; S]     (K = 64 tokens + 64 rows)
+// Delta solve (WY form): the 16x16 diagonal blocks D of I + M are inverted in
+// fp32 by forward substitution; with L = I + M - D and N = D^{-1} L (N^4 = 0)
+//   (I + M)^{-1} R = (I + N^2)(I - N) D^{-1} R,   R = [beta V | beta Btil]
+// as [N | X0] = D^{-1}[L | R], [N^2 | N X0] = N [N | X0], Z = X0 - N X0,
+// [Util | W] = Z + N^2 Z (Z kept exactly in TMEM as the accumulator start).
 //
-// P needs exp(Gam_t - Gam_s) split into a row factor and a column factor, and
-// exp(+|A| G) overflows fp32 for a whole chunk (|A| up to 16, G up to 64).  The
-// split therefore uses reference points between t and s, so every factor is
-// <= 1, at three levels (Yang et al. 2023, secondary chunking):
-//   L1  rows and columns in different 16-token blocks: reference = last token
-//       before the row block, one MMA per row block (N = 16, 32, 48);
-//   L2  same 16-block, row in its upper 8-half, column in the lower 8-half:
-//       reference = last token of the lower half;
-//   L3  same 8-token block: reference = the block's 4th token, factors up to
-//       exp(|A| * (sum of 4 g)) -- finite whenever |A| * 4 * max g is below
-//       ~69 (always for A_log <= ln 16 and g <= 1).  A per-chunk check picks
-//       an exact elementwise evaluation of those entries when it is not.
+// Precision: the L1/L2 operands (factors <= 1) are fp16; L3, P, Bhat^T, the
+// state and, in delta mode, R, X0, Z and U enter their MMAs as bf16 hi + lo
+// pairs (hi*hi + hi*lo + lo*hi); D^{-1}, L, N, N^2, W, Ctil are plain bf16.
 //
-// Precision: L1 and L2 operands (factors <= 1) are fp16; the operands of the
-// dominant products are kept as bf16 hi + lo pairs (x = hi + lo, ~16
-// significant bits): the L3 level runs as hi*hi + hi*lo + lo*hi, and P,
-// Bhat^T and the state enter the output MMA as both parts.  Everything else is plain bf16; accumulation is fp32 in TMEM and
-// the state itself is carried in fp32 registers.
-//
-// CTA = one (b, h) pair; warps 0-3 (128 threads, thread r <-> TMEM lane r)
-// do the math and thread 0 issues the MMAs; warp 4 streams the v, b, c tiles
-// of upcoming chunks with TMA (128-byte swizzle, zero fill past T and d) and
-// the g values with plain loads into a 2-stage ring.
+// CTA = one (b, h), 8 warps (thread r <-> TMEM lane r & 127; warps w and
+// w + 4 share a lane quarter and split the columns).  Thread 0 issues the MMAs
+// and the TMA loads of v, b, c (128 B swizzle, zero fill past T and d) into a
+// 2-stage ring: the load of chunk k + 2 goes out as soon as chunk k's last MMA
+// has finished with its stage.  Threads 0..63 fetch g (and beta) one chunk
+// ahead into registers.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -51,75 +61,133 @@ using namespace tc;
 using namespace fwdtc;
 
 constexpr int kStages = 2;
-constexpr int kThreads = 160;
+constexpr int kMath = 256;
+constexpr int kThreads = kMath;
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_RING = 0;                       // stage s: V, B, C tiles (8 KB each)
+constexpr uint32_t OFF_RING = 0;
 constexpr uint32_t STAGE_BYTES = 3 * 8192;
-constexpr uint32_t OFF_A1 = OFF_RING + kStages * STAGE_BYTES;   // 128 x 64
-constexpr uint32_t OFF_B1 = OFF_A1 + 16384;            // 16 + 32 + 48 rows
-constexpr uint32_t OFF_B1a = OFF_B1, OFF_B1b = OFF_B1 + 2048, OFF_B1c = OFF_B1 + 6144;
-constexpr uint32_t OFF_A2 = OFF_B1 + 12288;
-constexpr uint32_t OFF_B2 = OFF_A2 + 16384;
-constexpr uint32_t OFF_A3 = OFF_B2 + 8192;            // L3 row operand, hi and lo parts
-constexpr uint32_t OFF_A3L = OFF_A3 + 16384;
-constexpr uint32_t OFF_B3 = OFF_A3L + 16384;           // L3 column operand, hi and lo parts
-constexpr uint32_t OFF_B3L = OFF_B3 + 8192;
-constexpr uint32_t OFF_CH0 = OFF_B3L + 8192;           // [Bhat^T ; P]        (hi parts)
-constexpr uint32_t OFF_CH0L = OFF_CH0 + 16384;         // [Bhat^T ; P]        (lo parts)
-constexpr uint32_t OFF_CH1 = OFF_CH0L + 16384;         // [0 ; Ctil]
-constexpr uint32_t OFF_S = OFF_CH1 + 16384;            // state, bf16 [i][j], hi part
-constexpr uint32_t OFF_SL = OFF_S + 8192;              // state, lo part
-constexpr uint32_t OFF_SMALL = OFF_SL + 8192;
+constexpr uint32_t OFF_X = kStages * STAGE_BYTES;      // reused phase by phase (100 KB)
+//   phase 1: the three decay levels (rows 0..63 c-side, rows 64..127 beta b-side)
+constexpr uint32_t X_A1 = 0, X_B1a = 16384, X_B1b = 18432, X_B1c = 22528;
+constexpr uint32_t X_A2 = 28672, X_B2 = 45056, X_A3 = 53248, X_A3L = 69632, X_B3 = 86016, X_B3L = 94208;
+//   gated, after the levels: [0 ; Ctil]
+constexpr uint32_t X_CH1 = 0;
+//   delta phase 2: [N | X0] = Dinv [L | R]
+constexpr uint32_t X_DINV = 0, X_LRH = 16384, X_LRL = 40960, X_M32 = 57344, X_DI32 = 61440;
+//   delta phase 3: [N^2 | N X0] = N [N | X0]
+constexpr uint32_t X_NA = 0, X_NXH = 16384, X_NXL = 40960;
+//   delta phase 4: [Util | W] = Z + N^2 Z
+constexpr uint32_t X_N2A = 0, X_ZH = 16384, X_ZL = 32768;
+//   delta phase 5: the state products
+constexpr uint32_t X_CW = 0, X_UH = 16384, X_UL = 24576;
+constexpr uint32_t X_BYTES = 102400;
+constexpr uint32_t OFF_CH0 = OFF_X + X_BYTES;          // [Bhat^T ; P] hi
+constexpr uint32_t OFF_CH0L = OFF_CH0 + 16384;         // [Bhat^T ; P] lo
+constexpr uint32_t OFF_S = OFF_CH0L + 16384;           // state bf16 [i][j], hi
+constexpr uint32_t OFF_SL = OFF_S + 8192;              // state, lo
+constexpr uint32_t OFF_K = OFF_SL + 8192;              // decay constants, 8 tables x [8][64] fp32
+constexpr uint32_t OFF_SMALL = OFF_K + 16384;
 constexpr uint32_t SMEM_BYTES = OFF_SMALL + 4096 + 1024;
 
+// decay-constant tables (all entries <= 1), indexed [table][8-block][channel]
+enum { K_A1 = 0, K_A2, K_0, K_B1_1, K_B1_2, K_B1_3, K_B2, K_BH };
+
 // TMEM columns
-constexpr uint32_t TM_D1a = 0, TM_D1b = 16, TM_D1c = 48, TM_D2 = 128, TM_D3 = 192, TM_CH = 256;
+constexpr uint32_t TM_D1a = 0, TM_D1b = 16, TM_D1c = 48, TM_D2 = 96, TM_D3 = 160;
+constexpr uint32_t TM_CHG = 256;                       // gated: [dS ; O]
+constexpr uint32_t TM_NX = 256;                        // delta: [N | X0V | X0W]
+constexpr uint32_t TM_N2X = 0;                         // delta: [N^2 | N X0]
+constexpr uint32_t TM_W = 192;                         // delta: W
+constexpr uint32_t TM_U = 448;                         // delta: Util, then [U ; Ctil S]
+constexpr uint32_t TM_CHD = 384;                       // delta: [dS ; P U]
 constexpr uint32_t TM_COLS = 512;
 
 struct Small {
-    float G[64];          // inclusive cumulative g of the current chunk
-    float A2[64];         // A[i] * log2(e)
-    float decay[64];      // exp(Gam_63[i])
+    float G[64];
+    float A2[64];
+    float decay[64];
     float scan[64];
     float g[kStages][64];
-    uint64_t full[kStages], empty[kStages], mma;
+    float beta[kStages][64];
+    uint64_t full[kStages], mma;
     uint32_t tmem_base;
     uint32_t unsafe;
     uint32_t abort;
     float a2max;
 };
 
+__device__ __forceinline__ void st_split16(unsigned char* thi, unsigned char* tlo, int row, int col16,
+                                           const float (&v)[16])
+{
+    float a[8], b[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) { a[k] = v[k]; b[k] = v[8 + k]; }
+    st_row8_split(thi, tlo, row, 2 * col16, a);
+    st_row8_split(thi, tlo, row, 2 * col16 + 1, b);
+}
 
-__global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_constant__ TcParams p)
+__device__ __forceinline__ void st_plain16(unsigned char* t, int row, int col16, const float (&v)[16])
+{
+    float a[8], b[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) { a[k] = v[k]; b[k] = v[8 + k]; }
+    st_row8(t, row, 2 * col16, a);
+    st_row8(t, row, 2 * col16 + 1, b);
+}
+
+__device__ __forceinline__ void zero_chunk(unsigned char* tile, int row, int q)
+{
+    *reinterpret_cast<uint4*>(tile + sw128(row, 8 * q)) = make_uint4(0, 0, 0, 0);
+}
+
+// D[d] (+)= A x B over K = 64 (four K = 16 steps); A K-major, B K- or MN-major
+__device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a, uint32_t b, bool b_mn, uint32_t idesc, bool acc)
+{
+#pragma unroll
+    for (int ks = 0; ks < 4; ks++)
+        mma_bf16(d, sdesc(a + ks * 32, 16, 1024), sdesc(b + (b_mn ? ks * 2048 : ks * 32), 8192, 1024), idesc,
+                 (acc || ks > 0) ? 1u : 0u);
+}
+
+__device__ __forceinline__ const float* ktab(const unsigned char* sm, int tab, int k8)
+{
+    return reinterpret_cast<const float*>(sm + OFF_K) + (tab * 8 + k8) * 64;
+}
+
+template <bool DELTA>
+__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char* X = sm + OFF_X;
     Small& S = *reinterpret_cast<Small*>(sm + OFF_SMALL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int u = blockIdx.x, bb = u / p.H, h = u % p.H;
     const int T = p.T, H = p.H, dk = p.dk, dv = p.dv;
 
-    // ---------------------------------------------------------------- setup
     if (tid < 64) {
         const float A = tid < dk ? -expf(p.A_log[h * dk + tid]) : 0.f;
         S.A2[tid] = A * kLog2e;
     }
     if (tid == 0) {
-        for (int s = 0; s < kStages; s++) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
+        for (int s = 0; s < kStages; s++) mbar_init(&S.full[s], 1);
         mbar_init(&S.mma, 1);
         S.abort = 0;
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(&S.tmem_base, TM_COLS);
-    if (warp == 4 && lane == 0) {
+    if (tid == 0) {
         tma_prefetch_desc(&p.tm_v); tma_prefetch_desc(&p.tm_b); tma_prefetch_desc(&p.tm_c);
     }
-    // constant zero rows: CH1 rows 0..63 (they multiply S into dS); written by
-    // the math threads, which fence them for the tensor cores below
-    if (tid < 128)
-        for (int idx = tid; idx < 64 * 8; idx += 128)
-            *reinterpret_cast<uint4*>(sm + OFF_CH1 + idx * 16) = make_uint4(0, 0, 0, 0);
+    // g (and beta) of the first chunks
+    for (int k = 0; k < kStages; k++)
+        if (tid < kC) {
+            const int t = k * kC + tid;
+            const size_t row = ((size_t)bb * T + t) * H + h;
+            S.g[k][tid] = t < T ? __bfloat162float(p.g[row]) : 0.f;
+            if (DELTA) S.beta[k][tid] = t < T ? __bfloat162float(p.beta[row]) : 0.f;
+        }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -129,53 +197,55 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
         S.a2max = m;
     }
     const uint32_t tbase = S.tmem_base;
+    auto issue_load = [&](int k) {   // thread 0: TMA of chunk k into its stage
+        const int s = k % kStages;
+        unsigned char* st = sm + OFF_RING + s * STAGE_BYTES;
+        mbar_arrive_expect_tx(&S.full[s], STAGE_BYTES);
+        tma_load_4d(st, &p.tm_v, &S.full[s], 0, h, k * kC, bb);
+        tma_load_4d(st + 8192, &p.tm_b, &S.full[s], 0, h, k * kC, bb);
+        tma_load_4d(st + 16384, &p.tm_c, &S.full[s], 0, h, k * kC, bb);
+    };
+    int issued = 0;
+    if (tid == 0)
+        for (; issued < kStages && issued < p.nchunks; issued++) issue_load(issued);
 
-    if (warp == 4) {
-        // ---------------------------------------------------------- producer
-        int issued = 0;
-        for (int k = 0; k < p.nchunks; k++) {
-            const int s = k % kStages;
-            if (k >= kStages && !wait_or_abort(&S.empty[s], ((k / kStages) - 1) & 1, &S.abort, p.status)) break;
-            issued = k + 1;
-            for (int tt = lane; tt < kC; tt += 32) {
-                const int t = k * kC + tt;
-                S.g[s][tt] = t < T ? __bfloat162float(p.g[((size_t)bb * T + t) * H + h]) : 0.f;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                unsigned char* st = sm + OFF_RING + s * STAGE_BYTES;
-                mbar_arrive_expect_tx(&S.full[s], STAGE_BYTES);
-                tma_load_4d(st, &p.tm_v, &S.full[s], 0, h, k * kC, bb);
-                tma_load_4d(st + 8192, &p.tm_b, &S.full[s], 0, h, k * kC, bb);
-                tma_load_4d(st + 16384, &p.tm_c, &S.full[s], 0, h, k * kC, bb);
-            }
-            __syncwarp();
-        }
-        // after an abort, let the copies already issued land before exiting
-        if (*(volatile uint32_t*)&S.abort && lane == 0)
-            for (int k = issued > kStages ? issued - kStages : 0; k < issued; k++)
-                mbar_wait(&S.full[k % kStages], (k / kStages) & 1, nullptr, 1u << 20);
-    } else {
+    {
         // ---------------------------------------------------------- math
-        const int r = tid;             // 0..127, TMEM lane
-        const int t = r & 63, hc = r >> 6;
-        float Sreg[64];                // state row i = r (threads 0..63)
-        if (r < 64) {
+        const int r = tid;                       // 0..255
+        const int q4 = warp & 3, wh = warp >> 2;  // TMEM lane quarter, column half
+        const int trow = r & 127;                // TMEM lane / accumulator row
+        const uint32_t tl = tbase + ((uint32_t)(q4 * 32) << 16);
+        const bool state_row = q4 < 2;           // rows 0..63 of the accumulators
+        float Sreg[32];                          // state row trow, columns 32 wh .. 32 wh + 31
+        if (state_row) {
 #pragma unroll
-            for (int j = 0; j < 64; j++)
-                Sreg[j] = (p.h0 && r < dk && j < dv) ? p.h0[((size_t)u * dk + r) * dv + j] : 0.f;
+            for (int j = 0; j < 32; j++) {
+                const int jj = 32 * wh + j;
+                Sreg[j] = (p.h0 && trow < dk && jj < dv) ? p.h0[((size_t)u * dk + trow) * dv + jj] : 0.f;
+            }
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
+            for (int q = 0; q < 4; q++) {
                 float v8[8];
 #pragma unroll
                 for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
-                st_row8_split(sm + OFF_S, sm + OFF_SL, r, q, v8);
+                st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
             }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kMath);
         uint32_t mma_phase = 0;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        auto mma_wait_all = [&]() -> bool {
+            if (!wait_or_abort(&S.mma, mma_phase, &S.abort, p.status)) return false;
+            mma_phase ^= 1;
+            tc_fence_after();
+            return true;
+        };
+        auto smem_to_tc = [&]() {   // generic-proxy smem writes -> visible to the tensor cores
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar_sync(1, kMath);
+            tc_fence_after();
+        };
 
         for (int k = 0; k < p.nchunks; k++) {
             const int s = k % kStages;
@@ -183,8 +253,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
             unsigned char* sV = sm + OFF_RING + s * STAGE_BYTES;
             unsigned char* sB = sV + 8192;
             unsigned char* sCt = sV + 16384;
+            float g_next = 0.f, beta_next = 0.f;   // g, beta of chunk k + kStages (threads 0..63)
+            if (r < kC && k + kStages < p.nchunks) {
+                const int t = (k + kStages) * kC + r;
+                const size_t row = ((size_t)bb * T + t) * H + h;
+                if (t < T) {
+                    g_next = __bfloat162float(p.g[row]);
+                    if (DELTA) beta_next = __bfloat162float(p.beta[row]);
+                }
+            }
 
-            // (1) inclusive scan of g over the chunk
+            // (1) inclusive scan of g; overflow check of the anchors
             if (r < 64) {
                 float x = S.g[s][r];
 #pragma unroll
@@ -194,9 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
                 }
                 S.scan[r] = x;
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(1, kMath);
             if (r < 64) S.G[r] = S.scan[r] + (r >= 32 ? S.scan[31] : 0.f);
-            named_bar_sync(1, 128);
+            named_bar_sync(1, kMath);
             if (warp == 0) {
                 float span = 0.f;
                 if (lane < 8) {
@@ -206,220 +285,551 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_gated_kernel(const __grid_
                 const bool bad = __any_sync(0xffffffffu, span * S.a2max > kSafeLog2);
                 if (lane == 0) S.unsafe = bad ? 1u : 0u;
             }
-
-            // (2) decay-scaled operands
+            // decay constants per (8-block, reference point); every exponent <= 0
             {
-                const float Gt = S.G[t];
-                const int I = t >> 4;
-                const float Gr1 = I > 0 ? S.G[16 * I - 1] : 0.f;
-                const float Gr2 = S.G[16 * I + 7];
-                const float Gr3 = S.G[8 * (t >> 3) + 3];
+                float* K = reinterpret_cast<float*>(sm + OFF_K);
+#pragma unroll
+                for (int rep = 0; rep < 2; rep++) {
+                    const int pr = r + rep * kMath;
+                    const int k8 = pr >> 6, i = pr & 63, J = k8 >> 1;
+                    const float a2 = S.A2[i], Gref = S.G[8 * k8 + 3];
+                    K[(K_A1 * 8 + k8) * 64 + i] = J >= 1 ? exp2f(a2 * (Gref - S.G[16 * J - 1])) : 0.f;
+                    K[(K_A2 * 8 + k8) * 64 + i] = (k8 & 1) ? exp2f(a2 * (Gref - S.G[16 * J + 7])) : 0.f;
+                    K[(K_0 * 8 + k8) * 64 + i] = exp2f(a2 * Gref);
+                    K[(K_B1_1 * 8 + k8) * 64 + i] = J < 1 ? exp2f(a2 * (S.G[15] - Gref)) : 0.f;
+                    K[(K_B1_2 * 8 + k8) * 64 + i] = J < 2 ? exp2f(a2 * (S.G[31] - Gref)) : 0.f;
+                    K[(K_B1_3 * 8 + k8) * 64 + i] = J < 3 ? exp2f(a2 * (S.G[47] - Gref)) : 0.f;
+                    K[(K_B2 * 8 + k8) * 64 + i] = (k8 & 1) ? 0.f : exp2f(a2 * (S.G[16 * J + 7] - Gref));
+                    K[(K_BH * 8 + k8) * 64 + i] = exp2f(a2 * (S.G[63] - Gref));
+                }
+            }
+            named_bar_sync(1, kMath);
+
+            // (2) decay-scaled operands; thread = (row t, 16 channels)
+            const bool unsafe = S.unsafe != 0;
+            float keep[16];   // gated: Ctil row part; delta: beta Btil row part
+            {
+                const int t = r & 63, cq = r >> 6, k8 = t >> 3, I = t >> 4;
                 const bool upper = (t & 15) >= 8;
-#pragma unroll 1
-                for (int qq = 0; qq < 4; qq++) {
-                    const int q = hc * 4 + qq;
-                    float cv[8], bv[8], y[8];
+                const float Gt = S.G[t], Gr = S.G[8 * k8 + 3];
+                const float dG = Gt - Gr;
+                const float bet = DELTA ? S.beta[s][t] : 0.f;
+                const float* KA1 = ktab(sm, K_A1, k8);
+                const float* KA2 = ktab(sm, K_A2, k8);
+                const float* K0 = ktab(sm, K_0, k8);
+                const float* KB11 = ktab(sm, K_B1_1, k8);
+                const float* KB12 = ktab(sm, K_B1_2, k8);
+                const float* KB13 = ktab(sm, K_B1_3, k8);
+                const float* KB2 = ktab(sm, K_B2, k8);
+                // direct reference values for the overflow fallback
+                const float GI = I > 0 ? S.G[16 * I - 1] : 0.f, GJ7 = S.G[16 * I + 7];
+#pragma unroll
+                for (int qq = 0; qq < 2; qq++) {
+                    const int q = 2 * cq + qq;
+                    float cv[8], bv[8], a2[8], ax[8], bxp[8], bbx[8], y[8], z[8];
                     ld_row8(sCt, t, q, cv);
                     ld_row8(sB, t, q, bv);
-                    // rows (P side)
-                    if (I > 0) { scale8(cv, S.A2, q, Gt - Gr1, y); st_row8_f16(sm + OFF_A1, t, q, y); }
-                    if (upper) { scale8(cv, S.A2, q, Gt - Gr2, y); st_row8_f16(sm + OFF_A2, t, q, y); }
-                    scale8(cv, S.A2, q, Gt - Gr3, y); st_row8_split(sm + OFF_A3, sm + OFF_A3L, t, q, y);
-                    scale8(cv, S.A2, q, Gt, y); st_row8(sm + OFF_CH1, 64 + t, q, y);
-                    // columns (b side): row s = t of the B operands
-                    if (I < 1) { scale8(bv, S.A2, q, S.G[15] - Gt, y); st_row8_f16(sm + OFF_B1a, t, q, y); }
-                    if (I < 2) { scale8(bv, S.A2, q, S.G[31] - Gt, y); st_row8_f16(sm + OFF_B1b, t, q, y); }
-                    if (I < 3) { scale8(bv, S.A2, q, S.G[47] - Gt, y); st_row8_f16(sm + OFF_B1c, t, q, y); }
-                    if (!upper) { scale8(bv, S.A2, q, Gr2 - Gt, y); st_row8_f16(sm + OFF_B2, t, q, y); }
-                    scale8(bv, S.A2, q, Gr3 - Gt, y); st_row8_split(sm + OFF_B3, sm + OFF_B3L, t, q, y);
-                }
-                // Bhat^T: row i = t (channel), columns s in [32 hc, 32 hc + 32)
-                {
-                    const int i = t;
-                    const float a2 = S.A2[i], G63 = S.G[63];
-#pragma unroll 1
-                    for (int qq = 0; qq < 4; qq++) {
-                        float y8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        a2[e] = S.A2[8 * q + e];
+                        const float an = exp2f(a2[e] * dG), ai = exp2f(-a2[e] * dG);
+                        ax[e] = cv[e] * an;
+                        bxp[e] = bv[e] * ai;
+                        bbx[e] = bet * bv[e] * an;
+                    }
+                    if (I > 0) {
 #pragma unroll
                         for (int e = 0; e < 8; e++) {
-                            const int sc = 32 * hc + 8 * qq + e;
+                            const float f = unsafe ? exp2f(a2[e] * (Gt - GI)) : KA1[8 * q + e];
+                            y[e] = unsafe ? cv[e] * f : ax[e] * f;
+                            z[e] = unsafe ? bet * bv[e] * f : bbx[e] * f;
+                        }
+                        st_row8_f16(X + X_A1, t, q, y);
+                        if (DELTA) st_row8_f16(X + X_A1, 64 + t, q, z);
+                    }
+                    if (upper) {
+#pragma unroll
+                        for (int e = 0; e < 8; e++) {
+                            const float f = unsafe ? exp2f(a2[e] * (Gt - GJ7)) : KA2[8 * q + e];
+                            y[e] = unsafe ? cv[e] * f : ax[e] * f;
+                            z[e] = unsafe ? bet * bv[e] * f : bbx[e] * f;
+                        }
+                        st_row8_f16(X + X_A2, t, q, y);
+                        if (DELTA) st_row8_f16(X + X_A2, 64 + t, q, z);
+                    }
+                    st_row8_split(X + X_A3, X + X_A3L, t, q, ax);
+                    if (DELTA) st_row8_split(X + X_A3, X + X_A3L, 64 + t, q, bbx);
+                    // column side (row s = t of the B operands)
+                    if (I < 1) {
+#pragma unroll
+                        for (int e = 0; e < 8; e++)
+                            y[e] = unsafe ? bv[e] * exp2f(a2[e] * (S.G[15] - Gt)) : bxp[e] * KB11[8 * q + e];
+                        st_row8_f16(X + X_B1a, t, q, y);
+                    }
+                    if (I < 2) {
+#pragma unroll
+                        for (int e = 0; e < 8; e++)
+                            y[e] = unsafe ? bv[e] * exp2f(a2[e] * (S.G[31] - Gt)) : bxp[e] * KB12[8 * q + e];
+                        st_row8_f16(X + X_B1b, t, q, y);
+                    }
+                    if (I < 3) {
+#pragma unroll
+                        for (int e = 0; e < 8; e++)
+                            y[e] = unsafe ? bv[e] * exp2f(a2[e] * (S.G[47] - Gt)) : bxp[e] * KB13[8 * q + e];
+                        st_row8_f16(X + X_B1c, t, q, y);
+                    }
+                    if (!upper) {
+#pragma unroll
+                        for (int e = 0; e < 8; e++)
+                            y[e] = unsafe ? bv[e] * exp2f(a2[e] * (GJ7 - Gt)) : bxp[e] * KB2[8 * q + e];
+                        st_row8_f16(X + X_B2, t, q, y);
+                    }
+                    st_row8_split(X + X_B3, X + X_B3L, t, q, bxp);
+                    // chunk-start factor exp(A G_t): Ctil (gated) or beta Btil (delta)
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        const float f0 = unsafe ? exp2f(a2[e] * Gt) : K0[8 * q + e];
+                        keep[8 * qq + e] = DELTA ? (unsafe ? bet * bv[e] * f0 : bbx[e] * f0)
+                                                 : (unsafe ? cv[e] * f0 : ax[e] * f0);
+                    }
+                }
+            }
+            named_bar_sync(1, kMath);
+            // (2b) Bhat^T rows (i = channel), from the L3 column operand; decay vector
+            {
+                const int i = r & 63, sq = r >> 6;
+                const float a2 = S.A2[i], G63 = S.G[63];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    float y8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        const int sc = 16 * sq + 8 * h2 + e;
+                        if (unsafe) {
                             const float bval = bf2f(*reinterpret_cast<const uint16_t*>(sB + sw128(sc, i)));
                             y8[e] = bval * exp2f(a2 * (G63 - S.G[sc]));
+                        } else {
+                            const float b3 = bf2f(*reinterpret_cast<const uint16_t*>(X + X_B3 + sw128(sc, i))) +
+                                             bf2f(*reinterpret_cast<const uint16_t*>(X + X_B3L + sw128(sc, i)));
+                            y8[e] = b3 * ktab(sm, K_BH, sc >> 3)[i];
                         }
-                        st_row8_split(sm + OFF_CH0, sm + OFF_CH0L, i, 4 * hc + qq, y8);
                     }
+                    st_row8_split(sm + OFF_CH0, sm + OFF_CH0L, i, 2 * sq + h2, y8);
                 }
                 if (r < 64) S.decay[r] = exp2f(S.A2[r] * S.G[63]);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar_sync(1, 128);
-            tc_fence_after();
+            smem_to_tc();
 
-            // (3) the three levels of P
+            // (3) level MMAs
             if (r == 0) {
-                const uint32_t a1 = smem_u32(sm + OFF_A1), a2 = smem_u32(sm + OFF_A2), a3 = smem_u32(sm + OFF_A3);
-                const uint32_t b1[3] = {smem_u32(sm + OFF_B1a), smem_u32(sm + OFF_B1b), smem_u32(sm + OFF_B1c)};
+                const uint32_t x0 = smem_u32(X);
+                const uint32_t b1[3] = {x0 + X_B1a, x0 + X_B1b, x0 + X_B1c};
                 const uint32_t d1[3] = {TM_D1a, TM_D1b, TM_D1c};
+#pragma unroll
                 for (int I = 1; I <= 3; I++)
-                    for (int ks = 0; ks < 4; ks++)
-                        mma_bf16(tbase + d1[I - 1], sdesc(a1 + ks * 32, 16, 1024), sdesc(b1[I - 1] + ks * 32, 16, 1024),
-                                 idesc_f16(128, 16 * I, false, false), ks > 0);
-                for (int ks = 0; ks < 4; ks++)
-                    mma_bf16(tbase + TM_D2, sdesc(a2 + ks * 32, 16, 1024),
-                             sdesc(smem_u32(sm + OFF_B2) + ks * 32, 16, 1024), idesc_f16(128, 64, false, false), ks > 0);
-                const uint32_t a3l = smem_u32(sm + OFF_A3L);
-                const uint32_t b3 = smem_u32(sm + OFF_B3), b3l = smem_u32(sm + OFF_B3L);
-                const uint32_t l3a[3] = {a3, a3, a3l}, l3b[3] = {b3, b3l, b3};
-                for (int part = 0; part < 3; part++)
-                    for (int ks = 0; ks < 4; ks++)
-                        mma_bf16(tbase + TM_D3, sdesc(l3a[part] + ks * 32, 16, 1024), sdesc(l3b[part] + ks * 32, 16, 1024),
-                                 idesc_bf16(128, 64, false, false), (part | ks) > 0);
+                    mma_k64(tbase + d1[I - 1], x0 + X_A1, b1[I - 1], false, idesc_f16(128, 16 * I, false, false), false);
+                mma_k64(tbase + TM_D2, x0 + X_A2, x0 + X_B2, false, idesc_f16(128, 64, false, false), false);
+                const uint32_t id3 = idesc_bf16(128, 64, false, false);
+                mma_k64(tbase + TM_D3, x0 + X_A3, x0 + X_B3, false, id3, false);
+                mma_k64(tbase + TM_D3, x0 + X_A3, x0 + X_B3L, false, id3, true);
+                mma_k64(tbase + TM_D3, x0 + X_A3L, x0 + X_B3, false, id3, true);
                 mma_commit(&S.mma);
             }
-            if (!wait_or_abort(&S.mma, mma_phase, &S.abort, p.status)) break;
-            mma_phase ^= 1;
-            tc_fence_after();
+            if (!mma_wait_all()) break;
 
-            // (4) assemble P (rows t = 0..63 -> CH0 rows 64..127)
-            if (warp < 2) {
-                const bool unsafe = S.unsafe != 0;
-                const int tb = t >> 4;
-                float ew[8];   // exact same-8-block entries when the L3 split is unsafe
-                if (unsafe) {
-                    const int s0 = 8 * (t >> 3);
+            // (4) assemble P (lanes 0..63) and M (lanes 64..127); thread = (row, 32 columns)
+            {
+                const bool isM = q4 >= 2;
+                if (!isM || DELTA) {
+                    const int t = trow & 63, wl = q4 & 1, tb = t >> 4;
+                    float ew[8];
+                    if (unsafe) {
+                        const int s0 = 8 * (t >> 3);
+                        const float bet = DELTA ? S.beta[s][t] : 0.f;
 #pragma unroll
-                    for (int e = 0; e < 8; e++) {
-                        float acc = 0.f;
-                        const int sc = s0 + e;
-                        if (sc <= t) {
-                            for (int q = 0; q < 8; q++) {
-                                float cv[8], bv[8];
-                                ld_row8(sCt, t, q, cv);
-                                ld_row8(sB, sc, q, bv);
+                        for (int e = 0; e < 8; e++) {
+                            float acc = 0.f;
+                            const int sc = s0 + e;
+                            if (sc < t || (sc == t && !isM)) {
+                                for (int q = 0; q < 8; q++) {
+                                    float xv[8], bv[8];
+                                    ld_row8(isM ? sB : sCt, t, q, xv);
+                                    ld_row8(sB, sc, q, bv);
 #pragma unroll
-                                for (int kk = 0; kk < 8; kk++)
-                                    acc += cv[kk] * bv[kk] * exp2f(S.A2[8 * q + kk] * (S.G[t] - S.G[sc]));
+                                    for (int kk = 0; kk < 8; kk++)
+                                        acc += xv[kk] * bv[kk] * exp2f(S.A2[8 * q + kk] * (S.G[t] - S.G[sc]));
+                                }
+                            }
+                            ew[e] = isM ? bet * acc : acc;
+                        }
+                    }
+                    const int Ia = 2 * wl, Ib = 2 * wl + 1;
+                    const uint32_t colA = wl == 0 ? 0u : TM_D1b, colB = wl == 0 ? TM_D1a : TM_D1c;
+                    float* M32 = reinterpret_cast<float*>(X + X_M32);
+#pragma unroll
+                    for (int cc = 0; cc < 2; cc++) {
+                        const int cg = 2 * wh + cc;
+                        float out[16];
+                        if (16 * cg > 32 * wl + 31) {
+#pragma unroll
+                            for (int c = 0; c < 16; c++) out[c] = 0.f;
+                        } else {
+                            float v1a[16], v1b[16], v2[16], v3[16];
+                            if (Ia >= 1 && cg < Ia) tmem_ld16(tl + colA + 16 * cg, v1a);
+                            if (cg < Ib) tmem_ld16(tl + colB + 16 * cg, v1b);
+                            tmem_ld16(tl + TM_D2 + 16 * cg, v2);
+                            tmem_ld16(tl + TM_D3 + 16 * cg, v3);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 16; c++) {
+                                const int sc = 16 * cg + c;
+                                float val;
+                                if (sc > t || (isM && sc == t)) val = 0.f;
+                                else if ((sc >> 4) < tb) val = (tb == Ia) ? v1a[c] : v1b[c];
+                                else if ((sc >> 3) < (t >> 3)) val = v2[c];
+                                else val = unsafe ? ew[c & 7] : v3[c];
+                                out[c] = val;
                             }
                         }
-                        ew[e] = acc;
-                    }
-                }
+                        if (!isM) {
+                            st_split16(sm + OFF_CH0, sm + OFF_CH0L, 64 + t, cg, out);
+                        } else {
+                            float lpart[16];
 #pragma unroll
-                for (int cg = 0; cg < 4; cg++) {
-                    float out[16];
-                    if (16 * cg > 32 * warp + 31) {
+                            for (int c = 0; c < 16; c++) lpart[c] = (cg < tb) ? out[c] : 0.f;
+                            st_plain16(X + X_LRH, t, cg, lpart);
+                            if (cg == tb) {
 #pragma unroll
-                        for (int c = 0; c < 16; c++) out[c] = 0.f;
-                    } else {
-                        float v1a[16], v1b[16], v2[16], v3[16];
-                        const int Ia = 2 * warp, Ib = 2 * warp + 1;   // row blocks in this warp
-                        // warp 0 holds row blocks 0 and 1, warp 1 holds row blocks 2 and 3
-                        const uint32_t colA = warp == 0 ? 0u : TM_D1b, colB = warp == 0 ? TM_D1a : TM_D1c;
-                        if (Ia >= 1 && cg < Ia) tmem_ld16(tbase + lane_base + colA + 16 * cg, v1a);
-                        if (cg < Ib) tmem_ld16(tbase + lane_base + colB + 16 * cg, v1b);
-                        tmem_ld16(tbase + lane_base + TM_D2 + 16 * cg, v2);
-                        tmem_ld16(tbase + lane_base + TM_D3 + 16 * cg, v3);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 16; c++) {
-                            const int sc = 16 * cg + c;
-                            float val;
-                            if (sc > t) val = 0.f;
-                            else if ((sc >> 4) < tb) val = (tb == Ia) ? v1a[c] : v1b[c];
-                            else if ((sc >> 3) < (t >> 3)) val = v2[c];
-                            else val = unsafe ? ew[c & 7] : v3[c];
-                            out[c] = val;
+                                for (int c = 0; c < 16; c++) M32[(tb * 16 + (t & 15)) * 16 + c] = out[c];
+                            }
                         }
                     }
-                    float first[8], second[8];
-#pragma unroll
-                    for (int c = 0; c < 8; c++) { first[c] = out[c]; second[c] = out[8 + c]; }
-                    st_row8_split(sm + OFF_CH0, sm + OFF_CH0L, 64 + t, 2 * cg, first);
-                    st_row8_split(sm + OFF_CH0, sm + OFF_CH0L, 64 + t, 2 * cg + 1, second);
                 }
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar_sync(1, 128);
-            tc_fence_after();
-
-            // (5) [dS ; O] = [[Bhat^T, 0], [P, Ctil]] x [V ; S]
-            if (r == 0) {
-                const uint32_t ch0 = smem_u32(sm + OFF_CH0), ch0l = smem_u32(sm + OFF_CH0L);
-                const uint32_t ch1 = smem_u32(sm + OFF_CH1);
-                const uint32_t vt = smem_u32(sV), st = smem_u32(sm + OFF_S), stl = smem_u32(sm + OFF_SL);
-                const uint32_t id = idesc_bf16(128, 64, false, true);
-                const uint32_t pa[4] = {ch0, ch0l, ch1, ch1}, pb[4] = {vt, vt, st, stl};
-                for (int part = 0; part < 4; part++)
-                    for (int ks = 0; ks < 4; ks++)
-                        mma_bf16(tbase + TM_CH, sdesc(pa[part] + ks * 32, 16, 1024), sdesc(pb[part] + ks * 2048, 8192, 1024),
-                                 id, (part | ks) > 0);
-                mma_commit(&S.empty[s]);
-                mma_commit(&S.mma);
-            }
-            if (!wait_or_abort(&S.mma, mma_phase, &S.abort, p.status)) break;
-            mma_phase ^= 1;
-            tc_fence_after();
-
-            // (6) state update (rows 0..63) and output (rows 64..127)
-            if (r < 64) {
-                const float dec = S.decay[r];
+            {
+                const int t = r & 63, cq = r >> 6;
+                if (!DELTA) {
+                    // [0 ; Ctil] for the output MMA (the levels' space is free now)
 #pragma unroll
-                for (int cg = 0; cg < 4; cg++) {
+                    for (int qq = 0; qq < 2; qq++) {
+                        float y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++) y[e] = keep[8 * qq + e];
+                        st_row8(X + X_CH1, 64 + t, 2 * cq + qq, y);
+                        zero_chunk(X + X_CH1, t, 2 * cq + qq);
+                    }
+                } else {
+                    // R = [beta V | beta Btil]: hi in LRH blocks 1-2, lo in LRL blocks 0-1
+                    const float bet = S.beta[s][t];
+#pragma unroll
+                    for (int qq = 0; qq < 2; qq++) {
+                        const int q = 2 * cq + qq;
+                        float vv[8], y[8];
+                        ld_row8(sV, t, q, vv);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) y[e] = bet * vv[e];
+                        st_row8_split(X + X_LRH + 8192, X + X_LRL, t, q, y);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) y[e] = keep[8 * qq + e];
+                        st_row8_split(X + X_LRH + 16384, X + X_LRL + 8192, t, q, y);
+                    }
+                }
+            }
+
+            if constexpr (!DELTA) {
+                smem_to_tc();
+                // (5g) [dS ; O] = [[Bhat^T, 0], [P, Ctil]] x [V ; S]  (hi/lo parts)
+                if (r == 0) {
+                    const uint32_t ch0 = smem_u32(sm + OFF_CH0), ch0l = smem_u32(sm + OFF_CH0L);
+                    const uint32_t ch1 = smem_u32(X + X_CH1);
+                    const uint32_t vt = smem_u32(sV), st = smem_u32(sm + OFF_S), stl = smem_u32(sm + OFF_SL);
+                    const uint32_t id = idesc_bf16(128, 64, false, true);
+                    mma_k64(tbase + TM_CHG, ch0, vt, true, id, false);
+                    mma_k64(tbase + TM_CHG, ch0l, vt, true, id, true);
+                    mma_k64(tbase + TM_CHG, ch1, st, true, id, true);
+                    mma_k64(tbase + TM_CHG, ch1, stl, true, id, true);
+                    mma_commit(&S.mma);
+                }
+                if (!mma_wait_all()) break;
+            } else {
+                named_bar_sync(1, kMath);
+                // (5) exact inverse of the diagonal 16-blocks of I + M
+                if (r < 64) {
+                    const int J = r >> 4, c = r & 15;
+                    const float* M32 = reinterpret_cast<const float*>(X + X_M32) + J * 256;
+                    float xs[16];
+#pragma unroll
+                    for (int q = 0; q < 16; q++) {
+                        float acc = 0.f;
+#pragma unroll
+                        for (int pp = 0; pp < q; pp++)
+                            if (pp >= c) acc = fmaf(M32[q * 16 + pp], xs[pp], acc);
+                        xs[q] = (q < c) ? 0.f : (q == c ? 1.f : -acc);
+                    }
+                    float* DI32 = reinterpret_cast<float*>(X + X_DI32) + J * 256;
+#pragma unroll
+                    for (int q = 0; q < 16; q++) DI32[q * 16 + c] = xs[q];
+                }
+                named_bar_sync(1, kMath);
+                {
+                    // [Dinv ; 0]: row trow, 32 columns of half wh
+                    const int J = (trow & 63) >> 4;
+                    const float* DI32 = reinterpret_cast<const float*>(X + X_DI32) + J * 256 + (trow & 15) * 16;
+#pragma unroll
+                    for (int cc = 0; cc < 2; cc++) {
+                        const int cg = 2 * wh + cc;
+                        float v16[16];
+#pragma unroll
+                        for (int c = 0; c < 16; c++) v16[c] = (trow < 64 && cg == J) ? DI32[c] : 0.f;
+                        st_plain16(X + X_DINV, trow, cg, v16);
+                    }
+                }
+                smem_to_tc();
+
+                // (6) [N | X0] = Dinv [L | R]
+                if (r == 0) {
+                    const uint32_t x0 = smem_u32(X);
+                    mma_k64(tbase + TM_NX, x0 + X_DINV, x0 + X_LRH, true, idesc_bf16(128, 192, false, true), false);
+                    mma_k64(tbase + TM_NX + 64, x0 + X_DINV, x0 + X_LRL, true, idesc_bf16(128, 128, false, true),
+                            true);
+                    mma_commit(&S.mma);
+                }
+                if (!mma_wait_all()) break;
+
+                // (7) N -> A operand and B block; X0 -> hi/lo B blocks
+                if (state_row) {
+                    const int t = trow;
+#pragma unroll
+                    for (int gg = 0; gg < 6; gg++) {
+                        const int g = 6 * wh + gg;
+                        float v[16];
+                        tmem_ld16(tl + TM_NX + 16 * g, v);
+                        tmem_wait_ld();
+                        if (g < 4) {
+                            st_plain16(X + X_NA, t, g, v);
+                            st_plain16(X + X_NXH, t, g, v);
+                        } else {
+                            const int xg = g - 4;
+                            const uint32_t blk = (uint32_t)(xg >> 2) * 8192u;
+                            st_split16(X + X_NXH + 8192 + blk, X + X_NXL + blk, t, xg & 3, v);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) zero_chunk(X + X_NA, trow, 4 * wh + q);
+                }
+                smem_to_tc();
+
+                // (8) [N^2 | N X0] = N [N | X0]
+                if (r == 0) {
+                    const uint32_t x0 = smem_u32(X);
+                    mma_k64(tbase + TM_N2X, x0 + X_NA, x0 + X_NXH, true, idesc_bf16(128, 192, false, true), false);
+                    mma_k64(tbase + TM_N2X + 64, x0 + X_NA, x0 + X_NXL, true, idesc_bf16(128, 128, false, true), true);
+                    mma_commit(&S.mma);
+                }
+                if (!mma_wait_all()) break;
+
+                // (9) N^2 -> A operand; Z = X0 - N X0 -> hi/lo B blocks and, exactly, TMEM (Util | W)
+                if (state_row) {
+                    const int t = trow;
+#pragma unroll
+                    for (int gg = 0; gg < 6; gg++) {
+                        const int g = 6 * wh + gg;
+                        if (g < 4) {
+                            float v[16];
+                            tmem_ld16(tl + TM_N2X + 16 * g, v);
+                            tmem_wait_ld();
+                            st_plain16(X + X_N2A, t, g, v);
+                        } else {
+                            const int xg = g - 4;
+                            float x0v[16], nx[16];
+                            tmem_ld16(tl + TM_NX + 64 + 16 * xg, x0v);
+                            tmem_ld16(tl + TM_N2X + 64 + 16 * xg, nx);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 16; c++) x0v[c] -= nx[c];
+                            const uint32_t blk = (uint32_t)(xg >> 2) * 8192u;
+                            st_split16(X + X_ZH + blk, X + X_ZL + blk, t, xg & 3, x0v);
+                            tmem_st16(tl + (xg < 4 ? TM_U + 16 * xg : TM_W + 16 * (xg - 4)), x0v);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) zero_chunk(X + X_N2A, trow, 4 * wh + q);
+                    float zz[16];
+#pragma unroll
+                    for (int c = 0; c < 16; c++) zz[c] = 0.f;
+#pragma unroll
+                    for (int cg = 0; cg < 4; cg++) tmem_st16(tl + (wh == 0 ? TM_W : TM_U) + 16 * cg, zz);
+                }
+                tmem_wait_st();
+                smem_to_tc();
+
+                // (10) Util += N^2 ZV,  W += N^2 ZW
+                if (r == 0) {
+                    const uint32_t x0 = smem_u32(X);
+                    const uint32_t id = idesc_bf16(128, 64, false, true);
+                    mma_k64(tbase + TM_U, x0 + X_N2A, x0 + X_ZH, true, id, true);
+                    mma_k64(tbase + TM_U, x0 + X_N2A, x0 + X_ZL, true, id, true);
+                    mma_k64(tbase + TM_W, x0 + X_N2A, x0 + X_ZH + 8192, true, id, true);
+                    mma_k64(tbase + TM_W, x0 + X_N2A, x0 + X_ZL + 8192, true, id, true);
+                    mma_commit(&S.mma);
+                }
+                if (!mma_wait_all()) break;
+
+                // (11) CW = [-W ; Ctil]
+                if (state_row) {
+#pragma unroll
+                    for (int cc = 0; cc < 2; cc++) {
+                        const int cg = 2 * wh + cc;
+                        float v[16];
+                        tmem_ld16(tl + TM_W + 16 * cg, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; c++) v[c] = -v[c];
+                        st_plain16(X + X_CW, trow, cg, v);
+                    }
+                } else {
+                    const int t = trow - 64;
+                    const float Gt = S.G[t];
+#pragma unroll
+                    for (int qq = 0; qq < 4; qq++) {
+                        const int q = 4 * wh + qq;
+                        float cv[8], y[8];
+                        ld_row8(sCt, t, q, cv);
+                        scale8(cv, S.A2, q, Gt, y);
+                        st_row8(X + X_CW, trow, q, y);
+                    }
+                }
+                smem_to_tc();
+
+                // (12) [U ; Ctil S] = [Util ; 0] + [-W ; Ctil] S
+                if (r == 0) {
+                    const uint32_t x0 = smem_u32(X);
+                    const uint32_t id = idesc_bf16(128, 64, false, true);
+                    mma_k64(tbase + TM_U, x0 + X_CW, smem_u32(sm + OFF_S), true, id, true);
+                    mma_k64(tbase + TM_U, x0 + X_CW, smem_u32(sm + OFF_SL), true, id, true);
+                    mma_commit(&S.mma);
+                }
+                if (!mma_wait_all()) break;
+
+                // (13) U -> hi/lo B tiles
+                if (state_row) {
+#pragma unroll
+                    for (int cc = 0; cc < 2; cc++) {
+                        const int cg = 2 * wh + cc;
+                        float v[16];
+                        tmem_ld16(tl + TM_U + 16 * cg, v);
+                        tmem_wait_ld();
+                        st_split16(X + X_UH, X + X_UL, trow, cg, v);
+                    }
+                }
+                smem_to_tc();
+
+                // (14) [dS ; P U] = [Bhat^T ; P] U
+                if (r == 0) {
+                    const uint32_t x0 = smem_u32(X);
+                    const uint32_t ch0 = smem_u32(sm + OFF_CH0), ch0l = smem_u32(sm + OFF_CH0L);
+                    const uint32_t id = idesc_bf16(128, 64, false, true);
+                    mma_k64(tbase + TM_CHD, ch0, x0 + X_UH, true, id, false);
+                    mma_k64(tbase + TM_CHD, ch0l, x0 + X_UH, true, id, true);
+                    mma_k64(tbase + TM_CHD, ch0, x0 + X_UL, true, id, true);
+                    mma_commit(&S.mma);
+                }
+                if (!mma_wait_all()) break;
+            }
+
+            // (15) state update (lanes 0..63) and output (lanes 64..127), 32 columns per thread
+            const uint32_t tm_out = DELTA ? TM_CHD : TM_CHG;
+            if (state_row) {
+                const float dec = S.decay[trow];
+#pragma unroll
+                for (int cc = 0; cc < 2; cc++) {
                     float v[16];
-                    tmem_ld16(tbase + lane_base + TM_CH + 16 * cg, v);
+                    tmem_ld16(tl + tm_out + 32 * wh + 16 * cc, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 16; c++) Sreg[16 * cg + c] = fmaf(dec, Sreg[16 * cg + c], v[c]);
+                    for (int c = 0; c < 16; c++) Sreg[16 * cc + c] = fmaf(dec, Sreg[16 * cc + c], v[c]);
                 }
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
+                for (int q = 0; q < 4; q++) {
                     float v8[8];
 #pragma unroll
                     for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
-                    st_row8_split(sm + OFF_S, sm + OFF_SL, r, q, v8);
+                    st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
                 }
             } else {
-                const int tg = k * kC + t;
+                const int tg = k * kC + (trow - 64);
                 __nv_bfloat16* orow = p.o + (((size_t)bb * T + tg) * H + h) * dv;
 #pragma unroll
-                for (int cg = 0; cg < 4; cg++) {
+                for (int cc = 0; cc < 2; cc++) {
+                    const int col = 32 * wh + 16 * cc;
                     float v[16];
-                    tmem_ld16(tbase + lane_base + TM_CH + 16 * cg, v);
-                    tmem_wait_ld();
+                    tmem_ld16(tl + tm_out + col, v);
+                    if (DELTA) {
+                        float w2[16];
+                        tmem_ld16(tl + TM_U + col, w2);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; c++) v[c] += w2[c];
+                    } else {
+                        tmem_wait_ld();
+                    }
                     if (tg < T) {
 #pragma unroll
                         for (int hq = 0; hq < 2; hq++) {
-                            const int j0 = 16 * cg + 8 * hq;
+                            const int j0 = col + 8 * hq;
                             if (j0 < dv) {
-                                uint4 w;
-                                w.x = pack_bf16(v[8 * hq + 0], v[8 * hq + 1]);
-                                w.y = pack_bf16(v[8 * hq + 2], v[8 * hq + 3]);
-                                w.z = pack_bf16(v[8 * hq + 4], v[8 * hq + 5]);
-                                w.w = pack_bf16(v[8 * hq + 6], v[8 * hq + 7]);
-                                *reinterpret_cast<uint4*>(orow + j0) = w;
+                                uint4 wv;
+                                wv.x = pack_bf16(v[8 * hq + 0], v[8 * hq + 1]);
+                                wv.y = pack_bf16(v[8 * hq + 2], v[8 * hq + 3]);
+                                wv.z = pack_bf16(v[8 * hq + 4], v[8 * hq + 5]);
+                                wv.w = pack_bf16(v[8 * hq + 6], v[8 * hq + 7]);
+                                *reinterpret_cast<uint4*>(orow + j0) = wv;
                             }
                         }
                     }
                 }
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar_sync(1, 128);
-            tc_fence_after();
+            smem_to_tc();
+            // stage s is free again (every read of it, and the last MMA, are done)
+            if (k + kStages < p.nchunks) {
+                if (r < kC) {
+                    S.g[s][r] = g_next;
+                    if (DELTA) S.beta[s][r] = beta_next;
+                }
+                if (r == 0) issue_load(k + kStages), issued = k + kStages + 1;
+            }
         }
-        if (r < 64 && p.hT && r < dk) {
-            float* hrow = p.hT + ((size_t)u * dk + r) * dv;
+        if (state_row && p.hT && trow < dk) {
+            float* hrow = p.hT + ((size_t)u * dk + trow) * dv;
 #pragma unroll
-            for (int j = 0; j < 64; j++)
-                if (j < dv) hrow[j] = Sreg[j];
+            for (int j = 0; j < 32; j++)
+                if (32 * wh + j < dv) hrow[32 * wh + j] = Sreg[j];
         }
+        // after an abort, let the copies already issued land before exiting
+        if (tid == 0 && *(volatile uint32_t*)&S.abort)
+            for (int k = issued > kStages ? issued - kStages : 0; k < issued; k++)
+                mbar_wait(&S.full[k % kStages], (k / kStages) & 1, nullptr, 1u << 20);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tbase, TM_COLS);
+}
+
+template <bool DELTA>
+cudaError_t launch_t(const TcParams& p, int grid, cudaStream_t st)
+{
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<DELTA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    fwd_tc_kernel<DELTA><<<grid, kThreads, SMEM_BYTES, st>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -428,16 +838,13 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
 {
     *handled = false;
     if (a.io != GDN_BF16 || a.T <= 0) return cudaSuccess;
-    if (a.mode == GDN_DELTA) {
-        *handled = true;
-        return launch_fwd_tc_delta(a, st);
-    }
     TcParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map(&p.tm_v, a.v, a.B, a.T, a.H, a.dv) || !make_map(&p.tm_b, a.b, a.B, a.T, a.H, a.dk) ||
         !make_map(&p.tm_c, a.c, a.B, a.T, a.H, a.dk))
         return cudaErrorInvalidValue;
     p.g = (const __nv_bfloat16*)a.g;
+    p.beta = (const __nv_bfloat16*)a.beta;
     p.A_log = a.A_log;
     p.h0 = a.h0;
     p.o = (__nv_bfloat16*)a.o;
@@ -445,16 +852,8 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     p.status = (uint32_t*)a.ws;
     p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv = a.dv;
     p.nchunks = (a.T + kC - 1) / kC;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_tc_gated_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    fwd_tc_gated_kernel<<<a.B * a.H, kThreads, SMEM_BYTES, st>>>(p);
     *handled = true;
-    return cudaGetLastError();
+    return a.mode == GDN_DELTA ? launch_t<true>(p, a.B * a.H, st) : launch_t<false>(p, a.B * a.H, st);
 }
 
 }  // namespace gdn

@@ -46,7 +46,6 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward);
 cudaError_t launch_serial_fwd(const Args& a, cudaStream_t st);
 cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled);
-cudaError_t launch_fwd_tc_delta(const Args& a, cudaStream_t st);
 
 // Device status word helpers.
 enum : uint32_t { kDevOk = 0, kDevTimeout = 1 };

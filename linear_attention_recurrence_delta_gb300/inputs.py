@@ -116,6 +116,7 @@ class Workload:
     c_dist: str = "normal"     # "normal" | "l2norm"
     g_mu: float = 0.0          # g = sigmoid(N(g_mu, 1))
     h0_std: float = 0.0        # h0 = h0_std * N(0, 1) (0 => no h0)
+    alog_max: float = math.log(16.0)   # A_log ~ U(0, alog_max)
     notes: str = ""
 
     @property
@@ -183,7 +184,7 @@ def make_inputs(w: Workload) -> dict:
         out["beta"] = round_to(_sigmoid(normal(s, STREAMS["beta"], B * T * H)).reshape(B, T, H), w.dtype)
     else:
         out["beta"] = None
-    out["A_log"] = round_to(uniform(s, STREAMS["A_log"], H * dk).reshape(H, dk) * math.log(16.0), "f32")
+    out["A_log"] = round_to(uniform(s, STREAMS["A_log"], H * dk).reshape(H, dk) * w.alog_max, "f32")
     if w.h0_std > 0:
         out["h0"] = round_to(w.h0_std * normal(s, STREAMS["h0"], B * H * dk * dv).reshape(B, H, dk, dv), "f32")
     else:

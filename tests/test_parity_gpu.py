@@ -6,6 +6,7 @@ accumulation.  The oracle runs on the same seeded inputs, rounded to the I/O
 dtype, upcast exactly to fp64.
 """
 import functools
+import math
 
 import numpy as np
 import pytest
@@ -91,6 +92,16 @@ def test_fwd_no_h0_no_hT_single_unit(mode):
 def test_fwd_slow_decay(mode):
     """g ~ sigmoid(N(-4,1)): mean log-decay ~ -0.15/token, long memory."""
     w = I.custom(name=f"slow_{mode}", mode=mode, dtype="bf16", B=2, H=2, T=700, dk=64, dv=64, seed=3, g_mu=-4.0)
+    check_fwd(w)
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+@pytest.mark.parametrize("g_mu", [0.0, 3.0])
+def test_fwd_steep_decay(mode, g_mu):
+    """|A| up to 64 and g near 1: the 8-token decay factors would overflow, so
+    the kernels take their exact elementwise evaluation for those chunks."""
+    w = I.custom(name=f"steep_{mode}_{g_mu}", mode=mode, dtype="bf16", B=1, H=4, T=192, dk=64, dv=64, seed=8,
+                 g_mu=g_mu, alog_max=math.log(64.0), h0_std=0.2)
     check_fwd(w)
 
 
