@@ -73,14 +73,31 @@ __device__ __forceinline__ void st_row8_f16(unsigned char* tile, int row, int q,
 __device__ __forceinline__ void st_row8_split(unsigned char* thi, unsigned char* tlo, int row, int q,
                                               const float (&v)[8])
 {
-    float hi[8], lo[8];
+    uint32_t hp[4], lp[4];
 #pragma unroll
-    for (int k = 0; k < 8; k++) {
-        hi[k] = __bfloat162float(__float2bfloat16_rn(v[k]));
-        lo[k] = v[k] - hi[k];
+    for (int k = 0; k < 4; k++) {
+        hp[k] = pack_bf16(v[2 * k], v[2 * k + 1]);
+        const float h0 = __uint_as_float(hp[k] << 16), h1 = __uint_as_float(hp[k] & 0xFFFF0000u);
+        lp[k] = pack_bf16(v[2 * k] - h0, v[2 * k + 1] - h1);
     }
-    st_row8(thi, row, q, hi);
-    st_row8(tlo, row, q, lo);
+    const uint32_t off = sw128(row, 8 * q);
+    *reinterpret_cast<uint4*>(thi + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+    *reinterpret_cast<uint4*>(tlo + off) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
+}
+
+// 8 consecutive floats from shared memory (16-byte aligned)
+__device__ __forceinline__ void ld_f8(const float* p, float (&v)[8])
+{
+    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// 2^x on the SFU (ex2.approx, flush-to-zero; relative error ~2^-22)
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // x[k] * exp2(A2[8q+k] * dG) for the 8 channels of chunk q

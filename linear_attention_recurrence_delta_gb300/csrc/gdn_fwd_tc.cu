@@ -74,7 +74,9 @@ constexpr uint32_t X_A2 = 28672, X_B2 = 45056, X_A3 = 53248, X_A3L = 69632, X_B3
 //   gated, after the levels: [0 ; Ctil]
 constexpr uint32_t X_CH1 = 0;
 //   delta phase 2: [N | X0] = Dinv [L | R]
-constexpr uint32_t X_DINV = 0, X_LRH = 16384, X_LRL = 40960, X_M32 = 57344, X_DI32 = 61440;
+constexpr uint32_t X_DINV = 0, X_LRH = 16384, X_LRL = 40960, X_M32 = 57344, X_DI32 = 62464;
+// fp32 16x16 blocks with a padded row stride (conflict-free float4 rows)
+constexpr int kBS = 20;
 //   delta phase 3: [N^2 | N X0] = N [N | X0]
 constexpr uint32_t X_NA = 0, X_NXH = 16384, X_NXL = 40960;
 //   delta phase 4: [Util | W] = Z + N^2 Z
@@ -234,11 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         fence_proxy_async_smem();
         named_bar_sync(1, kMath);
         uint32_t mma_phase = 0;
+        // one warp polls the mbarrier; the others sleep in the named barrier
         auto mma_wait_all = [&]() -> bool {
-            if (!wait_or_abort(&S.mma, mma_phase, &S.abort, p.status)) return false;
+            if (warp == 0) wait_or_abort(&S.mma, mma_phase, &S.abort, p.status);
+            named_bar_sync(1, kMath);
             mma_phase ^= 1;
             tc_fence_after();
-            return true;
+            return *(volatile uint32_t*)&S.abort == 0;
         };
         auto smem_to_tc = [&]() {   // generic-proxy smem writes -> visible to the tensor cores
             fence_proxy_async_smem();
@@ -249,7 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
         for (int k = 0; k < p.nchunks; k++) {
             const int s = k % kStages;
-            if (!wait_or_abort(&S.full[s], (k / kStages) & 1, &S.abort, p.status)) break;
+            if (warp == 0) wait_or_abort(&S.full[s], (k / kStages) & 1, &S.abort, p.status);
+            named_bar_sync(1, kMath);
+            if (*(volatile uint32_t*)&S.abort) break;
             unsigned char* sV = sm + OFF_RING + s * STAGE_BYTES;
             unsigned char* sB = sV + 8192;
             unsigned char* sCt = sV + 16384;
@@ -293,14 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     const int pr = r + rep * kMath;
                     const int k8 = pr >> 6, i = pr & 63, J = k8 >> 1;
                     const float a2 = S.A2[i], Gref = S.G[8 * k8 + 3];
-                    K[(K_A1 * 8 + k8) * 64 + i] = J >= 1 ? exp2f(a2 * (Gref - S.G[16 * J - 1])) : 0.f;
-                    K[(K_A2 * 8 + k8) * 64 + i] = (k8 & 1) ? exp2f(a2 * (Gref - S.G[16 * J + 7])) : 0.f;
-                    K[(K_0 * 8 + k8) * 64 + i] = exp2f(a2 * Gref);
-                    K[(K_B1_1 * 8 + k8) * 64 + i] = J < 1 ? exp2f(a2 * (S.G[15] - Gref)) : 0.f;
-                    K[(K_B1_2 * 8 + k8) * 64 + i] = J < 2 ? exp2f(a2 * (S.G[31] - Gref)) : 0.f;
-                    K[(K_B1_3 * 8 + k8) * 64 + i] = J < 3 ? exp2f(a2 * (S.G[47] - Gref)) : 0.f;
-                    K[(K_B2 * 8 + k8) * 64 + i] = (k8 & 1) ? 0.f : exp2f(a2 * (S.G[16 * J + 7] - Gref));
-                    K[(K_BH * 8 + k8) * 64 + i] = exp2f(a2 * (S.G[63] - Gref));
+                    K[(K_A1 * 8 + k8) * 64 + i] = J >= 1 ? fast_exp2(a2 * (Gref - S.G[16 * J - 1])) : 0.f;
+                    K[(K_A2 * 8 + k8) * 64 + i] = (k8 & 1) ? fast_exp2(a2 * (Gref - S.G[16 * J + 7])) : 0.f;
+                    K[(K_0 * 8 + k8) * 64 + i] = fast_exp2(a2 * Gref);
+                    K[(K_B1_1 * 8 + k8) * 64 + i] = J < 1 ? fast_exp2(a2 * (S.G[15] - Gref)) : 0.f;
+                    K[(K_B1_2 * 8 + k8) * 64 + i] = J < 2 ? fast_exp2(a2 * (S.G[31] - Gref)) : 0.f;
+                    K[(K_B1_3 * 8 + k8) * 64 + i] = J < 3 ? fast_exp2(a2 * (S.G[47] - Gref)) : 0.f;
+                    K[(K_B2 * 8 + k8) * 64 + i] = (k8 & 1) ? 0.f : fast_exp2(a2 * (S.G[16 * J + 7] - Gref));
+                    K[(K_BH * 8 + k8) * 64 + i] = fast_exp2(a2 * (S.G[63] - Gref));
                 }
             }
             named_bar_sync(1, kMath);
@@ -314,83 +320,95 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const float Gt = S.G[t], Gr = S.G[8 * k8 + 3];
                 const float dG = Gt - Gr;
                 const float bet = DELTA ? S.beta[s][t] : 0.f;
-                const float* KA1 = ktab(sm, K_A1, k8);
-                const float* KA2 = ktab(sm, K_A2, k8);
-                const float* K0 = ktab(sm, K_0, k8);
-                const float* KB11 = ktab(sm, K_B1_1, k8);
-                const float* KB12 = ktab(sm, K_B1_2, k8);
-                const float* KB13 = ktab(sm, K_B1_3, k8);
-                const float* KB2 = ktab(sm, K_B2, k8);
-                // direct reference values for the overflow fallback
-                const float GI = I > 0 ? S.G[16 * I - 1] : 0.f, GJ7 = S.G[16 * I + 7];
+                if (!unsafe) {
+                    // fast path: anchor exp(A (G_t - G_r8)) times per-block constants
 #pragma unroll
-                for (int qq = 0; qq < 2; qq++) {
-                    const int q = 2 * cq + qq;
-                    float cv[8], bv[8], a2[8], ax[8], bxp[8], bbx[8], y[8], z[8];
-                    ld_row8(sCt, t, q, cv);
-                    ld_row8(sB, t, q, bv);
-#pragma unroll
-                    for (int e = 0; e < 8; e++) {
-                        a2[e] = S.A2[8 * q + e];
-                        const float an = exp2f(a2[e] * dG), ai = exp2f(-a2[e] * dG);
-                        ax[e] = cv[e] * an;
-                        bxp[e] = bv[e] * ai;
-                        bbx[e] = bet * bv[e] * an;
-                    }
-                    if (I > 0) {
+                    for (int qq = 0; qq < 2; qq++) {
+                        const int q = 2 * cq + qq;
+                        float cv[8], bv[8], a2[8], ax[8], bxp[8], bbx[8], y[8], z[8];
+                        ld_row8(sCt, t, q, cv);
+                        ld_row8(sB, t, q, bv);
+                        ld_f8(S.A2 + 8 * q, a2);
 #pragma unroll
                         for (int e = 0; e < 8; e++) {
-                            const float f = unsafe ? exp2f(a2[e] * (Gt - GI)) : KA1[8 * q + e];
-                            y[e] = unsafe ? cv[e] * f : ax[e] * f;
-                            z[e] = unsafe ? bet * bv[e] * f : bbx[e] * f;
+                            const float an = fast_exp2(a2[e] * dG), ai = fast_exp2(-a2[e] * dG);
+                            ax[e] = cv[e] * an;
+                            bxp[e] = bv[e] * ai;
+                            bbx[e] = bet * bv[e] * an;
                         }
-                        st_row8_f16(X + X_A1, t, q, y);
-                        if (DELTA) st_row8_f16(X + X_A1, 64 + t, q, z);
-                    }
-                    if (upper) {
+                        float kk[8];
+                        if (I > 0) {
+                            ld_f8(ktab(sm, K_A1, k8) + 8 * q, kk);
 #pragma unroll
-                        for (int e = 0; e < 8; e++) {
-                            const float f = unsafe ? exp2f(a2[e] * (Gt - GJ7)) : KA2[8 * q + e];
-                            y[e] = unsafe ? cv[e] * f : ax[e] * f;
-                            z[e] = unsafe ? bet * bv[e] * f : bbx[e] * f;
+                            for (int e = 0; e < 8; e++) { y[e] = ax[e] * kk[e]; z[e] = bbx[e] * kk[e]; }
+                            st_row8_f16(X + X_A1, t, q, y);
+                            if (DELTA) st_row8_f16(X + X_A1, 64 + t, q, z);
                         }
-                        st_row8_f16(X + X_A2, t, q, y);
-                        if (DELTA) st_row8_f16(X + X_A2, 64 + t, q, z);
-                    }
-                    st_row8_split(X + X_A3, X + X_A3L, t, q, ax);
-                    if (DELTA) st_row8_split(X + X_A3, X + X_A3L, 64 + t, q, bbx);
-                    // column side (row s = t of the B operands)
-                    if (I < 1) {
+                        if (upper) {
+                            ld_f8(ktab(sm, K_A2, k8) + 8 * q, kk);
 #pragma unroll
-                        for (int e = 0; e < 8; e++)
-                            y[e] = unsafe ? bv[e] * exp2f(a2[e] * (S.G[15] - Gt)) : bxp[e] * KB11[8 * q + e];
-                        st_row8_f16(X + X_B1a, t, q, y);
-                    }
-                    if (I < 2) {
+                            for (int e = 0; e < 8; e++) { y[e] = ax[e] * kk[e]; z[e] = bbx[e] * kk[e]; }
+                            st_row8_f16(X + X_A2, t, q, y);
+                            if (DELTA) st_row8_f16(X + X_A2, 64 + t, q, z);
+                        }
+                        st_row8_split(X + X_A3, X + X_A3L, t, q, ax);
+                        if (DELTA) st_row8_split(X + X_A3, X + X_A3L, 64 + t, q, bbx);
+                        if (I < 1) {
+                            ld_f8(ktab(sm, K_B1_1, k8) + 8 * q, kk);
 #pragma unroll
-                        for (int e = 0; e < 8; e++)
-                            y[e] = unsafe ? bv[e] * exp2f(a2[e] * (S.G[31] - Gt)) : bxp[e] * KB12[8 * q + e];
-                        st_row8_f16(X + X_B1b, t, q, y);
-                    }
-                    if (I < 3) {
+                            for (int e = 0; e < 8; e++) y[e] = bxp[e] * kk[e];
+                            st_row8_f16(X + X_B1a, t, q, y);
+                        }
+                        if (I < 2) {
+                            ld_f8(ktab(sm, K_B1_2, k8) + 8 * q, kk);
 #pragma unroll
-                        for (int e = 0; e < 8; e++)
-                            y[e] = unsafe ? bv[e] * exp2f(a2[e] * (S.G[47] - Gt)) : bxp[e] * KB13[8 * q + e];
-                        st_row8_f16(X + X_B1c, t, q, y);
-                    }
-                    if (!upper) {
+                            for (int e = 0; e < 8; e++) y[e] = bxp[e] * kk[e];
+                            st_row8_f16(X + X_B1b, t, q, y);
+                        }
+                        if (I < 3) {
+                            ld_f8(ktab(sm, K_B1_3, k8) + 8 * q, kk);
 #pragma unroll
-                        for (int e = 0; e < 8; e++)
-                            y[e] = unsafe ? bv[e] * exp2f(a2[e] * (GJ7 - Gt)) : bxp[e] * KB2[8 * q + e];
-                        st_row8_f16(X + X_B2, t, q, y);
-                    }
-                    st_row8_split(X + X_B3, X + X_B3L, t, q, bxp);
-                    // chunk-start factor exp(A G_t): Ctil (gated) or beta Btil (delta)
+                            for (int e = 0; e < 8; e++) y[e] = bxp[e] * kk[e];
+                            st_row8_f16(X + X_B1c, t, q, y);
+                        }
+                        if (!upper) {
+                            ld_f8(ktab(sm, K_B2, k8) + 8 * q, kk);
 #pragma unroll
-                    for (int e = 0; e < 8; e++) {
-                        const float f0 = unsafe ? exp2f(a2[e] * Gt) : K0[8 * q + e];
-                        keep[8 * qq + e] = DELTA ? (unsafe ? bet * bv[e] * f0 : bbx[e] * f0)
-                                                 : (unsafe ? cv[e] * f0 : ax[e] * f0);
+                            for (int e = 0; e < 8; e++) y[e] = bxp[e] * kk[e];
+                            st_row8_f16(X + X_B2, t, q, y);
+                        }
+                        st_row8_split(X + X_B3, X + X_B3L, t, q, bxp);
+                        ld_f8(ktab(sm, K_0, k8) + 8 * q, kk);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) keep[8 * qq + e] = (DELTA ? bbx[e] : ax[e]) * kk[e];
+                    }
+                } else {
+                    // fallback: every factor evaluated directly (all exponents <= 0 except L3's,
+                    // whose entries the assembly step replaces by exact sums)
+                    const float GI = I > 0 ? S.G[16 * I - 1] : 0.f, GJ7 = S.G[16 * I + 7];
+#pragma unroll
+                    for (int qq = 0; qq < 2; qq++) {
+                        const int q = 2 * cq + qq;
+                        float cv[8], bv[8], bbv[8], y[8], z[8];
+                        ld_row8(sCt, t, q, cv);
+                        ld_row8(sB, t, q, bv);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) bbv[e] = bet * bv[e];
+                        if (I > 0) {
+                            scale8(cv, S.A2, q, Gt - GI, y); st_row8_f16(X + X_A1, t, q, y);
+                            if (DELTA) { scale8(bbv, S.A2, q, Gt - GI, z); st_row8_f16(X + X_A1, 64 + t, q, z); }
+                        }
+                        if (upper) {
+                            scale8(cv, S.A2, q, Gt - GJ7, y); st_row8_f16(X + X_A2, t, q, y);
+                            if (DELTA) { scale8(bbv, S.A2, q, Gt - GJ7, z); st_row8_f16(X + X_A2, 64 + t, q, z); }
+                        }
+                        if (I < 1) { scale8(bv, S.A2, q, S.G[15] - Gt, y); st_row8_f16(X + X_B1a, t, q, y); }
+                        if (I < 2) { scale8(bv, S.A2, q, S.G[31] - Gt, y); st_row8_f16(X + X_B1b, t, q, y); }
+                        if (I < 3) { scale8(bv, S.A2, q, S.G[47] - Gt, y); st_row8_f16(X + X_B1c, t, q, y); }
+                        if (!upper) { scale8(bv, S.A2, q, GJ7 - Gt, y); st_row8_f16(X + X_B2, t, q, y); }
+                        scale8(DELTA ? bbv : cv, S.A2, q, Gt, y);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) keep[8 * qq + e] = y[e];
                     }
                 }
             }
@@ -399,24 +417,33 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             {
                 const int i = r & 63, sq = r >> 6;
                 const float a2 = S.A2[i], G63 = S.G[63];
+                if (!unsafe) {
 #pragma unroll
-                for (int h2 = 0; h2 < 2; h2++) {
-                    float y8[8];
+                    for (int h2 = 0; h2 < 2; h2++) {
+                        float y8[8];
 #pragma unroll
-                    for (int e = 0; e < 8; e++) {
-                        const int sc = 16 * sq + 8 * h2 + e;
-                        if (unsafe) {
-                            const float bval = bf2f(*reinterpret_cast<const uint16_t*>(sB + sw128(sc, i)));
-                            y8[e] = bval * exp2f(a2 * (G63 - S.G[sc]));
-                        } else {
+                        for (int e = 0; e < 8; e++) {
+                            const int sc = 16 * sq + 8 * h2 + e;
                             const float b3 = bf2f(*reinterpret_cast<const uint16_t*>(X + X_B3 + sw128(sc, i))) +
                                              bf2f(*reinterpret_cast<const uint16_t*>(X + X_B3L + sw128(sc, i)));
                             y8[e] = b3 * ktab(sm, K_BH, sc >> 3)[i];
                         }
+                        st_row8_split(sm + OFF_CH0, sm + OFF_CH0L, i, 2 * sq + h2, y8);
                     }
-                    st_row8_split(sm + OFF_CH0, sm + OFF_CH0L, i, 2 * sq + h2, y8);
+                } else {
+#pragma unroll 1
+                    for (int h2 = 0; h2 < 2; h2++) {
+                        float y8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++) {
+                            const int sc = 16 * sq + 8 * h2 + e;
+                            const float bval = bf2f(*reinterpret_cast<const uint16_t*>(sB + sw128(sc, i)));
+                            y8[e] = bval * exp2f(a2 * (G63 - S.G[sc]));
+                        }
+                        st_row8_split(sm + OFF_CH0, sm + OFF_CH0L, i, 2 * sq + h2, y8);
+                    }
                 }
-                if (r < 64) S.decay[r] = exp2f(S.A2[r] * S.G[63]);
+                if (r < 64) S.decay[r] = fast_exp2(S.A2[r] * S.G[63]);
             }
             smem_to_tc();
 
@@ -500,7 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             st_plain16(X + X_LRH, t, cg, lpart);
                             if (cg == tb) {
 #pragma unroll
-                                for (int c = 0; c < 16; c++) M32[(tb * 16 + (t & 15)) * 16 + c] = out[c];
+                                for (int c = 0; c < 16; c += 4)
+                                    *reinterpret_cast<float4*>(M32 + (tb * 16 + (t & 15)) * kBS + c) =
+                                        make_float4(out[c], out[c + 1], out[c + 2], out[c + 3]);
                             }
                         }
                     }
@@ -556,25 +585,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // (5) exact inverse of the diagonal 16-blocks of I + M
                 if (r < 64) {
                     const int J = r >> 4, c = r & 15;
-                    const float* M32 = reinterpret_cast<const float*>(X + X_M32) + J * 256;
+                    const float* M32 = reinterpret_cast<const float*>(X + X_M32) + J * 16 * kBS;
+                    // column c of (I + M_JJ)^{-1}, right-looking: once x_p is final,
+                    // subtract M[q][p] x_p from every later row q (independent FMAs)
                     float xs[16];
 #pragma unroll
-                    for (int q = 0; q < 16; q++) {
-                        float acc = 0.f;
+                    for (int q = 0; q < 16; q++) xs[q] = (q == c) ? 1.f : 0.f;
 #pragma unroll
-                        for (int pp = 0; pp < q; pp++)
-                            if (pp >= c) acc = fmaf(M32[q * 16 + pp], xs[pp], acc);
-                        xs[q] = (q < c) ? 0.f : (q == c ? 1.f : -acc);
+                    for (int pp = 0; pp < 15; pp++) {
+                        if (pp >= c) {
+                            const float xp = xs[pp];
+#pragma unroll
+                            for (int q = pp + 1; q < 16; q++) xs[q] = fmaf(-M32[q * kBS + pp], xp, xs[q]);
+                        }
                     }
-                    float* DI32 = reinterpret_cast<float*>(X + X_DI32) + J * 256;
+                    float* DI32 = reinterpret_cast<float*>(X + X_DI32) + J * 16 * kBS;
 #pragma unroll
-                    for (int q = 0; q < 16; q++) DI32[q * 16 + c] = xs[q];
+                    for (int q = 0; q < 16; q++) DI32[q * kBS + c] = xs[q];
                 }
                 named_bar_sync(1, kMath);
                 {
                     // [Dinv ; 0]: row trow, 32 columns of half wh
                     const int J = (trow & 63) >> 4;
-                    const float* DI32 = reinterpret_cast<const float*>(X + X_DI32) + J * 256 + (trow & 15) * 16;
+                    const float* DI32 = reinterpret_cast<const float*>(X + X_DI32) + (J * 16 + (trow & 15)) * kBS;
 #pragma unroll
                     for (int cc = 0; cc < 2; cc++) {
                         const int cg = 2 * wh + cc;
