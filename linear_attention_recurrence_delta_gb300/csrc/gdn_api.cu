@@ -28,11 +28,9 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward)
     size_t off = 256;  // status word
     if (backward) {
         const size_t units = (size_t)s.B * s.H;
-        const size_t nseg = (size_t)((s.T + kSerialSeg - 1) / kSerialSeg);
+        const size_t nblk = (size_t)((s.T + kSerialBlock - 1) / kSerialBlock);
         L.ck_off = off;
-        off = round_up(off + units * nseg * kStateSlot, 256);
-        L.scratch_off = off;
-        off = round_up(off + units * kSerialSeg * kStateSlot, 256);
+        off = round_up(off + units * nblk * kStateSlot, 256);
         L.dalog_off = off;
         off = round_up(off + units * (size_t)s.dk * 4, 256);
     }

@@ -31,13 +31,12 @@ struct Args {
 // Workspace carve-up.  The first 256 bytes always hold the device status word.
 struct WsLayout {
     size_t status_off = 0;        // uint32 status code, uint32 detail
-    size_t ck_off = 0;            // serial backward: state checkpoints
-    size_t scratch_off = 0;       // serial backward: per-token states of one segment
+    size_t ck_off = 0;            // serial backward: state entering every block of kSerialBlock tokens
     size_t dalog_off = 0;         // per-(b,h) dA_log partials, float [B*H, d_k]
     size_t total = 0;
 };
 
-constexpr int kSerialSeg = 16;                 // tokens per recompute segment
+constexpr int kSerialBlock = 32;               // tokens between backward checkpoints
 constexpr size_t kStateSlot = 16 * 256 * 4;    // one state snapshot (256 threads x 16 floats)
 
 WsLayout ws_layout(const gdn_shape_t& s, int backward);

@@ -1,0 +1,534 @@
+// gdn_serial_bwd.cu -- token-serial backward of the gated delta rule on the
+// CUDA cores (fp32 state and adjoint, packed fp32x2 arithmetic).
+//
+// The forward per token (gated: "GDN & MLA Mechanism Deep-Dive", Step 4;
+// delta: the delta-rule card of "HyMo-434M -- documentation portal"):
+//   h' = alpha_t (.) h_{t-1},  alpha_t = exp(g_t A),  A = -exp(A_log)
+//   x  = v_t                        (gated)
+//   x  = beta_t (v_t - h'^T b_t)    (delta)
+//   h_t = h' + b_t x^T,   o_t = h_t^T c_t.
+// Its adjoint, walked from the last token back with dH = dL/dh_t:
+//   dH  += c_t do_t^T;         dc_t = h_t do_t
+//   du   = dH^T b_t;           dv_t = beta du (delta) | du (gated)
+//   dr   = -beta du;           dbeta_t = du . (v_t - h'^T b_t)
+//   db_t = dH x + h' dr;       dH += b_t dr^T   (now dH = dL/dh')
+//   q = dH (.) h';  dg_t = sum_ij A_i q_ij;  dA_log_i += A_i g_t sum_j q_ij
+//   dH <- alpha_t (.) dH.
+//
+// One CTA per (batch, head) unit, 256 threads.  Warp w owns state columns
+// 8w..8w+7; lane = 8 jl + ig holds columns j0 = 8w + 2 jl and j0 + 1 and the
+// eight rows 8 ig .. 8 ig + 7, stored as four packed row pairs in an order
+// permuted by jl so that the sums over columns (dc, db) need no selects.
+// Recompute: the forward sweep keeps the state every 32 tokens in the
+// workspace; a 32-token block is recomputed into shared-memory snapshots every
+// 8 tokens, and each 4-token window is recomputed into registers and walked
+// backwards.  Per-warp row partials are summed across warps once per window.
+#include "gdn_internal.h"
+#include "serial_common.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace rec;
+
+constexpr int kBT = kSerialBlock;  // tokens per staged block = checkpoint interval
+constexpr int kSub = 8;            // tokens per shared-memory snapshot
+constexpr int kWin = 4;            // tokens per register window
+constexpr int kNQ = 2;             // row quantities summed over columns: dc, db
+
+template <typename IO>
+struct BwdSmem {
+    float A[kBT][64], Bv[kBT][64], Cv[kBT][64];                 // alpha_t, b_t, c_t
+    float V[kBT][64], DO[kBT][64], X[kBT][64], VR[kBT][64];     // v_t, do_t, x, v_t - h'^T b_t
+    float beta[kBT], g[kBT];
+    float Arow[64];
+    float2 snap[kBT / kSub][8][256];                             // per-thread state snapshots
+    float part[2][8][kWin][kNQ][64];                             // per-warp row partials
+    float dvb[2][kWin][64];
+    float bpart[2][8][kWin], gpart[2][8][kWin];
+    float red[8][64];
+    float rg[kBT], rbeta[kBT];
+    IO rb[kBT][64], rc[kBT][64], rv[kBT][64], rdo[kBT][64];     // raw bytes of the next block
+};
+
+struct Ctx {
+    int tid, lane, w, ig, jl, j0, m2, u, bb, h;
+    int roff[4];  // float offset of register pair p inside a 64-row vector
+};
+
+__device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+
+template <typename IO, bool DELTA>
+__device__ __forceinline__ void issue_block(const Args& a, BwdSmem<IO>& s, const Ctx& C, int t0, bool grad, bool vec,
+                                            float& greg, float& breg)
+{
+    const int tid = C.tid, dk = a.dk, dv = a.dv, T = a.T, H = a.H;
+    const int nt = min(kBT, T - t0);
+    const IO* bk = (const IO*)a.b;
+    const IO* c = (const IO*)a.c;
+    const IO* v = (const IO*)a.v;
+    const IO* dO = (const IO*)a.dO;
+    constexpr int E = 16 / sizeof(IO);
+    if (vec) {
+        const int cb = dk / E, cv = dv / E;
+        const int per = grad ? 2 * (cb + cv) : cb + cv;
+        for (int idx = tid; idx < nt * per; idx += 256) {
+            const int tt = idx / per;
+            int r = idx - tt * per;
+            const size_t row = ((size_t)C.bb * T + t0 + tt) * H + C.h;
+            if (r < cb) { cp_async16(&s.rb[tt][r * E], bk + row * dk + r * E); continue; }
+            r -= cb;
+            if (r < cv) { cp_async16(&s.rv[tt][r * E], v + row * dv + r * E); continue; }
+            r -= cv;
+            if (r < cb) { cp_async16(&s.rc[tt][r * E], c + row * dk + r * E); continue; }
+            r -= cb;
+            cp_async16(&s.rdo[tt][r * E], dO + row * dv + r * E);
+        }
+        cp_async_commit();
+    } else {
+        for (int idx = tid; idx < nt * 64; idx += 256) {
+            const int tt = idx >> 6, i = idx & 63;
+            const size_t row = ((size_t)C.bb * T + t0 + tt) * H + C.h;
+            if (i < dk) {
+                s.rb[tt][i] = bk[row * dk + i];
+                if (grad) s.rc[tt][i] = c[row * dk + i];
+            }
+            if (i < dv) {
+                s.rv[tt][i] = v[row * dv + i];
+                if (grad) s.rdo[tt][i] = dO[row * dv + i];
+            }
+        }
+    }
+    if (tid < nt) greg = to_f(((const IO*)a.g)[((size_t)C.bb * T + t0 + tid) * H + C.h]);
+    if (DELTA && tid >= 32 && tid - 32 < nt)
+        breg = to_f(((const IO*)a.beta)[((size_t)C.bb * T + t0 + tid - 32) * H + C.h]);
+}
+
+// Make the block issued last the current one.  Tokens past T become identity
+// steps (alpha = 1, every other input 0), so a block is always 32 tokens.
+template <typename IO, bool DELTA>
+__device__ __forceinline__ void finish_block(const Args& a, BwdSmem<IO>& s, const Ctx& C, int t0, bool grad,
+                                             float greg, float breg)
+{
+    const int tid = C.tid, dk = a.dk, dv = a.dv;
+    const int nt = min(kBT, a.T - t0);
+    if (tid < 32) s.rg[tid] = greg;
+    else if (tid < 64) s.rbeta[tid - 32] = breg;
+    cp_async_wait_all();
+    __syncthreads();
+    for (int idx = tid; idx < kBT * 64; idx += 256) {
+        const int tt = idx >> 6, i = idx & 63;
+        const bool ok = tt < nt;
+        s.A[tt][i] = ok ? expf(s.rg[tt] * s.Arow[i]) : 1.f;
+        s.Bv[tt][i] = ok && i < dk ? to_f(s.rb[tt][i]) : 0.f;
+        s.Cv[tt][i] = grad && ok && i < dk ? to_f(s.rc[tt][i]) : 0.f;
+        s.V[tt][i] = ok && i < dv ? to_f(s.rv[tt][i]) : 0.f;
+        s.DO[tt][i] = grad && ok && i < dv ? to_f(s.rdo[tt][i]) : 0.f;
+    }
+    if (tid < kBT) {
+        const bool ok = tid < nt;
+        s.g[tid] = ok ? s.rg[tid] : 0.f;
+        s.beta[tid] = DELTA && ok ? s.rbeta[tid] : 0.f;
+    }
+    __syncthreads();
+}
+
+// one forward step with the row reduction h'^T b (delta); optionally caches
+// x and v - h'^T b for the window recompute and the adjoint
+template <bool DELTA, bool CACHE>
+__device__ __forceinline__ void fwd_full(float2 (&S)[2][4], const float* A, const float* Bv, const float* V, float be,
+                                         float* X, float* VR, const Ctx& C)
+{
+    float2 a2[4], b2[4];
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        a2[p] = ld2(A + C.roff[p]);
+        b2[p] = ld2(Bv + C.roff[p]);
+    }
+    const float2 v2 = ld2(V + C.j0);
+    float2 hp[2][4];
+#pragma unroll
+    for (int c = 0; c < 2; c++)
+#pragma unroll
+        for (int p = 0; p < 4; p++) hp[c][p] = mul2(S[c][p], a2[p]);
+    float x0, x1;
+    if (DELTA) {
+        float2 r0 = mul2(hp[0][0], b2[0]), r1 = mul2(hp[1][0], b2[0]);
+#pragma unroll
+        for (int p = 1; p < 4; p++) {
+            r0 = fma2(hp[0][p], b2[p], r0);
+            r1 = fma2(hp[1][p], b2[p], r1);
+        }
+        float q0 = r0.x + r0.y, q1 = r1.x + r1.y;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            q0 += __shfl_xor_sync(kFull, q0, o);
+            q1 += __shfl_xor_sync(kFull, q1, o);
+        }
+        const float vr0 = v2.x - q0, vr1 = v2.y - q1;
+        x0 = be * vr0;
+        x1 = be * vr1;
+        if (CACHE && C.ig == 0) {
+            *reinterpret_cast<float2*>(X + C.j0) = f2(x0, x1);
+            *reinterpret_cast<float2*>(VR + C.j0) = f2(vr0, vr1);
+        }
+    } else {
+        x0 = v2.x;
+        x1 = v2.y;
+    }
+    const float2 xx0 = f2(x0, x0), xx1 = f2(x1, x1);
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        S[0][p] = fma2(b2[p], xx0, hp[0][p]);
+        S[1][p] = fma2(b2[p], xx1, hp[1][p]);
+    }
+}
+
+// one forward step with x already known (window recompute)
+__device__ __forceinline__ void fwd_cached(const float2 (&Si)[2][4], float2 (&So)[2][4], const float* A,
+                                           const float* Bv, const float* X, const Ctx& C)
+{
+    float2 a2[4], b2[4];
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        a2[p] = ld2(A + C.roff[p]);
+        b2[p] = ld2(Bv + C.roff[p]);
+    }
+    const float2 x2 = ld2(X + C.j0);
+    const float2 xx0 = f2(x2.x, x2.x), xx1 = f2(x2.y, x2.y);
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        So[0][p] = fma2(b2[p], xx0, mul2(Si[0][p], a2[p]));
+        So[1][p] = fma2(b2[p], xx1, mul2(Si[1][p], a2[p]));
+    }
+}
+
+// Sum four packed row pairs over the four column-pair lanes jl of a row
+// group (lanes ig, ig+8, ig+16, ig+24).  Pair p of lane (jl) holds rows
+// 2 (p ^ m2) of the group with m2 = 2 (jl & 1) + (jl >> 1); the result holds
+// rows 2 m2, 2 m2 + 1.
+__device__ __forceinline__ float2 colsum_pairs(const float2 (&x)[4])
+{
+    float2 y0, y1;
+    y0.x = x[0].x + __shfl_xor_sync(kFull, x[2].x, 8);
+    y0.y = x[0].y + __shfl_xor_sync(kFull, x[2].y, 8);
+    y1.x = x[1].x + __shfl_xor_sync(kFull, x[3].x, 8);
+    y1.y = x[1].y + __shfl_xor_sync(kFull, x[3].y, 8);
+    float2 z;
+    z.x = y0.x + __shfl_xor_sync(kFull, y1.x, 16);
+    z.y = y0.y + __shfl_xor_sync(kFull, y1.y, 16);
+    return z;
+}
+
+template <typename IO, bool DELTA>
+__global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, bool vec)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    BwdSmem<IO>& s = *reinterpret_cast<BwdSmem<IO>*>(smem_raw);
+    Ctx C;
+    C.tid = threadIdx.x;
+    C.lane = C.tid & 31;
+    C.w = C.tid >> 5;
+    C.ig = C.lane & 7;
+    C.jl = C.lane >> 3;
+    C.j0 = 8 * C.w + 2 * C.jl;
+    C.m2 = 2 * (C.jl & 1) + (C.jl >> 1);
+#pragma unroll
+    for (int p = 0; p < 4; p++) C.roff[p] = 8 * C.ig + 2 * (p ^ C.m2);
+    C.u = blockIdx.x;
+    C.bb = C.u / a.H;
+    C.h = C.u % a.H;
+    const int tid = C.tid, lane = C.lane, w = C.w;
+    const int dk = a.dk, dv = a.dv, T = a.T, H = a.H;
+    const int nblk = (T + kBT - 1) / kBT;
+    float2* ck = reinterpret_cast<float2*>((unsigned char*)a.ws + L.ck_off) + (size_t)C.u * nblk * 2048;
+    float* dA_part = reinterpret_cast<float*>((unsigned char*)a.ws + L.dalog_off) + (size_t)C.u * dk;
+
+    if (tid < 64) s.Arow[tid] = tid < dk ? -expf(a.A_log[C.h * dk + tid]) : 0.f;
+
+    // load a [B,H,dk,dv] fp32 matrix in this thread's register layout
+    auto load_state = [&](const float* src, float2 (&S)[2][4]) {
+#pragma unroll
+        for (int c = 0; c < 2; c++)
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+                const int i0 = C.roff[p], j = C.j0 + c;
+                float x0 = 0.f, x1 = 0.f;
+                if (src && j < dv) {
+                    if (i0 < dk) x0 = src[((size_t)C.u * dk + i0) * dv + j];
+                    if (i0 + 1 < dk) x1 = src[((size_t)C.u * dk + i0 + 1) * dv + j];
+                }
+                S[c][p] = f2(x0, x1);
+            }
+    };
+
+    float2 S[2][4];
+    load_state(a.h0, S);
+
+    // ---------------- forward sweep: state entering every block ----------------
+    float greg = 0.f, breg = 0.f;
+    __syncthreads();  // Arow
+    issue_block<IO, DELTA>(a, s, C, 0, false, vec, greg, breg);
+    for (int n = 0; n < nblk; n++) {
+#pragma unroll
+        for (int q = 0; q < 8; q++) ck[(size_t)n * 2048 + q * 256 + tid] = S[q >> 2][q & 3];
+        finish_block<IO, DELTA>(a, s, C, n * kBT, false, greg, breg);
+        if (n + 1 < nblk) issue_block<IO, DELTA>(a, s, C, (n + 1) * kBT, false, vec, greg, breg);
+        else issue_block<IO, DELTA>(a, s, C, n * kBT, true, vec, greg, breg);  // first block of the reverse walk
+#pragma unroll 1
+        for (int tt = 0; tt < kBT; tt++)
+            fwd_full<DELTA, false>(S, s.A[tt], s.Bv[tt], s.V[tt], s.beta[tt], nullptr, nullptr, C);
+    }
+
+    // ---------------- adjoint: dH = dh_T ----------------
+    float2 dS[2][4];
+    load_state(a.dhT, dS);
+    float2 Ap[4], dA_acc[4];  // A of this thread's row pairs; sum_t g_t sum_j q over its columns
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        Ap[p] = ld2(&s.Arow[C.roff[p]]);
+        dA_acc[p] = f2(0.f, 0.f);
+    }
+    const int ri = tid >> 2, rk = tid & 3;  // reduction-phase role: row ri, window token rk
+    int wbuf = 0;
+
+    // ---------------- reverse walk over blocks ----------------
+    for (int n = nblk - 1; n >= 0; n--) {
+        const int t0 = n * kBT;
+        float2 Sb[2][4];
+#pragma unroll
+        for (int q = 0; q < 8; q++) Sb[q >> 2][q & 3] = ck[(size_t)n * 2048 + q * 256 + tid];
+        finish_block<IO, DELTA>(a, s, C, t0, true, greg, breg);
+        if (n > 0) issue_block<IO, DELTA>(a, s, C, t0 - kBT, true, vec, greg, breg);
+        // block recompute: snapshots every 8 tokens, x and v - h'^T b cached
+#pragma unroll 1
+        for (int tt = 0; tt < kBT; tt++) {
+            if ((tt & (kSub - 1)) == 0) {
+#pragma unroll
+                for (int q = 0; q < 8; q++) s.snap[tt / kSub][q][tid] = Sb[q >> 2][q & 3];
+            }
+            fwd_full<DELTA, true>(Sb, s.A[tt], s.Bv[tt], s.V[tt], s.beta[tt], s.X[tt], s.VR[tt], C);
+        }
+        __syncwarp();
+        const float* Xsrc = DELTA ? &s.X[0][0] : &s.V[0][0];
+
+#pragma unroll 1
+        for (int wi = kBT / kWin - 1; wi >= 0; wi--) {
+            const int tw = kWin * wi;  // first token of the window inside the block
+            float2 W[kWin + 1][2][4];
+            {
+                const int sb = tw / kSub;
+#pragma unroll
+                for (int q = 0; q < 8; q++) W[0][q >> 2][q & 3] = s.snap[sb][q][tid];
+                if (tw & (kSub - 1)) {
+                    // advance from the snapshot to the window start
+#pragma unroll
+                    for (int k = 0; k < kWin; k++) {
+                        const int tt = sb * kSub + k;
+                        float2 Tm[2][4];
+                        fwd_cached(W[0], Tm, s.A[tt], s.Bv[tt], Xsrc + tt * 64, C);
+#pragma unroll
+                        for (int q = 0; q < 8; q++) W[0][q >> 2][q & 3] = Tm[q >> 2][q & 3];
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kWin; k++) {
+                    const int tt = tw + k;
+                    fwd_cached(W[k], W[k + 1], s.A[tt], s.Bv[tt], Xsrc + tt * 64, C);
+                }
+            }
+#pragma unroll
+            for (int k = kWin - 1; k >= 0; k--) {
+                const int tt = tw + k;
+                float2 a2[4], b2[4], c2[4];
+#pragma unroll
+                for (int p = 0; p < 4; p++) {
+                    a2[p] = ld2(&s.A[tt][C.roff[p]]);
+                    b2[p] = ld2(&s.Bv[tt][C.roff[p]]);
+                    c2[p] = ld2(&s.Cv[tt][C.roff[p]]);
+                }
+                const float2 do2 = ld2(&s.DO[tt][C.j0]);
+                const float2 d0 = f2(do2.x, do2.x), d1 = f2(do2.y, do2.y);
+                float2 pdc[4];
+#pragma unroll
+                for (int p = 0; p < 4; p++) {
+                    dS[0][p] = fma2(c2[p], d0, dS[0][p]);
+                    dS[1][p] = fma2(c2[p], d1, dS[1][p]);
+                    pdc[p] = fma2(W[k + 1][0][p], d0, mul2(W[k + 1][1][p], d1));
+                }
+                float du0, du1;
+                {
+                    float2 r0 = mul2(dS[0][0], b2[0]), r1 = mul2(dS[1][0], b2[0]);
+#pragma unroll
+                    for (int p = 1; p < 4; p++) {
+                        r0 = fma2(dS[0][p], b2[p], r0);
+                        r1 = fma2(dS[1][p], b2[p], r1);
+                    }
+                    du0 = r0.x + r0.y;
+                    du1 = r1.x + r1.y;
+#pragma unroll
+                    for (int o = 1; o < 8; o <<= 1) {
+                        du0 += __shfl_xor_sync(kFull, du0, o);
+                        du1 += __shfl_xor_sync(kFull, du1, o);
+                    }
+                }
+                const float2 x2 = ld2(Xsrc + tt * 64 + C.j0);
+                const float2 xx0 = f2(x2.x, x2.x), xx1 = f2(x2.y, x2.y);
+                float2 pdb[4];
+                float pbeta = 0.f, dv0, dv1;
+                const float2 gg = f2(s.g[tt], s.g[tt]);
+                float2 gq = f2(0.f, 0.f);
+                if (DELTA) {
+                    const float be = s.beta[tt];
+                    const float2 vr2 = ld2(&s.VR[tt][C.j0]);
+                    const float dr0 = -be * du0, dr1 = -be * du1;
+                    dv0 = be * du0;
+                    dv1 = be * du1;
+                    pbeta = du0 * vr2.x + du1 * vr2.y;
+                    const float2 e0 = f2(dr0, dr0), e1 = f2(dr1, dr1);
+#pragma unroll
+                    for (int p = 0; p < 4; p++) {
+                        const float2 hp0 = mul2(W[k][0][p], a2[p]), hp1 = mul2(W[k][1][p], a2[p]);
+                        pdb[p] = fma2(hp0, e0, fma2(hp1, e1, fma2(dS[0][p], xx0, mul2(dS[1][p], xx1))));
+                        const float2 g0 = fma2(b2[p], e0, dS[0][p]), g1 = fma2(b2[p], e1, dS[1][p]);
+                        const float2 qs = fma2(g0, hp0, mul2(g1, hp1));
+                        dA_acc[p] = fma2(gg, qs, dA_acc[p]);
+                        gq = fma2(Ap[p], qs, gq);
+                        dS[0][p] = mul2(g0, a2[p]);
+                        dS[1][p] = mul2(g1, a2[p]);
+                    }
+                } else {
+                    dv0 = du0;
+                    dv1 = du1;
+#pragma unroll
+                    for (int p = 0; p < 4; p++) {
+                        const float2 hp0 = mul2(W[k][0][p], a2[p]), hp1 = mul2(W[k][1][p], a2[p]);
+                        pdb[p] = fma2(dS[0][p], xx0, mul2(dS[1][p], xx1));
+                        const float2 qs = fma2(dS[0][p], hp0, mul2(dS[1][p], hp1));
+                        dA_acc[p] = fma2(gg, qs, dA_acc[p]);
+                        gq = fma2(Ap[p], qs, gq);
+                        dS[0][p] = mul2(dS[0][p], a2[p]);
+                        dS[1][p] = mul2(dS[1][p], a2[p]);
+                    }
+                }
+                const int rofs = 8 * C.ig + 2 * C.m2;
+                *reinterpret_cast<float2*>(&s.part[wbuf][w][k][0][rofs]) = colsum_pairs(pdc);
+                *reinterpret_cast<float2*>(&s.part[wbuf][w][k][1][rofs]) = colsum_pairs(pdb);
+                float gs = gq.x + gq.y;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) gs += __shfl_xor_sync(kFull, gs, o);
+                if (DELTA) {
+                    pbeta += __shfl_xor_sync(kFull, pbeta, 8);
+                    pbeta += __shfl_xor_sync(kFull, pbeta, 16);
+                }
+                if (lane == 0) {
+                    s.gpart[wbuf][w][k] = gs;
+                    if (DELTA) s.bpart[wbuf][w][k] = pbeta;
+                }
+                if (C.ig == 0) *reinterpret_cast<float2*>(&s.dvb[wbuf][k][C.j0]) = f2(dv0, dv1);
+            }
+            __syncthreads();
+
+            // ---- reduction phase: thread (row ri, token rk) of this window ----
+            {
+                const int tt = tw + rk, t = t0 + tt;
+                const bool live = t < T;
+                float dc = 0.f, db = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < 8; ww++) {
+                    dc += s.part[wbuf][ww][rk][0][ri];
+                    db += s.part[wbuf][ww][rk][1][ri];
+                }
+                const size_t row = ((size_t)C.bb * T + t) * H + C.h;
+                if (live && ri < dk) {
+                    ((IO*)a.dc)[row * dk + ri] = from_f<IO>(dc);
+                    ((IO*)a.db)[row * dk + ri] = from_f<IO>(db);
+                }
+                if (live && ri < dv) ((IO*)a.dv_)[row * dv + ri] = from_f<IO>(s.dvb[wbuf][rk][ri]);
+                if (tid < kWin && t0 + tw + tid < T) {
+                    const size_t rowk = ((size_t)C.bb * T + t0 + tw + tid) * H + C.h;
+                    float sg = 0.f, sb = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < 8; ww++) {
+                        sg += s.gpart[wbuf][ww][tid];
+                        sb += s.bpart[wbuf][ww][tid];
+                    }
+                    ((IO*)a.dg)[rowk] = from_f<IO>(sg);
+                    if (DELTA) ((IO*)a.dbeta)[rowk] = from_f<IO>(sb);
+                }
+            }
+            wbuf ^= 1;
+        }
+    }
+    if (a.dh0) {
+#pragma unroll
+        for (int c = 0; c < 2; c++)
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+                const int i0 = C.roff[p], j = C.j0 + c;
+                if (j < dv) {
+                    if (i0 < dk) a.dh0[((size_t)C.u * dk + i0) * dv + j] = dS[c][p].x;
+                    if (i0 + 1 < dk) a.dh0[((size_t)C.u * dk + i0 + 1) * dv + j] = dS[c][p].y;
+                }
+            }
+    }
+    // dA_log partial of this unit: A_i sum_t g_t sum_j q_ij
+    {
+        const float2 z = colsum_pairs(dA_acc);
+        *reinterpret_cast<float2*>(&s.red[w][8 * C.ig + 2 * C.m2]) = z;
+        __syncthreads();
+        if (tid < dk) {
+            float acc = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < 8; ww++) acc += s.red[ww][tid];
+            dA_part[tid] = acc * s.Arow[tid];
+        }
+    }
+}
+
+// dA_log[h, i] = sum_b partial[b, h, i]  (fixed order, deterministic)
+__global__ void reduce_dalog_kernel(const float* part, float* dA_log, int B, int H, int dk)
+{
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= H * dk) return;
+    const int h = idx / dk, i = idx % dk;
+    float acc = 0.f;
+    for (int b = 0; b < B; b++) acc += part[((size_t)b * H + h) * dk + i];
+    dA_log[idx] = acc;
+}
+
+static bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+template <typename IO, bool DELTA>
+cudaError_t launch_t(const Args& a, const WsLayout& L, cudaStream_t st)
+{
+    const size_t smem = sizeof(BwdSmem<IO>);
+    cudaError_t e = cudaFuncSetAttribute(serial_bwd_kernel<IO, DELTA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    const size_t sz = sizeof(IO);
+    const bool vec = (a.dk * sz) % 16 == 0 && (a.dv * sz) % 16 == 0 && al16(a.b) && al16(a.c) && al16(a.v) &&
+                     al16(a.dO);
+    serial_bwd_kernel<IO, DELTA><<<a.B * a.H, 256, smem, st>>>(a, L, vec);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st)
+{
+    gdn_shape_t sh{a.B, a.H, a.T, a.dk, a.dv, a.mode, a.io};
+    const WsLayout L = ws_layout(sh, 1);
+    cudaError_t e;
+    if (a.io == GDN_BF16)
+        e = a.mode == GDN_DELTA ? launch_t<__nv_bfloat16, true>(a, L, st) : launch_t<__nv_bfloat16, false>(a, L, st);
+    else
+        e = a.mode == GDN_DELTA ? launch_t<float, true>(a, L, st) : launch_t<float, false>(a, L, st);
+    if (e != cudaSuccess) return e;
+    const int n = a.H * a.dk;
+    reduce_dalog_kernel<<<(n + 127) / 128, 128, 0, st>>>(
+        reinterpret_cast<const float*>((const unsigned char*)a.ws + L.dalog_off), a.dA_log, a.B, a.H, a.dk);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

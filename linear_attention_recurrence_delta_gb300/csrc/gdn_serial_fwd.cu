@@ -1,0 +1,230 @@
+// gdn_serial_fwd.cu -- token-serial forward of the gated delta rule on the
+// CUDA cores (fp32 state, packed fp32x2 arithmetic).
+//
+// Follows the per-token recurrence of "GDN & MLA Mechanism Deep-Dive", Step 4
+// (gated: h_t = alpha_t (.) h_{t-1} + b_t v_t^T) and the delta-rule card of
+// "HyMo-434M -- documentation portal" (h_t = h' + beta_t b_t (v_t - h'^T b_t)^T
+// with h' = alpha_t (.) h_{t-1}); both read o_t = h_t^T c_t, and
+// alpha_t = exp(g_t A), A = -exp(A_log).
+//
+// Columns j of the state never mix (the erase term acts on rows), so a CTA
+// owns 32 columns of one (batch, head) unit and needs no other CTA.  Thread
+// layout: warp w owns columns 8w..8w+7 of the CTA's 32; lane = 4 jl + ig
+// holds the 16 consecutive rows 16 ig .. 16 ig + 15 of column 8w + jl as 8
+// packed pairs.  A sum over rows is 8 packed products in-thread plus two
+// shuffles.  Inputs stream through shared memory in blocks of 32 tokens: the
+// next block's raw bytes arrive by cp.async while the current one computes.
+#include "gdn_internal.h"
+#include "serial_common.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace rec;
+
+constexpr int kTB = 32;    // tokens per staged block
+constexpr int kCols = 32;  // state columns per CTA
+
+template <typename IO>
+struct FwdSmem {
+    float A[kTB][kRowPad];   // alpha_t per state row
+    float Bv[kTB][kRowPad];  // b_t
+    float Cv[kTB][kRowPad];  // c_t
+    float V[kTB][kCols];     // v_t on this CTA's columns
+    float O[kTB][kCols];     // o_t staging for coalesced stores
+    float beta[kTB];
+    float Arow[64];          // A = -exp(A_log) of this head
+    float rg[kTB], rbeta[kTB];
+    IO rb[kTB][64], rc[kTB][64], rv[kTB][kCols];  // raw bytes of the next block
+};
+
+struct Unit {
+    int bb, h, u, jc0, ncols;
+};
+
+// Start fetching block [t0, t0+nt): row vectors by cp.async (or plain loads
+// when rows are not 16-byte aligned), g and beta into registers.
+template <typename IO, bool DELTA>
+__device__ __forceinline__ void issue_block(const Args& a, FwdSmem<IO>& s, const Unit& U, int t0, int nt, bool vec,
+                                            float& greg, float& breg)
+{
+    const int tid = threadIdx.x, dk = a.dk, dv = a.dv, T = a.T, H = a.H;
+    const IO* bk = (const IO*)a.b;
+    const IO* c = (const IO*)a.c;
+    const IO* v = (const IO*)a.v;
+    constexpr int E = 16 / sizeof(IO);
+    if (vec) {
+        const int cb = dk / E, cv = U.ncols / E, per = 2 * cb + cv;
+        for (int idx = tid; idx < nt * per; idx += blockDim.x) {
+            const int tt = idx / per, r = idx - tt * per;
+            const size_t row = ((size_t)U.bb * T + t0 + tt) * H + U.h;
+            if (r < cb) cp_async16(&s.rb[tt][r * E], bk + row * dk + r * E);
+            else if (r < 2 * cb) cp_async16(&s.rc[tt][(r - cb) * E], c + row * dk + (r - cb) * E);
+            else cp_async16(&s.rv[tt][(r - 2 * cb) * E], v + row * dv + U.jc0 + (r - 2 * cb) * E);
+        }
+        cp_async_commit();
+    } else {
+        for (int idx = tid; idx < nt * 64; idx += blockDim.x) {
+            const int tt = idx >> 6, i = idx & 63;
+            const size_t row = ((size_t)U.bb * T + t0 + tt) * H + U.h;
+            if (i < dk) {
+                s.rb[tt][i] = bk[row * dk + i];
+                s.rc[tt][i] = c[row * dk + i];
+            }
+            if (i < U.ncols) s.rv[tt][i] = v[row * dv + U.jc0 + i];
+        }
+    }
+    if (tid < nt) greg = to_f(((const IO*)a.g)[((size_t)U.bb * T + t0 + tid) * H + U.h]);
+    if (DELTA && tid >= 32 && tid - 32 < nt)
+        breg = to_f(((const IO*)a.beta)[((size_t)U.bb * T + t0 + tid - 32) * H + U.h]);
+}
+
+// raw block -> fp32 staged arrays (alpha computed here, once per row and token)
+template <typename IO, bool DELTA>
+__device__ __forceinline__ void convert_block(const Args& a, FwdSmem<IO>& s, const Unit& U, int nt)
+{
+    const int tid = threadIdx.x, dk = a.dk;
+    for (int idx = tid; idx < nt * 64; idx += blockDim.x) {
+        const int tt = idx >> 6, i = idx & 63;
+        float xa = 0.f, xb = 0.f, xc = 0.f;
+        if (i < dk) {
+            xa = expf(s.rg[tt] * s.Arow[i]);
+            xb = to_f(s.rb[tt][i]);
+            xc = to_f(s.rc[tt][i]);
+        }
+        const int p = prow(i);
+        s.A[tt][p] = xa;
+        s.Bv[tt][p] = xb;
+        s.Cv[tt][p] = xc;
+    }
+    for (int idx = tid; idx < nt * kCols; idx += blockDim.x) {
+        const int tt = idx / kCols, q = idx - tt * kCols;
+        s.V[tt][q] = q < U.ncols ? to_f(s.rv[tt][q]) : 0.f;
+    }
+    if (tid < nt) s.beta[tid] = DELTA ? s.rbeta[tid] : 0.f;
+}
+
+template <typename IO, bool DELTA>
+__global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    FwdSmem<IO>& s = *reinterpret_cast<FwdSmem<IO>*>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int ig = lane & 3, jl = lane >> 2, cl = 8 * w + jl;
+    Unit U;
+    U.u = blockIdx.y;
+    U.bb = U.u / a.H;
+    U.h = U.u % a.H;
+    U.jc0 = blockIdx.x * kCols;
+    U.ncols = min(kCols, a.dv - U.jc0);
+    const int j = U.jc0 + cl, dk = a.dk, dv = a.dv, T = a.T, H = a.H;
+    const int nblk = (T + kTB - 1) / kTB;
+
+    if (tid < 64) s.Arow[tid] = tid < dk ? -expf(a.A_log[U.h * dk + tid]) : 0.f;
+
+    // state: rows 16 ig + 2p, 16 ig + 2p + 1 of column j in h[p]
+    float2 h[8];
+#pragma unroll
+    for (int p = 0; p < 8; p++) {
+        const int i0 = 16 * ig + 2 * p;
+        float x0 = 0.f, x1 = 0.f;
+        if (a.h0 && j < dv) {
+            if (i0 < dk) x0 = a.h0[((size_t)U.u * dk + i0) * dv + j];
+            if (i0 + 1 < dk) x1 = a.h0[((size_t)U.u * dk + i0 + 1) * dv + j];
+        }
+        h[p] = f2(x0, x1);
+    }
+
+    float greg = 0.f, breg = 0.f;
+    issue_block<IO, DELTA>(a, s, U, 0, min(kTB, T), vec, greg, breg);
+    if (tid < 32) s.rg[tid] = greg;
+    else if (tid < 64) s.rbeta[tid - 32] = breg;
+    cp_async_wait_all();
+    __syncthreads();
+    convert_block<IO, DELTA>(a, s, U, min(kTB, T));
+    __syncthreads();
+    if (nblk > 1) issue_block<IO, DELTA>(a, s, U, kTB, min(kTB, T - kTB), vec, greg, breg);
+
+    IO* o = (IO*)a.o;
+    for (int n = 0; n < nblk; n++) {
+        const int t0 = n * kTB, nt = min(kTB, T - t0);
+#pragma unroll 4
+        for (int tt = 0; tt < nt; tt++) {
+            float2 av[8], bv[8];
+            ld_rows16(&s.A[tt][20 * ig], av);
+            ld_rows16(&s.Bv[tt][20 * ig], bv);
+            float2 hp[8];
+#pragma unroll
+            for (int p = 0; p < 8; p++) hp[p] = mul2(h[p], av[p]);
+            float x;
+            if (DELTA) {
+                float r = dot8x2(hp, bv);
+                r += __shfl_xor_sync(kFull, r, 1);
+                r += __shfl_xor_sync(kFull, r, 2);
+                x = s.beta[tt] * (s.V[tt][cl] - r);
+            } else {
+                x = s.V[tt][cl];
+            }
+            const float2 xx = f2(x, x);
+#pragma unroll
+            for (int p = 0; p < 8; p++) h[p] = fma2(bv[p], xx, hp[p]);
+            float2 cv[8];
+            ld_rows16(&s.Cv[tt][20 * ig], cv);
+            float ov = dot8x2(h, cv);
+            ov += __shfl_xor_sync(kFull, ov, 1);
+            ov += __shfl_xor_sync(kFull, ov, 2);
+            if (ig == 0) s.O[tt][cl] = ov;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < nt * U.ncols; idx += blockDim.x) {
+            const int tt = idx / U.ncols, q = idx - tt * U.ncols;
+            o[(((size_t)U.bb * T + t0 + tt) * H + U.h) * dv + U.jc0 + q] = from_f<IO>(s.O[tt][q]);
+        }
+        if (n + 1 < nblk) {
+            if (tid < 32) s.rg[tid] = greg;
+            else if (tid < 64) s.rbeta[tid - 32] = breg;
+            cp_async_wait_all();
+            __syncthreads();
+            convert_block<IO, DELTA>(a, s, U, min(kTB, T - t0 - kTB));
+            __syncthreads();
+            if (n + 2 < nblk)
+                issue_block<IO, DELTA>(a, s, U, t0 + 2 * kTB, min(kTB, T - t0 - 2 * kTB), vec, greg, breg);
+        }
+    }
+
+    if (a.hT && j < dv) {
+#pragma unroll
+        for (int p = 0; p < 8; p++) {
+            const int i0 = 16 * ig + 2 * p;
+            if (i0 < dk) a.hT[((size_t)U.u * dk + i0) * dv + j] = h[p].x;
+            if (i0 + 1 < dk) a.hT[((size_t)U.u * dk + i0 + 1) * dv + j] = h[p].y;
+        }
+    }
+}
+
+static bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+template <typename IO, bool DELTA>
+cudaError_t launch_t(const Args& a, cudaStream_t st)
+{
+    const size_t smem = sizeof(FwdSmem<IO>);
+    cudaError_t e = cudaFuncSetAttribute(serial_fwd_kernel<IO, DELTA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    const size_t sz = sizeof(IO);
+    const bool vec = (a.dk * sz) % 16 == 0 && (a.dv * sz) % 16 == 0 && al16(a.b) && al16(a.c) && al16(a.v);
+    dim3 grid((a.dv + kCols - 1) / kCols, a.B * a.H);
+    serial_fwd_kernel<IO, DELTA><<<grid, 128, smem, st>>>(a, vec);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_serial_fwd(const Args& a, cudaStream_t st)
+{
+    if (a.io == GDN_BF16)
+        return a.mode == GDN_DELTA ? launch_t<__nv_bfloat16, true>(a, st) : launch_t<__nv_bfloat16, false>(a, st);
+    return a.mode == GDN_DELTA ? launch_t<float, true>(a, st) : launch_t<float, false>(a, st);
+}
+
+}  // namespace gdn
