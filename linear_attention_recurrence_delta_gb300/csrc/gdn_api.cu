@@ -29,8 +29,10 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward)
     if (backward) {
         const size_t units = (size_t)s.B * s.H;
         const size_t nblk = (size_t)((s.T + kSerialBlock - 1) / kSerialBlock);
-        L.ck_off = off;
-        off = round_up(off + units * nblk * kStateSlot, 256);
+        L.snap_off = off;
+        off = round_up(off + units * nblk * (kSerialBlock / kSerialSnap) * kStateSlot, 256);
+        L.xvr_off = off;
+        if (s.mode == GDN_DELTA) off = round_up(off + units * nblk * kSerialBlock * 128 * sizeof(float), 256);
         L.dalog_off = off;
         off = round_up(off + units * (size_t)s.dk * 4, 256);
     }

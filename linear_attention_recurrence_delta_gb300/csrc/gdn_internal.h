@@ -31,12 +31,14 @@ struct Args {
 // Workspace carve-up.  The first 256 bytes always hold the device status word.
 struct WsLayout {
     size_t status_off = 0;        // uint32 status code, uint32 detail
-    size_t ck_off = 0;            // serial backward: state entering every block of kSerialBlock tokens
+    size_t snap_off = 0;          // serial backward: state entering every kSerialSnap tokens
+    size_t xvr_off = 0;           // serial backward, delta: x and v - h'^T b of every token
     size_t dalog_off = 0;         // per-(b,h) dA_log partials, float [B*H, d_k]
     size_t total = 0;
 };
 
-constexpr int kSerialBlock = 32;               // tokens between backward checkpoints
+constexpr int kSerialBlock = 32;               // tokens per backward block
+constexpr int kSerialSnap = 8;                 // tokens between backward state snapshots
 constexpr size_t kStateSlot = 16 * 256 * 4;    // one state snapshot (256 threads x 16 floats)
 
 WsLayout ws_layout(const gdn_shape_t& s, int backward);

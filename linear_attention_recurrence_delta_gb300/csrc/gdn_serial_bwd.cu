@@ -19,10 +19,11 @@
 // 8w..8w+7; lane = 8 jl + ig holds columns j0 = 8w + 2 jl and j0 + 1 and the
 // eight rows 8 ig .. 8 ig + 7, stored as four packed row pairs in an order
 // permuted by jl so that the sums over columns (dc, db) need no selects.
-// Recompute: the forward sweep keeps the state every 32 tokens in the
-// workspace; a 32-token block is recomputed into shared-memory snapshots every
-// 8 tokens, and each 4-token window is recomputed into registers and walked
-// backwards.  Per-warp row partials are summed across warps once per window.
+// Recompute: the forward sweep writes the state every 8 tokens (and, delta,
+// x and v - h'^T b of every token) to the workspace; the reverse walk brings
+// back one 32-token block of them at a time by cp.async, recomputes each
+// 4-token window into registers from its snapshot and walks it backwards.
+// Per-warp row partials are summed across warps once per window.
 #include "gdn_internal.h"
 #include "serial_common.cuh"
 
@@ -32,7 +33,7 @@ namespace {
 using namespace rec;
 
 constexpr int kBT = kSerialBlock;  // tokens per staged block = checkpoint interval
-constexpr int kSub = 8;            // tokens per shared-memory snapshot
+constexpr int kSub = kSerialSnap;  // tokens per state snapshot
 constexpr int kWin = 4;            // tokens per register window
 constexpr int kNQ = 2;             // row quantities summed over columns: dc, db
 
@@ -41,7 +42,7 @@ struct BwdSmem {
     float A[kBT][64], Bv[kBT][64], Cv[kBT][64];                 // alpha_t, b_t, c_t
     float V[kBT][64], DO[kBT][64], X[kBT][64], VR[kBT][64];     // v_t, do_t, x, v_t - h'^T b_t
     float beta[kBT], g[kBT];
-    float Arow[64];
+    float Arow[64], Arow2[64];  // A and A log2(e)
     float2 snap[kBT / kSub][8][256];                             // per-thread state snapshots
     float part[2][8][kWin][kNQ][64];                             // per-warp row partials
     float dvb[2][kWin][64];
@@ -119,7 +120,7 @@ __device__ __forceinline__ void finish_block(const Args& a, BwdSmem<IO>& s, cons
     for (int idx = tid; idx < kBT * 64; idx += 256) {
         const int tt = idx >> 6, i = idx & 63;
         const bool ok = tt < nt;
-        s.A[tt][i] = ok ? expf(s.rg[tt] * s.Arow[i]) : 1.f;
+        s.A[tt][i] = ok ? decay<IO>(s.rg[tt], s.Arow[i], s.Arow2[i]) : 1.f;
         s.Bv[tt][i] = ok && i < dk ? to_f(s.rb[tt][i]) : 0.f;
         s.Cv[tt][i] = grad && ok && i < dk ? to_f(s.rc[tt][i]) : 0.f;
         s.V[tt][i] = ok && i < dv ? to_f(s.rv[tt][i]) : 0.f;
@@ -241,10 +242,16 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
     const int tid = C.tid, lane = C.lane, w = C.w;
     const int dk = a.dk, dv = a.dv, T = a.T, H = a.H;
     const int nblk = (T + kBT - 1) / kBT;
-    float2* ck = reinterpret_cast<float2*>((unsigned char*)a.ws + L.ck_off) + (size_t)C.u * nblk * 2048;
+    constexpr int kSnapPerBlk = kBT / kSub;
+    float2* gsnap = reinterpret_cast<float2*>((unsigned char*)a.ws + L.snap_off) + (size_t)C.u * nblk * kSnapPerBlk * 2048;
+    float* gxvr = reinterpret_cast<float*>((unsigned char*)a.ws + L.xvr_off) + (size_t)C.u * nblk * kBT * 128;
     float* dA_part = reinterpret_cast<float*>((unsigned char*)a.ws + L.dalog_off) + (size_t)C.u * dk;
 
-    if (tid < 64) s.Arow[tid] = tid < dk ? -expf(a.A_log[C.h * dk + tid]) : 0.f;
+    if (tid < 64) {
+        const float Ai = tid < dk ? -expf(a.A_log[C.h * dk + tid]) : 0.f;
+        s.Arow[tid] = Ai;
+        s.Arow2[tid] = Ai * 1.4426950408889634f;
+    }
 
     // load a [B,H,dk,dv] fp32 matrix in this thread's register layout
     auto load_state = [&](const float* src, float2 (&S)[2][4]) {
@@ -270,15 +277,24 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
     __syncthreads();  // Arow
     issue_block<IO, DELTA>(a, s, C, 0, false, vec, greg, breg);
     for (int n = 0; n < nblk; n++) {
-#pragma unroll
-        for (int q = 0; q < 8; q++) ck[(size_t)n * 2048 + q * 256 + tid] = S[q >> 2][q & 3];
         finish_block<IO, DELTA>(a, s, C, n * kBT, false, greg, breg);
         if (n + 1 < nblk) issue_block<IO, DELTA>(a, s, C, (n + 1) * kBT, false, vec, greg, breg);
         else issue_block<IO, DELTA>(a, s, C, n * kBT, true, vec, greg, breg);  // first block of the reverse walk
+        float2* snap_n = gsnap + (size_t)n * kSnapPerBlk * 2048;
+        float* xvr_n = gxvr + (size_t)n * kBT * 128;
 #pragma unroll 1
-        for (int tt = 0; tt < kBT; tt++)
-            fwd_full<DELTA, false>(S, s.A[tt], s.Bv[tt], s.V[tt], s.beta[tt], nullptr, nullptr, C);
+        for (int tt = 0; tt < kBT; tt++) {
+            if ((tt & (kSub - 1)) == 0) {
+#pragma unroll
+                for (int q = 0; q < 8; q++) snap_n[((tt / kSub) * 8 + q) * 256 + tid] = S[q >> 2][q & 3];
+            }
+            fwd_full<DELTA, DELTA>(S, s.A[tt], s.Bv[tt], s.V[tt], s.beta[tt], xvr_n + tt * 64,
+                                   xvr_n + kBT * 64 + tt * 64, C);
+        }
     }
+
+    // the reverse walk reads back what other threads stored in the sweep
+    __syncthreads();
 
     // ---------------- adjoint: dH = dh_T ----------------
     float2 dS[2][4];
@@ -289,27 +305,26 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
         Ap[p] = ld2(&s.Arow[C.roff[p]]);
         dA_acc[p] = f2(0.f, 0.f);
     }
-    const int ri = tid >> 2, rk = tid & 3;  // reduction-phase role: row ri, window token rk
+    const int ri = tid & 63, rk = tid >> 6;  // reduction-phase role: row ri, window token rk
     int wbuf = 0;
 
     // ---------------- reverse walk over blocks ----------------
     for (int n = nblk - 1; n >= 0; n--) {
         const int t0 = n * kBT;
-        float2 Sb[2][4];
-#pragma unroll
-        for (int q = 0; q < 8; q++) Sb[q >> 2][q & 3] = ck[(size_t)n * 2048 + q * 256 + tid];
+        // this block's snapshots (and x, v - h'^T b) from the forward sweep
+        {
+            const float4* src = reinterpret_cast<const float4*>(gsnap + (size_t)n * kSnapPerBlk * 2048);
+            float4* dst = reinterpret_cast<float4*>(&s.snap[0][0][0]);
+            for (int idx = tid; idx < kSnapPerBlk * 2048 / 2; idx += 256) cp_async16(dst + idx, src + idx);
+            if (DELTA) {
+                const float4* sx = reinterpret_cast<const float4*>(gxvr + (size_t)n * kBT * 128);
+                float4* dx = reinterpret_cast<float4*>(&s.X[0][0]);
+                for (int idx = tid; idx < kBT * 128 / 4; idx += 256) cp_async16(dx + idx, sx + idx);
+            }
+            cp_async_commit();
+        }
         finish_block<IO, DELTA>(a, s, C, t0, true, greg, breg);
         if (n > 0) issue_block<IO, DELTA>(a, s, C, t0 - kBT, true, vec, greg, breg);
-        // block recompute: snapshots every 8 tokens, x and v - h'^T b cached
-#pragma unroll 1
-        for (int tt = 0; tt < kBT; tt++) {
-            if ((tt & (kSub - 1)) == 0) {
-#pragma unroll
-                for (int q = 0; q < 8; q++) s.snap[tt / kSub][q][tid] = Sb[q >> 2][q & 3];
-            }
-            fwd_full<DELTA, true>(Sb, s.A[tt], s.Bv[tt], s.V[tt], s.beta[tt], s.X[tt], s.VR[tt], C);
-        }
-        __syncwarp();
         const float* Xsrc = DELTA ? &s.X[0][0] : &s.V[0][0];
 
 #pragma unroll 1

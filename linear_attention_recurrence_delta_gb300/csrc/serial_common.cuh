@@ -37,6 +37,23 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
+// 2^x on the special-function unit (relative error about 2^-22)
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// alpha = exp(g A): the library expf for fp32 I/O; for bf16 I/O the SFU exp2
+// of g (A log2 e), whose ~1e-6 relative error is far below bf16 rounding
+template <typename IO>
+__device__ __forceinline__ float decay(float g, float A, float A_log2e)
+{
+    if (sizeof(IO) == 4) return expf(g * A);
+    return ex2_approx(g * A_log2e);
+}
+
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
