@@ -68,6 +68,15 @@ def io_bytes(w, backward=False):
     return rd + wr + 2 * state + 2 * w.H * w.dk * 4
 
 
+def fwd_kernel_name(w):
+    """The kernel gdn_fwd launches for workload w (one launch per call)."""
+    if w.T <= 8:
+        return "decode_kernel (one launch)"
+    if w.dtype == "bf16":
+        return f"fwd_tc_kernel<{w.mode}> (one launch)"
+    return f"serial_fwd_kernel<f32, {w.mode}> (one launch)"
+
+
 class ClockSampler:
     """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
 
@@ -291,7 +300,7 @@ def main():
     achieved = fwd_bytes / (launch_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
-                "kernel": "gdn_fwd (one launch)", "bytes_per_launch": fwd_bytes, "launch_ms": launch_ms}
+                "kernel": fwd_kernel_name(w), "bytes_per_launch": fwd_bytes, "launch_ms": launch_ms}
     # launches of our kernels per forward step: the forward kernel itself
     gpu_launches = 1 * args.steps
 
@@ -343,7 +352,8 @@ def main():
             "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16", "data": "synthetic",
             "config": {"workload": w.name, "pass": "fwd", "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
                        "mode": w.mode, "io": w.dtype, "parallelism": "replicas" if world > 1 else "single",
-                       "l2": f"inputs {fwd_bytes / 1e6:.1f} MB > 129 MB L2, no flush"},
+                       "l2": (f"inputs+outputs {fwd_bytes / 1e6:.1f} MB > 129 MB L2, no flush" if fwd_bytes > 129e6
+                              else f"inputs+outputs {fwd_bytes / 1e6:.1f} MB fit the 129 MB L2: L2-warm, no flush")},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "fwd_bwd": fwdbwd, "clocks": clocks,
             "gpu_launches": gpu_launches,
         }

@@ -95,6 +95,10 @@ size_t gdn_workspace_bytes(const gdn_shape_t* shape, int backward);
 
 /* Forward pass.  Reads v, b, c, g, beta (NULL iff mode == GDN_GATED), A_log,
  * h0 (NULL => zero initial state); writes o and hT (NULL => not written).
+ * hT may be the same buffer as h0: the state is then updated in place, as in
+ * token-by-token decoding ("GDN & MLA Mechanism Deep-Dive", Step 4: the
+ * state is all a head carries from one token to the next).  Sequences of at
+ * most 8 tokens take a kernel laid out for that case.
  * ws must be device memory of at least gdn_workspace_bytes(shape, 0) bytes,
  * 256-byte aligned.  Returns GDN_OK once the work is enqueued on `stream`. */
 gdn_status_t gdn_fwd(const gdn_shape_t* shape,

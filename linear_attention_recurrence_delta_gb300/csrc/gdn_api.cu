@@ -120,13 +120,14 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape, const void* v, const v
     a.ws = ws; a.ws_bytes = ws_bytes;
     const size_t state_bytes = (size_t)a.B * a.H * a.dk * a.dv * sizeof(float);
     if (a.T == 0) {
-        if (hT) {
+        if (hT && hT != h0) {
             cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, state_bytes, cudaMemcpyDeviceToDevice, st)
                                : cudaMemsetAsync(hT, 0, state_bytes, st);
             if (e != cudaSuccess) return GDN_ERR_CUDA;
         }
         return GDN_OK;
     }
+    if (a.T <= decode_max_tokens()) return launch_decode(a, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     bool handled = false;
     if (a.io == GDN_BF16) {
         if (launch_fwd_tc(a, st, &handled) != cudaSuccess) return GDN_ERR_CUDA;

@@ -47,6 +47,8 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward);
 cudaError_t launch_serial_fwd(const Args& a, cudaStream_t st);
 cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled);
+cudaError_t launch_decode(const Args& a, cudaStream_t st);   // 1 <= T <= decode_max_tokens()
+int decode_max_tokens();
 
 // Device status word helpers.
 enum : uint32_t { kDevOk = 0, kDevTimeout = 1 };

@@ -152,6 +152,10 @@ WORKLOADS = {
         "delta_bf16_1x16x32768x64_slowdecay", "delta", "bf16", 1, 16, 32768, 64, 64, seed=6,
         backward=True, b_dist="l2norm", c_dist="l2norm", g_mu=-4.0,
         notes="added slow-decay stress input"),
+    # added: one decoding step (T = 1) of a large batch, state in and out
+    "delta_bf16_decode_512x16x1x64": Workload(
+        "delta_bf16_decode_512x16x1x64", "delta", "bf16", 512, 16, 1, 64, 64, seed=7,
+        b_dist="l2norm", c_dist="l2norm", h0_std=0.1, notes="added single-token decode step"),
 }
 
 
