@@ -36,6 +36,29 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward)
         L.dalog_off = off;
         off = round_up(off + units * (size_t)s.dk * 4, 256);
     }
+    if (!backward && s.T > 0) {
+        const int P = tsplit_factor(s);
+        if (P > 1) {
+            const size_t vunits = (size_t)s.B * P * s.H;
+            const size_t st = vunits * s.dk * s.dv * sizeof(float);
+            L.ts_h_off = off;
+            off = round_up(off + st, 256);
+            L.ts_s_off = off;
+            off = round_up(off + st, 256);
+            if (s.mode == GDN_DELTA) {
+                const size_t sq = vunits * s.dk * s.dk * sizeof(float);
+                const size_t tk = (size_t)s.B * s.T * s.H * s.dk * (s.io == GDN_BF16 ? 2 : 4);
+                L.ts_a_off = off;
+                off = round_up(off + sq, 256);
+                L.ts_i_off = off;
+                off = round_up(off + sq, 256);
+                L.ts_zv_off = off;
+                off = round_up(off + tk, 256);
+                L.ts_so_off = off;
+                off = round_up(off + tk, 256);
+            }
+        }
+    }
     L.total = off;
     return L;
 }
@@ -90,6 +113,19 @@ static Args make_args(const gdn_shape_t* s)
     return a;
 }
 
+// One forward over the whole shape: few tokens -> decode kernel; bf16 ->
+// tcgen05 chunked kernel; fp32 -> token-serial kernel.
+static cudaError_t fwd_core(const Args& a, cudaStream_t st)
+{
+    if (a.T <= decode_max_tokens()) return launch_decode(a, st);
+    bool handled = false;
+    if (a.io == GDN_BF16) {
+        const cudaError_t e = launch_fwd_tc(a, st, &handled);
+        if (e != cudaSuccess) return e;
+    }
+    return handled ? cudaSuccess : launch_serial_fwd(a, st);
+}
+
 }  // namespace gdn
 
 using namespace gdn;
@@ -127,13 +163,9 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape, const void* v, const v
         }
         return GDN_OK;
     }
-    if (a.T <= decode_max_tokens()) return launch_decode(a, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-    bool handled = false;
-    if (a.io == GDN_BF16) {
-        if (launch_fwd_tc(a, st, &handled) != cudaSuccess) return GDN_ERR_CUDA;
-    }
-    if (!handled && launch_serial_fwd(a, st) != cudaSuccess) return GDN_ERR_CUDA;
-    return GDN_OK;
+    const int P = tsplit_factor(*shape);
+    const cudaError_t e = P > 1 ? launch_fwd_tsplit(a, ws_layout(*shape, 0), P, st, fwd_core) : fwd_core(a, st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape, const void* v, const void* b, const void* c,

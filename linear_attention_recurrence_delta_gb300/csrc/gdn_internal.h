@@ -34,9 +34,18 @@ struct WsLayout {
     size_t snap_off = 0;          // serial backward: state entering every kSerialSnap tokens
     size_t xvr_off = 0;           // serial backward, delta: x and v - h'^T b of every token
     size_t dalog_off = 0;         // per-(b,h) dA_log partials, float [B*H, d_k]
+    // forward split in time (long sequences over few heads), see gdn_tsplit.cu
+    size_t ts_h_off = 0;          // leaving states from a zero start   [B*P, H, d_k, d_v]
+    size_t ts_s_off = 0;          // entering states of the segments    [B*P, H, d_k, d_v]
+    size_t ts_a_off = 0;          // delta: segment transitions          [B*P, H, d_k, d_k]
+    size_t ts_i_off = 0;          // delta: identity starting states     [B*P, H, d_k, d_k]
+    size_t ts_zv_off = 0;         // delta: zero values                  [B, T, H, d_k] (I/O dtype)
+    size_t ts_so_off = 0;         // delta: outputs of the transition run [B, T, H, d_k] (I/O dtype)
     size_t total = 0;
 };
 
+constexpr long kSplitSMs = 152;                // a forward is split in time only while B*H*P <= this
+constexpr int kSplitMinTokens = 512;           // and every segment keeps at least this many tokens
 constexpr int kSerialBlock = 32;               // tokens per backward block
 constexpr int kSerialSnap = 8;                 // tokens between backward state snapshots
 constexpr size_t kStateSlot = 16 * 256 * 4;    // one state snapshot (256 threads x 16 floats)
@@ -48,6 +57,9 @@ cudaError_t launch_serial_fwd(const Args& a, cudaStream_t st);
 cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled);
 cudaError_t launch_decode(const Args& a, cudaStream_t st);   // 1 <= T <= decode_max_tokens()
+int tsplit_factor(const gdn_shape_t& s);       // segments P of a time-split forward, 1 = no split
+cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
+                              cudaError_t (*fwd_core)(const Args&, cudaStream_t));
 int decode_max_tokens();
 
 // Device status word helpers.

@@ -107,3 +107,17 @@ def test_bwd_rejects_bad_arguments_before_any_device_work(lib):
     assert call(ws_bytes=256) == 5
     assert call(dA_log=FAKE + 4) == 3
     assert call(b=FAKE + 2) == 3
+
+
+def test_time_split_workspace():
+    """Long sequences over few heads take the time-split forward, whose workspace holds per-segment states
+    (delta: also transitions and a zero-value tensor); many heads or short sequences need none."""
+    lib = gdn
+    few = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0)
+    many = lib.gdn_workspace_bytes(lib.make_shape(8, 16, 4096, 64, 64, "delta", "bf16"), 0)
+    gated = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "gated", "bf16"), 0)
+    short = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 1000, 64, 64, "delta", "bf16"), 0)
+    assert many == 256 and short == 256
+    # P = 8 segments: 2 x 128 states (16 KB) + 2 x 128 transitions + zero values and scratch outputs
+    assert few >= 256 + 4 * 128 * 16384 + 2 * 32768 * 16 * 64 * 2
+    assert 256 + 2 * 128 * 16384 <= gated < few

@@ -1,0 +1,51 @@
+"""Forward split in time (long sequences over few heads) against the fp64 oracle.
+
+When B*H*P fits the GPU for some P >= 4 (delta) or 3 (gated) dividing T with
+at least 512 tokens per segment, gdn_fwd runs every segment from a zero
+state, (delta) every segment's transition from the identity with v = 0, a
+scan over segments and every segment again from its true entering state.
+These shapes take that path; the 1 x 16 x 32768 workload test covers it too.
+"""
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_recurrence_delta_gb300 as gdn
+import oracle
+from linear_attention_recurrence_delta_gb300 import inputs as I
+from tests.gdn_testlib import TOL, assert_close, dev, dev32, run_fwd, tdtype
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_fwd(w, x):
+    return oracle.gdn_fwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], mode=w.mode)
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+@pytest.mark.parametrize("io,B,H,T,d", [("bf16", 1, 4, 4096, 64), ("bf16", 2, 3, 3072, 56), ("f32", 1, 2, 2048, 32)])
+def test_tsplit_parity(mode, io, B, H, T, d):
+    w = I.custom(name=f"ts_{mode}_{io}_{B}x{H}x{T}x{d}", mode=mode, dtype=io, B=B, H=H, T=T, dk=d, dv=d,
+                 seed=T + d, h0_std=0.3, b_dist="l2norm" if mode == "delta" else "normal/8", c_dist="l2norm",
+                 g_mu=-1.0)
+    x = I.make_inputs(w)
+    o, hT = run_fwd(w, x)
+    ro, rhT = oracle_fwd(w, x)
+    assert_close(o, ro, TOL[io], f"{w.name} o")
+    assert_close(hT, rhT, TOL[io], f"{w.name} hT")
+
+
+def test_tsplit_in_place_state():
+    """hT may alias h0 on the split path as well."""
+    w = I.custom(name="ts_inplace", mode="delta", dtype="bf16", B=1, H=4, T=4096, dk=64, dv=64, seed=12,
+                 h0_std=0.3, b_dist="l2norm", c_dist="l2norm", g_mu=-2.0)
+    x = I.make_inputs(w)
+    s = gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.mode, w.dtype)
+    t = {k: dev(x[k], "bf16") for k in ("v", "b", "c", "g", "beta")}
+    state = dev32(x["h0"])
+    o = torch.empty((w.B, w.T, w.H, w.dv), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(gdn.gdn_workspace_bytes(s, 0), dtype=torch.uint8, device="cuda")
+    gdn.check(gdn.gdn_fwd(s, t["v"], t["b"], t["c"], t["g"], t["beta"], dev32(x["A_log"]), state, o, state, ws))
+    ro, rhT = oracle_fwd(w, x)
+    assert_close(o.double().cpu().numpy(), ro, TOL["bf16"], "o")
+    assert_close(state.double().cpu().numpy(), rhT, TOL["bf16"], "state")
