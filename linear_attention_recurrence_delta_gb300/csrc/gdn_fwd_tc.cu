@@ -109,7 +109,6 @@ struct Small {
     float G[64];
     float A2[64];
     float decay[64];
-    float scan[64];
     float g[kStages][64];
     float beta[kStages][64];
     uint64_t full[kStages], mma;
@@ -270,19 +269,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             }
 
             // (1) inclusive scan of g; overflow check of the anchors
-            if (r < 64) {
-                float x = S.g[s][r];
+            if (warp == 0) {
+                // lane l scans the pair (2l, 2l+1)
+                const float ga = S.g[s][2 * lane], gb = S.g[s][2 * lane + 1];
+                float x = ga + gb;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, x, o);
                     if (lane >= o) x += y;
                 }
-                S.scan[r] = x;
-            }
-            named_bar_sync(1, kMath);
-            if (r < 64) S.G[r] = S.scan[r] + (r >= 32 ? S.scan[31] : 0.f);
-            named_bar_sync(1, kMath);
-            if (warp == 0) {
+                const float ex = __shfl_up_sync(0xffffffffu, x, 1);
+                S.G[2 * lane] = (lane > 0 ? ex : 0.f) + ga;
+                S.G[2 * lane + 1] = x;
+                __syncwarp();
                 float span = 0.f;
                 if (lane < 8) {
                     const float g0 = S.G[8 * lane], g3 = S.G[8 * lane + 3], g7 = S.G[8 * lane + 7];
@@ -291,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const bool bad = __any_sync(0xffffffffu, span * S.a2max > kSafeLog2);
                 if (lane == 0) S.unsafe = bad ? 1u : 0u;
             }
+            named_bar_sync(1, kMath);   // G and the overflow flag
             // decay constants per (8-block, reference point); every exponent <= 0
             {
                 float* K = reinterpret_cast<float*>(sm + OFF_K);
@@ -412,8 +412,25 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     }
                 }
             }
-            named_bar_sync(1, kMath);
-            // (2b) Bhat^T rows (i = channel), from the L3 column operand; decay vector
+            smem_to_tc();
+
+            // (3) level MMAs
+            if (r == 0) {
+                const uint32_t x0 = smem_u32(X);
+                const uint32_t b1[3] = {x0 + X_B1a, x0 + X_B1b, x0 + X_B1c};
+                const uint32_t d1[3] = {TM_D1a, TM_D1b, TM_D1c};
+#pragma unroll
+                for (int I = 1; I <= 3; I++)
+                    mma_k64(tbase + d1[I - 1], x0 + X_A1, b1[I - 1], false, idesc_f16(128, 16 * I, false, false), false);
+                mma_k64(tbase + TM_D2, x0 + X_A2, x0 + X_B2, false, idesc_f16(128, 64, false, false), false);
+                const uint32_t id3 = idesc_bf16(128, 64, false, false);
+                mma_k64(tbase + TM_D3, x0 + X_A3, x0 + X_B3, false, id3, false);
+                mma_k64(tbase + TM_D3, x0 + X_A3, x0 + X_B3L, false, id3, true);
+                mma_k64(tbase + TM_D3, x0 + X_A3L, x0 + X_B3, false, id3, true);
+                mma_commit(&S.mma);
+            }
+            // (2b) Bhat^T rows (i = channel), from the L3 column operand; decay vector.  Runs while the
+            // level MMAs execute: it reads their operands and writes only [Bhat^T ; P] rows 0..63.
             {
                 const int i = r & 63, sq = r >> 6;
                 const float a2 = S.A2[i], G63 = S.G[63];
@@ -444,23 +461,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     }
                 }
                 if (r < 64) S.decay[r] = fast_exp2(S.A2[r] * S.G[63]);
-            }
-            smem_to_tc();
-
-            // (3) level MMAs
-            if (r == 0) {
-                const uint32_t x0 = smem_u32(X);
-                const uint32_t b1[3] = {x0 + X_B1a, x0 + X_B1b, x0 + X_B1c};
-                const uint32_t d1[3] = {TM_D1a, TM_D1b, TM_D1c};
-#pragma unroll
-                for (int I = 1; I <= 3; I++)
-                    mma_k64(tbase + d1[I - 1], x0 + X_A1, b1[I - 1], false, idesc_f16(128, 16 * I, false, false), false);
-                mma_k64(tbase + TM_D2, x0 + X_A2, x0 + X_B2, false, idesc_f16(128, 64, false, false), false);
-                const uint32_t id3 = idesc_bf16(128, 64, false, false);
-                mma_k64(tbase + TM_D3, x0 + X_A3, x0 + X_B3, false, id3, false);
-                mma_k64(tbase + TM_D3, x0 + X_A3, x0 + X_B3L, false, id3, true);
-                mma_k64(tbase + TM_D3, x0 + X_A3L, x0 + X_B3, false, id3, true);
-                mma_commit(&S.mma);
             }
             if (!mma_wait_all()) break;
 
