@@ -22,43 +22,73 @@ static bool shape_ok(const gdn_shape_t& s)
     return true;
 }
 
+// the serial backward's buffers for shape s, placed from `off`
+static size_t place_bwd_core(const gdn_shape_t& s, WsLayout& L, size_t off)
+{
+    const size_t units = (size_t)s.B * s.H;
+    const size_t nblk = (size_t)((s.T + kSerialBlock - 1) / kSerialBlock);
+    L.snap_off = off;
+    off = round_up(off + units * nblk * (kSerialBlock / kSerialSnap) * kStateSlot, 256);
+    L.xvr_off = off;
+    if (s.mode == GDN_DELTA) off = round_up(off + units * nblk * kSerialBlock * 128 * sizeof(float), 256);
+    L.dalog_off = off;
+    return round_up(off + units * (size_t)s.dk * 4, 256);
+}
+
+// buffers of a time split into P segments (see gdn_tsplit.cu), placed from `off`
+static size_t place_tsplit(const gdn_shape_t& s, int P, bool backward, WsLayout& L, size_t off)
+{
+    const size_t vunits = (size_t)s.B * P * s.H;
+    const size_t st = vunits * s.dk * s.dv * sizeof(float);
+    const size_t esz = s.io == GDN_BF16 ? 2 : 4;
+    L.ts_h_off = off;
+    off = round_up(off + st, 256);
+    L.ts_s_off = off;
+    off = round_up(off + st, 256);
+    if (s.mode == GDN_DELTA) {
+        const size_t sq = vunits * s.dk * s.dk * sizeof(float);
+        const size_t tk = (size_t)s.B * s.T * s.H * s.dk * esz;
+        L.ts_a_off = off;
+        off = round_up(off + sq, 256);
+        L.ts_i_off = off;
+        off = round_up(off + sq, 256);
+        L.ts_zv_off = off;
+        off = round_up(off + tk, 256);
+        L.ts_so_off = off;
+        off = round_up(off + tk, 256);
+    }
+    if (backward) {
+        L.ts_o_off = off;
+        off = round_up(off + (size_t)s.B * s.T * s.H * s.dv * esz, 256);
+        L.ts_g_off = off;
+        off = round_up(off + st, 256);
+        L.ts_e_off = off;
+        off = round_up(off + st, 256);
+    }
+    return off;
+}
+
+WsLayout ws_layout_bwd_core(const gdn_shape_t& s)
+{
+    WsLayout L;
+    L.total = place_bwd_core(s, L, 256);
+    return L;
+}
+
 WsLayout ws_layout(const gdn_shape_t& s, int backward)
 {
     WsLayout L;
     size_t off = 256;  // status word
+    const int P = s.T > 0 ? tsplit_factor(s, backward) : 1;
     if (backward) {
-        const size_t units = (size_t)s.B * s.H;
-        const size_t nblk = (size_t)((s.T + kSerialBlock - 1) / kSerialBlock);
-        L.snap_off = off;
-        off = round_up(off + units * nblk * (kSerialBlock / kSerialSnap) * kStateSlot, 256);
-        L.xvr_off = off;
-        if (s.mode == GDN_DELTA) off = round_up(off + units * nblk * kSerialBlock * 128 * sizeof(float), 256);
-        L.dalog_off = off;
-        off = round_up(off + units * (size_t)s.dk * 4, 256);
-    }
-    if (!backward && s.T > 0) {
-        const int P = tsplit_factor(s);
+        gdn_shape_t core = s;
         if (P > 1) {
-            const size_t vunits = (size_t)s.B * P * s.H;
-            const size_t st = vunits * s.dk * s.dv * sizeof(float);
-            L.ts_h_off = off;
-            off = round_up(off + st, 256);
-            L.ts_s_off = off;
-            off = round_up(off + st, 256);
-            if (s.mode == GDN_DELTA) {
-                const size_t sq = vunits * s.dk * s.dk * sizeof(float);
-                const size_t tk = (size_t)s.B * s.T * s.H * s.dk * (s.io == GDN_BF16 ? 2 : 4);
-                L.ts_a_off = off;
-                off = round_up(off + sq, 256);
-                L.ts_i_off = off;
-                off = round_up(off + sq, 256);
-                L.ts_zv_off = off;
-                off = round_up(off + tk, 256);
-                L.ts_so_off = off;
-                off = round_up(off + tk, 256);
-            }
+            core.B = s.B * P;
+            core.T = s.T / P;
         }
+        off = place_bwd_core(core, L, off);
     }
+    if (P > 1) off = place_tsplit(s, P, backward != 0, L, off);
     L.total = off;
     return L;
 }
@@ -163,7 +193,7 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape, const void* v, const v
         }
         return GDN_OK;
     }
-    const int P = tsplit_factor(*shape);
+    const int P = tsplit_factor(*shape, 0);
     const cudaError_t e = P > 1 ? launch_fwd_tsplit(a, ws_layout(*shape, 0), P, st, fwd_core) : fwd_core(a, st);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -194,8 +224,9 @@ extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape, const void* v, const v
     a.v = v; a.b = b; a.c = c; a.g = g; a.beta = beta; a.A_log = A_log; a.h0 = h0;
     a.dO = dO; a.dhT = dhT; a.dv_ = dv; a.db = db; a.dc = dc; a.dg = dg; a.dbeta = dbeta;
     a.dA_log = dA_log; a.dh0 = dh0; a.ws = ws; a.ws_bytes = ws_bytes;
-    if (launch_serial_bwd(a, st) != cudaSuccess) return GDN_ERR_CUDA;
-    return GDN_OK;
+    const int P = a.T > 0 ? tsplit_factor(*shape, 1) : 1;
+    const cudaError_t e = P > 1 ? launch_bwd_tsplit(a, ws_layout(*shape, 1), P, st, fwd_core) : launch_serial_bwd(a, st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 extern "C" gdn_status_t gdn_last_device_status(const void* ws, gdn_stream_t stream)

@@ -41,6 +41,10 @@ struct WsLayout {
     size_t ts_i_off = 0;          // delta: identity starting states     [B*P, H, d_k, d_k]
     size_t ts_zv_off = 0;         // delta: zero values                  [B, T, H, d_k] (I/O dtype)
     size_t ts_so_off = 0;         // delta: outputs of the transition run [B, T, H, d_k] (I/O dtype)
+    // backward split in time
+    size_t ts_o_off = 0;          // forward outputs of the state runs   [B, T, H, d_v] (I/O dtype)
+    size_t ts_g_off = 0;          // segment adjoints from a zero end gradient [B*P, H, d_k, d_v]
+    size_t ts_e_off = 0;          // end gradients of the segments       [B*P, H, d_k, d_v]
     size_t total = 0;
 };
 
@@ -51,14 +55,17 @@ constexpr int kSerialSnap = 8;                 // tokens between backward state 
 constexpr size_t kStateSlot = 16 * 256 * 4;    // one state snapshot (256 threads x 16 floats)
 
 WsLayout ws_layout(const gdn_shape_t& s, int backward);
+WsLayout ws_layout_bwd_core(const gdn_shape_t& s);   // the serial backward's own buffers only
 
 // Launchers (enqueue on `st`, return cudaGetLastError()).
 cudaError_t launch_serial_fwd(const Args& a, cudaStream_t st);
 cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled);
 cudaError_t launch_decode(const Args& a, cudaStream_t st);   // 1 <= T <= decode_max_tokens()
-int tsplit_factor(const gdn_shape_t& s);       // segments P of a time-split forward, 1 = no split
+int tsplit_factor(const gdn_shape_t& s, int backward);   // segments P of a time split, 1 = no split
 cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
+                              cudaError_t (*fwd_core)(const Args&, cudaStream_t));
+cudaError_t launch_bwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
                               cudaError_t (*fwd_core)(const Args&, cudaStream_t));
 int decode_max_tokens();
 

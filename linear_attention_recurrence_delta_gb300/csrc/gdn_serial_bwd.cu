@@ -533,7 +533,7 @@ cudaError_t launch_t(const Args& a, const WsLayout& L, cudaStream_t st)
 cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st)
 {
     gdn_shape_t sh{a.B, a.H, a.T, a.dk, a.dv, a.mode, a.io};
-    const WsLayout L = ws_layout(sh, 1);
+    const WsLayout L = ws_layout_bwd_core(sh);
     cudaError_t e;
     if (a.io == GDN_BF16)
         e = a.mode == GDN_DELTA ? launch_t<__nv_bfloat16, true>(a, L, st) : launch_t<__nv_bfloat16, false>(a, L, st);

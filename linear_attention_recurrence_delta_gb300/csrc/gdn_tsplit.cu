@@ -16,6 +16,16 @@
 // A [B, T, H, d] tensor cut into P segments of T/P tokens is, byte for byte,
 // a [B*P, T/P, H, d] tensor, so steps 1, 2 and 4 are the ordinary forward on
 // that shape and no input moves.
+//
+// The backward splits the same way.  With the segments' entering states S_p
+// from steps 1-3, the adjoint dL/dS_p of a segment is G_p + A_p^T E_p, where
+// G_p is the segment's own backward started from a zero end gradient and E_p
+// the gradient at its end (dh_T for the last one, dL/dS_{p+1} otherwise):
+//   5. every segment's backward from S_p with a zero end gradient -> G_p
+//   6. a reverse scan  E_{p-1} = G_p + A_p^T E_p,  dh0 = G_0 + A_0^T E_0
+//   7. every segment's backward again from S_p with end gradient E_p
+// Step 7's gradients are the true ones; dA_log sums over all (batch,
+// segment) pairs, which the backward's own reduction over its batch does.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
@@ -92,12 +102,66 @@ __global__ void __launch_bounds__(256) scan_kernel(const float* Abuf, const floa
         for (int idx = tid; idx < dk * dv; idx += 256) hT[(size_t)u * dk * dv + idx] = S[idx / dv][idx % dv];
 }
 
+// Step 6 for one (batch, head): E_{P-1} = dh_T; E_{p-1} = G_p + A_p^T E_p;
+// stores every E_p (the end gradients of step 7) and dh0 = G_0 + A_0^T E_0.
+template <typename IO, bool DELTA>
+__global__ void __launch_bounds__(256) bscan_kernel(const float* Abuf, const float* Gbuf, const float* dhT,
+                                                    float* Ebuf, float* dh0, const IO* g, const float* A_log, int B,
+                                                    int H, int T, int P, int dk, int dv)
+{
+    __shared__ float E[64][65];
+    __shared__ float At[64][65];
+    __shared__ float dec[64];
+    const int u = blockIdx.x, bb = u / H, h = u % H, tid = threadIdx.x;
+    const int Ts = T / P;
+    for (int idx = tid; idx < dk * dv; idx += 256) E[idx / dv][idx % dv] = dhT ? dhT[(size_t)u * dk * dv + idx] : 0.f;
+    __syncthreads();
+    for (int p = P - 1; p >= 0; p--) {
+        const size_t vu = ((size_t)(bb * P + p) * H + h);
+        for (int idx = tid; idx < dk * dv; idx += 256) Ebuf[vu * dk * dv + idx] = E[idx / dv][idx % dv];
+        if (DELTA) {
+            for (int idx = tid; idx < dk * dk; idx += 256) At[idx / dk][idx % dk] = Abuf[vu * dk * dk + idx];
+        } else if (tid < dk) {
+            float gs = 0.f;
+            for (int t = 0; t < Ts; t++) gs += (float)g[((size_t)bb * T + (size_t)p * Ts + t) * H + h];
+            dec[tid] = expf(gs * -expf(A_log[h * dk + tid]));
+        }
+        __syncthreads();
+        float acc[16];
+#pragma unroll
+        for (int q = 0; q < 16; q++) {
+            const int idx = tid + 256 * q;
+            if (idx < dk * dv) {
+                const int i = idx / dv, j = idx % dv;
+                float v = Gbuf[vu * dk * dv + idx];
+                if (DELTA) {
+                    for (int k = 0; k < dk; k++) v = fmaf(At[k][i], E[k][j], v);
+                } else {
+                    v = fmaf(dec[i], E[i][j], v);
+                }
+                acc[q] = v;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 16; q++) {
+            const int idx = tid + 256 * q;
+            if (idx < dk * dv) E[idx / dv][idx % dv] = acc[q];
+        }
+        __syncthreads();
+    }
+    if (dh0)
+        for (int idx = tid; idx < dk * dv; idx += 256) dh0[(size_t)u * dk * dv + idx] = E[idx / dv][idx % dv];
+}
+
 }  // namespace
 
-int tsplit_factor(const gdn_shape_t& s)
+int tsplit_factor(const gdn_shape_t& s, int backward)
 {
     const long units = (long)s.B * s.H;
-    const int min_p = s.mode == GDN_DELTA ? 4 : 3;  // three (delta) or two (gated) passes must still pay
+    // forward: three passes (delta) or two (gated) must still pay; backward: two backward passes, the
+    // forward passes are cheap beside them
+    const int min_p = backward ? 3 : (s.mode == GDN_DELTA ? 4 : 3);
     const long cap = kSplitSMs / units;
     for (long p = cap; p >= min_p; p--) {
         if (s.T % p) continue;
@@ -107,8 +171,11 @@ int tsplit_factor(const gdn_shape_t& s)
     return 1;
 }
 
-cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
-                              cudaError_t (*fwd_core)(const Args&, cudaStream_t))
+// Steps 1-3: the entering state of every segment into L.ts_s_off and, if
+// hT is given, the leaving state of the whole sequence.  `a.o` receives the
+// outputs of step 1, which are not the final ones.
+static cudaError_t tsplit_states(const Args& a, const WsLayout& L, int P, cudaStream_t st,
+                                 cudaError_t (*fwd_core)(const Args&, cudaStream_t))
 {
     unsigned char* ws = (unsigned char*)a.ws;
     float* Hbuf = (float*)(ws + L.ts_h_off);
@@ -121,7 +188,7 @@ cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
     const size_t vunits = (size_t)a.B * P * a.H;
     cudaError_t e;
 
-    // 1. leaving states from a zero start (o is written here and overwritten in step 4)
+    // 1. leaving states from a zero start
     Args r = a;
     r.B = a.B * P;
     r.T = Ts;
@@ -163,13 +230,73 @@ cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
             scan_kernel<float, false><<<units, 256, 0, st>>>(Abuf, Hbuf, a.h0, Sst, a.hT, (const float*)a.g,
                                                              a.A_log, a.B, a.H, a.T, P, a.dk, a.dv);
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
+cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
+                              cudaError_t (*fwd_core)(const Args&, cudaStream_t))
+{
+    cudaError_t e = tsplit_states(a, L, P, st, fwd_core);
+    if (e != cudaSuccess) return e;
     // 4. every segment again from its true entering state: the outputs
-    Args f = r;
-    f.h0 = Sst;
+    Args f = a;
+    f.B = a.B * P;
+    f.T = a.T / P;
+    f.h0 = (const float*)((unsigned char*)a.ws + L.ts_s_off);
     f.hT = nullptr;
     return fwd_core(f, st);
+}
+
+cudaError_t launch_bwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
+                              cudaError_t (*fwd_core)(const Args&, cudaStream_t))
+{
+    unsigned char* ws = (unsigned char*)a.ws;
+    const float* Sst = (const float*)(ws + L.ts_s_off);
+    float* Gbuf = (float*)(ws + L.ts_g_off);
+    float* Ebuf = (float*)(ws + L.ts_e_off);
+    cudaError_t e;
+
+    // 1-3. entering states of the segments (outputs of step 1 go to scratch)
+    Args fa = a;
+    fa.o = ws + L.ts_o_off;
+    fa.hT = nullptr;
+    if ((e = tsplit_states(fa, L, P, st, fwd_core)) != cudaSuccess) return e;
+
+    // 5. every segment's backward from a zero end gradient: G_p in Gbuf
+    Args b = a;
+    b.B = a.B * P;
+    b.T = a.T / P;
+    b.h0 = Sst;
+    b.dhT = nullptr;
+    b.dh0 = Gbuf;
+    if ((e = launch_serial_bwd(b, st)) != cudaSuccess) return e;
+
+    // 6. reverse scan of the end gradients; dh0 of the whole sequence
+    const int units = a.B * a.H;
+    const float* Abuf = (const float*)(ws + L.ts_a_off);
+    if (a.io == GDN_BF16) {
+        if (a.mode == GDN_DELTA)
+            bscan_kernel<__nv_bfloat16, true><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0,
+                                                                      (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H,
+                                                                      a.T, P, a.dk, a.dv);
+        else
+            bscan_kernel<__nv_bfloat16, false><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0,
+                                                                       (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H,
+                                                                       a.T, P, a.dk, a.dv);
+    } else {
+        if (a.mode == GDN_DELTA)
+            bscan_kernel<float, true><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0, (const float*)a.g,
+                                                             a.A_log, a.B, a.H, a.T, P, a.dk, a.dv);
+        else
+            bscan_kernel<float, false><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0, (const float*)a.g,
+                                                              a.A_log, a.B, a.H, a.T, P, a.dk, a.dv);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    // 7. every segment's backward again with its true end gradient
+    b.dhT = Ebuf;
+    b.dh0 = nullptr;
+    return launch_serial_bwd(b, st);
 }
 
 }  // namespace gdn
