@@ -68,6 +68,33 @@ def io_bytes(w, backward=False):
     return rd + wr + 2 * state + 2 * w.H * w.dk * 4
 
 
+def tsplit_factor(w, backward):
+    """Segments of the library's time split for workload w (1 = none); mirrors the rule in
+    csrc/gdn_tsplit.cu: B*H*P <= 152 SMs, T divisible by P, >= 512 tokens per segment, P >= 4 for a delta
+    forward and >= 3 otherwise."""
+    units = w.B * w.H
+    min_p = 3 if backward else (4 if w.mode == "delta" else 3)
+    for p in range(152 // units, min_p - 1, -1):
+        if w.T % p == 0 and w.T // p >= 512:
+            return p
+    return 1
+
+
+def fwd_launches(w):
+    """Kernels one gdn_fwd call launches."""
+    if tsplit_factor(w, False) == 1:
+        return 1
+    return 5 if w.mode == "delta" else 3   # state run, (identity, transition run), scan, output run
+
+
+def bwd_launches(w):
+    """Kernels one gdn_bwd call launches."""
+    if tsplit_factor(w, True) == 1:
+        return 2                            # backward + dA_log reduction
+    states = 4 if w.mode == "delta" else 2
+    return states + 2 + 1 + 2               # state passes, backward x2 (+ reductions), reverse scan
+
+
 def fwd_kernel_name(w):
     """The kernel gdn_fwd launches for workload w (one launch per call)."""
     if w.T <= 8:
@@ -302,29 +329,75 @@ def main():
                 "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
                 "kernel": fwd_kernel_name(w), "bytes_per_launch": fwd_bytes, "launch_ms": launch_ms}
     # launches of our kernels per forward step: the forward kernel itself
-    gpu_launches = 1 * args.steps
+    gpu_launches = fwd_launches(w) * args.steps
 
-    # end to end through the C ABI with host buffers
-    hx = {k: (None if v is None else v.cpu().pin_memory()) for k, v in t.items() if k != "dO"}
+    # End to end through the C ABI with host buffers.  Every step copies its inputs from pinned host memory,
+    # runs gdn_fwd and reads its outputs back; as a serving loop would, step k+1's input copies overlap
+    # step k's forward and step k-1's output copies (three streams, two device buffer sets).
+    in_keys = [k for k in ("v", "b", "c", "g", "beta") if t[k] is not None]
+    hx = {k: t[k].cpu().pin_memory() for k in in_keys}
     hA = A_log.cpu().pin_memory()
-    ho = torch.empty(o.shape, dtype=dt).pin_memory()
-    hhT = torch.empty(hT.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in hx.values() if v is not None) + hA.numel() * 4
-    d2h = ho.numel() * ho.element_size() + hhT.numel() * 4
+    hh0 = h0.cpu().pin_memory() if h0 is not None else None
+    dbuf = [{k: torch.empty_like(t[k]) for k in in_keys} for _ in range(2)]
+    dA = [torch.empty_like(A_log) for _ in range(2)]
+    dh0 = [torch.empty_like(h0) if h0 is not None else None for _ in range(2)]
+    dout = [(torch.empty_like(o), torch.empty_like(hT)) for _ in range(2)]
+    hout = [(torch.empty(o.shape, dtype=dt).pin_memory(), torch.empty(hT.shape, dtype=torch.float32).pin_memory())
+            for _ in range(2)]
+    h2d = sum(v.numel() * v.element_size() for v in hx.values()) + hA.numel() * 4 + \
+        (hh0.numel() * 4 if hh0 is not None else 0)
+    d2h = o.numel() * o.element_size() + hT.numel() * 4
+    s_in, s_fw, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_fw = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    ws_e2e = torch.empty(gdn.gdn_workspace_bytes(s, 0), dtype=torch.uint8, device="cuda")
 
-    def e2e_step():
-        for k, v in hx.items():
-            if v is not None:
-                t[k].copy_(v, non_blocking=True)
-        A_log.copy_(hA, non_blocking=True)
-        fwd()
-        ho.copy_(o, non_blocking=True)
-        hhT.copy_(hT, non_blocking=True)
+    def e2e_run(K):
+        for e in ev_fw + ev_out:
+            e.record(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(s_in)
+        for k in range(K):
+            j = k % 2
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_fw[j])            # the forward that last read this buffer set is done
+                for key in in_keys:
+                    dbuf[j][key].copy_(hx[key], non_blocking=True)
+                dA[j].copy_(hA, non_blocking=True)
+                if hh0 is not None:
+                    dh0[j].copy_(hh0, non_blocking=True)
+                ev_in[j].record(s_in)
+            s_fw.wait_event(ev_in[j])
+            s_fw.wait_event(ev_out[j])               # its outputs were read back
+            d = dbuf[j]
+            gdn.check(gdn.gdn_fwd(s, d["v"], d["b"], d["c"], d["g"], d.get("beta"), dA[j], dh0[j], dout[j][0],
+                                  dout[j][1], ws_e2e, stream=s_fw), "gdn_fwd")
+            ev_fw[j].record(s_fw)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_fw[j])
+                hout[j][0].copy_(dout[j][0], non_blocking=True)
+                hout[j][1].copy_(dout[j][1], non_blocking=True)
+                ev_out[j].record(s_out)
+        s_out.wait_event(ev_out[(K - 1) % 2])
+        end.record(s_out)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
 
-    e2e_total, _ = timed(e2e_step, max(3, args.steps // 2), 3)
-    e2e_ms = e2e_total / max(3, args.steps // 2)
+    Ke = max(6, args.steps)
+    e2e_run(3)
+    barrier()
+    e2e_total = max_over_ranks(e2e_run(Ke))
+    barrier()
+    e2e_ms = e2e_total / Ke
+    got = hout[(Ke - 1) % 2][0].to(torch.float32)
+    ref = o.to(torch.float32).cpu()
+    assert torch.equal(got, ref), "end-to-end outputs differ from the device-resident run"
     e2e = {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "overlap": "step k+1 inputs in, step k forward, step k-1 outputs out on three streams"}
+    gpu_launches += fwd_launches(w) * Ke
 
     fwdbwd = None
     if not args.no_bwd:
@@ -336,7 +409,7 @@ def main():
         fb_ms = fb_total / kb
         fwdbwd = {"value": world * tokens / (fb_ms * 1e-3), "unit": "tokens/s", "ms_per_step": fb_ms,
                   "bwd_bytes": io_bytes(w, backward=True)}
-        gpu_launches += 3 * kb   # fwd kernel + backward kernel + dA_log reduction
+        gpu_launches += (fwd_launches(w) + bwd_launches(w)) * kb
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
