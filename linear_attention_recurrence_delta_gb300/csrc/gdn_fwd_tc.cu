@@ -417,11 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // (3) level MMAs
             if (r == 0) {
                 const uint32_t x0 = smem_u32(X);
-                const uint32_t b1[3] = {x0 + X_B1a, x0 + X_B1b, x0 + X_B1c};
-                const uint32_t d1[3] = {TM_D1a, TM_D1b, TM_D1c};
-#pragma unroll
-                for (int I = 1; I <= 3; I++)
-                    mma_k64(tbase + d1[I - 1], x0 + X_A1, b1[I - 1], false, idesc_f16(128, 16 * I, false, false), false);
+                // L1 for all three row blocks in one N = 96 product: the column operands B1a | B1b | B1c
+                // (16, 32, 48 rows) are contiguous, and so are their accumulators D1a | D1b | D1c
+                static_assert(X_B1b == X_B1a + 16 * 128 && X_B1c == X_B1b + 32 * 128, "L1 column operands");
+                static_assert(TM_D1b == TM_D1a + 16 && TM_D1c == TM_D1b + 32, "L1 accumulators");
+                mma_k64(tbase + TM_D1a, x0 + X_A1, x0 + X_B1a, false, idesc_f16(128, 96, false, false), false);
                 mma_k64(tbase + TM_D2, x0 + X_A2, x0 + X_B2, false, idesc_f16(128, 64, false, false), false);
                 const uint32_t id3 = idesc_bf16(128, 64, false, false);
                 mma_k64(tbase + TM_D3, x0 + X_A3, x0 + X_B3, false, id3, false);
