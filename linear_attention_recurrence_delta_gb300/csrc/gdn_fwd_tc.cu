@@ -19,8 +19,9 @@
 // around a reference point r between s and t, so no factor overflows (|A| up
 // to 16 over a chunk reaches exp(+-1024)); secondary chunking after Yang et al.
 // 2023 (Gated Linear Attention):
-//   L1  different 16-blocks: r = last token before the row block, one MMA per
-//       row block (N = 16, 32, 48); factors <= 1;
+//   L1  different 16-blocks: r = last token before the row block; the three
+//       row blocks' column operands (16, 32, 48 rows) form one N = 96 MMA;
+//       factors <= 1;
 //   L2  same 16-block, row in the upper and column in the lower 8-half:
 //       r = last token of the lower half; factors <= 1;
 //   L3  same 8-block: r = the block's 4th token; factors up to
