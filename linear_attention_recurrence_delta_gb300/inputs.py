@@ -152,6 +152,11 @@ WORKLOADS = {
         "delta_bf16_1x16x32768x64_slowdecay", "delta", "bf16", 1, 16, 32768, 64, 64, seed=6,
         backward=True, b_dist="l2norm", c_dist="l2norm", g_mu=-4.0,
         notes="added slow-decay stress input"),
+    # added: the production-scale head shape of "HyMo-434M -- documentation portal", Worked example
+    # (40 heads, d_state = headdim = 32) at the 8 x 4096 batch of the delta workload
+    "delta_bf16_8x40x4096x32": Workload(
+        "delta_bf16_8x40x4096x32", "delta", "bf16", 8, 40, 4096, 32, 32, seed=8,
+        b_dist="l2norm", c_dist="l2norm", notes="added 40-head d = 32 shape"),
     # added: one decoding step (T = 1) of a large batch, state in and out
     "delta_bf16_decode_512x16x1x64": Workload(
         "delta_bf16_decode_512x16x1x64", "delta", "bf16", 512, 16, 1, 64, 64, seed=7,

@@ -165,3 +165,12 @@ def test_workload_delta_bf16_1x16x32768x64_fwd_bwd():
     w = I.WORKLOADS["delta_bf16_1x16x32768x64_bwd"]
     check_fwd(w)
     check_bwd(w)
+
+
+def test_shape_40_heads_d32_fwd_bwd():
+    """The production head shape (40 heads, d_k = d_v = 32) at two batch rows of 4096 tokens: forward, and the
+    backward on three heads."""
+    base = I.WORKLOADS["delta_bf16_8x40x4096x32"]
+    w = base.with_(name="delta_bf16_2x40x4096x32", B=2, backward=True)
+    check_fwd(w)
+    check_bwd(w, units=[0, 17, 39])
