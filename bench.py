@@ -241,7 +241,7 @@ def main():
     import torch
 
     import linear_attention_recurrence_delta_gb300 as gdn
-    from linear_attention_recurrence_delta_gb300 import _build
+    from linear_attention_recurrence_delta_gb300 import _build, replicas
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -255,7 +255,7 @@ def main():
     gdn.load()
 
     base = I.WORKLOADS[args.workload]
-    w = base.with_(seed=base.seed + 1000 * rank) if world > 1 else base
+    w = replicas.rank_workload(base, rank, world)
     wb = w.with_(backward=True)
     x = I.make_inputs(wb)
     s = gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.mode, w.dtype)
@@ -291,11 +291,7 @@ def main():
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if dist is None:
-            return v
-        tt = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        return float(tt.item())
+        return replicas.max_over_ranks(v, dist, device="cuda")
 
     def timed(step_fn, K, W):
         for _ in range(W):
@@ -319,7 +315,7 @@ def main():
         total_ms, launch_ms = timed(fwd, args.steps, args.warmup)
     clocks = clk.summary()
     ms_per_step = total_ms / args.steps
-    value = world * tokens / (ms_per_step * 1e-3)
+    value = replicas.whole_job_tokens_per_s(tokens, world, ms_per_step)
     gdn.check(gdn.gdn_last_device_status(ws), "device status")
 
     peaks, peak_kind = load_peaks()
@@ -394,7 +390,7 @@ def main():
     got = hout[(Ke - 1) % 2][0].to(torch.float32)
     ref = o.to(torch.float32).cpu()
     assert torch.equal(got, ref), "end-to-end outputs differ from the device-resident run"
-    e2e = {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    e2e = {"value": replicas.whole_job_tokens_per_s(tokens, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "overlap": "step k+1 inputs in, step k forward, step k-1 outputs out on three streams"}
     gpu_launches += fwd_launches(w) * Ke
@@ -407,7 +403,7 @@ def main():
         kb = max(3, args.steps // 4)
         fb_total, fb_launch = timed(fb, kb, 3)
         fb_ms = fb_total / kb
-        fwdbwd = {"value": world * tokens / (fb_ms * 1e-3), "unit": "tokens/s", "ms_per_step": fb_ms,
+        fwdbwd = {"value": replicas.whole_job_tokens_per_s(tokens, world, fb_ms), "unit": "tokens/s", "ms_per_step": fb_ms,
                   "bwd_bytes": io_bytes(w, backward=True)}
         gpu_launches += (fwd_launches(w) + bwd_launches(w)) * kb
 
