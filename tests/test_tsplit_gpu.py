@@ -69,3 +69,22 @@ def test_tsplit_backward_parity(mode, io, B, H, T, d):
             assert got[k] is None
             continue
         assert_close(got[k], ref[k], TOL[io], f"{w.name} {k}")
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+def test_tsplit_ragged_segments(mode):
+    """T = 3000 over 4 heads splits into 5 segments of 600 tokens: every segment ends inside a chunk."""
+    from tests.gdn_testlib import run_bwd
+    w = I.custom(name=f"tsr_{mode}", mode=mode, dtype="bf16", B=1, H=4, T=3000, dk=64, dv=64, seed=21,
+                 h0_std=0.3, b_dist="l2norm" if mode == "delta" else "normal/8", c_dist="l2norm", g_mu=-1.5,
+                 backward=True)
+    x = I.make_inputs(w)
+    o, hT = run_fwd(w, x)
+    ro, rhT = oracle_fwd(w, x)
+    assert_close(o, ro, TOL["bf16"], "o")
+    assert_close(hT, rhT, TOL["bf16"], "hT")
+    got = run_bwd(w, x)
+    ref = oracle.gdn_bwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], x["dO"], None, mode=w.mode)
+    for k in ("dv", "db", "dc", "dg", "dbeta", "dA_log", "dh0"):
+        if ref[k] is not None:
+            assert_close(got[k], ref[k], TOL["bf16"], k)
