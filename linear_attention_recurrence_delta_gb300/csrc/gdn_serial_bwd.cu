@@ -40,7 +40,8 @@ constexpr int kNQ = 2;             // row quantities summed over columns: dc, db
 template <typename IO>
 struct BwdSmem {
     float A[kBT][64], Bv[kBT][64], Cv[kBT][64];                 // alpha_t, b_t, c_t
-    float V[kBT][64], DO[kBT][64], X[kBT][64], VR[kBT][64];     // v_t, do_t, x, v_t - h'^T b_t
+    float V[kBT][64], DO[kBT][64];                               // v_t, do_t
+    float XV[2][2][kBT][64];      // two buffers of [x ; v_t - h'^T b_t] (the next block's arrives early)
     float beta[kBT], g[kBT];
     float Arow[64], Arow2[64];  // A and A log2(e)
     float2 snap[kBT / kSub][8][256];                             // per-thread state snapshots
@@ -109,13 +110,14 @@ __device__ __forceinline__ void issue_block(const Args& a, BwdSmem<IO>& s, const
 // steps (alpha = 1, every other input 0), so a block is always 32 tokens.
 template <typename IO, bool DELTA>
 __device__ __forceinline__ void finish_block(const Args& a, BwdSmem<IO>& s, const Ctx& C, int t0, bool grad,
-                                             float greg, float breg)
+                                             float greg, float breg, bool leave_newest = false)
 {
     const int tid = C.tid, dk = a.dk, dv = a.dv;
     const int nt = min(kBT, a.T - t0);
     if (tid < 32) s.rg[tid] = greg;
     else if (tid < 64) s.rbeta[tid - 32] = breg;
-    cp_async_wait_all();
+    if (leave_newest) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+    else cp_async_wait_all();
     __syncthreads();
     for (int idx = tid; idx < kBT * 64; idx += 256) {
         const int tt = idx >> 6, i = idx & 63;
@@ -308,24 +310,35 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
     const int ri = tid & 63, rk = tid >> 6;  // reduction-phase role: row ri, window token rk
     int wbuf = 0;
 
+    // Snapshots and x cache of block n come back from the workspace: the x cache one block ahead into the other
+    // buffer, snapshot sb of block n-1 as soon as block n's windows are done with slot sb.
+    auto fetch_snap = [&](int n, int sb) {
+        const float4* src = reinterpret_cast<const float4*>(gsnap + ((size_t)n * kSnapPerBlk + sb) * 2048);
+        float4* dst = reinterpret_cast<float4*>(&s.snap[sb][0][0]);
+        for (int idx = tid; idx < 2048 / 2; idx += 256) cp_async16(dst + idx, src + idx);
+    };
+    auto fetch_xv = [&](int n) {
+        if (!DELTA) return;
+        const float4* sx = reinterpret_cast<const float4*>(gxvr + (size_t)n * kBT * 128);
+        float4* dx = reinterpret_cast<float4*>(&s.XV[n & 1][0][0][0]);
+        for (int idx = tid; idx < kBT * 128 / 4; idx += 256) cp_async16(dx + idx, sx + idx);
+    };
+    for (int sb = 0; sb < kSnapPerBlk; sb++) fetch_snap(nblk - 1, sb);
+    fetch_xv(nblk - 1);
+    cp_async_commit();
+
     // ---------------- reverse walk over blocks ----------------
     for (int n = nblk - 1; n >= 0; n--) {
         const int t0 = n * kBT;
-        // this block's snapshots (and x, v - h'^T b) from the forward sweep
-        {
-            const float4* src = reinterpret_cast<const float4*>(gsnap + (size_t)n * kSnapPerBlk * 2048);
-            float4* dst = reinterpret_cast<float4*>(&s.snap[0][0][0]);
-            for (int idx = tid; idx < kSnapPerBlk * 2048 / 2; idx += 256) cp_async16(dst + idx, src + idx);
-            if (DELTA) {
-                const float4* sx = reinterpret_cast<const float4*>(gxvr + (size_t)n * kBT * 128);
-                float4* dx = reinterpret_cast<float4*>(&s.X[0][0]);
-                for (int idx = tid; idx < kBT * 128 / 4; idx += 256) cp_async16(dx + idx, sx + idx);
-            }
+        // waits for this block's inputs, x cache and snapshots but the last (slot 0, needed from window 1 on)
+        finish_block<IO, DELTA>(a, s, C, t0, true, greg, breg, n < nblk - 1);
+        if (n > 0) {
+            issue_block<IO, DELTA>(a, s, C, t0 - kBT, true, vec, greg, breg);
+            fetch_xv(n - 1);
             cp_async_commit();
         }
-        finish_block<IO, DELTA>(a, s, C, t0, true, greg, breg);
-        if (n > 0) issue_block<IO, DELTA>(a, s, C, t0 - kBT, true, vec, greg, breg);
-        const float* Xsrc = DELTA ? &s.X[0][0] : &s.V[0][0];
+        const float* Xsrc = DELTA ? &s.XV[n & 1][0][0][0] : &s.V[0][0];
+        const float* VRsrc = &s.XV[n & 1][1][0][0];
 
 #pragma unroll 1
         for (int wi = kBT / kWin - 1; wi >= 0; wi--) {
@@ -395,7 +408,7 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
                 float2 gq = f2(0.f, 0.f);
                 if (DELTA) {
                     const float be = s.beta[tt];
-                    const float2 vr2 = ld2(&s.VR[tt][C.j0]);
+                    const float2 vr2 = ld2(VRsrc + tt * 64 + C.j0);
                     const float dr0 = -be * du0, dr1 = -be * du1;
                     dv0 = be * du0;
                     dv1 = be * du1;
@@ -442,7 +455,12 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
                 }
                 if (C.ig == 0) *reinterpret_cast<float2*>(&s.dvb[wbuf][k][C.j0]) = f2(dv0, dv1);
             }
+            if (wi == 2 && n < nblk - 1) cp_async_wait_all();   // snapshot slot 0, read from window 1 on
             __syncthreads();
+            if (n > 0 && (tw & (kSub - 1)) == 0) {   // slot tw / kSub is done for this block
+                fetch_snap(n - 1, tw / kSub);
+                cp_async_commit();
+            }
 
             // ---- reduction phase: thread (row ri, token rk) of this window ----
             {
