@@ -64,6 +64,17 @@ typedef enum {
     GDN_DELTA = 1    /* decay, then erase-and-write with key b_t     */
 } gdn_mode_t;
 
+/* Option bits OR'ed into gdn_shape_t.mode. */
+enum {
+    /* g (and, in delta mode, beta) arrive as logits, before their sigmoid
+     * ("GDN & MLA Mechanism Deep-Dive", Gated delta rule: g_t is the sigmoid
+     * of a projection; beta follows the same convention here).  The kernels
+     * apply sigmoid() as they load them, and gdn_bwd returns dg and dbeta
+     * with respect to the logits.  Without the bit both arrive already in
+     * [0, 1] and the gradients are with respect to those values. */
+    GDN_GATE_LOGITS = 0x100
+};
+
 typedef enum {
     GDN_F32 = 0,     /* float32 I/O (computed in fp32 on CUDA cores) */
     GDN_BF16 = 1     /* bfloat16 I/O, fp32 accumulation              */

@@ -31,7 +31,12 @@ struct TcParams {
     float* hT;
     uint32_t* status;
     int B, H, T, dk, dv, nchunks;
+    int logits;   // g, beta arrive before their sigmoid
 };
+
+// g or beta as the rule uses it: the logistic function of a logit (SFU exponential;
+// this path takes bf16 inputs), or the value itself
+__device__ __forceinline__ float gate_in(float x, int logits) { return logits ? 1.f / (1.f + __expf(-x)) : x; }
 
 __device__ __forceinline__ float bf2f(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
 

@@ -135,6 +135,16 @@ static gdn_status_t check_common(const gdn_shape_t* s, const void* v, const void
     return GDN_OK;
 }
 
+// Split the option bits off the mode: `out` gets the plain mode, `logits` the
+// GDN_GATE_LOGITS bit.  False if the mode carries an unknown bit.
+static bool split_mode(const gdn_shape_t* in, gdn_shape_t* out, int* logits)
+{
+    *out = *in;
+    *logits = (in->mode & GDN_GATE_LOGITS) != 0;
+    out->mode = in->mode & ~GDN_GATE_LOGITS;
+    return (out->mode & ~0xff) == 0;
+}
+
 static Args make_args(const gdn_shape_t* s)
 {
     Args a;
@@ -160,18 +170,27 @@ static cudaError_t fwd_core(const Args& a, cudaStream_t st)
 
 using namespace gdn;
 
-extern "C" size_t gdn_workspace_bytes(const gdn_shape_t* shape, int backward)
+extern "C" size_t gdn_workspace_bytes(const gdn_shape_t* shape_in, int backward)
 {
-    if (!shape || !shape_ok(*shape)) return 0;
+    gdn_shape_t sh;
+    int logits = 0;
+    if (!shape_in || !split_mode(shape_in, &sh, &logits)) return 0;
+    const gdn_shape_t* shape = &sh;
+    if (!shape_ok(*shape)) return 0;
     if ((shape->mode != GDN_GATED && shape->mode != GDN_DELTA) || (shape->io != GDN_F32 && shape->io != GDN_BF16))
         return 0;
     return ws_layout(*shape, backward ? 1 : 0).total;
 }
 
-extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape, const void* v, const void* b, const void* c,
+extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, const void* b, const void* c,
                                 const void* g, const void* beta, const float* A_log, const float* h0,
                                 void* o, float* hT, void* ws, size_t ws_bytes, gdn_stream_t stream)
 {
+    gdn_shape_t sh;
+    int logits = 0;
+    if (!shape_in) return GDN_ERR_NULL;
+    if (!split_mode(shape_in, &sh, &logits)) return GDN_ERR_MODE;
+    const gdn_shape_t* shape = &sh;
     gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 0);
     if (r != GDN_OK) return r;
     if (!o && shape->T > 0) return GDN_ERR_NULL;
@@ -183,7 +202,7 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape, const void* v, const v
     if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return GDN_ERR_CUDA;
     Args a = make_args(shape);
     a.v = v; a.b = b; a.c = c; a.g = g; a.beta = beta; a.A_log = A_log; a.h0 = h0; a.o = o; a.hT = hT;
-    a.ws = ws; a.ws_bytes = ws_bytes;
+    a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits;
     const size_t state_bytes = (size_t)a.B * a.H * a.dk * a.dv * sizeof(float);
     if (a.T == 0) {
         if (hT && hT != h0) {
@@ -198,12 +217,17 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape, const void* v, const v
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape, const void* v, const void* b, const void* c,
+extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape_in, const void* v, const void* b, const void* c,
                                 const void* g, const void* beta, const float* A_log, const float* h0,
                                 const void* dO, const float* dhT, void* dv, void* db, void* dc, void* dg,
                                 void* dbeta, float* dA_log, float* dh0, void* ws, size_t ws_bytes,
                                 gdn_stream_t stream)
 {
+    gdn_shape_t sh;
+    int logits = 0;
+    if (!shape_in) return GDN_ERR_NULL;
+    if (!split_mode(shape_in, &sh, &logits)) return GDN_ERR_MODE;
+    const gdn_shape_t* shape = &sh;
     gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 1);
     if (r != GDN_OK) return r;
     const bool tok = shape->T > 0;
@@ -223,7 +247,7 @@ extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape, const void* v, const v
     Args a = make_args(shape);
     a.v = v; a.b = b; a.c = c; a.g = g; a.beta = beta; a.A_log = A_log; a.h0 = h0;
     a.dO = dO; a.dhT = dhT; a.dv_ = dv; a.db = db; a.dc = dc; a.dg = dg; a.dbeta = dbeta;
-    a.dA_log = dA_log; a.dh0 = dh0; a.ws = ws; a.ws_bytes = ws_bytes;
+    a.dA_log = dA_log; a.dh0 = dh0; a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits;
     const int P = a.T > 0 ? tsplit_factor(*shape, 1) : 1;
     const cudaError_t e = P > 1 ? launch_bwd_tsplit(a, ws_layout(*shape, 1), P, st, fwd_core) : launch_serial_bwd(a, st);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

@@ -42,7 +42,7 @@ __device__ __forceinline__ void load_tokens(const Args& a, int u, TokRegs& r)
         r.g[q] = r.b[q] = r.c[q] = r.v[q] = 0.f;
         if (tt < T) {
             const size_t row = ((size_t)bb * T + tt) * H + h;
-            r.g[q] = to_f(((const IO*)a.g)[row]);
+            r.g[q] = gate(to_f(((const IO*)a.g)[row]), a.logits);
             if (i < dk) {
                 r.b[q] = to_f(((const IO*)a.b)[row * dk + i]);
                 r.c[q] = to_f(((const IO*)a.c)[row * dk + i]);
@@ -50,7 +50,7 @@ __device__ __forceinline__ void load_tokens(const Args& a, int u, TokRegs& r)
             if (i < dv) r.v[q] = to_f(((const IO*)a.v)[row * dv + i]);
         }
     }
-    r.beta = (DELTA && tid < T) ? to_f(((const IO*)a.beta)[((size_t)bb * T + tid) * H + h]) : 0.f;
+    r.beta = (DELTA && tid < T) ? gate(to_f(((const IO*)a.beta)[((size_t)bb * T + tid) * H + h]), a.logits) : 0.f;
 }
 
 // the unit's fp32 state (d_k x d_v, contiguous) into a shared buffer by cp.async

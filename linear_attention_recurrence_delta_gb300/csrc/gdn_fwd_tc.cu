@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (tid < kC) {
             const int t = k * kC + tid;
             const size_t row = ((size_t)bb * T + t) * H + h;
-            S.g[k][tid] = t < T ? __bfloat162float(p.g[row]) : 0.f;
-            if (DELTA) S.beta[k][tid] = t < T ? __bfloat162float(p.beta[row]) : 0.f;
+            S.g[k][tid] = t < T ? gate_in(__bfloat162float(p.g[row]), p.logits) : 0.f;
+            if (DELTA) S.beta[k][tid] = t < T ? gate_in(__bfloat162float(p.beta[row]), p.logits) : 0.f;
         }
     tc_fence_before();
     __syncthreads();
@@ -829,8 +829,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // stage s is free again (every read of it, and the last MMA, are done)
             if (k + kStages < p.nchunks) {
                 if (r < kC) {
-                    S.g[s][r] = g_next;
-                    if (DELTA) S.beta[s][r] = beta_next;
+                    // (the sigmoid of a logit is taken here, where the loaded value is first used,
+                    // so the load's latency stays hidden behind the chunk)
+                    // tokens past T keep g = beta = 0 (an identity step)
+                    const bool tok = (k + kStages) * kC + r < T;
+                    S.g[s][r] = tok ? gate_in(g_next, p.logits) : 0.f;
+                    if (DELTA) S.beta[s][r] = tok ? gate_in(beta_next, p.logits) : 0.f;
                 }
                 if (r == 0) issue_load(k + kStages), issued = k + kStages + 1;
             }
@@ -885,6 +889,7 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     p.hT = a.hT;
     p.status = (uint32_t*)a.ws;
     p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv = a.dv;
+    p.logits = a.logits;
     p.nchunks = (a.T + kC - 1) / kC;
     *handled = true;
     return a.mode == GDN_DELTA ? launch_t<true>(p, a.B * a.H, st) : launch_t<false>(p, a.B * a.H, st);

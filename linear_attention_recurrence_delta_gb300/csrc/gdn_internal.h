@@ -12,6 +12,7 @@ namespace gdn {
 // Everything one gdn_fwd / gdn_bwd call needs, already validated.
 struct Args {
     int B, H, T, dk, dv, mode, io;
+    int logits;            // g, beta arrive before their sigmoid (GDN_GATE_LOGITS)
     const void *v, *b, *c, *g, *beta;
     const float* A_log;
     const float* h0;

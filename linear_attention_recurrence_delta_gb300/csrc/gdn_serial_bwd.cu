@@ -101,9 +101,9 @@ __device__ __forceinline__ void issue_block(const Args& a, BwdSmem<IO>& s, const
             }
         }
     }
-    if (tid < nt) greg = to_f(((const IO*)a.g)[((size_t)C.bb * T + t0 + tid) * H + C.h]);
+    if (tid < nt) greg = gate(to_f(((const IO*)a.g)[((size_t)C.bb * T + t0 + tid) * H + C.h]), a.logits);
     if (DELTA && tid >= 32 && tid - 32 < nt)
-        breg = to_f(((const IO*)a.beta)[((size_t)C.bb * T + t0 + tid - 32) * H + C.h]);
+        breg = gate(to_f(((const IO*)a.beta)[((size_t)C.bb * T + t0 + tid - 32) * H + C.h]), a.logits);
 }
 
 // Make the block issued last the current one.  Tokens past T become identity
@@ -485,6 +485,11 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
                     for (int ww = 0; ww < 8; ww++) {
                         sg += s.gpart[wbuf][ww][tid];
                         sb += s.bpart[wbuf][ww][tid];
+                    }
+                    if (a.logits) {   // through the sigmoid: d sigma(z) / dz = sigma (1 - sigma)
+                        const float gv = s.g[tw + ri], bv = s.beta[tw + ri];
+                        sg *= gv * (1.f - gv);
+                        sb *= bv * (1.f - bv);
                     }
                     ((IO*)a.dg)[rowk] = from_f<IO>(sg);
                     if (DELTA) ((IO*)a.dbeta)[rowk] = from_f<IO>(sb);

@@ -74,9 +74,9 @@ __device__ __forceinline__ void issue_block(const Args& a, FwdSmem<IO>& s, const
             if (i < U.ncols) s.rv[tt][i] = v[row * dv + U.jc0 + i];
         }
     }
-    if (tid < nt) greg = to_f(((const IO*)a.g)[((size_t)U.bb * T + t0 + tid) * H + U.h]);
+    if (tid < nt) greg = gate(to_f(((const IO*)a.g)[((size_t)U.bb * T + t0 + tid) * H + U.h]), a.logits);
     if (DELTA && tid >= 32 && tid - 32 < nt)
-        breg = to_f(((const IO*)a.beta)[((size_t)U.bb * T + t0 + tid - 32) * H + U.h]);
+        breg = gate(to_f(((const IO*)a.beta)[((size_t)U.bb * T + t0 + tid - 32) * H + U.h]), a.logits);
 }
 
 // raw block -> fp32 staged arrays (alpha computed here, once per row and token)

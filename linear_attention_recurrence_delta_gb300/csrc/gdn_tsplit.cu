@@ -48,7 +48,7 @@ __global__ void eye_kernel(float* I, size_t n_units, int dk)
 template <typename IO, bool DELTA>
 __global__ void __launch_bounds__(256) scan_kernel(const float* Abuf, const float* Hbuf, const float* h0, float* Sst,
                                                    float* hT, const IO* g, const float* A_log, int B, int H, int T,
-                                                   int P, int dk, int dv)
+                                                   int P, int dk, int dv, int logits)
 {
     __shared__ float S[64][65];
     __shared__ float At[64][65];
@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(256) scan_kernel(const float* Abuf, const floa
             // decay of the whole segment: exp(A_i sum_t g_t)
             float gs = 0.f;
             for (int t = 0; t < Ts; t++) {
-                const IO gv = g[((size_t)bb * T + (size_t)p * Ts + t) * H + h];
-                gs += (float)gv;
+                const float gv = (float)g[((size_t)bb * T + (size_t)p * Ts + t) * H + h];
+                gs += logits ? 1.f / (1.f + expf(-gv)) : gv;
             }
             dec[tid] = expf(gs * -expf(A_log[h * dk + tid]));
         }
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const float* Abuf, const floa
 template <typename IO, bool DELTA>
 __global__ void __launch_bounds__(256) bscan_kernel(const float* Abuf, const float* Gbuf, const float* dhT,
                                                     float* Ebuf, float* dh0, const IO* g, const float* A_log, int B,
-                                                    int H, int T, int P, int dk, int dv)
+                                                    int H, int T, int P, int dk, int dv, int logits)
 {
     __shared__ float E[64][65];
     __shared__ float At[64][65];
@@ -123,7 +123,10 @@ __global__ void __launch_bounds__(256) bscan_kernel(const float* Abuf, const flo
             for (int idx = tid; idx < dk * dk; idx += 256) At[idx / dk][idx % dk] = Abuf[vu * dk * dk + idx];
         } else if (tid < dk) {
             float gs = 0.f;
-            for (int t = 0; t < Ts; t++) gs += (float)g[((size_t)bb * T + (size_t)p * Ts + t) * H + h];
+            for (int t = 0; t < Ts; t++) {
+                const float gv = (float)g[((size_t)bb * T + (size_t)p * Ts + t) * H + h];
+                gs += logits ? 1.f / (1.f + expf(-gv)) : gv;
+            }
             dec[tid] = expf(gs * -expf(A_log[h * dk + tid]));
         }
         __syncthreads();
@@ -217,18 +220,18 @@ static cudaError_t tsplit_states(const Args& a, const WsLayout& L, int P, cudaSt
         if (a.mode == GDN_DELTA)
             scan_kernel<__nv_bfloat16, true><<<units, 256, 0, st>>>(Abuf, Hbuf, a.h0, Sst, a.hT,
                                                                      (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H,
-                                                                     a.T, P, a.dk, a.dv);
+                                                                     a.T, P, a.dk, a.dv, a.logits);
         else
             scan_kernel<__nv_bfloat16, false><<<units, 256, 0, st>>>(Abuf, Hbuf, a.h0, Sst, a.hT,
                                                                       (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H,
-                                                                      a.T, P, a.dk, a.dv);
+                                                                      a.T, P, a.dk, a.dv, a.logits);
     } else {
         if (a.mode == GDN_DELTA)
             scan_kernel<float, true><<<units, 256, 0, st>>>(Abuf, Hbuf, a.h0, Sst, a.hT, (const float*)a.g, a.A_log,
-                                                            a.B, a.H, a.T, P, a.dk, a.dv);
+                                                            a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
         else
             scan_kernel<float, false><<<units, 256, 0, st>>>(Abuf, Hbuf, a.h0, Sst, a.hT, (const float*)a.g,
-                                                             a.A_log, a.B, a.H, a.T, P, a.dk, a.dv);
+                                                             a.A_log, a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
     }
     return cudaGetLastError();
 }
@@ -278,18 +281,18 @@ cudaError_t launch_bwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
         if (a.mode == GDN_DELTA)
             bscan_kernel<__nv_bfloat16, true><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0,
                                                                       (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H,
-                                                                      a.T, P, a.dk, a.dv);
+                                                                      a.T, P, a.dk, a.dv, a.logits);
         else
             bscan_kernel<__nv_bfloat16, false><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0,
                                                                        (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H,
-                                                                       a.T, P, a.dk, a.dv);
+                                                                       a.T, P, a.dk, a.dv, a.logits);
     } else {
         if (a.mode == GDN_DELTA)
             bscan_kernel<float, true><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0, (const float*)a.g,
-                                                             a.A_log, a.B, a.H, a.T, P, a.dk, a.dv);
+                                                             a.A_log, a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
         else
             bscan_kernel<float, false><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0, (const float*)a.g,
-                                                              a.A_log, a.B, a.H, a.T, P, a.dk, a.dv);
+                                                              a.A_log, a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

@@ -54,6 +54,10 @@ __device__ __forceinline__ float decay(float g, float A, float A_log2e)
     return ex2_approx(g * A_log2e);
 }
 
+// logistic function, for g and beta given as logits (GDN_GATE_LOGITS)
+__device__ __forceinline__ float sigmoidf(float z) { return 1.f / (1.f + expf(-z)); }
+__device__ __forceinline__ float gate(float x, int logits) { return logits ? sigmoidf(x) : x; }
+
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }

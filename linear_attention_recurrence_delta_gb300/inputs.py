@@ -116,6 +116,7 @@ class Workload:
     c_dist: str = "normal"     # "normal" | "l2norm"
     g_mu: float = 0.0          # g = sigmoid(N(g_mu, 1))
     h0_std: float = 0.0        # h0 = h0_std * N(0, 1) (0 => no h0)
+    gate_logits: bool = False  # g (and beta) drawn as logits N(g_mu, 1) (N(0, 1)), not passed through a sigmoid
     alog_max: float = math.log(16.0)   # A_log ~ U(0, alog_max)
     notes: str = ""
 
@@ -188,9 +189,10 @@ def make_inputs(w: Workload) -> dict:
     out["v"] = round_to(normal(s, STREAMS["v"], B * T * H * dv).reshape(B, T, H, dv), w.dtype)
     out["b"] = round_to(_draw_keys(s, STREAMS["b"], (B, T, H, dk), w.b_dist), w.dtype)
     out["c"] = round_to(_draw_keys(s, STREAMS["c"], (B, T, H, dk), w.c_dist), w.dtype)
-    out["g"] = round_to(_sigmoid(w.g_mu + normal(s, STREAMS["g"], B * T * H)).reshape(B, T, H), w.dtype)
+    squash = (lambda z: z) if w.gate_logits else _sigmoid
+    out["g"] = round_to(squash(w.g_mu + normal(s, STREAMS["g"], B * T * H)).reshape(B, T, H), w.dtype)
     if w.mode == "delta":
-        out["beta"] = round_to(_sigmoid(normal(s, STREAMS["beta"], B * T * H)).reshape(B, T, H), w.dtype)
+        out["beta"] = round_to(squash(normal(s, STREAMS["beta"], B * T * H)).reshape(B, T, H), w.dtype)
     else:
         out["beta"] = None
     out["A_log"] = round_to(uniform(s, STREAMS["A_log"], H * dk).reshape(H, dk) * w.alog_max, "f32")

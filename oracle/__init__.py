@@ -188,3 +188,27 @@ def gdn_bwd(v, b, c, g, beta, A_log, h0, dO, dhT=None, mode="gated", seg=64, thr
                                          _p(out["dh0"]), int(seg), a, e), B, H, threads)
     out["dA_log"] = dA_unit.reshape(B, H, dk).sum(axis=0)
     return out
+
+
+def sigmoid(z):
+    """The logistic function in fp64: g as the rule uses it, from its logit
+    ("GDN & MLA Mechanism Deep-Dive", Gated delta rule: g is the sigmoid of a
+    projection); beta takes the same form here."""
+    z = _f64(z)
+    return None if z is None else 1.0 / (1.0 + np.exp(-z))
+
+
+def gdn_fwd_logits(v, b, c, zg, zbeta, A_log, h0=None, mode="gated", **kw):
+    """gdn_fwd with g (and beta) given as logits: the rule on sigmoid(zg), sigmoid(zbeta)."""
+    return gdn_fwd(v, b, c, sigmoid(zg), sigmoid(zbeta), A_log, h0, mode=mode, **kw)
+
+
+def gdn_bwd_logits(v, b, c, zg, zbeta, A_log, h0, dO, dhT=None, mode="gated", **kw):
+    """gdn_bwd with g (and beta) given as logits; dg and dbeta are with respect to the logits
+    (the chain rule through the sigmoid: d sigmoid(z)/dz = sigmoid(z) (1 - sigmoid(z)))."""
+    g, be = sigmoid(zg), sigmoid(zbeta)
+    out = gdn_bwd(v, b, c, g, be, A_log, h0, dO, dhT, mode=mode, **kw)
+    out["dg"] = out["dg"] * g * (1.0 - g)
+    if be is not None:
+        out["dbeta"] = out["dbeta"] * be * (1.0 - be)
+    return out

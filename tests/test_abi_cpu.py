@@ -131,3 +131,15 @@ def test_time_split_backward_workspace():
     fwd_split = gdn.gdn_workspace_bytes(gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0)
     # same tokens and heads: the backward's own buffers are equal, the split adds at least the forward's
     assert few >= many + fwd_split - 256 + 32768 * 16 * 64 * 2 + 2 * 128 * 16384
+
+
+def test_gate_logits_option_bit():
+    """GDN_GATE_LOGITS rides in the mode field: the workspace is the same with or without it, and a mode
+    with an unknown bit is rejected (size 0)."""
+    plain = gdn.make_shape(2, 4, 300, 64, 64, "delta", "bf16")
+    logit = gdn.make_shape(2, 4, 300, 64, 64, "delta", "bf16", gate_logits=True)
+    assert logit.mode == gdn.GDN_DELTA | gdn.GDN_GATE_LOGITS
+    for bwd in (0, 1):
+        assert gdn.gdn_workspace_bytes(logit, bwd) == gdn.gdn_workspace_bytes(plain, bwd) > 0
+    bad = gdn.make_shape(2, 4, 300, 64, 64, gdn.GDN_DELTA | 0x200, "bf16")
+    assert gdn.gdn_workspace_bytes(bad, 0) == 0

@@ -233,3 +233,38 @@ def test_backward_segment_length_irrelevant():
     for k in a:
         if a[k] is not None:
             np.testing.assert_allclose(a[k], b[k], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+def test_logit_gates_finite_differences(mode):
+    """g and beta given as logits: the forward is the rule on their sigmoids (the
+    logistic function written out here, not the oracle's), and the logit
+    gradients match central differences of L = <o, dO> + <h_T, dh_T>."""
+    x = draw(mode, B=1, H=1, T=30, dk=4, dv=5, seed=9, h0_std=0.5)
+    rng = np.random.default_rng(11)
+    zg = rng.normal(size=x["g"].shape)
+    zb = rng.normal(size=x["g"].shape) if mode == "delta" else None
+    logistic = lambda z: None if z is None else np.exp(z) / (np.exp(z) + 1.0)
+    o_l, h_l = oracle.gdn_fwd_logits(x["v"], x["b"], x["c"], zg, zb, x["A_log"], x["h0"], mode=mode)
+    o_p, h_p = oracle.gdn_fwd(x["v"], x["b"], x["c"], logistic(zg), logistic(zb), x["A_log"], x["h0"], mode=mode)
+    np.testing.assert_allclose(o_l, o_p, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(h_l, h_p, rtol=0, atol=1e-13)
+    dO = rng.normal(size=x["v"].shape)
+    dhT = rng.normal(size=(1, 1, 4, 5))
+    gr = oracle.gdn_bwd_logits(x["v"], x["b"], x["c"], zg, zb, x["A_log"], x["h0"], dO, dhT, mode=mode)
+
+    def loss(zg_, zb_):
+        o, hT = oracle.gdn_fwd_logits(x["v"], x["b"], x["c"], zg_, zb_, x["A_log"], x["h0"], mode=mode, threads=1)
+        return float((o * dO).sum() + (hT * dhT).sum())
+
+    eps = 1e-6
+    for name, z, grad in [("dg", zg, gr["dg"])] + ([("dbeta", zb, gr["dbeta"])] if mode == "delta" else []):
+        for k in range(z.size):
+            p = z.reshape(-1).copy(); p[k] += eps
+            m = z.reshape(-1).copy(); m[k] -= eps
+            if name == "dg":
+                fd = (loss(p.reshape(z.shape), zb) - loss(m.reshape(z.shape), zb)) / (2 * eps)
+            else:
+                fd = (loss(zg, p.reshape(z.shape)) - loss(zg, m.reshape(z.shape))) / (2 * eps)
+            an = grad.reshape(-1)[k]
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (name, k, fd, an)
