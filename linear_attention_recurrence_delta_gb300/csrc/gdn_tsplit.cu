@@ -43,118 +43,133 @@ __global__ void eye_kernel(float* I, size_t n_units, int dk)
     }
 }
 
-// Step 3 for one (batch, head): S_0 = h0; S_{p+1} = A_p S_p + H_p; stores every
-// S_p (the entering states of step 4) and, if asked, S_P as h_T.
-template <typename IO, bool DELTA>
-__global__ void __launch_bounds__(256) scan_kernel(const float* Abuf, const float* Hbuf, const float* h0, float* Sst,
-                                                   float* hT, const IO* g, const float* A_log, int B, int H, int T,
-                                                   int P, int dk, int dv, int logits)
+// The scans over segments, one CTA per (batch, head), P sequential steps of a
+// 64 x 64 x 64 fp32 product:
+//   forward (steps 3):  X_0 = h0;   X_{p+1} = A_p X_p + H_p;     stores X_p, ends with h_T
+//   reverse (step 6):   X = dh_T;   X <- A_p^T X + G_p (p = P-1 .. 0); stores X before
+//                                   each update (the end gradients), ends with dh0
+// Delta: A_p from the transition runs; gated: A_p = diag(exp(A sum_{t in p} g_t)).
+// Thread t owns the 4 x 4 output tile rows 4 (t >> 4) .., columns 4 (t & 15) ..;
+// the product reads one float4 of A (transposed in shared memory) and one of X
+// per 16 FMAs.  The segment sums of g are fixed-order block reductions.
+constexpr int kSP = 68;   // padded row stride of the 64 x 64 tiles
+constexpr int kMaxSeg = 152;
+
+template <typename IO, bool DELTA, bool REVERSE>
+__global__ void __launch_bounds__(256) seg_scan_kernel(const float* Abuf, const float* Add, const float* X0,
+                                                       float* Xst, float* Xend, const IO* g, const float* A_log,
+                                                       int B, int H, int T, int P, int dk, int dv, int logits)
 {
-    __shared__ float S[64][65];
-    __shared__ float At[64][65];
+    __shared__ __align__(16) float Xs[64][kSP];
+    __shared__ __align__(16) float MT[64][kSP];   // MT[k][i] = M[i][k], M = A_p (forward) or A_p^T (reverse)
     __shared__ float dec[64];
-    const int u = blockIdx.x, bb = u / H, h = u % H, tid = threadIdx.x;
-    const int Ts = T / P;
-    for (int idx = tid; idx < dk * dv; idx += 256) {
-        const int i = idx / dv, j = idx % dv;
-        S[i][j] = h0 ? h0[(size_t)u * dk * dv + idx] : 0.f;
+    __shared__ float gseg[kMaxSeg];
+    __shared__ float red[8][kMaxSeg];
+    const int u = blockIdx.x, bb = u / H, h = u % H, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int Ts = T / P, i0 = 4 * (tid >> 4), j0 = 4 * (tid & 15);
+    const size_t S = (size_t)dk * dv;
+
+    for (int idx = tid; idx < 64 * kSP; idx += 256) {
+        const int i = idx / kSP, j = idx % kSP;
+        Xs[i][j] = (X0 && i < dk && j < dv) ? X0[(size_t)u * S + (size_t)i * dv + j] : 0.f;
+        if (!DELTA) MT[i][j] = 0.f;
+    }
+    if (!DELTA) {
+        // sum of the gates of every segment: each thread its strided tokens, then the warps in order
+        for (int p = 0; p < P; p++) {
+            float part = 0.f;
+            for (int t = tid; t < Ts; t += 256) {
+                const float gv = (float)g[((size_t)bb * T + (size_t)p * Ts + t) * H + h];
+                part += logits ? 1.f / (1.f + expf(-gv)) : gv;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (lane == 0) red[w][p] = part;
+        }
+        __syncthreads();
+        for (int p = tid; p < P; p += 256) {
+            float sum = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < 8; ww++) sum += red[ww][p];
+            gseg[p] = sum;
+        }
     }
     __syncthreads();
-    for (int p = 0; p < P; p++) {
-        const size_t vu = ((size_t)(bb * P + p) * H + h);  // unit of the [B*P, T/P, H] view
-        for (int idx = tid; idx < dk * dv; idx += 256) Sst[vu * dk * dv + idx] = S[idx / dv][idx % dv];
+
+    for (int step = 0; step < P; step++) {
+        const int p = REVERSE ? P - 1 - step : step;
+        const size_t vu = ((size_t)(bb * P + p) * H + h);   // unit of the [B*P, T/P, H] view
+        for (int idx = tid; idx < dk * dv; idx += 256) Xst[vu * S + idx] = Xs[idx / dv][idx % dv];
         if (DELTA) {
-            for (int idx = tid; idx < dk * dk; idx += 256) At[idx / dk][idx % dk] = Abuf[vu * dk * dk + idx];
-        } else if (tid < dk) {
-            // decay of the whole segment: exp(A_i sum_t g_t)
-            float gs = 0.f;
-            for (int t = 0; t < Ts; t++) {
-                const float gv = (float)g[((size_t)bb * T + (size_t)p * Ts + t) * H + h];
-                gs += logits ? 1.f / (1.f + expf(-gv)) : gv;
+            const float* A = Abuf + vu * dk * dk;
+            for (int idx = tid; idx < 64 * 64; idx += 256) {
+                const int r = idx >> 6, c = idx & 63;    // MT[r][c]
+                float x = 0.f;
+                if (r < dk && c < dk) x = REVERSE ? A[r * dk + c] : A[c * dk + r];
+                MT[r][c] = x;
             }
-            dec[tid] = expf(gs * -expf(A_log[h * dk + tid]));
+        } else if (tid < 64) {
+            dec[tid] = tid < dk ? expf(gseg[p] * -expf(A_log[h * dk + tid])) : 0.f;
         }
         __syncthreads();
-        float acc[16];
+        float acc[4][4];
 #pragma unroll
-        for (int q = 0; q < 16; q++) {
-            const int idx = tid + 256 * q;
-            if (idx < dk * dv) {
-                const int i = idx / dv, j = idx % dv;
-                float v = Hbuf[vu * dk * dv + idx];
-                if (DELTA) {
-                    for (int k = 0; k < dk; k++) v = fmaf(At[i][k], S[k][j], v);
-                } else {
-                    v = fmaf(dec[i], S[i][j], v);
-                }
-                acc[q] = v;
+        for (int a = 0; a < 4; a++)
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const int i = i0 + a, j = j0 + c;
+                acc[a][c] = (i < dk && j < dv) ? Add[vu * S + (size_t)i * dv + j] : 0.f;
+            }
+        if (DELTA) {
+            for (int k = 0; k < dk; k++) {
+                const float4 m = *reinterpret_cast<const float4*>(&MT[k][i0]);
+                const float4 x = *reinterpret_cast<const float4*>(&Xs[k][j0]);
+                const float mv[4] = {m.x, m.y, m.z, m.w}, xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int a = 0; a < 4; a++)
+#pragma unroll
+                    for (int c = 0; c < 4; c++) acc[a][c] = fmaf(mv[a], xv[c], acc[a][c]);
+            }
+        } else {
+#pragma unroll
+            for (int a = 0; a < 4; a++) {
+                const float4 x = *reinterpret_cast<const float4*>(&Xs[i0 + a][j0]);
+                acc[a][0] = fmaf(dec[i0 + a], x.x, acc[a][0]);
+                acc[a][1] = fmaf(dec[i0 + a], x.y, acc[a][1]);
+                acc[a][2] = fmaf(dec[i0 + a], x.z, acc[a][2]);
+                acc[a][3] = fmaf(dec[i0 + a], x.w, acc[a][3]);
             }
         }
         __syncthreads();
 #pragma unroll
-        for (int q = 0; q < 16; q++) {
-            const int idx = tid + 256 * q;
-            if (idx < dk * dv) S[idx / dv][idx % dv] = acc[q];
-        }
+        for (int a = 0; a < 4; a++)
+            *reinterpret_cast<float4*>(&Xs[i0 + a][j0]) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
         __syncthreads();
     }
-    if (hT)
-        for (int idx = tid; idx < dk * dv; idx += 256) hT[(size_t)u * dk * dv + idx] = S[idx / dv][idx % dv];
+    if (Xend)
+        for (int idx = tid; idx < dk * dv; idx += 256) Xend[(size_t)u * S + idx] = Xs[idx / dv][idx % dv];
 }
 
-// Step 6 for one (batch, head): E_{P-1} = dh_T; E_{p-1} = G_p + A_p^T E_p;
-// stores every E_p (the end gradients of step 7) and dh0 = G_0 + A_0^T E_0.
-template <typename IO, bool DELTA>
-__global__ void __launch_bounds__(256) bscan_kernel(const float* Abuf, const float* Gbuf, const float* dhT,
-                                                    float* Ebuf, float* dh0, const IO* g, const float* A_log, int B,
-                                                    int H, int T, int P, int dk, int dv, int logits)
+template <bool REVERSE>
+static void launch_seg_scan(const Args& a, int P, const float* Abuf, const float* Add, const float* X0, float* Xst,
+                            float* Xend, cudaStream_t st)
 {
-    __shared__ float E[64][65];
-    __shared__ float At[64][65];
-    __shared__ float dec[64];
-    const int u = blockIdx.x, bb = u / H, h = u % H, tid = threadIdx.x;
-    const int Ts = T / P;
-    for (int idx = tid; idx < dk * dv; idx += 256) E[idx / dv][idx % dv] = dhT ? dhT[(size_t)u * dk * dv + idx] : 0.f;
-    __syncthreads();
-    for (int p = P - 1; p >= 0; p--) {
-        const size_t vu = ((size_t)(bb * P + p) * H + h);
-        for (int idx = tid; idx < dk * dv; idx += 256) Ebuf[vu * dk * dv + idx] = E[idx / dv][idx % dv];
-        if (DELTA) {
-            for (int idx = tid; idx < dk * dk; idx += 256) At[idx / dk][idx % dk] = Abuf[vu * dk * dk + idx];
-        } else if (tid < dk) {
-            float gs = 0.f;
-            for (int t = 0; t < Ts; t++) {
-                const float gv = (float)g[((size_t)bb * T + (size_t)p * Ts + t) * H + h];
-                gs += logits ? 1.f / (1.f + expf(-gv)) : gv;
-            }
-            dec[tid] = expf(gs * -expf(A_log[h * dk + tid]));
-        }
-        __syncthreads();
-        float acc[16];
-#pragma unroll
-        for (int q = 0; q < 16; q++) {
-            const int idx = tid + 256 * q;
-            if (idx < dk * dv) {
-                const int i = idx / dv, j = idx % dv;
-                float v = Gbuf[vu * dk * dv + idx];
-                if (DELTA) {
-                    for (int k = 0; k < dk; k++) v = fmaf(At[k][i], E[k][j], v);
-                } else {
-                    v = fmaf(dec[i], E[i][j], v);
-                }
-                acc[q] = v;
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int q = 0; q < 16; q++) {
-            const int idx = tid + 256 * q;
-            if (idx < dk * dv) E[idx / dv][idx % dv] = acc[q];
-        }
-        __syncthreads();
+    const int units = a.B * a.H;
+    if (a.io == GDN_BF16) {
+        if (a.mode == GDN_DELTA)
+            seg_scan_kernel<__nv_bfloat16, true, REVERSE><<<units, 256, 0, st>>>(
+                Abuf, Add, X0, Xst, Xend, (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
+        else
+            seg_scan_kernel<__nv_bfloat16, false, REVERSE><<<units, 256, 0, st>>>(
+                Abuf, Add, X0, Xst, Xend, (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
+    } else {
+        if (a.mode == GDN_DELTA)
+            seg_scan_kernel<float, true, REVERSE><<<units, 256, 0, st>>>(
+                Abuf, Add, X0, Xst, Xend, (const float*)a.g, a.A_log, a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
+        else
+            seg_scan_kernel<float, false, REVERSE><<<units, 256, 0, st>>>(
+                Abuf, Add, X0, Xst, Xend, (const float*)a.g, a.A_log, a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
     }
-    if (dh0)
-        for (int idx = tid; idx < dk * dv; idx += 256) dh0[(size_t)u * dk * dv + idx] = E[idx / dv][idx % dv];
 }
 
 }  // namespace
@@ -215,24 +230,7 @@ static cudaError_t tsplit_states(const Args& a, const WsLayout& L, int P, cudaSt
     }
 
     // 3. scan over segments
-    const int units = a.B * a.H;
-    if (a.io == GDN_BF16) {
-        if (a.mode == GDN_DELTA)
-            scan_kernel<__nv_bfloat16, true><<<units, 256, 0, st>>>(Abuf, Hbuf, a.h0, Sst, a.hT,
-                                                                     (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H,
-                                                                     a.T, P, a.dk, a.dv, a.logits);
-        else
-            scan_kernel<__nv_bfloat16, false><<<units, 256, 0, st>>>(Abuf, Hbuf, a.h0, Sst, a.hT,
-                                                                      (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H,
-                                                                      a.T, P, a.dk, a.dv, a.logits);
-    } else {
-        if (a.mode == GDN_DELTA)
-            scan_kernel<float, true><<<units, 256, 0, st>>>(Abuf, Hbuf, a.h0, Sst, a.hT, (const float*)a.g, a.A_log,
-                                                            a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
-        else
-            scan_kernel<float, false><<<units, 256, 0, st>>>(Abuf, Hbuf, a.h0, Sst, a.hT, (const float*)a.g,
-                                                             a.A_log, a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
-    }
+    launch_seg_scan<false>(a, P, Abuf, Hbuf, a.h0, Sst, a.hT, st);
     return cudaGetLastError();
 }
 
@@ -275,25 +273,8 @@ cudaError_t launch_bwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
     if ((e = launch_serial_bwd(b, st)) != cudaSuccess) return e;
 
     // 6. reverse scan of the end gradients; dh0 of the whole sequence
-    const int units = a.B * a.H;
     const float* Abuf = (const float*)(ws + L.ts_a_off);
-    if (a.io == GDN_BF16) {
-        if (a.mode == GDN_DELTA)
-            bscan_kernel<__nv_bfloat16, true><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0,
-                                                                      (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H,
-                                                                      a.T, P, a.dk, a.dv, a.logits);
-        else
-            bscan_kernel<__nv_bfloat16, false><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0,
-                                                                       (const __nv_bfloat16*)a.g, a.A_log, a.B, a.H,
-                                                                       a.T, P, a.dk, a.dv, a.logits);
-    } else {
-        if (a.mode == GDN_DELTA)
-            bscan_kernel<float, true><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0, (const float*)a.g,
-                                                             a.A_log, a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
-        else
-            bscan_kernel<float, false><<<units, 256, 0, st>>>(Abuf, Gbuf, a.dhT, Ebuf, a.dh0, (const float*)a.g,
-                                                              a.A_log, a.B, a.H, a.T, P, a.dk, a.dv, a.logits);
-    }
+    launch_seg_scan<true>(a, P, Abuf, Gbuf, a.dhT, Ebuf, a.dh0, st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     // 7. every segment's backward again with its true end gradient
