@@ -259,13 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             unsigned char* sV = sm + OFF_RING + s * STAGE_BYTES;
             unsigned char* sB = sV + 8192;
             unsigned char* sCt = sV + 16384;
-            float g_next = 0.f, beta_next = 0.f;   // g, beta of chunk k + kStages (threads 0..63)
+            // g, beta of chunk k + kStages (threads 0..63), kept as raw bf16 until they are stored so that
+            // nothing waits on the loads inside the chunk
+            __nv_bfloat16 g_next = __float2bfloat16(0.f), beta_next = __float2bfloat16(0.f);
             if (r < kC && k + kStages < p.nchunks) {
                 const int t = (k + kStages) * kC + r;
                 const size_t row = ((size_t)bb * T + t) * H + h;
                 if (t < T) {
-                    g_next = __bfloat162float(p.g[row]);
-                    if (DELTA) beta_next = __bfloat162float(p.beta[row]);
+                    g_next = p.g[row];
+                    if (DELTA) beta_next = p.beta[row];
                 }
             }
 
@@ -833,8 +835,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     // so the load's latency stays hidden behind the chunk)
                     // tokens past T keep g = beta = 0 (an identity step)
                     const bool tok = (k + kStages) * kC + r < T;
-                    S.g[s][r] = tok ? gate_in(g_next, p.logits) : 0.f;
-                    if (DELTA) S.beta[s][r] = tok ? gate_in(beta_next, p.logits) : 0.f;
+                    S.g[s][r] = tok ? gate_in(__bfloat162float(g_next), p.logits) : 0.f;
+                    if (DELTA) S.beta[s][r] = tok ? gate_in(__bfloat162float(beta_next), p.logits) : 0.f;
                 }
                 if (r == 0) issue_load(k + kStages), issued = k + kStages + 1;
             }
