@@ -27,30 +27,31 @@ constexpr int kDecCtasPerSm = 4;   // 64 registers x 256 threads: four CTAs fill
 
 // One unit's token inputs held in registers until they are staged: thread t
 // owns elements idx = t + 256 q of the [T][64] rows (T <= 8, so q < 2).
-struct TokRegs {
-    float g[2], b[2], c[2], v[2];
-    float beta;
+template <typename IO>
+struct TokRegs {   // raw I/O values: converted when staged, so nothing waits on the loads meanwhile
+    IO g[2], b[2], c[2], v[2];
+    IO beta;
 };
 
 template <typename IO, bool DELTA>
-__device__ __forceinline__ void load_tokens(const Args& a, int u, TokRegs& r)
+__device__ __forceinline__ void load_tokens(const Args& a, int u, TokRegs<IO>& r)
 {
     const int tid = threadIdx.x, bb = u / a.H, h = u % a.H, dk = a.dk, dv = a.dv, T = a.T, H = a.H;
 #pragma unroll
     for (int q = 0; q < 2; q++) {
         const int idx = tid + 256 * q, tt = idx >> 6, i = idx & 63;
-        r.g[q] = r.b[q] = r.c[q] = r.v[q] = 0.f;
+        r.g[q] = r.b[q] = r.c[q] = r.v[q] = from_f<IO>(0.f);
         if (tt < T) {
             const size_t row = ((size_t)bb * T + tt) * H + h;
-            r.g[q] = gate(to_f(((const IO*)a.g)[row]), a.logits);
+            r.g[q] = ((const IO*)a.g)[row];
             if (i < dk) {
-                r.b[q] = to_f(((const IO*)a.b)[row * dk + i]);
-                r.c[q] = to_f(((const IO*)a.c)[row * dk + i]);
+                r.b[q] = ((const IO*)a.b)[row * dk + i];
+                r.c[q] = ((const IO*)a.c)[row * dk + i];
             }
-            if (i < dv) r.v[q] = to_f(((const IO*)a.v)[row * dv + i]);
+            if (i < dv) r.v[q] = ((const IO*)a.v)[row * dv + i];
         }
     }
-    r.beta = (DELTA && tid < T) ? gate(to_f(((const IO*)a.beta)[((size_t)bb * T + tid) * H + h]), a.logits) : 0.f;
+    r.beta = (DELTA && tid < T) ? ((const IO*)a.beta)[((size_t)bb * T + tid) * H + h] : from_f<IO>(0.f);
 }
 
 // the unit's fp32 state (d_k x d_v, contiguous) into a shared buffer by cp.async
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(256) decode_kernel(Args a, bool vec4)
     const bool pre = vec4 && a.h0 != nullptr;   // state prefetch by cp.async (rows of whole 16-byte quads)
     IO* o = (IO*)a.o;
 
-    TokRegs tr;
+    TokRegs<IO> tr;
     int u = blockIdx.x;
     load_tokens<IO, DELTA>(a, u, tr);
     if (pre) issue_state(a, u, snext[0]);
@@ -91,13 +92,13 @@ __global__ void __launch_bounds__(256) decode_kernel(Args a, bool vec4)
         for (int q = 0; q < 2; q++) {
             const int idx = tid + 256 * q, tt = idx >> 6, i = idx & 63;
             if (tt < kDecMaxT) {
-                sAl[tt][i] = i < dk ? expf(tr.g[q] * -expf(a.A_log[h * dk + i])) : 0.f;
-                sB[tt][i] = tr.b[q];
-                sC[tt][i] = tr.c[q];
-                sV[tt][i] = tr.v[q];
+                sAl[tt][i] = i < dk ? expf(gate(to_f(tr.g[q]), a.logits) * -expf(a.A_log[h * dk + i])) : 0.f;
+                sB[tt][i] = to_f(tr.b[q]);
+                sC[tt][i] = to_f(tr.c[q]);
+                sV[tt][i] = to_f(tr.v[q]);
             }
         }
-        if (DELTA && tid < kDecMaxT) sbeta[tid] = tr.beta;
+        if (DELTA && tid < kDecMaxT) sbeta[tid] = gate(to_f(tr.beta), a.logits);
         if (un < units) {
             load_tokens<IO, DELTA>(a, un, tr);
             if (pre) issue_state(a, un, snext[buf ^ 1]);

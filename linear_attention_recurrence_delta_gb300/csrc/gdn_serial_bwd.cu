@@ -62,7 +62,7 @@ __device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast
 
 template <typename IO, bool DELTA>
 __device__ __forceinline__ void issue_block(const Args& a, BwdSmem<IO>& s, const Ctx& C, int t0, bool grad, bool vec,
-                                            float& greg, float& breg)
+                                            IO& greg, IO& breg)
 {
     const int tid = C.tid, dk = a.dk, dv = a.dv, T = a.T, H = a.H;
     const int nt = min(kBT, T - t0);
@@ -101,21 +101,22 @@ __device__ __forceinline__ void issue_block(const Args& a, BwdSmem<IO>& s, const
             }
         }
     }
-    if (tid < nt) greg = gate(to_f(((const IO*)a.g)[((size_t)C.bb * T + t0 + tid) * H + C.h]), a.logits);
+    // g, beta stay raw until finish_block stores them: nothing waits on these loads meanwhile
+    if (tid < nt) greg = ((const IO*)a.g)[((size_t)C.bb * T + t0 + tid) * H + C.h];
     if (DELTA && tid >= 32 && tid - 32 < nt)
-        breg = gate(to_f(((const IO*)a.beta)[((size_t)C.bb * T + t0 + tid - 32) * H + C.h]), a.logits);
+        breg = ((const IO*)a.beta)[((size_t)C.bb * T + t0 + tid - 32) * H + C.h];
 }
 
 // Make the block issued last the current one.  Tokens past T become identity
 // steps (alpha = 1, every other input 0), so a block is always 32 tokens.
 template <typename IO, bool DELTA>
 __device__ __forceinline__ void finish_block(const Args& a, BwdSmem<IO>& s, const Ctx& C, int t0, bool grad,
-                                             float greg, float breg, bool leave_newest = false)
+                                             IO greg, IO breg, bool leave_newest = false)
 {
     const int tid = C.tid, dk = a.dk, dv = a.dv;
     const int nt = min(kBT, a.T - t0);
-    if (tid < 32) s.rg[tid] = greg;
-    else if (tid < 64) s.rbeta[tid - 32] = breg;
+    if (tid < 32) s.rg[tid] = gate(to_f(greg), a.logits);
+    else if (tid < 64) s.rbeta[tid - 32] = gate(to_f(breg), a.logits);
     if (leave_newest) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
     else cp_async_wait_all();
     __syncthreads();
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
     load_state(a.h0, S);
 
     // ---------------- forward sweep: state entering every block ----------------
-    float greg = 0.f, breg = 0.f;
+    IO greg = from_f<IO>(0.f), breg = from_f<IO>(0.f);
     __syncthreads();  // Arow
     issue_block<IO, DELTA>(a, s, C, 0, false, vec, greg, breg);
     for (int n = 0; n < nblk; n++) {

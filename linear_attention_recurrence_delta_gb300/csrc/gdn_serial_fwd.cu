@@ -46,7 +46,7 @@ struct Unit {
 // when rows are not 16-byte aligned), g and beta into registers.
 template <typename IO, bool DELTA>
 __device__ __forceinline__ void issue_block(const Args& a, FwdSmem<IO>& s, const Unit& U, int t0, int nt, bool vec,
-                                            float& greg, float& breg)
+                                            IO& greg, IO& breg)
 {
     const int tid = threadIdx.x, dk = a.dk, dv = a.dv, T = a.T, H = a.H;
     const IO* bk = (const IO*)a.b;
@@ -74,9 +74,10 @@ __device__ __forceinline__ void issue_block(const Args& a, FwdSmem<IO>& s, const
             if (i < U.ncols) s.rv[tt][i] = v[row * dv + U.jc0 + i];
         }
     }
-    if (tid < nt) greg = gate(to_f(((const IO*)a.g)[((size_t)U.bb * T + t0 + tid) * H + U.h]), a.logits);
+    // g, beta stay raw until they are stored at the end of the block: nothing waits on these loads meanwhile
+    if (tid < nt) greg = ((const IO*)a.g)[((size_t)U.bb * T + t0 + tid) * H + U.h];
     if (DELTA && tid >= 32 && tid - 32 < nt)
-        breg = gate(to_f(((const IO*)a.beta)[((size_t)U.bb * T + t0 + tid - 32) * H + U.h]), a.logits);
+        breg = ((const IO*)a.beta)[((size_t)U.bb * T + t0 + tid - 32) * H + U.h];
 }
 
 // raw block -> fp32 staged arrays (alpha computed here, once per row and token)
@@ -135,10 +136,10 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
         h[p] = f2(x0, x1);
     }
 
-    float greg = 0.f, breg = 0.f;
+    IO greg = from_f<IO>(0.f), breg = from_f<IO>(0.f);
     issue_block<IO, DELTA>(a, s, U, 0, min(kTB, T), vec, greg, breg);
-    if (tid < 32) s.rg[tid] = greg;
-    else if (tid < 64) s.rbeta[tid - 32] = breg;
+    if (tid < 32) s.rg[tid] = gate(to_f(greg), a.logits);
+    else if (tid < 64) s.rbeta[tid - 32] = gate(to_f(breg), a.logits);
     cp_async_wait_all();
     __syncthreads();
     convert_block<IO, DELTA>(a, s, U, min(kTB, T));
@@ -181,8 +182,8 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
             o[(((size_t)U.bb * T + t0 + tt) * H + U.h) * dv + U.jc0 + q] = from_f<IO>(s.O[tt][q]);
         }
         if (n + 1 < nblk) {
-            if (tid < 32) s.rg[tid] = greg;
-            else if (tid < 64) s.rbeta[tid - 32] = breg;
+            if (tid < 32) s.rg[tid] = gate(to_f(greg), a.logits);
+            else if (tid < 64) s.rbeta[tid - 32] = gate(to_f(breg), a.logits);
             cp_async_wait_all();
             __syncthreads();
             convert_block<IO, DELTA>(a, s, U, min(kTB, T - t0 - kTB));
