@@ -70,8 +70,10 @@ def io_bytes(w, backward=False):
 
 def tsplit_factor(w, backward):
     """Segments of the library's time split for workload w (1 = none); mirrors the rule in
-    csrc/gdn_tsplit.cu: B*H*P <= 152 SMs, T divisible by P, >= 512 tokens per segment, P >= 4 for a delta
-    forward and >= 3 otherwise."""
+    csrc/gdn_tsplit.cu: heads at most 64 wide, B*H*P <= 152 SMs, T divisible by P, >= 512 tokens per
+    segment, P >= 4 for a delta forward and >= 3 otherwise."""
+    if w.dk > 64 or w.dv > 64:
+        return 1
     units = w.B * w.H
     min_p = 3 if backward else (4 if w.mode == "delta" else 3)
     for p in range(152 // units, min_p - 1, -1):
@@ -87,10 +89,18 @@ def fwd_launches(w):
     return 5 if w.mode == "delta" else 3   # state run, (identity, transition run), scan, output run
 
 
+def bwd_slabs(w):
+    """Column slabs of the serial backward (64 value columns per CTA up to d_k = 64, 32 above)."""
+    cols = 64 if w.dk <= 64 else 32
+    return -(-w.dv // cols)
+
+
 def bwd_launches(w):
     """Kernels one gdn_bwd call launches."""
     if tsplit_factor(w, True) == 1:
-        return 2                            # backward + dA_log reduction
+        # backward, the slabs' partial sums of db, dc, dg (, dbeta) if several, dA_log reduction
+        sums = (4 if w.mode == "delta" else 3) if bwd_slabs(w) > 1 else 0
+        return 2 + sums
     states = 4 if w.mode == "delta" else 2
     return states + 2 + 1 + 2               # state passes, backward x2 (+ reductions), reverse scan
 
@@ -99,9 +109,9 @@ def fwd_kernel_name(w):
     """The kernel gdn_fwd launches for workload w (one launch per call)."""
     if w.T <= 8:
         return "decode_kernel (one launch)"
-    if w.dtype == "bf16":
+    if w.dtype == "bf16" and w.dk <= 64:
         return f"fwd_tc_kernel<{w.mode}> (one launch)"
-    return f"serial_fwd_kernel<f32, {w.mode}> (one launch)"
+    return f"serial_fwd_kernel<{w.dtype}, {w.mode}> (one launch)"
 
 
 class ClockSampler:

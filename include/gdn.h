@@ -41,7 +41,8 @@
  *
  * Limits: B, H >= 1; T >= 0 (with T = 0 the per-token pointers may be NULL:
  * the forward copies h0, or zeros, to hT; the backward writes dh0 = dhT and
- * dA_log = 0); 1 <= d_k, d_v <= 64.  With io = GDN_BF16, d_k
+ * dA_log = 0); 1 <= d_k, d_v <= 128 (the tensor-core forward takes
+ * d_k <= 64, wider keys the token-serial kernels).  With io = GDN_BF16, d_k
  * and d_v must be multiples of 8 and every bf16 pointer 16-byte aligned;
  * with io = GDN_F32, every pointer 4-byte aligned.  float32 state and A_log
  * pointers must be 16-byte aligned.  Outputs must not alias inputs.

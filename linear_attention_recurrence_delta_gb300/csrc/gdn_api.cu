@@ -14,7 +14,7 @@ static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 static bool shape_ok(const gdn_shape_t& s)
 {
     if (s.B < 1 || s.H < 1 || s.T < 0) return false;
-    if (s.dk < 1 || s.dk > 64 || s.dv < 1 || s.dv > 64) return false;
+    if (s.dk < 1 || s.dk > 128 || s.dv < 1 || s.dv > 128) return false;
     if (s.io == GDN_BF16 && ((s.dk % 8) || (s.dv % 8))) return false;
     // keep every element offset inside a signed 64-bit range with margin
     const double elems = (double)s.B * s.T * s.H * 64.0;
@@ -25,14 +25,22 @@ static bool shape_ok(const gdn_shape_t& s)
 // the serial backward's buffers for shape s, placed from `off`
 static size_t place_bwd_core(const gdn_shape_t& s, WsLayout& L, size_t off)
 {
-    const size_t units = (size_t)s.B * s.H;
+    const size_t nslab = (size_t)bwd_slabs(s.dk, s.dv);
+    const size_t ctas = (size_t)s.B * s.H * nslab;   // one CTA per unit and column slab
     const size_t nblk = (size_t)((s.T + kSerialBlock - 1) / kSerialBlock);
     L.snap_off = off;
-    off = round_up(off + units * nblk * (kSerialBlock / kSerialSnap) * kStateSlot, 256);
+    off = round_up(off + ctas * nblk * (kSerialBlock / kSerialSnap) * kStateSlot, 256);
     L.xvr_off = off;
-    if (s.mode == GDN_DELTA) off = round_up(off + units * nblk * kSerialBlock * 128 * sizeof(float), 256);
+    if (s.mode == GDN_DELTA)
+        off = round_up(off + ctas * nblk * kSerialBlock * 2 * bwd_cols(s.dk) * sizeof(float), 256);
     L.dalog_off = off;
-    return round_up(off + units * (size_t)s.dk * 4, 256);
+    off = round_up(off + ctas * (size_t)s.dk * 4, 256);
+    L.slab_off = off;
+    if (nslab > 1) {
+        const size_t ntok = (size_t)s.B * s.T * s.H;
+        off = round_up(off + nslab * ntok * (2 * (size_t)s.dk + 2) * sizeof(float), 256);
+    }
+    return off;
 }
 
 // buffers of a time split into P segments (see gdn_tsplit.cu), placed from `off`

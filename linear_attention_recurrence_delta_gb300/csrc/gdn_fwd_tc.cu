@@ -167,6 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int u = blockIdx.x, bb = u / p.H, h = u % p.H;
     const int T = p.T, H = p.H, dk = p.dk, dv = p.dv;
+    // value columns jc0 .. jc0 + nv - 1 of the unit (columns of the state never mix, so wider values are
+    // split in 64-column slabs over blockIdx.y; the slabs repeat the decay and solve work of the keys)
+    const int jc0 = 64 * (int)blockIdx.y, nv = min(64, dv - jc0);
 
     if (tid < 64) {
         const float A = tid < dk ? -expf(p.A_log[h * dk + tid]) : 0.f;
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const int s = k % kStages;
         unsigned char* st = sm + OFF_RING + s * STAGE_BYTES;
         mbar_arrive_expect_tx(&S.full[s], STAGE_BYTES);
-        tma_load_4d(st, &p.tm_v, &S.full[s], 0, h, k * kC, bb);
+        tma_load_4d(st, &p.tm_v, &S.full[s], jc0, h, k * kC, bb);
         tma_load_4d(st + 8192, &p.tm_b, &S.full[s], 0, h, k * kC, bb);
         tma_load_4d(st + 16384, &p.tm_c, &S.full[s], 0, h, k * kC, bb);
     };
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
             for (int j = 0; j < 32; j++) {
                 const int jj = 32 * wh + j;
-                Sreg[j] = (p.h0 && trow < dk && jj < dv) ? p.h0[((size_t)u * dk + trow) * dv + jj] : 0.f;
+                Sreg[j] = (p.h0 && trow < dk && jj < nv) ? p.h0[((size_t)u * dk + trow) * dv + jc0 + jj] : 0.f;
             }
 #pragma unroll
             for (int q = 0; q < 4; q++) {
@@ -796,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
             } else {
                 const int tg = k * kC + (trow - 64);
-                __nv_bfloat16* orow = p.o + (((size_t)bb * T + tg) * H + h) * dv;
+                __nv_bfloat16* orow = p.o + (((size_t)bb * T + tg) * H + h) * dv + jc0;
 #pragma unroll
                 for (int cc = 0; cc < 2; cc++) {
                     const int col = 32 * wh + 16 * cc;
@@ -815,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                         for (int hq = 0; hq < 2; hq++) {
                             const int j0 = col + 8 * hq;
-                            if (j0 < dv) {
+                            if (j0 < nv) {
                                 uint4 wv;
                                 wv.x = pack_bf16(v[8 * hq + 0], v[8 * hq + 1]);
                                 wv.y = pack_bf16(v[8 * hq + 2], v[8 * hq + 3]);
@@ -842,10 +845,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             }
         }
         if (state_row && p.hT && trow < dk) {
-            float* hrow = p.hT + ((size_t)u * dk + trow) * dv;
+            float* hrow = p.hT + ((size_t)u * dk + trow) * dv + jc0;
 #pragma unroll
             for (int j = 0; j < 32; j++)
-                if (32 * wh + j < dv) hrow[32 * wh + j] = Sreg[j];
+                if (32 * wh + j < nv) hrow[32 * wh + j] = Sreg[j];
         }
         // after an abort, let the copies already issued land before exiting
         if (tid == 0 && *(volatile uint32_t*)&S.abort)
@@ -859,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 }
 
 template <bool DELTA>
-cudaError_t launch_t(const TcParams& p, int grid, cudaStream_t st)
+cudaError_t launch_t(const TcParams& p, dim3 grid, cudaStream_t st)
 {
     static bool attr_set = false;
     if (!attr_set) {
@@ -877,7 +880,7 @@ cudaError_t launch_t(const TcParams& p, int grid, cudaStream_t st)
 cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
 {
     *handled = false;
-    if (a.io != GDN_BF16 || a.T <= 0) return cudaSuccess;
+    if (a.io != GDN_BF16 || a.T <= 0 || a.dk > 64) return cudaSuccess;
     TcParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map(&p.tm_v, a.v, a.B, a.T, a.H, a.dv) || !make_map(&p.tm_b, a.b, a.B, a.T, a.H, a.dk) ||
@@ -894,7 +897,8 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     p.logits = a.logits;
     p.nchunks = (a.T + kC - 1) / kC;
     *handled = true;
-    return a.mode == GDN_DELTA ? launch_t<true>(p, a.B * a.H, st) : launch_t<false>(p, a.B * a.H, st);
+    const dim3 grid(a.B * a.H, (a.dv + 63) / 64);
+    return a.mode == GDN_DELTA ? launch_t<true>(p, grid, st) : launch_t<false>(p, grid, st);
 }
 
 }  // namespace gdn

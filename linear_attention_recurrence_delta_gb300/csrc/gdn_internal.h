@@ -34,7 +34,9 @@ struct WsLayout {
     size_t status_off = 0;        // uint32 status code, uint32 detail
     size_t snap_off = 0;          // serial backward: state entering every kSerialSnap tokens
     size_t xvr_off = 0;           // serial backward, delta: x and v - h'^T b of every token
-    size_t dalog_off = 0;         // per-(b,h) dA_log partials, float [B*H, d_k]
+    size_t dalog_off = 0;         // per-(b,h) dA_log partials, float [B*H, slabs, d_k]
+    size_t slab_off = 0;          // serial backward over several column slabs: fp32 partial sums
+                                  // db, dc [slabs][B,T,H,d_k]; dg, dbeta [slabs][B,T,H]
     // forward split in time (long sequences over few heads), see gdn_tsplit.cu
     size_t ts_h_off = 0;          // leaving states from a zero start   [B*P, H, d_k, d_v]
     size_t ts_s_off = 0;          // entering states of the segments    [B*P, H, d_k, d_v]
@@ -54,6 +56,11 @@ constexpr int kSplitMinTokens = 512;           // and every segment keeps at lea
 constexpr int kSerialBlock = 32;               // tokens per backward block
 constexpr int kSerialSnap = 8;                 // tokens between backward state snapshots
 constexpr size_t kStateSlot = 16 * 256 * 4;    // one state snapshot (256 threads x 16 floats)
+
+// The serial backward covers d_k <= 64 with 64 value columns per CTA and
+// d_k <= 128 with 32; wider values take several column slabs.
+inline int bwd_cols(int dk) { return dk <= 64 ? 64 : 32; }
+inline int bwd_slabs(int dk, int dv) { return (dv + bwd_cols(dk) - 1) / bwd_cols(dk); }
 
 WsLayout ws_layout(const gdn_shape_t& s, int backward);
 WsLayout ws_layout_bwd_core(const gdn_shape_t& s);   // the serial backward's own buffers only

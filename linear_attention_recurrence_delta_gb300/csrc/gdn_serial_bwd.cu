@@ -15,10 +15,17 @@
 //   q = dH (.) h';  dg_t = sum_ij A_i q_ij;  dA_log_i += A_i g_t sum_j q_ij
 //   dH <- alpha_t (.) dH.
 //
-// One CTA per (batch, head) unit, 256 threads.  Warp w owns state columns
-// 8w..8w+7; lane = 8 jl + ig holds columns j0 = 8w + 2 jl and j0 + 1 and the
-// eight rows 8 ig .. 8 ig + 7, stored as four packed row pairs in an order
-// permuted by jl so that the sums over columns (dc, db) need no selects.
+// One CTA per (batch, head) unit and slab of value columns, 256 threads.
+// KIG lanes of a warp share a column pair, each holding eight rows: KIG = 8
+// covers d_k <= 64 with 64 columns per CTA, KIG = 16 covers d_k <= 128 with 32
+// columns per CTA.  Warp w owns columns 2 NJ w .. 2 NJ w + 2 NJ - 1 of its slab
+// (NJ = 32 / KIG column pairs per warp); lane = KIG jl + ig holds columns
+// j0 = 2 NJ w + 2 jl and j0 + 1 and the rows 8 ig .. 8 ig + 7, stored as four
+// packed row pairs in an order permuted by jl so that the sums over columns
+// (dc, db) need no selects.  Columns of the state never mix, so slabs are
+// independent except for the sums over columns (db, dc, dg, dbeta, dA_log):
+// with more than one slab each writes fp32 partials that a second kernel adds
+// in a fixed order.
 // Recompute: the forward sweep writes the state every 8 tokens (and, delta,
 // x and v - h'^T b of every token) to the workspace; the reverse walk brings
 // back one 32-token block of them at a time by cp.async, recomputes each
@@ -37,42 +44,59 @@ constexpr int kSub = kSerialSnap;  // tokens per state snapshot
 constexpr int kWin = 4;            // tokens per register window
 constexpr int kNQ = 2;             // row quantities summed over columns: dc, db
 
-template <typename IO>
+template <int KIG>
+struct Cfg {
+    static constexpr int ROWS = 8 * KIG;           // state rows covered (d_k <= ROWS)
+    static constexpr int NJ = 32 / KIG;            // column pairs per warp
+    static constexpr int COLS = 16 * NJ;           // value columns per CTA
+    static constexpr int PBUF = KIG == 8 ? 2 : 1;  // row-partial buffers (one, and a barrier more, at 128 rows)
+};
+
+template <typename IO, int KIG>
 struct BwdSmem {
-    float A[kBT][64], Bv[kBT][64], Cv[kBT][64];                 // alpha_t, b_t, c_t
-    float V[kBT][64], DO[kBT][64];                               // v_t, do_t
-    float XV[2][2][kBT][64];      // two buffers of [x ; v_t - h'^T b_t] (the next block's arrives early)
+    static constexpr int R = Cfg<KIG>::ROWS, NC = Cfg<KIG>::COLS;
+    float A[kBT][R], Bv[kBT][R], Cv[kBT][R];                     // alpha_t, b_t, c_t
+    float V[kBT][NC], DO[kBT][NC];                               // v_t, do_t on the slab's columns
+    float XV[2][2][kBT][NC];      // two buffers of [x ; v_t - h'^T b_t] (the next block's arrives early)
     float beta[kBT], g[kBT];
-    float Arow[64], Arow2[64];  // A and A log2(e)
+    float Arow[R], Arow2[R];      // A and A log2(e)
     float2 snap[kBT / kSub][8][256];                             // per-thread state snapshots
-    float part[2][8][kWin][kNQ][64];                             // per-warp row partials
-    float dvb[2][kWin][64];
+    float part[Cfg<KIG>::PBUF][8][kWin][kNQ][R];                 // per-warp row partials
+    float dvb[2][kWin][NC];
     float bpart[2][8][kWin], gpart[2][8][kWin];
-    float red[8][64];
+    float red[8][R];
     float rg[kBT], rbeta[kBT];
-    IO rb[kBT][64], rc[kBT][64], rv[kBT][64], rdo[kBT][64];     // raw bytes of the next block
+    IO rb[kBT][R], rc[kBT][R], rv[kBT][NC], rdo[kBT][NC];       // raw bytes of the next block
 };
 
 struct Ctx {
     int tid, lane, w, ig, jl, j0, m2, u, bb, h;
-    int roff[4];  // float offset of register pair p inside a 64-row vector
+    int jc0, nv;  // first value column of the slab, columns in it
+    int roff[4];  // float offset of register pair p inside a row vector
+};
+
+// where the sums over columns go: the outputs themselves (one slab) or fp32
+// per-slab partials [slab][...] that reduce_slabs_kernel adds up
+struct Outs {
+    float *db, *dc, *dg, *dbeta;  // partial buffers, or NULL for direct output
 };
 
 __device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
 
-template <typename IO, bool DELTA>
-__device__ __forceinline__ void issue_block(const Args& a, BwdSmem<IO>& s, const Ctx& C, int t0, bool grad, bool vec,
-                                            IO& greg, IO& breg)
+template <typename IO, bool DELTA, int KIG>
+__device__ __forceinline__ void issue_block(const Args& a, BwdSmem<IO, KIG>& s, const Ctx& C, int t0, bool grad,
+                                            bool vec, IO& greg, IO& breg)
 {
-    const int tid = C.tid, dk = a.dk, dv = a.dv, T = a.T, H = a.H;
+    constexpr int R = Cfg<KIG>::ROWS;
+    const int tid = C.tid, dk = a.dk, dv = a.dv, T = a.T, H = a.H, nv = C.nv;
+    const IO* vs = (const IO*)a.v + C.jc0;     // the slab's columns
+    const IO* dOs = (const IO*)a.dO + C.jc0;
     const int nt = min(kBT, T - t0);
     const IO* bk = (const IO*)a.b;
     const IO* c = (const IO*)a.c;
-    const IO* v = (const IO*)a.v;
-    const IO* dO = (const IO*)a.dO;
     constexpr int E = 16 / sizeof(IO);
     if (vec) {
-        const int cb = dk / E, cv = dv / E;
+        const int cb = dk / E, cv = nv / E;
         const int per = grad ? 2 * (cb + cv) : cb + cv;
         for (int idx = tid; idx < nt * per; idx += 256) {
             const int tt = idx / per;
@@ -80,24 +104,24 @@ __device__ __forceinline__ void issue_block(const Args& a, BwdSmem<IO>& s, const
             const size_t row = ((size_t)C.bb * T + t0 + tt) * H + C.h;
             if (r < cb) { cp_async16(&s.rb[tt][r * E], bk + row * dk + r * E); continue; }
             r -= cb;
-            if (r < cv) { cp_async16(&s.rv[tt][r * E], v + row * dv + r * E); continue; }
+            if (r < cv) { cp_async16(&s.rv[tt][r * E], vs + row * dv + r * E); continue; }
             r -= cv;
             if (r < cb) { cp_async16(&s.rc[tt][r * E], c + row * dk + r * E); continue; }
             r -= cb;
-            cp_async16(&s.rdo[tt][r * E], dO + row * dv + r * E);
+            cp_async16(&s.rdo[tt][r * E], dOs + row * dv + r * E);
         }
         cp_async_commit();
     } else {
-        for (int idx = tid; idx < nt * 64; idx += 256) {
-            const int tt = idx >> 6, i = idx & 63;
+        for (int idx = tid; idx < nt * R; idx += 256) {
+            const int tt = idx / R, i = idx % R;
             const size_t row = ((size_t)C.bb * T + t0 + tt) * H + C.h;
             if (i < dk) {
                 s.rb[tt][i] = bk[row * dk + i];
                 if (grad) s.rc[tt][i] = c[row * dk + i];
             }
-            if (i < dv) {
-                s.rv[tt][i] = v[row * dv + i];
-                if (grad) s.rdo[tt][i] = dO[row * dv + i];
+            if (i < nv) {
+                s.rv[tt][i] = vs[row * dv + i];
+                if (grad) s.rdo[tt][i] = dOs[row * dv + i];
             }
         }
     }
@@ -109,26 +133,36 @@ __device__ __forceinline__ void issue_block(const Args& a, BwdSmem<IO>& s, const
 
 // Make the block issued last the current one.  Tokens past T become identity
 // steps (alpha = 1, every other input 0), so a block is always 32 tokens.
-template <typename IO, bool DELTA>
-__device__ __forceinline__ void finish_block(const Args& a, BwdSmem<IO>& s, const Ctx& C, int t0, bool grad,
+template <typename IO, bool DELTA, int KIG>
+__device__ __forceinline__ void finish_block(const Args& a, BwdSmem<IO, KIG>& s, const Ctx& C, int t0, bool grad,
                                              IO greg, IO breg, bool leave_newest = false)
 {
-    const int tid = C.tid, dk = a.dk, dv = a.dv;
+    constexpr int R = Cfg<KIG>::ROWS, NC = Cfg<KIG>::COLS;
+    const int tid = C.tid, dk = a.dk, nv = C.nv;
     const int nt = min(kBT, a.T - t0);
     if (tid < 32) s.rg[tid] = gate(to_f(greg), a.logits);
     else if (tid < 64) s.rbeta[tid - 32] = gate(to_f(breg), a.logits);
     if (leave_newest) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
     else cp_async_wait_all();
     __syncthreads();
-    for (int idx = tid; idx < kBT * 64; idx += 256) {
-        const int tt = idx >> 6, i = idx & 63;
+    for (int idx = tid; idx < kBT * R; idx += 256) {
+        const int tt = idx / R, i = idx % R;
         const bool ok = tt < nt;
         s.A[tt][i] = ok ? decay<IO>(s.rg[tt], s.Arow[i], s.Arow2[i]) : 1.f;
         s.Bv[tt][i] = ok && i < dk ? to_f(s.rb[tt][i]) : 0.f;
         s.Cv[tt][i] = grad && ok && i < dk ? to_f(s.rc[tt][i]) : 0.f;
-        s.V[tt][i] = ok && i < dv ? to_f(s.rv[tt][i]) : 0.f;
-        s.DO[tt][i] = grad && ok && i < dv ? to_f(s.rdo[tt][i]) : 0.f;
+        if (R == NC) {   // rows and columns in one pass
+            s.V[tt][i] = ok && i < nv ? to_f(s.rv[tt][i]) : 0.f;
+            s.DO[tt][i] = grad && ok && i < nv ? to_f(s.rdo[tt][i]) : 0.f;
+        }
     }
+    if (R != NC)
+        for (int idx = tid; idx < kBT * NC; idx += 256) {
+            const int tt = idx / NC, i = idx % NC;
+            const bool ok = tt < nt;
+            s.V[tt][i] = ok && i < nv ? to_f(s.rv[tt][i]) : 0.f;
+            s.DO[tt][i] = grad && ok && i < nv ? to_f(s.rdo[tt][i]) : 0.f;
+        }
     if (tid < kBT) {
         const bool ok = tid < nt;
         s.g[tid] = ok ? s.rg[tid] : 0.f;
@@ -139,7 +173,7 @@ __device__ __forceinline__ void finish_block(const Args& a, BwdSmem<IO>& s, cons
 
 // one forward step with the row reduction h'^T b (delta); optionally caches
 // x and v - h'^T b for the window recompute and the adjoint
-template <bool DELTA, bool CACHE>
+template <bool DELTA, bool CACHE, int KIG>
 __device__ __forceinline__ void fwd_full(float2 (&S)[2][4], const float* A, const float* Bv, const float* V, float be,
                                          float* X, float* VR, const Ctx& C)
 {
@@ -165,7 +199,7 @@ __device__ __forceinline__ void fwd_full(float2 (&S)[2][4], const float* A, cons
         }
         float q0 = r0.x + r0.y, q1 = r1.x + r1.y;
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
+        for (int o = 1; o < KIG; o <<= 1) {
             q0 += __shfl_xor_sync(kFull, q0, o);
             q1 += __shfl_xor_sync(kFull, q1, o);
         }
@@ -208,9 +242,9 @@ __device__ __forceinline__ void fwd_cached(const float2 (&Si)[2][4], float2 (&So
 }
 
 // Sum four packed row pairs over the four column-pair lanes jl of a row
-// group (lanes ig, ig+8, ig+16, ig+24).  Pair p of lane (jl) holds rows
-// 2 (p ^ m2) of the group with m2 = 2 (jl & 1) + (jl >> 1); the result holds
-// rows 2 m2, 2 m2 + 1.
+// group (KIG = 8: lanes ig, ig+8, ig+16, ig+24).  Pair p of lane (jl) holds
+// rows 2 (p ^ m2) of the group with m2 = 2 (jl & 1) + (jl >> 1); the result
+// holds rows 2 m2, 2 m2 + 1.
 __device__ __forceinline__ float2 colsum_pairs(const float2 (&x)[4])
 {
     float2 y0, y1;
@@ -224,33 +258,58 @@ __device__ __forceinline__ float2 colsum_pairs(const float2 (&x)[4])
     return z;
 }
 
-template <typename IO, bool DELTA>
-__global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, bool vec)
+// The same over the two column-pair lanes of a row group at KIG = 16 (lanes
+// ig, ig+16), with m2 = 2 jl: lane jl ends with rows 4 jl .. 4 jl + 3.
+__device__ __forceinline__ float4 colsum_pairs2(const float2 (&x)[4])
 {
+    float4 z;
+    z.x = x[0].x + __shfl_xor_sync(kFull, x[2].x, 16);
+    z.y = x[0].y + __shfl_xor_sync(kFull, x[2].y, 16);
+    z.z = x[1].x + __shfl_xor_sync(kFull, x[3].x, 16);
+    z.w = x[1].y + __shfl_xor_sync(kFull, x[3].y, 16);
+    return z;
+}
+
+// the warp's sum over its columns of four packed row pairs, into a row vector
+template <int KIG>
+__device__ __forceinline__ void colsum_store(const float2 (&x)[4], float* rowvec, const Ctx& C)
+{
+    if (KIG == 8) *reinterpret_cast<float2*>(rowvec + 8 * C.ig + 2 * C.m2) = colsum_pairs(x);
+    else *reinterpret_cast<float4*>(rowvec + 8 * C.ig + 4 * C.jl) = colsum_pairs2(x);
+}
+
+template <typename IO, bool DELTA, int KIG>
+__global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, Outs out, bool vec)
+{
+    constexpr int R = Cfg<KIG>::ROWS, NJ = Cfg<KIG>::NJ, NC = Cfg<KIG>::COLS, PBUF = Cfg<KIG>::PBUF;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    BwdSmem<IO>& s = *reinterpret_cast<BwdSmem<IO>*>(smem_raw);
+    BwdSmem<IO, KIG>& s = *reinterpret_cast<BwdSmem<IO, KIG>*>(smem_raw);
     Ctx C;
     C.tid = threadIdx.x;
     C.lane = C.tid & 31;
     C.w = C.tid >> 5;
-    C.ig = C.lane & 7;
-    C.jl = C.lane >> 3;
-    C.j0 = 8 * C.w + 2 * C.jl;
-    C.m2 = 2 * (C.jl & 1) + (C.jl >> 1);
+    C.ig = C.lane % KIG;
+    C.jl = C.lane / KIG;
+    C.j0 = 2 * NJ * C.w + 2 * C.jl;
+    C.m2 = KIG == 8 ? 2 * (C.jl & 1) + (C.jl >> 1) : 2 * C.jl;
 #pragma unroll
     for (int p = 0; p < 4; p++) C.roff[p] = 8 * C.ig + 2 * (p ^ C.m2);
     C.u = blockIdx.x;
     C.bb = C.u / a.H;
     C.h = C.u % a.H;
+    C.jc0 = NC * (int)blockIdx.y;
+    C.nv = min(NC, a.dv - C.jc0);
     const int tid = C.tid, lane = C.lane, w = C.w;
-    const int dk = a.dk, dv = a.dv, T = a.T, H = a.H;
+    const int dk = a.dk, dv = a.dv, T = a.T, H = a.H, nv = C.nv;
     const int nblk = (T + kBT - 1) / kBT;
+    const size_t cta = (size_t)C.u * gridDim.y + blockIdx.y;   // this CTA's workspace slot
     constexpr int kSnapPerBlk = kBT / kSub;
-    float2* gsnap = reinterpret_cast<float2*>((unsigned char*)a.ws + L.snap_off) + (size_t)C.u * nblk * kSnapPerBlk * 2048;
-    float* gxvr = reinterpret_cast<float*>((unsigned char*)a.ws + L.xvr_off) + (size_t)C.u * nblk * kBT * 128;
-    float* dA_part = reinterpret_cast<float*>((unsigned char*)a.ws + L.dalog_off) + (size_t)C.u * dk;
+    float2* gsnap = reinterpret_cast<float2*>((unsigned char*)a.ws + L.snap_off) + cta * nblk * kSnapPerBlk * 2048;
+    float* gxvr = reinterpret_cast<float*>((unsigned char*)a.ws + L.xvr_off) + cta * nblk * kBT * 2 * NC;
+    float* dA_part = reinterpret_cast<float*>((unsigned char*)a.ws + L.dalog_off) + cta * dk;
+    const size_t slab_tok = (size_t)blockIdx.y * a.B * T * H;   // offset of this slab's partials, in tokens
 
-    if (tid < 64) {
+    if (tid < R) {
         const float Ai = tid < dk ? -expf(a.A_log[C.h * dk + tid]) : 0.f;
         s.Arow[tid] = Ai;
         s.Arow2[tid] = Ai * 1.4426950408889634f;
@@ -264,9 +323,9 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
             for (int p = 0; p < 4; p++) {
                 const int i0 = C.roff[p], j = C.j0 + c;
                 float x0 = 0.f, x1 = 0.f;
-                if (src && j < dv) {
-                    if (i0 < dk) x0 = src[((size_t)C.u * dk + i0) * dv + j];
-                    if (i0 + 1 < dk) x1 = src[((size_t)C.u * dk + i0 + 1) * dv + j];
+                if (src && j < nv) {
+                    if (i0 < dk) x0 = src[((size_t)C.u * dk + i0) * dv + C.jc0 + j];
+                    if (i0 + 1 < dk) x1 = src[((size_t)C.u * dk + i0 + 1) * dv + C.jc0 + j];
                 }
                 S[c][p] = f2(x0, x1);
             }
@@ -278,21 +337,21 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
     // ---------------- forward sweep: state entering every block ----------------
     IO greg = from_f<IO>(0.f), breg = from_f<IO>(0.f);
     __syncthreads();  // Arow
-    issue_block<IO, DELTA>(a, s, C, 0, false, vec, greg, breg);
+    issue_block<IO, DELTA, KIG>(a, s, C, 0, false, vec, greg, breg);
     for (int n = 0; n < nblk; n++) {
-        finish_block<IO, DELTA>(a, s, C, n * kBT, false, greg, breg);
-        if (n + 1 < nblk) issue_block<IO, DELTA>(a, s, C, (n + 1) * kBT, false, vec, greg, breg);
-        else issue_block<IO, DELTA>(a, s, C, n * kBT, true, vec, greg, breg);  // first block of the reverse walk
+        finish_block<IO, DELTA, KIG>(a, s, C, n * kBT, false, greg, breg);
+        if (n + 1 < nblk) issue_block<IO, DELTA, KIG>(a, s, C, (n + 1) * kBT, false, vec, greg, breg);
+        else issue_block<IO, DELTA, KIG>(a, s, C, n * kBT, true, vec, greg, breg);  // first block of the reverse walk
         float2* snap_n = gsnap + (size_t)n * kSnapPerBlk * 2048;
-        float* xvr_n = gxvr + (size_t)n * kBT * 128;
+        float* xvr_n = gxvr + (size_t)n * kBT * 2 * NC;
 #pragma unroll 1
         for (int tt = 0; tt < kBT; tt++) {
             if ((tt & (kSub - 1)) == 0) {
 #pragma unroll
                 for (int q = 0; q < 8; q++) snap_n[((tt / kSub) * 8 + q) * 256 + tid] = S[q >> 2][q & 3];
             }
-            fwd_full<DELTA, DELTA>(S, s.A[tt], s.Bv[tt], s.V[tt], s.beta[tt], xvr_n + tt * 64,
-                                   xvr_n + kBT * 64 + tt * 64, C);
+            fwd_full<DELTA, DELTA, KIG>(S, s.A[tt], s.Bv[tt], s.V[tt], s.beta[tt], xvr_n + tt * NC,
+                                        xvr_n + kBT * NC + tt * NC, C);
         }
     }
 
@@ -308,7 +367,6 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
         Ap[p] = ld2(&s.Arow[C.roff[p]]);
         dA_acc[p] = f2(0.f, 0.f);
     }
-    const int ri = tid & 63, rk = tid >> 6;  // reduction-phase role: row ri, window token rk
     int wbuf = 0;
 
     // Snapshots and x cache of block n come back from the workspace: the x cache one block ahead into the other
@@ -320,9 +378,9 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
     };
     auto fetch_xv = [&](int n) {
         if (!DELTA) return;
-        const float4* sx = reinterpret_cast<const float4*>(gxvr + (size_t)n * kBT * 128);
+        const float4* sx = reinterpret_cast<const float4*>(gxvr + (size_t)n * kBT * 2 * NC);
         float4* dx = reinterpret_cast<float4*>(&s.XV[n & 1][0][0][0]);
-        for (int idx = tid; idx < kBT * 128 / 4; idx += 256) cp_async16(dx + idx, sx + idx);
+        for (int idx = tid; idx < kBT * 2 * NC / 4; idx += 256) cp_async16(dx + idx, sx + idx);
     };
     for (int sb = 0; sb < kSnapPerBlk; sb++) fetch_snap(nblk - 1, sb);
     fetch_xv(nblk - 1);
@@ -332,9 +390,9 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
     for (int n = nblk - 1; n >= 0; n--) {
         const int t0 = n * kBT;
         // waits for this block's inputs, x cache and snapshots but the last (slot 0, needed from window 1 on)
-        finish_block<IO, DELTA>(a, s, C, t0, true, greg, breg, n < nblk - 1);
+        finish_block<IO, DELTA, KIG>(a, s, C, t0, true, greg, breg, n < nblk - 1);
         if (n > 0) {
-            issue_block<IO, DELTA>(a, s, C, t0 - kBT, true, vec, greg, breg);
+            issue_block<IO, DELTA, KIG>(a, s, C, t0 - kBT, true, vec, greg, breg);
             fetch_xv(n - 1);
             cp_async_commit();
         }
@@ -344,6 +402,7 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
 #pragma unroll 1
         for (int wi = kBT / kWin - 1; wi >= 0; wi--) {
             const int tw = kWin * wi;  // first token of the window inside the block
+            const int pb = PBUF == 2 ? wbuf : 0;
             float2 W[kWin + 1][2][4];
             {
                 const int sb = tw / kSub;
@@ -355,7 +414,7 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
                     for (int k = 0; k < kWin; k++) {
                         const int tt = sb * kSub + k;
                         float2 Tm[2][4];
-                        fwd_cached(W[0], Tm, s.A[tt], s.Bv[tt], Xsrc + tt * 64, C);
+                        fwd_cached(W[0], Tm, s.A[tt], s.Bv[tt], Xsrc + tt * NC, C);
 #pragma unroll
                         for (int q = 0; q < 8; q++) W[0][q >> 2][q & 3] = Tm[q >> 2][q & 3];
                     }
@@ -363,7 +422,7 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
 #pragma unroll
                 for (int k = 0; k < kWin; k++) {
                     const int tt = tw + k;
-                    fwd_cached(W[k], W[k + 1], s.A[tt], s.Bv[tt], Xsrc + tt * 64, C);
+                    fwd_cached(W[k], W[k + 1], s.A[tt], s.Bv[tt], Xsrc + tt * NC, C);
                 }
             }
 #pragma unroll
@@ -396,12 +455,12 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
                     du0 = r0.x + r0.y;
                     du1 = r1.x + r1.y;
 #pragma unroll
-                    for (int o = 1; o < 8; o <<= 1) {
+                    for (int o = 1; o < KIG; o <<= 1) {
                         du0 += __shfl_xor_sync(kFull, du0, o);
                         du1 += __shfl_xor_sync(kFull, du1, o);
                     }
                 }
-                const float2 x2 = ld2(Xsrc + tt * 64 + C.j0);
+                const float2 x2 = ld2(Xsrc + tt * NC + C.j0);
                 const float2 xx0 = f2(x2.x, x2.x), xx1 = f2(x2.y, x2.y);
                 float2 pdb[4];
                 float pbeta = 0.f, dv0, dv1;
@@ -409,7 +468,7 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
                 float2 gq = f2(0.f, 0.f);
                 if (DELTA) {
                     const float be = s.beta[tt];
-                    const float2 vr2 = ld2(VRsrc + tt * 64 + C.j0);
+                    const float2 vr2 = ld2(VRsrc + tt * NC + C.j0);
                     const float dr0 = -be * du0, dr1 = -be * du1;
                     dv0 = be * du0;
                     dv1 = be * du1;
@@ -440,15 +499,14 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
                         dS[1][p] = mul2(dS[1][p], a2[p]);
                     }
                 }
-                const int rofs = 8 * C.ig + 2 * C.m2;
-                *reinterpret_cast<float2*>(&s.part[wbuf][w][k][0][rofs]) = colsum_pairs(pdc);
-                *reinterpret_cast<float2*>(&s.part[wbuf][w][k][1][rofs]) = colsum_pairs(pdb);
+                colsum_store<KIG>(pdc, s.part[pb][w][k][0], C);
+                colsum_store<KIG>(pdb, s.part[pb][w][k][1], C);
                 float gs = gq.x + gq.y;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) gs += __shfl_xor_sync(kFull, gs, o);
                 if (DELTA) {
-                    pbeta += __shfl_xor_sync(kFull, pbeta, 8);
-                    pbeta += __shfl_xor_sync(kFull, pbeta, 16);
+#pragma unroll
+                    for (int o = KIG; o < 32; o <<= 1) pbeta += __shfl_xor_sync(kFull, pbeta, o);
                 }
                 if (lane == 0) {
                     s.gpart[wbuf][w][k] = gs;
@@ -465,20 +523,29 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
 
             // ---- reduction phase: thread (row ri, token rk) of this window ----
             {
-                const int tt = tw + rk, t = t0 + tt;
-                const bool live = t < T;
-                float dc = 0.f, db = 0.f;
 #pragma unroll
-                for (int ww = 0; ww < 8; ww++) {
-                    dc += s.part[wbuf][ww][rk][0][ri];
-                    db += s.part[wbuf][ww][rk][1][ri];
+                for (int e0 = 0; e0 < kWin * R; e0 += 256) {   // one pass at 64 rows, two at 128
+                    const int e = e0 + tid, ri = e % R, rk = e / R;
+                    const int tt = tw + rk, t = t0 + tt;
+                    const bool live = t < T;
+                    float dc = 0.f, db = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < 8; ww++) {
+                        dc += s.part[pb][ww][rk][0][ri];
+                        db += s.part[pb][ww][rk][1][ri];
+                    }
+                    const size_t row = ((size_t)C.bb * T + t) * H + C.h;
+                    if (live && ri < dk) {
+                        if (out.db) {
+                            out.dc[(slab_tok + row) * dk + ri] = dc;
+                            out.db[(slab_tok + row) * dk + ri] = db;
+                        } else {
+                            ((IO*)a.dc)[row * dk + ri] = from_f<IO>(dc);
+                            ((IO*)a.db)[row * dk + ri] = from_f<IO>(db);
+                        }
+                    }
+                    if (live && ri < nv) ((IO*)a.dv_)[row * dv + C.jc0 + ri] = from_f<IO>(s.dvb[wbuf][rk][ri]);
                 }
-                const size_t row = ((size_t)C.bb * T + t) * H + C.h;
-                if (live && ri < dk) {
-                    ((IO*)a.dc)[row * dk + ri] = from_f<IO>(dc);
-                    ((IO*)a.db)[row * dk + ri] = from_f<IO>(db);
-                }
-                if (live && ri < dv) ((IO*)a.dv_)[row * dv + ri] = from_f<IO>(s.dvb[wbuf][rk][ri]);
                 if (tid < kWin && t0 + tw + tid < T) {
                     const size_t rowk = ((size_t)C.bb * T + t0 + tw + tid) * H + C.h;
                     float sg = 0.f, sb = 0.f;
@@ -488,14 +555,20 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
                         sb += s.bpart[wbuf][ww][tid];
                     }
                     if (a.logits) {   // through the sigmoid: d sigma(z) / dz = sigma (1 - sigma)
-                        const float gv = s.g[tw + ri], bv = s.beta[tw + ri];
+                        const float gv = s.g[tw + tid], bv = s.beta[tw + tid];
                         sg *= gv * (1.f - gv);
                         sb *= bv * (1.f - bv);
                     }
-                    ((IO*)a.dg)[rowk] = from_f<IO>(sg);
-                    if (DELTA) ((IO*)a.dbeta)[rowk] = from_f<IO>(sb);
+                    if (out.dg) {
+                        out.dg[slab_tok + rowk] = sg;
+                        if (DELTA) out.dbeta[slab_tok + rowk] = sb;
+                    } else {
+                        ((IO*)a.dg)[rowk] = from_f<IO>(sg);
+                        if (DELTA) ((IO*)a.dbeta)[rowk] = from_f<IO>(sb);
+                    }
                 }
             }
+            if (PBUF == 1) __syncthreads();   // the single partial buffer is read out before the next window
             wbuf ^= 1;
         }
     }
@@ -505,51 +578,84 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
 #pragma unroll
             for (int p = 0; p < 4; p++) {
                 const int i0 = C.roff[p], j = C.j0 + c;
-                if (j < dv) {
-                    if (i0 < dk) a.dh0[((size_t)C.u * dk + i0) * dv + j] = dS[c][p].x;
-                    if (i0 + 1 < dk) a.dh0[((size_t)C.u * dk + i0 + 1) * dv + j] = dS[c][p].y;
+                if (j < nv) {
+                    if (i0 < dk) a.dh0[((size_t)C.u * dk + i0) * dv + C.jc0 + j] = dS[c][p].x;
+                    if (i0 + 1 < dk) a.dh0[((size_t)C.u * dk + i0 + 1) * dv + C.jc0 + j] = dS[c][p].y;
                 }
             }
     }
     // dA_log partial of this unit: A_i sum_t g_t sum_j q_ij
     {
-        const float2 z = colsum_pairs(dA_acc);
-        *reinterpret_cast<float2*>(&s.red[w][8 * C.ig + 2 * C.m2]) = z;
+        colsum_store<KIG>(dA_acc, s.red[w], C);
         __syncthreads();
-        if (tid < dk) {
+        for (int i = tid; i < dk; i += 256) {
             float acc = 0.f;
 #pragma unroll
-            for (int ww = 0; ww < 8; ww++) acc += s.red[ww][tid];
-            dA_part[tid] = acc * s.Arow[tid];
+            for (int ww = 0; ww < 8; ww++) acc += s.red[ww][i];
+            dA_part[i] = acc * s.Arow[i];
         }
     }
 }
 
-// dA_log[h, i] = sum_b partial[b, h, i]  (fixed order, deterministic)
-__global__ void reduce_dalog_kernel(const float* part, float* dA_log, int B, int H, int dk)
+// dA_log[h, i] = sum_b sum_slab partial[b, h, slab, i]  (fixed order, deterministic)
+__global__ void reduce_dalog_kernel(const float* part, float* dA_log, int B, int H, int dk, int nslab)
 {
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= H * dk) return;
     const int h = idx / dk, i = idx % dk;
     float acc = 0.f;
-    for (int b = 0; b < B; b++) acc += part[((size_t)b * H + h) * dk + i];
+    for (int b = 0; b < B; b++)
+        for (int sl = 0; sl < nslab; sl++) acc += part[(((size_t)b * H + h) * nslab + sl) * dk + i];
     dA_log[idx] = acc;
+}
+
+// out[i] = sum_slab part[slab][i], slabs in order (deterministic)
+template <typename IO>
+__global__ void reduce_slabs_kernel(const float* part, IO* outp, size_t n, int nslab)
+{
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        float acc = part[i];
+        for (int sl = 1; sl < nslab; sl++) acc += part[(size_t)sl * n + i];
+        outp[i] = from_f<IO>(acc);
+    }
 }
 
 static bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
-template <typename IO, bool DELTA>
-cudaError_t launch_t(const Args& a, const WsLayout& L, cudaStream_t st)
+template <typename IO, bool DELTA, int KIG>
+cudaError_t launch_t(const Args& a, const WsLayout& L, int nslab, cudaStream_t st)
 {
-    const size_t smem = sizeof(BwdSmem<IO>);
-    cudaError_t e = cudaFuncSetAttribute(serial_bwd_kernel<IO, DELTA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    const size_t smem = sizeof(BwdSmem<IO, KIG>);
+    cudaError_t e = cudaFuncSetAttribute(serial_bwd_kernel<IO, DELTA, KIG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const size_t sz = sizeof(IO);
     const bool vec = (a.dk * sz) % 16 == 0 && (a.dv * sz) % 16 == 0 && al16(a.b) && al16(a.c) && al16(a.v) &&
                      al16(a.dO);
-    serial_bwd_kernel<IO, DELTA><<<a.B * a.H, 256, smem, st>>>(a, L, vec);
+    Outs out{nullptr, nullptr, nullptr, nullptr};
+    const size_t ntok = (size_t)a.B * a.T * a.H;
+    if (nslab > 1) {
+        unsigned char* w = (unsigned char*)a.ws + L.slab_off;
+        out.db = reinterpret_cast<float*>(w);
+        out.dc = out.db + nslab * ntok * a.dk;
+        out.dg = out.dc + nslab * ntok * a.dk;
+        out.dbeta = out.dg + nslab * ntok;
+    }
+    serial_bwd_kernel<IO, DELTA, KIG><<<dim3(a.B * a.H, nslab), 256, smem, st>>>(a, L, out, vec);
+    if ((e = cudaGetLastError()) != cudaSuccess || nslab == 1) return e;
+    const int blocks = 4 * 152;
+    reduce_slabs_kernel<IO><<<blocks, 256, 0, st>>>(out.db, (IO*)a.db, ntok * a.dk, nslab);
+    reduce_slabs_kernel<IO><<<blocks, 256, 0, st>>>(out.dc, (IO*)a.dc, ntok * a.dk, nslab);
+    reduce_slabs_kernel<IO><<<blocks, 256, 0, st>>>(out.dg, (IO*)a.dg, ntok, nslab);
+    if (DELTA) reduce_slabs_kernel<IO><<<blocks, 256, 0, st>>>(out.dbeta, (IO*)a.dbeta, ntok, nslab);
     return cudaGetLastError();
+}
+
+template <typename IO, bool DELTA>
+cudaError_t launch_rows(const Args& a, const WsLayout& L, cudaStream_t st)
+{
+    const int nslab = bwd_slabs(a.dk, a.dv);
+    return a.dk <= 64 ? launch_t<IO, DELTA, 8>(a, L, nslab, st) : launch_t<IO, DELTA, 16>(a, L, nslab, st);
 }
 
 }  // namespace
@@ -560,13 +666,14 @@ cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st)
     const WsLayout L = ws_layout_bwd_core(sh);
     cudaError_t e;
     if (a.io == GDN_BF16)
-        e = a.mode == GDN_DELTA ? launch_t<__nv_bfloat16, true>(a, L, st) : launch_t<__nv_bfloat16, false>(a, L, st);
+        e = a.mode == GDN_DELTA ? launch_rows<__nv_bfloat16, true>(a, L, st) : launch_rows<__nv_bfloat16, false>(a, L, st);
     else
-        e = a.mode == GDN_DELTA ? launch_t<float, true>(a, L, st) : launch_t<float, false>(a, L, st);
+        e = a.mode == GDN_DELTA ? launch_rows<float, true>(a, L, st) : launch_rows<float, false>(a, L, st);
     if (e != cudaSuccess) return e;
     const int n = a.H * a.dk;
     reduce_dalog_kernel<<<(n + 127) / 128, 128, 0, st>>>(
-        reinterpret_cast<const float*>((const unsigned char*)a.ws + L.dalog_off), a.dA_log, a.B, a.H, a.dk);
+        reinterpret_cast<const float*>((const unsigned char*)a.ws + L.dalog_off), a.dA_log, a.B, a.H, a.dk,
+        bwd_slabs(a.dk, a.dv));
     return cudaGetLastError();
 }
 

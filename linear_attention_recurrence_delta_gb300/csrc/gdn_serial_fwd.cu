@@ -8,11 +8,12 @@
 // alpha_t = exp(g_t A), A = -exp(A_log).
 //
 // Columns j of the state never mix (the erase term acts on rows), so a CTA
-// owns 32 columns of one (batch, head) unit and needs no other CTA.  Thread
-// layout: warp w owns columns 8w..8w+7 of the CTA's 32; lane = 4 jl + ig
-// holds the 16 consecutive rows 16 ig .. 16 ig + 15 of column 8w + jl as 8
-// packed pairs.  A sum over rows is 8 packed products in-thread plus two
-// shuffles.  Inputs stream through shared memory in blocks of 32 tokens: the
+// owns a slab of columns of one (batch, head) unit and needs no other CTA.
+// Thread layout: LPC lanes share a column, each holding 16 consecutive rows
+// as 8 packed pairs (LPC = 4 covers d_k <= 64 with 32 columns per CTA, LPC = 8
+// covers d_k <= 128 with 16); warp w owns columns (32 / LPC) w + jl, and
+// lane = LPC jl + ig holds rows 16 ig .. 16 ig + 15.  A sum over rows is 8
+// packed products in-thread plus log2(LPC) shuffles.  Inputs stream through shared memory in blocks of 32 tokens: the
 // next block's raw bytes arrive by cp.async while the current one computes.
 #include "gdn_internal.h"
 #include "serial_common.cuh"
@@ -23,19 +24,26 @@ namespace {
 using namespace rec;
 
 constexpr int kTB = 32;    // tokens per staged block
-constexpr int kCols = 32;  // state columns per CTA
 
-template <typename IO>
+template <int LPC>
+struct FCfg {
+    static constexpr int ROWS = 16 * LPC;          // state rows covered
+    static constexpr int PAD = ROWS + ROWS / 4;    // padded row-vector length (see prow)
+    static constexpr int COLS = 128 / LPC;         // state columns per CTA (4 warps)
+};
+
+template <typename IO, int LPC>
 struct FwdSmem {
-    float A[kTB][kRowPad];   // alpha_t per state row
-    float Bv[kTB][kRowPad];  // b_t
-    float Cv[kTB][kRowPad];  // c_t
-    float V[kTB][kCols];     // v_t on this CTA's columns
-    float O[kTB][kCols];     // o_t staging for coalesced stores
+    static constexpr int R = FCfg<LPC>::ROWS, NC = FCfg<LPC>::COLS, PAD = FCfg<LPC>::PAD;
+    float A[kTB][PAD];       // alpha_t per state row
+    float Bv[kTB][PAD];      // b_t
+    float Cv[kTB][PAD];      // c_t
+    float V[kTB][NC];        // v_t on this CTA's columns
+    float O[kTB][NC];        // o_t staging for coalesced stores
     float beta[kTB];
-    float Arow[64];          // A = -exp(A_log) of this head
+    float Arow[R];           // A = -exp(A_log) of this head
     float rg[kTB], rbeta[kTB];
-    IO rb[kTB][64], rc[kTB][64], rv[kTB][kCols];  // raw bytes of the next block
+    IO rb[kTB][R], rc[kTB][R], rv[kTB][NC];  // raw bytes of the next block
 };
 
 struct Unit {
@@ -44,10 +52,11 @@ struct Unit {
 
 // Start fetching block [t0, t0+nt): row vectors by cp.async (or plain loads
 // when rows are not 16-byte aligned), g and beta into registers.
-template <typename IO, bool DELTA>
-__device__ __forceinline__ void issue_block(const Args& a, FwdSmem<IO>& s, const Unit& U, int t0, int nt, bool vec,
-                                            IO& greg, IO& breg)
+template <typename IO, bool DELTA, int LPC>
+__device__ __forceinline__ void issue_block(const Args& a, FwdSmem<IO, LPC>& s, const Unit& U, int t0, int nt,
+                                            bool vec, IO& greg, IO& breg)
 {
+    constexpr int R = FCfg<LPC>::ROWS;
     const int tid = threadIdx.x, dk = a.dk, dv = a.dv, T = a.T, H = a.H;
     const IO* bk = (const IO*)a.b;
     const IO* c = (const IO*)a.c;
@@ -64,8 +73,8 @@ __device__ __forceinline__ void issue_block(const Args& a, FwdSmem<IO>& s, const
         }
         cp_async_commit();
     } else {
-        for (int idx = tid; idx < nt * 64; idx += blockDim.x) {
-            const int tt = idx >> 6, i = idx & 63;
+        for (int idx = tid; idx < nt * R; idx += blockDim.x) {
+            const int tt = idx / R, i = idx % R;
             const size_t row = ((size_t)U.bb * T + t0 + tt) * H + U.h;
             if (i < dk) {
                 s.rb[tt][i] = bk[row * dk + i];
@@ -81,12 +90,13 @@ __device__ __forceinline__ void issue_block(const Args& a, FwdSmem<IO>& s, const
 }
 
 // raw block -> fp32 staged arrays (alpha computed here, once per row and token)
-template <typename IO, bool DELTA>
-__device__ __forceinline__ void convert_block(const Args& a, FwdSmem<IO>& s, const Unit& U, int nt)
+template <typename IO, bool DELTA, int LPC>
+__device__ __forceinline__ void convert_block(const Args& a, FwdSmem<IO, LPC>& s, const Unit& U, int nt)
 {
+    constexpr int R = FCfg<LPC>::ROWS, NC = FCfg<LPC>::COLS;
     const int tid = threadIdx.x, dk = a.dk;
-    for (int idx = tid; idx < nt * 64; idx += blockDim.x) {
-        const int tt = idx >> 6, i = idx & 63;
+    for (int idx = tid; idx < nt * R; idx += blockDim.x) {
+        const int tt = idx / R, i = idx % R;
         float xa = 0.f, xb = 0.f, xc = 0.f;
         if (i < dk) {
             xa = expf(s.rg[tt] * s.Arow[i]);
@@ -98,30 +108,31 @@ __device__ __forceinline__ void convert_block(const Args& a, FwdSmem<IO>& s, con
         s.Bv[tt][p] = xb;
         s.Cv[tt][p] = xc;
     }
-    for (int idx = tid; idx < nt * kCols; idx += blockDim.x) {
-        const int tt = idx / kCols, q = idx - tt * kCols;
+    for (int idx = tid; idx < nt * NC; idx += blockDim.x) {
+        const int tt = idx / NC, q = idx - tt * NC;
         s.V[tt][q] = q < U.ncols ? to_f(s.rv[tt][q]) : 0.f;
     }
     if (tid < nt) s.beta[tid] = DELTA ? s.rbeta[tid] : 0.f;
 }
 
-template <typename IO, bool DELTA>
+template <typename IO, bool DELTA, int LPC>
 __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
 {
+    constexpr int R = FCfg<LPC>::ROWS, NC = FCfg<LPC>::COLS;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    FwdSmem<IO>& s = *reinterpret_cast<FwdSmem<IO>*>(smem_raw);
+    FwdSmem<IO, LPC>& s = *reinterpret_cast<FwdSmem<IO, LPC>*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int ig = lane & 3, jl = lane >> 2, cl = 8 * w + jl;
+    const int ig = lane % LPC, jl = lane / LPC, cl = (32 / LPC) * w + jl;
     Unit U;
     U.u = blockIdx.y;
     U.bb = U.u / a.H;
     U.h = U.u % a.H;
-    U.jc0 = blockIdx.x * kCols;
-    U.ncols = min(kCols, a.dv - U.jc0);
+    U.jc0 = blockIdx.x * NC;
+    U.ncols = min(NC, a.dv - U.jc0);
     const int j = U.jc0 + cl, dk = a.dk, dv = a.dv, T = a.T, H = a.H;
     const int nblk = (T + kTB - 1) / kTB;
 
-    if (tid < 64) s.Arow[tid] = tid < dk ? -expf(a.A_log[U.h * dk + tid]) : 0.f;
+    for (int i = tid; i < R; i += 128) s.Arow[i] = i < dk ? -expf(a.A_log[U.h * dk + i]) : 0.f;
 
     // state: rows 16 ig + 2p, 16 ig + 2p + 1 of column j in h[p]
     float2 h[8];
@@ -137,14 +148,14 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
     }
 
     IO greg = from_f<IO>(0.f), breg = from_f<IO>(0.f);
-    issue_block<IO, DELTA>(a, s, U, 0, min(kTB, T), vec, greg, breg);
+    issue_block<IO, DELTA, LPC>(a, s, U, 0, min(kTB, T), vec, greg, breg);
     if (tid < 32) s.rg[tid] = gate(to_f(greg), a.logits);
     else if (tid < 64) s.rbeta[tid - 32] = gate(to_f(breg), a.logits);
     cp_async_wait_all();
     __syncthreads();
-    convert_block<IO, DELTA>(a, s, U, min(kTB, T));
+    convert_block<IO, DELTA, LPC>(a, s, U, min(kTB, T));
     __syncthreads();
-    if (nblk > 1) issue_block<IO, DELTA>(a, s, U, kTB, min(kTB, T - kTB), vec, greg, breg);
+    if (nblk > 1) issue_block<IO, DELTA, LPC>(a, s, U, kTB, min(kTB, T - kTB), vec, greg, breg);
 
     IO* o = (IO*)a.o;
     for (int n = 0; n < nblk; n++) {
@@ -160,8 +171,8 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
             float x;
             if (DELTA) {
                 float r = dot8x2(hp, bv);
-                r += __shfl_xor_sync(kFull, r, 1);
-                r += __shfl_xor_sync(kFull, r, 2);
+#pragma unroll
+                for (int o = 1; o < LPC; o <<= 1) r += __shfl_xor_sync(kFull, r, o);
                 x = s.beta[tt] * (s.V[tt][cl] - r);
             } else {
                 x = s.V[tt][cl];
@@ -172,8 +183,8 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
             float2 cv[8];
             ld_rows16(&s.Cv[tt][20 * ig], cv);
             float ov = dot8x2(h, cv);
-            ov += __shfl_xor_sync(kFull, ov, 1);
-            ov += __shfl_xor_sync(kFull, ov, 2);
+#pragma unroll
+            for (int o = 1; o < LPC; o <<= 1) ov += __shfl_xor_sync(kFull, ov, o);
             if (ig == 0) s.O[tt][cl] = ov;
         }
         __syncthreads();
@@ -186,10 +197,10 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
             else if (tid < 64) s.rbeta[tid - 32] = gate(to_f(breg), a.logits);
             cp_async_wait_all();
             __syncthreads();
-            convert_block<IO, DELTA>(a, s, U, min(kTB, T - t0 - kTB));
+            convert_block<IO, DELTA, LPC>(a, s, U, min(kTB, T - t0 - kTB));
             __syncthreads();
             if (n + 2 < nblk)
-                issue_block<IO, DELTA>(a, s, U, t0 + 2 * kTB, min(kTB, T - t0 - 2 * kTB), vec, greg, breg);
+                issue_block<IO, DELTA, LPC>(a, s, U, t0 + 2 * kTB, min(kTB, T - t0 - 2 * kTB), vec, greg, breg);
         }
     }
 
@@ -205,18 +216,25 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
 
 static bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
-template <typename IO, bool DELTA>
-cudaError_t launch_t(const Args& a, cudaStream_t st)
+template <typename IO, bool DELTA, int LPC>
+cudaError_t launch_lpc(const Args& a, cudaStream_t st)
 {
-    const size_t smem = sizeof(FwdSmem<IO>);
-    cudaError_t e = cudaFuncSetAttribute(serial_fwd_kernel<IO, DELTA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    const size_t smem = sizeof(FwdSmem<IO, LPC>);
+    cudaError_t e = cudaFuncSetAttribute(serial_fwd_kernel<IO, DELTA, LPC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const size_t sz = sizeof(IO);
     const bool vec = (a.dk * sz) % 16 == 0 && (a.dv * sz) % 16 == 0 && al16(a.b) && al16(a.c) && al16(a.v);
-    dim3 grid((a.dv + kCols - 1) / kCols, a.B * a.H);
-    serial_fwd_kernel<IO, DELTA><<<grid, 128, smem, st>>>(a, vec);
+    constexpr int NC = FCfg<LPC>::COLS;
+    dim3 grid((a.dv + NC - 1) / NC, a.B * a.H);
+    serial_fwd_kernel<IO, DELTA, LPC><<<grid, 128, smem, st>>>(a, vec);
     return cudaGetLastError();
+}
+
+template <typename IO, bool DELTA>
+cudaError_t launch_t(const Args& a, cudaStream_t st)
+{
+    return a.dk <= 64 ? launch_lpc<IO, DELTA, 4>(a, st) : launch_lpc<IO, DELTA, 8>(a, st);
 }
 
 }  // namespace

@@ -177,6 +177,8 @@ static void launch_seg_scan(const Args& a, int P, const float* Abuf, const float
 int tsplit_factor(const gdn_shape_t& s, int backward)
 {
     const long units = (long)s.B * s.H;
+    // the segment scan keeps 64 x 64 tiles: wider heads are not split
+    if (s.dk > 64 || s.dv > 64) return 1;
     // forward: three passes (delta) or two (gated) must still pay; backward: two backward passes, the
     // forward passes are cheap beside them
     const int min_p = backward ? 3 : (s.mode == GDN_DELTA ? 4 : 3);

@@ -158,6 +158,10 @@ WORKLOADS = {
     "delta_bf16_8x40x4096x32": Workload(
         "delta_bf16_8x40x4096x32", "delta", "bf16", 8, 40, 4096, 32, 32, seed=8,
         b_dist="l2norm", c_dist="l2norm", notes="added 40-head d = 32 shape"),
+    # added: heads 128 wide (d_k = d_v = 128) at the 8 x 4096 x 16-head batch of the delta workload
+    "delta_bf16_8x16x4096x128": Workload(
+        "delta_bf16_8x16x4096x128", "delta", "bf16", 8, 16, 4096, 128, 128, seed=9,
+        backward=True, b_dist="l2norm", c_dist="l2norm", notes="added 128-wide heads"),
     # added: one decoding step (T = 1) of a large batch, state in and out
     "delta_bf16_decode_512x16x1x64": Workload(
         "delta_bf16_decode_512x16x1x64", "delta", "bf16", 512, 16, 1, 64, 64, seed=7,

@@ -53,7 +53,8 @@ def test_workspace_sizes(lib):
     assert f >= 256 and f % 256 == 0
     assert b > f and b % 256 == 0
     assert gdn.gdn_workspace_bytes(gdn.make_shape(1, 1, 0, 8, 8), 1) >= 256
-    for bad in (gdn.make_shape(0, 1, 8, 8, 8), gdn.make_shape(1, 1, 8, 65, 8), gdn.make_shape(1, 1, 8, 8, 0),
+    for bad in (gdn.make_shape(0, 1, 8, 8, 8), gdn.make_shape(1, 1, 8, 129, 8), gdn.make_shape(1, 1, 8, 8, 0),
+                gdn.make_shape(1, 1, 8, 8, 136, "delta", "bf16"),
                 gdn.make_shape(1, 1, -1, 8, 8), gdn.make_shape(1, 1, 8, 12, 8, "gated", "bf16"),
                 gdn.make_shape(1, 1, 8, 8, 8, 7, "bf16"), gdn.make_shape(1, 1, 8, 8, 8, "gated", 5)):
         assert gdn.gdn_workspace_bytes(bad, 0) == 0
@@ -86,7 +87,7 @@ def test_fwd_rejects_bad_arguments_before_any_device_work(lib):
     assert call_fwd(s, fwd_args(v=FAKE + 2)) == 3                 # misaligned bf16 tensor
     assert call_fwd(s, fwd_args(ws=FAKE + 16)) == 3               # misaligned workspace
     assert call_fwd(gdn.make_shape(2, 2, 64, 12, 16, "gated", "bf16"), fwd_args()) == 2
-    assert call_fwd(gdn.make_shape(2, 2, 64, 16, 72, "gated", "f32"), fwd_args()) == 2
+    assert call_fwd(gdn.make_shape(2, 2, 64, 16, 132, "gated", "f32"), fwd_args()) == 2
     assert call_fwd(gdn.make_shape(0, 2, 64, 16, 16, "gated", "f32"), fwd_args()) == 2
     assert call_fwd(gdn.make_shape(2, 2, 64, 16, 16, 3, "f32"), fwd_args()) == 4
 
@@ -107,6 +108,24 @@ def test_bwd_rejects_bad_arguments_before_any_device_work(lib):
     assert call(ws_bytes=256) == 5
     assert call(dA_log=FAKE + 4) == 3
     assert call(b=FAKE + 2) == 3
+
+
+def test_wide_head_workspace(lib):
+    """Heads up to 128 wide: the forward needs no workspace; the backward's buffers grow with its column slabs
+    (64 value columns per CTA up to d_k = 64, 32 above), and with more than one slab it adds fp32 partial sums
+    of db, dc [slabs, B, T, H, d_k] and dg, dbeta [slabs, B, T, H]."""
+    B, H, T = 2, 4, 256
+    assert gdn.gdn_workspace_bytes(gdn.make_shape(B, H, T, 128, 128, "delta", "bf16"), 0) == 256
+    one = gdn.gdn_workspace_bytes(gdn.make_shape(B, H, T, 64, 64, "delta", "bf16"), 1)
+    two = gdn.gdn_workspace_bytes(gdn.make_shape(B, H, T, 64, 128, "delta", "bf16"), 1)
+    four = gdn.gdn_workspace_bytes(gdn.make_shape(B, H, T, 128, 128, "delta", "bf16"), 1)
+    ntok = B * T * H
+    assert two >= 2 * (one - 256) + 2 * ntok * (2 * 64 + 2) * 4
+    assert four >= 4 * ntok * (2 * 128 + 2) * 4 + 4 * B * H * (T // 32) * 4 * 16384
+    # d_k = 128 with d_v = 32: one slab, no partial sums -- status word, snapshots every 8 tokens (16 KB),
+    # x and v - h'^T b of every token on 32 columns, dA_log partials
+    narrow = gdn.gdn_workspace_bytes(gdn.make_shape(B, H, T, 128, 32, "delta", "bf16"), 1)
+    assert narrow == 256 + B * H * (T // 8) * 16384 + B * H * T * 2 * 32 * 4 + B * H * 128 * 4
 
 
 def test_time_split_workspace():
