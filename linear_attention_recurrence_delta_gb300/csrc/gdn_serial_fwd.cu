@@ -23,18 +23,18 @@ namespace {
 
 using namespace rec;
 
-constexpr int kTB = 32;    // tokens per staged block
-
 template <int LPC>
 struct FCfg {
     static constexpr int ROWS = 16 * LPC;          // state rows covered
     static constexpr int PAD = ROWS + ROWS / 4;    // padded row-vector length (see prow)
     static constexpr int COLS = 128 / LPC;         // state columns per CTA (4 warps)
+    // tokens per staged block: 16 at 128 rows keeps the CTA near 42 KB of shared memory, five per SM
+    static constexpr int TB = LPC == 4 ? 32 : 16;
 };
 
 template <typename IO, int LPC>
 struct FwdSmem {
-    static constexpr int R = FCfg<LPC>::ROWS, NC = FCfg<LPC>::COLS, PAD = FCfg<LPC>::PAD;
+    static constexpr int R = FCfg<LPC>::ROWS, NC = FCfg<LPC>::COLS, PAD = FCfg<LPC>::PAD, kTB = FCfg<LPC>::TB;
     float A[kTB][PAD];       // alpha_t per state row
     float Bv[kTB][PAD];      // b_t
     float Cv[kTB][PAD];      // c_t
@@ -118,7 +118,7 @@ __device__ __forceinline__ void convert_block(const Args& a, FwdSmem<IO, LPC>& s
 template <typename IO, bool DELTA, int LPC>
 __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
 {
-    constexpr int R = FCfg<LPC>::ROWS, NC = FCfg<LPC>::COLS;
+    constexpr int R = FCfg<LPC>::ROWS, NC = FCfg<LPC>::COLS, kTB = FCfg<LPC>::TB;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     FwdSmem<IO, LPC>& s = *reinterpret_cast<FwdSmem<IO, LPC>*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -149,8 +149,8 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
 
     IO greg = from_f<IO>(0.f), breg = from_f<IO>(0.f);
     issue_block<IO, DELTA, LPC>(a, s, U, 0, min(kTB, T), vec, greg, breg);
-    if (tid < 32) s.rg[tid] = gate(to_f(greg), a.logits);
-    else if (tid < 64) s.rbeta[tid - 32] = gate(to_f(breg), a.logits);
+    if (tid < kTB) s.rg[tid] = gate(to_f(greg), a.logits);
+    else if (tid >= 32 && tid < 32 + kTB) s.rbeta[tid - 32] = gate(to_f(breg), a.logits);
     cp_async_wait_all();
     __syncthreads();
     convert_block<IO, DELTA, LPC>(a, s, U, min(kTB, T));
@@ -193,8 +193,8 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
             o[(((size_t)U.bb * T + t0 + tt) * H + U.h) * dv + U.jc0 + q] = from_f<IO>(s.O[tt][q]);
         }
         if (n + 1 < nblk) {
-            if (tid < 32) s.rg[tid] = gate(to_f(greg), a.logits);
-            else if (tid < 64) s.rbeta[tid - 32] = gate(to_f(breg), a.logits);
+            if (tid < kTB) s.rg[tid] = gate(to_f(greg), a.logits);
+            else if (tid >= 32 && tid < 32 + kTB) s.rbeta[tid - 32] = gate(to_f(breg), a.logits);
             cp_async_wait_all();
             __syncthreads();
             convert_block<IO, DELTA, LPC>(a, s, U, min(kTB, T - t0 - kTB));
