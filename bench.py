@@ -52,6 +52,13 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one forward launch, from an ncu capture of the
+# kernel as it stands (profiles/fwd_tc_delta_8x16x4096x64.md); a workload without a capture reports null.
+MEASURED_TRAFFIC = {
+    "delta_bf16_8x16x4096x64": 203576832 + 45135872,
+}
+
+
 def io_bytes(w, backward=False):
     """Algorithmic HBM bytes of one forward (or backward) launch over workload w:
     every input read once, every output written once."""
@@ -332,7 +339,8 @@ def main():
     fwd_bytes = io_bytes(w)
     achieved = fwd_bytes / (launch_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
+                "frac": achieved / peaks["hbm_gbs"], "traffic": MEASURED_TRAFFIC.get(w.name),
+                "peak_kind": peak_kind,
                 "kernel": fwd_kernel_name(w), "bytes_per_launch": fwd_bytes, "launch_ms": launch_ms}
     # launches of our kernels per forward step: the forward kernel itself
     gpu_launches = fwd_launches(w) * args.steps
