@@ -212,3 +212,60 @@ def gdn_bwd_logits(v, b, c, zg, zbeta, A_log, h0, dO, dhT=None, mode="gated", **
     if be is not None:
         out["dbeta"] = out["dbeta"] * be * (1.0 - be)
     return out
+
+
+NORM_EPS = 1e-12
+
+
+def l2_normalize(x):
+    """Each vector of the last axis divided by its Euclidean norm, in fp64: x / max(||x||, 1e-12).
+
+    The pages do not spell out a normalisation of b and c; this is the plain reading of an L2
+    normalisation of a key vector (the floor of 1e-12 keeps an all-zero vector, such as a padded
+    token, at zero)."""
+    x = _f64(x)
+    n = np.sqrt((x * x).sum(axis=-1, keepdims=True))
+    return x / np.maximum(n, NORM_EPS)
+
+
+def l2_normalize_vjp(x, d):
+    """Gradient through l2_normalize: for y = x / n with n = ||x|| > 1e-12, dL/dx = (d - y <y, d>) / n;
+    below the floor y = x / 1e-12 and dL/dx = d / 1e-12."""
+    x, d = _f64(x), _f64(d)
+    n = np.sqrt((x * x).sum(axis=-1, keepdims=True))
+    big = n > NORM_EPS
+    ns = np.where(big, n, NORM_EPS)
+    y = x / ns
+    return np.where(big, (d - y * (y * d).sum(axis=-1, keepdims=True)) / ns, d / NORM_EPS)
+
+
+def gdn_fwd_opts(v, b, c, g, beta, A_log, h0=None, mode="gated", gate_logits=False, norm_bc=False, **kw):
+    """gdn_fwd with the library's option bits: g (and beta) as logits, and/or b and c given before their
+    L2 normalisation (the rule then runs on l2_normalize(b), l2_normalize(c))."""
+    if gate_logits:
+        g, beta = sigmoid(g), sigmoid(beta)
+    if norm_bc:
+        b, c = l2_normalize(b), l2_normalize(c)
+    return gdn_fwd(v, b, c, g, beta, A_log, h0, mode=mode, **kw)
+
+
+def gdn_bwd_opts(v, b, c, g, beta, A_log, h0, dO, dhT=None, mode="gated", gate_logits=False, norm_bc=False,
+                 **kw):
+    """gdn_bwd with the option bits of gdn_fwd_opts; gradients are with respect to the inputs as given
+    (logits, and b and c before normalisation)."""
+    if gate_logits:
+        return _logit_grads(gdn_bwd_opts(v, b, c, sigmoid(g), sigmoid(beta), A_log, h0, dO, dhT, mode=mode,
+                                         norm_bc=norm_bc, **kw), sigmoid(g), sigmoid(beta))
+    if not norm_bc:
+        return gdn_bwd(v, b, c, g, beta, A_log, h0, dO, dhT, mode=mode, **kw)
+    out = gdn_bwd(v, l2_normalize(b), l2_normalize(c), g, beta, A_log, h0, dO, dhT, mode=mode, **kw)
+    out["db"] = l2_normalize_vjp(b, out["db"])
+    out["dc"] = l2_normalize_vjp(c, out["dc"])
+    return out
+
+
+def _logit_grads(out, g, be):
+    out["dg"] = out["dg"] * g * (1.0 - g)
+    if be is not None:
+        out["dbeta"] = out["dbeta"] * be * (1.0 - be)
+    return out

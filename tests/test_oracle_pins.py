@@ -268,3 +268,65 @@ def test_logit_gates_finite_differences(mode):
                 fd = (loss(zg, p.reshape(z.shape)) - loss(zg, m.reshape(z.shape))) / (2 * eps)
             an = grad.reshape(-1)[k]
             assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (name, k, fd, an)
+
+
+def test_l2_normalize_closed_forms():
+    """Unit length, unchanged direction, invariance to positive scaling, zero stays zero, and a
+    3-4-5 vector by hand."""
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=(3, 7, 2, 9))
+    y = oracle.l2_normalize(x)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), 1.0, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(y * np.linalg.norm(x, axis=-1, keepdims=True), x, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(oracle.l2_normalize(3.5 * x), y, rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(oracle.l2_normalize(np.zeros((2, 4))), np.zeros((2, 4)))
+    np.testing.assert_allclose(oracle.l2_normalize(np.array([3.0, -4.0])), [0.6, -0.8], rtol=0, atol=1e-16)
+    # the gradient is orthogonal to the vector (moving along x does not change x / ||x||)
+    d = rng.normal(size=x.shape)
+    gx = oracle.l2_normalize_vjp(x, d)
+    np.testing.assert_allclose((gx * x).sum(axis=-1), 0.0, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+@pytest.mark.parametrize("logits", [False, True])
+def test_norm_bc_finite_differences(mode, logits):
+    """b and c given before their L2 normalisation (with and without logit gates): the forward equals the
+    rule on b / ||b||, c / ||c|| computed here with numpy, and the gradients with respect to the raw b, c
+    (and the gates) match central differences of L = <o, dO> + <h_T, dh_T>."""
+    x = draw(mode, B=1, H=1, T=12, dk=4, dv=3, seed=13, h0_std=0.5)
+    rng = np.random.default_rng(17)
+    b = 2.0 * rng.normal(size=x["b"].shape)
+    c = 0.7 * rng.normal(size=x["c"].shape)
+    g, be = x["g"], x["beta"]
+    if logits:
+        g = rng.normal(size=g.shape)
+        be = rng.normal(size=g.shape) if mode == "delta" else None
+    kw = dict(mode=mode, gate_logits=logits, norm_bc=True)
+    o_n, h_n = oracle.gdn_fwd_opts(x["v"], b, c, g, be, x["A_log"], x["h0"], **kw)
+    unit = lambda a: a / np.sqrt((a ** 2).sum(axis=-1, keepdims=True))
+    o_p, h_p = oracle.gdn_fwd_opts(x["v"], unit(b), unit(c), g, be, x["A_log"], x["h0"], mode=mode,
+                                   gate_logits=logits)
+    np.testing.assert_allclose(o_n, o_p, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(h_n, h_p, rtol=0, atol=1e-13)
+    dO = rng.normal(size=x["v"].shape)
+    dhT = rng.normal(size=(1, 1, 4, 3))
+    gr = oracle.gdn_bwd_opts(x["v"], b, c, g, be, x["A_log"], x["h0"], dO, dhT, **kw)
+
+    def loss(**over):
+        a = dict(b=b, c=c, g=g, beta=be)
+        a.update(over)
+        o, hT = oracle.gdn_fwd_opts(x["v"], a["b"], a["c"], a["g"], a["beta"], x["A_log"], x["h0"], threads=1,
+                                    **kw)
+        return float((o * dO).sum() + (hT * dhT).sum())
+
+    eps = 1e-6
+    checks = [("db", "b", b), ("dc", "c", c)]
+    if logits:
+        checks += [("dg", "g", g)] + ([("dbeta", "beta", be)] if mode == "delta" else [])
+    for name, arg, z in checks:
+        for k in range(z.size):
+            p = z.reshape(-1).copy(); p[k] += eps
+            m = z.reshape(-1).copy(); m[k] -= eps
+            fd = (loss(**{arg: p.reshape(z.shape)}) - loss(**{arg: m.reshape(z.shape)})) / (2 * eps)
+            an = gr[name].reshape(-1)[k]
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (name, k, fd, an)
