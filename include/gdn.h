@@ -18,7 +18,8 @@
  * state carried serially from chunk to chunk.
  *
  * Inputs arrive already transformed: g and beta after their sigmoid (values
- * in [0, 1]), and in delta mode b already L2-normalised by the caller.  The
+ * in [0, 1]), and in delta mode b already L2-normalised by the caller --
+ * unless the option bits below ask the kernels to apply those steps.  The
  * library applies no 1/sqrt(d) scale, no output norm and no state clamp
  * ("Signed-state caveat": HyMo does not bound the state norm).
  *
@@ -73,7 +74,15 @@ enum {
      * apply sigmoid() as they load them, and gdn_bwd returns dg and dbeta
      * with respect to the logits.  Without the bit both arrive already in
      * [0, 1] and the gradients are with respect to those values. */
-    GDN_GATE_LOGITS = 0x100
+    GDN_GATE_LOGITS = 0x100,
+    /* b and c arrive before their L2 normalisation: every kernel divides
+     * b_t and c_t by their Euclidean norm over d_k (floored at 1e-12, so an
+     * all-zero vector stays zero) before the rule uses them, and gdn_bwd
+     * returns db and dc with respect to the vectors as given.  The pages do
+     * not spell out this step; it is the plain L2 normalisation of a key and
+     * a read vector, fused so that no separate pass over b and c is needed.
+     * Without the bit b and c are used as given. */
+    GDN_NORM_BC = 0x200
 };
 
 typedef enum {

@@ -19,6 +19,7 @@ import threading
 
 GDN_GATED, GDN_DELTA = 0, 1
 GDN_GATE_LOGITS = 0x100      # option bit: g and beta arrive before their sigmoid
+GDN_NORM_BC = 0x200          # option bit: b and c arrive before their L2 normalisation
 GDN_F32, GDN_BF16 = 0, 1
 GDN_OK = 0
 STATUS_NAMES = {
@@ -47,11 +48,13 @@ class gdn_shape_t(ctypes.Structure):
                 f"mode={self.mode}, io={self.io})")
 
 
-def make_shape(B, H, T, dk, dv, mode="gated", io="bf16", gate_logits=False) -> gdn_shape_t:
+def make_shape(B, H, T, dk, dv, mode="gated", io="bf16", gate_logits=False, norm_bc=False) -> gdn_shape_t:
     m = {"gated": GDN_GATED, "delta": GDN_DELTA}.get(mode, mode)
     d = {"f32": GDN_F32, "bf16": GDN_BF16}.get(io, io)
     if gate_logits:
         m = int(m) | GDN_GATE_LOGITS
+    if norm_bc:
+        m = int(m) | GDN_NORM_BC
     return gdn_shape_t(int(B), int(H), int(T), int(dk), int(dv), int(m), int(d))
 
 

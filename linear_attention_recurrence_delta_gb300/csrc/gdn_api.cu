@@ -23,7 +23,7 @@ static bool shape_ok(const gdn_shape_t& s)
 }
 
 // the serial backward's buffers for shape s, placed from `off`
-static size_t place_bwd_core(const gdn_shape_t& s, WsLayout& L, size_t off)
+static size_t place_bwd_core(const gdn_shape_t& s, WsLayout& L, size_t off, int norm)
 {
     const size_t nslab = (size_t)bwd_slabs(s.dk, s.dv);
     const size_t ctas = (size_t)s.B * s.H * nslab;   // one CTA per unit and column slab
@@ -36,7 +36,7 @@ static size_t place_bwd_core(const gdn_shape_t& s, WsLayout& L, size_t off)
     L.dalog_off = off;
     off = round_up(off + ctas * (size_t)s.dk * 4, 256);
     L.slab_off = off;
-    if (nslab > 1) {
+    if (bwd_partials(s.dk, s.dv, norm)) {
         const size_t ntok = (size_t)s.B * s.T * s.H;
         off = round_up(off + nslab * ntok * (2 * (size_t)s.dk + 2) * sizeof(float), 256);
     }
@@ -76,14 +76,14 @@ static size_t place_tsplit(const gdn_shape_t& s, int P, bool backward, WsLayout&
     return off;
 }
 
-WsLayout ws_layout_bwd_core(const gdn_shape_t& s)
+WsLayout ws_layout_bwd_core(const gdn_shape_t& s, int norm)
 {
     WsLayout L;
-    L.total = place_bwd_core(s, L, 256);
+    L.total = place_bwd_core(s, L, 256, norm);
     return L;
 }
 
-WsLayout ws_layout(const gdn_shape_t& s, int backward)
+WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm)
 {
     WsLayout L;
     size_t off = 256;  // status word
@@ -94,7 +94,7 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward)
             core.B = s.B * P;
             core.T = s.T / P;
         }
-        off = place_bwd_core(core, L, off);
+        off = place_bwd_core(core, L, off, norm);
     }
     if (P > 1) off = place_tsplit(s, P, backward != 0, L, off);
     L.total = off;
@@ -122,7 +122,7 @@ static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 static gdn_status_t check_common(const gdn_shape_t* s, const void* v, const void* b, const void* c,
                                  const void* g, const void* beta, const float* A_log, const float* h0,
-                                 void* ws, size_t ws_bytes, int backward)
+                                 void* ws, size_t ws_bytes, int backward, int norm)
 {
     if (!s) return GDN_ERR_NULL;
     if (s->mode != GDN_GATED && s->mode != GDN_DELTA) return GDN_ERR_MODE;
@@ -139,17 +139,19 @@ static gdn_status_t check_common(const gdn_shape_t* s, const void* v, const void
         (beta && !aligned(beta, s->io == GDN_BF16 ? 2 : 4)))
         return GDN_ERR_ALIGN;
     if (!aligned(A_log, 16) || (h0 && !aligned(h0, 16)) || !aligned(ws, 256)) return GDN_ERR_ALIGN;
-    if (ws_bytes < ws_layout(*s, backward).total) return GDN_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(*s, backward, norm).total) return GDN_ERR_WORKSPACE;
     return GDN_OK;
 }
 
 // Split the option bits off the mode: `out` gets the plain mode, `logits` the
-// GDN_GATE_LOGITS bit.  False if the mode carries an unknown bit.
-static bool split_mode(const gdn_shape_t* in, gdn_shape_t* out, int* logits)
+// GDN_GATE_LOGITS bit, `norm` the GDN_NORM_BC bit.  False if the mode carries
+// an unknown bit.
+static bool split_mode(const gdn_shape_t* in, gdn_shape_t* out, int* logits, int* norm)
 {
     *out = *in;
     *logits = (in->mode & GDN_GATE_LOGITS) != 0;
-    out->mode = in->mode & ~GDN_GATE_LOGITS;
+    *norm = (in->mode & GDN_NORM_BC) != 0;
+    out->mode = in->mode & ~(GDN_GATE_LOGITS | GDN_NORM_BC);
     return (out->mode & ~0xff) == 0;
 }
 
@@ -181,13 +183,13 @@ using namespace gdn;
 extern "C" size_t gdn_workspace_bytes(const gdn_shape_t* shape_in, int backward)
 {
     gdn_shape_t sh;
-    int logits = 0;
-    if (!shape_in || !split_mode(shape_in, &sh, &logits)) return 0;
+    int logits = 0, norm = 0;
+    if (!shape_in || !split_mode(shape_in, &sh, &logits, &norm)) return 0;
     const gdn_shape_t* shape = &sh;
     if (!shape_ok(*shape)) return 0;
     if ((shape->mode != GDN_GATED && shape->mode != GDN_DELTA) || (shape->io != GDN_F32 && shape->io != GDN_BF16))
         return 0;
-    return ws_layout(*shape, backward ? 1 : 0).total;
+    return ws_layout(*shape, backward ? 1 : 0, norm).total;
 }
 
 extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, const void* b, const void* c,
@@ -195,11 +197,11 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, cons
                                 void* o, float* hT, void* ws, size_t ws_bytes, gdn_stream_t stream)
 {
     gdn_shape_t sh;
-    int logits = 0;
+    int logits = 0, norm = 0;
     if (!shape_in) return GDN_ERR_NULL;
-    if (!split_mode(shape_in, &sh, &logits)) return GDN_ERR_MODE;
+    if (!split_mode(shape_in, &sh, &logits, &norm)) return GDN_ERR_MODE;
     const gdn_shape_t* shape = &sh;
-    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 0);
+    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 0, norm);
     if (r != GDN_OK) return r;
     if (!o && shape->T > 0) return GDN_ERR_NULL;
     const size_t ioa = shape->io == GDN_BF16 ? 16 : 4;
@@ -210,7 +212,7 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, cons
     if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return GDN_ERR_CUDA;
     Args a = make_args(shape);
     a.v = v; a.b = b; a.c = c; a.g = g; a.beta = beta; a.A_log = A_log; a.h0 = h0; a.o = o; a.hT = hT;
-    a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits;
+    a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits; a.norm = norm;
     const size_t state_bytes = (size_t)a.B * a.H * a.dk * a.dv * sizeof(float);
     if (a.T == 0) {
         if (hT && hT != h0) {
@@ -221,7 +223,7 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, cons
         return GDN_OK;
     }
     const int P = tsplit_factor(*shape, 0);
-    const cudaError_t e = P > 1 ? launch_fwd_tsplit(a, ws_layout(*shape, 0), P, st, fwd_core) : fwd_core(a, st);
+    const cudaError_t e = P > 1 ? launch_fwd_tsplit(a, ws_layout(*shape, 0, norm), P, st, fwd_core) : fwd_core(a, st);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -232,11 +234,11 @@ extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape_in, const void* v, cons
                                 gdn_stream_t stream)
 {
     gdn_shape_t sh;
-    int logits = 0;
+    int logits = 0, norm = 0;
     if (!shape_in) return GDN_ERR_NULL;
-    if (!split_mode(shape_in, &sh, &logits)) return GDN_ERR_MODE;
+    if (!split_mode(shape_in, &sh, &logits, &norm)) return GDN_ERR_MODE;
     const gdn_shape_t* shape = &sh;
-    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 1);
+    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 1, norm);
     if (r != GDN_OK) return r;
     const bool tok = shape->T > 0;
     if ((tok && (!dO || !dv || !db || !dc || !dg)) || !dA_log) return GDN_ERR_NULL;
@@ -255,9 +257,9 @@ extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape_in, const void* v, cons
     Args a = make_args(shape);
     a.v = v; a.b = b; a.c = c; a.g = g; a.beta = beta; a.A_log = A_log; a.h0 = h0;
     a.dO = dO; a.dhT = dhT; a.dv_ = dv; a.db = db; a.dc = dc; a.dg = dg; a.dbeta = dbeta;
-    a.dA_log = dA_log; a.dh0 = dh0; a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits;
+    a.dA_log = dA_log; a.dh0 = dh0; a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits; a.norm = norm;
     const int P = a.T > 0 ? tsplit_factor(*shape, 1) : 1;
-    const cudaError_t e = P > 1 ? launch_bwd_tsplit(a, ws_layout(*shape, 1), P, st, fwd_core) : launch_serial_bwd(a, st);
+    const cudaError_t e = P > 1 ? launch_bwd_tsplit(a, ws_layout(*shape, 1, norm), P, st, fwd_core) : launch_serial_bwd(a, st);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -98,6 +98,7 @@ struct DecSmem {
     float snext[2][ROWS * 64];   // double-buffered incoming states
     float sAl[kDecMaxT][ROWS], sB[kDecMaxT][ROWS], sC[kDecMaxT][ROWS], sV[kDecMaxT][64];
     float sbeta[kDecMaxT];
+    float nb[kDecMaxT], nc[kDecMaxT];   // GDN_NORM_BC: 1 / max(||b_t||, floor), the same for c_t
     float redR[8][64], redO[8][64];
     float xcol[64];
 };
@@ -153,6 +154,16 @@ __global__ void __launch_bounds__(256) decode_kernel(Args a, bool vec4, int nsla
             else cp_async_wait_all();
         }
         __syncthreads();
+        if (a.norm) {   // inverse norms of the staged b_t and c_t, one thread per vector
+            if (tid < 2 * T) {
+                const int tt = tid >> 1;
+                const float* x = (tid & 1) ? S.sC[tt] : S.sB[tt];
+                float q = 0.f;
+                for (int i = 0; i < dk; i++) q = fmaf(x[i], x[i], q);
+                (tid & 1 ? S.nc : S.nb)[tt] = 1.f / fmaxf(sqrtf(q), kNormFloor);
+            }
+            __syncthreads();
+        }
 
         // state entries (row rg + 16 k, columns j0 .. j0 + 3 of the slab)
         float hs[K][4];
@@ -180,11 +191,12 @@ __global__ void __launch_bounds__(256) decode_kernel(Args a, bool vec4, int nsla
 
         for (int tt = 0; tt < T; tt++) {
             float al[K], bk[K], ck[K];
+            const float nbt = a.norm ? S.nb[tt] : 1.f, nct = a.norm ? S.nc[tt] : 1.f;
 #pragma unroll
             for (int k = 0; k < K; k++) {
                 al[k] = S.sAl[tt][rg + 16 * k];
-                bk[k] = S.sB[tt][rg + 16 * k];
-                ck[k] = S.sC[tt][rg + 16 * k];
+                bk[k] = S.sB[tt][rg + 16 * k] * nbt;
+                ck[k] = S.sC[tt][rg + 16 * k] * nct;
             }
             float hp[K][4];
 #pragma unroll

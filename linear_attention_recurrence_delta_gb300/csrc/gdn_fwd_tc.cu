@@ -112,12 +112,14 @@ struct Small {
     float decay[64];
     float g[kStages][64];
     float beta[kStages][64];
+    float nb[64], nc[64];   // GDN_NORM_BC: 1 / max(||b_t||, floor), the same for c_t, of the current chunk
     uint64_t full[kStages], mma;
     uint32_t tmem_base;
     uint32_t unsafe;
     uint32_t abort;
     float a2max;
 };
+static_assert(sizeof(Small) <= 4096, "the small-state block has a 4 KB slot");
 
 __device__ __forceinline__ void st_split16(unsigned char* thi, unsigned char* tlo, int row, int col16,
                                            const float (&v)[16])
@@ -157,7 +159,8 @@ __device__ __forceinline__ const float* ktab(const unsigned char* sm, int tab, i
     return reinterpret_cast<const float*>(sm + OFF_K) + (tab * 8 + k8) * 64;
 }
 
-template <bool DELTA>
+// NORM: b and c arrive before their L2 normalisation (a template flag, so the plain kernel carries no trace of it)
+template <bool DELTA, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -295,8 +298,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 const bool bad = __any_sync(0xffffffffu, span * S.a2max > kSafeLog2);
                 if (lane == 0) S.unsafe = bad ? 1u : 0u;
+            } else if (NORM && r < 32 + 128) {
+                // meanwhile warps 1..4: inverse norms of the chunk's b (rows 0..63) and c rows
+                const int vr = r - 32, t = vr & 63;
+                float sq = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    float x8[8];
+                    ld_row8(vr < 64 ? sB : sCt, t, q, x8);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) sq = fmaf(x8[e], x8[e], sq);
+                }
+                const float inv = 1.f / fmaxf(sqrtf(sq), kNormFloor);
+                if (vr < 64) S.nb[t] = inv;
+                else S.nc[t] = inv;
             }
-            named_bar_sync(1, kMath);   // G and the overflow flag
+            named_bar_sync(1, kMath);   // G, the overflow flag (and the inverse norms)
             // decay constants per (8-block, reference point); every exponent <= 0
             {
                 float* K = reinterpret_cast<float*>(sm + OFF_K);
@@ -326,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const float Gt = S.G[t], Gr = S.G[8 * k8 + 3];
                 const float dG = Gt - Gr;
                 const float bet = DELTA ? S.beta[s][t] : 0.f;
+                const float nbt = NORM ? S.nb[t] : 1.f, nct = NORM ? S.nc[t] : 1.f;
                 if (!unsafe) {
                     // fast path: anchor exp(A (G_t - G_r8)) times per-block constants
 #pragma unroll
@@ -335,6 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         ld_row8(sCt, t, q, cv);
                         ld_row8(sB, t, q, bv);
                         ld_f8(S.A2 + 8 * q, a2);
+                        if (NORM) {
+#pragma unroll
+                            for (int e = 0; e < 8; e++) { cv[e] *= nct; bv[e] *= nbt; }
+                        }
 #pragma unroll
                         for (int e = 0; e < 8; e++) {
                             const float an = fast_exp2(a2[e] * dG), ai = fast_exp2(-a2[e] * dG);
@@ -399,7 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         ld_row8(sCt, t, q, cv);
                         ld_row8(sB, t, q, bv);
 #pragma unroll
-                        for (int e = 0; e < 8; e++) bbv[e] = bet * bv[e];
+                        for (int e = 0; e < 8; e++) {
+                            cv[e] *= nct;
+                            bv[e] *= nbt;
+                            bbv[e] = bet * bv[e];
+                        }
                         if (I > 0) {
                             scale8(cv, S.A2, q, Gt - GI, y); st_row8_f16(X + X_A1, t, q, y);
                             if (DELTA) { scale8(bbv, S.A2, q, Gt - GI, z); st_row8_f16(X + X_A1, 64 + t, q, z); }
@@ -460,7 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                         for (int e = 0; e < 8; e++) {
                             const int sc = 16 * sq + 8 * h2 + e;
-                            const float bval = bf2f(*reinterpret_cast<const uint16_t*>(sB + sw128(sc, i)));
+                            const float bval = bf2f(*reinterpret_cast<const uint16_t*>(sB + sw128(sc, i))) *
+                                               (NORM ? S.nb[sc] : 1.f);
                             y8[e] = bval * exp2f(a2 * (G63 - S.G[sc]));
                         }
                         st_row8_split(sm + OFF_CH0, sm + OFF_CH0L, i, 2 * sq + h2, y8);
@@ -492,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                     for (int kk = 0; kk < 8; kk++)
                                         acc += xv[kk] * bv[kk] * exp2f(S.A2[8 * q + kk] * (S.G[t] - S.G[sc]));
                                 }
+                                if (NORM) acc *= (isM ? S.nb[t] : S.nc[t]) * S.nb[sc];
                             }
                             ew[e] = isM ? bet * acc : acc;
                         }
@@ -736,6 +764,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         const int q = 4 * wh + qq;
                         float cv[8], y[8];
                         ld_row8(sCt, t, q, cv);
+                        if (NORM) {
+#pragma unroll
+                            for (int e = 0; e < 8; e++) cv[e] *= S.nc[t];
+                        }
                         scale8(cv, S.A2, q, Gt, y);
                         st_row8(X + X_CW, trow, q, y);
                     }
@@ -861,17 +893,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (warp == 0) tmem_dealloc(tbase, TM_COLS);
 }
 
-template <bool DELTA>
+template <bool DELTA, bool NORM>
 cudaError_t launch_t(const TcParams& p, dim3 grid, cudaStream_t st)
 {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<DELTA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<DELTA, NORM>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    fwd_tc_kernel<DELTA><<<grid, kThreads, SMEM_BYTES, st>>>(p);
+    fwd_tc_kernel<DELTA, NORM><<<grid, kThreads, SMEM_BYTES, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -898,7 +930,9 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     p.nchunks = (a.T + kC - 1) / kC;
     *handled = true;
     const dim3 grid(a.B * a.H, (a.dv + 63) / 64);
-    return a.mode == GDN_DELTA ? launch_t<true>(p, grid, st) : launch_t<false>(p, grid, st);
+    if (a.norm)
+        return a.mode == GDN_DELTA ? launch_t<true, true>(p, grid, st) : launch_t<false, true>(p, grid, st);
+    return a.mode == GDN_DELTA ? launch_t<true, false>(p, grid, st) : launch_t<false, false>(p, grid, st);
 }
 
 }  // namespace gdn

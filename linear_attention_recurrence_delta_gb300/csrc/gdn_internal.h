@@ -13,6 +13,7 @@ namespace gdn {
 struct Args {
     int B, H, T, dk, dv, mode, io;
     int logits;            // g, beta arrive before their sigmoid (GDN_GATE_LOGITS)
+    int norm;              // b, c arrive before their L2 normalisation (GDN_NORM_BC)
     const void *v, *b, *c, *g, *beta;
     const float* A_log;
     const float* h0;
@@ -62,8 +63,13 @@ constexpr size_t kStateSlot = 16 * 256 * 4;    // one state snapshot (256 thread
 inline int bwd_cols(int dk) { return dk <= 64 ? 64 : 32; }
 inline int bwd_slabs(int dk, int dv) { return (dv + bwd_cols(dk) - 1) / bwd_cols(dk); }
 
-WsLayout ws_layout(const gdn_shape_t& s, int backward);
-WsLayout ws_layout_bwd_core(const gdn_shape_t& s);   // the serial backward's own buffers only
+// `norm`: GDN_NORM_BC is set (the backward then routes db, dc through fp32 partials)
+WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm = 0);
+WsLayout ws_layout_bwd_core(const gdn_shape_t& s, int norm = 0);   // the serial backward's own buffers only
+
+// the serial backward writes fp32 partial sums of db, dc, dg, dbeta (rather than its outputs) when
+// it has several column slabs or must still apply the normalisation's Jacobian
+inline bool bwd_partials(int dk, int dv, int norm) { return bwd_slabs(dk, dv) > 1 || norm; }
 
 // Launchers (enqueue on `st`, return cudaGetLastError()).
 cudaError_t launch_serial_fwd(const Args& a, cudaStream_t st);
@@ -76,6 +82,8 @@ cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
 cudaError_t launch_bwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
                               cudaError_t (*fwd_core)(const Args&, cudaStream_t));
 int decode_max_tokens();
+
+constexpr float kNormFloor = 1e-12f;   // L2 normalisation: x / max(||x||, kNormFloor)
 
 // Device status word helpers.
 enum : uint32_t { kDevOk = 0, kDevTimeout = 1 };

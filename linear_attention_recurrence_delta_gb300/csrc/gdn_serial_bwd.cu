@@ -66,6 +66,7 @@ struct BwdSmem {
     float bpart[2][8][kWin], gpart[2][8][kWin];
     float red[8][R];
     float rg[kBT], rbeta[kBT];
+    float nb[kBT], nc[kBT];       // GDN_NORM_BC: 1 / max(||b_t||, floor), the same for c_t
     IO rb[kBT][R], rc[kBT][R], rv[kBT][NC], rdo[kBT][NC];       // raw bytes of the next block
 };
 
@@ -145,12 +146,25 @@ __device__ __forceinline__ void finish_block(const Args& a, BwdSmem<IO, KIG>& s,
     if (leave_newest) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
     else cp_async_wait_all();
     __syncthreads();
+    if (a.norm) {   // inverse norms of the block's b_t (and c_t), one thread per vector
+        if (tid < 2 * nt) {
+            const int tt = tid >> 1;
+            const IO* x = (tid & 1) ? s.rc[tt] : s.rb[tt];
+            float q = 0.f;
+            if (!(tid & 1) || grad)
+                for (int k = 0, i = tt % dk; k < dk; k++, i = i + 1 < dk ? i + 1 : 0)   // rotated: fewer bank conflicts
+                    q = fmaf(to_f(x[i]), to_f(x[i]), q);
+            (tid & 1 ? s.nc : s.nb)[tt] = 1.f / fmaxf(sqrtf(q), kNormFloor);
+        }
+        __syncthreads();
+    }
     for (int idx = tid; idx < kBT * R; idx += 256) {
         const int tt = idx / R, i = idx % R;
         const bool ok = tt < nt;
+        const float sb = a.norm && ok ? s.nb[tt] : 1.f, sc = a.norm && ok ? s.nc[tt] : 1.f;
         s.A[tt][i] = ok ? decay<IO>(s.rg[tt], s.Arow[i], s.Arow2[i]) : 1.f;
-        s.Bv[tt][i] = ok && i < dk ? to_f(s.rb[tt][i]) : 0.f;
-        s.Cv[tt][i] = grad && ok && i < dk ? to_f(s.rc[tt][i]) : 0.f;
+        s.Bv[tt][i] = ok && i < dk ? to_f(s.rb[tt][i]) * sb : 0.f;
+        s.Cv[tt][i] = grad && ok && i < dk ? to_f(s.rc[tt][i]) * sc : 0.f;
         if (R == NC) {   // rows and columns in one pass
             s.V[tt][i] = ok && i < nv ? to_f(s.rv[tt][i]) : 0.f;
             s.DO[tt][i] = grad && ok && i < nv ? to_f(s.rdo[tt][i]) : 0.f;
@@ -620,6 +634,50 @@ __global__ void reduce_slabs_kernel(const float* part, IO* outp, size_t n, int n
     }
 }
 
+// db or dc of each (token, head) row: the column slabs' fp32 partials added in order, then, with
+// GDN_NORM_BC, taken through the normalisation y = x / max(||x||, floor) of the vector x as given:
+// dL/dx = (d - y <y, d>) / ||x|| (d / floor below the floor).  One warp per row, d_k <= 128.
+template <typename IO>
+__global__ void finish_keys_kernel(const float* part, const IO* x, IO* outp, size_t nrows, int dk, int nslab,
+                                   size_t slab_stride, int norm)
+{
+    const int lane = threadIdx.x & 31;
+    const size_t wpb = blockDim.x / 32;
+    for (size_t row = blockIdx.x * wpb + (threadIdx.x >> 5); row < nrows; row += (size_t)gridDim.x * wpb) {
+        float d[4], xv[4];
+        float q = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int i = lane + 32 * k;
+            d[k] = xv[k] = 0.f;
+            if (i < dk) {
+                const size_t at = row * dk + i;
+                float acc = part[at];
+                for (int sl = 1; sl < nslab; sl++) acc += part[(size_t)sl * slab_stride + at];
+                d[k] = acc;
+                xv[k] = to_f(x[at]);
+                q = fmaf(xv[k], xv[k], q);
+            }
+        }
+        if (norm) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(kFull, q, o);
+            const float n = sqrtf(q), inv = 1.f / fmaxf(n, kNormFloor);
+            float yd = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; k++) yd = fmaf(xv[k] * inv, d[k], yd);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) yd += __shfl_xor_sync(kFull, yd, o);
+            const bool big = n > kNormFloor;
+#pragma unroll
+            for (int k = 0; k < 4; k++) d[k] = big ? (d[k] - xv[k] * inv * yd) * inv : d[k] * inv;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            if (lane + 32 * k < dk) outp[row * dk + lane + 32 * k] = from_f<IO>(d[k]);
+    }
+}
+
 static bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 template <typename IO, bool DELTA, int KIG>
@@ -634,7 +692,8 @@ cudaError_t launch_t(const Args& a, const WsLayout& L, int nslab, cudaStream_t s
                      al16(a.dO);
     Outs out{nullptr, nullptr, nullptr, nullptr};
     const size_t ntok = (size_t)a.B * a.T * a.H;
-    if (nslab > 1) {
+    const bool partials = bwd_partials(a.dk, a.dv, a.norm);
+    if (partials) {
         unsigned char* w = (unsigned char*)a.ws + L.slab_off;
         out.db = reinterpret_cast<float*>(w);
         out.dc = out.db + nslab * ntok * a.dk;
@@ -642,10 +701,13 @@ cudaError_t launch_t(const Args& a, const WsLayout& L, int nslab, cudaStream_t s
         out.dbeta = out.dg + nslab * ntok;
     }
     serial_bwd_kernel<IO, DELTA, KIG><<<dim3(a.B * a.H, nslab), 256, smem, st>>>(a, L, out, vec);
-    if ((e = cudaGetLastError()) != cudaSuccess || nslab == 1) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess || !partials) return e;
     const int blocks = 4 * 152;
-    reduce_slabs_kernel<IO><<<blocks, 256, 0, st>>>(out.db, (IO*)a.db, ntok * a.dk, nslab);
-    reduce_slabs_kernel<IO><<<blocks, 256, 0, st>>>(out.dc, (IO*)a.dc, ntok * a.dk, nslab);
+    const size_t slab_keys = ntok * a.dk;
+    finish_keys_kernel<IO><<<blocks, 256, 0, st>>>(out.db, (const IO*)a.b, (IO*)a.db, ntok, a.dk, nslab, slab_keys,
+                                                   a.norm);
+    finish_keys_kernel<IO><<<blocks, 256, 0, st>>>(out.dc, (const IO*)a.c, (IO*)a.dc, ntok, a.dk, nslab, slab_keys,
+                                                   a.norm);
     reduce_slabs_kernel<IO><<<blocks, 256, 0, st>>>(out.dg, (IO*)a.dg, ntok, nslab);
     if (DELTA) reduce_slabs_kernel<IO><<<blocks, 256, 0, st>>>(out.dbeta, (IO*)a.dbeta, ntok, nslab);
     return cudaGetLastError();
@@ -663,7 +725,7 @@ cudaError_t launch_rows(const Args& a, const WsLayout& L, cudaStream_t st)
 cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st)
 {
     gdn_shape_t sh{a.B, a.H, a.T, a.dk, a.dv, a.mode, a.io};
-    const WsLayout L = ws_layout_bwd_core(sh);
+    const WsLayout L = ws_layout_bwd_core(sh, a.norm);
     cudaError_t e;
     if (a.io == GDN_BF16)
         e = a.mode == GDN_DELTA ? launch_rows<__nv_bfloat16, true>(a, L, st) : launch_rows<__nv_bfloat16, false>(a, L, st);

@@ -43,7 +43,8 @@ struct FwdSmem {
     float beta[kTB];
     float Arow[R];           // A = -exp(A_log) of this head
     float rg[kTB], rbeta[kTB];
-    IO rb[kTB][R], rc[kTB][R], rv[kTB][NC];  // raw bytes of the next block
+    float nb[kTB], nc[kTB];  // GDN_NORM_BC: 1 / max(||b_t||, floor), the same for c_t
+    IO rb[kTB][R], rc[kTB][R], rv[kTB][NC];  // raw bytes of the next block (rc directly after rb)
 };
 
 struct Unit {
@@ -95,6 +96,19 @@ __device__ __forceinline__ void convert_block(const Args& a, FwdSmem<IO, LPC>& s
 {
     constexpr int R = FCfg<LPC>::ROWS, NC = FCfg<LPC>::COLS;
     const int tid = threadIdx.x, dk = a.dk;
+    if (a.norm) {   // inverse norms of the block's b_t and c_t, one thread per vector
+        for (int v = tid; v < 2 * nt; v += blockDim.x) {
+            const int tt = v >> 1;
+            const IO* x = &s.rb[0][0] + (size_t)((v & 1) * FCfg<LPC>::TB + tt) * R;   // rc follows rb
+            float q = 0.f;
+            for (int k = 0, i = tt % dk; k < dk; k++, i = i + 1 < dk ? i + 1 : 0)   // rotated: fewer bank conflicts
+                q = fmaf(to_f(x[i]), to_f(x[i]), q);
+            const float inv = 1.f / fmaxf(sqrtf(q), kNormFloor);
+            if (v & 1) s.nc[tt] = inv;
+            else s.nb[tt] = inv;
+        }
+        __syncthreads();
+    }
     for (int idx = tid; idx < nt * R; idx += blockDim.x) {
         const int tt = idx / R, i = idx % R;
         float xa = 0.f, xb = 0.f, xc = 0.f;
@@ -102,6 +116,10 @@ __device__ __forceinline__ void convert_block(const Args& a, FwdSmem<IO, LPC>& s
             xa = expf(s.rg[tt] * s.Arow[i]);
             xb = to_f(s.rb[tt][i]);
             xc = to_f(s.rc[tt][i]);
+            if (a.norm) {
+                xb *= s.nb[tt];
+                xc *= s.nc[tt];
+            }
         }
         const int p = prow(i);
         s.A[tt][p] = xa;

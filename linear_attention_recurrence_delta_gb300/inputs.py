@@ -117,6 +117,7 @@ class Workload:
     g_mu: float = 0.0          # g = sigmoid(N(g_mu, 1))
     h0_std: float = 0.0        # h0 = h0_std * N(0, 1) (0 => no h0)
     gate_logits: bool = False  # g (and beta) drawn as logits N(g_mu, 1) (N(0, 1)), not passed through a sigmoid
+    norm_bc: bool = False      # the library normalises b and c itself (GDN_NORM_BC); draw them unnormalised
     alog_max: float = math.log(16.0)   # A_log ~ U(0, alog_max)
     notes: str = ""
 
@@ -213,7 +214,7 @@ def make_inputs(w: Workload) -> dict:
 def custom(name="custom", mode="gated", dtype="bf16", B=1, H=1, T=64, dk=64, dv=64, seed=0,
            **kw) -> Workload:
     """A workload of arbitrary shape (used by the edge-case tests)."""
-    if mode == "delta":
+    if mode == "delta" and not kw.get("norm_bc"):
         kw.setdefault("b_dist", "l2norm")
         kw.setdefault("c_dist", "l2norm")
     return Workload(name, mode, dtype, B, H, T, dk, dv, seed, **kw)

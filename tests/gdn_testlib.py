@@ -26,7 +26,8 @@ def dev32(x, device="cuda"):
 
 
 def shape_of(w):
-    return gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.mode, w.dtype, gate_logits=w.gate_logits)
+    return gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.mode, w.dtype, gate_logits=w.gate_logits,
+                          norm_bc=w.norm_bc)
 
 
 def run_fwd(w, x, want_hT=True, stream=None):

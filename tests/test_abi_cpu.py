@@ -160,5 +160,21 @@ def test_gate_logits_option_bit():
     assert logit.mode == gdn.GDN_DELTA | gdn.GDN_GATE_LOGITS
     for bwd in (0, 1):
         assert gdn.gdn_workspace_bytes(logit, bwd) == gdn.gdn_workspace_bytes(plain, bwd) > 0
-    bad = gdn.make_shape(2, 4, 300, 64, 64, gdn.GDN_DELTA | 0x200, "bf16")
+    bad = gdn.make_shape(2, 4, 300, 64, 64, gdn.GDN_DELTA | 0x400, "bf16")
     assert gdn.gdn_workspace_bytes(bad, 0) == 0
+
+
+def test_norm_bc_option_bit():
+    """GDN_NORM_BC rides in the mode field too (alone or with GDN_GATE_LOGITS).  The forward's workspace is
+    unchanged; the backward adds fp32 partials of db, dc [B, T, H, d_k] and dg, dbeta [B, T, H] even with a
+    single column slab, because the normalisation's Jacobian is applied after the column sums."""
+    B, H, T, d = 2, 4, 300, 64
+    plain = gdn.make_shape(B, H, T, d, d, "delta", "bf16")
+    norm = gdn.make_shape(B, H, T, d, d, "delta", "bf16", norm_bc=True)
+    both = gdn.make_shape(B, H, T, d, d, "delta", "bf16", gate_logits=True, norm_bc=True)
+    assert norm.mode == gdn.GDN_DELTA | gdn.GDN_NORM_BC
+    assert both.mode == gdn.GDN_DELTA | gdn.GDN_NORM_BC | gdn.GDN_GATE_LOGITS
+    assert gdn.gdn_workspace_bytes(norm, 0) == gdn.gdn_workspace_bytes(plain, 0) == 256
+    extra = B * T * H * (2 * d + 2) * 4
+    assert gdn.gdn_workspace_bytes(norm, 1) >= gdn.gdn_workspace_bytes(plain, 1) + extra
+    assert gdn.gdn_workspace_bytes(both, 1) == gdn.gdn_workspace_bytes(norm, 1)
