@@ -112,6 +112,30 @@ def bwd_launches(w):
     return states + 2 + 1 + 2               # state passes, backward x2 (+ reductions), reverse scan
 
 
+def tc_fwd_ex2_per_launch(w):
+    """exp2 evaluations of one tcgen05 forward launch on workload w (overflow-safe chunks), from the kernel:
+    per chunk and head, the anchors exp(A (G_t - G_r)) and their inverses (2 per token and channel: 2 * 64 * 64),
+    the per-(8-block, reference) constant tables (42 of the 64 (table, 8-block) pairs are live, per channel:
+    42 * 64) and the chunk's decay row (64).  None for the other kernels."""
+    if w.T <= 8 or w.dtype != "bf16" or w.dk > 64 or tsplit_factor(w, False) > 1:
+        return None
+    chunks = -(-w.T // 64) * w.B * w.H * -(-w.dv // 64)
+    return chunks * (2 * 64 * 64 + 42 * 64 + 64)
+
+
+def ex2_rate():
+    """exp2 evaluations per second of the special-function units (libgdn_probe.so), or None."""
+    import ctypes
+    path = os.path.join(ROOT, "linear_attention_recurrence_delta_gb300", "libgdn_probe.so")
+    if not os.path.exists(path):
+        return None
+    lib = ctypes.CDLL(path)
+    lib.gdn_probe_ex2_rate.restype = ctypes.c_int
+    lib.gdn_probe_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double)]
+    r = ctypes.c_double(0.0)
+    return r.value if lib.gdn_probe_ex2_rate(ctypes.byref(r)) == 0 else None
+
+
 def fwd_kernel_name(w):
     """The kernel gdn_fwd launches for workload w (one launch per call)."""
     if w.T <= 8:
@@ -345,6 +369,15 @@ def main():
     # launches of our kernels per forward step: the forward kernel itself
     gpu_launches = fwd_launches(w) * args.steps
 
+    # secondary bound: the forward's exponentials on the special-function units (measured rate)
+    mufu = None
+    n_ex2 = tc_fwd_ex2_per_launch(w)
+    rate = ex2_rate() if n_ex2 else None
+    if rate:
+        floor_ms = n_ex2 / rate * 1e3
+        mufu = {"ex2_per_s": rate, "ex2_per_launch": n_ex2, "floor_ms": floor_ms,
+                "frac_of_launch": floor_ms / launch_ms}
+
     # End to end through the C ABI with host buffers.  Every step copies its inputs from pinned host memory,
     # runs gdn_fwd and reads its outputs back; as a serving loop would, step k+1's input copies overlap
     # step k's forward and step k-1's output copies (three streams, two device buffer sets).
@@ -442,7 +475,7 @@ def main():
                        "l2": (f"inputs+outputs {fwd_bytes / 1e6:.1f} MB > 129 MB L2, no flush" if fwd_bytes > 129e6
                               else f"inputs+outputs {fwd_bytes / 1e6:.1f} MB fit the 129 MB L2: L2-warm, no flush")},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "fwd_bwd": fwdbwd, "clocks": clocks,
-            "gpu_launches": gpu_launches,
+            "gpu_launches": gpu_launches, "mufu": mufu,
         }
         print(json.dumps(line))
     if dist is not None:
