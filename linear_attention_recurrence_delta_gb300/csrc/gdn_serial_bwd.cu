@@ -185,19 +185,33 @@ __device__ __forceinline__ void finish_block(const Args& a, BwdSmem<IO, KIG>& s,
     __syncthreads();
 }
 
+// one token's staged row vectors as this thread uses them (loaded a token ahead in the forward sweep)
+struct TokRows {
+    float2 a2[4], b2[4], v2;
+    float be;
+};
+
+__device__ __forceinline__ void load_tok(TokRows& r, const float* A, const float* Bv, const float* V, float be,
+                                         const Ctx& C)
+{
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        r.a2[p] = ld2(A + C.roff[p]);
+        r.b2[p] = ld2(Bv + C.roff[p]);
+    }
+    r.v2 = ld2(V + C.j0);
+    r.be = be;
+}
+
 // one forward step with the row reduction h'^T b (delta); optionally caches
 // x and v - h'^T b for the window recompute and the adjoint
 template <bool DELTA, bool CACHE, int KIG>
-__device__ __forceinline__ void fwd_full(float2 (&S)[2][4], const float* A, const float* Bv, const float* V, float be,
-                                         float* X, float* VR, const Ctx& C)
+__device__ __forceinline__ void fwd_full(float2 (&S)[2][4], const TokRows& r, float* X, float* VR, const Ctx& C)
 {
-    float2 a2[4], b2[4];
-#pragma unroll
-    for (int p = 0; p < 4; p++) {
-        a2[p] = ld2(A + C.roff[p]);
-        b2[p] = ld2(Bv + C.roff[p]);
-    }
-    const float2 v2 = ld2(V + C.j0);
+    const float2 (&a2)[4] = r.a2;
+    const float2 (&b2)[4] = r.b2;
+    const float2 v2 = r.v2;
+    const float be = r.be;
     float2 hp[2][4];
 #pragma unroll
     for (int c = 0; c < 2; c++)
@@ -358,14 +372,18 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
         else issue_block<IO, DELTA, KIG>(a, s, C, n * kBT, true, vec, greg, breg);  // first block of the reverse walk
         float2* snap_n = gsnap + (size_t)n * kSnapPerBlk * 2048;
         float* xvr_n = gxvr + (size_t)n * kBT * 2 * NC;
-#pragma unroll 1
+        // the next token's row vectors are loaded while this one computes
+        TokRows cur, nxt;
+        load_tok(nxt, s.A[0], s.Bv[0], s.V[0], s.beta[0], C);
+#pragma unroll 2
         for (int tt = 0; tt < kBT; tt++) {
+            cur = nxt;
+            if (tt + 1 < kBT) load_tok(nxt, s.A[tt + 1], s.Bv[tt + 1], s.V[tt + 1], s.beta[tt + 1], C);
             if ((tt & (kSub - 1)) == 0) {
 #pragma unroll
                 for (int q = 0; q < 8; q++) snap_n[((tt / kSub) * 8 + q) * 256 + tid] = S[q >> 2][q & 3];
             }
-            fwd_full<DELTA, DELTA, KIG>(S, s.A[tt], s.Bv[tt], s.V[tt], s.beta[tt], xvr_n + tt * NC,
-                                        xvr_n + kBT * NC + tt * NC, C);
+            fwd_full<DELTA, DELTA, KIG>(S, cur, xvr_n + tt * NC, xvr_n + kBT * NC + tt * NC, C);
         }
     }
 
