@@ -32,7 +32,14 @@ struct TcParams {
     uint32_t* status;
     int B, H, T, dk, dv, nchunks;
     int logits;   // g, beta arrive before their sigmoid
+    int starve_chunk;        // failure-path test hook: the loads of this chunk are never issued (-1: none)
+    uint64_t wait_ns;        // limit of every bounded wait
 };
+
+// Limit of a bounded wait: a chunk's loads or products take microseconds, so two
+// seconds only expire when something that should arrive never will.
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kTestWaitNs = 200000000ull;   // under the failure-path test hook
 
 // g or beta as the rule uses it: the logistic function of a logit (SFU exponential;
 // this path takes bf16 inputs), or the value itself
@@ -115,10 +122,10 @@ __device__ __forceinline__ void scale8(const float (&x)[8], const float* A2, int
 // Bounded wait; after the first expiry every later wait returns at once, the
 // status word records the timeout and the kernel winds down.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* abort_flag,
-                                              uint32_t* status)
+                                              uint32_t* status, uint64_t limit_ns)
 {
     if (*(volatile uint32_t*)abort_flag) return false;
-    if (mbar_wait(bar, parity, nullptr, 1u << 24)) return true;
+    if (mbar_wait(bar, parity, nullptr, limit_ns)) return true;
     *(volatile uint32_t*)abort_flag = 1;
     atomicExch(status, kDevTimeout);
     return false;

@@ -52,6 +52,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stdlib.h>
 
 #include "fwd_tc_common.cuh"
 
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     }
     const uint32_t tbase = S.tmem_base;
     auto issue_load = [&](int k) {   // thread 0: TMA of chunk k into its stage
+        if (k == p.starve_chunk) return;   // failure-path test hook: this stage never fills
         const int s = k % kStages;
         unsigned char* st = sm + OFF_RING + s * STAGE_BYTES;
         mbar_arrive_expect_tx(&S.full[s], STAGE_BYTES);
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         uint32_t mma_phase = 0;
         // one warp polls the mbarrier; the others sleep in the named barrier
         auto mma_wait_all = [&]() -> bool {
-            if (warp == 0) wait_or_abort(&S.mma, mma_phase, &S.abort, p.status);
+            if (warp == 0) wait_or_abort(&S.mma, mma_phase, &S.abort, p.status, p.wait_ns);
             named_bar_sync(1, kMath);
             mma_phase ^= 1;
             tc_fence_after();
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
         for (int k = 0; k < p.nchunks; k++) {
             const int s = k % kStages;
-            if (warp == 0) wait_or_abort(&S.full[s], (k / kStages) & 1, &S.abort, p.status);
+            if (warp == 0) wait_or_abort(&S.full[s], (k / kStages) & 1, &S.abort, p.status, p.wait_ns);
             named_bar_sync(1, kMath);
             if (*(volatile uint32_t*)&S.abort) break;
             unsigned char* sV = sm + OFF_RING + s * STAGE_BYTES;
@@ -885,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         // after an abort, let the copies already issued land before exiting
         if (tid == 0 && *(volatile uint32_t*)&S.abort)
             for (int k = issued > kStages ? issued - kStages : 0; k < issued; k++)
-                mbar_wait(&S.full[k % kStages], (k / kStages) & 1, nullptr, 1u << 20);
+                mbar_wait(&S.full[k % kStages], (k / kStages) & 1, nullptr, p.wait_ns);
     }
     tc_fence_before();
     __syncthreads();
@@ -928,6 +930,15 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv = a.dv;
     p.logits = a.logits;
     p.nchunks = (a.T + kC - 1) / kC;
+    // Failure-path test hook: with GDN_TEST_STARVE_CHUNK=k in the environment the loads of chunk k are never
+    // issued, so its bounded wait expires (after kTestWaitNs), the kernel winds down and the status word reads
+    // GDN_ERR_TIMEOUT.  Without the variable nothing changes.
+    p.starve_chunk = -1;
+    p.wait_ns = kWaitNs;
+    if (const char* e = getenv("GDN_TEST_STARVE_CHUNK")) {
+        p.starve_chunk = atoi(e);
+        p.wait_ns = kTestWaitNs;
+    }
     *handled = true;
     const dim3 grid(a.B * a.H, (a.dv + 63) / 64);
     if (a.norm)

@@ -53,13 +53,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false (and sets *err to 1 if err is not null) when the limit is reached.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
-                                          uint32_t limit = 1u << 26)
+__device__ __forceinline__ uint64_t global_ns()
 {
-    for (uint32_t i = 0; i < limit; i++)
-        if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase with the given parity to complete: gives up after
+// limit_ns nanoseconds of the global timer (and, as a backstop, after 2^30
+// polls).  Returns false (and sets *err to 1 if err is not null) on expiry.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < (1u << 24); i++) {
+#pragma unroll 1
+        for (int k = 0; k < 64; k++)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) break;
+    }
     if (err) atomicExch(err, 1u);
     return false;
 }

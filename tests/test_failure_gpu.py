@@ -1,0 +1,73 @@
+"""The failure path of the bounded device waits, exercised without faulting the GPU.
+
+Every wait of the tcgen05 forward (a chunk's loads, the tensor-core products) has a
+time limit; on expiry the kernel records GDN_ERR_TIMEOUT in the workspace status
+word, lets the copies it issued land, frees its tensor memory and returns.  The
+test makes a wait run out by the library's test hook GDN_TEST_STARVE_CHUNK=k (the
+loads of chunk k are never issued, so nothing ever completes that stage) and
+checks the status the host reads, the time it took, and that the same context
+then runs a normal forward to parity.
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_recurrence_delta_gb300 as gdn
+import oracle
+from linear_attention_recurrence_delta_gb300 import inputs as I
+from tests.gdn_testlib import TOL, assert_close, dev, dev32, run_fwd, shape_of, tdtype
+
+pytestmark = pytest.mark.gpu
+
+GDN_ERR_TIMEOUT = 7
+
+
+def fwd_raw(w, x):
+    """gdn_fwd without the status check: returns (call status, device status, seconds)."""
+    s = shape_of(w)
+    t = {k: dev(x[k], w.dtype) for k in ("v", "b", "c", "g", "beta")}
+    o = torch.empty((w.B, w.T, w.H, w.dv), dtype=tdtype(w.dtype), device="cuda")
+    hT = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+    ws = torch.empty(gdn.gdn_workspace_bytes(s, 0), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rc = gdn.gdn_fwd(s, t["v"], t["b"], t["c"], t["g"], t["beta"], dev32(x["A_log"]), None, o, hT, ws)
+    st = gdn.gdn_last_device_status(ws)
+    return rc, st, time.perf_counter() - t0
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+@pytest.mark.parametrize("chunk", [0, 2])
+def test_starved_load_times_out_and_context_survives(monkeypatch, mode, chunk):
+    w = I.custom(name=f"starve_{mode}_{chunk}", mode=mode, dtype="bf16", B=2, H=4, T=256, dk=64, dv=64, seed=3)
+    x = I.make_inputs(w)
+    monkeypatch.setenv("GDN_TEST_STARVE_CHUNK", str(chunk))
+    rc, st, secs = fwd_raw(w, x)
+    assert rc == gdn.GDN_OK               # the launch itself succeeded
+    assert st == GDN_ERR_TIMEOUT          # the device reported the expired wait
+    assert secs < 10.0
+    monkeypatch.delenv("GDN_TEST_STARVE_CHUNK")
+    o, hT = run_fwd(w, x)                 # the context is still usable
+    ro, rhT = oracle.gdn_fwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], None, mode=mode)
+    assert_close(o, ro, TOL["bf16"], "o after the timeout")
+    assert_close(hT, rhT, TOL["bf16"], "hT after the timeout")
+
+
+def test_stale_status_word_is_cleared():
+    """A status word left poisoned in the workspace by an earlier call does not leak into the next one."""
+    w = I.custom(name="poison", mode="delta", dtype="bf16", B=1, H=2, T=130, dk=64, dv=64, seed=8)
+    x = I.make_inputs(w)
+    s = shape_of(w)
+    t = {k: dev(x[k], w.dtype) for k in ("v", "b", "c", "g", "beta")}
+    o = torch.empty((w.B, w.T, w.H, w.dv), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(gdn.gdn_workspace_bytes(s, 0), dtype=torch.uint8, device="cuda")
+    ws[:8].view(torch.int32)[0] = GDN_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    assert gdn.gdn_last_device_status(ws) != gdn.GDN_OK
+    rc = gdn.gdn_fwd(s, t["v"], t["b"], t["c"], t["g"], t["beta"], dev32(x["A_log"]), None, o, None, ws)
+    assert rc == gdn.GDN_OK
+    assert gdn.gdn_last_device_status(ws) == gdn.GDN_OK
+    ro, _ = oracle.gdn_fwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], None, mode="delta")
+    assert_close(o.double().cpu().numpy(), ro, TOL["bf16"], "o")
