@@ -82,7 +82,12 @@ enum {
      * not spell out this step; it is the plain L2 normalisation of a key and
      * a read vector, fused so that no separate pass over b and c is needed.
      * Without the bit b and c are used as given. */
-    GDN_NORM_BC = 0x200
+    GDN_NORM_BC = 0x200,
+    /* After the kernels, scan every output (forward: o and hT; backward:
+     * every gradient) for NaN and Inf; gdn_last_device_status then reports
+     * GDN_ERR_NONFINITE if one was found.  A diagnostic for training runs:
+     * it costs one read of the outputs and changes no result. */
+    GDN_CHECK_FINITE = 0x400
 };
 
 typedef enum {
@@ -99,7 +104,9 @@ typedef enum {
     GDN_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than required     */
     GDN_ERR_CUDA = 6,        /* a CUDA call or kernel launch failed         */
     GDN_ERR_TIMEOUT = 7,     /* a bounded device-side wait expired          */
-    GDN_ERR_DEVICE = 8       /* the current device is not an sm_103 GPU     */
+    GDN_ERR_DEVICE = 8,      /* the current device is not an sm_103 GPU     */
+    GDN_ERR_NONFINITE = 9    /* an output holds NaN or Inf (checked only
+                                with GDN_CHECK_FINITE)                      */
 } gdn_status_t;
 
 typedef struct {

@@ -20,11 +20,13 @@ import threading
 GDN_GATED, GDN_DELTA = 0, 1
 GDN_GATE_LOGITS = 0x100      # option bit: g and beta arrive before their sigmoid
 GDN_NORM_BC = 0x200          # option bit: b and c arrive before their L2 normalisation
+GDN_CHECK_FINITE = 0x400     # option bit: scan the outputs for NaN / Inf (status GDN_ERR_NONFINITE)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_OK = 0
 STATUS_NAMES = {
     0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_ALIGN", 4: "GDN_ERR_MODE",
     5: "GDN_ERR_WORKSPACE", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_DEVICE",
+    9: "GDN_ERR_NONFINITE",
 }
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -48,13 +50,16 @@ class gdn_shape_t(ctypes.Structure):
                 f"mode={self.mode}, io={self.io})")
 
 
-def make_shape(B, H, T, dk, dv, mode="gated", io="bf16", gate_logits=False, norm_bc=False) -> gdn_shape_t:
+def make_shape(B, H, T, dk, dv, mode="gated", io="bf16", gate_logits=False, norm_bc=False,
+               check_finite=False) -> gdn_shape_t:
     m = {"gated": GDN_GATED, "delta": GDN_DELTA}.get(mode, mode)
     d = {"f32": GDN_F32, "bf16": GDN_BF16}.get(io, io)
     if gate_logits:
         m = int(m) | GDN_GATE_LOGITS
     if norm_bc:
         m = int(m) | GDN_NORM_BC
+    if check_finite:
+        m = int(m) | GDN_CHECK_FINITE
     return gdn_shape_t(int(B), int(H), int(T), int(dk), int(dv), int(m), int(d))
 
 

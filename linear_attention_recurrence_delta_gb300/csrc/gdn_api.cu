@@ -144,14 +144,15 @@ static gdn_status_t check_common(const gdn_shape_t* s, const void* v, const void
 }
 
 // Split the option bits off the mode: `out` gets the plain mode, `logits` the
-// GDN_GATE_LOGITS bit, `norm` the GDN_NORM_BC bit.  False if the mode carries
-// an unknown bit.
-static bool split_mode(const gdn_shape_t* in, gdn_shape_t* out, int* logits, int* norm)
+// GDN_GATE_LOGITS bit, `norm` the GDN_NORM_BC bit, `check` (if not null) the
+// GDN_CHECK_FINITE bit.  False if the mode carries an unknown bit.
+static bool split_mode(const gdn_shape_t* in, gdn_shape_t* out, int* logits, int* norm, int* check = nullptr)
 {
     *out = *in;
     *logits = (in->mode & GDN_GATE_LOGITS) != 0;
     *norm = (in->mode & GDN_NORM_BC) != 0;
-    out->mode = in->mode & ~(GDN_GATE_LOGITS | GDN_NORM_BC);
+    if (check) *check = (in->mode & GDN_CHECK_FINITE) != 0;
+    out->mode = in->mode & ~(GDN_GATE_LOGITS | GDN_NORM_BC | GDN_CHECK_FINITE);
     return (out->mode & ~0xff) == 0;
 }
 
@@ -197,9 +198,9 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, cons
                                 void* o, float* hT, void* ws, size_t ws_bytes, gdn_stream_t stream)
 {
     gdn_shape_t sh;
-    int logits = 0, norm = 0;
+    int logits = 0, norm = 0, check = 0;
     if (!shape_in) return GDN_ERR_NULL;
-    if (!split_mode(shape_in, &sh, &logits, &norm)) return GDN_ERR_MODE;
+    if (!split_mode(shape_in, &sh, &logits, &norm, &check)) return GDN_ERR_MODE;
     const gdn_shape_t* shape = &sh;
     gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 0, norm);
     if (r != GDN_OK) return r;
@@ -223,7 +224,11 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, cons
         return GDN_OK;
     }
     const int P = tsplit_factor(*shape, 0);
-    const cudaError_t e = P > 1 ? launch_fwd_tsplit(a, ws_layout(*shape, 0, norm), P, st, fwd_core) : fwd_core(a, st);
+    cudaError_t e = P > 1 ? launch_fwd_tsplit(a, ws_layout(*shape, 0, norm), P, st, fwd_core) : fwd_core(a, st);
+    if (e == cudaSuccess && check) {
+        e = launch_check_finite(o, (size_t)a.B * a.T * a.H * a.dv, a.io, ws, st);
+        if (e == cudaSuccess && hT) e = launch_check_finite(hT, state_bytes / sizeof(float), GDN_F32, ws, st);
+    }
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -234,9 +239,9 @@ extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape_in, const void* v, cons
                                 gdn_stream_t stream)
 {
     gdn_shape_t sh;
-    int logits = 0, norm = 0;
+    int logits = 0, norm = 0, check = 0;
     if (!shape_in) return GDN_ERR_NULL;
-    if (!split_mode(shape_in, &sh, &logits, &norm)) return GDN_ERR_MODE;
+    if (!split_mode(shape_in, &sh, &logits, &norm, &check)) return GDN_ERR_MODE;
     const gdn_shape_t* shape = &sh;
     gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 1, norm);
     if (r != GDN_OK) return r;
@@ -259,7 +264,15 @@ extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape_in, const void* v, cons
     a.dO = dO; a.dhT = dhT; a.dv_ = dv; a.db = db; a.dc = dc; a.dg = dg; a.dbeta = dbeta;
     a.dA_log = dA_log; a.dh0 = dh0; a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits; a.norm = norm;
     const int P = a.T > 0 ? tsplit_factor(*shape, 1) : 1;
-    const cudaError_t e = P > 1 ? launch_bwd_tsplit(a, ws_layout(*shape, 1, norm), P, st, fwd_core) : launch_serial_bwd(a, st);
+    cudaError_t e = P > 1 ? launch_bwd_tsplit(a, ws_layout(*shape, 1, norm), P, st, fwd_core) : launch_serial_bwd(a, st);
+    if (e == cudaSuccess && check) {
+        const size_t ntok = (size_t)a.B * a.T * a.H, st_n = (size_t)a.B * a.H * a.dk * a.dv;
+        const struct { const void* p; size_t n; int io; } outs[] = {
+            {dv, ntok * a.dv, a.io}, {db, ntok * a.dk, a.io}, {dc, ntok * a.dk, a.io}, {dg, ntok, a.io},
+            {dbeta, ntok, a.io}, {dA_log, (size_t)a.H * a.dk, GDN_F32}, {dh0, st_n, GDN_F32}};
+        for (const auto& x : outs)
+            if (e == cudaSuccess && x.p && x.n) e = launch_check_finite(x.p, x.n, x.io, ws, st);
+    }
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -269,7 +282,8 @@ extern "C" gdn_status_t gdn_last_device_status(const void* ws, gdn_stream_t stre
     uint32_t word[2] = {0, 0};
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
     if (cudaMemcpy(word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
-    return word[0] == kDevOk ? GDN_OK : GDN_ERR_TIMEOUT;
+    if (word[0] != kDevOk) return GDN_ERR_TIMEOUT;
+    return word[1] != 0 ? GDN_ERR_NONFINITE : GDN_OK;
 }
 
 extern "C" const char* gdn_status_string(gdn_status_t s)
@@ -284,6 +298,7 @@ extern "C" const char* gdn_status_string(gdn_status_t s)
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA call failed";
         case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait expired";
         case GDN_ERR_DEVICE: return "GDN_ERR_DEVICE: the current device is not sm_103";
+        case GDN_ERR_NONFINITE: return "GDN_ERR_NONFINITE: an output holds NaN or Inf";
     }
     return "unknown gdn status";
 }

@@ -103,7 +103,8 @@ struct DecSmem {
     float xcol[64];
 };
 
-template <typename IO, bool DELTA, int ROWS>
+// NORM: b and c arrive before their L2 normalisation (a template flag, so the plain kernel carries no trace of it)
+template <typename IO, bool DELTA, int ROWS, bool NORM>
 __global__ void __launch_bounds__(256) decode_kernel(Args a, bool vec4, int nslab)
 {
     constexpr int K = ROWS / 16;   // state rows per thread
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(256) decode_kernel(Args a, bool vec4, int nsla
             else cp_async_wait_all();
         }
         __syncthreads();
-        if (a.norm) {   // inverse norms of the staged b_t and c_t, one thread per vector
+        if (NORM) {   // inverse norms of the staged b_t and c_t, one thread per vector
             if (tid < 2 * T) {
                 const int tt = tid >> 1;
                 const float* x = (tid & 1) ? S.sC[tt] : S.sB[tt];
@@ -191,12 +192,18 @@ __global__ void __launch_bounds__(256) decode_kernel(Args a, bool vec4, int nsla
 
         for (int tt = 0; tt < T; tt++) {
             float al[K], bk[K], ck[K];
-            const float nbt = a.norm ? S.nb[tt] : 1.f, nct = a.norm ? S.nc[tt] : 1.f;
 #pragma unroll
             for (int k = 0; k < K; k++) {
                 al[k] = S.sAl[tt][rg + 16 * k];
-                bk[k] = S.sB[tt][rg + 16 * k] * nbt;
-                ck[k] = S.sC[tt][rg + 16 * k] * nct;
+                bk[k] = S.sB[tt][rg + 16 * k];
+                ck[k] = S.sC[tt][rg + 16 * k];
+            }
+            if (NORM) {
+#pragma unroll
+                for (int k = 0; k < K; k++) {
+                    bk[k] *= S.nb[tt];
+                    ck[k] *= S.nc[tt];
+                }
             }
             float hp[K][4];
 #pragma unroll
@@ -269,7 +276,7 @@ __global__ void __launch_bounds__(256) decode_kernel(Args a, bool vec4, int nsla
     }
 }
 
-template <typename IO, bool DELTA, int ROWS>
+template <typename IO, bool DELTA, int ROWS, bool NORM>
 cudaError_t launch_rows(const Args& a, cudaStream_t st)
 {
     // float4 state access needs whole 16-byte column quads in every row
@@ -277,14 +284,14 @@ cudaError_t launch_rows(const Args& a, cudaStream_t st)
                       (!a.hT || ((uintptr_t)a.hT & 15) == 0);
     const size_t smem = ROWS == 64 ? 0 : sizeof(DecSmem<ROWS>);   // 64 rows: static shared memory
     if (smem) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<IO, DELTA, ROWS>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<IO, DELTA, ROWS, NORM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     int sms = 0, dev = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<IO, DELTA, ROWS>, 256, smem) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<IO, DELTA, ROWS, NORM>, 256, smem) !=
             cudaSuccess)
         return cudaErrorUnknown;
     if (per_sm < 1) per_sm = 1;
@@ -292,14 +299,15 @@ cudaError_t launch_rows(const Args& a, cudaStream_t st)
     const int nslab = (a.dv + 63) / 64;
     const int items = a.B * a.H * nslab;
     const int grid = items < sms * per_sm ? items : sms * per_sm;
-    decode_kernel<IO, DELTA, ROWS><<<grid, 256, smem, st>>>(a, vec4, nslab);
+    decode_kernel<IO, DELTA, ROWS, NORM><<<grid, 256, smem, st>>>(a, vec4, nslab);
     return cudaGetLastError();
 }
 
 template <typename IO, bool DELTA>
 cudaError_t launch_t(const Args& a, cudaStream_t st)
 {
-    return a.dk <= 64 ? launch_rows<IO, DELTA, 64>(a, st) : launch_rows<IO, DELTA, 128>(a, st);
+    if (a.norm) return a.dk <= 64 ? launch_rows<IO, DELTA, 64, true>(a, st) : launch_rows<IO, DELTA, 128, true>(a, st);
+    return a.dk <= 64 ? launch_rows<IO, DELTA, 64, false>(a, st) : launch_rows<IO, DELTA, 128, false>(a, st);
 }
 
 }  // namespace

@@ -86,6 +86,11 @@ int decode_max_tokens();
 constexpr float kNormFloor = 1e-12f;   // L2 normalisation: x / max(||x||, kNormFloor)
 
 // Device status word helpers.
+// word 0: a bounded wait expired; word 1: GDN_CHECK_FINITE found NaN or Inf in an output
 enum : uint32_t { kDevOk = 0, kDevTimeout = 1 };
+
+// GDN_CHECK_FINITE: flag word 1 of the status block if any of the n elements is NaN or Inf
+// (io: GDN_BF16 or GDN_F32 element type)
+cudaError_t launch_check_finite(const void* p, size_t n, int io, void* ws, cudaStream_t st);
 
 }  // namespace gdn

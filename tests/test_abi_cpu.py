@@ -160,7 +160,7 @@ def test_gate_logits_option_bit():
     assert logit.mode == gdn.GDN_DELTA | gdn.GDN_GATE_LOGITS
     for bwd in (0, 1):
         assert gdn.gdn_workspace_bytes(logit, bwd) == gdn.gdn_workspace_bytes(plain, bwd) > 0
-    bad = gdn.make_shape(2, 4, 300, 64, 64, gdn.GDN_DELTA | 0x400, "bf16")
+    bad = gdn.make_shape(2, 4, 300, 64, 64, gdn.GDN_DELTA | 0x800, "bf16")
     assert gdn.gdn_workspace_bytes(bad, 0) == 0
 
 
@@ -178,3 +178,13 @@ def test_norm_bc_option_bit():
     extra = B * T * H * (2 * d + 2) * 4
     assert gdn.gdn_workspace_bytes(norm, 1) >= gdn.gdn_workspace_bytes(plain, 1) + extra
     assert gdn.gdn_workspace_bytes(both, 1) == gdn.gdn_workspace_bytes(norm, 1)
+
+
+def test_check_finite_option_bit():
+    """GDN_CHECK_FINITE changes no workspace size and combines with the other bits."""
+    plain = gdn.make_shape(2, 4, 300, 64, 64, "delta", "bf16")
+    chk = gdn.make_shape(2, 4, 300, 64, 64, "delta", "bf16", gate_logits=True, check_finite=True)
+    assert chk.mode == gdn.GDN_DELTA | gdn.GDN_GATE_LOGITS | gdn.GDN_CHECK_FINITE
+    for bwd in (0, 1):
+        assert gdn.gdn_workspace_bytes(chk, bwd) == gdn.gdn_workspace_bytes(plain, bwd) > 0
+    assert gdn.gdn_status_string(9).startswith("GDN_ERR_NONFINITE")

@@ -71,3 +71,57 @@ def test_stale_status_word_is_cleared():
     assert gdn.gdn_last_device_status(ws) == gdn.GDN_OK
     ro, _ = oracle.gdn_fwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], None, mode="delta")
     assert_close(o.double().cpu().numpy(), ro, TOL["bf16"], "o")
+
+
+GDN_ERR_NONFINITE = 9
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+def test_check_finite_flags_nan_outputs(mode, io):
+    """GDN_CHECK_FINITE: a NaN in one value element reaches the outputs, and the status word says so; clean
+    inputs leave it GDN_OK; without the bit nothing is checked."""
+    w = I.custom(name=f"fin_{mode}_{io}", mode=mode, dtype=io, B=1, H=2, T=100, dk=64, dv=64, seed=21)
+    x = I.make_inputs(w)
+    bad = dict(x)
+    bad["v"] = x["v"].copy()
+    bad["v"][0, 37, 1, 5] = np.nan
+
+    def status(inputs, check):
+        s = gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, mode, io, check_finite=check)
+        t = {k: dev(inputs[k], io) for k in ("v", "b", "c", "g", "beta")}
+        o = torch.empty((w.B, w.T, w.H, w.dv), dtype=tdtype(io), device="cuda")
+        hT = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+        ws = torch.empty(gdn.gdn_workspace_bytes(s, 0), dtype=torch.uint8, device="cuda")
+        gdn.check(gdn.gdn_fwd(s, t["v"], t["b"], t["c"], t["g"], t["beta"], dev32(inputs["A_log"]), None, o, hT, ws))
+        return gdn.gdn_last_device_status(ws)
+
+    assert status(x, True) == gdn.GDN_OK
+    assert status(bad, True) == GDN_ERR_NONFINITE
+    assert status(bad, False) == gdn.GDN_OK
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+def test_check_finite_backward(mode):
+    """The backward's check covers every gradient: a NaN in one output-gradient element is reported."""
+    w = I.custom(name=f"finb_{mode}", mode=mode, dtype="bf16", B=1, H=2, T=70, dk=32, dv=32, seed=22,
+                 backward=True)
+    x = I.make_inputs(w)
+    B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
+
+    def status(dO):
+        s = gdn.make_shape(B, H, T, dk, dv, mode, "bf16", check_finite=True)
+        t = {k: dev(x[k], "bf16") for k in ("v", "b", "c", "g", "beta")}
+        g = {k: torch.empty(sh, dtype=torch.bfloat16, device="cuda") for k, sh in
+             (("dv", (B, T, H, dv)), ("db", (B, T, H, dk)), ("dc", (B, T, H, dk)), ("dg", (B, T, H)))}
+        dbeta = torch.empty((B, T, H), dtype=torch.bfloat16, device="cuda") if mode == "delta" else None
+        dA = torch.empty((H, dk), dtype=torch.float32, device="cuda")
+        ws = torch.empty(gdn.gdn_workspace_bytes(s, 1), dtype=torch.uint8, device="cuda")
+        gdn.check(gdn.gdn_bwd(s, t["v"], t["b"], t["c"], t["g"], t["beta"], dev32(x["A_log"]), None,
+                              dev(dO, "bf16"), None, g["dv"], g["db"], g["dc"], g["dg"], dbeta, dA, None, ws))
+        return gdn.gdn_last_device_status(ws)
+
+    assert status(x["dO"]) == gdn.GDN_OK
+    bad = x["dO"].copy()
+    bad[0, 50, 1, 3] = np.inf
+    assert status(bad) == GDN_ERR_NONFINITE
