@@ -40,7 +40,7 @@
  * detect on the device (an expired bounded wait) are written to a status
  * word at the start of the workspace, which gdn_last_device_status reads.
  *
- * Limits: B, H >= 1; T >= 0 (with T = 0 the per-token pointers may be NULL:
+ * Limits: B, H >= 1 and B * H <= 2^26; T >= 0 (with T = 0 the per-token pointers may be NULL:
  * the forward copies h0, or zeros, to hT; the backward writes dh0 = dhT and
  * dA_log = 0); 1 <= d_k, d_v <= 128 (the tensor-core forward takes
  * d_k <= 64, wider keys the token-serial kernels).  With io = GDN_BF16, d_k

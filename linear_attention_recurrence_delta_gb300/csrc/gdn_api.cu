@@ -14,6 +14,8 @@ static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 static bool shape_ok(const gdn_shape_t& s)
 {
     if (s.B < 1 || s.H < 1 || s.T < 0) return false;
+    // (batch, head) units index grids and int unit counters: at most 2^26 of them
+    if ((double)s.B * s.H > (double)(1 << 26)) return false;
     if (s.dk < 1 || s.dk > 128 || s.dv < 1 || s.dv > 128) return false;
     if (s.io == GDN_BF16 && ((s.dk % 8) || (s.dv % 8))) return false;
     // keep every element offset inside a signed 64-bit range with margin

@@ -141,11 +141,13 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
     FwdSmem<IO, LPC>& s = *reinterpret_cast<FwdSmem<IO, LPC>*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int ig = lane % LPC, jl = lane / LPC, cl = (32 / LPC) * w + jl;
+    // one flat index over (unit, column slab), a unit's slabs adjacent so that they share b and c in L2
+    const int nslab = (a.dv + NC - 1) / NC;
     Unit U;
-    U.u = blockIdx.y;
+    U.u = blockIdx.x / nslab;
     U.bb = U.u / a.H;
     U.h = U.u % a.H;
-    U.jc0 = blockIdx.x * NC;
+    U.jc0 = (blockIdx.x % nslab) * NC;
     U.ncols = min(NC, a.dv - U.jc0);
     const int j = U.jc0 + cl, dk = a.dk, dv = a.dv, T = a.T, H = a.H;
     const int nblk = (T + kTB - 1) / kTB;
@@ -244,7 +246,7 @@ cudaError_t launch_lpc(const Args& a, cudaStream_t st)
     const size_t sz = sizeof(IO);
     const bool vec = (a.dk * sz) % 16 == 0 && (a.dv * sz) % 16 == 0 && al16(a.b) && al16(a.c) && al16(a.v);
     constexpr int NC = FCfg<LPC>::COLS;
-    dim3 grid((a.dv + NC - 1) / NC, a.B * a.H);
+    const unsigned grid = (unsigned)((a.dv + NC - 1) / NC) * (unsigned)(a.B * a.H);
     serial_fwd_kernel<IO, DELTA, LPC><<<grid, 128, smem, st>>>(a, vec);
     return cudaGetLastError();
 }

@@ -54,7 +54,7 @@ def test_workspace_sizes(lib):
     assert b > f and b % 256 == 0
     assert gdn.gdn_workspace_bytes(gdn.make_shape(1, 1, 0, 8, 8), 1) >= 256
     for bad in (gdn.make_shape(0, 1, 8, 8, 8), gdn.make_shape(1, 1, 8, 129, 8), gdn.make_shape(1, 1, 8, 8, 0),
-                gdn.make_shape(1, 1, 8, 8, 136, "delta", "bf16"),
+                gdn.make_shape(1, 1, 8, 8, 136, "delta", "bf16"), gdn.make_shape(1 << 14, 1 << 13, 1, 8, 8),
                 gdn.make_shape(1, 1, -1, 8, 8), gdn.make_shape(1, 1, 8, 12, 8, "gated", "bf16"),
                 gdn.make_shape(1, 1, 8, 8, 8, 7, "bf16"), gdn.make_shape(1, 1, 8, 8, 8, "gated", 5)):
         assert gdn.gdn_workspace_bytes(bad, 0) == 0

@@ -174,3 +174,11 @@ def test_shape_40_heads_d32_fwd_bwd():
     w = base.with_(name="delta_bf16_2x40x4096x32", B=2, backward=True)
     check_fwd(w)
     check_bwd(w, units=[0, 17, 39])
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+def test_fwd_many_units_serial(mode):
+    """More (batch, head) units than a grid's y dimension holds (65535): the token-serial forward (fp32 I/O)
+    indexes them on one flat grid."""
+    w = I.custom(name=f"many_{mode}", mode=mode, dtype="f32", B=35000, H=2, T=11, dk=8, dv=8, seed=12, h0_std=0.3)
+    check_fwd(w)
