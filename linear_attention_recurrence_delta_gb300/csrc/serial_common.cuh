@@ -23,10 +23,9 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 // A staged per-token row vector (alpha, b or c over the d_k state rows) keeps
-// rows 16q..16q+15 at offsets 20q..20q+15: a thread that owns 16 consecutive
-// rows reads them as four 16-byte loads, and the four row groups of a warp
-// land in disjoint banks.
-constexpr int kRowPad = 80;
+// rows 16q..16q+15 at offsets 20q..20q+15 (a padded length of 5/4 of the rows):
+// a thread that owns 16 consecutive rows reads them as four 16-byte loads, and
+// the row groups of a warp land in disjoint banks.
 __device__ __forceinline__ int prow(int i) { return i + ((i >> 4) << 2); }
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
