@@ -110,7 +110,7 @@ constexpr uint32_t TM_COLS = 512;
 struct Small {
     float G[64];
     float A2[64];
-    float decay[64];
+    float decay[2][64];     // exp(Gam_63) of the chunk, by chunk parity (read by the chunk's deferred epilogue)
     float g[kStages][64];
     float beta[kStages][64];
     float nb[64], nc[64];   // GDN_NORM_BC: 1 / max(||b_t||, floor), the same for c_t, of the current chunk
@@ -243,6 +243,63 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
         fence_proxy_async_smem();
         named_bar_sync(1, kMath);
+        // (15) chunk kk's state update (lanes 0..63) and output (lanes 64..127), 32 columns per thread.  It runs
+        // while the next chunk's level products execute (they write TMEM columns 0..223 and read the operand
+        // region; this reads the output columns and writes the state tiles, which only the tail products read).
+        auto epilogue = [&](int kk) {
+            const uint32_t tm_out = DELTA ? TM_CHD : TM_CHG;
+            if (state_row) {
+                const float dec = S.decay[kk & 1][trow];
+#pragma unroll
+                for (int cc = 0; cc < 2; cc++) {
+                    float v[16];
+                    tmem_ld16(tl + tm_out + 32 * wh + 16 * cc, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; c++) Sreg[16 * cc + c] = fmaf(dec, Sreg[16 * cc + c], v[c]);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    float v8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
+                    st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
+                }
+            } else {
+                const int tg = kk * kC + (trow - 64);
+                __nv_bfloat16* orow = p.o + (((size_t)bb * T + tg) * H + h) * dv + jc0;
+#pragma unroll
+                for (int cc = 0; cc < 2; cc++) {
+                    const int col = 32 * wh + 16 * cc;
+                    float v[16];
+                    tmem_ld16(tl + tm_out + col, v);
+                    if (DELTA) {
+                        float w2[16];
+                        tmem_ld16(tl + TM_U + col, w2);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; c++) v[c] += w2[c];
+                    } else {
+                        tmem_wait_ld();
+                    }
+                    if (tg < T) {
+#pragma unroll
+                        for (int hq = 0; hq < 2; hq++) {
+                            const int j0 = col + 8 * hq;
+                            if (j0 < nv) {
+                                uint4 wv;
+                                wv.x = pack_bf16(v[8 * hq + 0], v[8 * hq + 1]);
+                                wv.y = pack_bf16(v[8 * hq + 2], v[8 * hq + 3]);
+                                wv.z = pack_bf16(v[8 * hq + 4], v[8 * hq + 5]);
+                                wv.w = pack_bf16(v[8 * hq + 6], v[8 * hq + 7]);
+                                *reinterpret_cast<uint4*>(orow + j0) = wv;
+                            }
+                        }
+                    }
+                }
+            }
+        };
+        int pending = -1;   // chunk whose epilogue has not run yet
         uint32_t mma_phase = 0;
         // one warp polls the mbarrier; the others sleep in the named barrier
         auto mma_wait_all = [&]() -> bool {
@@ -495,8 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         st_row8_split(sm + OFF_CH0, sm + OFF_CH0L, i, 2 * sq + h2, y8);
                     }
                 }
-                if (r < 64) S.decay[r] = fast_exp2(S.A2[r] * S.G[63]);
+                if (r < 64) S.decay[k & 1][r] = fast_exp2(S.A2[r] * S.G[63]);
             }
+            if (pending >= 0) epilogue(pending), pending = -1;   // the previous chunk's, under the level products
             if (!mma_wait_all()) break;
 
             // (4) assemble P (lanes 0..63) and M (lanes 64..127); thread = (row, 32 columns)
@@ -812,58 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 if (!mma_wait_all()) break;
             }
 
-            // (15) state update (lanes 0..63) and output (lanes 64..127), 32 columns per thread
-            const uint32_t tm_out = DELTA ? TM_CHD : TM_CHG;
-            if (state_row) {
-                const float dec = S.decay[trow];
-#pragma unroll
-                for (int cc = 0; cc < 2; cc++) {
-                    float v[16];
-                    tmem_ld16(tl + tm_out + 32 * wh + 16 * cc, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 16; c++) Sreg[16 * cc + c] = fmaf(dec, Sreg[16 * cc + c], v[c]);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    float v8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
-                    st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
-                }
-            } else {
-                const int tg = k * kC + (trow - 64);
-                __nv_bfloat16* orow = p.o + (((size_t)bb * T + tg) * H + h) * dv + jc0;
-#pragma unroll
-                for (int cc = 0; cc < 2; cc++) {
-                    const int col = 32 * wh + 16 * cc;
-                    float v[16];
-                    tmem_ld16(tl + tm_out + col, v);
-                    if (DELTA) {
-                        float w2[16];
-                        tmem_ld16(tl + TM_U + col, w2);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 16; c++) v[c] += w2[c];
-                    } else {
-                        tmem_wait_ld();
-                    }
-                    if (tg < T) {
-#pragma unroll
-                        for (int hq = 0; hq < 2; hq++) {
-                            const int j0 = col + 8 * hq;
-                            if (j0 < nv) {
-                                uint4 wv;
-                                wv.x = pack_bf16(v[8 * hq + 0], v[8 * hq + 1]);
-                                wv.y = pack_bf16(v[8 * hq + 2], v[8 * hq + 3]);
-                                wv.z = pack_bf16(v[8 * hq + 4], v[8 * hq + 5]);
-                                wv.w = pack_bf16(v[8 * hq + 6], v[8 * hq + 7]);
-                                *reinterpret_cast<uint4*>(orow + j0) = wv;
-                            }
-                        }
-                    }
-                }
-            }
+            pending = k;   // its state update and outputs run under the next chunk's level products
             smem_to_tc();
             // stage s is free again (every read of it, and the last MMA, are done)
             if (k + kStages < p.nchunks) {
@@ -878,6 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 if (r == 0) issue_load(k + kStages), issued = k + kStages + 1;
             }
         }
+        if (pending >= 0 && *(volatile uint32_t*)&S.abort == 0) epilogue(pending);
         if (state_row && p.hT && trow < dk) {
             float* hrow = p.hT + ((size_t)u * dk + trow) * dv + jc0;
 #pragma unroll
