@@ -84,7 +84,8 @@ constexpr uint32_t X_NA = 0, X_NXH = 16384, X_NXL = 40960;
 //   delta phase 4: [Util | W] = Z + N^2 Z
 constexpr uint32_t X_N2A = 0, X_ZH = 16384, X_ZL = 32768;
 //   delta phase 5: the state products
-constexpr uint32_t X_CW = 0, X_UH = 16384, X_UL = 24576;
+//   (CW sits past the phase-4 operands so that its Ctil rows can be built while the phase-4 products run)
+constexpr uint32_t X_CW = 49152, X_UH = 16384, X_UL = 24576;
 constexpr uint32_t X_BYTES = 102400;
 constexpr uint32_t OFF_CH0 = OFF_X + X_BYTES;          // [Bhat^T ; P] hi
 constexpr uint32_t OFF_CH0L = OFF_CH0 + 16384;         // [Bhat^T ; P] lo
@@ -802,21 +803,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     mma_k64(tbase + TM_W, x0 + X_N2A, x0 + X_ZL + 8192, true, id, true);
                     mma_commit(&S.mma);
                 }
-                if (!mma_wait_all()) break;
-
-                // (11) CW = [-W ; Ctil]
-                if (state_row) {
-#pragma unroll
-                    for (int cc = 0; cc < 2; cc++) {
-                        const int cg = 2 * wh + cc;
-                        float v[16];
-                        tmem_ld16(tl + TM_W + 16 * cg, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 16; c++) v[c] = -v[c];
-                        st_plain16(X + X_CW, trow, cg, v);
-                    }
-                } else {
+                // (11) CW = [-W ; Ctil]: the Ctil rows (output lanes) while the products run
+                static_assert(X_CW >= X_ZL + 16384 && X_CW + 16384 <= X_BYTES, "CW clear of the phase-4 operands");
+                if (!state_row) {
                     const int t = trow - 64;
                     const float Gt = S.G[t];
 #pragma unroll
@@ -830,6 +819,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         }
                         scale8(cv, S.A2, q, Gt, y);
                         st_row8(X + X_CW, trow, q, y);
+                    }
+                }
+                if (!mma_wait_all()) break;
+                if (state_row) {   // the -W rows
+#pragma unroll
+                    for (int cc = 0; cc < 2; cc++) {
+                        const int cg = 2 * wh + cc;
+                        float v[16];
+                        tmem_ld16(tl + TM_W + 16 * cg, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; c++) v[c] = -v[c];
+                        st_plain16(X + X_CW, trow, cg, v);
                     }
                 }
                 smem_to_tc();
