@@ -109,7 +109,7 @@ constexpr uint32_t TM_CHD = 384;                       // delta: [dS ; P U]
 constexpr uint32_t TM_COLS = 512;
 
 struct Small {
-    float G[64];
+    float G[2][64];         // inclusive scan of g within the chunk, by chunk parity
     float A2[64];
     float decay[2][64];     // exp(Gam_63) of the chunk, by chunk parity (read by the chunk's deferred epilogue)
     float g[kStages][64];
@@ -117,7 +117,7 @@ struct Small {
     float nb[64], nc[64];   // GDN_NORM_BC: 1 / max(||b_t||, floor), the same for c_t, of the current chunk
     uint64_t full[kStages], mma;
     uint32_t tmem_base;
-    uint32_t unsafe;
+    uint32_t unsafe[2];     // the chunk's anchors could overflow, by chunk parity
     uint32_t abort;
     float a2max;
 };
@@ -300,6 +300,59 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
             }
         };
+        // (1) chunk kk's inclusive scan of g and the overflow check of its anchors (one warp), into G[kk & 1] and
+        // unsafe[kk & 1]; then its decay constants per (8-block, reference point), every exponent <= 0, into the
+        // constant tables (read by the chunk's operand and Bhat steps only)
+        auto scan = [&](int kk) {
+            float* Gn = S.G[kk & 1];
+            // lane l scans the pair (2l, 2l+1)
+            const float ga = S.g[kk % kStages][2 * lane], gb = S.g[kk % kStages][2 * lane + 1];
+            float x = ga + gb;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const float ex = __shfl_up_sync(0xffffffffu, x, 1);
+            Gn[2 * lane] = (lane > 0 ? ex : 0.f) + ga;
+            Gn[2 * lane + 1] = x;
+            __syncwarp();
+            float span = 0.f;
+            if (lane < 8) {
+                const float g0 = Gn[8 * lane], g3 = Gn[8 * lane + 3], g7 = Gn[8 * lane + 7];
+                span = fmaxf(g3 - g0, g7 - g3);
+            }
+            const bool bad = __any_sync(0xffffffffu, span * S.a2max > kSafeLog2);
+            if (lane == 0) S.unsafe[kk & 1] = bad ? 1u : 0u;
+        };
+        auto table_entry = [&](const float* Gn, int pr) {   // pr = 64 k8 + i
+            float* K = reinterpret_cast<float*>(sm + OFF_K);
+            const int k8 = pr >> 6, i = pr & 63, J = k8 >> 1;
+            const float a2 = S.A2[i], Gref = Gn[8 * k8 + 3];
+            K[(K_A1 * 8 + k8) * 64 + i] = J >= 1 ? fast_exp2(a2 * (Gref - Gn[16 * J - 1])) : 0.f;
+            K[(K_A2 * 8 + k8) * 64 + i] = (k8 & 1) ? fast_exp2(a2 * (Gref - Gn[16 * J + 7])) : 0.f;
+            K[(K_0 * 8 + k8) * 64 + i] = fast_exp2(a2 * Gref);
+            K[(K_B1_1 * 8 + k8) * 64 + i] = J < 1 ? fast_exp2(a2 * (Gn[15] - Gref)) : 0.f;
+            K[(K_B1_2 * 8 + k8) * 64 + i] = J < 2 ? fast_exp2(a2 * (Gn[31] - Gref)) : 0.f;
+            K[(K_B1_3 * 8 + k8) * 64 + i] = J < 3 ? fast_exp2(a2 * (Gn[47] - Gref)) : 0.f;
+            K[(K_B2 * 8 + k8) * 64 + i] = (k8 & 1) ? 0.f : fast_exp2(a2 * (Gn[16 * J + 7] - Gref));
+            K[(K_BH * 8 + k8) * 64 + i] = fast_exp2(a2 * (Gn[63] - Gref));
+        };
+        // all eight warps
+        auto prep_all = [&](int kk) {
+            if (warp == 0) scan(kk);
+            named_bar_sync(1, kMath);   // G and the overflow flag
+#pragma unroll
+            for (int rep = 0; rep < 2; rep++) table_entry(S.G[kk & 1], r + rep * kMath);
+        };
+        // warps 2, 3, 6, 7 (the two schedulers the inverse step leaves idle), named barrier 2 among them
+        auto prep_idle = [&](int kk) {
+            const int gw = (warp & 1) + ((warp >> 2) << 1), gt = 32 * gw + lane;
+            if (gw == 0) scan(kk);
+            named_bar_sync(2, 128);
+#pragma unroll
+            for (int rep = 0; rep < 4; rep++) table_entry(S.G[kk & 1], gt + rep * 128);
+        };
         int pending = -1;   // chunk whose epilogue has not run yet
         uint32_t mma_phase = 0;
         // one warp polls the mbarrier; the others sleep in the named barrier
@@ -317,6 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tc_fence_after();
         };
 
+        if (DELTA) {   // chunk 0's scan and constants (later chunks': under the previous chunk's inverse step)
+            prep_all(0);
+            named_bar_sync(1, kMath);
+        }
         for (int k = 0; k < p.nchunks; k++) {
             const int s = k % kStages;
             if (warp == 0) wait_or_abort(&S.full[s], (k / kStages) & 1, &S.abort, p.status, p.wait_ns);
@@ -337,29 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
             }
 
-            // (1) inclusive scan of g; overflow check of the anchors
-            if (warp == 0) {
-                // lane l scans the pair (2l, 2l+1)
-                const float ga = S.g[s][2 * lane], gb = S.g[s][2 * lane + 1];
-                float x = ga + gb;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += y;
-                }
-                const float ex = __shfl_up_sync(0xffffffffu, x, 1);
-                S.G[2 * lane] = (lane > 0 ? ex : 0.f) + ga;
-                S.G[2 * lane + 1] = x;
-                __syncwarp();
-                float span = 0.f;
-                if (lane < 8) {
-                    const float g0 = S.G[8 * lane], g3 = S.G[8 * lane + 3], g7 = S.G[8 * lane + 7];
-                    span = fmaxf(g3 - g0, g7 - g3);
-                }
-                const bool bad = __any_sync(0xffffffffu, span * S.a2max > kSafeLog2);
-                if (lane == 0) S.unsafe = bad ? 1u : 0u;
-            } else if (NORM && r < 32 + 128) {
-                // meanwhile warps 1..4: inverse norms of the chunk's b (rows 0..63) and c rows
+            // (1) the chunk's scan of g, overflow check and decay constants: gated here; delta in the previous
+            // chunk's inverse step (by its idle warps) or before the loop.  The inverse norms of b and c
+            // (GDN_NORM_BC) need the chunk's tiles, so warps 1..4 compute them here.
+            if (NORM && r >= 32 && r < 32 + 128) {
                 const int vr = r - 32, t = vr & 63;
                 float sq = 0.f;
 #pragma unroll
@@ -373,34 +411,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 if (vr < 64) S.nb[t] = inv;
                 else S.nc[t] = inv;
             }
-            named_bar_sync(1, kMath);   // G, the overflow flag (and the inverse norms)
-            // decay constants per (8-block, reference point); every exponent <= 0
-            {
-                float* K = reinterpret_cast<float*>(sm + OFF_K);
-#pragma unroll
-                for (int rep = 0; rep < 2; rep++) {
-                    const int pr = r + rep * kMath;
-                    const int k8 = pr >> 6, i = pr & 63, J = k8 >> 1;
-                    const float a2 = S.A2[i], Gref = S.G[8 * k8 + 3];
-                    K[(K_A1 * 8 + k8) * 64 + i] = J >= 1 ? fast_exp2(a2 * (Gref - S.G[16 * J - 1])) : 0.f;
-                    K[(K_A2 * 8 + k8) * 64 + i] = (k8 & 1) ? fast_exp2(a2 * (Gref - S.G[16 * J + 7])) : 0.f;
-                    K[(K_0 * 8 + k8) * 64 + i] = fast_exp2(a2 * Gref);
-                    K[(K_B1_1 * 8 + k8) * 64 + i] = J < 1 ? fast_exp2(a2 * (S.G[15] - Gref)) : 0.f;
-                    K[(K_B1_2 * 8 + k8) * 64 + i] = J < 2 ? fast_exp2(a2 * (S.G[31] - Gref)) : 0.f;
-                    K[(K_B1_3 * 8 + k8) * 64 + i] = J < 3 ? fast_exp2(a2 * (S.G[47] - Gref)) : 0.f;
-                    K[(K_B2 * 8 + k8) * 64 + i] = (k8 & 1) ? 0.f : fast_exp2(a2 * (S.G[16 * J + 7] - Gref));
-                    K[(K_BH * 8 + k8) * 64 + i] = fast_exp2(a2 * (S.G[63] - Gref));
-                }
-            }
-            named_bar_sync(1, kMath);
+            if (!DELTA) prep_all(k);
+            if (!DELTA || NORM) named_bar_sync(1, kMath);   // the decay constants (and the inverse norms)
+            const float* Gc = S.G[k & 1];
 
             // (2) decay-scaled operands; thread = (row t, 16 channels)
-            const bool unsafe = S.unsafe != 0;
+            const bool unsafe = S.unsafe[k & 1] != 0;
             float keep[16];   // gated: Ctil row part; delta: beta Btil row part
             {
                 const int t = r & 63, cq = r >> 6, k8 = t >> 3, I = t >> 4;
                 const bool upper = (t & 15) >= 8;
-                const float Gt = S.G[t], Gr = S.G[8 * k8 + 3];
+                const float Gt = Gc[t], Gr = Gc[8 * k8 + 3];
                 const float dG = Gt - Gr;
                 const float bet = DELTA ? S.beta[s][t] : 0.f;
                 const float nbt = NORM ? S.nb[t] : 1.f, nct = NORM ? S.nc[t] : 1.f;
@@ -473,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 } else {
                     // fallback: every factor evaluated directly (all exponents <= 0 except L3's,
                     // whose entries the assembly step replaces by exact sums)
-                    const float GI = I > 0 ? S.G[16 * I - 1] : 0.f, GJ7 = S.G[16 * I + 7];
+                    const float GI = I > 0 ? Gc[16 * I - 1] : 0.f, GJ7 = Gc[16 * I + 7];
 #pragma unroll
                     for (int qq = 0; qq < 2; qq++) {
                         const int q = 2 * cq + qq;
@@ -494,9 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             scale8(cv, S.A2, q, Gt - GJ7, y); st_row8_f16(X + X_A2, t, q, y);
                             if (DELTA) { scale8(bbv, S.A2, q, Gt - GJ7, z); st_row8_f16(X + X_A2, 64 + t, q, z); }
                         }
-                        if (I < 1) { scale8(bv, S.A2, q, S.G[15] - Gt, y); st_row8_f16(X + X_B1a, t, q, y); }
-                        if (I < 2) { scale8(bv, S.A2, q, S.G[31] - Gt, y); st_row8_f16(X + X_B1b, t, q, y); }
-                        if (I < 3) { scale8(bv, S.A2, q, S.G[47] - Gt, y); st_row8_f16(X + X_B1c, t, q, y); }
+                        if (I < 1) { scale8(bv, S.A2, q, Gc[15] - Gt, y); st_row8_f16(X + X_B1a, t, q, y); }
+                        if (I < 2) { scale8(bv, S.A2, q, Gc[31] - Gt, y); st_row8_f16(X + X_B1b, t, q, y); }
+                        if (I < 3) { scale8(bv, S.A2, q, Gc[47] - Gt, y); st_row8_f16(X + X_B1c, t, q, y); }
                         if (!upper) { scale8(bv, S.A2, q, GJ7 - Gt, y); st_row8_f16(X + X_B2, t, q, y); }
                         scale8(DELTA ? bbv : cv, S.A2, q, Gt, y);
 #pragma unroll
@@ -525,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // level MMAs execute: it reads their operands and writes only [Bhat^T ; P] rows 0..63.
             {
                 const int i = r & 63, sq = r >> 6;
-                const float a2 = S.A2[i], G63 = S.G[63];
+                const float a2 = S.A2[i], G63 = Gc[63];
                 if (!unsafe) {
 #pragma unroll
                     for (int h2 = 0; h2 < 2; h2++) {
@@ -548,12 +569,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             const int sc = 16 * sq + 8 * h2 + e;
                             const float bval = bf2f(*reinterpret_cast<const uint16_t*>(sB + sw128(sc, i))) *
                                                (NORM ? S.nb[sc] : 1.f);
-                            y8[e] = bval * exp2f(a2 * (G63 - S.G[sc]));
+                            y8[e] = bval * exp2f(a2 * (G63 - Gc[sc]));
                         }
                         st_row8_split(sm + OFF_CH0, sm + OFF_CH0L, i, 2 * sq + h2, y8);
                     }
                 }
-                if (r < 64) S.decay[k & 1][r] = fast_exp2(S.A2[r] * S.G[63]);
+                if (r < 64) S.decay[k & 1][r] = fast_exp2(S.A2[r] * Gc[63]);
             }
             if (pending >= 0) epilogue(pending), pending = -1;   // the previous chunk's, under the level products
             if (!mma_wait_all()) break;
@@ -578,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                     ld_row8(sB, sc, q, bv);
 #pragma unroll
                                     for (int kk = 0; kk < 8; kk++)
-                                        acc += xv[kk] * bv[kk] * exp2f(S.A2[8 * q + kk] * (S.G[t] - S.G[sc]));
+                                        acc += xv[kk] * bv[kk] * exp2f(S.A2[8 * q + kk] * (Gc[t] - Gc[sc]));
                                 }
                                 if (NORM) acc *= (isM ? S.nb[t] : S.nc[t]) * S.nb[sc];
                             }
@@ -697,6 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     float* DI32 = reinterpret_cast<float*>(X + X_DI32) + J * 16 * kBS;
 #pragma unroll
                     for (int q = 0; q < 16; q++) DI32[q * kBS + c] = xs[q];
+                } else if ((warp & 2) && k + 1 < p.nchunks) {
+                    prep_idle(k + 1);   // meanwhile warps 2, 3, 6, 7: the next chunk's scan and constants
                 }
                 named_bar_sync(1, kMath);
                 {
@@ -807,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 static_assert(X_CW >= X_ZL + 16384 && X_CW + 16384 <= X_BYTES, "CW clear of the phase-4 operands");
                 if (!state_row) {
                     const int t = trow - 64;
-                    const float Gt = S.G[t];
+                    const float Gt = Gc[t];
 #pragma unroll
                     for (int qq = 0; qq < 4; qq++) {
                         const int q = 4 * wh + qq;
