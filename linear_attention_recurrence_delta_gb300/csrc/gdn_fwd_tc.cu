@@ -370,10 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tc_fence_after();
         };
 
-        if (DELTA) {   // chunk 0's scan and constants (later chunks': under the previous chunk's inverse step)
-            prep_all(0);
-            named_bar_sync(1, kMath);
-        }
+        // chunk 0's scan and constants; later chunks' run on idle warps under the previous chunk's inverse step
+        // (delta) or output product (gated)
+        prep_all(0);
+        named_bar_sync(1, kMath);
         for (int k = 0; k < p.nchunks; k++) {
             const int s = k % kStages;
             if (warp == 0) wait_or_abort(&S.full[s], (k / kStages) & 1, &S.abort, p.status, p.wait_ns);
@@ -394,9 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
             }
 
-            // (1) the chunk's scan of g, overflow check and decay constants: gated here; delta in the previous
-            // chunk's inverse step (by its idle warps) or before the loop.  The inverse norms of b and c
-            // (GDN_NORM_BC) need the chunk's tiles, so warps 1..4 compute them here.
+            // (1) the chunk's scan of g, overflow check and decay constants are ready (made by idle warps during the
+            // previous chunk, or before the loop).  The inverse norms of b and c (GDN_NORM_BC) need the chunk's
+            // tiles, so warps 1..4 compute them here.
             if (NORM && r >= 32 && r < 32 + 128) {
                 const int vr = r - 32, t = vr & 63;
                 float sq = 0.f;
@@ -411,8 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 if (vr < 64) S.nb[t] = inv;
                 else S.nc[t] = inv;
             }
-            if (!DELTA) prep_all(k);
-            if (!DELTA || NORM) named_bar_sync(1, kMath);   // the decay constants (and the inverse norms)
+            if (NORM) named_bar_sync(1, kMath);   // the inverse norms
             const float* Gc = S.G[k & 1];
 
             // (2) decay-scaled operands; thread = (row t, 16 channels)
@@ -695,6 +694,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     mma_k64(tbase + TM_CHG, ch1, stl, true, id, true);
                     mma_commit(&S.mma);
                 }
+                // meanwhile warps 2, 3, 6, 7: the next chunk's scan and constants (G and the tables are the
+                // current chunk's no longer: both were last read before this product)
+                if ((warp & 2) && k + 1 < p.nchunks) prep_idle(k + 1);
                 if (!mma_wait_all()) break;
             } else {
                 named_bar_sync(1, kMath);
