@@ -725,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 named_bar_sync(1, kMath);
                 {
-                    // [Dinv ; 0]: row trow, 32 columns of half wh
+                    // [Dinv ; Dinv]: row trow, 32 columns of half wh.  The copy in rows 64..127 puts a copy of
+                    // [N | X0] in TMEM lanes 64..127, so that the output-lane warps convert half of it.
                     const int J = (trow & 63) >> 4;
                     const float* DI32 = reinterpret_cast<const float*>(X + X_DI32) + (J * 16 + (trow & 15)) * kBS;
 #pragma unroll
@@ -733,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         const int cg = 2 * wh + cc;
                         float v16[16];
 #pragma unroll
-                        for (int c = 0; c < 16; c++) v16[c] = (trow < 64 && cg == J) ? DI32[c] : 0.f;
+                        for (int c = 0; c < 16; c++) v16[c] = (cg == J) ? DI32[c] : 0.f;
                         st_plain16(X + X_DINV, trow, cg, v16);
                     }
                 }
@@ -749,12 +750,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 if (!mma_wait_all()) break;
 
-                // (7) N -> A operand and B block; X0 -> hi/lo B blocks
-                if (state_row) {
-                    const int t = trow;
+                // (7) N -> A operand and B block; X0 -> hi/lo B blocks.  Twelve 16-column groups of token t: groups
+                // 0..5 from the state lanes, 6..11 from their copy in the output lanes.  (Rows 64..127 of the A
+                // operand keep Dinv: the N^2 product's lanes 64..127 are never read, and the N^2 step zeroes them
+                // before the product that needs them zero.)
+                {
+                    const int t = trow & 63;
+                    const int gb = (state_row ? 0 : 6) + 3 * wh;
 #pragma unroll
-                    for (int gg = 0; gg < 6; gg++) {
-                        const int g = 6 * wh + gg;
+                    for (int gg = 0; gg < 3; gg++) {
+                        const int g = gb + gg;
                         float v[16];
                         tmem_ld16(tl + TM_NX + 16 * g, v);
                         tmem_wait_ld();
@@ -767,9 +772,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             st_split16(X + X_NXH + 8192 + blk, X + X_NXL + blk, t, xg & 3, v);
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; q++) zero_chunk(X + X_NA, trow, 4 * wh + q);
                 }
                 smem_to_tc();
 
