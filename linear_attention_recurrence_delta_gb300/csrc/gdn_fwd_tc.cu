@@ -787,26 +787,31 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // (9) N^2 -> A operand; Z = X0 - N X0 -> hi/lo B blocks and, exactly, TMEM (Util | W)
                 if (state_row) {
                     const int t = trow;
+                    auto zgroup = [&](int xg) {   // Z columns 16 xg .. 16 xg + 15 (two TMEM loads)
+                        float x0v[16], nx[16];
+                        tmem_ld16(tl + TM_NX + 64 + 16 * xg, x0v);
+                        tmem_ld16(tl + TM_N2X + 64 + 16 * xg, nx);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int gg = 0; gg < 6; gg++) {
-                        const int g = 6 * wh + gg;
-                        if (g < 4) {
+                        for (int c = 0; c < 16; c++) x0v[c] -= nx[c];
+                        const uint32_t blk = (uint32_t)(xg >> 2) * 8192u;
+                        st_split16(X + X_ZH + blk, X + X_ZL + blk, t, xg & 3, x0v);
+                        tmem_st16(tl + (xg < 4 ? TM_U + 16 * xg : TM_W + 16 * (xg - 4)), x0v);
+                    };
+                    // ten TMEM loads per column half: N^2 (4 groups, one load each) and Z groups 0..2, or Z 3..7
+                    if (wh == 0) {
+#pragma unroll
+                        for (int g = 0; g < 4; g++) {
                             float v[16];
                             tmem_ld16(tl + TM_N2X + 16 * g, v);
                             tmem_wait_ld();
                             st_plain16(X + X_N2A, t, g, v);
-                        } else {
-                            const int xg = g - 4;
-                            float x0v[16], nx[16];
-                            tmem_ld16(tl + TM_NX + 64 + 16 * xg, x0v);
-                            tmem_ld16(tl + TM_N2X + 64 + 16 * xg, nx);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int c = 0; c < 16; c++) x0v[c] -= nx[c];
-                            const uint32_t blk = (uint32_t)(xg >> 2) * 8192u;
-                            st_split16(X + X_ZH + blk, X + X_ZL + blk, t, xg & 3, x0v);
-                            tmem_st16(tl + (xg < 4 ? TM_U + 16 * xg : TM_W + 16 * (xg - 4)), x0v);
                         }
+#pragma unroll
+                        for (int xg = 0; xg < 3; xg++) zgroup(xg);
+                    } else {
+#pragma unroll
+                        for (int xg = 3; xg < 8; xg++) zgroup(xg);
                     }
                 } else {
 #pragma unroll
