@@ -608,9 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     const int Ia = 2 * wl, Ib = 2 * wl + 1;
                     const uint32_t colA = wl == 0 ? 0u : TM_D1b, colB = wl == 0 ? TM_D1a : TM_D1c;
                     float* M32 = reinterpret_cast<float*>(X + X_M32);
+                    // gated: column groups wh and wh + 2, interleaved over the two halves, because the causal
+                    // zeros sit in the high groups of the low rows (a half of groups {0, 1} or {2, 3} does 8 or 0
+                    // TMEM loads, these at most 7); measured faster for gated, not for delta
 #pragma unroll
                     for (int cc = 0; cc < 2; cc++) {
-                        const int cg = 2 * wh + cc;
+                        const int cg = DELTA ? 2 * wh + cc : wh + 2 * cc;
                         float out[16];
                         if (16 * cg > 32 * wl + 31) {
 #pragma unroll
