@@ -435,6 +435,7 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
         for (int wi = kBT / kWin - 1; wi >= 0; wi--) {
             const int tw = kWin * wi;  // first token of the window inside the block
             const int pb = PBUF == 2 ? wbuf : 0;
+            float gsv[kWin], pbv[kWin];   // this lane's dg and dbeta partials of the window's tokens
             float2 W[kWin + 1][2][4];
             {
                 const int sb = tw / kSub;
@@ -533,18 +534,35 @@ __global__ void __launch_bounds__(256, 1) serial_bwd_kernel(Args a, WsLayout L, 
                 }
                 colsum_store<KIG>(pdc, s.part[pb][w][k][0], C);
                 colsum_store<KIG>(pdb, s.part[pb][w][k][1], C);
-                float gs = gq.x + gq.y;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) gs += __shfl_xor_sync(kFull, gs, o);
-                if (DELTA) {
-#pragma unroll
-                    for (int o = KIG; o < 32; o <<= 1) pbeta += __shfl_xor_sync(kFull, pbeta, o);
-                }
-                if (lane == 0) {
-                    s.gpart[wbuf][w][k] = gs;
-                    if (DELTA) s.bpart[wbuf][w][k] = pbeta;
-                }
+                gsv[k] = gq.x + gq.y;   // warp sums taken for the whole window below
+                pbv[k] = pbeta;
                 if (C.ig == 0) *reinterpret_cast<float2*>(&s.dvb[wbuf][k][C.j0]) = f2(dv0, dv1);
+            }
+            // the window's four dg (and dbeta) warp sums at once: a reduce-scatter over lane bits 4 and 3 leaves
+            // token (lane >> 3) & 3 in lanes 8 (lane >> 3), then the remaining lanes are summed (dg only; dbeta's
+            // partials are equal across the row lanes)
+            {
+                static_assert(kWin == 4, "the window reduce-scatter is written for four tokens");
+                const bool h16 = lane & 16, h8 = lane & 8;
+                float a0 = (h16 ? gsv[2] : gsv[0]) + __shfl_xor_sync(kFull, h16 ? gsv[0] : gsv[2], 16);
+                float a1 = (h16 ? gsv[3] : gsv[1]) + __shfl_xor_sync(kFull, h16 ? gsv[1] : gsv[3], 16);
+                float g1 = (h8 ? a1 : a0) + __shfl_xor_sync(kFull, h8 ? a0 : a1, 8);
+#pragma unroll
+                for (int o = 4; o > 0; o >>= 1) g1 += __shfl_xor_sync(kFull, g1, o);
+                if ((lane & 7) == 0) s.gpart[wbuf][w][(lane >> 3) & 3] = g1;
+                if (DELTA) {
+                    float b0 = (h16 ? pbv[2] : pbv[0]) + __shfl_xor_sync(kFull, h16 ? pbv[0] : pbv[2], 16);
+                    float b1 = (h16 ? pbv[3] : pbv[1]) + __shfl_xor_sync(kFull, h16 ? pbv[1] : pbv[3], 16);
+                    if (KIG == 8) {   // jl = lane >> 3: sum over lane bits 4 and 3
+                        const float bb = (h8 ? b1 : b0) + __shfl_xor_sync(kFull, h8 ? b0 : b1, 8);
+                        if ((lane & 7) == 0) s.bpart[wbuf][w][(lane >> 3) & 3] = bb;
+                    } else {          // jl = lane >> 4: sum over lane bit 4 only
+                        if ((lane & 15) == 0) {
+                            s.bpart[wbuf][w][2 * (lane >> 4)] = b0;
+                            s.bpart[wbuf][w][2 * (lane >> 4) + 1] = b1;
+                        }
+                    }
+                }
             }
             if (wi == 2 && n < nblk - 1) cp_async_wait_all();   // snapshot slot 0, read from window 1 on
             __syncthreads();
