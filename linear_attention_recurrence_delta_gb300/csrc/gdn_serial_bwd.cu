@@ -70,6 +70,28 @@ struct BwdSmem {
     IO rb[kBT][R], rc[kBT][R], rv[kBT][NC], rdo[kBT][NC];       // raw bytes of the next block
 };
 
+// eight consecutive staged values: raw I/O (16 bytes of bf16, 32 of fp32) -> fp32, and fp32 -> shared
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8])
+{
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        v[2 * k] = __uint_as_float(w[k] << 16);
+        v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8])
+{
+    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8])
+{
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
 struct Ctx {
     int tid, lane, w, ig, jl, j0, m2, u, bb, h;
     int jc0, nv;  // first value column of the slab, columns in it
@@ -158,25 +180,59 @@ __device__ __forceinline__ void finish_block(const Args& a, BwdSmem<IO, KIG>& s,
         }
         __syncthreads();
     }
-    for (int idx = tid; idx < kBT * R; idx += 256) {
-        const int tt = idx / R, i = idx % R;
-        const bool ok = tt < nt;
-        const float sb = a.norm && ok ? s.nb[tt] : 1.f, sc = a.norm && ok ? s.nc[tt] : 1.f;
-        s.A[tt][i] = ok ? decay<IO>(s.rg[tt], s.Arow[i], s.Arow2[i]) : 1.f;
-        s.Bv[tt][i] = ok && i < dk ? to_f(s.rb[tt][i]) * sb : 0.f;
-        s.Cv[tt][i] = grad && ok && i < dk ? to_f(s.rc[tt][i]) * sc : 0.f;
-        if (R == NC) {   // rows and columns in one pass
-            s.V[tt][i] = ok && i < nv ? to_f(s.rv[tt][i]) : 0.f;
-            s.DO[tt][i] = grad && ok && i < nv ? to_f(s.rdo[tt][i]) : 0.f;
+    if (sizeof(IO) == 4) {   // fp32 I/O: element by element (measured faster than the 8-wide form here)
+        for (int idx = tid; idx < kBT * R; idx += 256) {
+            const int tt = idx / R, i = idx % R;
+            const bool ok = tt < nt;
+            const float sb = a.norm && ok ? s.nb[tt] : 1.f, sc = a.norm && ok ? s.nc[tt] : 1.f;
+            s.A[tt][i] = ok ? decay<IO>(s.rg[tt], s.Arow[i], s.Arow2[i]) : 1.f;
+            s.Bv[tt][i] = ok && i < dk ? to_f(s.rb[tt][i]) * sb : 0.f;
+            s.Cv[tt][i] = grad && ok && i < dk ? to_f(s.rc[tt][i]) * sc : 0.f;
         }
-    }
-    if (R != NC)
         for (int idx = tid; idx < kBT * NC; idx += 256) {
             const int tt = idx / NC, i = idx % NC;
             const bool ok = tt < nt;
             s.V[tt][i] = ok && i < nv ? to_f(s.rv[tt][i]) : 0.f;
             s.DO[tt][i] = grad && ok && i < nv ? to_f(s.rdo[tt][i]) : 0.f;
         }
+    } else {
+    // bf16: eight consecutive values per thread, one 16-byte raw load and two 16-byte stores per array
+    for (int ch = tid; ch < kBT * (R / 8); ch += 256) {
+        const int tt = ch / (R / 8), i0 = (ch % (R / 8)) * 8;
+        const bool ok = tt < nt;
+        const float sb = a.norm && ok ? s.nb[tt] : 1.f, sc = a.norm && ok ? s.nc[tt] : 1.f;
+        const float gt = s.rg[tt];
+        float av[8], bv[8], cv[8];
+        load8(&s.rb[tt][i0], bv);
+        if (grad) load8(&s.rc[tt][i0], cv);
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const int i = i0 + e;
+            const bool live = ok && i < dk;
+            av[e] = ok ? decay<IO>(gt, s.Arow[i], s.Arow2[i]) : 1.f;
+            bv[e] = live ? bv[e] * sb : 0.f;
+            cv[e] = grad && live ? cv[e] * sc : 0.f;
+        }
+        store8(&s.A[tt][i0], av);
+        store8(&s.Bv[tt][i0], bv);
+        store8(&s.Cv[tt][i0], cv);
+    }
+    for (int ch = tid; ch < kBT * (NC / 8); ch += 256) {
+        const int tt = ch / (NC / 8), j0 = (ch % (NC / 8)) * 8;
+        const bool ok = tt < nt;
+        float vv[8], dd[8];
+        load8(&s.rv[tt][j0], vv);
+        if (grad) load8(&s.rdo[tt][j0], dd);
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const bool live = ok && j0 + e < nv;
+            vv[e] = live ? vv[e] : 0.f;
+            dd[e] = grad && live ? dd[e] : 0.f;
+        }
+        store8(&s.V[tt][j0], vv);
+        store8(&s.DO[tt][j0], dd);
+    }
+    }
     if (tid < kBT) {
         const bool ok = tid < nt;
         s.g[tid] = ok ? s.rg[tid] : 0.f;
