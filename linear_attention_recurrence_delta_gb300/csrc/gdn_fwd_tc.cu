@@ -354,6 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             for (int rep = 0; rep < 4; rep++) table_entry(S.G[kk & 1], gt + rep * 128);
         };
         int pending = -1;   // chunk whose epilogue has not run yet
+        // token row of thread r in the decay-scaled operand step (and of its keep[] values)
+        // (gated only: measured faster there, slower in delta mode, whose rows also store the b-side operands)
+        auto op_row = [](int rr) { return DELTA ? (rr & 63) : (rr & 31) + 32 * (((rr >> 5) ^ (rr >> 7)) & 1); };
         uint32_t mma_phase = 0;
         // one warp polls the mbarrier; the others sleep in the named barrier
         auto mma_wait_all = [&]() -> bool {
@@ -418,7 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const bool unsafe = S.unsafe[k & 1] != 0;
             float keep[16];   // gated: Ctil row part; delta: beta Btil row part
             {
-                const int t = r & 63, cq = r >> 6, k8 = t >> 3, I = t >> 4;
+                // gated: rows of blocks 0-1 store more operand tiles than rows of blocks 2-3; the row half
+                // alternates with bit 2 of the warp so that each scheduler (warp mod 4) gets one of each
+                const int t = op_row(r), cq = r >> 6, k8 = t >> 3, I = t >> 4;
                 const bool upper = (t & 15) >= 8;
                 const float Gt = Gc[t], Gr = Gc[8 * k8 + 3];
                 const float dG = Gt - Gr;
@@ -654,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
             }
             {
-                const int t = r & 63, cq = r >> 6;
+                const int t = op_row(r), cq = r >> 6;   // the rows whose keep[] this thread holds
                 if (!DELTA) {
                     // [0 ; Ctil] for the output MMA (the levels' space is free now)
 #pragma unroll
