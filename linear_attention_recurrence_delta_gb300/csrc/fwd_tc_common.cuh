@@ -28,6 +28,7 @@ struct TcParams {
     const float* A_log;
     const float* h0;
     __nv_bfloat16* o;
+    float* o32;              // if not null: o is written here in fp32 instead (time-split intermediate runs)
     float* hT;
     uint32_t* status;
     int B, H, T, dk, dv, nchunks;

@@ -65,11 +65,11 @@ static size_t place_tsplit(const gdn_shape_t& s, int P, bool backward, WsLayout&
         L.ts_zv_off = off;
         off = round_up(off + tk, 256);
         L.ts_so_off = off;
-        off = round_up(off + tk, 256);
+        off = round_up(off + (size_t)s.B * s.T * s.H * s.dk * sizeof(float), 256);
     }
+    L.ts_o_off = off;
+    off = round_up(off + (size_t)s.B * s.T * s.H * s.dv * sizeof(float), 256);
     if (backward) {
-        L.ts_o_off = off;
-        off = round_up(off + (size_t)s.B * s.T * s.H * s.dv * esz, 256);
         L.ts_g_off = off;
         off = round_up(off + st, 256);
         L.ts_e_off = off;

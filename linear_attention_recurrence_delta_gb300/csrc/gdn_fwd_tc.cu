@@ -268,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
             } else {
                 const int tg = kk * kC + (trow - 64);
-                __nv_bfloat16* orow = p.o + (((size_t)bb * T + tg) * H + h) * dv + jc0;
+                const size_t orow_at = (((size_t)bb * T + tg) * H + h) * dv + jc0;
+                __nv_bfloat16* orow = p.o + orow_at;
 #pragma unroll
                 for (int cc = 0; cc < 2; cc++) {
                     const int col = 32 * wh + 16 * cc;
@@ -287,7 +288,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                         for (int hq = 0; hq < 2; hq++) {
                             const int j0 = col + 8 * hq;
-                            if (j0 < nv) {
+                            if (j0 < nv && p.o32) {   // fp32 output (time-split intermediate runs)
+                                float* q = p.o32 + orow_at + j0;
+                                *reinterpret_cast<float4*>(q) =
+                                    make_float4(v[8 * hq + 0], v[8 * hq + 1], v[8 * hq + 2], v[8 * hq + 3]);
+                                *reinterpret_cast<float4*>(q + 4) =
+                                    make_float4(v[8 * hq + 4], v[8 * hq + 5], v[8 * hq + 6], v[8 * hq + 7]);
+                            } else if (j0 < nv) {
                                 uint4 wv;
                                 wv.x = pack_bf16(v[8 * hq + 0], v[8 * hq + 1]);
                                 wv.y = pack_bf16(v[8 * hq + 2], v[8 * hq + 3]);
@@ -975,6 +982,7 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     p.A_log = a.A_log;
     p.h0 = a.h0;
     p.o = (__nv_bfloat16*)a.o;
+    p.o32 = a.o32;
     p.hT = a.hT;
     p.status = (uint32_t*)a.ws;
     p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv = a.dv;

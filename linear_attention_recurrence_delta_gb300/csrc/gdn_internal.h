@@ -18,6 +18,8 @@ struct Args {
     const float* A_log;
     const float* h0;
     void* o;
+    float* o32;            // forward, bf16 I/O: write o in fp32 here instead of `o` (intermediate runs of the
+                           // time split; the tcgen05 kernel honours it, the other bf16 paths are never asked)
     float* hT;
     // backward only
     const void* dO;
@@ -44,9 +46,9 @@ struct WsLayout {
     size_t ts_a_off = 0;          // delta: segment transitions          [B*P, H, d_k, d_k]
     size_t ts_i_off = 0;          // delta: identity starting states     [B*P, H, d_k, d_k]
     size_t ts_zv_off = 0;         // delta: zero values                  [B, T, H, d_k] (I/O dtype)
-    size_t ts_so_off = 0;         // delta: outputs of the transition run [B, T, H, d_k] (I/O dtype)
+    size_t ts_so_off = 0;         // delta: outputs of the transition run [B, T, H, d_k] fp32
     // backward split in time
-    size_t ts_o_off = 0;          // forward outputs of the state runs   [B, T, H, d_v] (I/O dtype)
+    size_t ts_o_off = 0;          // outputs of the zero-start runs      [B, T, H, d_v] fp32
     size_t ts_g_off = 0;          // segment adjoints from a zero end gradient [B*P, H, d_k, d_v]
     size_t ts_e_off = 0;          // end gradients of the segments       [B*P, H, d_k, d_v]
     size_t total = 0;

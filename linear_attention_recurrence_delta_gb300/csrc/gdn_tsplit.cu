@@ -12,10 +12,16 @@
 //   1. every segment runs from a zero state          -> H_s      (parallel)
 //   2. delta: every segment runs with v = 0 from I   -> A_s      (parallel)
 //   3. a scan over segments  S_{p+1} = A_p S_p + H_p             (serial, small)
-//   4. every segment runs again from its S_p         -> o        (parallel)
+//   4. the outputs: the forward is linear in the entering state, so with
+//      Phi_t the transition from the segment start through token t,
+//        o_t = o0_t + S_p^T (Phi_t^T c_t),
+//      o0_t the zero-start output of step 1 and Phi_t^T c_t the output of the
+//      transition run of step 2 (delta) or c_t (.) exp(A Gam_t), Gam_t the sum
+//      of g over the segment through t (gated); both runs keep their outputs
+//      in fp32 for this                                          (parallel)
 // A [B, T, H, d] tensor cut into P segments of T/P tokens is, byte for byte,
-// a [B*P, T/P, H, d] tensor, so steps 1, 2 and 4 are the ordinary forward on
-// that shape and no input moves.
+// a [B*P, T/P, H, d] tensor, so steps 1 and 2 are the ordinary forward on that
+// shape and no input moves.
 //
 // The backward splits the same way.  With the segments' entering states S_p
 // from steps 1-3, the adjoint dL/dS_p of a segment is G_p + A_p^T E_p, where
@@ -40,6 +46,139 @@ __global__ void eye_kernel(float* I, size_t n_units, int dk)
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < n; idx += (size_t)gridDim.x * blockDim.x) {
         const int r = (int)((idx / dk) % dk), c = (int)(idx % dk);
         I[idx] = r == c ? 1.f : 0.f;
+    }
+}
+
+// Step 4 for one (view batch, head) unit and a run of kOutRun of its segment's tokens: o_t = o0_t + S_p^T q_t
+// with q_t = Phi_t^T c_t (delta: from the transition run; gated: c_t (.) exp(A Gam_t)).  Thread (j, r) holds
+// column j of S_p in registers; the run goes in sub-tiles of 64 tokens whose q and o0 rows are staged in
+// shared memory, thread (j, r) computing tokens r, r + 4, ... of each.  Gated: the gates of the segment
+// before the run are a fixed-order block sum, then a running inclusive scan over the sub-tiles.
+constexpr int kOutTile = 64;
+constexpr int kOutRun = 512;
+
+template <typename IO, bool DELTA>
+__global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const float* so, const IO* c, const IO* g,
+                                                         const float* A_log, const float* Sst, IO* o, int H, int Ts,
+                                                         int dk, int dv, int logits, int norm)
+{
+    __shared__ __align__(16) float q[kOutTile][64];
+    __shared__ __align__(16) float oz[kOutTile][64];
+    __shared__ float Gam[kOutTile];
+    __shared__ float red[8];
+    __shared__ float Arow[64];
+    const int u = blockIdx.x, bv = u / H, h = u % H, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int j = tid & 63, r = tid >> 6;
+    const int run0 = kOutRun * blockIdx.y, run_end = min(Ts, run0 + kOutRun);
+    auto row = [&](int t) { return ((size_t)bv * Ts + t) * H + h; };   // token row of the [B*P, T/P, H] view
+    auto gate_at = [&](int t) {
+        const float gv = (float)g[row(t)];
+        return logits ? 1.f / (1.f + expf(-gv)) : gv;
+    };
+
+    float Scol[64];
+#pragma unroll
+    for (int i = 0; i < 64; i++) Scol[i] = (i < dk && j < dv) ? Sst[((size_t)u * dk + i) * dv + j] : 0.f;
+
+    float base = 0.f;   // gated: sum of the segment's gates before the current sub-tile
+    if (!DELTA) {
+        if (tid < 64) Arow[tid] = tid < dk ? -expf(A_log[h * dk + tid]) : 0.f;
+        float part = 0.f;
+        for (int t = tid; t < run0; t += 256) part += gate_at(t);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) red[w] = part;
+        __syncthreads();
+#pragma unroll
+        for (int ww = 0; ww < 8; ww++) base += red[ww];
+    }
+
+    for (int t0 = run0; t0 < run_end; t0 += kOutTile) {
+        const int nt = min(kOutTile, run_end - t0);
+        __syncthreads();   // the previous sub-tile's rows are consumed
+        if (!DELTA && w == 0) {   // inclusive scan of the sub-tile's gates (two per lane) on top of `base`
+            const float ga = 2 * lane < nt ? gate_at(t0 + 2 * lane) : 0.f;
+            const float gb = 2 * lane + 1 < nt ? gate_at(t0 + 2 * lane + 1) : 0.f;
+            float x = ga + gb;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            const float ex = __shfl_up_sync(0xffffffffu, x, 1);
+            Gam[2 * lane] = base + (lane > 0 ? ex : 0.f) + ga;
+            Gam[2 * lane + 1] = base + x;
+        }
+        // the sub-tile's o0 (and, delta, q) rows: four 16-byte quads per thread and array, all in flight at once
+        // (whole quads need rows of a multiple of 4 floats; otherwise element by element)
+        if ((dv & 3) == 0 && (!DELTA || (dk & 3) == 0)) {
+            float4 xo[4], xq[4];
+#pragma unroll
+            for (int m = 0; m < 4; m++) {
+                const int idx = tid + 256 * m, tt = idx >> 4, c4 = 4 * (idx & 15);
+                const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                xo[m] = (tt < nt && c4 < dv) ? *reinterpret_cast<const float4*>(o0 + row(t0 + tt) * dv + c4) : z4;
+                if (DELTA)
+                    xq[m] = (tt < nt && c4 < dk) ? *reinterpret_cast<const float4*>(so + row(t0 + tt) * dk + c4)
+                                                 : z4;
+            }
+#pragma unroll
+            for (int m = 0; m < 4; m++) {
+                const int idx = tid + 256 * m, tt = idx >> 4, c4 = 4 * (idx & 15);
+                *reinterpret_cast<float4*>(&oz[tt][c4]) = xo[m];
+                if (DELTA) *reinterpret_cast<float4*>(&q[tt][c4]) = xq[m];
+            }
+        } else {
+            for (int idx = tid; idx < kOutTile * 64; idx += 256) {
+                const int tt = idx >> 6, jj = idx & 63;
+                oz[tt][jj] = (tt < nt && jj < dv) ? o0[row(t0 + tt) * dv + jj] : 0.f;
+                if (DELTA) q[tt][jj] = (tt < nt && jj < dk) ? so[row(t0 + tt) * dk + jj] : 0.f;
+            }
+        }
+        if (!DELTA) {
+            float cv[16];   // the sub-tile's c rows, all loads in flight before the exponentials
+#pragma unroll
+            for (int m = 0; m < 16; m++) {
+                const int idx = tid + 256 * m, tt = idx >> 6, i = idx & 63;
+                cv[m] = (tt < nt && i < dk) ? (float)c[row(t0 + tt) * dk + i] : 0.f;
+            }
+            __syncthreads();   // Gam
+#pragma unroll
+            for (int m = 0; m < 16; m++) {
+                const int idx = tid + 256 * m, tt = idx >> 6, i = idx & 63;
+                q[tt][i] = cv[m] * expf(Arow[i] * Gam[tt]);
+            }
+            if (norm) {   // c_t / max(||c_t||, floor): one warp per token row
+                __syncthreads();
+                for (int tt = w; tt < nt; tt += 8) {
+                    float sq = 0.f;
+                    for (int i = lane; i < dk; i += 32) {
+                        const float x = (float)c[row(t0 + tt) * dk + i];
+                        sq = fmaf(x, x, sq);
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                    const float inv = 1.f / fmaxf(sqrtf(sq), kNormFloor);
+                    for (int i = lane; i < 64; i += 32) q[tt][i] *= inv;
+                }
+            }
+            base = Gam[kOutTile - 1];   // (tokens past the run's end add zero)
+        }
+        __syncthreads();
+        if (j < dv) {
+            for (int tt = r; tt < nt; tt += 4) {
+                float acc = oz[tt][j];
+#pragma unroll
+                for (int i = 0; i < 64; i += 4) {
+                    const float4 qq = *reinterpret_cast<const float4*>(&q[tt][i]);
+                    acc = fmaf(Scol[i], qq.x, acc);
+                    acc = fmaf(Scol[i + 1], qq.y, acc);
+                    acc = fmaf(Scol[i + 2], qq.z, acc);
+                    acc = fmaf(Scol[i + 3], qq.w, acc);
+                }
+                o[row(t0 + tt) * dv + j] = (IO)acc;
+            }
+        }
     }
 }
 
@@ -192,8 +331,9 @@ int tsplit_factor(const gdn_shape_t& s, int backward)
 }
 
 // Steps 1-3: the entering state of every segment into L.ts_s_off and, if
-// hT is given, the leaving state of the whole sequence.  `a.o` receives the
-// outputs of step 1, which are not the final ones.
+// hT is given, the leaving state of the whole sequence; the zero-start outputs
+// (step 1) into L.ts_o_off and, delta, the transition run's (step 2) into
+// L.ts_so_off, both fp32.
 static cudaError_t tsplit_states(const Args& a, const WsLayout& L, int P, cudaStream_t st,
                                  cudaError_t (*fwd_core)(const Args&, cudaStream_t))
 {
@@ -203,7 +343,9 @@ static cudaError_t tsplit_states(const Args& a, const WsLayout& L, int P, cudaSt
     float* Sst = (float*)(ws + L.ts_s_off);
     float* Ibuf = (float*)(ws + L.ts_i_off);
     void* zv = ws + L.ts_zv_off;
-    void* so = ws + L.ts_so_off;
+    float* so = (float*)(ws + L.ts_so_off);
+    float* o0 = (float*)(ws + L.ts_o_off);
+    const bool bf = a.io == GDN_BF16;
     const int Ts = a.T / P;
     const size_t vunits = (size_t)a.B * P * a.H;
     cudaError_t e;
@@ -214,6 +356,8 @@ static cudaError_t tsplit_states(const Args& a, const WsLayout& L, int P, cudaSt
     r.T = Ts;
     r.h0 = nullptr;
     r.hT = Hbuf;
+    r.o = bf ? a.o : (void*)o0;   // the zero-start outputs, in fp32 (o0)
+    r.o32 = bf ? o0 : nullptr;
     if ((e = fwd_core(r, st)) != cudaSuccess) return e;
 
     // 2. delta: transitions A_s = h_end with v = 0 from the identity
@@ -225,7 +369,8 @@ static cudaError_t tsplit_states(const Args& a, const WsLayout& L, int P, cudaSt
         Args t = r;
         t.dv = a.dk;
         t.v = zv;
-        t.o = so;
+        t.o = bf ? a.o : (void*)so;   // Phi_t^T c_t, in fp32 (so)
+        t.o32 = bf ? so : nullptr;
         t.h0 = Ibuf;
         t.hT = Abuf;
         if ((e = fwd_core(t, st)) != cudaSuccess) return e;
@@ -241,13 +386,33 @@ cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
 {
     cudaError_t e = tsplit_states(a, L, P, st, fwd_core);
     if (e != cudaSuccess) return e;
-    // 4. every segment again from its true entering state: the outputs
-    Args f = a;
-    f.B = a.B * P;
-    f.T = a.T / P;
-    f.h0 = (const float*)((unsigned char*)a.ws + L.ts_s_off);
-    f.hT = nullptr;
-    return fwd_core(f, st);
+    // 4. o_t = o0_t + S_p^T Phi_t^T c_t
+    const unsigned char* ws = (const unsigned char*)a.ws;
+    const float* o0 = (const float*)(ws + L.ts_o_off);
+    const float* so = (const float*)(ws + L.ts_so_off);
+    const float* Sst = (const float*)(ws + L.ts_s_off);
+    const int Ts = a.T / P;
+    const dim3 grid(a.B * P * a.H, (Ts + kOutRun - 1) / kOutRun);
+    if (a.io == GDN_BF16) {
+        if (a.mode == GDN_DELTA)
+            tsplit_out_kernel<__nv_bfloat16, true><<<grid, 256, 0, st>>>(
+                o0, so, (const __nv_bfloat16*)a.c, (const __nv_bfloat16*)a.g, a.A_log, Sst, (__nv_bfloat16*)a.o, a.H,
+                Ts, a.dk, a.dv, a.logits, a.norm);
+        else
+            tsplit_out_kernel<__nv_bfloat16, false><<<grid, 256, 0, st>>>(
+                o0, so, (const __nv_bfloat16*)a.c, (const __nv_bfloat16*)a.g, a.A_log, Sst, (__nv_bfloat16*)a.o, a.H,
+                Ts, a.dk, a.dv, a.logits, a.norm);
+    } else {
+        if (a.mode == GDN_DELTA)
+            tsplit_out_kernel<float, true><<<grid, 256, 0, st>>>(o0, so, (const float*)a.c, (const float*)a.g, a.A_log,
+                                                                 Sst, (float*)a.o, a.H, Ts, a.dk, a.dv, a.logits,
+                                                                 a.norm);
+        else
+            tsplit_out_kernel<float, false><<<grid, 256, 0, st>>>(o0, so, (const float*)a.c, (const float*)a.g,
+                                                                  a.A_log, Sst, (float*)a.o, a.H, Ts, a.dk, a.dv,
+                                                                  a.logits, a.norm);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
@@ -259,9 +424,8 @@ cudaError_t launch_bwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
     float* Ebuf = (float*)(ws + L.ts_e_off);
     cudaError_t e;
 
-    // 1-3. entering states of the segments (outputs of step 1 go to scratch)
+    // 1-3. entering states of the segments (the runs' outputs are not needed here)
     Args fa = a;
-    fa.o = ws + L.ts_o_off;
     fa.hT = nullptr;
     if ((e = tsplit_states(fa, L, P, st, fwd_core)) != cudaSuccess) return e;
 

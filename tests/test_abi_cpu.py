@@ -137,19 +137,20 @@ def test_time_split_workspace():
     gated = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "gated", "bf16"), 0)
     short = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 1000, 64, 64, "delta", "bf16"), 0)
     assert many == 256 and short == 256
-    # P = 8 segments: 2 x 128 states (16 KB) + 2 x 128 transitions + zero values and scratch outputs
-    assert few >= 256 + 4 * 128 * 16384 + 2 * 32768 * 16 * 64 * 2
+    # P = 8 segments: 2 x 128 states (16 KB) + 2 x 128 transitions + zero values (bf16) and the fp32 outputs
+    # of the zero-start and transition runs
+    assert few >= 256 + 4 * 128 * 16384 + 32768 * 16 * 64 * 2 + 2 * 32768 * 16 * 64 * 4
     assert 256 + 2 * 128 * 16384 <= gated < few
 
 
 def test_time_split_backward_workspace():
     """The backward splits long sequences over few heads too: its workspace adds the forward split's
-    buffers, the state-run outputs and two sets of per-segment adjoints to its own."""
+    buffers (which hold the zero-start runs' fp32 outputs) and two sets of per-segment adjoints to its own."""
     few = gdn.gdn_workspace_bytes(gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 1)
     many = gdn.gdn_workspace_bytes(gdn.make_shape(16, 8, 4096, 64, 64, "delta", "bf16"), 1)
     fwd_split = gdn.gdn_workspace_bytes(gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0)
     # same tokens and heads: the backward's own buffers are equal, the split adds at least the forward's
-    assert few >= many + fwd_split - 256 + 32768 * 16 * 64 * 2 + 2 * 128 * 16384
+    assert few >= many + fwd_split - 256 + 2 * 128 * 16384
 
 
 def test_gate_logits_option_bit():
