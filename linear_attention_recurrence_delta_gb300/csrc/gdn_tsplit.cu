@@ -76,9 +76,13 @@ __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const 
         return logits ? 1.f / (1.f + expf(-gv)) : gv;
     };
 
-    float Scol[64];
+    float2 Scol[32];   // rows 2k, 2k + 1 of column j, for packed fp32x2 products
 #pragma unroll
-    for (int i = 0; i < 64; i++) Scol[i] = (i < dk && j < dv) ? Sst[((size_t)u * dk + i) * dv + j] : 0.f;
+    for (int k = 0; k < 32; k++) {
+        const int i = 2 * k;
+        Scol[k].x = (i < dk && j < dv) ? Sst[((size_t)u * dk + i) * dv + j] : 0.f;
+        Scol[k].y = (i + 1 < dk && j < dv) ? Sst[((size_t)u * dk + i + 1) * dv + j] : 0.f;
+    }
 
     float base = 0.f;   // gated: sum of the segment's gates before the current sub-tile
     if (!DELTA) {
@@ -167,16 +171,15 @@ __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const 
         __syncthreads();
         if (j < dv) {
             for (int tt = r; tt < nt; tt += 4) {
-                float acc = oz[tt][j];
+                // two chains of packed fp32x2 FMAs, added in a fixed order
+                float2 acc0 = make_float2(oz[tt][j], 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int i = 0; i < 64; i += 4) {
                     const float4 qq = *reinterpret_cast<const float4*>(&q[tt][i]);
-                    acc = fmaf(Scol[i], qq.x, acc);
-                    acc = fmaf(Scol[i + 1], qq.y, acc);
-                    acc = fmaf(Scol[i + 2], qq.z, acc);
-                    acc = fmaf(Scol[i + 3], qq.w, acc);
+                    acc0 = __ffma2_rn(Scol[i / 2], make_float2(qq.x, qq.y), acc0);
+                    acc1 = __ffma2_rn(Scol[i / 2 + 1], make_float2(qq.z, qq.w), acc1);
                 }
-                o[row(t0 + tt) * dv + j] = (IO)acc;
+                o[row(t0 + tt) * dv + j] = (IO)((acc0.x + acc0.y) + (acc1.x + acc1.y));
             }
         }
     }
