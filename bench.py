@@ -93,7 +93,7 @@ def fwd_launches(w):
     """Kernels one gdn_fwd call launches."""
     if tsplit_factor(w, False) == 1:
         return 1
-    return 5 if w.mode == "delta" else 3   # state run, (identity, transition run), scan, output run
+    return 5 if w.mode == "delta" else 3   # zero-start run, (identity, transition run), scan, output kernel
 
 
 def bwd_slabs(w):
