@@ -48,7 +48,12 @@
 // and the TMA loads of v, b, c (128 B swizzle, zero fill past T and d) into a
 // 2-stage ring: the load of chunk k + 2 goes out as soon as chunk k's last MMA
 // has finished with its stage.  Threads 0..63 fetch g (and beta) one chunk
-// ahead into registers.
+// ahead into registers.  The kernel is latency-bound, so independent work runs
+// where warps would wait: chunk k's state update and output stores under
+// chunk k+1's level products, chunk k+1's scan of g and decay constants on
+// warps 2, 3, 6, 7 (the schedulers the critical path leaves free) under chunk
+// k's diagonal-block inverse (delta) or output product (gated), and (delta)
+// the Ctil rows of [-W ; Ctil] under the W products.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
