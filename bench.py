@@ -78,11 +78,11 @@ def io_bytes(w, backward=False):
 def tsplit_factor(w, backward):
     """Segments of the library's time split for workload w (1 = none); mirrors the rule in
     csrc/gdn_tsplit.cu: heads at most 64 wide, B*H*P <= 152 SMs, T divisible by P, >= 512 tokens per
-    segment, P >= 4 for a delta forward and >= 3 otherwise."""
+    segment, P >= 4 for a delta forward, >= 3 for a gated one and >= 2 for a backward."""
     if w.dk > 64 or w.dv > 64:
         return 1
     units = w.B * w.H
-    min_p = 3 if backward else (4 if w.mode == "delta" else 3)
+    min_p = 2 if backward else (4 if w.mode == "delta" else 3)
     for p in range(152 // units, min_p - 1, -1):
         if w.T % p == 0 and w.T // p >= 512:
             return p

@@ -25,11 +25,13 @@
 //
 // The backward splits the same way.  With the segments' entering states S_p
 // from steps 1-3, the adjoint dL/dS_p of a segment is G_p + A_p^T E_p, where
-// G_p is the segment's own backward started from a zero end gradient and E_p
-// the gradient at its end (dh_T for the last one, dL/dS_{p+1} otherwise):
-//   5. every segment's backward from S_p with a zero end gradient -> G_p
+// G_p is its adjoint with a zero end gradient and E_p the gradient at its end
+// (dh_T for the last one, dL/dS_{p+1} otherwise).  The outputs depend on S_p
+// only through o_t = S_p^T (Phi_t^T c_t) + (terms free of S_p), so
+//   5. G_p = sum_t (Phi_t^T c_t) do_t^T over the segment: the transition
+//      run's outputs (delta) or c_t (.) exp(A Gam_t) (gated) against dO
 //   6. a reverse scan  E_{p-1} = G_p + A_p^T E_p,  dh0 = G_0 + A_0^T E_0
-//   7. every segment's backward again from S_p with end gradient E_p
+//   7. every segment's backward from S_p with end gradient E_p
 // Step 7's gradients are the true ones; dA_log sums over all (batch,
 // segment) pairs, which the backward's own reduction over its batch does.
 #include <cuda_bf16.h>
@@ -185,6 +187,89 @@ __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const 
     }
 }
 
+// Step 5 for one (view batch, head) unit: G[i][j] = sum_t q_t[i] do_t[j] over the segment's tokens, q_t as in
+// tsplit_out_kernel.  Thread t accumulates the 4 x 4 tile rows 4 (t >> 4) .., columns 4 (t & 15) .. in fp32 over
+// 64-token sub-tiles of q and dO staged in shared memory, in token order (deterministic).
+template <typename IO, bool DELTA>
+__global__ void __launch_bounds__(256) tsplit_gp_kernel(const float* so, const IO* c, const IO* g, const IO* dO,
+                                                        const float* A_log, float* G, int H, int Ts, int dk, int dv,
+                                                        int logits, int norm)
+{
+    __shared__ __align__(16) float q[kOutTile][64];
+    __shared__ __align__(16) float dd[kOutTile][64];
+    __shared__ float Gam[kOutTile];
+    __shared__ float Arow[64];
+    const int u = blockIdx.x, bv = u / H, h = u % H, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int i0 = 4 * (tid >> 4), j0 = 4 * (tid & 15);
+    auto row = [&](int t) { return ((size_t)bv * Ts + t) * H + h; };
+    if (!DELTA && tid < 64) Arow[tid] = tid < dk ? -expf(A_log[h * dk + tid]) : 0.f;
+    float acc[4][4] = {};
+    float base = 0.f;
+    for (int t0 = 0; t0 < Ts; t0 += kOutTile) {
+        const int nt = min(kOutTile, Ts - t0);
+        __syncthreads();   // the previous sub-tile is consumed (and Arow is set)
+        if (!DELTA && w == 0) {
+            auto gate_at = [&](int t) {
+                const float gv = (float)g[row(t)];
+                return logits ? 1.f / (1.f + expf(-gv)) : gv;
+            };
+            const float ga = 2 * lane < nt ? gate_at(t0 + 2 * lane) : 0.f;
+            const float gb = 2 * lane + 1 < nt ? gate_at(t0 + 2 * lane + 1) : 0.f;
+            float x = ga + gb;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            const float ex = __shfl_up_sync(0xffffffffu, x, 1);
+            Gam[2 * lane] = base + (lane > 0 ? ex : 0.f) + ga;
+            Gam[2 * lane + 1] = base + x;
+        }
+        for (int idx = tid; idx < kOutTile * 64; idx += 256) {
+            const int tt = idx >> 6, jj = idx & 63;
+            dd[tt][jj] = (tt < nt && jj < dv) ? (float)dO[row(t0 + tt) * dv + jj] : 0.f;
+            if (DELTA) q[tt][jj] = (tt < nt && jj < dk) ? so[row(t0 + tt) * dk + jj] : 0.f;
+        }
+        if (!DELTA) {
+            __syncthreads();   // Gam
+            for (int idx = tid; idx < kOutTile * 64; idx += 256) {
+                const int tt = idx >> 6, i = idx & 63;
+                q[tt][i] = (tt < nt && i < dk) ? (float)c[row(t0 + tt) * dk + i] * expf(Arow[i] * Gam[tt]) : 0.f;
+            }
+            if (norm) {
+                __syncthreads();
+                for (int tt = w; tt < nt; tt += 8) {
+                    float sq = 0.f;
+                    for (int i = lane; i < dk; i += 32) {
+                        const float x = (float)c[row(t0 + tt) * dk + i];
+                        sq = fmaf(x, x, sq);
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                    const float inv = 1.f / fmaxf(sqrtf(sq), kNormFloor);
+                    for (int i = lane; i < 64; i += 32) q[tt][i] *= inv;
+                }
+            }
+            base = Gam[kOutTile - 1];
+        }
+        __syncthreads();
+        for (int tt = 0; tt < nt; tt++) {
+            const float4 qa = *reinterpret_cast<const float4*>(&q[tt][i0]);
+            const float4 da = *reinterpret_cast<const float4*>(&dd[tt][j0]);
+            const float qv[4] = {qa.x, qa.y, qa.z, qa.w}, dvv[4] = {da.x, da.y, da.z, da.w};
+#pragma unroll
+            for (int a = 0; a < 4; a++)
+#pragma unroll
+                for (int b = 0; b < 4; b++) acc[a][b] = fmaf(qv[a], dvv[b], acc[a][b]);
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; a++)
+#pragma unroll
+        for (int b = 0; b < 4; b++)
+            if (i0 + a < dk && j0 + b < dv) G[((size_t)u * dk + i0 + a) * dv + j0 + b] = acc[a][b];
+}
+
 // The scans over segments, one CTA per (batch, head), P sequential steps of a
 // 64 x 64 x 64 fp32 product:
 //   forward (steps 3):  X_0 = h0;   X_{p+1} = A_p X_p + H_p;     stores X_p, ends with h_T
@@ -321,9 +406,9 @@ int tsplit_factor(const gdn_shape_t& s, int backward)
     const long units = (long)s.B * s.H;
     // the segment scan keeps 64 x 64 tiles: wider heads are not split
     if (s.dk > 64 || s.dv > 64) return 1;
-    // forward: three passes (delta) or two (gated) must still pay; backward: two backward passes, the
-    // forward passes are cheap beside them
-    const int min_p = backward ? 3 : (s.mode == GDN_DELTA ? 4 : 3);
+    // forward: three passes (delta) or two (gated) must still pay; backward: one backward pass over T / P,
+    // the forward passes and the G_p reduction are cheap beside it
+    const int min_p = backward ? 2 : (s.mode == GDN_DELTA ? 4 : 3);
     const long cap = kSplitSMs / units;
     for (long p = cap; p >= min_p; p--) {
         if (s.T % p) continue;
@@ -432,21 +517,41 @@ cudaError_t launch_bwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
     fa.hT = nullptr;
     if ((e = tsplit_states(fa, L, P, st, fwd_core)) != cudaSuccess) return e;
 
-    // 5. every segment's backward from a zero end gradient: G_p in Gbuf
+    // 5. G_p = sum_t (Phi_t^T c_t) do_t^T over each segment
+    const float* so = (const float*)(ws + L.ts_so_off);
+    const int Ts = a.T / P;
+    const int vunits = a.B * P * a.H;
+    if (a.io == GDN_BF16) {
+        if (a.mode == GDN_DELTA)
+            tsplit_gp_kernel<__nv_bfloat16, true><<<vunits, 256, 0, st>>>(
+                so, (const __nv_bfloat16*)a.c, (const __nv_bfloat16*)a.g, (const __nv_bfloat16*)a.dO, a.A_log, Gbuf,
+                a.H, Ts, a.dk, a.dv, a.logits, a.norm);
+        else
+            tsplit_gp_kernel<__nv_bfloat16, false><<<vunits, 256, 0, st>>>(
+                so, (const __nv_bfloat16*)a.c, (const __nv_bfloat16*)a.g, (const __nv_bfloat16*)a.dO, a.A_log, Gbuf,
+                a.H, Ts, a.dk, a.dv, a.logits, a.norm);
+    } else {
+        if (a.mode == GDN_DELTA)
+            tsplit_gp_kernel<float, true><<<vunits, 256, 0, st>>>(so, (const float*)a.c, (const float*)a.g,
+                                                                  (const float*)a.dO, a.A_log, Gbuf, a.H, Ts, a.dk,
+                                                                  a.dv, a.logits, a.norm);
+        else
+            tsplit_gp_kernel<float, false><<<vunits, 256, 0, st>>>(so, (const float*)a.c, (const float*)a.g,
+                                                                   (const float*)a.dO, a.A_log, Gbuf, a.H, Ts, a.dk,
+                                                                   a.dv, a.logits, a.norm);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     Args b = a;
     b.B = a.B * P;
     b.T = a.T / P;
     b.h0 = Sst;
-    b.dhT = nullptr;
-    b.dh0 = Gbuf;
-    if ((e = launch_serial_bwd(b, st)) != cudaSuccess) return e;
 
     // 6. reverse scan of the end gradients; dh0 of the whole sequence
     const float* Abuf = (const float*)(ws + L.ts_a_off);
     launch_seg_scan<true>(a, P, Abuf, Gbuf, a.dhT, Ebuf, a.dh0, st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    // 7. every segment's backward again with its true end gradient
+    // 7. every segment's backward with its true end gradient
     b.dhT = Ebuf;
     b.dh0 = nullptr;
     return launch_serial_bwd(b, st);

@@ -54,8 +54,9 @@ def test_tsplit_in_place_state():
 @pytest.mark.parametrize("mode", ["gated", "delta"])
 @pytest.mark.parametrize("io,B,H,T,d", [("bf16", 1, 4, 4096, 64), ("bf16", 2, 3, 3072, 56), ("f32", 1, 2, 2048, 32)])
 def test_tsplit_backward_parity(mode, io, B, H, T, d):
-    """The split backward: segment adjoints from a zero end gradient, a reverse scan of the end gradients,
-    then every segment's backward again; every gradient against the oracle, with h0 and dh_T given."""
+    """The split backward: segment adjoints G_p = sum_t (Phi_t^T c_t) do_t^T, a reverse scan of the end
+    gradients, then every segment's backward from its entering state; every gradient against the oracle, with h0
+    and dh_T given."""
     from tests.gdn_testlib import run_bwd
     w = I.custom(name=f"tsb_{mode}_{io}_{B}x{H}x{T}x{d}", mode=mode, dtype=io, B=B, H=H, T=T, dk=d, dv=d,
                  seed=3 * T + d, h0_std=0.3, b_dist="l2norm" if mode == "delta" else "normal/8", c_dist="l2norm",
@@ -88,3 +89,19 @@ def test_tsplit_ragged_segments(mode):
     for k in ("dv", "db", "dc", "dg", "dbeta", "dA_log", "dh0"):
         if ref[k] is not None:
             assert_close(got[k], ref[k], TOL["bf16"], k)
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+def test_tsplit_backward_two_segments(mode):
+    """40 heads over 1024 tokens: the forward stays whole, the backward splits into two segments of 512."""
+    from tests.gdn_testlib import run_bwd
+    w = I.custom(name=f"tsb2_{mode}", mode=mode, dtype="f32", B=1, H=40, T=1024, dk=32, dv=32, seed=33,
+                 h0_std=0.3, b_dist="l2norm" if mode == "delta" else "normal/8", c_dist="l2norm", g_mu=-1.0,
+                 backward=True)
+    x = I.make_inputs(w)
+    dhT = I.round_to(0.4 * I.normal(92, 1, w.H * 32 * 32).reshape(1, w.H, 32, 32), "f32")
+    got = run_bwd(w, x, dhT=dhT)
+    ref = oracle.gdn_bwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], x["dO"], dhT, mode=w.mode)
+    for k in ("dv", "db", "dc", "dg", "dbeta", "dA_log", "dh0"):
+        if ref[k] is not None:
+            assert_close(got[k], ref[k], TOL["f32"], k)
