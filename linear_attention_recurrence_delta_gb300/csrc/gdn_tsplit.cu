@@ -54,18 +54,31 @@ __global__ void eye_kernel(float* I, size_t n_units, int dk)
 // Step 4 for one (view batch, head) unit and a run of kOutRun of its segment's tokens: o_t = o0_t + S_p^T q_t
 // with q_t = Phi_t^T c_t (delta: from the transition run; gated: c_t (.) exp(A Gam_t)).  Thread (j, r) holds
 // column j of S_p in registers; the run goes in sub-tiles of 64 tokens whose q and o0 rows are staged in
-// shared memory, thread (j, r) computing tokens r, r + 4, ... of each.  Gated: the gates of the segment
-// before the run are a fixed-order block sum, then a running inclusive scan over the sub-tiles.
+// shared memory, thread (j, r) computing tokens r, r + 4, ... of each.  With rows of whole 16-byte quads the
+// next sub-tile's o0 (and, delta, q) rows stream in by cp.async into a second buffer while one computes.
+// Gated: the gates of the segment before the run are a fixed-order block sum, then a running inclusive scan
+// over the sub-tiles.
 constexpr int kOutTile = 64;
 constexpr int kOutRun = 512;
+
+struct OutSmem {
+    float q[2][kOutTile][64];
+    float oz[2][kOutTile][64];
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+{
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
 
 template <typename IO, bool DELTA>
 __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const float* so, const IO* c, const IO* g,
                                                          const float* A_log, const float* Sst, IO* o, int H, int Ts,
                                                          int dk, int dv, int logits, int norm)
 {
-    __shared__ __align__(16) float q[kOutTile][64];
-    __shared__ __align__(16) float oz[kOutTile][64];
+    extern __shared__ __align__(16) unsigned char out_smem[];
+    OutSmem& sm = *reinterpret_cast<OutSmem*>(out_smem);
     __shared__ float Gam[kOutTile];
     __shared__ float red[8];
     __shared__ float Arow[64];
@@ -99,9 +112,36 @@ __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const 
         for (int ww = 0; ww < 8; ww++) base += red[ww];
     }
 
-    for (int t0 = run0; t0 < run_end; t0 += kOutTile) {
+    // the sub-tile from t0 into buffer sb by cp.async (zeros past the run and the row width), one commit group
+    const bool quads = (dv & 3) == 0 && (!DELTA || (dk & 3) == 0);
+    auto stage_async = [&](int t0, int sb) {
         const int nt = min(kOutTile, run_end - t0);
-        __syncthreads();   // the previous sub-tile's rows are consumed
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const int idx = tid + 256 * m, tt = idx >> 4, c4 = 4 * (idx & 15);
+            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            float* od = &sm.oz[sb][tt][c4];
+            if (tt < nt && c4 < dv) cp_async16(od, o0 + row(t0 + tt) * dv + c4);
+            else *reinterpret_cast<float4*>(od) = z4;
+            if (DELTA) {
+                float* qd = &sm.q[sb][tt][c4];
+                if (tt < nt && c4 < dk) cp_async16(qd, so + row(t0 + tt) * dk + c4);
+                else *reinterpret_cast<float4*>(qd) = z4;
+            }
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+    if (quads) stage_async(run0, 0);
+
+    for (int t0 = run0, sb = 0; t0 < run_end; t0 += kOutTile, sb ^= 1) {
+        const int nt = min(kOutTile, run_end - t0);
+        float (*q)[64] = sm.q[sb];
+        float (*oz)[64] = sm.oz[sb];
+        __syncthreads();   // the previous sub-tile's rows are consumed: its buffer takes the next sub-tile's
+        if (quads) {
+            if (t0 + kOutTile < run_end) stage_async(t0 + kOutTile, sb ^ 1);
+            else asm volatile("cp.async.commit_group;\n" ::: "memory");
+        }
         if (!DELTA && w == 0) {   // inclusive scan of the sub-tile's gates (two per lane) on top of `base`
             const float ga = 2 * lane < nt ? gate_at(t0 + 2 * lane) : 0.f;
             const float gb = 2 * lane + 1 < nt ? gate_at(t0 + 2 * lane + 1) : 0.f;
@@ -115,26 +155,9 @@ __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const 
             Gam[2 * lane] = base + (lane > 0 ? ex : 0.f) + ga;
             Gam[2 * lane + 1] = base + x;
         }
-        // the sub-tile's o0 (and, delta, q) rows: four 16-byte quads per thread and array, all in flight at once
-        // (whole quads need rows of a multiple of 4 floats; otherwise element by element)
-        if ((dv & 3) == 0 && (!DELTA || (dk & 3) == 0)) {
-            float4 xo[4], xq[4];
-#pragma unroll
-            for (int m = 0; m < 4; m++) {
-                const int idx = tid + 256 * m, tt = idx >> 4, c4 = 4 * (idx & 15);
-                const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                xo[m] = (tt < nt && c4 < dv) ? *reinterpret_cast<const float4*>(o0 + row(t0 + tt) * dv + c4) : z4;
-                if (DELTA)
-                    xq[m] = (tt < nt && c4 < dk) ? *reinterpret_cast<const float4*>(so + row(t0 + tt) * dk + c4)
-                                                 : z4;
-            }
-#pragma unroll
-            for (int m = 0; m < 4; m++) {
-                const int idx = tid + 256 * m, tt = idx >> 4, c4 = 4 * (idx & 15);
-                *reinterpret_cast<float4*>(&oz[tt][c4]) = xo[m];
-                if (DELTA) *reinterpret_cast<float4*>(&q[tt][c4]) = xq[m];
-            }
-        } else {
+        // the sub-tile's o0 (and, delta, q) rows: in flight since the previous sub-tile, or (rows not of whole
+        // quads) element by element now
+        if (!quads) {
             for (int idx = tid; idx < kOutTile * 64; idx += 256) {
                 const int tt = idx >> 6, jj = idx & 63;
                 oz[tt][jj] = (tt < nt && jj < dv) ? o0[row(t0 + tt) * dv + jj] : 0.f;
@@ -170,6 +193,7 @@ __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const 
             }
             base = Gam[kOutTile - 1];   // (tokens past the run's end add zero)
         }
+        if (quads) asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // this sub-tile's group
         __syncthreads();
         if (j < dv) {
             for (int tt = r; tt < nt; tt += 4) {
@@ -187,56 +211,139 @@ __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const 
     }
 }
 
-// Step 5 for one (view batch, head) unit: G[i][j] = sum_t q_t[i] do_t[j] over the segment's tokens, q_t as in
-// tsplit_out_kernel.  Thread t accumulates the 4 x 4 tile rows 4 (t >> 4) .., columns 4 (t & 15) .. in fp32 over
-// 64-token sub-tiles of q and dO staged in shared memory, in token order (deterministic).
+template <typename IO>
+cudaError_t out_smem_attr(int bytes)
+{
+    cudaError_t e = cudaFuncSetAttribute(tsplit_out_kernel<IO, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tsplit_out_kernel<IO, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e;
+}
+
+// Step 5 for one (view batch, head) unit and a run of kGpRun of its segment's tokens: the run's share
+// sum_t q_t do_t^T of G_p, q_t as in tsplit_out_kernel.  Thread t accumulates rows 4 (t >> 4) .. + 3, columns
+// 4 (t & 15) .. + 3 in fp32 (packed pairs) over 64-token sub-tiles of q and dO staged in shared memory, in
+// token order; with rows of whole 16-byte pieces the next sub-tile streams in by cp.async while one computes.
+// One run per segment writes G_p itself; otherwise each run writes a partial that gp_reduce_kernel adds up in
+// run order (deterministic).
+constexpr int kGpRun = 512;
+
+struct GpSmem {
+    float q[2][kOutTile][64];
+    float d[2][kOutTile][64];   // dO rows as stored (bf16 use the first half of each row's bytes)
+};
+
+__device__ __forceinline__ void ld4(const float* p, float (&x)[4])
+{
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+__device__ __forceinline__ void ld4(const __nv_bfloat16* p, float (&x)[4])
+{
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xffff0000u);
+    x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+
 template <typename IO, bool DELTA>
 __global__ void __launch_bounds__(256) tsplit_gp_kernel(const float* so, const IO* c, const IO* g, const IO* dO,
                                                         const float* A_log, float* G, int H, int Ts, int dk, int dv,
                                                         int logits, int norm)
 {
-    __shared__ __align__(16) float q[kOutTile][64];
-    __shared__ __align__(16) float dd[kOutTile][64];
+    extern __shared__ __align__(16) unsigned char gp_smem[];
+    GpSmem& sm = *reinterpret_cast<GpSmem*>(gp_smem);
     __shared__ float Gam[kOutTile];
+    __shared__ float red[8];
     __shared__ float Arow[64];
     const int u = blockIdx.x, bv = u / H, h = u % H, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int i0 = 4 * (tid >> 4), j0 = 4 * (tid & 15);
-    auto row = [&](int t) { return ((size_t)bv * Ts + t) * H + h; };
-    if (!DELTA && tid < 64) Arow[tid] = tid < dk ? -expf(A_log[h * dk + tid]) : 0.f;
-    float acc[4][4] = {};
-    float base = 0.f;
-    for (int t0 = 0; t0 < Ts; t0 += kOutTile) {
-        const int nt = min(kOutTile, Ts - t0);
-        __syncthreads();   // the previous sub-tile is consumed (and Arow is set)
-        if (!DELTA && w == 0) {
-            auto gate_at = [&](int t) {
-                const float gv = (float)g[row(t)];
-                return logits ? 1.f / (1.f + expf(-gv)) : gv;
-            };
-            const float ga = 2 * lane < nt ? gate_at(t0 + 2 * lane) : 0.f;
-            const float gb = 2 * lane + 1 < nt ? gate_at(t0 + 2 * lane + 1) : 0.f;
-            float x = ga + gb;
+    const int run0 = kGpRun * blockIdx.y, run_end = min(Ts, run0 + kGpRun);
+    auto row = [&](int t) { return ((size_t)bv * Ts + t) * H + h; };   // token row of the [B*P, T/P, H] view
+    auto gate_at = [&](int t) {
+        const float gv = (float)g[row(t)];
+        return logits ? 1.f / (1.f + expf(-gv)) : gv;
+    };
+    constexpr int E = 16 / sizeof(IO);   // dO elements per 16-byte piece
+
+    float base = 0.f;   // gated: sum of the segment's gates before the current sub-tile
+    if (!DELTA) {
+        if (tid < 64) Arow[tid] = tid < dk ? -expf(A_log[h * dk + tid]) : 0.f;
+        float part = 0.f;
+        for (int t = tid; t < run0; t += 256) part += gate_at(t);
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, x, off);
-                if (lane >= off) x += y;
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) red[w] = part;
+        __syncthreads();
+#pragma unroll
+        for (int ww = 0; ww < 8; ww++) base += red[ww];
+    }
+
+    // rows past the sub-tile are never read and columns past d_k / d_v only reach accumulators that are not
+    // stored, so the staging leaves them as they are
+    const bool pieces = (dv % E) == 0 && ((uintptr_t)dO & 15) == 0 && (!DELTA || (dk & 3) == 0);
+    auto stage_async = [&](int t0, int sb) {
+        const int nt = min(kOutTile, run_end - t0);
+        IO* dd = reinterpret_cast<IO*>(&sm.d[sb][0][0]);
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const int idx = tid + 256 * m;
+            if (DELTA) {
+                const int tt = idx >> 4, c4 = 4 * (idx & 15);
+                if (tt < nt && c4 < dk) cp_async16(&sm.q[sb][tt][c4], so + row(t0 + tt) * dk + c4);
             }
-            const float ex = __shfl_up_sync(0xffffffffu, x, 1);
-            Gam[2 * lane] = base + (lane > 0 ? ex : 0.f) + ga;
-            Gam[2 * lane + 1] = base + x;
+            const int tt = idx / (64 / E), ce = E * (idx % (64 / E));
+            if (tt < nt && ce < dv) cp_async16(dd + tt * 64 + ce, dO + row(t0 + tt) * dv + ce);
         }
-        for (int idx = tid; idx < kOutTile * 64; idx += 256) {
-            const int tt = idx >> 6, jj = idx & 63;
-            dd[tt][jj] = (tt < nt && jj < dv) ? (float)dO[row(t0 + tt) * dv + jj] : 0.f;
-            if (DELTA) q[tt][jj] = (tt < nt && jj < dk) ? so[row(t0 + tt) * dk + jj] : 0.f;
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+    if (pieces) stage_async(run0, 0);
+
+    float2 acc[4][2];
+#pragma unroll
+    for (int a = 0; a < 4; a++) acc[a][0] = acc[a][1] = make_float2(0.f, 0.f);
+    for (int t0 = run0, sb = 0; t0 < run_end; t0 += kOutTile, sb ^= 1) {
+        const int nt = min(kOutTile, run_end - t0);
+        float (*q)[64] = sm.q[sb];
+        const IO* dd = reinterpret_cast<const IO*>(&sm.d[sb][0][0]);
+        __syncthreads();   // the previous sub-tile is consumed: its buffer takes the next one
+        if (pieces) {
+            if (t0 + kOutTile < run_end) stage_async(t0 + kOutTile, sb ^ 1);
+            else asm volatile("cp.async.commit_group;\n" ::: "memory");
+        } else {
+            IO* dw = reinterpret_cast<IO*>(&sm.d[sb][0][0]);
+            for (int idx = tid; idx < kOutTile * 64; idx += 256) {
+                const int tt = idx >> 6, jj = idx & 63;
+                if (tt < nt && jj < dv) dw[tt * 64 + jj] = dO[row(t0 + tt) * dv + jj];
+                if (DELTA && tt < nt) q[tt][jj] = jj < dk ? so[row(t0 + tt) * dk + jj] : 0.f;
+            }
         }
         if (!DELTA) {
-            __syncthreads();   // Gam
-            for (int idx = tid; idx < kOutTile * 64; idx += 256) {
-                const int tt = idx >> 6, i = idx & 63;
-                q[tt][i] = (tt < nt && i < dk) ? (float)c[row(t0 + tt) * dk + i] * expf(Arow[i] * Gam[tt]) : 0.f;
+            if (w == 0) {   // inclusive scan of the sub-tile's gates (two per lane) on top of `base`
+                const float ga = 2 * lane < nt ? gate_at(t0 + 2 * lane) : 0.f;
+                const float gb = 2 * lane + 1 < nt ? gate_at(t0 + 2 * lane + 1) : 0.f;
+                float x = ga + gb;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, off);
+                    if (lane >= off) x += y;
+                }
+                const float ex = __shfl_up_sync(0xffffffffu, x, 1);
+                Gam[2 * lane] = base + (lane > 0 ? ex : 0.f) + ga;
+                Gam[2 * lane + 1] = base + x;
             }
-            if (norm) {
+            float cv[16];   // the sub-tile's c rows, all loads in flight before the exponentials
+#pragma unroll
+            for (int m = 0; m < 16; m++) {
+                const int idx = tid + 256 * m, tt = idx >> 6, i = idx & 63;
+                cv[m] = (tt < nt && i < dk) ? (float)c[row(t0 + tt) * dk + i] : 0.f;
+            }
+            __syncthreads();   // Gam
+#pragma unroll
+            for (int m = 0; m < 16; m++) {
+                const int idx = tid + 256 * m, tt = idx >> 6, i = idx & 63;
+                q[tt][i] = cv[m] * expf(Arow[i] * Gam[tt]);
+            }
+            if (norm) {   // c_t / max(||c_t||, floor): one warp per token row
                 __syncthreads();
                 for (int tt = w; tt < nt; tt += 8) {
                     float sq = 0.f;
@@ -250,24 +357,53 @@ __global__ void __launch_bounds__(256) tsplit_gp_kernel(const float* so, const I
                     for (int i = lane; i < 64; i += 32) q[tt][i] *= inv;
                 }
             }
-            base = Gam[kOutTile - 1];
+            base = Gam[kOutTile - 1];   // (tokens past the run's end add zero)
         }
+        if (pieces) asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // this sub-tile's group
         __syncthreads();
         for (int tt = 0; tt < nt; tt++) {
-            const float4 qa = *reinterpret_cast<const float4*>(&q[tt][i0]);
-            const float4 da = *reinterpret_cast<const float4*>(&dd[tt][j0]);
-            const float qv[4] = {qa.x, qa.y, qa.z, qa.w}, dvv[4] = {da.x, da.y, da.z, da.w};
+            float qv[4], dv4[4];
+            ld4(&q[tt][i0], qv);
+            ld4(dd + tt * 64 + j0, dv4);
+            const float2 d01 = make_float2(dv4[0], dv4[1]), d23 = make_float2(dv4[2], dv4[3]);
 #pragma unroll
-            for (int a = 0; a < 4; a++)
-#pragma unroll
-                for (int b = 0; b < 4; b++) acc[a][b] = fmaf(qv[a], dvv[b], acc[a][b]);
+            for (int a = 0; a < 4; a++) {
+                const float2 qa = make_float2(qv[a], qv[a]);
+                acc[a][0] = __ffma2_rn(qa, d01, acc[a][0]);
+                acc[a][1] = __ffma2_rn(qa, d23, acc[a][1]);
+            }
         }
     }
+    float* Gout = G + (size_t)(u * gridDim.y + blockIdx.y) * dk * dv;
 #pragma unroll
-    for (int a = 0; a < 4; a++)
+    for (int a = 0; a < 4; a++) {
+        const float r[4] = {acc[a][0].x, acc[a][0].y, acc[a][1].x, acc[a][1].y};
 #pragma unroll
         for (int b = 0; b < 4; b++)
-            if (i0 + a < dk && j0 + b < dv) G[((size_t)u * dk + i0 + a) * dv + j0 + b] = acc[a][b];
+            if (i0 + a < dk && j0 + b < dv) Gout[(size_t)(i0 + a) * dv + j0 + b] = r[b];
+    }
+}
+
+// G_p = the runs' partials [unit][run][d_k x d_v] added in run order
+__global__ void gp_reduce_kernel(const float* part, float* G, int units, int runs, int n)
+{
+    const size_t total = (size_t)units * n;
+    for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+        const size_t u = e / n, k = e - u * n;
+        const float* p = part + u * runs * n + k;
+        float x = 0.f;
+        for (int r = 0; r < runs; r++) x += p[(size_t)r * n];
+        G[e] = x;
+    }
+}
+
+template <typename IO>
+cudaError_t gp_smem_attr(int bytes)
+{
+    cudaError_t e = cudaFuncSetAttribute(tsplit_gp_kernel<IO, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tsplit_gp_kernel<IO, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e;
 }
 
 // The scans over segments, one CTA per (batch, head), P sequential steps of a
@@ -481,22 +617,26 @@ cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
     const float* Sst = (const float*)(ws + L.ts_s_off);
     const int Ts = a.T / P;
     const dim3 grid(a.B * P * a.H, (Ts + kOutRun - 1) / kOutRun);
+    const int osm = (int)sizeof(OutSmem);
+    cudaError_t e2;
+    if ((e2 = out_smem_attr<__nv_bfloat16>(osm)) != cudaSuccess || (e2 = out_smem_attr<float>(osm)) != cudaSuccess)
+        return e2;
     if (a.io == GDN_BF16) {
         if (a.mode == GDN_DELTA)
-            tsplit_out_kernel<__nv_bfloat16, true><<<grid, 256, 0, st>>>(
+            tsplit_out_kernel<__nv_bfloat16, true><<<grid, 256, osm, st>>>(
                 o0, so, (const __nv_bfloat16*)a.c, (const __nv_bfloat16*)a.g, a.A_log, Sst, (__nv_bfloat16*)a.o, a.H,
                 Ts, a.dk, a.dv, a.logits, a.norm);
         else
-            tsplit_out_kernel<__nv_bfloat16, false><<<grid, 256, 0, st>>>(
+            tsplit_out_kernel<__nv_bfloat16, false><<<grid, 256, osm, st>>>(
                 o0, so, (const __nv_bfloat16*)a.c, (const __nv_bfloat16*)a.g, a.A_log, Sst, (__nv_bfloat16*)a.o, a.H,
                 Ts, a.dk, a.dv, a.logits, a.norm);
     } else {
         if (a.mode == GDN_DELTA)
-            tsplit_out_kernel<float, true><<<grid, 256, 0, st>>>(o0, so, (const float*)a.c, (const float*)a.g, a.A_log,
+            tsplit_out_kernel<float, true><<<grid, 256, osm, st>>>(o0, so, (const float*)a.c, (const float*)a.g, a.A_log,
                                                                  Sst, (float*)a.o, a.H, Ts, a.dk, a.dv, a.logits,
                                                                  a.norm);
         else
-            tsplit_out_kernel<float, false><<<grid, 256, 0, st>>>(o0, so, (const float*)a.c, (const float*)a.g,
+            tsplit_out_kernel<float, false><<<grid, 256, osm, st>>>(o0, so, (const float*)a.c, (const float*)a.g,
                                                                   a.A_log, Sst, (float*)a.o, a.H, Ts, a.dk, a.dv,
                                                                   a.logits, a.norm);
     }
@@ -517,30 +657,42 @@ cudaError_t launch_bwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
     fa.hT = nullptr;
     if ((e = tsplit_states(fa, L, P, st, fwd_core)) != cudaSuccess) return e;
 
-    // 5. G_p = sum_t (Phi_t^T c_t) do_t^T over each segment
+    // 5. G_p = sum_t (Phi_t^T c_t) do_t^T over each segment, by runs of kGpRun tokens; with several runs their
+    //    partials go where the zero-start outputs were (dead in the backward: at most 2 T/P / kGpRun * d_k <=
+    //    T/P * d_v / 4 floats per unit, within its T/P * d_v)
     const float* so = (const float*)(ws + L.ts_so_off);
     const int Ts = a.T / P;
     const int vunits = a.B * P * a.H;
+    const int runs = (Ts + kGpRun - 1) / kGpRun;
+    float* Gpart = runs > 1 ? (float*)(ws + L.ts_o_off) : Gbuf;
+    const dim3 ggrid(vunits, runs);
+    const int gsm = (int)sizeof(GpSmem);
+    if ((e = gp_smem_attr<__nv_bfloat16>(gsm)) != cudaSuccess || (e = gp_smem_attr<float>(gsm)) != cudaSuccess)
+        return e;
     if (a.io == GDN_BF16) {
         if (a.mode == GDN_DELTA)
-            tsplit_gp_kernel<__nv_bfloat16, true><<<vunits, 256, 0, st>>>(
-                so, (const __nv_bfloat16*)a.c, (const __nv_bfloat16*)a.g, (const __nv_bfloat16*)a.dO, a.A_log, Gbuf,
+            tsplit_gp_kernel<__nv_bfloat16, true><<<ggrid, 256, gsm, st>>>(
+                so, (const __nv_bfloat16*)a.c, (const __nv_bfloat16*)a.g, (const __nv_bfloat16*)a.dO, a.A_log, Gpart,
                 a.H, Ts, a.dk, a.dv, a.logits, a.norm);
         else
-            tsplit_gp_kernel<__nv_bfloat16, false><<<vunits, 256, 0, st>>>(
-                so, (const __nv_bfloat16*)a.c, (const __nv_bfloat16*)a.g, (const __nv_bfloat16*)a.dO, a.A_log, Gbuf,
+            tsplit_gp_kernel<__nv_bfloat16, false><<<ggrid, 256, gsm, st>>>(
+                so, (const __nv_bfloat16*)a.c, (const __nv_bfloat16*)a.g, (const __nv_bfloat16*)a.dO, a.A_log, Gpart,
                 a.H, Ts, a.dk, a.dv, a.logits, a.norm);
     } else {
         if (a.mode == GDN_DELTA)
-            tsplit_gp_kernel<float, true><<<vunits, 256, 0, st>>>(so, (const float*)a.c, (const float*)a.g,
-                                                                  (const float*)a.dO, a.A_log, Gbuf, a.H, Ts, a.dk,
-                                                                  a.dv, a.logits, a.norm);
-        else
-            tsplit_gp_kernel<float, false><<<vunits, 256, 0, st>>>(so, (const float*)a.c, (const float*)a.g,
-                                                                   (const float*)a.dO, a.A_log, Gbuf, a.H, Ts, a.dk,
+            tsplit_gp_kernel<float, true><<<ggrid, 256, gsm, st>>>(so, (const float*)a.c, (const float*)a.g,
+                                                                   (const float*)a.dO, a.A_log, Gpart, a.H, Ts, a.dk,
                                                                    a.dv, a.logits, a.norm);
+        else
+            tsplit_gp_kernel<float, false><<<ggrid, 256, gsm, st>>>(so, (const float*)a.c, (const float*)a.g,
+                                                                    (const float*)a.dO, a.A_log, Gpart, a.H, Ts, a.dk,
+                                                                    a.dv, a.logits, a.norm);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (runs > 1) {
+        gp_reduce_kernel<<<256, 256, 0, st>>>(Gpart, Gbuf, vunits, runs, a.dk * a.dv);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     Args b = a;
     b.B = a.B * P;
     b.T = a.T / P;

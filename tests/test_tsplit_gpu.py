@@ -105,3 +105,34 @@ def test_tsplit_backward_two_segments(mode):
     for k in ("dv", "db", "dc", "dg", "dbeta", "dA_log", "dh0"):
         if ref[k] is not None:
             assert_close(got[k], ref[k], TOL["f32"], k)
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+def test_tsplit_backward_dO_offset(mode):
+    """fp32 dO need only be 4-byte aligned: an upstream gradient starting 4 bytes into its buffer takes the split
+    backward's element-wise staging instead of 16-byte copies.  T = 3000 over two heads: five segments of 600
+    tokens, each summed in two runs."""
+    w = I.custom(name=f"tso_{mode}", mode=mode, dtype="f32", B=1, H=2, T=3000, dk=32, dv=32, seed=57, h0_std=0.3,
+                 b_dist="l2norm" if mode == "delta" else "normal/8", c_dist="l2norm", g_mu=-1.0, backward=True)
+    x = I.make_inputs(w)
+    s = gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.mode, w.dtype)
+    t = {k: dev(x[k], "f32") for k in ("v", "b", "c", "g", "beta")}
+    n = w.B * w.T * w.H * w.dv
+    raw = torch.zeros(n + 1, dtype=torch.float32, device="cuda")
+    dO = raw[1:].view(w.B, w.T, w.H, w.dv)
+    dO.copy_(dev(x["dO"], "f32"))
+    assert dO.data_ptr() % 16 != 0
+    out = {k: torch.empty_like(t[k]) for k in ("v", "b", "c", "g")}
+    dbeta = torch.empty_like(t["beta"]) if mode == "delta" else None
+    dA = torch.empty((w.H, w.dk), dtype=torch.float32, device="cuda")
+    dh0 = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+    ws = torch.empty(gdn.gdn_workspace_bytes(s, 1), dtype=torch.uint8, device="cuda")
+    gdn.check(gdn.gdn_bwd(s, t["v"], t["b"], t["c"], t["g"], t["beta"] if mode == "delta" else None,
+                          dev32(x["A_log"]), dev32(x["h0"]), dO, None, out["v"], out["b"], out["c"], out["g"], dbeta,
+                          dA, dh0, ws))
+    gdn.check(gdn.gdn_last_device_status(ws), "device status")
+    ref = oracle.gdn_bwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], x["dO"], None, mode=w.mode)
+    got = {"dv": out["v"], "db": out["b"], "dc": out["c"], "dg": out["g"], "dbeta": dbeta, "dA_log": dA, "dh0": dh0}
+    for k, v in got.items():
+        if ref[k] is not None:
+            assert_close(v.double().cpu().numpy(), ref[k], TOL["f32"], k)
