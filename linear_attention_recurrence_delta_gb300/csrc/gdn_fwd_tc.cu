@@ -33,15 +33,17 @@
 // it fails every factor is evaluated directly and the L3 entries elementwise
 // in fp32.
 //
-// Delta solve (WY form): the 16x16 diagonal blocks D of I + M are inverted in
-// fp32 by forward substitution; with L = I + M - D and N = D^{-1} L (N^4 = 0)
-//   (I + M)^{-1} R = (I + N^2)(I - N) D^{-1} R,   R = [beta V | beta Btil]
-// as [N | X0] = D^{-1}[L | R], [N^2 | N X0] = N [N | X0], Z = X0 - N X0,
-// [Util | W] = Z + N^2 Z (Z kept exactly in TMEM as the accumulator start).
+// Delta solve (WY form): D, the two 32x32 diagonal blocks of I + M, is
+// inverted in fp32: its 16x16 diagonal blocks by forward substitution, and
+// each 32-block [[A, 0], [C, B]] as [[A^-1, 0], [-B^-1 C A^-1, B^-1]].  With
+// L = I + M - D (rows 32..63, columns 0..31 only), N = D^{-1} L has N^2 = 0, so
+//   (I + M)^{-1} R = (I - N) D^{-1} R,   R = [beta V | beta Btil]
+// as [N | X0] = D^{-1}[L | R], then [Util | W] = X0 - N X0 (X0 kept exactly in
+// TMEM as the accumulator start).
 //
 // Precision: the L1/L2 operands (factors <= 1) are fp16; L3, P, Bhat^T, the
-// state and, in delta mode, R, X0, Z and U enter their MMAs as bf16 hi + lo
-// pairs (hi*hi + hi*lo + lo*hi); D^{-1}, L, N, N^2, W, Ctil are plain bf16.
+// state and, in delta mode, R, X0 and U enter their MMAs as bf16 hi + lo
+// pairs (hi*hi + hi*lo + lo*hi); D^{-1}, L, N, W, Ctil are plain bf16.
 //
 // CTA = one (b, h), 8 warps (thread r <-> TMEM lane r & 127; warps w and
 // w + 4 share a lane quarter and split the columns).  Thread 0 issues the MMAs
@@ -80,17 +82,18 @@ constexpr uint32_t X_A1 = 0, X_B1a = 16384, X_B1b = 18432, X_B1c = 22528;
 constexpr uint32_t X_A2 = 28672, X_B2 = 45056, X_A3 = 53248, X_A3L = 69632, X_B3 = 86016, X_B3L = 94208;
 //   gated, after the levels: [0 ; Ctil]
 constexpr uint32_t X_CH1 = 0;
-//   delta phase 2: [N | X0] = Dinv [L | R]
-constexpr uint32_t X_DINV = 0, X_LRH = 16384, X_LRL = 40960, X_M32 = 57344, X_DI32 = 62464;
+//   delta phase 2: [N | X0] = Dinv [L | R], Dinv the inverse of the diagonal 32-blocks; fp32 staging of the
+//   diagonal 16-blocks (M32), their inverses (DI32), the 16-blocks below them (C32) and the inverses' coupling
+//   blocks (E32)
+constexpr uint32_t X_DINV = 0, X_LRH = 16384, X_LRL = 40960;
+constexpr uint32_t X_M32 = 57344, X_DI32 = 62464, X_C32 = 67584, X_E32 = 70144;
 // fp32 16x16 blocks with a padded row stride (conflict-free float4 rows)
 constexpr int kBS = 20;
-//   delta phase 3: [N^2 | N X0] = N [N | X0]
-constexpr uint32_t X_NA = 0, X_NXH = 16384, X_NXL = 40960;
-//   delta phase 4: [Util | W] = Z + N^2 Z
-constexpr uint32_t X_N2A = 0, X_ZH = 16384, X_ZL = 32768;
-//   delta phase 5: the state products
-//   (CW sits past the phase-4 operands so that its Ctil rows can be built while the phase-4 products run)
-constexpr uint32_t X_CW = 49152, X_UH = 16384, X_UL = 24576;
+//   delta phase 3: [Util | W] = X0 - N X0 (A = -N; X0 as hi/lo B blocks)
+constexpr uint32_t X_NA = 0, X_X0H = 24576, X_X0L = 40960;
+//   delta phase 4: the state products
+//   (CW sits past the phase-3 operands so that its Ctil rows can be built while the phase-3 products run)
+constexpr uint32_t X_CW = 57344, X_UH = 16384, X_UL = 24576;
 constexpr uint32_t X_BYTES = 102400;
 constexpr uint32_t OFF_CH0 = OFF_X + X_BYTES;          // [Bhat^T ; P] hi
 constexpr uint32_t OFF_CH0L = OFF_CH0 + 16384;         // [Bhat^T ; P] lo
@@ -107,10 +110,9 @@ enum { K_A1 = 0, K_A2, K_0, K_B1_1, K_B1_2, K_B1_3, K_B2, K_BH };
 constexpr uint32_t TM_D1a = 0, TM_D1b = 16, TM_D1c = 48, TM_D2 = 96, TM_D3 = 160;
 constexpr uint32_t TM_CHG = 256;                       // gated: [dS ; O]
 constexpr uint32_t TM_NX = 256;                        // delta: [N | X0V | X0W]
-constexpr uint32_t TM_N2X = 0;                         // delta: [N^2 | N X0]
-constexpr uint32_t TM_W = 192;                         // delta: W
-constexpr uint32_t TM_U = 448;                         // delta: Util, then [U ; Ctil S]
-constexpr uint32_t TM_CHD = 384;                       // delta: [dS ; P U]
+constexpr uint32_t TM_U = TM_NX + 64;                  // delta: X0V -> Util, then [U ; Ctil S]
+constexpr uint32_t TM_W = TM_NX + 128;                 // delta: X0W -> W
+constexpr uint32_t TM_CHD = TM_NX + 128;               // delta: [dS ; P U] (W is consumed by then)
 constexpr uint32_t TM_COLS = 512;
 
 struct Small {
@@ -656,14 +658,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (!isM) {
                             st_split16(sm + OFF_CH0, sm + OFF_CH0L, 64 + t, cg, out);
                         } else {
+                            // L: the column blocks left of the row's 32-block; the diagonal 16-block (M32) and,
+                            // in the upper 16-block of a 32-block, the one below the diagonal (C32) in fp32
                             float lpart[16];
 #pragma unroll
-                            for (int c = 0; c < 16; c++) lpart[c] = (cg < tb) ? out[c] : 0.f;
+                            for (int c = 0; c < 16; c++) lpart[c] = (cg < (tb & 2)) ? out[c] : 0.f;
                             st_plain16(X + X_LRH, t, cg, lpart);
-                            if (cg == tb) {
+                            float* f32 = nullptr;
+                            if (cg == tb) f32 = M32 + (tb * 16 + (t & 15)) * kBS;
+                            else if ((tb & 1) && cg == tb - 1)
+                                f32 = reinterpret_cast<float*>(X + X_C32) + ((tb >> 1) * 16 + (t & 15)) * kBS;
+                            if (f32) {
 #pragma unroll
                                 for (int c = 0; c < 16; c += 4)
-                                    *reinterpret_cast<float4*>(M32 + (tb * 16 + (t & 15)) * kBS + c) =
+                                    *reinterpret_cast<float4*>(f32 + c) =
                                         make_float4(out[c], out[c + 1], out[c + 2], out[c + 3]);
                             }
                         }
@@ -740,6 +748,55 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     float* DI32 = reinterpret_cast<float*>(X + X_DI32) + J * 16 * kBS;
 #pragma unroll
                     for (int q = 0; q < 16; q++) DI32[q * kBS + c] = xs[q];
+                    // (5b) the 32-block [[A, 0], [C, B]] of I + M formed by the 16-blocks 2 w, 2 w + 1 (this warp's)
+                    // has the inverse [[A^-1, 0], [E, B^-1]], E = -B^-1 C A^-1: lane (half hf, column c) forms
+                    // F = C A^-1 on rows 8 hf .. 8 hf + 7 of column c, trades them with lane ^ 16, then E on the
+                    // same rows.  It runs while the idle warps prepare the next chunk.
+                    __syncwarp();
+                    {
+                        const int hf = lane >> 4, q0 = 8 * hf;
+                        const float* Ai = reinterpret_cast<const float*>(X + X_DI32) + (2 * warp) * 16 * kBS;
+                        const float* Bi = Ai + 16 * kBS;
+                        const float* Cb = reinterpret_cast<const float*>(X + X_C32) + warp * 16 * kBS;
+                        float acol[16];
+#pragma unroll
+                        for (int m = 0; m < 16; m++) acol[m] = Ai[m * kBS + c];
+                        float f[8];
+#pragma unroll
+                        for (int kq = 0; kq < 8; kq++) {
+                            float x = 0.f;
+#pragma unroll
+                            for (int m = 0; m < 16; m += 4) {
+                                const float4 cr = *reinterpret_cast<const float4*>(Cb + (q0 + kq) * kBS + m);
+                                x = fmaf(cr.x, acol[m], x);
+                                x = fmaf(cr.y, acol[m + 1], x);
+                                x = fmaf(cr.z, acol[m + 2], x);
+                                x = fmaf(cr.w, acol[m + 3], x);
+                            }
+                            f[kq] = x;
+                        }
+                        float fc[16];   // column c of F
+#pragma unroll
+                        for (int kq = 0; kq < 8; kq++) {
+                            const float o = __shfl_xor_sync(0xffffffffu, f[kq], 16);
+                            fc[kq] = hf ? o : f[kq];
+                            fc[8 + kq] = hf ? f[kq] : o;
+                        }
+                        float* Eb = reinterpret_cast<float*>(X + X_E32) + warp * 16 * kBS;
+#pragma unroll
+                        for (int kq = 0; kq < 8; kq++) {
+                            float x = 0.f;
+#pragma unroll
+                            for (int m = 0; m < 16; m += 4) {
+                                const float4 br = *reinterpret_cast<const float4*>(Bi + (q0 + kq) * kBS + m);
+                                x = fmaf(br.x, fc[m], x);
+                                x = fmaf(br.y, fc[m + 1], x);
+                                x = fmaf(br.z, fc[m + 2], x);
+                                x = fmaf(br.w, fc[m + 3], x);
+                            }
+                            Eb[(q0 + kq) * kBS + c] = -x;
+                        }
+                    }
                 } else if ((warp & 2) && k + 1 < p.nchunks) {
                     prep_idle(k + 1);   // meanwhile warps 2, 3, 6, 7: the next chunk's scan and constants
                 }
@@ -749,12 +806,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     // [N | X0] in TMEM lanes 64..127, so that the output-lane warps convert half of it.
                     const int J = (trow & 63) >> 4;
                     const float* DI32 = reinterpret_cast<const float*>(X + X_DI32) + (J * 16 + (trow & 15)) * kBS;
+                    const float* E32 = reinterpret_cast<const float*>(X + X_E32) + ((J >> 1) * 16 + (trow & 15)) * kBS;
 #pragma unroll
                     for (int cc = 0; cc < 2; cc++) {
                         const int cg = 2 * wh + cc;
+                        const float* src = (cg == J) ? DI32 : ((J & 1) && cg == J - 1) ? E32 : nullptr;
                         float v16[16];
 #pragma unroll
-                        for (int c = 0; c < 16; c++) v16[c] = (cg == J) ? DI32[c] : 0.f;
+                        for (int c = 0; c < 16; c += 4) {
+                            const float4 x = src ? *reinterpret_cast<const float4*>(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            v16[c] = x.x; v16[c + 1] = x.y; v16[c + 2] = x.z; v16[c + 3] = x.w;
+                        }
                         st_plain16(X + X_DINV, trow, cg, v16);
                     }
                 }
@@ -770,10 +832,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 if (!mma_wait_all()) break;
 
-                // (7) N -> A operand and B block; X0 -> hi/lo B blocks.  Twelve 16-column groups of token t: groups
-                // 0..5 from the state lanes, 6..11 from their copy in the output lanes.  (Rows 64..127 of the A
-                // operand keep Dinv: the N^2 product's lanes 64..127 are never read, and the N^2 step zeroes them
-                // before the product that needs them zero.)
+                // (7) -N -> A operand; X0 -> hi/lo B blocks.  Twelve 16-column groups of token t: groups 0..5 from
+                // the state lanes, 6..11 from their copy in the output lanes.  The output lanes then clear their
+                // rows of the A operand and of TMEM columns TM_U .. TM_U + 127 (each thread only columns that it
+                // has read itself, or that nobody reads), so that [U ; Ctil S] starts from [Util ; 0].
                 {
                     const int t = trow & 63;
                     const int gb = (state_row ? 0 : 6) + 3 * wh;
@@ -784,79 +846,45 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         tmem_ld16(tl + TM_NX + 16 * g, v);
                         tmem_wait_ld();
                         if (g < 4) {
+#pragma unroll
+                            for (int c = 0; c < 16; c++) v[c] = -v[c];
                             st_plain16(X + X_NA, t, g, v);
-                            st_plain16(X + X_NXH, t, g, v);
                         } else {
                             const int xg = g - 4;
                             const uint32_t blk = (uint32_t)(xg >> 2) * 8192u;
-                            st_split16(X + X_NXH + 8192 + blk, X + X_NXL + blk, t, xg & 3, v);
+                            st_split16(X + X_X0H + blk, X + X_X0L + blk, t, xg & 3, v);
                         }
+                    }
+                    if (!state_row) {
+#pragma unroll
+                        for (int q = 0; q < 4; q++) zero_chunk(X + X_NA, trow, 4 * wh + q);
+                        float zz[16];
+#pragma unroll
+                        for (int c = 0; c < 16; c++) zz[c] = 0.f;
+                        // half 0 read X0 groups 2..4 (columns TM_U + 32 .. + 79), half 1 groups 5..7
+                        if (wh == 0) {
+#pragma unroll
+                            for (int xg = 0; xg < 5; xg++) tmem_st16(tl + TM_U + 16 * xg, zz);
+                        } else {
+#pragma unroll
+                            for (int xg = 5; xg < 8; xg++) tmem_st16(tl + TM_U + 16 * xg, zz);
+                        }
+                        tmem_wait_st();
                     }
                 }
                 smem_to_tc();
 
-                // (8) [N^2 | N X0] = N [N | X0]
+                // (8) [Util | W] = X0 - N X0, accumulated onto X0 (exact in TMEM)
                 if (r == 0) {
                     const uint32_t x0 = smem_u32(X);
-                    mma_k64(tbase + TM_N2X, x0 + X_NA, x0 + X_NXH, true, idesc_bf16(128, 192, false, true), false);
-                    mma_k64(tbase + TM_N2X + 64, x0 + X_NA, x0 + X_NXL, true, idesc_bf16(128, 128, false, true), true);
-                    mma_commit(&S.mma);
-                }
-                if (!mma_wait_all()) break;
-
-                // (9) N^2 -> A operand; Z = X0 - N X0 -> hi/lo B blocks and, exactly, TMEM (Util | W)
-                if (state_row) {
-                    const int t = trow;
-                    auto zgroup = [&](int xg) {   // Z columns 16 xg .. 16 xg + 15 (two TMEM loads)
-                        float x0v[16], nx[16];
-                        tmem_ld16(tl + TM_NX + 64 + 16 * xg, x0v);
-                        tmem_ld16(tl + TM_N2X + 64 + 16 * xg, nx);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 16; c++) x0v[c] -= nx[c];
-                        const uint32_t blk = (uint32_t)(xg >> 2) * 8192u;
-                        st_split16(X + X_ZH + blk, X + X_ZL + blk, t, xg & 3, x0v);
-                        tmem_st16(tl + (xg < 4 ? TM_U + 16 * xg : TM_W + 16 * (xg - 4)), x0v);
-                    };
-                    // ten TMEM loads per column half: N^2 (4 groups, one load each) and Z groups 0..2, or Z 3..7
-                    if (wh == 0) {
-#pragma unroll
-                        for (int g = 0; g < 4; g++) {
-                            float v[16];
-                            tmem_ld16(tl + TM_N2X + 16 * g, v);
-                            tmem_wait_ld();
-                            st_plain16(X + X_N2A, t, g, v);
-                        }
-#pragma unroll
-                        for (int xg = 0; xg < 3; xg++) zgroup(xg);
-                    } else {
-#pragma unroll
-                        for (int xg = 3; xg < 8; xg++) zgroup(xg);
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; q++) zero_chunk(X + X_N2A, trow, 4 * wh + q);
-                    float zz[16];
-#pragma unroll
-                    for (int c = 0; c < 16; c++) zz[c] = 0.f;
-#pragma unroll
-                    for (int cg = 0; cg < 4; cg++) tmem_st16(tl + (wh == 0 ? TM_W : TM_U) + 16 * cg, zz);
-                }
-                tmem_wait_st();
-                smem_to_tc();
-
-                // (10) Util += N^2 ZV,  W += N^2 ZW
-                if (r == 0) {
-                    const uint32_t x0 = smem_u32(X);
-                    const uint32_t id = idesc_bf16(128, 64, false, true);
-                    mma_k64(tbase + TM_U, x0 + X_N2A, x0 + X_ZH, true, id, true);
-                    mma_k64(tbase + TM_U, x0 + X_N2A, x0 + X_ZL, true, id, true);
-                    mma_k64(tbase + TM_W, x0 + X_N2A, x0 + X_ZH + 8192, true, id, true);
-                    mma_k64(tbase + TM_W, x0 + X_N2A, x0 + X_ZL + 8192, true, id, true);
+                    const uint32_t id = idesc_bf16(128, 128, false, true);
+                    mma_k64(tbase + TM_U, x0 + X_NA, x0 + X_X0H, true, id, true);
+                    mma_k64(tbase + TM_U, x0 + X_NA, x0 + X_X0L, true, id, true);
                     mma_commit(&S.mma);
                 }
                 // (11) CW = [-W ; Ctil]: the Ctil rows (output lanes) while the products run
-                static_assert(X_CW >= X_ZL + 16384 && X_CW + 16384 <= X_BYTES, "CW clear of the phase-4 operands");
+                static_assert(X_CW >= X_X0L + 16384 && X_CW + 16384 <= X_BYTES, "CW clear of the phase-3 operands");
+                static_assert(X_E32 + 2 * 16 * kBS * 4 <= X_CW + 16384, "fp32 staging inside the operand region");
                 if (!state_row) {
                     const int t = trow - 64;
                     const float Gt = Gc[t];
