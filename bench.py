@@ -140,7 +140,8 @@ def fwd_kernel_name(w):
     """The kernel gdn_fwd launches for workload w (one launch per call)."""
     if w.T <= 8:
         return "decode_kernel (one launch)"
-    if w.dtype == "bf16" and w.dk <= 64:
+    serial_first = w.mode == "delta" and w.dk <= 32 and w.dv <= 32 and w.B * w.H > 2 * 152
+    if w.dtype == "bf16" and w.dk <= 64 and not serial_first:
         return f"fwd_tc_kernel<{w.mode}> (one launch)"
     return f"serial_fwd_kernel<{w.dtype}, {w.mode}> (one launch)"
 

@@ -54,7 +54,8 @@ struct WsLayout {
     size_t total = 0;
 };
 
-constexpr long kSplitSMs = 152;                // a forward is split in time only while B*H*P <= this
+constexpr long kSplitSMs = 152;                // a forward is split in time only while B*H*P <= this (also
+                                               // the wave size of the one-CTA-per-SM tensor-core forward)
 constexpr int kSplitMinTokens = 512;           // and every segment keeps at least this many tokens
 constexpr int kSerialBlock = 32;               // tokens per backward block
 constexpr int kSerialSnap = 8;                 // tokens between backward state snapshots

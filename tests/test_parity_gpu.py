@@ -24,7 +24,8 @@ def cached_inputs(w):
 
 
 def oracle_fwd(w, x):
-    return oracle.gdn_fwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], mode=w.mode)
+    return oracle.gdn_fwd_opts(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], mode=w.mode,
+                               gate_logits=w.gate_logits, norm_bc=w.norm_bc)
 
 
 def check_fwd(w, x=None, want_hT=True):
@@ -174,6 +175,33 @@ def test_shape_40_heads_d32_fwd_bwd():
     w = base.with_(name="delta_bf16_2x40x4096x32", B=2, backward=True)
     check_fwd(w)
     check_bwd(w, units=[0, 17, 39])
+
+
+@pytest.mark.parametrize("mode,opts", [("delta", {}), ("delta", {"norm_bc": True, "gate_logits": True}),
+                                       ("gated", {})])
+@pytest.mark.parametrize("B,H,T,dk,dv", [(8, 40, 300, 32, 32), (4, 80, 150, 24, 16)])
+def test_fwd_narrow_many_heads(mode, opts, B, H, T, dk, dv):
+    """More than 304 (batch, head) units of heads at most 32 wide: delta takes the token-serial forward in bf16
+    (several CTAs per SM beat three waves of the one-CTA-per-SM tensor-core kernel), gated stays on the tensor
+    cores; both against the oracle on every unit."""
+    w = I.custom(name=f"narrow_{mode}_{B}x{H}x{T}x{dk}x{dv}", mode=mode, dtype="bf16", B=B, H=H, T=T, dk=dk, dv=dv,
+                 seed=B + H + dk, h0_std=0.3, **opts)
+    check_fwd(w)
+
+
+def test_fwd_40_heads_full_size_sampled():
+    """The 8 x 40 x 4096 x 32 delta forward at full size (the token-serial path), three (batch, head) units against
+    the oracle run on those units alone."""
+    w = I.WORKLOADS["delta_bf16_8x40x4096x32"]
+    x = cached_inputs(w)
+    o, hT = run_fwd(w, x)
+    for bb, hh in ((0, 0), (3, 17), (7, 39)):
+        xs = {k: (None if x[k] is None else x[k][bb:bb + 1, :, hh:hh + 1] if k in ("v", "b", "c", "g", "beta")
+                  else x[k][hh:hh + 1] if k == "A_log" else x[k][bb:bb + 1, hh:hh + 1] if k == "h0" else x[k])
+              for k in ("v", "b", "c", "g", "beta", "A_log", "h0")}
+        ro, rhT = oracle.gdn_fwd(xs["v"], xs["b"], xs["c"], xs["g"], xs["beta"], xs["A_log"], xs["h0"], mode="delta")
+        assert_close(o[bb:bb + 1, :, hh:hh + 1], ro, TOL["bf16"], f"o unit ({bb}, {hh})")
+        assert_close(hT[bb:bb + 1, hh:hh + 1], rhT, TOL["bf16"], f"hT unit ({bb}, {hh})")
 
 
 @pytest.mark.parametrize("mode", ["gated", "delta"])
