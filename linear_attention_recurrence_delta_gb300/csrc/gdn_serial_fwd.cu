@@ -180,11 +180,28 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
     IO* o = (IO*)a.o;
     for (int n = 0; n < nblk; n++) {
         const int t0 = n * kTB, nt = min(kTB, T - t0);
+        // the next token's row vectors load while this one computes (they do not depend on the state)
+        float2 avn[8], bvn[8], cvn[8];
+        ld_rows16(&s.A[0][20 * ig], avn);
+        ld_rows16(&s.Bv[0][20 * ig], bvn);
+        ld_rows16(&s.Cv[0][20 * ig], cvn);
+        float vn = s.V[0][cl], betn = s.beta[0];
 #pragma unroll 4
         for (int tt = 0; tt < nt; tt++) {
-            float2 av[8], bv[8];
-            ld_rows16(&s.A[tt][20 * ig], av);
-            ld_rows16(&s.Bv[tt][20 * ig], bv);
+            float2 av[8], bv[8], cv[8];
+#pragma unroll
+            for (int p = 0; p < 8; p++) {
+                av[p] = avn[p];
+                bv[p] = bvn[p];
+                cv[p] = cvn[p];
+            }
+            const float vt = vn, bet = betn;
+            const int tn = tt + 1 < nt ? tt + 1 : tt;
+            ld_rows16(&s.A[tn][20 * ig], avn);
+            ld_rows16(&s.Bv[tn][20 * ig], bvn);
+            ld_rows16(&s.Cv[tn][20 * ig], cvn);
+            vn = s.V[tn][cl];
+            betn = s.beta[tn];
             float2 hp[8];
 #pragma unroll
             for (int p = 0; p < 8; p++) hp[p] = mul2(h[p], av[p]);
@@ -193,15 +210,13 @@ __global__ void __launch_bounds__(128) serial_fwd_kernel(Args a, bool vec)
                 float r = dot8x2(hp, bv);
 #pragma unroll
                 for (int o = 1; o < LPC; o <<= 1) r += __shfl_xor_sync(kFull, r, o);
-                x = s.beta[tt] * (s.V[tt][cl] - r);
+                x = bet * (vt - r);
             } else {
-                x = s.V[tt][cl];
+                x = vt;
             }
             const float2 xx = f2(x, x);
 #pragma unroll
             for (int p = 0; p < 8; p++) h[p] = fma2(bv[p], xx, hp[p]);
-            float2 cv[8];
-            ld_rows16(&s.Cv[tt][20 * ig], cv);
             float ov = dot8x2(h, cv);
 #pragma unroll
             for (int o = 1; o < LPC; o <<= 1) ov += __shfl_xor_sync(kFull, ov, o);
