@@ -469,17 +469,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                             for (int e = 0; e < 8; e++) { y[e] = ax[e] * kk[e]; z[e] = bbx[e] * kk[e]; }
                             st_row8_f16(X + X_A1, t, q, y);
-                            if (DELTA) st_row8_f16(X + X_A1, 64 + t, q, z);
+                            st_row8_f16(X + X_A1, 64 + t, q, *(DELTA ? &z : &y));
                         }
                         if (upper) {
                             ld_f8(ktab(sm, K_A2, k8) + 8 * q, kk);
 #pragma unroll
                             for (int e = 0; e < 8; e++) { y[e] = ax[e] * kk[e]; z[e] = bbx[e] * kk[e]; }
                             st_row8_f16(X + X_A2, t, q, y);
-                            if (DELTA) st_row8_f16(X + X_A2, 64 + t, q, z);
+                            st_row8_f16(X + X_A2, 64 + t, q, *(DELTA ? &z : &y));
                         }
                         st_row8_split(X + X_A3, X + X_A3L, t, q, ax);
-                        if (DELTA) st_row8_split(X + X_A3, X + X_A3L, 64 + t, q, bbx);
+                        st_row8_split(X + X_A3, X + X_A3L, 64 + t, q, *(DELTA ? &bbx : &ax));
                         if (I < 1) {
                             ld_f8(ktab(sm, K_B1_1, k8) + 8 * q, kk);
 #pragma unroll
@@ -528,10 +528,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (I > 0) {
                             scale8(cv, S.A2, q, Gt - GI, y); st_row8_f16(X + X_A1, t, q, y);
                             if (DELTA) { scale8(bbv, S.A2, q, Gt - GI, z); st_row8_f16(X + X_A1, 64 + t, q, z); }
+                            else st_row8_f16(X + X_A1, 64 + t, q, y);
                         }
                         if (upper) {
                             scale8(cv, S.A2, q, Gt - GJ7, y); st_row8_f16(X + X_A2, t, q, y);
                             if (DELTA) { scale8(bbv, S.A2, q, Gt - GJ7, z); st_row8_f16(X + X_A2, 64 + t, q, z); }
+                            else st_row8_f16(X + X_A2, 64 + t, q, y);
                         }
                         if (I < 1) { scale8(bv, S.A2, q, Gc[15] - Gt, y); st_row8_f16(X + X_B1a, t, q, y); }
                         if (I < 2) { scale8(bv, S.A2, q, Gc[31] - Gt, y); st_row8_f16(X + X_B1b, t, q, y); }
@@ -597,10 +599,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             if (pending >= 0) epilogue(pending), pending = -1;   // the previous chunk's, under the level products
             if (!mma_wait_all()) break;
 
-            // (4) assemble P (lanes 0..63) and M (lanes 64..127); thread = (row, 32 columns)
+            // (4) assemble P (lanes 0..63) and M (lanes 64..127); thread = (row, 32 columns).  Gated: lanes
+            // 64..127 hold a copy of P (the level operands repeat the c-side rows there), and every thread takes
+            // one 16-column group of its row
             {
-                const bool isM = q4 >= 2;
-                if (!isM || DELTA) {
+                const bool isM = DELTA && q4 >= 2;
+                {
                     const int t = trow & 63, wl = q4 & 1, tb = t >> 4;
                     float ew[8];
                     if (unsafe) {
@@ -627,12 +631,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     const int Ia = 2 * wl, Ib = 2 * wl + 1;
                     const uint32_t colA = wl == 0 ? 0u : TM_D1b, colB = wl == 0 ? TM_D1a : TM_D1c;
                     float* M32 = reinterpret_cast<float*>(X + X_M32);
-                    // gated: column groups wh and wh + 2, interleaved over the two halves, because the causal
-                    // zeros sit in the high groups of the low rows (a half of groups {0, 1} or {2, 3} does 8 or 0
-                    // TMEM loads, these at most 7); measured faster for gated, not for delta
+                    // gated: the four threads of a row (two lane halves x two column halves) take one group each,
+                    // so that the TMEM loads of the lower triangle (rows 0..31: 3, 2, 0, 0 per group; rows 32..63:
+                    // 4, 4, 3, 2) come to at most 7 per scheduler instead of 13
+                    const int lo = q4 >> 1;
 #pragma unroll
-                    for (int cc = 0; cc < 2; cc++) {
-                        const int cg = DELTA ? 2 * wh + cc : wh + 2 * cc;
+                    for (int cc = 0; cc < (DELTA ? 2 : 1); cc++) {
+                        const int cg = DELTA ? 2 * wh + cc : (wh ? (wl ? 3 - lo : 2 + lo) : lo);
                         float out[16];
                         if (16 * cg > 32 * wl + 31) {
 #pragma unroll
