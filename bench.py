@@ -55,7 +55,7 @@ def load_peaks():
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one forward launch, from an ncu capture of the
 # kernel as it stands (profiles/fwd_tc_delta_8x16x4096x64.md); a workload without a capture reports null.
 MEASURED_TRAFFIC = {
-    "delta_bf16_8x16x4096x64": 203568128 + 44328704,
+    "delta_bf16_8x16x4096x64": 203568384 + 43997440,
 }
 
 
