@@ -75,18 +75,16 @@ def io_bytes(w, backward=False):
     return rd + wr + 2 * state + 2 * w.H * w.dk * 4
 
 
+def plan(w, backward):
+    """The library's own answer (gdn_plan) for workload w: time segments and forward kernel."""
+    import linear_attention_recurrence_delta_gb300 as gdn
+    s = gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.mode, w.dtype, gate_logits=w.gate_logits, norm_bc=w.norm_bc)
+    return gdn.gdn_plan(s, backward)
+
+
 def tsplit_factor(w, backward):
-    """Segments of the library's time split for workload w (1 = none); mirrors the rule in
-    csrc/gdn_tsplit.cu: heads at most 64 wide, B*H*P <= 152 SMs, T divisible by P, >= 512 tokens per
-    segment, P >= 4 for a delta forward, >= 3 for a gated one and >= 2 for a backward."""
-    if w.dk > 64 or w.dv > 64:
-        return 1
-    units = w.B * w.H
-    min_p = 2 if backward else (4 if w.mode == "delta" else 3)
-    for p in range(152 // units, min_p - 1, -1):
-        if w.T % p == 0 and w.T // p >= 512:
-            return p
-    return 1
+    """Segments of the library's time split for workload w (1 = none)."""
+    return plan(w, backward).segments
 
 
 def fwd_launches(w):
@@ -108,8 +106,10 @@ def bwd_launches(w):
         # backward, the slabs' partial sums of db, dc, dg (, dbeta) if several, dA_log reduction
         sums = (4 if w.mode == "delta" else 3) if bwd_slabs(w) > 1 else 0
         return 2 + sums
-    states = 4 if w.mode == "delta" else 2
-    return states + 2 + 1 + 2               # state passes, backward x2 (+ reductions), reverse scan
+    P = tsplit_factor(w, True)
+    states = 4 if w.mode == "delta" else 2  # zero-start run, (identity, transition run), scan
+    runs = -(-(w.T // P) // 512)            # G_p by runs of 512 tokens, their partials summed if several
+    return states + 1 + (1 if runs > 1 else 0) + 1 + 2   # G_p (+ sum), reverse scan, backward + dA_log sum
 
 
 def tc_fwd_ex2_per_launch(w):
@@ -117,7 +117,7 @@ def tc_fwd_ex2_per_launch(w):
     per chunk and head, the anchors exp(A (G_t - G_r)) and their inverses (2 per token and channel: 2 * 64 * 64),
     the per-(8-block, reference) constant tables (42 of the 64 (table, 8-block) pairs are live, per channel:
     42 * 64) and the chunk's decay row (64).  None for the other kernels."""
-    if w.T <= 8 or w.dtype != "bf16" or w.dk > 64 or tsplit_factor(w, False) > 1:
+    if plan(w, False).fwd_kernel != 2 or tsplit_factor(w, False) > 1:
         return None
     chunks = -(-w.T // 64) * w.B * w.H * -(-w.dv // 64)
     return chunks * (2 * 64 * 64 + 42 * 64 + 64)
@@ -137,11 +137,11 @@ def ex2_rate():
 
 
 def fwd_kernel_name(w):
-    """The kernel gdn_fwd launches for workload w (one launch per call)."""
-    if w.T <= 8:
+    """The kernel gdn_fwd launches for workload w (one launch per call), as gdn_plan reports it."""
+    k = plan(w, False).fwd_kernel
+    if k == 1:
         return "decode_kernel (one launch)"
-    serial_first = w.mode == "delta" and w.dk <= 32 and w.dv <= 32 and w.B * w.H > 2 * 152
-    if w.dtype == "bf16" and w.dk <= 64 and not serial_first:
+    if k == 2:
         return f"fwd_tc_kernel<{w.mode}> (one launch)"
     return f"serial_fwd_kernel<{w.dtype}, {w.mode}> (one launch)"
 

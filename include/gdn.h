@@ -121,6 +121,34 @@ typedef struct {
  * at least 256 (the device status word lives in the first bytes). */
 size_t gdn_workspace_bytes(const gdn_shape_t* shape, int backward);
 
+/* How the library runs a shape.  Host only: it touches no device and is
+ * answered from the shape alone, by the rules the calls themselves follow.
+ *   segments    gdn_fwd (backward = 0) or gdn_bwd (backward = 1) cuts the
+ *               sequence into this many equal segments that run side by side
+ *               (the state a segment passes on is an affine map of the state
+ *               it receives, "GDN & MLA Mechanism Deep-Dive", Step 5: chunked
+ *               recurrence; a scan over the segments joins them); 1 = no
+ *               split.  Long sequences over few heads are split.
+ *   fwd_kernel  the kernel of the forward runs the call makes (gdn_kernel_t):
+ *               gdn_fwd's own runs; gdn_bwd's forward runs over the segments
+ *               under a split, GDN_KERNEL_NONE without one (the serial
+ *               backward recomputes the forward itself).  Also NONE for T = 0.
+ * Returns GDN_OK, or the error the call would return for the shape alone
+ * (GDN_ERR_NULL, GDN_ERR_MODE, GDN_ERR_SHAPE). */
+typedef enum {
+    GDN_KERNEL_NONE = 0,
+    GDN_KERNEL_DECODE = 1,        /* T <= 8: state-streaming decode kernel      */
+    GDN_KERNEL_TENSOR_CORE = 2,   /* chunked tcgen05 forward (bf16, d_k <= 64)  */
+    GDN_KERNEL_SERIAL = 3         /* token-serial forward on the CUDA cores     */
+} gdn_kernel_t;
+
+typedef struct {
+    int segments;
+    int fwd_kernel;   /* gdn_kernel_t */
+} gdn_plan_t;
+
+gdn_status_t gdn_plan(const gdn_shape_t* shape, int backward, gdn_plan_t* plan);
+
 /* Forward pass.  Reads v, b, c, g, beta (NULL iff mode == GDN_GATED), A_log,
  * h0 (NULL => zero initial state); writes o and hT (NULL => not written).
  * hT may be the same buffer as h0: the state is then updated in place, as in

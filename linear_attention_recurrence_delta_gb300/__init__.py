@@ -23,6 +23,8 @@ GDN_NORM_BC = 0x200          # option bit: b and c arrive before their L2 normal
 GDN_CHECK_FINITE = 0x400     # option bit: scan the outputs for NaN / Inf (status GDN_ERR_NONFINITE)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_OK = 0
+GDN_KERNEL_NONE, GDN_KERNEL_DECODE, GDN_KERNEL_TENSOR_CORE, GDN_KERNEL_SERIAL = 0, 1, 2, 3
+KERNEL_NAMES = {0: "none", 1: "decode", 2: "tensor_core", 3: "serial"}
 STATUS_NAMES = {
     0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_ALIGN", 4: "GDN_ERR_MODE",
     5: "GDN_ERR_WORKSPACE", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_DEVICE",
@@ -50,6 +52,10 @@ class gdn_shape_t(ctypes.Structure):
                 f"mode={self.mode}, io={self.io})")
 
 
+class gdn_plan_t(ctypes.Structure):
+    _fields_ = [("segments", ctypes.c_int), ("fwd_kernel", ctypes.c_int)]
+
+
 def make_shape(B, H, T, dk, dv, mode="gated", io="bf16", gate_logits=False, norm_bc=False,
                check_finite=False) -> gdn_shape_t:
     m = {"gated": GDN_GATED, "delta": GDN_DELTA}.get(mode, mode)
@@ -75,6 +81,8 @@ def load(path: str | None = None):
             vp, sz, sp = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(gdn_shape_t)
             lib.gdn_workspace_bytes.argtypes = [sp, ctypes.c_int]
             lib.gdn_workspace_bytes.restype = sz
+            lib.gdn_plan.argtypes = [sp, ctypes.c_int, ctypes.POINTER(gdn_plan_t)]
+            lib.gdn_plan.restype = ctypes.c_int
             lib.gdn_fwd.argtypes = [sp] + [vp] * 9 + [vp, sz, vp]
             lib.gdn_fwd.restype = ctypes.c_int
             lib.gdn_bwd.argtypes = [sp] + [vp] * 16 + [vp, sz, vp]
@@ -112,6 +120,13 @@ def _stream(stream):
 
 def gdn_workspace_bytes(shape: gdn_shape_t, backward: int) -> int:
     return int(load().gdn_workspace_bytes(ctypes.byref(shape), int(backward)))
+
+
+def gdn_plan(shape: gdn_shape_t, backward: int) -> gdn_plan_t:
+    """How the library runs the shape (host only): time segments and forward kernel; raises GdnError."""
+    plan = gdn_plan_t()
+    check(int(load().gdn_plan(ctypes.byref(shape), int(backward), ctypes.byref(plan))), "gdn_plan")
+    return plan
 
 
 def gdn_fwd(shape, v, b, c, g, beta, A_log, h0, o, hT, ws, ws_bytes=None, stream=None) -> int:

@@ -176,6 +176,15 @@ static bool serial_first(const Args& a)
     return a.mode == GDN_DELTA && a.dk <= 32 && a.dv <= 32 && (long)a.B * a.H > 2 * kSplitSMs;
 }
 
+// the kernel fwd_core launches for a (view) shape
+static gdn_kernel_t fwd_kernel_of(const Args& a)
+{
+    if (a.T <= 0) return GDN_KERNEL_NONE;
+    if (a.T <= decode_max_tokens()) return GDN_KERNEL_DECODE;
+    if (a.io == GDN_BF16 && !serial_first(a) && a.dk <= 64) return GDN_KERNEL_TENSOR_CORE;
+    return GDN_KERNEL_SERIAL;
+}
+
 static cudaError_t fwd_core(const Args& a, cudaStream_t st)
 {
     if (a.T <= decode_max_tokens()) return launch_decode(a, st);
@@ -190,6 +199,24 @@ static cudaError_t fwd_core(const Args& a, cudaStream_t st)
 }  // namespace gdn
 
 using namespace gdn;
+
+extern "C" gdn_status_t gdn_plan(const gdn_shape_t* shape_in, int backward, gdn_plan_t* plan)
+{
+    gdn_shape_t sh;
+    int logits = 0, norm = 0;
+    if (!shape_in || !plan) return GDN_ERR_NULL;
+    if (!split_mode(shape_in, &sh, &logits, &norm)) return GDN_ERR_MODE;
+    if ((sh.mode != GDN_GATED && sh.mode != GDN_DELTA) || (sh.io != GDN_F32 && sh.io != GDN_BF16))
+        return GDN_ERR_MODE;
+    if (!shape_ok(sh)) return GDN_ERR_SHAPE;
+    const int P = sh.T > 0 ? tsplit_factor(sh, backward ? 1 : 0) : 1;
+    Args a = make_args(&sh);   // the runs' view: P segments of one sequence are P batch rows
+    a.B = sh.B * P;
+    a.T = sh.T / P;
+    plan->segments = P;
+    plan->fwd_kernel = (backward && P == 1) ? GDN_KERNEL_NONE : fwd_kernel_of(a);
+    return GDN_OK;
+}
 
 extern "C" size_t gdn_workspace_bytes(const gdn_shape_t* shape_in, int backward)
 {

@@ -189,3 +189,41 @@ def test_check_finite_option_bit():
     for bwd in (0, 1):
         assert gdn.gdn_workspace_bytes(chk, bwd) == gdn.gdn_workspace_bytes(plain, bwd) > 0
     assert gdn.gdn_status_string(9).startswith("GDN_ERR_NONFINITE")
+
+
+def test_plan_reports_split_and_kernel():
+    """gdn_plan answers from the shape alone, by the rules the calls dispatch with: the time split for long
+    sequences over few heads (forward at least 4 segments in delta mode, 3 in gated mode, backward at least 2),
+    the decode kernel up to 8 tokens, the tensor-core forward for bf16 keys up to 64 wide except delta heads up to
+    32 wide over more than 304 units, the token-serial forward otherwise."""
+    K = gdn
+
+    def plan(*a, bw=0, **kw):
+        p = gdn.gdn_plan(gdn.make_shape(*a, **kw), bw)
+        return p.segments, p.fwd_kernel
+
+    assert plan(1, 16, 32768, 64, 64, "delta", "bf16") == (8, K.GDN_KERNEL_TENSOR_CORE)
+    assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=1) == (8, K.GDN_KERNEL_TENSOR_CORE)
+    assert plan(8, 16, 4096, 64, 64, "delta", "bf16") == (1, K.GDN_KERNEL_TENSOR_CORE)
+    assert plan(8, 16, 4096, 64, 64, "delta", "bf16", bw=1) == (1, K.GDN_KERNEL_NONE)
+    assert plan(1, 40, 1024, 32, 32, "delta", "f32") == (1, K.GDN_KERNEL_SERIAL)   # 152 / 40: 3 < 4 segments
+    assert plan(1, 40, 1024, 32, 32, "delta", "f32", bw=1) == (2, K.GDN_KERNEL_SERIAL)
+    assert plan(8, 40, 4096, 32, 32, "delta", "bf16") == (1, K.GDN_KERNEL_SERIAL)
+    assert plan(8, 40, 4096, 32, 32, "gated", "bf16") == (1, K.GDN_KERNEL_TENSOR_CORE)
+    assert plan(4, 40, 4096, 32, 32, "delta", "bf16") == (1, K.GDN_KERNEL_TENSOR_CORE)  # 160 units
+    assert plan(512, 16, 1, 64, 64, "delta", "bf16") == (1, K.GDN_KERNEL_DECODE)
+    assert plan(8, 16, 4096, 128, 128, "delta", "bf16") == (1, K.GDN_KERNEL_SERIAL)
+    assert plan(1, 16, 0, 64, 64, "gated", "bf16") == (1, K.GDN_KERNEL_NONE)
+    assert plan(1, 4, 3000, 64, 64, "gated", "bf16", gate_logits=True) == (5, K.GDN_KERNEL_TENSOR_CORE)
+    # a split forward is exactly one whose workspace holds more than the 256-byte status word
+    for a in [(1, 16, 32768, 64, 64, "delta", "bf16"), (1, 16, 32768, 64, 64, "gated", "bf16"),
+              (2, 3, 3072, 56, 56, "gated", "bf16"), (1, 16, 1000, 64, 64, "delta", "bf16"),
+              (8, 16, 4096, 64, 64, "delta", "bf16"), (1, 2, 4096, 128, 128, "delta", "bf16")]:
+        s = gdn.make_shape(*a)
+        assert (gdn.gdn_plan(s, 0).segments > 1) == (gdn.gdn_workspace_bytes(s, 0) > 256), a
+    # the errors the calls return for the shape alone
+    for bad, status in [(gdn.make_shape(1, 1, 10, 12, 8, "delta", "bf16"), 2),
+                        (gdn.make_shape(1, 1, 10, 8, 8, gdn.GDN_DELTA | 0x800, "bf16"), 4)]:
+        with pytest.raises(gdn.GdnError) as e:
+            gdn.gdn_plan(bad, 0)
+        assert e.value.status == status
