@@ -37,9 +37,13 @@
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
+#include "serial_common.cuh"
 
 namespace gdn {
 namespace {
+
+using rec::cp_async16;
+using rec::cp_async_commit;
 
 // identity d_k x d_k states for the transition runs
 __global__ void eye_kernel(float* I, size_t n_units, int dk)
@@ -66,11 +70,6 @@ struct OutSmem {
     float oz[2][kOutTile][64];
 };
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
-{
-    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
-}
 
 template <typename IO, bool DELTA>
 __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const float* so, const IO* c, const IO* g,
@@ -129,7 +128,7 @@ __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const 
                 else *reinterpret_cast<float4*>(qd) = z4;
             }
         }
-        asm volatile("cp.async.commit_group;\n" ::: "memory");
+        cp_async_commit();
     };
     if (quads) stage_async(run0, 0);
 
@@ -140,7 +139,7 @@ __global__ void __launch_bounds__(256) tsplit_out_kernel(const float* o0, const 
         __syncthreads();   // the previous sub-tile's rows are consumed: its buffer takes the next sub-tile's
         if (quads) {
             if (t0 + kOutTile < run_end) stage_async(t0 + kOutTile, sb ^ 1);
-            else asm volatile("cp.async.commit_group;\n" ::: "memory");
+            else cp_async_commit();
         }
         if (!DELTA && w == 0) {   // inclusive scan of the sub-tile's gates (two per lane) on top of `base`
             const float ga = 2 * lane < nt ? gate_at(t0 + 2 * lane) : 0.f;
@@ -294,7 +293,7 @@ __global__ void __launch_bounds__(256) tsplit_gp_kernel(const float* so, const I
             const int tt = idx / (64 / E), ce = E * (idx % (64 / E));
             if (tt < nt && ce < dv) cp_async16(dd + tt * 64 + ce, dO + row(t0 + tt) * dv + ce);
         }
-        asm volatile("cp.async.commit_group;\n" ::: "memory");
+        cp_async_commit();
     };
     if (pieces) stage_async(run0, 0);
 
@@ -308,7 +307,7 @@ __global__ void __launch_bounds__(256) tsplit_gp_kernel(const float* so, const I
         __syncthreads();   // the previous sub-tile is consumed: its buffer takes the next one
         if (pieces) {
             if (t0 + kOutTile < run_end) stage_async(t0 + kOutTile, sb ^ 1);
-            else asm volatile("cp.async.commit_group;\n" ::: "memory");
+            else cp_async_commit();
         } else {
             IO* dw = reinterpret_cast<IO*>(&sm.d[sb][0][0]);
             for (int idx = tid; idx < kOutTile * 64; idx += 256) {
