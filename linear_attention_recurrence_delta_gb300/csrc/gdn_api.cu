@@ -176,7 +176,7 @@ static bool serial_first(const Args& a)
     return a.mode == GDN_DELTA && a.dk <= 32 && a.dv <= 32 && (long)a.B * a.H > 2 * kSplitSMs;
 }
 
-// the kernel fwd_core launches for a (view) shape
+// the forward kernel for a (view) shape: fwd_core dispatches on it and gdn_plan reports it
 static gdn_kernel_t fwd_kernel_of(const Args& a)
 {
     if (a.T <= 0) return GDN_KERNEL_NONE;
@@ -185,15 +185,20 @@ static gdn_kernel_t fwd_kernel_of(const Args& a)
     return GDN_KERNEL_SERIAL;
 }
 
+// the one place that picks a forward kernel; gdn_plan reports the same choice
 static cudaError_t fwd_core(const Args& a, cudaStream_t st)
 {
-    if (a.T <= decode_max_tokens()) return launch_decode(a, st);
-    bool handled = false;
-    if (a.io == GDN_BF16 && !serial_first(a)) {
+    switch (fwd_kernel_of(a)) {
+    case GDN_KERNEL_DECODE:
+        return launch_decode(a, st);
+    case GDN_KERNEL_TENSOR_CORE: {
+        bool handled = false;
         const cudaError_t e = launch_fwd_tc(a, st, &handled);
-        if (e != cudaSuccess) return e;
+        return (e != cudaSuccess || handled) ? e : cudaErrorInvalidValue;   // the kernel refused a shape it takes
     }
-    return handled ? cudaSuccess : launch_serial_fwd(a, st);
+    default:
+        return launch_serial_fwd(a, st);
+    }
 }
 
 }  // namespace gdn
