@@ -330,3 +330,51 @@ def test_norm_bc_finite_differences(mode, logits):
             fd = (loss(**{arg: p.reshape(z.shape)}) - loss(**{arg: m.reshape(z.shape)})) / (2 * eps)
             an = gr[name].reshape(-1)[k]
             assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (name, k, fd, an)
+
+
+# ---------------------------------------------------------------------------
+# the affine segment map behind the time split ("GDN & MLA Mechanism Deep-Dive", Step 5: the state is carried
+# from chunk to chunk by a closed-form map of the state entering it)
+# ---------------------------------------------------------------------------
+
+def _transition_run(x, mode):
+    """The same tokens with v = 0 from the identity state: (q_t = Phi_t^T c_t, Phi_T)."""
+    B, T, H, dk = x["b"].shape
+    eye = np.broadcast_to(np.eye(dk), (B, H, dk, dk)).copy()
+    return oracle.gdn_fwd(np.zeros((B, T, H, dk)), x["b"], x["c"], x["g"], x["beta"], x["A_log"], eye, mode=mode)
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+def test_segment_map_is_affine(mode):
+    """From h0 the state after the tokens is Phi_T h0 + H and every output is o0_t + h0^T q_t, where (o0, H) is
+    the run from a zero state and (q, Phi_T) the run with v = 0 from the identity; in gated mode Phi_T is
+    diag(exp(A sum_t g_t)) and q_t = c_t (.) exp(A G_t).  Non-square states (d_k = 4, d_v = 5) catch a
+    transposed operand."""
+    x = draw(mode, B=2, H=2, T=37, dk=4, dv=5, h0_std=0.7)
+    o, hT = oracle.gdn_fwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], mode=mode)
+    o0, Hs = oracle.gdn_fwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], None, mode=mode)
+    q, Phi = _transition_run(x, mode)
+    np.testing.assert_allclose(hT, Phi @ x["h0"] + Hs, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o, o0 + np.einsum("bhkv,bthk->bthv", x["h0"], q), rtol=0, atol=1e-12)
+    if mode == "gated":
+        A = A_of(x)                                              # [H, d_k]
+        G = np.cumsum(x["g"], axis=1)                            # [B, T, H]
+        np.testing.assert_allclose(Phi, np.einsum("bhk,kl->bhkl", np.exp(A[None] * G[:, -1, :, None]),
+                                                  np.eye(4)), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(q, x["c"] * np.exp(A[None, None] * G[..., None]), rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+def test_entering_state_adjoint(mode):
+    """The adjoint of the entering state is sum_t q_t do_t^T + Phi_T^T dh_T (q_t = Phi_t^T c_t as above): with
+    no end gradient this is the segment adjoint G_p of the split backward, and the second term is the step of its
+    reverse scan over segments."""
+    x = draw(mode, B=2, H=2, T=29, dk=4, dv=5, h0_std=0.7, backward=True)
+    q, Phi = _transition_run(x, mode)
+    G = np.einsum("bthk,bthv->bhkv", q, x["dO"])
+    ref = oracle.gdn_bwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], x["dO"], None, mode=mode)
+    scale = np.abs(G).max()
+    np.testing.assert_allclose(ref["dh0"], G, rtol=0, atol=1e-12 * scale)
+    dhT = 0.5 * I.normal(77, 1, 2 * 2 * 4 * 5).reshape(2, 2, 4, 5)
+    ref2 = oracle.gdn_bwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], x["dO"], dhT, mode=mode)
+    np.testing.assert_allclose(ref2["dh0"], G + np.swapaxes(Phi, -1, -2) @ dhT, rtol=0, atol=1e-12 * scale)
