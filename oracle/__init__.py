@@ -269,3 +269,6 @@ def _logit_grads(out, g, be):
     if be is not None:
         out["dbeta"] = out["dbeta"] * be * (1.0 - be)
     return out
+
+
+from .chunked_bwd import gdn_bwd_chunked  # noqa: E402  (the chunked reverse mode, numpy)

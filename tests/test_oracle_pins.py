@@ -378,3 +378,22 @@ def test_entering_state_adjoint(mode):
     dhT = 0.5 * I.normal(77, 1, 2 * 2 * 4 * 5).reshape(2, 2, 4, 5)
     ref2 = oracle.gdn_bwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], x["dO"], dhT, mode=mode)
     np.testing.assert_allclose(ref2["dh0"], G + np.swapaxes(Phi, -1, -2) @ dhT, rtol=0, atol=1e-12 * scale)
+
+
+@pytest.mark.parametrize("mode", ["gated", "delta"])
+@pytest.mark.parametrize("T,chunk,dk,dv", [(37, 16, 4, 5), (130, 64, 8, 6), (64, 64, 5, 5), (9, 1, 3, 4)])
+def test_chunked_backward_equals_serial(mode, T, chunk, dk, dv):
+    """The reverse mode of the chunked form ("GDN & MLA Mechanism Deep-Dive", Step 5), walked chunk by chunk
+    backwards, gives the serial backward's gradients: ragged last chunks, non-square states, h0 and dh_T given,
+    and chunk = 1 (the chunked form reduces to the token recurrence)."""
+    w = I.custom(mode=mode, dtype="f32", B=2, H=2, T=T, dk=dk, dv=dv, seed=T + dk, h0_std=0.5, backward=True)
+    x = I.make_inputs(w)
+    dhT = 0.3 * I.normal(5, 1, 2 * 2 * dk * dv).reshape(2, 2, dk, dv)
+    args = (x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], x["dO"], dhT)
+    ref = oracle.gdn_bwd(*args, mode=mode)
+    got = oracle.gdn_bwd_chunked(*args, mode=mode, chunk=chunk)
+    for k in ("dv", "db", "dc", "dg", "dbeta", "dA_log", "dh0"):
+        if ref[k] is None:
+            assert got[k] is None
+            continue
+        np.testing.assert_allclose(got[k], ref[k], rtol=0, atol=1e-12 * np.abs(ref[k]).max(), err_msg=k)
