@@ -10,6 +10,22 @@ the library is missing or cannot be loaded, the first call raises.
 The operation ("GDN & MLA Mechanism Deep-Dive", Step 4 and Step 5; delta rule
 from the card "01 GDN recurrence" of "HyMo-434M -- documentation portal"),
 layouts and limits are documented in ``include/gdn.h``.
+
+A forward and backward on torch tensors (v, b, c [B, T, H, d] bf16; g, beta
+[B, T, H] bf16; A_log [H, d_k] fp32; states [B, H, d_k, d_v] fp32)::
+
+    import linear_attention_recurrence_delta_gb300 as gdn
+    s = gdn.make_shape(B, H, T, dk, dv, "delta", "bf16")          # or "gated" (beta = None)
+    ws = torch.empty(gdn.gdn_workspace_bytes(s, 1), dtype=torch.uint8, device="cuda")
+    gdn.check(gdn.gdn_fwd(s, v, b, c, g, beta, A_log, h0, o, hT, ws))
+    gdn.check(gdn.gdn_bwd(s, v, b, c, g, beta, A_log, h0, dO, dhT,
+                          dv, db, dc, dg, dbeta, dA_log, dh0, ws))
+    gdn.check(gdn.gdn_last_device_status(ws))                      # synchronises; GDN_OK or the kernels' error
+
+``h0``, ``hT``, ``dhT``, ``dh0`` may be None; ``make_shape(..., gate_logits=True,
+norm_bc=True)`` moves the gates' sigmoid and the L2 normalisation of b and c
+into the kernels, and ``gdn_plan(s, backward)`` tells which kernels a call
+will use.
 """
 from __future__ import annotations
 
