@@ -1,7 +1,8 @@
 """GB300 (sm_103a) gated delta rule: Python binding of libgdn's C ABI.
 
 The functions below carry the C names (``gdn_fwd``, ``gdn_bwd``,
-``gdn_workspace_bytes``, ``gdn_last_device_status``, ``gdn_status_string``)
+``gdn_bwd_noalloc``, ``gdn_workspace_bytes``, ``gdn_plan``,
+``gdn_last_device_status``, ``gdn_status_string``)
 and only marshal arguments: torch tensors become device pointers, ``None``
 becomes NULL, and the stream defaults to torch's current stream.  Every step
 of the computation runs in libgdn's CUDA kernels.  There is no fallback: if
