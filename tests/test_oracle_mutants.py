@@ -64,3 +64,37 @@ def test_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
         except (AssertionError, ValueError, FloatingPointError):
             caught.append(pin)
     assert caught, f"no pin caught the planted mistake {name}"
+
+
+# the chunked reverse mode (numpy) against the serial backward: each planted mistake must break the equality
+CHUNKED_SRC = os.path.join(os.path.dirname(oracle.__file__), "chunked_bwd.py")
+
+CHUNKED_MUTANTS = {
+    "no_state_decay_grad": ("    dGam[-1] += (dSn * S).sum(axis=1) * E[-1]\n", ""),
+    "bh_decay_sign": ('    dGam -= dBh * f["Bh"]\n', '    dGam += dBh * f["Bh"]\n'),
+    "solve_not_transposed": ('np.linalg.solve(f["Mmat"].T, dU)', 'np.linalg.solve(f["Mmat"], dU)'),
+    "dbeta_drop_K": (' + (dMm * f["K"]).sum(axis=1)', ''),
+    "dg_forward_cumsum": ("np.cumsum(dG[::-1])[::-1]", "np.cumsum(dG)"),
+    "dQ_strict_mask": ("dQ = (dO @ U.T) * np.tril(np.ones((L, L)))", "dQ = (dO @ U.T) * np.tril(np.ones((L, L)), -1)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CHUNKED_MUTANTS))
+def test_chunked_backward_pin_catches_planted_mistake(name, tmp_path, monkeypatch):
+    import importlib.util
+    old, new = CHUNKED_MUTANTS[name]
+    src = open(CHUNKED_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found"
+    path = tmp_path / "chunked_mutant.py"
+    path.write_text(src.replace(old, new))
+    spec = importlib.util.spec_from_file_location("chunked_mutant", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    monkeypatch.setattr(pins.oracle, "gdn_bwd_chunked", mod.gdn_bwd_chunked)
+    caught = []
+    for mode in ("gated", "delta"):
+        try:
+            pins.test_chunked_backward_equals_serial(mode, 37, 16, 4, 5)
+        except AssertionError:
+            caught.append(mode)
+    assert caught, f"no pin caught the chunked-backward mutant {name}"
