@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import linear_attention_recurrence_delta_gb300 as gdn
@@ -227,3 +228,41 @@ def test_plan_reports_split_and_kernel():
         with pytest.raises(gdn.GdnError) as e:
             gdn.gdn_plan(bad, 0)
         assert e.value.status == status
+
+
+def test_plan_and_workspace_agree_on_random_shapes():
+    """Over random shapes, valid or not: gdn_plan succeeds exactly when both workspace sizes are non-zero; a split
+    has T divisible by its segments, at least 512 tokens per segment, heads at most 64 wide and at most 152
+    (batch, head, segment) units (forward: at least 4 segments in delta mode, 3 in gated mode); a forward splits
+    exactly when its workspace holds more than the status word; the forward kernel is NONE only without tokens."""
+    rng = np.random.default_rng(7)
+    for _ in range(3000):
+        B = int(rng.choice([1, 2, 3, 8, 64, 512]))
+        H = int(rng.choice([1, 2, 4, 16, 40, 100]))
+        T = int(rng.choice([0, 1, 5, 8, 9, 100, 1024, 3000, 4096, 32768]))
+        dk = int(rng.choice([8, 16, 24, 32, 56, 64, 72, 128, 130, 12]))
+        dv = int(rng.choice([8, 16, 32, 64, 96, 128, 20]))
+        mode = str(rng.choice(["gated", "delta"]))
+        io = str(rng.choice(["bf16", "f32"]))
+        s = gdn.make_shape(B, H, T, dk, dv, mode, io)
+        w0, w1 = gdn.gdn_workspace_bytes(s, 0), gdn.gdn_workspace_bytes(s, 1)
+        for bw in (0, 1):
+            try:
+                p = gdn.gdn_plan(s, bw)
+            except gdn.GdnError:
+                assert w0 == 0 and w1 == 0, (B, H, T, dk, dv, mode, io)
+                continue
+            assert w0 > 0 and w1 > 0
+            P = p.segments
+            assert P >= 1 and (T % P == 0 if T else P == 1)
+            if P > 1:
+                assert T // P >= 512 and dk <= 64 and dv <= 64 and B * H * P <= 152
+                if not bw:
+                    assert P >= (4 if mode == "delta" else 3)
+            if not bw:
+                assert (P > 1) == (w0 > 256)
+                assert (p.fwd_kernel == gdn.GDN_KERNEL_NONE) == (T == 0)
+                if 0 < T <= 8:
+                    assert p.fwd_kernel == gdn.GDN_KERNEL_DECODE
+                if p.fwd_kernel == gdn.GDN_KERNEL_TENSOR_CORE:
+                    assert io == "bf16" and dk <= 64
