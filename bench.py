@@ -52,11 +52,49 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one forward launch, from an ncu capture of the
-# kernel as it stands (profiles/fwd_tc_delta_8x16x4096x64.md); a workload without a capture reports null.
-MEASURED_TRAFFIC = {
-    "delta_bf16_8x16x4096x64": 203568384 + 43997440,
-}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one forward launch from an ncu capture, with the
+# SHA-256 of the kernel's source files at the time of the capture.  When a source no longer matches, the counters
+# describe another kernel and the line reports traffic = null until the capture is retaken.
+MEASURED_TRAFFIC = {}
+
+
+def source_digest(files):
+    """SHA-256 over the named files of the library's csrc/ (in the order given)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "linear_attention_recurrence_delta_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(name):
+    """Captured DRAM bytes per launch for workload `name`, or None if absent or captured on other sources."""
+    rec = MEASURED_TRAFFIC.get(name)
+    if rec is None:
+        return None
+    return rec["bytes"] if source_digest(rec["files"]) == rec["sha256"] else None
+
+
+def chunk_flops(w, backward=False):
+    """Algorithmic tensor FLOPs of the chunked form over workload w (chunks of C = 64, full tiles).
+
+    Per chunk and head, the contractions of the closed form (2 * m * n * k each):
+      forward, both modes: P = (c-side) (b-side)^T        2 C^2 d_k
+                           O = Ctil S + P U              2 C d_k d_v + 2 C^2 d_v
+                           S' = Bhat^T U                 2 C d_k d_v
+      forward, delta adds: K (the b b^T scores)          2 C^2 d_k
+                           [Util | W] = (I+M)^-1 R       2 C^2 (d_v + d_k)
+                           U = Util - W S                2 C d_k d_v
+      backward: the forward's products again (recomputed) plus their transposes: every forward product
+      X = A B contributes dA = dX B^T and dB = A^T dX, i.e. twice its own FLOPs.
+    """
+    C, dk, dv = 64, w.dk, w.dv
+    f = 2 * C * C * dk + 2 * C * dk * dv + 2 * C * C * dv + 2 * C * dk * dv
+    if w.mode == "delta":
+        f += 2 * C * C * dk + 2 * C * C * (dv + dk) + 2 * C * dk * dv
+    chunks = -(-w.T // C) * w.B * w.H
+    return chunks * f * (3 if backward else 1)
 
 
 def io_bytes(w, backward=False):
@@ -124,16 +162,62 @@ def tc_fwd_ex2_per_launch(w):
 
 
 def ex2_rate():
-    """exp2 evaluations per second of the special-function units (libgdn_probe.so), or None."""
+    """exp2 evaluations per second of the special-function units, measured by bench_probes/ex2_rate.cu (built
+    here into _build/libgdn_probe.so, outside the library), or None if it cannot be built."""
     import ctypes
-    path = os.path.join(ROOT, "linear_attention_recurrence_delta_gb300", "libgdn_probe.so")
-    if not os.path.exists(path):
-        return None
+    from linear_attention_recurrence_delta_gb300 import _build
+    src = os.path.join(ROOT, "bench_probes", "ex2_rate.cu")
+    path = os.path.join(ROOT, "_build", "libgdn_probe.so")
+    if not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(src):
+        os.makedirs(os.path.dirname(path), exist_ok=True)
+        cmd = [_build.nvcc(), "-std=c++17", "-O3", "-Xcompiler", "-fPIC", *_build.ARCH, "-shared", src, "-o", path,
+               "-lcudart"]
+        if subprocess.run(cmd, capture_output=True).returncode != 0:
+            return None
     lib = ctypes.CDLL(path)
     lib.gdn_probe_ex2_rate.restype = ctypes.c_int
     lib.gdn_probe_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double)]
     r = ctypes.c_double(0.0)
     return r.value if lib.gdn_probe_ex2_rate(ctypes.byref(r)) == 0 else None
+
+
+def host_link(nbytes_in, nbytes_out, reps=5):
+    """Host link bandwidth with pinned buffers of the end-to-end step's sizes (copy engines, cudaMemcpyAsync):
+    host->device alone, device->host alone, and both directions at once; GB/s, best of `reps`."""
+    import torch
+    hi = torch.empty(nbytes_in, dtype=torch.uint8).pin_memory()
+    di = torch.empty(nbytes_in, dtype=torch.uint8, device="cuda")
+    ho = torch.empty(nbytes_out, dtype=torch.uint8).pin_memory()
+    do = torch.empty(nbytes_out, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def best(fn):
+        out = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            out.append(time.perf_counter() - t0)
+        return min(out)
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            di.copy_(hi, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            ho.copy_(do, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_in, t_out, t_both = best(h2d), best(d2h), best(both)
+    return {"h2d_gbs": nbytes_in / t_in / 1e9, "d2h_gbs": nbytes_out / t_out / 1e9,
+            "both_gbs": (nbytes_in + nbytes_out) / t_both / 1e9, "both_ms": t_both * 1e3,
+            "how": "pinned host buffers of the step's input and output bytes, cudaMemcpyAsync on two streams, "
+                   "best of %d, host wall clock around a device synchronise" % reps}
 
 
 def fwd_kernel_name(w):
@@ -144,6 +228,22 @@ def fwd_kernel_name(w):
     if k == 2:
         return f"fwd_tc_kernel<{w.mode}> (one launch)"
     return f"serial_fwd_kernel<{w.dtype}, {w.mode}> (one launch)"
+
+
+def roofline_of(nbytes, flops, ms, peaks, peak_kind):
+    """Roofline of a launch (or step) of `ms` milliseconds moving `nbytes` algorithmic bytes and doing `flops`
+    algorithmic tensor FLOPs: time = max(bytes / HBM, FLOPs / bf16 dense peak); the bound is the larger term."""
+    hbm_ms = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+    flop_ms = flops / (peaks["bf16_tflops"] * 1e12) * 1e3
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    r = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+         "frac": achieved / peaks["hbm_gbs"], "peak_kind": peak_kind, "bytes_per_launch": nbytes,
+         "launch_ms": ms, "hbm_floor_ms": hbm_ms, "flops_per_launch": flops, "flop_floor_ms": flop_ms,
+         "tensor_frac": flops / (ms * 1e-3) / (peaks["bf16_tflops"] * 1e12)}
+    if flop_ms > hbm_ms:
+        r.update({"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
+                  "unit": "TFLOP/s", "frac": flop_ms / ms})
+    return r
 
 
 class ClockSampler:
@@ -362,11 +462,8 @@ def main():
 
     peaks, peak_kind = load_peaks()
     fwd_bytes = io_bytes(w)
-    achieved = fwd_bytes / (launch_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": MEASURED_TRAFFIC.get(w.name),
-                "peak_kind": peak_kind,
-                "kernel": fwd_kernel_name(w), "bytes_per_launch": fwd_bytes, "launch_ms": launch_ms}
+    roofline = roofline_of(fwd_bytes, chunk_flops(w), launch_ms, peaks, peak_kind)
+    roofline.update({"traffic": measured_traffic(w.name), "kernel": fwd_kernel_name(w)})
     # launches of our kernels per forward step: the forward kernel itself
     gpu_launches = fwd_launches(w) * args.steps
 
@@ -442,9 +539,11 @@ def main():
     got = hout[(Ke - 1) % 2][0].to(torch.float32)
     ref = o.to(torch.float32).cpu()
     assert torch.equal(got, ref), "end-to-end outputs differ from the device-resident run"
+    link = host_link(h2d, d2h)
     e2e = {"value": replicas.whole_job_tokens_per_s(tokens, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-           "overlap": "step k+1 inputs in, step k forward, step k-1 outputs out on three streams"}
+           "overlap": "step k+1 inputs in, step k forward, step k-1 outputs out on three streams",
+           "host_link": link, "link_floor_ms": link["both_ms"], "frac_of_link_floor": link["both_ms"] / e2e_ms}
     gpu_launches += fwd_launches(w) * Ke
 
     fwdbwd = None
@@ -455,8 +554,11 @@ def main():
         kb = max(3, args.steps // 4)
         fb_total, fb_launch = timed(fb, kb, 3)
         fb_ms = fb_total / kb
-        fwdbwd = {"value": replicas.whole_job_tokens_per_s(tokens, world, fb_ms), "unit": "tokens/s", "ms_per_step": fb_ms,
-                  "bwd_bytes": io_bytes(w, backward=True)}
+        fb_bytes = fwd_bytes + io_bytes(w, backward=True)
+        fb_flops = chunk_flops(w) + chunk_flops(w, backward=True)
+        fwdbwd = {"value": replicas.whole_job_tokens_per_s(tokens, world, fb_ms), "unit": "tokens/s",
+                  "ms_per_step": fb_ms, "bwd_bytes": io_bytes(w, backward=True),
+                  "roofline": roofline_of(fb_bytes, fb_flops, fb_ms, peaks, peak_kind)}
         gpu_launches += (fwd_launches(w) + bwd_launches(w)) * kb
 
     cpu = None

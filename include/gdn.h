@@ -40,6 +40,12 @@
  * detect on the device (an expired bounded wait) are written to a status
  * word at the start of the workspace, which gdn_last_device_status reads.
  *
+ * Test hook: the library's own failure-path tests set the environment
+ * variable GDN_TEST_STARVE_CHUNK=k before a process's first call; the
+ * tensor-core forward then never loads chunk k, its bounded wait expires and
+ * the device status reads GDN_ERR_TIMEOUT.  It is read once per process and
+ * must not be set in production.
+ *
  * Limits: B, H >= 1 and B * H <= 2^26; T >= 0 (with T = 0 the per-token pointers may be NULL:
  * the forward copies h0, or zeros, to hT; the backward writes dh0 = dhT and
  * dA_log = 0); 1 <= d_k, d_v <= 128 (the tensor-core forward takes
@@ -184,20 +190,32 @@ gdn_status_t gdn_bwd(const gdn_shape_t* shape,
  * afford cudaMalloc's implicit device synchronisation, plugins inside a host
  * framework that owns all device memory and offers them no allocator, and
  * processes that reserve their memory at start-up and forbid later
- * allocations.  Arguments, results and errors are those of gdn_bwd; the
- * workspace is a 32 MiB array inside the library (one per GPU that loads it,
- * held until the process exits).  Shapes whose gdn_workspace_bytes(shape, 1)
- * exceeds 32 MiB are rejected with GDN_ERR_WORKSPACE before anything is
- * enqueued.  All calls on a device share that array: calls that may overlap
- * on the GPU race and must be ordered by the caller.  The first call on each
- * device looks up the array's address (cudaGetSymbolAddress) with that device
- * current; make it before any stream capture on that device. */
+ * allocations.  Arguments and results are those of gdn_bwd; the workspace is
+ * a 32 MiB array inside the library (one per GPU that loads it, held until
+ * the process exits).  Errors: the shape's own errors as gdn_bwd returns them
+ * (GDN_ERR_NULL, GDN_ERR_MODE, GDN_ERR_SHAPE), then GDN_ERR_WORKSPACE if
+ * gdn_workspace_bytes(shape, 1) exceeds 32 MiB, GDN_ERR_DEVICE on a GPU that
+ * is not sm_103, then gdn_bwd's own checks; nothing is enqueued on an error.
+ * The status the kernels leave on the device (an expired wait, or with
+ * GDN_CHECK_FINITE a non-finite gradient) is read by gdn_bwd_noalloc_status.
+ * All calls on a device share the array: calls that may overlap on the GPU
+ * race and must be ordered by the caller.  Each call looks up the array's
+ * device address (cudaGetSymbolAddress) on the current device; the first
+ * lookup on a device may load the library's device code, so make the first
+ * call before any stream capture on that device. */
 gdn_status_t gdn_bwd_noalloc(const gdn_shape_t* shape,
                              const void* v, const void* b, const void* c,
                              const void* g, const void* beta, const float* A_log,
                              const float* h0, const void* dO, const float* dhT,
                              void* dv, void* db, void* dc, void* dg, void* dbeta,
                              float* dA_log, float* dh0, gdn_stream_t stream);
+
+/* gdn_last_device_status for the array gdn_bwd_noalloc uses as its workspace
+ * on the current device: synchronises `stream`, then returns GDN_OK,
+ * GDN_ERR_TIMEOUT or GDN_ERR_NONFINITE as left by the last gdn_bwd_noalloc
+ * call on this device (GDN_ERR_CUDA if a CUDA call fails, GDN_ERR_DEVICE on a
+ * GPU that is not sm_103).  Allocates nothing. */
+gdn_status_t gdn_bwd_noalloc_status(gdn_stream_t stream);
 
 /* Synchronises `stream` and returns the status the kernels of the last call
  * that used `ws` left in it (GDN_OK, GDN_ERR_TIMEOUT), or GDN_ERR_CUDA if the

@@ -1,7 +1,7 @@
 """GB300 (sm_103a) gated delta rule: Python binding of libgdn's C ABI.
 
 The functions below carry the C names (``gdn_fwd``, ``gdn_bwd``,
-``gdn_bwd_noalloc``, ``gdn_workspace_bytes``, ``gdn_plan``,
+``gdn_bwd_noalloc``, ``gdn_bwd_noalloc_status``, ``gdn_workspace_bytes``, ``gdn_plan``,
 ``gdn_last_device_status``, ``gdn_status_string``)
 and only marshal arguments: torch tensors become device pointers, ``None``
 becomes NULL, and the stream defaults to torch's current stream.  Every step
@@ -106,6 +106,8 @@ def load(path: str | None = None):
             lib.gdn_bwd.restype = ctypes.c_int
             lib.gdn_bwd_noalloc.argtypes = [sp] + [vp] * 16 + [vp]
             lib.gdn_bwd_noalloc.restype = ctypes.c_int
+            lib.gdn_bwd_noalloc_status.argtypes = [vp]
+            lib.gdn_bwd_noalloc_status.restype = ctypes.c_int
             lib.gdn_last_device_status.argtypes = [vp, vp]
             lib.gdn_last_device_status.restype = ctypes.c_int
             lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -169,6 +171,11 @@ def gdn_bwd_noalloc(shape, v, b, c, g, beta, A_log, h0, dO, dhT, dv, db, dc, dg,
     return int(load().gdn_bwd_noalloc(ctypes.byref(shape), _ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(beta),
                                       _ptr(A_log), _ptr(h0), _ptr(dO), _ptr(dhT), _ptr(dv), _ptr(db), _ptr(dc),
                                       _ptr(dg), _ptr(dbeta), _ptr(dA_log), _ptr(dh0), _stream(stream)))
+
+
+def gdn_bwd_noalloc_status(stream=None) -> int:
+    """gdn_last_device_status of the array gdn_bwd_noalloc uses as its workspace (synchronises)."""
+    return int(load().gdn_bwd_noalloc_status(_stream(stream)))
 
 
 def gdn_last_device_status(ws, stream=None) -> int:

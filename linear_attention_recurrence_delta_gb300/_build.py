@@ -3,8 +3,7 @@
 Every translation unit is compiled for sm_103a only, in parallel, then linked
 into ``linear_attention_recurrence_delta_gb300/libgdn.so``.  Object files go to
 ``_build/`` at the repository root.  A rebuild happens only when a source or
-header is newer than the library.  The measurement aid in ``probe/`` (the exp2
-throughput of the special-function units) becomes ``libgdn_probe.so``.
+header is newer than the library.
 """
 from __future__ import annotations
 
@@ -19,8 +18,6 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
-PROBE_SRC = os.path.join(PKG, "probe", "ex2_rate.cu")
-PROBE_LIB = os.path.join(PKG, "libgdn_probe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -47,21 +44,7 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build_probe(force: bool = False) -> str:
-    """libgdn_probe.so: the exp2-throughput probe (one translation unit)."""
-    if not force and os.path.exists(PROBE_LIB) and os.path.getmtime(PROBE_LIB) >= os.path.getmtime(PROBE_SRC):
-        return PROBE_LIB
-    tmp = PROBE_LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), "-std=c++17", "-O3", "-Xcompiler", "-fPIC", *ARCH, "-shared", PROBE_SRC, "-o", tmp, "-lcudart"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed on {PROBE_SRC}:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, PROBE_LIB)
-    return PROBE_LIB
-
-
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    build_probe(force)
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)

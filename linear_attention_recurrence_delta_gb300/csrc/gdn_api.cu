@@ -3,6 +3,7 @@
 // gdn_last_device_status, whose job is to synchronise and read back.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "gdn_internal.h"
@@ -105,7 +106,7 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm)
 
 static int cached_dev_ok[64];  // 0 unknown, 1 ok, 2 not sm_103
 
-static gdn_status_t check_device()
+gdn_status_t check_device()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
@@ -118,6 +119,15 @@ static gdn_status_t check_device()
         cached_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
     }
     return cached_dev_ok[dev] == 1 ? GDN_OK : GDN_ERR_DEVICE;
+}
+
+int test_starve_chunk()
+{
+    static const int k = [] {
+        const char* e = getenv("GDN_TEST_STARVE_CHUNK");
+        return e ? atoi(e) : -1;
+    }();
+    return k;
 }
 
 static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }

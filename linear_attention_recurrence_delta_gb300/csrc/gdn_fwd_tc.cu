@@ -1026,15 +1026,10 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv = a.dv;
     p.logits = a.logits;
     p.nchunks = (a.T + kC - 1) / kC;
-    // Failure-path test hook: with GDN_TEST_STARVE_CHUNK=k in the environment the loads of chunk k are never
-    // issued, so its bounded wait expires (after kTestWaitNs), the kernel winds down and the status word reads
-    // GDN_ERR_TIMEOUT.  Without the variable nothing changes.
-    p.starve_chunk = -1;
-    p.wait_ns = kWaitNs;
-    if (const char* e = getenv("GDN_TEST_STARVE_CHUNK")) {
-        p.starve_chunk = atoi(e);
-        p.wait_ns = kTestWaitNs;
-    }
+    // failure-path test hook (read once per process, see test_starve_chunk): the loads of that chunk are never
+    // issued, so its bounded wait expires after kTestWaitNs and the status word reads GDN_ERR_TIMEOUT
+    p.starve_chunk = test_starve_chunk();
+    p.wait_ns = p.starve_chunk >= 0 ? kTestWaitNs : kWaitNs;
     *handled = true;
     const dim3 grid(a.B * a.H, (a.dv + 63) / 64);
     if (a.norm)

@@ -86,6 +86,15 @@ cudaError_t launch_bwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStrea
                               cudaError_t (*fwd_core)(const Args&, cudaStream_t));
 int decode_max_tokens();
 
+// Failure-path test hook, for the library's own tests only: the value of the environment variable
+// GDN_TEST_STARVE_CHUNK, read once per process (-1 when it is not set).  With it set to k, the tensor-core
+// forward never issues the loads of chunk k, so that chunk's bounded wait expires, the kernel winds down and the
+// status word reads GDN_ERR_TIMEOUT.  Set it before the process's first forward call.
+int test_starve_chunk();
+
+// GDN_OK if the current device is an sm_103 GPU, GDN_ERR_DEVICE if not, GDN_ERR_CUDA if it cannot be queried
+gdn_status_t check_device();
+
 constexpr float kNormFloor = 1e-12f;   // L2 normalisation: x / max(||x||, kNormFloor)
 
 // Device status word helpers.
