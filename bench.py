@@ -140,6 +140,8 @@ def bwd_slabs(w):
 
 def bwd_launches(w):
     """Kernels one gdn_bwd call launches."""
+    if plan(w, True).bwd_kernel == 2:
+        return 4   # chunked backward: prep, chain, gradients, dA_log sum
     if tsplit_factor(w, True) == 1:
         # backward, the slabs' partial sums of db, dc, dg (, dbeta) if several, dA_log reduction
         sums = (4 if w.mode == "delta" else 3) if bwd_slabs(w) > 1 else 0

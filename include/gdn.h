@@ -137,8 +137,14 @@ size_t gdn_workspace_bytes(const gdn_shape_t* shape, int backward);
  *               split.  Long sequences over few heads are split.
  *   fwd_kernel  the kernel of the forward runs the call makes (gdn_kernel_t):
  *               gdn_fwd's own runs; gdn_bwd's forward runs over the segments
- *               under a split, GDN_KERNEL_NONE without one (the serial
- *               backward recomputes the forward itself).  Also NONE for T = 0.
+ *               under a split, GDN_KERNEL_NONE otherwise (both backward
+ *               kernels recompute the forward themselves).  NONE for T = 0.
+ *   bwd_kernel  (backward = 1) the backward kernel (gdn_bwd_kernel_t):
+ *               GDN_BWD_TENSOR_CORE, the chunked reverse recurrence on tcgen05
+ *               (bf16, d_k and d_v <= 64, no option bits: three passes over
+ *               the chunks, a chain over the chunk boundaries between them);
+ *               GDN_BWD_SERIAL, the token-serial reverse walk (every other
+ *               shape); GDN_BWD_NONE for backward = 0 or T = 0.
  * Returns GDN_OK, or the error the call would return for the shape alone
  * (GDN_ERR_NULL, GDN_ERR_MODE, GDN_ERR_SHAPE). */
 typedef enum {
@@ -148,9 +154,16 @@ typedef enum {
     GDN_KERNEL_SERIAL = 3         /* token-serial forward on the CUDA cores     */
 } gdn_kernel_t;
 
+typedef enum {
+    GDN_BWD_NONE = 0,
+    GDN_BWD_SERIAL = 1,           /* token-serial reverse walk (CUDA cores)     */
+    GDN_BWD_TENSOR_CORE = 2       /* chunked reverse recurrence on tcgen05      */
+} gdn_bwd_kernel_t;
+
 typedef struct {
     int segments;
     int fwd_kernel;   /* gdn_kernel_t */
+    int bwd_kernel;   /* gdn_bwd_kernel_t */
 } gdn_plan_t;
 
 gdn_status_t gdn_plan(const gdn_shape_t* shape, int backward, gdn_plan_t* plan);
@@ -171,7 +184,9 @@ gdn_status_t gdn_fwd(const gdn_shape_t* shape,
 
 /* Backward pass: gradients of L(o, h_T) given dL/do = dO and dL/dh_T = dhT
  * (NULL => zero).  Takes the forward's inputs again (the forward is
- * recomputed inside; nothing from gdn_fwd is kept).  Writes dv, db, dc, dg,
+ * recomputed inside; nothing from gdn_fwd is kept).  gdn_plan tells which
+ * backward kernel a shape takes; both give the same gradients within the
+ * tolerance of the I/O dtype, and each is deterministic (fixed-order sums).  Writes dv, db, dc, dg,
  * dbeta (NULL iff mode == GDN_GATED) in dtype `io`, dA_log [H, d_k] float32
  * (overwritten, summed over the batch) and dh0 (NULL => not written).
  * dg and dbeta are gradients with respect to the post-sigmoid g and beta.

@@ -42,6 +42,8 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_OK = 0
 GDN_KERNEL_NONE, GDN_KERNEL_DECODE, GDN_KERNEL_TENSOR_CORE, GDN_KERNEL_SERIAL = 0, 1, 2, 3
 KERNEL_NAMES = {0: "none", 1: "decode", 2: "tensor_core", 3: "serial"}
+GDN_BWD_NONE, GDN_BWD_SERIAL, GDN_BWD_TENSOR_CORE = 0, 1, 2
+BWD_KERNEL_NAMES = {0: "none", 1: "serial", 2: "tensor_core"}
 STATUS_NAMES = {
     0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_ALIGN", 4: "GDN_ERR_MODE",
     5: "GDN_ERR_WORKSPACE", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_DEVICE",
@@ -70,7 +72,7 @@ class gdn_shape_t(ctypes.Structure):
 
 
 class gdn_plan_t(ctypes.Structure):
-    _fields_ = [("segments", ctypes.c_int), ("fwd_kernel", ctypes.c_int)]
+    _fields_ = [("segments", ctypes.c_int), ("fwd_kernel", ctypes.c_int), ("bwd_kernel", ctypes.c_int)]
 
 
 def make_shape(B, H, T, dk, dv, mode="gated", io="bf16", gate_logits=False, norm_bc=False,

@@ -86,11 +86,45 @@ WsLayout ws_layout_bwd_core(const gdn_shape_t& s, int norm)
     return L;
 }
 
-WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm)
+int bwd_split(const gdn_shape_t& s, int logits, int norm)
+{
+    if (s.T <= 0 || chunk_bwd_applies(s, logits, norm)) return 1;
+    return tsplit_factor(s, 1);
+}
+
+// the chunked backward's per-chunk records, placed from `off`
+static size_t place_chunk_bwd(const gdn_shape_t& s, WsLayout& L, size_t off)
+{
+    const size_t nq = (size_t)s.B * s.H * (size_t)((s.T + 63) / 64);
+    const size_t rec = nq * 64 * 64 * sizeof(float);
+    if (s.mode == GDN_DELTA) {
+        L.cb_phi_off = off;
+        off = round_up(off + rec, 256);
+    }
+    L.cb_dlt_off = off;
+    off = round_up(off + rec, 256);
+    L.cb_y_off = off;
+    off = round_up(off + rec, 256);
+    L.cb_st_off = off;
+    off = round_up(off + rec, 256);
+    L.cb_dst_off = off;
+    off = round_up(off + rec, 256);
+    L.cb_ec_off = off;
+    off = round_up(off + nq * 64 * sizeof(float), 256);
+    L.cb_da_off = off;
+    off = round_up(off + nq * 64 * sizeof(float), 256);
+    return off;
+}
+
+WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm, int logits)
 {
     WsLayout L;
     size_t off = 256;  // status word
-    const int P = s.T > 0 ? tsplit_factor(s, backward) : 1;
+    if (backward && chunk_bwd_applies(s, logits, norm)) {
+        L.total = place_chunk_bwd(s, L, off);
+        return L;
+    }
+    const int P = s.T > 0 ? (backward ? bwd_split(s, logits, norm) : tsplit_factor(s, 0)) : 1;
     if (backward) {
         gdn_shape_t core = s;
         if (P > 1) {
@@ -134,7 +168,7 @@ static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 static gdn_status_t check_common(const gdn_shape_t* s, const void* v, const void* b, const void* c,
                                  const void* g, const void* beta, const float* A_log, const float* h0,
-                                 void* ws, size_t ws_bytes, int backward, int norm)
+                                 void* ws, size_t ws_bytes, int backward, int norm, int logits)
 {
     if (!s) return GDN_ERR_NULL;
     if (s->mode != GDN_GATED && s->mode != GDN_DELTA) return GDN_ERR_MODE;
@@ -151,7 +185,7 @@ static gdn_status_t check_common(const gdn_shape_t* s, const void* v, const void
         (beta && !aligned(beta, s->io == GDN_BF16 ? 2 : 4)))
         return GDN_ERR_ALIGN;
     if (!aligned(A_log, 16) || (h0 && !aligned(h0, 16)) || !aligned(ws, 256)) return GDN_ERR_ALIGN;
-    if (ws_bytes < ws_layout(*s, backward, norm).total) return GDN_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(*s, backward, norm, logits).total) return GDN_ERR_WORKSPACE;
     return GDN_OK;
 }
 
@@ -224,12 +258,14 @@ extern "C" gdn_status_t gdn_plan(const gdn_shape_t* shape_in, int backward, gdn_
     if ((sh.mode != GDN_GATED && sh.mode != GDN_DELTA) || (sh.io != GDN_F32 && sh.io != GDN_BF16))
         return GDN_ERR_MODE;
     if (!shape_ok(sh)) return GDN_ERR_SHAPE;
-    const int P = sh.T > 0 ? tsplit_factor(sh, backward ? 1 : 0) : 1;
+    const int P = sh.T > 0 ? (backward ? bwd_split(sh, logits, norm) : tsplit_factor(sh, 0)) : 1;
     Args a = make_args(&sh);   // the runs' view: P segments of one sequence are P batch rows
     a.B = sh.B * P;
     a.T = sh.T / P;
     plan->segments = P;
     plan->fwd_kernel = (backward && P == 1) ? GDN_KERNEL_NONE : fwd_kernel_of(a);
+    plan->bwd_kernel = !backward || sh.T <= 0 ? GDN_BWD_NONE
+                       : chunk_bwd_applies(sh, logits, norm) ? GDN_BWD_TENSOR_CORE : GDN_BWD_SERIAL;
     return GDN_OK;
 }
 
@@ -242,7 +278,7 @@ extern "C" size_t gdn_workspace_bytes(const gdn_shape_t* shape_in, int backward)
     if (!shape_ok(*shape)) return 0;
     if ((shape->mode != GDN_GATED && shape->mode != GDN_DELTA) || (shape->io != GDN_F32 && shape->io != GDN_BF16))
         return 0;
-    return ws_layout(*shape, backward ? 1 : 0, norm).total;
+    return ws_layout(*shape, backward ? 1 : 0, norm, logits).total;
 }
 
 extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, const void* b, const void* c,
@@ -254,7 +290,7 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, cons
     if (!shape_in) return GDN_ERR_NULL;
     if (!split_mode(shape_in, &sh, &logits, &norm, &check)) return GDN_ERR_MODE;
     const gdn_shape_t* shape = &sh;
-    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 0, norm);
+    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 0, norm, logits);
     if (r != GDN_OK) return r;
     if (!o && shape->T > 0) return GDN_ERR_NULL;
     const size_t ioa = shape->io == GDN_BF16 ? 16 : 4;
@@ -295,7 +331,7 @@ extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape_in, const void* v, cons
     if (!shape_in) return GDN_ERR_NULL;
     if (!split_mode(shape_in, &sh, &logits, &norm, &check)) return GDN_ERR_MODE;
     const gdn_shape_t* shape = &sh;
-    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 1, norm);
+    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 1, norm, logits);
     if (r != GDN_OK) return r;
     const bool tok = shape->T > 0;
     if ((tok && (!dO || !dv || !db || !dc || !dg)) || !dA_log) return GDN_ERR_NULL;
@@ -315,8 +351,14 @@ extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape_in, const void* v, cons
     a.v = v; a.b = b; a.c = c; a.g = g; a.beta = beta; a.A_log = A_log; a.h0 = h0;
     a.dO = dO; a.dhT = dhT; a.dv_ = dv; a.db = db; a.dc = dc; a.dg = dg; a.dbeta = dbeta;
     a.dA_log = dA_log; a.dh0 = dh0; a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits; a.norm = norm;
-    const int P = a.T > 0 ? tsplit_factor(*shape, 1) : 1;
-    cudaError_t e = P > 1 ? launch_bwd_tsplit(a, ws_layout(*shape, 1, norm), P, st, fwd_core) : launch_serial_bwd(a, st);
+    cudaError_t e;
+    if (a.T > 0 && chunk_bwd_applies(*shape, logits, norm)) {
+        e = launch_chunk_bwd(a, ws_layout(*shape, 1, norm, logits), st);
+    } else {
+        const int P = bwd_split(*shape, logits, norm);
+        e = P > 1 ? launch_bwd_tsplit(a, ws_layout(*shape, 1, norm, logits), P, st, fwd_core)
+                  : launch_serial_bwd(a, st);
+    }
     if (e == cudaSuccess && check) {
         const size_t ntok = (size_t)a.B * a.T * a.H, st_n = (size_t)a.B * a.H * a.dk * a.dv;
         const struct { const void* p; size_t n; int io; } outs[] = {

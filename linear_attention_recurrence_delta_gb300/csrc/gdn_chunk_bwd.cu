@@ -1,0 +1,1689 @@
+// gdn_chunk_bwd.cu -- the chunked backward of the gated delta rule on tcgen05
+// tensor cores (bf16 I/O, d_k, d_v <= 64): three chunk-level passes instead of a
+// token-serial walk.
+//
+// "GDN & MLA Mechanism Deep-Dive", Step 5 (Chunked recurrence) solves each chunk
+// of C = 64 tokens in closed form; with S the state entering a chunk,
+//   gated: U = V;  delta ("HyMo-434M -- documentation portal", card 01):
+//          (I + diag(beta) K) U = diag(beta) (V - Btil S),  U = Util - W S
+//   O = Ctil S + P U,   S' = diag(E) S + Bhat^T U,
+// with P, K the decay-weighted c.b and b.b scores, Ctil = c (.) exp(A G_t),
+// Btil = b (.) exp(A G_t), Bhat = b (.) exp(A (G_63 - G_t)), E = exp(A G_63) and
+// G_t the inclusive sum of g within the chunk.  The chunk's map of states is
+// affine, S' = Phi S + Delta with Phi = diag(E) - Bhat^T W (gated: diag(E)) and
+// Delta = Bhat^T Util (gated: Bhat^T V), and its outputs are O = Qc S + P Util
+// with Qc = Ctil - P W (gated: Ctil).  So the adjoint of the entering state is
+//   dS = Phi^T dS' + Y,   Y = Qc^T dO.
+// The backward is therefore:
+//   1. chunk_prep_kernel, one chunk at a time over every chunk of every head
+//      (no chunk waits for another): Phi (delta), Delta and Y of each chunk;
+//   2. chunk_chain_kernel, per head and 16-column slab of the state: the
+//      states entering the chunks (S_{k+1} = Phi_k S_k + Delta_k from h0) and the
+//      adjoints leaving them (dS_k = Phi_k^T dS_{k+1} + Y_k from dh_T), fp32;
+//   3. chunk_grad_kernel, again one chunk at a time: with S and dS' of the
+//      chunk known, every token gradient of the chunk by the reverse mode of its
+//      closed form (the transposed contractions of the forward, on tcgen05).
+//
+// Decay split.  exp(A (G_t - G_s)) (s <= t) must be split into a row and a
+// column factor without overflow (|A| up to 16 over 64 tokens reaches
+// exp(+-1024)):
+//   * tokens in different 16-blocks (t in block I > block of s): reference at
+//     the last token before block I; both factors are <= 1, the operands fp16,
+//     and one N = 96 product covers the three row blocks (their column operands
+//     stacked: 16, 32 and 48 rows);
+//   * tokens in the same 16-block ("near" pairs, the largest entries): fp32 on
+//     the CUDA cores, exp(A (G_t - G_s)) = alpha_t / alpha_s with the anchor
+//     alpha_t = exp(A (G_t - G_r)) at the 4th token r of t's 8-block (a factor
+//     at most exp(|A| * sum of 4 g)), times exp(A (G_r' - G_r)) <= 1 when t and s
+//     lie in different 8-halves.  A chunk whose anchors could overflow
+//     (|A| log2(e) * 4-token span > 100) evaluates every near pair directly.
+//
+// Delta solve (WY form, as in the forward): D = the 32-blocks of I + M
+// (M = diag(beta) K) is inverted in fp32 (16-blocks by forward substitution and
+// their coupling block), L = the block below them, N = D^-1 L with N^2 = 0, so
+//   (I + M)^-1 R = (I - N) D^-1 R   and   (I + M)^-T Z = D^-T (I - N^T) Z.
+//
+// Precision: the 16-block level's operands (factors <= 1) are fp16; every other
+// product takes its derived operands as bf16 hi + lo pairs against exact bf16
+// inputs (hi*x + lo*x), or hi*hi + hi*lo + lo*hi between two derived operands.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include "chunk_common.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace tc;
+using namespace fwdtc;
+using namespace chunk;
+
+constexpr int kThreads = 256;
+constexpr int kBS = 20;   // padded row stride of the fp32 16 x 16 blocks (conflict-free float4 rows)
+
+struct CbParams {
+    CUtensorMap tm_v, tm_b, tm_c, tm_do;
+    const __nv_bfloat16* g;
+    const __nv_bfloat16* beta;
+    const float* A_log;
+    // per chunk q = unit * nchunks + k, each [64][64] fp32 (rows = key channel i, columns = value column j)
+    float* phi;     // delta: Phi of the chunk (S' = Phi S + Delta)
+    float* dlt;     // Delta
+    float* ych;     // Y = Qc^T dO
+    float* ec;      // gated: [q][64] exp(A G_63)
+    float* st;      // the state entering the chunk
+    float* dst;     // the adjoint of the state leaving the chunk
+    const float* h0;
+    const float* dhT;
+    float* dh0;
+    __nv_bfloat16 *dv, *db, *dc, *dg, *dbeta;
+    float* dA_part;   // [q][64]: sum_t G_t dGam_t[i] of the chunk (times A in the reduction)
+    uint32_t* status;
+    int B, H, T, dk, dv_, nchunks, nq;
+    uint64_t wait_ns;
+    int starve;       // failure-path test hook: the chunk q whose loads are never issued (-1: none)
+};
+
+// ---------------------------------------------------------------- shared memory
+constexpr uint32_t OFF_STAGE = 0;                        // b, c, v, dO tiles (TMA)
+constexpr uint32_t ST_B = 0, ST_C = 8192, ST_V = 16384, ST_DO = 24576;
+constexpr uint32_t OFF_ALPHA = 32768;                    // fp32 [64][64] anchors alpha_t[i]
+constexpr uint32_t OFF_YB = 49152;                       // fp32 [64][64] b_t[i] / alpha_t[i]
+constexpr uint32_t OFF_TAB = 65536;                      // KAP [4][64], EC [64] (fp32)
+constexpr uint32_t OFF_SMALL = 67584;
+constexpr uint32_t OFF_X = 81920;                        // phase region
+
+struct Small {
+    float G[64];
+    float A2[64];
+    float g[64];
+    float beta[64];
+    float sd[4][64];     // grad: partial sums over value columns of dS'[i][j] S[i][j]
+    float rs[2][2][64];  // grad: per (kind, column half) row partial sums
+    float colsum[4][64];
+    float dgp[4][64];    // grad: per channel quarter partial sums of dG_t
+    uint64_t full, mma;
+    uint32_t tmem_base, abort, unsafe;
+    float a2max;
+};
+static_assert(sizeof(Small) <= OFF_X - OFF_SMALL, "small block");
+
+struct Tab {
+    float KAP[4][64];
+    float EC[64];
+};
+static_assert(sizeof(Tab) <= OFF_SMALL - OFF_TAB, "tables");
+
+// prep layout (offsets within the phase region)
+namespace pl {
+constexpr uint32_t A1 = 0, B1 = 16384, LR = 28672, LRL = 53248, NEAR = 69632, P = 78848, BH = 95232,
+                   MS = 111616, DINV = 126976, BYTES = 143360;
+constexpr uint32_t NA = 0, X0 = 28672, WU = 28672, QC = 0;
+// gated: [Bhat | Ctil] hi, then lo
+constexpr uint32_t GA = 0;
+}  // namespace pl
+
+// grad layout
+namespace gl {
+constexpr uint32_t A1 = 0, B1 = 16384, LR = 28672, LRL = 53248, NEAR = 69632, P = 78848, KP = 95232,
+                   MS = 103424, DINV = 118784, BYTES = 135168;
+constexpr uint32_t NA = 0, X0 = 28672;
+constexpr uint32_t NW = 16384, U = 28672, DSN = 61440;              // U_hi | S_hi | U_lo | S_lo
+constexpr uint32_t BHH = 16384, BHL = 103424;
+constexpr uint32_t DU = 78848, Z = 0, DOR = 78848, ZR = 118784;
+constexpr uint32_t AD = 28672, NEARD = 61440, SEG = 28672;
+constexpr uint32_t DC = 78848, DB = 95232, DG = 111616;
+}  // namespace gl
+
+// fp32 sub-blocks inside MS: the diagonal 16-blocks of M, the 16-blocks below them inside each 32-block,
+// the diagonal blocks' inverses and the 32-blocks' coupling blocks
+constexpr uint32_t MS_M32 = 0, MS_C32 = 4 * 16 * kBS * 4, MS_DI32 = MS_C32 + 2 * 16 * kBS * 4,
+                   MS_E32 = MS_DI32 + 4 * 16 * kBS * 4, MS_BYTES = MS_E32 + 2 * 16 * kBS * 4;
+static_assert(MS_BYTES <= pl::DINV - pl::MS && MS_BYTES <= gl::DINV - gl::MS, "MS blocks");
+
+// TMEM columns
+constexpr uint32_t TM_D1 = 0;       // 16-block level [P ; K] (96 columns)
+constexpr uint32_t TM_NX = 96;      // [N | X0V | X0W] -> [N | Util | W]
+constexpr uint32_t TM_UT = TM_NX + 64, TM_W = TM_NX + 128;
+constexpr uint32_t TM_COLS = 512;
+
+__device__ __forceinline__ float* fptr(unsigned char* base, uint32_t off) { return reinterpret_cast<float*>(base + off); }
+
+__device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(tmap), "r"(c0),
+                 "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- the common front of prep and grad
+// Everything below runs with 256 threads: r = thread, trow = r & 127 = TMEM lane, q4 = lane quarter,
+// wh = column half.
+struct Ctx {
+    unsigned char* sm;
+    unsigned char* X;
+    Small* S;
+    Tab* KT;
+    float* ALPHA;
+    float* YB;
+    uint32_t tbase, tl;
+    int r, warp, lane, q4, wh, trow;
+    uint32_t mma_phase;
+};
+
+__device__ __forceinline__ void bar_all() { named_bar_sync(1, kThreads); }
+
+__device__ __forceinline__ void smem_to_tc()
+{
+    fence_proxy_async_smem();
+    tc_fence_before();
+    bar_all();
+    tc_fence_after();
+}
+
+// one warp polls the MMA barrier, the others wait at the named barrier
+__device__ __forceinline__ bool mma_wait(Ctx& c, const CbParams& p)
+{
+    if (c.warp == 0) wait_or_abort(&c.S->mma, c.mma_phase, &c.S->abort, p.status, p.wait_ns);
+    bar_all();
+    c.mma_phase ^= 1;
+    tc_fence_after();
+    return *(volatile uint32_t*)&c.S->abort == 0;
+}
+
+// (1) scan of g (warp 0), overflow check of the anchors, decay tables
+__device__ __forceinline__ void front_scan(Ctx& c)
+{
+    Small& S = *c.S;
+    if (c.warp == 0) {
+        const float ga = S.g[2 * c.lane], gb = S.g[2 * c.lane + 1];
+        float x = ga + gb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (c.lane >= o) x += y;
+        }
+        const float ex = __shfl_up_sync(0xffffffffu, x, 1);
+        S.G[2 * c.lane] = (c.lane > 0 ? ex : 0.f) + ga;
+        S.G[2 * c.lane + 1] = x;
+        float m = fmaxf(fabsf(S.A2[c.lane]), fabsf(S.A2[c.lane + 32]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        __syncwarp();
+        float span = 0.f;
+        if (c.lane < 8) {
+            const float g0 = S.G[8 * c.lane], g3 = S.G[8 * c.lane + 3], g7 = S.G[8 * c.lane + 7];
+            span = fmaxf(g3 - g0, g7 - g3);
+        }
+        const bool bad = __any_sync(0xffffffffu, span * m > kSafeLog2);
+        if (c.lane == 0) S.unsafe = bad ? 1u : 0u;
+    }
+    bar_all();
+    {
+        const int J = c.r >> 6, i = c.r & 63;
+        const float a2 = S.A2[i];
+        c.KT->KAP[J][i] = fast_exp2(a2 * (S.G[16 * J + 11] - S.G[16 * J + 3]));
+        if (J == 0) c.KT->EC[i] = fast_exp2(a2 * S.G[63]);
+    }
+}
+
+// (2) anchors of token t = r & 63 over channels 16 cq .. 16 cq + 15 (cq = r >> 6): ALPHA, YB; the 16-block level
+// operands A1 = [c f1 ; b f1] (rows t >= 16) and B1 (the column operands of row blocks 1..3), fp16.
+__device__ __forceinline__ void front_operands(Ctx& c, unsigned char* A1, unsigned char* B1, bool with_b_rows)
+{
+    Small& S = *c.S;
+    const int t = c.r & 63, cq = c.r >> 6, k8 = t >> 3, I = t >> 4;
+    const float Gt = S.G[t], dG = Gt - S.G[8 * k8 + 3];
+    const unsigned char* sB = c.sm + OFF_STAGE + ST_B;
+    const unsigned char* sC = c.sm + OFF_STAGE + ST_C;
+    float bv[16], cv[16];
+    ld16_bf16(sB, t, cq, bv);
+    ld16_bf16(sC, t, cq, cv);
+    float al[16], yb[16];
+#pragma unroll
+    for (int e = 0; e < 16; e++) {
+        const float a2 = S.A2[16 * cq + e];
+        al[e] = fast_exp2(a2 * dG);
+        yb[e] = bv[e] * fast_exp2(-a2 * dG);
+    }
+    float* arow = c.ALPHA + t * 64 + 16 * cq;
+    float* yrow = c.YB + t * 64 + 16 * cq;
+#pragma unroll
+    for (int e = 0; e < 16; e += 4) {
+        *reinterpret_cast<float4*>(arow + e) = make_float4(al[e], al[e + 1], al[e + 2], al[e + 3]);
+        *reinterpret_cast<float4*>(yrow + e) = make_float4(yb[e], yb[e + 1], yb[e + 2], yb[e + 3]);
+    }
+    // row factor of the 16-block level: exp(A (G_t - G_{16 I - 1})) <= 1
+    float y[16], z[16];
+    if (I >= 1) {
+        const float Gref = S.G[16 * I - 1];
+#pragma unroll
+        for (int e = 0; e < 16; e++) {
+            const float f = fast_exp2(S.A2[16 * cq + e] * (Gt - Gref));
+            y[e] = cv[e] * f;
+            z[e] = bv[e] * f;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 16; e++) y[e] = z[e] = 0.f;
+    }
+    st16_f16(A1, t, cq, y);
+    if (with_b_rows) st16_f16(A1, 64 + t, cq, z);
+    // column factors towards row blocks J > I: exp(A (G_{16 J - 1} - G_t)) <= 1
+#pragma unroll
+    for (int J = 1; J <= 3; J++) {
+        if (t < 16 * J) {
+            const float Gref = S.G[16 * J - 1];
+#pragma unroll
+            for (int e = 0; e < 16; e++) y[e] = bv[e] * fast_exp2(S.A2[16 * cq + e] * (Gref - Gt));
+            st16_f16(B1, seg_base(J) + t, cq, y);
+        }
+    }
+}
+
+// (3) the 16-block level product D1 = A1 B1^T (M = 128: rows 0..63 the c side, 64..127 the b side; N = 96)
+__device__ __forceinline__ void issue_level(uint32_t tbase, const unsigned char* A1, const unsigned char* B1)
+{
+    mma_tiles(tbase + TM_D1, smem_u32(A1), false, 0, 0, smem_u32(B1), false, 0, 0, 4,
+              idesc_f16(128, 96, false, false), false);
+}
+
+// (4) near pairs (same 16-block), fp32: warp w takes 16-block J = w & 3 of P (w < 4, c side) or K (b side).
+// Lane = (token tl16 of the block, channel half hh).  Writes NEAR[mat][J][t][s] (s <= t for P, s < t for K,
+// zero elsewhere), kBS-free layout [2][4][16][17].
+__device__ __forceinline__ void front_near(Ctx& c, float* NEAR, bool want_k)
+{
+    Small& S = *c.S;
+    const int J = c.warp & 3, mat = c.warp >> 2;
+    if (mat == 1 && !want_k) return;
+    const int tl16 = c.lane & 15, hh = c.lane >> 4, t = 16 * J + tl16;
+    const unsigned char* sL = c.sm + OFF_STAGE + (mat ? ST_B : ST_C);
+    float* out = NEAR + ((mat * 4 + J) * 16 + tl16) * 17;
+    if (!S.unsafe) {
+        float x[32], xe[32];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            float v8[8];
+            ld_row8(sL, t, 4 * hh + q, v8);
+#pragma unroll
+            for (int e = 0; e < 8; e++) x[8 * q + e] = v8[e] * c.ALPHA[t * 64 + 32 * hh + 8 * q + e];
+        }
+        const bool upper = tl16 >= 8;
+#pragma unroll
+        for (int e = 0; e < 32; e++) xe[e] = upper ? x[e] * c.KT->KAP[J][32 * hh + e] : x[e];
+#pragma unroll 1
+        for (int sl = 0; sl < 16; sl++) {
+            const float* yr = c.YB + (16 * J + sl) * 64 + 32 * hh;
+            float acc0 = 0.f, acc1 = 0.f;
+            if (sl < 8) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 yv = *reinterpret_cast<const float4*>(yr + e);
+                    acc0 = fmaf(xe[e], yv.x, acc0);
+                    acc1 = fmaf(xe[e + 1], yv.y, acc1);
+                    acc0 = fmaf(xe[e + 2], yv.z, acc0);
+                    acc1 = fmaf(xe[e + 3], yv.w, acc1);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 yv = *reinterpret_cast<const float4*>(yr + e);
+                    acc0 = fmaf(x[e], yv.x, acc0);
+                    acc1 = fmaf(x[e + 1], yv.y, acc1);
+                    acc0 = fmaf(x[e + 2], yv.z, acc0);
+                    acc1 = fmaf(x[e + 3], yv.w, acc1);
+                }
+            }
+            float d = acc0 + acc1;
+            d += __shfl_xor_sync(0xffffffffu, d, 16);
+            const bool keep = mat ? (sl < tl16) : (sl <= tl16);
+            if (hh == 0) out[sl] = keep ? d : 0.f;
+        }
+    } else {
+        // every factor evaluated directly (the anchors could overflow)
+        float x[32];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            float v8[8];
+            ld_row8(sL, t, 4 * hh + q, v8);
+#pragma unroll
+            for (int e = 0; e < 8; e++) x[8 * q + e] = v8[e];
+        }
+        const unsigned char* sB = c.sm + OFF_STAGE + ST_B;
+        const float Gt = S.G[t];
+#pragma unroll 1
+        for (int sl = 0; sl < 16; sl++) {
+            const int s = 16 * J + sl;
+            const float dG = Gt - S.G[s];
+            float acc = 0.f;
+            if (s <= t) {
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    float b8[8];
+                    ld_row8(sB, s, 4 * hh + q, b8);
+#pragma unroll
+                    for (int e = 0; e < 8; e++)
+                        acc = fmaf(x[8 * q + e] * b8[e], exp2f(S.A2[32 * hh + 8 * q + e] * dG), acc);
+                }
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+            const bool keep = mat ? (sl < tl16) : (sl <= tl16);
+            if (hh == 0) out[sl] = keep ? acc : 0.f;
+        }
+    }
+}
+
+// (5) P and K of row t = trow & 63 (lanes 0..63: P, 64..127: K), columns 32 wh .. 32 wh + 31, from the
+// 16-block level (TMEM) and the near pairs.  v[0..31] receives the row part.
+__device__ __forceinline__ void assemble_row(Ctx& c, const float* NEAR, float (&v)[32])
+{
+    const int t = c.trow & 63, isK = c.trow >> 6, I = t >> 4;
+    // a warp's 32 rows span the 16-blocks Ia and Ia + 1; every TMEM load is warp-uniform, each lane then takes
+    // the one of its block
+    const int Ia = 2 * (c.q4 & 1), Ib = Ia + 1;
+#pragma unroll
+    for (int h2 = 0; h2 < 2; h2++) {
+        const int cg = 2 * c.wh + h2;
+        float da[16], db[16];
+        if (cg < Ia) tmem_ld16(c.tl + TM_D1 + seg_base(Ia) + 16 * cg, da);
+        if (cg < Ib) tmem_ld16(c.tl + TM_D1 + seg_base(Ib) + 16 * cg, db);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e++) {
+            const int s = 16 * cg + e;
+            float val = 0.f;
+            if ((s >> 4) < I) val = (I == Ia) ? da[e] : db[e];
+            else if ((s >> 4) == I) val = NEAR[((isK * 4 + I) * 16 + (t & 15)) * 17 + (s & 15)];
+            v[16 * h2 + e] = val;
+        }
+    }
+}
+
+// (6) the exact inverses of the diagonal 16-blocks of I + M (threads 0..63) and, per 32-block, its coupling
+// block E = -B^-1 C A^-1 (warp w < 2 for 32-block w).  Reads M32, C32; writes DI32, E32.
+__device__ __forceinline__ void solve_blocks(Ctx& c, unsigned char* MS)
+{
+    if (c.r >= 64) return;
+    const int J = c.r >> 4, col = c.r & 15;
+    const float* M32 = fptr(MS, MS_M32) + J * 16 * kBS;
+    float xs[16];
+#pragma unroll
+    for (int q = 0; q < 16; q++) xs[q] = (q == col) ? 1.f : 0.f;
+#pragma unroll
+    for (int pp = 0; pp < 15; pp++) {
+        if (pp >= col) {
+            const float xp = xs[pp];
+#pragma unroll
+            for (int q = pp + 1; q < 16; q++) xs[q] = fmaf(-M32[q * kBS + pp], xp, xs[q]);
+        }
+    }
+    float* DI32 = fptr(MS, MS_DI32) + J * 16 * kBS;
+#pragma unroll
+    for (int q = 0; q < 16; q++) DI32[q * kBS + col] = xs[q];
+    __syncwarp();
+    const int hf = c.lane >> 4, q0 = 8 * hf;
+    const float* Ai = fptr(MS, MS_DI32) + (2 * c.warp) * 16 * kBS;
+    const float* Bi = Ai + 16 * kBS;
+    const float* Cb = fptr(MS, MS_C32) + c.warp * 16 * kBS;
+    float acol[16];
+#pragma unroll
+    for (int m = 0; m < 16; m++) acol[m] = Ai[m * kBS + col];
+    float f[8];
+#pragma unroll
+    for (int kq = 0; kq < 8; kq++) {
+        float x = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; m += 4) {
+            const float4 cr = *reinterpret_cast<const float4*>(Cb + (q0 + kq) * kBS + m);
+            x = fmaf(cr.x, acol[m], x);
+            x = fmaf(cr.y, acol[m + 1], x);
+            x = fmaf(cr.z, acol[m + 2], x);
+            x = fmaf(cr.w, acol[m + 3], x);
+        }
+        f[kq] = x;
+    }
+    float fc[16];
+#pragma unroll
+    for (int kq = 0; kq < 8; kq++) {
+        const float o = __shfl_xor_sync(0xffffffffu, f[kq], 16);
+        fc[kq] = hf ? o : f[kq];
+        fc[8 + kq] = hf ? f[kq] : o;
+    }
+    float* Eb = fptr(MS, MS_E32) + c.warp * 16 * kBS;
+#pragma unroll
+    for (int kq = 0; kq < 8; kq++) {
+        float x = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; m += 4) {
+            const float4 br = *reinterpret_cast<const float4*>(Bi + (q0 + kq) * kBS + m);
+            x = fmaf(br.x, fc[m], x);
+            x = fmaf(br.y, fc[m + 1], x);
+            x = fmaf(br.z, fc[m + 2], x);
+            x = fmaf(br.w, fc[m + 3], x);
+        }
+        Eb[(q0 + kq) * kBS + col] = -x;
+    }
+}
+
+// (6b) the tile [Dinv ; Dinv] (K-major, 128 rows; read MN-major it is [Dinv^T | Dinv^T])
+__device__ __forceinline__ void write_dinv(Ctx& c, unsigned char* MS, unsigned char* DINV)
+{
+    const int t = c.trow & 63, J = t >> 4;
+    const float* DI32 = fptr(MS, MS_DI32) + (J * 16 + (t & 15)) * kBS;
+    const float* E32 = fptr(MS, MS_E32) + ((J >> 1) * 16 + (t & 15)) * kBS;
+#pragma unroll
+    for (int h2 = 0; h2 < 2; h2++) {
+        const int cg = 2 * c.wh + h2;
+        const float* src = (cg == J) ? DI32 : ((J & 1) && cg == J - 1) ? E32 : nullptr;
+        float v16[16];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            const float4 x = src ? *reinterpret_cast<const float4*>(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v16[e] = x.x; v16[e + 1] = x.y; v16[e + 2] = x.z; v16[e + 3] = x.w;
+        }
+        st16_bf16(DINV, c.trow, cg, v16);
+    }
+}
+
+// The delta front after the level product: assemble P (into the hi/lo tile Pt) and M = diag(beta) K
+// (L part into LR block 0, diagonal and coupling 16-blocks into MS, optionally K strictly below the diagonal,
+// packed, into KP), invert the 32-blocks, write [Dinv ; Dinv], run [N | X0] = Dinv [L | R] and
+// [Util | W] = X0 - N X0 (both copies in TMEM lanes 0..63 and 64..127).  R was written by the operand step.
+// Returns false on an abort.
+template <bool DELTA>
+__device__ bool front_solve(Ctx& c, const CbParams& p, unsigned char* NEARb, unsigned char* Pt, unsigned char* LR,
+                            unsigned char* LRL, unsigned char* MS, unsigned char* DINV, unsigned char* NA,
+                            unsigned char* X0, float* KP)
+{
+    Small& S = *c.S;
+    const int t = c.trow & 63, isK = c.trow >> 6, I = t >> 4;
+    {
+        float v[32];
+        assemble_row(c, reinterpret_cast<const float*>(NEARb), v);
+        if (!isK) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; h2++) {
+                float w16[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) w16[e] = v[16 * h2 + e];
+                st16_split(Pt, Pt + 8192, t, 2 * c.wh + h2, w16);
+            }
+        } else if (DELTA) {
+            const float bet = S.beta[t];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; h2++) {
+                const int cg = 2 * c.wh + h2;
+                float m16[16], l16[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    m16[e] = bet * v[16 * h2 + e];
+                    l16[e] = (I >= 2 && cg < 2) ? m16[e] : 0.f;
+                }
+                st16_bf16(LR, t, cg, l16);
+                float* f32 = nullptr;
+                if (cg == I) f32 = fptr(MS, MS_M32) + (I * 16 + (t & 15)) * kBS;
+                else if ((I & 1) && cg == I - 1) f32 = fptr(MS, MS_C32) + ((I >> 1) * 16 + (t & 15)) * kBS;
+                if (f32) {
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4*>(f32 + e) = make_float4(m16[e], m16[e + 1], m16[e + 2], m16[e + 3]);
+                }
+                if (KP) {
+#pragma unroll
+                    for (int e = 0; e < 16; e++) {
+                        const int s = 16 * cg + e;
+                        if (s < t) KP[t * (t - 1) / 2 + s] = v[16 * h2 + e];
+                    }
+                }
+            }
+        }
+    }
+    if (!DELTA) return true;
+    bar_all();
+    solve_blocks(c, MS);
+    bar_all();
+    write_dinv(c, MS, DINV);
+    smem_to_tc();
+    if (c.r == 0) {
+        const uint32_t dinv = smem_u32(DINV);
+        mma_tiles(c.tbase + TM_NX, dinv, false, 0, 0, smem_u32(LR), true, 8192, 0, 4,
+                  idesc_bf16(128, 192, false, true), false);
+        mma_tiles(c.tbase + TM_NX + 64, dinv, false, 0, 0, smem_u32(LRL), true, 8192, 0, 4,
+                  idesc_bf16(128, 128, false, true), true);
+        mma_commit(&S.mma);
+    }
+    if (!mma_wait(c, p)) return false;
+    // -N -> [-N ; -N] (K-major A); X0 -> hi/lo MN-major B blocks.  Twelve 16-column groups of token t:
+    // groups 0..5 from lanes 0..63, 6..11 from their copy in lanes 64..127.
+    {
+        const int gb = (isK ? 6 : 0) + 3 * c.wh;
+#pragma unroll
+        for (int gg = 0; gg < 3; gg++) {
+            const int g = gb + gg;
+            float v[16];
+            tmem_ld16(c.tl + TM_NX + 16 * g, v);
+            tmem_wait_ld();
+            if (g < 4) {
+#pragma unroll
+                for (int e = 0; e < 16; e++) v[e] = -v[e];
+                st16_bf16(NA, t, g, v);
+                st16_bf16(NA, 64 + t, g, v);
+            } else {
+                const int xg = g - 4;
+                const uint32_t blk = (uint32_t)(xg >> 2) * 8192u;
+                st16_split(X0 + blk, X0 + 16384 + blk, t, xg & 3, v);
+            }
+        }
+    }
+    smem_to_tc();
+    if (c.r == 0) {
+        const uint32_t id = idesc_bf16(128, 128, false, true);
+        mma_tiles(c.tbase + TM_UT, smem_u32(NA), false, 0, 0, smem_u32(X0), true, 8192, 0, 4, id, true);
+        mma_tiles(c.tbase + TM_UT, smem_u32(NA), false, 0, 0, smem_u32(X0 + 16384), true, 8192, 0, 4, id, true);
+        mma_commit(&S.mma);
+    }
+    return mma_wait(c, p);
+}
+
+// the operand step's R = [beta V | beta Btil] rows (thread t = r & 63, channels / columns 16 cq ..): hi in LR
+// blocks 1, 2, lo in LRL blocks 0, 1
+__device__ __forceinline__ void write_R(Ctx& c, unsigned char* LR, unsigned char* LRL)
+{
+    Small& S = *c.S;
+    const int t = c.r & 63, cq = c.r >> 6;
+    const float bet = S.beta[t], Gt = S.G[t];
+    float vv[16], bv[16], y[16];
+    ld16_bf16(c.sm + OFF_STAGE + ST_V, t, cq, vv);
+    ld16_bf16(c.sm + OFF_STAGE + ST_B, t, cq, bv);
+#pragma unroll
+    for (int e = 0; e < 16; e++) y[e] = bet * vv[e];
+    st16_split(LR + 8192, LRL, t, cq, y);
+#pragma unroll
+    for (int e = 0; e < 16; e++) y[e] = bet * bv[e] * fast_exp2(S.A2[16 * cq + e] * Gt);
+    st16_split(LR + 16384, LRL + 8192, t, cq, y);
+}
+
+// per-chunk inputs: g, beta (threads 0..127) and A2 of the chunk's head (threads 128..191)
+__device__ __forceinline__ void load_small(Ctx& c, const CbParams& p, int bb, int h, int t0)
+{
+    Small& S = *c.S;
+    const int r = c.r;
+    if (r < 64) {
+        const int t = t0 + r;
+        S.g[r] = t < p.T ? __bfloat162float(p.g[((size_t)bb * p.T + t) * p.H + h]) : 0.f;
+    } else if (r < 128) {
+        const int tt = r - 64, t = t0 + tt;
+        S.beta[tt] = (p.beta && t < p.T) ? __bfloat162float(p.beta[((size_t)bb * p.T + t) * p.H + h]) : 0.f;
+    } else if (r < 192) {
+        const int i = r - 128;
+        S.A2[i] = i < p.dk ? -expf(p.A_log[h * p.dk + i]) * kLog2e : 0.f;
+    }
+}
+
+__device__ __forceinline__ void issue_tma(const CbParams& p, Small& S, unsigned char* sm, int q)
+{
+    if (q == p.starve) return;   // failure-path test hook: this chunk's loads never arrive
+    const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
+    unsigned char* st = sm + OFF_STAGE;
+    mbar_arrive_expect_tx(&S.full, 4 * 8192);
+    tma_load_4d(st + ST_B, &p.tm_b, &S.full, 0, h, 64 * k, bb);
+    tma_load_4d(st + ST_C, &p.tm_c, &S.full, 0, h, 64 * k, bb);
+    tma_load_4d(st + ST_V, &p.tm_v, &S.full, 0, h, 64 * k, bb);
+    tma_load_4d(st + ST_DO, &p.tm_do, &S.full, 0, h, 64 * k, bb);
+}
+
+__device__ __forceinline__ void prefetch_tma(const CbParams& p, int q)
+{
+    const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
+    tma_prefetch_l2(&p.tm_b, 0, h, 64 * k, bb);
+    tma_prefetch_l2(&p.tm_c, 0, h, 64 * k, bb);
+    tma_prefetch_l2(&p.tm_v, 0, h, 64 * k, bb);
+    tma_prefetch_l2(&p.tm_do, 0, h, 64 * k, bb);
+}
+
+// kernel set-up shared by prep and grad; returns the context
+__device__ __forceinline__ Ctx setup(unsigned char* smem_raw, const CbParams& p)
+{
+    Ctx c;
+    c.sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    c.X = c.sm + OFF_X;
+    c.S = reinterpret_cast<Small*>(c.sm + OFF_SMALL);
+    c.KT = reinterpret_cast<Tab*>(c.sm + OFF_TAB);
+    c.ALPHA = reinterpret_cast<float*>(c.sm + OFF_ALPHA);
+    c.YB = reinterpret_cast<float*>(c.sm + OFF_YB);
+    c.r = threadIdx.x;
+    c.warp = c.r >> 5;
+    c.lane = c.r & 31;
+    c.q4 = c.warp & 3;
+    c.wh = c.warp >> 2;
+    c.trow = c.r & 127;
+    c.mma_phase = 0;
+    Small& S = *c.S;
+    if (c.r == 0) {
+        mbar_init(&S.full, 1);
+        mbar_init(&S.mma, 1);
+        S.abort = 0;
+        fence_mbar_init();
+    }
+    if (c.warp == 0) tmem_alloc(&S.tmem_base, TM_COLS);
+    if (c.r == 0) {
+        tma_prefetch_desc(&p.tm_b); tma_prefetch_desc(&p.tm_c); tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    c.tbase = S.tmem_base;
+    c.tl = c.tbase + ((uint32_t)(c.q4 * 32) << 16);
+    return c;
+}
+
+__device__ __forceinline__ void teardown(Ctx& c, const CbParams& p, int issued_q, uint32_t full_phase)
+{
+    // after an abort, let the copy still in flight land before exiting
+    if (c.r == 0 && *(volatile uint32_t*)&c.S->abort && issued_q >= 0 && issued_q != p.starve)
+        mbar_wait(&c.S->full, full_phase, nullptr, p.wait_ns);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (c.warp == 0) tmem_dealloc(c.tbase, TM_COLS);
+}
+
+// ================================================================= pass 1: prep
+template <bool DELTA>
+__global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_constant__ CbParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    Ctx c = setup(smem_raw, p);
+    Small& S = *c.S;
+    unsigned char* X = c.X;
+    uint32_t full_phase = 0;
+    int q = blockIdx.x;
+    int pending = -1;   // chunk whose loads are in flight
+    if (c.r == 0 && q < p.nq) { issue_tma(p, S, c.sm, q); pending = q; }
+    for (; q < p.nq; q += gridDim.x) {
+        const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
+        load_small(c, p, bb, h, 64 * k);
+        if (c.r == 0 && q + (int)gridDim.x < p.nq) prefetch_tma(p, q + gridDim.x);
+        if (c.warp == 0) wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns);
+        bar_all();
+        if (*(volatile uint32_t*)&S.abort) break;
+        full_phase ^= 1;
+        pending = -1;
+        front_scan(c);
+        bar_all();
+        const int t = c.r & 63, cq = c.r >> 6;
+        if constexpr (!DELTA) {
+            // [Bhat | Ctil] hi, lo: natural [t][i] tiles, read MN-major as [Bhat^T ; Ctil^T]
+            float bv[16], cv[16], y[16], z[16];
+            ld16_bf16(c.sm + OFF_STAGE + ST_B, t, cq, bv);
+            ld16_bf16(c.sm + OFF_STAGE + ST_C, t, cq, cv);
+            const float Gt = S.G[t], G63 = S.G[63];
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+                const float a2 = S.A2[16 * cq + e];
+                y[e] = bv[e] * fast_exp2(a2 * (G63 - Gt));
+                z[e] = cv[e] * fast_exp2(a2 * Gt);
+            }
+            st16_split(X + pl::GA, X + pl::GA + 16384, t, cq, y);
+            st16_split(X + pl::GA + 8192, X + pl::GA + 24576, t, cq, z);
+            smem_to_tc();
+            if (c.r == 0) {
+                // [Bhat^T V | Bhat^T dO ; Ctil^T V | Ctil^T dO]
+                const uint32_t id = idesc_bf16(128, 128, true, true);
+                const uint32_t vd = smem_u32(c.sm + OFF_STAGE + ST_V);
+                mma_tiles(c.tbase, smem_u32(X + pl::GA), true, 8192, 0, vd, true, 8192, 0, 4, id, false);
+                mma_tiles(c.tbase, smem_u32(X + pl::GA + 16384), true, 8192, 0, vd, true, 8192, 0, 4, id, true);
+                mma_commit(&S.mma);
+            }
+            if (!mma_wait(c, p)) break;
+            // Delta = rows 0..63, columns 0..63; Y = rows 64..127, columns 64..127
+            {
+                const int i = c.trow & 63;
+                float* dst = (c.trow < 64 ? p.dlt : p.ych) + ((size_t)q * 64 + i) * 64;
+                const uint32_t col0 = c.trow < 64 ? 0u : 64u;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    float v[16];
+                    tmem_ld16(c.tl + col0 + 32 * c.wh + 16 * h2, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4*>(dst + 32 * c.wh + 16 * h2 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                }
+                if (c.r < 64) p.ec[(size_t)q * 64 + c.r] = c.KT->EC[c.r];
+            }
+        } else {
+            front_operands(c, X + pl::A1, X + pl::B1, true);
+            write_R(c, X + pl::LR, X + pl::LRL);
+            {
+                // Bhat natural [s][i] (read MN-major as Bhat^T)
+                float bv[16], y[16];
+                ld16_bf16(c.sm + OFF_STAGE + ST_B, t, cq, bv);
+                const float Gt = S.G[t], G63 = S.G[63];
+#pragma unroll
+                for (int e = 0; e < 16; e++) y[e] = bv[e] * fast_exp2(S.A2[16 * cq + e] * (G63 - Gt));
+                st16_split(X + pl::BH, X + pl::BH + 8192, t, cq, y);
+            }
+            smem_to_tc();
+            if (c.r == 0) {
+                issue_level(c.tbase, X + pl::A1, X + pl::B1);
+                mma_commit(&S.mma);
+            }
+            front_near(c, fptr(X, pl::NEAR), true);
+            bar_all();
+            if (!mma_wait(c, p)) break;
+            if (!front_solve<true>(c, p, X + pl::NEAR, X + pl::P, X + pl::LR, X + pl::LRL, X + pl::MS, X + pl::DINV,
+                                   X + pl::NA, X + pl::X0, nullptr))
+                break;
+            // [Util | W] -> [W | Util] hi/lo MN-major B blocks (W block 0, Util block 1)
+            {
+                const bool isW = c.trow < 64;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int cg = 2 * c.wh + h2;
+                    float v[16];
+                    tmem_ld16(c.tl + (isW ? TM_W : TM_UT) + 16 * cg, v);
+                    tmem_wait_ld();
+                    const uint32_t blk = isW ? 0u : 8192u;
+                    st16_split(X + pl::WU + blk, X + pl::WU + 16384 + blk, c.trow & 63, cg, v);
+                }
+            }
+            smem_to_tc();
+            if (c.r == 0) {
+                // [Phi' | Delta] = Bhat^T [W | Util] (TMEM 288..415), P W (416..479)
+                const uint32_t idA = idesc_bf16(128, 128, true, true);
+                const uint32_t bh = smem_u32(X + pl::BH), wu = smem_u32(X + pl::WU);
+                mma_tiles(c.tbase + 288, bh, true, 8192, 0, wu, true, 8192, 0, 4, idA, false);
+                mma_tiles(c.tbase + 288, bh, true, 8192, 0, wu + 16384, true, 8192, 0, 4, idA, true);
+                mma_tiles(c.tbase + 288, bh + 8192, true, 8192, 0, wu, true, 8192, 0, 4, idA, true);
+                const uint32_t idB = idesc_bf16(128, 64, false, true);
+                const uint32_t pp = smem_u32(X + pl::P);
+                mma_tiles(c.tbase + 416, pp, false, 0, 0, wu, true, 8192, 0, 4, idB, false);
+                mma_tiles(c.tbase + 416, pp, false, 0, 0, wu + 16384, true, 8192, 0, 4, idB, true);
+                mma_tiles(c.tbase + 416, pp + 8192, false, 0, 0, wu, true, 8192, 0, 4, idB, true);
+                mma_commit(&S.mma);
+            }
+            if (!mma_wait(c, p)) break;
+            // lanes 0..63: Phi = diag(E) - Bhat^T W and Delta out; lanes 64..127: Qc = Ctil - P W (hi/lo, natural)
+            if (c.trow < 64) {
+                const int i = c.trow;
+                float* dphi = p.phi + ((size_t)q * 64 + i) * 64;
+                float* ddl = p.dlt + ((size_t)q * 64 + i) * 64;
+                const float eci = c.KT->EC[i];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int c0 = 32 * c.wh + 16 * h2;
+                    float a[16], b[16];
+                    tmem_ld16(c.tl + 288 + c0, a);
+                    tmem_ld16(c.tl + 352 + c0, b);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; e++) a[e] = (c0 + e == i ? eci : 0.f) - a[e];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4) {
+                        *reinterpret_cast<float4*>(dphi + c0 + e) = make_float4(a[e], a[e + 1], a[e + 2], a[e + 3]);
+                        *reinterpret_cast<float4*>(ddl + c0 + e) = make_float4(b[e], b[e + 1], b[e + 2], b[e + 3]);
+                    }
+                }
+            } else {
+                // the P W rows sit in lanes 0..63; the lanes 64..127 threads read them through the copy below
+            }
+            bar_all();
+            // Qc rows: token t in lanes 0..63 of the P W accumulator; threads of lanes 0..63 write them
+            if (c.trow < 64) {
+                const int tt = c.trow;
+                float cv[16];
+                const float Gt = S.G[tt];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int cg = 2 * c.wh + h2;
+                    float pw[16];
+                    tmem_ld16(c.tl + 416 + 16 * cg, pw);
+                    tmem_wait_ld();
+                    ld16_bf16(c.sm + OFF_STAGE + ST_C, tt, cg, cv);
+                    float y[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e++) y[e] = cv[e] * fast_exp2(S.A2[16 * cg + e] * Gt) - pw[e];
+                    st16_split(X + pl::QC, X + pl::QC + 8192, tt, cg, y);
+                }
+            }
+            smem_to_tc();
+            if (c.r == 0) {
+                // Y = Qc^T dO (TMEM 96..159)
+                const uint32_t id = idesc_bf16(128, 64, true, true);
+                const uint32_t qc = smem_u32(X + pl::QC), dO = smem_u32(c.sm + OFF_STAGE + ST_DO);
+                mma_tiles(c.tbase + 96, qc, true, 8192, 0, dO, true, 8192, 0, 4, id, false);
+                mma_tiles(c.tbase + 96, qc + 8192, true, 8192, 0, dO, true, 8192, 0, 4, id, true);
+                mma_commit(&S.mma);
+            }
+            if (!mma_wait(c, p)) break;
+            if (c.trow < 64) {
+                const int i = c.trow;
+                float* dy = p.ych + ((size_t)q * 64 + i) * 64;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int c0 = 32 * c.wh + 16 * h2;
+                    float v[16];
+                    tmem_ld16(c.tl + 96 + c0, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4*>(dy + c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                }
+            }
+        }
+        // the stage is free: the next chunk's loads
+        tc_fence_before();
+        bar_all();
+        tc_fence_after();
+        if (q + (int)gridDim.x < p.nq) {
+            if (c.r == 0) issue_tma(p, S, c.sm, q + gridDim.x);
+            pending = q + gridDim.x;
+        }
+    }
+    teardown(c, p, pending, full_phase);
+}
+
+// ================================================================= pass 2: chain
+// One CTA per (unit, 16-column slab of the state), 256 threads: thread = (row i = r >> 2, columns
+// 16 slab + 4 (r & 3) .. + 3).  Forward: S_0 = h0, st[k] = S_k, S_{k+1} = Phi_k S_k + Delta_k.  Reverse:
+// dS = dhT, dst[k] = dS, dS <- Phi_k^T dS + Y_k; dh0 = dS.  The next chunk's records are loaded into registers
+// while the current step computes; Phi and the slab of S alternate between two shared-memory buffers, so one
+// barrier per step suffices.
+template <bool DELTA>
+__global__ void __launch_bounds__(256) chunk_chain_kernel(const __grid_constant__ CbParams p)
+{
+    __shared__ __align__(16) float Ph[2][64][68];
+    __shared__ __align__(16) float Sv[2][64][20];
+    const int u = blockIdx.x >> 2, slab = blockIdx.x & 3;
+    const int r = threadIdx.x, i = r >> 2, jq = r & 3, j0 = 16 * slab + 4 * jq;
+    const int dk = p.dk, dv = p.dv_, nk = p.nchunks;
+    const size_t qb = (size_t)u * nk;
+    float4 pf[4];
+    auto load_phi = [&](int k) {
+        const float4* src = reinterpret_cast<const float4*>(p.phi + (qb + k) * 4096);
+#pragma unroll
+        for (int m = 0; m < 4; m++) pf[m] = src[r + 256 * m];
+    };
+    auto store_phi = [&](int buf) {
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const int e = r + 256 * m, row = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4*>(&Ph[buf][row][c4]) = pf[m];
+        }
+    };
+    auto rec4 = [&](const float* base, int k) {
+        return *reinterpret_cast<const float4*>(base + (qb + k) * 4096 + i * 64 + j0);
+    };
+    float s[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const int j = j0 + e;
+        s[e] = (p.h0 && i < dk && j < dv) ? p.h0[((size_t)u * dk + i) * dv + j] : 0.f;
+    }
+    // ---- forward
+    if (DELTA) { load_phi(0); store_phi(0); }
+    float4 d = rec4(p.dlt, 0);
+    float ecv = DELTA ? 0.f : p.ec[qb * 64 + i];
+    for (int k = 0; k < nk; k++) {
+        *reinterpret_cast<float4*>(p.st + (qb + k) * 4096 + i * 64 + j0) = make_float4(s[0], s[1], s[2], s[3]);
+        const bool more = k + 1 < nk;
+        float4 dn = d;
+        float ecn = ecv;
+        if (more) {
+            dn = rec4(p.dlt, k + 1);
+            if (!DELTA) ecn = p.ec[(qb + k + 1) * 64 + i];
+        }
+        if (DELTA) {
+            *reinterpret_cast<float4*>(&Sv[k & 1][i][4 * jq]) = make_float4(s[0], s[1], s[2], s[3]);
+            if (more) load_phi(k + 1);
+            __syncthreads();
+            float a[4] = {d.x, d.y, d.z, d.w};
+            const float* prow = Ph[k & 1][i];
+#pragma unroll 8
+            for (int m = 0; m < 64; m++) {
+                const float ph = prow[m];
+                const float4 sv = *reinterpret_cast<const float4*>(&Sv[k & 1][m][4 * jq]);
+                a[0] = fmaf(ph, sv.x, a[0]);
+                a[1] = fmaf(ph, sv.y, a[1]);
+                a[2] = fmaf(ph, sv.z, a[2]);
+                a[3] = fmaf(ph, sv.w, a[3]);
+            }
+            if (more) store_phi((k + 1) & 1);
+#pragma unroll
+            for (int e = 0; e < 4; e++) s[e] = a[e];
+        } else {
+            s[0] = fmaf(ecv, s[0], d.x);
+            s[1] = fmaf(ecv, s[1], d.y);
+            s[2] = fmaf(ecv, s[2], d.z);
+            s[3] = fmaf(ecv, s[3], d.w);
+        }
+        d = dn;
+        ecv = ecn;
+    }
+    // ---- reverse
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const int j = j0 + e;
+        s[e] = (p.dhT && i < dk && j < dv) ? p.dhT[((size_t)u * dk + i) * dv + j] : 0.f;
+    }
+    __syncthreads();
+    if (DELTA) { load_phi(nk - 1); store_phi((nk - 1) & 1); }
+    float4 y = rec4(p.ych, nk - 1);
+    ecv = DELTA ? 0.f : p.ec[(qb + nk - 1) * 64 + i];
+    for (int k = nk - 1; k >= 0; k--) {
+        *reinterpret_cast<float4*>(p.dst + (qb + k) * 4096 + i * 64 + j0) = make_float4(s[0], s[1], s[2], s[3]);
+        const bool more = k > 0;
+        float4 yn = y;
+        float ecn = ecv;
+        if (more) {
+            yn = rec4(p.ych, k - 1);
+            if (!DELTA) ecn = p.ec[(qb + k - 1) * 64 + i];
+        }
+        if (DELTA) {
+            // buffers indexed by k & 1 as in the forward (k descends: the next step uses the other buffer)
+            *reinterpret_cast<float4*>(&Sv[k & 1][i][4 * jq]) = make_float4(s[0], s[1], s[2], s[3]);
+            if (more) load_phi(k - 1);
+            __syncthreads();
+            // (Phi^T dS)[i][j] = sum_m Phi[m][i] dS[m][j]
+            float a[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll 8
+            for (int m = 0; m < 64; m++) {
+                const float pv = Ph[k & 1][m][i];
+                const float4 sv = *reinterpret_cast<const float4*>(&Sv[k & 1][m][4 * jq]);
+                a[0] = fmaf(pv, sv.x, a[0]);
+                a[1] = fmaf(pv, sv.y, a[1]);
+                a[2] = fmaf(pv, sv.z, a[2]);
+                a[3] = fmaf(pv, sv.w, a[3]);
+            }
+            if (more) store_phi((k - 1) & 1);
+#pragma unroll
+            for (int e = 0; e < 4; e++) s[e] = a[e];
+        } else {
+            s[0] = fmaf(ecv, s[0], y.x);
+            s[1] = fmaf(ecv, s[1], y.y);
+            s[2] = fmaf(ecv, s[2], y.z);
+            s[3] = fmaf(ecv, s[3], y.w);
+        }
+        y = yn;
+        ecv = ecn;
+    }
+    if (p.dh0 && i < dk) {
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const int j = j0 + e;
+            if (j < dv) p.dh0[((size_t)u * dk + i) * dv + j] = s[e];
+        }
+    }
+}
+
+// ================================================================= pass 3: gradients
+template <bool DELTA>
+__global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_constant__ CbParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    Ctx c = setup(smem_raw, p);
+    Small& S = *c.S;
+    unsigned char* X = c.X;
+    const unsigned char* sB = c.sm + OFF_STAGE + ST_B;
+    const unsigned char* sC = c.sm + OFF_STAGE + ST_C;
+    const unsigned char* sV = c.sm + OFF_STAGE + ST_V;
+    const unsigned char* sDO = c.sm + OFF_STAGE + ST_DO;
+    uint32_t full_phase = 0;
+    int q = blockIdx.x;
+    int pending = -1;
+    if (c.r == 0 && q < p.nq) issue_tma(p, S, c.sm, q);
+    if (q < p.nq) pending = q;
+    const int trow = c.trow, tt = trow & 63, isK = trow >> 6, wh = c.wh;
+    for (; q < p.nq; q += gridDim.x) {
+        const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
+        const int t0 = 64 * k, L = min(64, p.T - t0);
+        load_small(c, p, bb, h, t0);
+        if (c.r == 0 && q + (int)gridDim.x < p.nq) prefetch_tma(p, q + gridDim.x);
+        if (c.warp == 0) wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns);
+        bar_all();
+        if (*(volatile uint32_t*)&S.abort) break;
+        full_phase ^= 1;
+        pending = -1;
+        front_scan(c);
+        bar_all();
+        const int t = c.r & 63, cq = c.r >> 6;
+
+        // ---- front: level operands, R, the level product, near pairs, P (and M, the solve)
+        front_operands(c, X + gl::A1, X + gl::B1, true);
+        if (DELTA) write_R(c, X + gl::LR, X + gl::LRL);
+        smem_to_tc();
+        if (c.r == 0) {
+            issue_level(c.tbase, X + gl::A1, X + gl::B1);
+            mma_commit(&S.mma);
+        }
+        front_near(c, fptr(X, gl::NEAR), DELTA);
+        bar_all();
+        if (!mma_wait(c, p)) break;
+        if (!front_solve<DELTA>(c, p, X + gl::NEAR, X + gl::P, X + gl::LR, X + gl::LRL, X + gl::MS, X + gl::DINV,
+                                X + gl::NA, X + gl::X0, DELTA ? fptr(X, gl::KP) : nullptr))
+            break;
+        if (!DELTA) bar_all();
+
+        // ---- S, dS' of the chunk (fp32 from the chain) -> hi/lo tiles [i][j]; sum_j dS'[i][j] S[i][j]
+        {
+            const float* srow = p.st + ((size_t)q * 64 + t) * 64 + 16 * cq;
+            const float* drow = p.dst + ((size_t)q * 64 + t) * 64 + 16 * cq;
+            float sv[16], dv16[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 a = *reinterpret_cast<const float4*>(srow + e);
+                const float4 b = *reinterpret_cast<const float4*>(drow + e);
+                sv[e] = a.x; sv[e + 1] = a.y; sv[e + 2] = a.z; sv[e + 3] = a.w;
+                dv16[e] = b.x; dv16[e + 1] = b.y; dv16[e + 2] = b.z; dv16[e + 3] = b.w;
+            }
+            float sdp = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; e++) sdp = fmaf(dv16[e], sv[e], sdp);
+            S.sd[cq][t] = sdp;
+            st16_split(X + gl::U + 8192, X + gl::U + 24576, t, cq, sv);
+            st16_split(X + gl::DSN, X + gl::DSN + 8192, t, cq, dv16);
+            if (!DELTA) {
+                // U = V: the value tile copied into U_hi, U_lo = 0
+                float vv[16];
+                ld16_bf16(sV, t, cq, vv);
+                st16_bf16(X + gl::U, t, cq, vv);
+                zero16(X + gl::U + 16384, t, cq);
+            }
+        }
+        if (DELTA) {
+            // -W (plain bf16, K-major [t][i]) for U = Util - W S
+            if (!isK) {
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int cg = 2 * wh + h2;
+                    float v[16];
+                    tmem_ld16(c.tl + TM_W + 16 * cg, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; e++) v[e] = -v[e];
+                    st16_bf16(X + gl::NW, tt, cg, v);
+                }
+            }
+            smem_to_tc();
+            if (c.r == 0) {
+                const uint32_t id = idesc_bf16(128, 64, false, true);
+                const uint32_t nw = smem_u32(X + gl::NW), sh = smem_u32(X + gl::U + 8192);
+                mma_tiles(c.tbase + TM_UT, nw, false, 0, 0, sh, true, 8192, 0, 4, id, true);
+                mma_tiles(c.tbase + TM_UT, nw, false, 0, 0, sh + 16384, true, 8192, 0, 4, id, true);
+                mma_commit(&S.mma);
+            }
+            if (!mma_wait(c, p)) break;
+            // U -> hi/lo [s][j]
+            if (!isK) {
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int cg = 2 * wh + h2;
+                    float v[16];
+                    tmem_ld16(c.tl + TM_UT + 16 * cg, v);
+                    tmem_wait_ld();
+                    st16_split(X + gl::U, X + gl::U + 16384, tt, cg, v);
+                }
+            }
+        }
+        // Bhat natural [t][i] hi/lo (K-major A of B^ dS')
+        {
+            float bv[16], y[16];
+            ld16_bf16(sB, t, cq, bv);
+            const float Gt = S.G[t], G63 = S.G[63];
+#pragma unroll
+            for (int e = 0; e < 16; e++) y[e] = bv[e] * fast_exp2(S.A2[16 * cq + e] * (G63 - Gt));
+            st16_split(X + gl::BHH, X + gl::BHL, t, cq, y);
+        }
+        smem_to_tc();
+        // ---- dU = P^T dO + Bhat dS'  (TMEM 288)
+        if (c.r == 0) {
+            const uint32_t idA = idesc_bf16(128, 64, true, true), idB = idesc_bf16(128, 64, false, true);
+            const uint32_t pt = smem_u32(X + gl::P), dO = smem_u32(sDO);
+            const uint32_t bh = smem_u32(X + gl::BHH), bl = smem_u32(X + gl::BHL), dsn = smem_u32(X + gl::DSN);
+            mma_tiles(c.tbase + 288, pt, true, 8192, 0, dO, true, 8192, 0, 4, idA, false);
+            mma_tiles(c.tbase + 288, pt + 8192, true, 8192, 0, dO, true, 8192, 0, 4, idA, true);
+            mma_tiles(c.tbase + 288, bh, false, 0, 0, dsn, true, 8192, 0, 4, idB, true);
+            mma_tiles(c.tbase + 288, bh, false, 0, 0, dsn + 8192, true, 8192, 0, 4, idB, true);
+            mma_tiles(c.tbase + 288, bl, false, 0, 0, dsn, true, 8192, 0, 4, idB, true);
+            mma_commit(&S.mma);
+        }
+        if (!mma_wait(c, p)) break;
+        const size_t tokrow = ((size_t)bb * p.T + t0 + tt) * p.H + h;   // (b, t0 + tt, h) row of the token tensors
+        if (!DELTA) {
+            // dv = dU
+            if (!isK && tt < L) {
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int c0 = 32 * wh + 16 * h2;
+                    float v[16];
+                    tmem_ld16(c.tl + 288 + c0, v);
+                    tmem_wait_ld();
+                    __nv_bfloat16* dst = p.dv + tokrow * p.dv_ + c0;
+#pragma unroll
+                    for (int e = 0; e < 16; e += 8) {
+                        if (c0 + e < p.dv_) {
+                            uint4 w;
+                            w.x = pack_bf16(v[e], v[e + 1]); w.y = pack_bf16(v[e + 2], v[e + 3]);
+                            w.z = pack_bf16(v[e + 4], v[e + 5]); w.w = pack_bf16(v[e + 6], v[e + 7]);
+                            *reinterpret_cast<uint4*>(dst + e) = w;
+                        }
+                    }
+                }
+            }
+        } else {
+            // dU -> hi/lo [s][j] (MN-major B)
+            if (!isK) {
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int cg = 2 * wh + h2;
+                    float v[16];
+                    tmem_ld16(c.tl + 288 + 16 * cg, v);
+                    tmem_wait_ld();
+                    st16_split(X + gl::DU, X + gl::DU + 8192, tt, cg, v);
+                }
+            }
+            smem_to_tc();
+            // Z = dU - N^T dU (accumulated onto dU)
+            if (c.r == 0) {
+                const uint32_t id = idesc_bf16(128, 64, true, true);
+                const uint32_t na = smem_u32(X + gl::NA), du = smem_u32(X + gl::DU);
+                mma_tiles(c.tbase + 288, na, true, 8192, 0, du, true, 8192, 0, 4, id, true);
+                mma_tiles(c.tbase + 288, na, true, 8192, 0, du + 8192, true, 8192, 0, 4, id, true);
+                mma_commit(&S.mma);
+            }
+            if (!mma_wait(c, p)) break;
+            if (!isK) {
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int cg = 2 * wh + h2;
+                    float v[16];
+                    tmem_ld16(c.tl + 288 + 16 * cg, v);
+                    tmem_wait_ld();
+                    st16_split(X + gl::Z, X + gl::Z + 8192, tt, cg, v);
+                }
+            }
+            smem_to_tc();
+            // dR = Dinv^T Z (TMEM 352; lanes 64..127 hold a copy)
+            if (c.r == 0) {
+                const uint32_t id = idesc_bf16(128, 64, true, true);
+                const uint32_t di = smem_u32(X + gl::DINV), z = smem_u32(X + gl::Z);
+                mma_tiles(c.tbase + 352, di, true, 8192, 0, z, true, 8192, 0, 4, id, false);
+                mma_tiles(c.tbase + 352, di, true, 8192, 0, z + 8192, true, 8192, 0, 4, id, true);
+                mma_commit(&S.mma);
+            }
+            if (!mma_wait(c, p)) break;
+            // dR: lanes 0..63 -> dv = beta dR (global) and dR hi/lo rows of the A operands [dO ; dR_hi] and
+            // [0 ; dR_lo]; lanes 64..127 -> the dO copy and zero rows, and sum_j dR[t][j] V[t][j]
+            {
+                const float bet = S.beta[tt];
+                float part = 0.f;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int cg = 2 * wh + h2, c0 = 16 * cg;
+                    float v[16];
+                    tmem_ld16(c.tl + 352 + c0, v);
+                    tmem_wait_ld();
+                    if (!isK) {
+                        st16_split(X + gl::DOR + 8192, X + gl::ZR + 8192, tt, cg, v);
+                        if (tt < L) {
+                            __nv_bfloat16* dst = p.dv + tokrow * p.dv_ + c0;
+#pragma unroll
+                            for (int e = 0; e < 16; e += 8) {
+                                if (c0 + e < p.dv_) {
+                                    uint4 w;
+                                    w.x = pack_bf16(bet * v[e], bet * v[e + 1]);
+                                    w.y = pack_bf16(bet * v[e + 2], bet * v[e + 3]);
+                                    w.z = pack_bf16(bet * v[e + 4], bet * v[e + 5]);
+                                    w.w = pack_bf16(bet * v[e + 6], bet * v[e + 7]);
+                                    *reinterpret_cast<uint4*>(dst + e) = w;
+                                }
+                            }
+                        }
+                    } else {
+                        float vv[16];
+                        ld16_bf16(sV, tt, cg, vv);
+#pragma unroll
+                        for (int e = 0; e < 16; e++) part = fmaf(v[e], vv[e], part);
+                        // dO row copy (same row, same swizzle) and the zero rows
+                        const uint32_t o0 = sw128(tt, c0), o1 = sw128(tt, c0 + 8);
+                        *reinterpret_cast<uint4*>(X + gl::DOR + o0) = *reinterpret_cast<const uint4*>(sDO + o0);
+                        *reinterpret_cast<uint4*>(X + gl::DOR + o1) = *reinterpret_cast<const uint4*>(sDO + o1);
+                        zero16(X + gl::ZR, tt, cg);
+                    }
+                }
+                if (isK) S.rs[0][wh][tt] = part;
+            }
+        }
+        smem_to_tc();
+        // ---- [dO ; dR] [U | S]^T (TMEM 0..127) and dBhat = U dS'^T (TMEM 128..191)
+        if (c.r == 0) {
+            const uint32_t id8 = idesc_bf16(128, 128, false, false), id9 = idesc_bf16(128, 64, false, false);
+            const uint32_t uh = smem_u32(X + gl::U), ul = uh + 16384, dsn = smem_u32(X + gl::DSN);
+            const uint32_t ah = DELTA ? smem_u32(X + gl::DOR) : smem_u32(sDO);
+            mma_tiles(c.tbase + 0, ah, false, 0, 0, uh, false, 0, 0, 4, id8, false);
+            mma_tiles(c.tbase + 0, ah, false, 0, 0, ul, false, 0, 0, 4, id8, true);
+            if (DELTA) mma_tiles(c.tbase + 0, smem_u32(X + gl::ZR), false, 0, 0, uh, false, 0, 0, 4, id8, true);
+            mma_tiles(c.tbase + 128, uh, false, 0, 0, dsn, false, 0, 0, 4, id9, false);
+            mma_tiles(c.tbase + 128, uh, false, 0, 0, dsn + 8192, false, 0, 0, 4, id9, true);
+            if (DELTA) mma_tiles(c.tbase + 128, ul, false, 0, 0, dsn, false, 0, 0, 4, id9, true);
+            mma_commit(&S.mma);
+        }
+        if (!mma_wait(c, p)) break;
+        // ---- dQ (lanes 0..63) and dK = -beta (dR U^T) below the diagonal (lanes 64..127): the 16-block level's
+        // operand A_d = [dQ | dK] by segments (fp16, K-major [t][seg], two 64-wide K blocks), the near entries in
+        // fp32; (delta) the rest of dbeta
+        {
+            const int I = tt >> 4;
+            const float bet = DELTA ? S.beta[tt] : 0.f;
+            float row[64];
+#pragma unroll
+            for (int g4 = 0; g4 < 4; g4++) {
+                float v[16];
+                tmem_ld16(c.tl + 16 * g4, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    const int s = 16 * g4 + e;
+                    row[s] = isK ? ((DELTA && s < tt) ? -bet * v[e] : 0.f) : (s <= tt ? v[e] : 0.f);
+                }
+            }
+            if (DELTA && isK) {
+                // dbeta_t = sum_j dR V - sum_i Btil (dR S^T) - sum_{s<t} (dR U^T) K   (dMm = -dR U^T)
+                float part = 0.f;
+                const float Gt = S.G[tt];
+                const float* KP = fptr(X, gl::KP);
+#pragma unroll
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int cg = 2 * wh + h2;
+                    float drs[16], dru[16], bv[16];
+                    tmem_ld16(c.tl + 64 + 16 * cg, drs);
+                    tmem_ld16(c.tl + 16 * cg, dru);
+                    tmem_wait_ld();
+                    ld16_bf16(sB, tt, cg, bv);
+#pragma unroll
+                    for (int e = 0; e < 16; e++) {
+                        const int s = 16 * cg + e;
+                        part -= bv[e] * fast_exp2(S.A2[s] * Gt) * drs[e];
+                        if (s < tt) part -= dru[e] * KP[tt * (tt - 1) / 2 + s];
+                    }
+                }
+                S.rs[1][wh][tt] = part;
+            }
+            // A_d row trow: segment I's columns (lo .. lo + 16 I) hold the row's values for s < 16 I
+            const int lo16 = seg_base(I) >> 4;
+#pragma unroll
+            for (int g4 = 0; g4 < 4; g4++) {
+                const int sgrp = 4 * wh + g4 - lo16;   // 16-column group of s this segment group holds
+                const bool valid = sgrp >= 0 && sgrp < I;
+                float v[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    const float x = sgrp == 0 ? row[e] : (sgrp == 1 ? row[16 + e] : row[32 + e]);
+                    v[e] = valid ? x : 0.f;
+                }
+                st16_f16(X + gl::AD + (uint32_t)wh * 16384u, trow, g4, v);
+            }
+            // near entries (same 16-block), by one of the row's two threads
+            if (wh == (I >> 1)) {
+                float* nd = fptr(X, gl::NEARD) + ((isK * 4 + I) * 16 + (tt & 15)) * 17;
+#pragma unroll
+                for (int e = 0; e < 16; e++)
+                    nd[e] = I == 0 ? row[e] : (I == 1 ? row[16 + e] : (I == 2 ? row[32 + e] : row[48 + e]));
+            }
+        }
+        // the 16-block level's operands again (their space was reused)
+        front_operands(c, X + gl::A1, X + gl::B1, true);
+        smem_to_tc();
+        if (c.r == 0) {
+            // dA1 = A_d B1 (TMEM 192..255): rows 0..63 -> dc, 64..127 -> db (row side)
+            mma_tiles(c.tbase + 192, smem_u32(X + gl::AD), false, 0, 16384, smem_u32(X + gl::B1), true, 8192, 0, 6,
+                      idesc_f16(128, 64, false, true), false);
+            // dB1 = A_d^T A1 (TMEM 256..319): rows = segments (column side)
+            mma_tiles(c.tbase + 256, smem_u32(X + gl::AD), true, 16384, 0, smem_u32(X + gl::A1), true, 8192, 0, 8,
+                      idesc_f16(128, 64, true, true), false);
+            mma_commit(&S.mma);
+        }
+        // ---- near pairs, reverse (fp32), thread = (token t, channels 16 cq ..): row side (P, K) and column side
+        float nc[16], nb[16], ng[16];
+        {
+            const float* ND = fptr(X, gl::NEARD);
+            const int J = t >> 4, tl16 = t & 15;
+            float cv[16], bv[16], al[16], ai[16];
+            ld16_bf16(sC, t, cq, cv);
+            ld16_bf16(sB, t, cq, bv);
+            const float Gt = S.G[t], dGa = Gt - S.G[8 * (t >> 3) + 3];
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+                al[e] = c.ALPHA[t * 64 + 16 * cq + e];
+                ai[e] = fast_exp2(-S.A2[16 * cq + e] * dGa);
+            }
+            float rP[16], rK[16], cP[16], cK[16];
+#pragma unroll
+            for (int e = 0; e < 16; e++) rP[e] = rK[e] = cP[e] = cK[e] = 0.f;
+            const bool unsafe = S.unsafe != 0;
+#pragma unroll 1
+            for (int sl = 0; sl < 16; sl++) {
+                const int s = 16 * J + sl;
+                if (sl <= tl16) {
+                    // row side: P[t][s], K[t][s] with column s
+                    const float wq = ND[((0 * 4 + J) * 16 + tl16) * 17 + sl];
+                    const float wk = DELTA ? ND[((1 * 4 + J) * 16 + tl16) * 17 + sl] : 0.f;
+                    if (!unsafe) {
+                        const bool cross = tl16 >= 8 && sl < 8;
+                        const float* yr = c.YB + s * 64 + 16 * cq;
+#pragma unroll
+                        for (int e = 0; e < 16; e++) {
+                            const float kap = cross ? c.KT->KAP[J][16 * cq + e] : 1.f;
+                            const float y = yr[e] * kap;
+                            rP[e] = fmaf(wq, y, rP[e]);
+                            rK[e] = fmaf(wk, y, rK[e]);
+                        }
+                    } else {
+                        float b8[16];
+                        ld16_bf16(sB, s, cq, b8);
+                        const float dG = Gt - S.G[s];
+#pragma unroll
+                        for (int e = 0; e < 16; e++) {
+                            const float y = b8[e] * exp2f(S.A2[16 * cq + e] * dG);
+                            rP[e] = fmaf(wq, y, rP[e]);
+                            rK[e] = fmaf(wk, y, rK[e]);
+                        }
+                    }
+                }
+                if (sl >= tl16) {
+                    // column side: P[s][t], K[s][t] with row s
+                    const float wq = ND[((0 * 4 + J) * 16 + sl) * 17 + tl16];
+                    const float wk = DELTA ? ND[((1 * 4 + J) * 16 + sl) * 17 + tl16] : 0.f;
+                    float cs[16], bs[16];
+                    ld16_bf16(sC, s, cq, cs);
+                    ld16_bf16(sB, s, cq, bs);
+                    if (!unsafe) {
+                        const bool cross = sl >= 8 && tl16 < 8;
+                        const float* as = c.ALPHA + s * 64 + 16 * cq;
+#pragma unroll
+                        for (int e = 0; e < 16; e++) {
+                            const float kap = cross ? c.KT->KAP[J][16 * cq + e] : 1.f;
+                            const float x = as[e] * kap;
+                            cP[e] = fmaf(wq, cs[e] * x, cP[e]);
+                            cK[e] = fmaf(wk, bs[e] * x, cK[e]);
+                        }
+                    } else {
+                        const float dG = S.G[s] - Gt;
+#pragma unroll
+                        for (int e = 0; e < 16; e++) {
+                            const float x = exp2f(S.A2[16 * cq + e] * dG);
+                            cP[e] = fmaf(wq, cs[e] * x, cP[e]);
+                            cK[e] = fmaf(wk, bs[e] * x, cK[e]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+                const float ra = unsafe ? 1.f : al[e], ca = unsafe ? 1.f : ai[e];
+                const float dl_c = ra * rP[e], dl_b = ra * rK[e], dr = ca * (cP[e] + cK[e]);
+                nc[e] = dl_c;
+                nb[e] = dl_b + dr;
+                ng[e] = cv[e] * dl_c + bv[e] * dl_b - bv[e] * dr;
+            }
+        }
+        bar_all();
+        if (!mma_wait(c, p)) break;
+        // ---- epilogue: dense terms (lanes 0..63), the b-side rows (lanes 64..127), the segments' column side
+        float* DC = fptr(X, gl::DC);
+        float* DB = fptr(X, gl::DB);
+        float* DG = fptr(X, gl::DG);
+        float* PB = fptr(X, gl::SEG + 24576);   // [64][64] dBhat Bhat, then G_t dGam
+        float* SEGv = fptr(X, gl::SEG);          // [96][64] dB1 h1
+        if (!isK) {
+            const int I = tt >> 4;
+            const float Gt = S.G[tt], G63 = S.G[63], Gref = I >= 1 ? S.G[16 * I - 1] : 0.f;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; h2++) {
+                const int cg = 2 * wh + h2, c0 = 16 * cg;
+                float dct[16], dbh[16], da1[16], cv[16], bv[16];
+                tmem_ld16(c.tl + 64 + c0, dct);
+                tmem_ld16(c.tl + 128 + c0, dbh);
+                tmem_ld16(c.tl + 192 + c0, da1);
+                tmem_wait_ld();
+                ld16_bf16(sC, tt, cg, cv);
+                ld16_bf16(sB, tt, cg, bv);
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    const float a2 = S.A2[c0 + e];
+                    const float Et = fast_exp2(a2 * Gt), Eh = fast_exp2(a2 * (G63 - Gt));
+                    const float f1 = I >= 1 ? fast_exp2(a2 * (Gt - Gref)) : 0.f;
+                    const float dcv = dct[e] * Et + da1[e] * f1;
+                    DC[tt * 64 + c0 + e] = dcv;
+                    DB[tt * 64 + c0 + e] = dbh[e] * Eh;
+                    DG[tt * 64 + c0 + e] = dct[e] * cv[e] * Et - dbh[e] * bv[e] * Eh + da1[e] * f1 * cv[e];
+                    PB[tt * 64 + c0 + e] = dbh[e] * bv[e] * Eh;
+                }
+            }
+        }
+        // segment rows (TMEM lanes 0..95): dB1[seg][i] times the column factor
+        if (trow < 96) {
+            const int I = trow < 16 ? 1 : (trow < 48 ? 2 : 3), s = trow - seg_base(I);
+            const float Gref = S.G[16 * I - 1], Gs = S.G[s];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; h2++) {
+                const int c0 = 32 * wh + 16 * h2;
+                float v[16];
+                tmem_ld16(c.tl + 256 + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; e++) SEGv[trow * 64 + c0 + e] = v[e] * fast_exp2(S.A2[c0 + e] * (Gref - Gs));
+            }
+        }
+        bar_all();
+        if (DELTA && isK) {
+            const int I = tt >> 4;
+            const float Gt = S.G[tt], Gref = I >= 1 ? S.G[16 * I - 1] : 0.f, bet = S.beta[tt];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; h2++) {
+                const int cg = 2 * wh + h2, c0 = 16 * cg;
+                float drs[16], da1[16], bv[16];
+                tmem_ld16(c.tl + 64 + c0, drs);
+                tmem_ld16(c.tl + 192 + c0, da1);
+                tmem_wait_ld();
+                ld16_bf16(sB, tt, cg, bv);
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    const float a2 = S.A2[c0 + e];
+                    const float Et = fast_exp2(a2 * Gt);
+                    const float f1 = I >= 1 ? fast_exp2(a2 * (Gt - Gref)) : 0.f;
+                    const float dbt = -bet * drs[e];   // dBtil
+                    DB[tt * 64 + c0 + e] += dbt * Et + da1[e] * f1;
+                    DG[tt * 64 + c0 + e] += dbt * bv[e] * Et + da1[e] * f1 * bv[e];
+                }
+            }
+        } else if (c.r < 64) {
+            // column sums over tokens of dBhat Bhat (fixed order)
+            float acc = 0.f;
+            for (int s = 0; s < 64; s++) acc += PB[s * 64 + c.r];
+            S.colsum[0][c.r] = acc;
+        }
+        if (DELTA && c.r >= 128 && c.r < 192) {
+            // dbeta of the chunk's tokens (both column halves of every part)
+            const int tq = c.r - 128;
+            if (tq < L) {
+                const float db_ = S.rs[0][0][tq] + S.rs[0][1][tq] + S.rs[1][0][tq] + S.rs[1][1][tq];
+                p.dbeta[((size_t)bb * p.T + t0 + tq) * p.H + h] = __float2bfloat16_rn(db_);
+            }
+        }
+        bar_all();
+        // ---- gather, thread = (token t, channels 16 cq ..): dc, db out; dGam -> dg, dA
+        {
+            float gsum = 0.f;
+            float bv[16];
+            ld16_bf16(sB, t, cq, bv);
+            float dcv[16], dbv[16], dgv[16];
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+                const int i = 16 * cq + e;
+                float seg = 0.f;
+#pragma unroll
+                for (int I = 1; I <= 3; I++)
+                    if (t < 16 * I) seg += SEGv[(seg_base(I) + t) * 64 + i];
+                dcv[e] = DC[t * 64 + i] + nc[e];
+                dbv[e] = DB[t * 64 + i] + seg + nb[e];
+                float gam = DG[t * 64 + i] - bv[e] * seg + ng[e];
+                if (t == 63) {
+                    const float sdi = S.sd[0][i] + S.sd[1][i] + S.sd[2][i] + S.sd[3][i];
+                    gam += S.colsum[0][i] + sdi * c.KT->EC[i];
+                }
+                dgv[e] = gam;
+                gsum = fmaf(S.A2[i], gam, gsum);
+            }
+            if (t < L) {
+                const size_t base = ((size_t)bb * p.T + t0 + t) * p.H + h;
+                __nv_bfloat16* pc = p.dc + base * p.dk + 16 * cq;
+                __nv_bfloat16* pb = p.db + base * p.dk + 16 * cq;
+#pragma unroll
+                for (int e = 0; e < 16; e += 8) {
+                    if (16 * cq + e < p.dk) {
+                        uint4 w;
+                        w.x = pack_bf16(dcv[e], dcv[e + 1]); w.y = pack_bf16(dcv[e + 2], dcv[e + 3]);
+                        w.z = pack_bf16(dcv[e + 4], dcv[e + 5]); w.w = pack_bf16(dcv[e + 6], dcv[e + 7]);
+                        *reinterpret_cast<uint4*>(pc + e) = w;
+                        w.x = pack_bf16(dbv[e], dbv[e + 1]); w.y = pack_bf16(dbv[e + 2], dbv[e + 3]);
+                        w.z = pack_bf16(dbv[e + 4], dbv[e + 5]); w.w = pack_bf16(dbv[e + 6], dbv[e + 7]);
+                        *reinterpret_cast<uint4*>(pb + e) = w;
+                    }
+                }
+            }
+            const float Gt = S.G[t];
+#pragma unroll
+            for (int e = 0; e < 16; e++) PB[t * 64 + 16 * cq + e] = Gt * dgv[e];
+            S.dgp[cq][t] = gsum / kLog2e;   // dG_t partial (A = A2 / log2 e)
+        }
+        bar_all();
+        if (c.warp == 0) {
+            // dg = reverse cumulative sum of dG over the chunk's tokens
+            float a = 0.f, b = 0.f;
+            const int t2 = 2 * c.lane;
+#pragma unroll
+            for (int cq2 = 0; cq2 < 4; cq2++) { a += S.dgp[cq2][t2]; b += S.dgp[cq2][t2 + 1]; }
+            // suffix sums: x = a + b per lane, scan from the top
+            float x = a + b;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, x, o);
+                if (c.lane + o < 32) x += y;
+            }
+            const float after = __shfl_down_sync(0xffffffffu, x, 1);   // sum over pairs above this lane
+            const float tail = c.lane < 31 ? after : 0.f;
+            const float dg1 = b + tail, dg0 = a + dg1;
+            if (t2 < L) p.dg[((size_t)bb * p.T + t0 + t2) * p.H + h] = __float2bfloat16_rn(dg0);
+            if (t2 + 1 < L) p.dg[((size_t)bb * p.T + t0 + t2 + 1) * p.H + h] = __float2bfloat16_rn(dg1);
+        } else if (c.r >= 64 && c.r < 128) {
+            // dA partial: sum_t G_t dGam_t[i] (fixed order)
+            const int i = c.r - 64;
+            float acc = 0.f;
+            for (int s = 0; s < 64; s++) acc += PB[s * 64 + i];
+            p.dA_part[(size_t)q * 64 + i] = acc;
+        }
+        // the stage is free: the next chunk's loads
+        tc_fence_before();
+        bar_all();
+        tc_fence_after();
+        if (q + (int)gridDim.x < p.nq) {
+            if (c.r == 0) issue_tma(p, S, c.sm, q + gridDim.x);
+            pending = q + gridDim.x;
+        }
+    }
+    teardown(c, p, pending, full_phase);
+}
+
+// dA_log[h][i] = A[h][i] sum over batch rows and chunks of the chunk partials (fixed order)
+__global__ void chunk_dalog_kernel(const float* __restrict__ part, const float* __restrict__ A_log,
+                                   float* __restrict__ dA_log, int B, int H, int dk, int nchunks)
+{
+    const int h = blockIdx.x, i = threadIdx.x;
+    if (i >= dk) return;
+    float acc = 0.f;
+    for (int bb = 0; bb < B; bb++) {
+        const size_t qb = ((size_t)bb * H + h) * nchunks;
+        for (int k = 0; k < nchunks; k++) acc += part[(qb + k) * 64 + i];
+    }
+    dA_log[h * dk + i] = -expf(A_log[h * dk + i]) * acc;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, uint32_t bytes)
+{
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host side
+cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
+{
+    CbParams p;
+    memset(&p, 0, sizeof(p));
+    if (!make_map(&p.tm_v, a.v, a.B, a.T, a.H, a.dv) || !make_map(&p.tm_b, a.b, a.B, a.T, a.H, a.dk) ||
+        !make_map(&p.tm_c, a.c, a.B, a.T, a.H, a.dk) || !make_map(&p.tm_do, a.dO, a.B, a.T, a.H, a.dv))
+        return cudaErrorInvalidValue;
+    unsigned char* ws = (unsigned char*)a.ws;
+    p.g = (const __nv_bfloat16*)a.g;
+    p.beta = (const __nv_bfloat16*)a.beta;
+    p.A_log = a.A_log;
+    p.phi = (float*)(ws + Lw.cb_phi_off);
+    p.dlt = (float*)(ws + Lw.cb_dlt_off);
+    p.ych = (float*)(ws + Lw.cb_y_off);
+    p.ec = (float*)(ws + Lw.cb_ec_off);
+    p.st = (float*)(ws + Lw.cb_st_off);
+    p.dst = (float*)(ws + Lw.cb_dst_off);
+    p.dA_part = (float*)(ws + Lw.cb_da_off);
+    p.h0 = a.h0;
+    p.dhT = a.dhT;
+    p.dh0 = a.dh0;
+    p.dv = (__nv_bfloat16*)a.dv_;
+    p.db = (__nv_bfloat16*)a.db;
+    p.dc = (__nv_bfloat16*)a.dc;
+    p.dg = (__nv_bfloat16*)a.dg;
+    p.dbeta = (__nv_bfloat16*)a.dbeta;
+    p.status = (uint32_t*)a.ws;
+    p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv_ = a.dv;
+    p.nchunks = (a.T + 63) / 64;
+    p.nq = a.B * a.H * p.nchunks;
+    p.starve = test_starve_chunk();
+    p.wait_ns = p.starve >= 0 ? kTestWaitNs : kWaitNs;
+    const bool delta = a.mode == GDN_DELTA;
+    constexpr uint32_t prep_bytes = OFF_X + pl::BYTES + 1024, grad_bytes = OFF_X + gl::BYTES + 1024;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e;
+        if ((e = set_smem(chunk_prep_kernel<true>, prep_bytes)) != cudaSuccess) return e;
+        if ((e = set_smem(chunk_prep_kernel<false>, prep_bytes)) != cudaSuccess) return e;
+        if ((e = set_smem(chunk_grad_kernel<true>, grad_bytes)) != cudaSuccess) return e;
+        if ((e = set_smem(chunk_grad_kernel<false>, grad_bytes)) != cudaSuccess) return e;
+        attr = true;
+    }
+    int sms = 152;
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const int grid = p.nq < sms ? p.nq : sms;
+    if (delta) chunk_prep_kernel<true><<<grid, kThreads, prep_bytes, st>>>(p);
+    else chunk_prep_kernel<false><<<grid, kThreads, prep_bytes, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int units = a.B * a.H;
+    if (delta) chunk_chain_kernel<true><<<units * 4, 256, 0, st>>>(p);
+    else chunk_chain_kernel<false><<<units * 4, 256, 0, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (delta) chunk_grad_kernel<true><<<grid, kThreads, grad_bytes, st>>>(p);
+    else chunk_grad_kernel<false><<<grid, kThreads, grad_bytes, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    chunk_dalog_kernel<<<a.H, 64, 0, st>>>(p.dA_part, a.A_log, a.dA_log, a.B, a.H, a.dk, p.nchunks);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -51,6 +51,14 @@ struct WsLayout {
     size_t ts_o_off = 0;          // outputs of the zero-start runs      [B, T, H, d_v] fp32
     size_t ts_g_off = 0;          // segment adjoints from a zero end gradient [B*P, H, d_k, d_v]
     size_t ts_e_off = 0;          // end gradients of the segments       [B*P, H, d_k, d_v]
+    // chunked backward (gdn_chunk_bwd.cu): per chunk of 64 tokens, [B*H*chunks][64][64] fp32 records
+    size_t cb_phi_off = 0;        // delta: the chunk's state transition Phi
+    size_t cb_dlt_off = 0;        // the state the chunk leaves from a zero start
+    size_t cb_y_off = 0;          // the chunk's share of the entering state's adjoint
+    size_t cb_st_off = 0;         // the state entering the chunk
+    size_t cb_dst_off = 0;        // the adjoint of the state leaving the chunk
+    size_t cb_ec_off = 0;         // gated: the chunk's decay [B*H*chunks][64]
+    size_t cb_da_off = 0;         // per-chunk dA partials [B*H*chunks][64]
     size_t total = 0;
 };
 
@@ -66,8 +74,17 @@ constexpr size_t kStateSlot = 16 * 256 * 4;    // one state snapshot (256 thread
 inline int bwd_cols(int dk) { return dk <= 64 ? 64 : 32; }
 inline int bwd_slabs(int dk, int dv) { return (dv + bwd_cols(dk) - 1) / bwd_cols(dk); }
 
-// `norm`: GDN_NORM_BC is set (the backward then routes db, dc through fp32 partials)
-WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm = 0);
+// `norm`: GDN_NORM_BC is set (the backward then routes db, dc through fp32 partials); `logits`: GDN_GATE_LOGITS
+WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm = 0, int logits = 0);
+
+// The chunked tensor-core backward takes bf16 heads up to 64 wide without the option bits; other backward
+// calls take the token-serial one (with its time split for long sequences over few heads).
+inline bool chunk_bwd_applies(const gdn_shape_t& s, int logits, int norm)
+{
+    return s.io == GDN_BF16 && s.T > 0 && s.dk <= 64 && s.dv <= 64 && !logits && !norm;
+}
+// segments of the backward's time split (1 = none; never with the chunked backward)
+int bwd_split(const gdn_shape_t& s, int logits, int norm);
 WsLayout ws_layout_bwd_core(const gdn_shape_t& s, int norm = 0);   // the serial backward's own buffers only
 
 // the serial backward writes fp32 partial sums of db, dc, dg, dbeta (rather than its outputs) when
@@ -79,6 +96,7 @@ cudaError_t launch_serial_fwd(const Args& a, cudaStream_t st);
 cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled);
 cudaError_t launch_decode(const Args& a, cudaStream_t st);   // 1 <= T <= decode_max_tokens()
+cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& L, cudaStream_t st);   // chunk_bwd_applies()
 int tsplit_factor(const gdn_shape_t& s, int backward);   // segments P of a time split, 1 = no split
 cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
                               cudaError_t (*fwd_core)(const Args&, cudaStream_t));

@@ -145,23 +145,42 @@ def test_time_split_workspace():
 
 
 def test_time_split_backward_workspace():
-    """The backward splits long sequences over few heads too: its workspace adds the forward split's
-    buffers (which hold the zero-start runs' fp32 outputs) and two sets of per-segment adjoints to its own."""
-    few = gdn.gdn_workspace_bytes(gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 1)
-    many = gdn.gdn_workspace_bytes(gdn.make_shape(16, 8, 4096, 64, 64, "delta", "bf16"), 1)
+    """The token-serial backward splits long sequences over few heads too (shapes the chunked backward does not
+    take, e.g. with logit gates): its workspace adds the forward split's buffers (which hold the zero-start runs'
+    fp32 outputs) and two sets of per-segment adjoints to its own."""
+    kw = dict(gate_logits=True)
+    few = gdn.gdn_workspace_bytes(gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16", **kw), 1)
+    many = gdn.gdn_workspace_bytes(gdn.make_shape(16, 8, 4096, 64, 64, "delta", "bf16", **kw), 1)
     fwd_split = gdn.gdn_workspace_bytes(gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0)
     # same tokens and heads: the backward's own buffers are equal, the split adds at least the forward's
     assert few >= many + fwd_split - 256 + 2 * 128 * 16384
 
 
+def test_chunked_backward_workspace():
+    """The chunked backward (bf16, heads up to 64 wide, no option bits) keeps per chunk of 64 tokens five fp32
+    64 x 64 records in delta mode (transition, zero-start state, adjoint share, entering state, leaving adjoint),
+    four in gated mode, and two rows of 64 floats (decay, dA partial), after the 256-byte status word."""
+    for mode, nrec in (("delta", 5), ("gated", 4)):
+        for B, H, T, d in ((8, 16, 4096, 64), (1, 16, 32768, 64), (2, 3, 100, 56), (1, 1, 1, 8)):
+            s = gdn.make_shape(B, H, T, d, d, mode, "bf16")
+            nq = B * H * -(-T // 64)
+            want = 256 + nrec * nq * 16384 + 2 * -(-(nq * 256) // 256) * 256
+            assert gdn.gdn_workspace_bytes(s, 1) == want, (mode, B, H, T, d)
+            p = gdn.gdn_plan(s, 1)
+            assert (p.segments, p.fwd_kernel, p.bwd_kernel) == (1, gdn.GDN_KERNEL_NONE, gdn.GDN_BWD_TENSOR_CORE)
+
+
 def test_gate_logits_option_bit():
-    """GDN_GATE_LOGITS rides in the mode field: the workspace is the same with or without it, and a mode
-    with an unknown bit is rejected (size 0)."""
+    """GDN_GATE_LOGITS rides in the mode field: the forward's workspace is the same with or without it, the
+    backward takes the token-serial kernel with it (and the chunked one without), and a mode with an unknown bit
+    is rejected (size 0)."""
     plain = gdn.make_shape(2, 4, 300, 64, 64, "delta", "bf16")
     logit = gdn.make_shape(2, 4, 300, 64, 64, "delta", "bf16", gate_logits=True)
     assert logit.mode == gdn.GDN_DELTA | gdn.GDN_GATE_LOGITS
-    for bwd in (0, 1):
-        assert gdn.gdn_workspace_bytes(logit, bwd) == gdn.gdn_workspace_bytes(plain, bwd) > 0
+    assert gdn.gdn_workspace_bytes(logit, 0) == gdn.gdn_workspace_bytes(plain, 0) > 0
+    assert gdn.gdn_workspace_bytes(logit, 1) > 0 and gdn.gdn_workspace_bytes(plain, 1) > 0
+    assert gdn.gdn_plan(logit, 1).bwd_kernel == gdn.GDN_BWD_SERIAL
+    assert gdn.gdn_plan(plain, 1).bwd_kernel == gdn.GDN_BWD_TENSOR_CORE
     bad = gdn.make_shape(2, 4, 300, 64, 64, gdn.GDN_DELTA | 0x800, "bf16")
     assert gdn.gdn_workspace_bytes(bad, 0) == 0
 
@@ -171,12 +190,13 @@ def test_norm_bc_option_bit():
     unchanged; the backward adds fp32 partials of db, dc [B, T, H, d_k] and dg, dbeta [B, T, H] even with a
     single column slab, because the normalisation's Jacobian is applied after the column sums."""
     B, H, T, d = 2, 4, 300, 64
-    plain = gdn.make_shape(B, H, T, d, d, "delta", "bf16")
+    plain = gdn.make_shape(B, H, T, d, d, "delta", "bf16", gate_logits=True)   # the token-serial backward too
     norm = gdn.make_shape(B, H, T, d, d, "delta", "bf16", norm_bc=True)
     both = gdn.make_shape(B, H, T, d, d, "delta", "bf16", gate_logits=True, norm_bc=True)
     assert norm.mode == gdn.GDN_DELTA | gdn.GDN_NORM_BC
     assert both.mode == gdn.GDN_DELTA | gdn.GDN_NORM_BC | gdn.GDN_GATE_LOGITS
     assert gdn.gdn_workspace_bytes(norm, 0) == gdn.gdn_workspace_bytes(plain, 0) == 256
+    assert gdn.gdn_plan(norm, 1).bwd_kernel == gdn.GDN_BWD_SERIAL
     extra = B * T * H * (2 * d + 2) * 4
     assert gdn.gdn_workspace_bytes(norm, 1) >= gdn.gdn_workspace_bytes(plain, 1) + extra
     assert gdn.gdn_workspace_bytes(both, 1) == gdn.gdn_workspace_bytes(norm, 1)
@@ -184,7 +204,7 @@ def test_norm_bc_option_bit():
 
 def test_check_finite_option_bit():
     """GDN_CHECK_FINITE changes no workspace size and combines with the other bits."""
-    plain = gdn.make_shape(2, 4, 300, 64, 64, "delta", "bf16")
+    plain = gdn.make_shape(2, 4, 300, 64, 64, "delta", "bf16", gate_logits=True)
     chk = gdn.make_shape(2, 4, 300, 64, 64, "delta", "bf16", gate_logits=True, check_finite=True)
     assert chk.mode == gdn.GDN_DELTA | gdn.GDN_GATE_LOGITS | gdn.GDN_CHECK_FINITE
     for bwd in (0, 1):
@@ -204,7 +224,8 @@ def test_plan_reports_split_and_kernel():
         return p.segments, p.fwd_kernel
 
     assert plan(1, 16, 32768, 64, 64, "delta", "bf16") == (8, K.GDN_KERNEL_TENSOR_CORE)
-    assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=1) == (8, K.GDN_KERNEL_TENSOR_CORE)
+    assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=1) == (1, K.GDN_KERNEL_NONE)   # chunked backward
+    assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=1, gate_logits=True) == (8, K.GDN_KERNEL_TENSOR_CORE)
     assert plan(8, 16, 4096, 64, 64, "delta", "bf16") == (1, K.GDN_KERNEL_TENSOR_CORE)
     assert plan(8, 16, 4096, 64, 64, "delta", "bf16", bw=1) == (1, K.GDN_KERNEL_NONE)
     assert plan(1, 40, 1024, 32, 32, "delta", "f32") == (1, K.GDN_KERNEL_SERIAL)   # 152 / 40: 3 < 4 segments
@@ -259,6 +280,14 @@ def test_plan_and_workspace_agree_on_random_shapes():
                 assert T // P >= 512 and dk <= 64 and dv <= 64 and B * H * P <= 152
                 if not bw:
                     assert P >= (4 if mode == "delta" else 3)
+            chunked = io == "bf16" and dk <= 64 and dv <= 64 and T > 0
+            if bw:
+                want = gdn.GDN_BWD_NONE if T == 0 else (gdn.GDN_BWD_TENSOR_CORE if chunked else gdn.GDN_BWD_SERIAL)
+                assert p.bwd_kernel == want
+                if chunked:
+                    assert P == 1 and p.fwd_kernel == gdn.GDN_KERNEL_NONE
+            else:
+                assert p.bwd_kernel == gdn.GDN_BWD_NONE
             if not bw:
                 assert (P > 1) == (w0 > 256)
                 assert (p.fwd_kernel == gdn.GDN_KERNEL_NONE) == (T == 0)

@@ -15,12 +15,12 @@ from linear_attention_recurrence_delta_gb300 import inputs as I  # noqa: E402
 
 
 @pytest.mark.parametrize("name,kernel,fwd,bwd", [
-    ("delta_bf16_8x16x4096x64", "fwd_tc_kernel<delta>", 1, 2),                 # backward + dA_log sum
-    ("gated_bf16_8x16x4096x56_bwd", "fwd_tc_kernel<gated>", 1, 2),
-    ("delta_bf16_1x16x32768x64_bwd", "fwd_tc_kernel<delta>", 5, 9),            # the time split, 8 segments
-    ("delta_bf16_8x40x4096x32", "serial_fwd_kernel<bf16, delta>", 1, 2),       # narrow heads, 320 units
+    ("delta_bf16_8x16x4096x64", "fwd_tc_kernel<delta>", 1, 4),    # chunked backward: prep, chain, grads, dA_log
+    ("gated_bf16_8x16x4096x56_bwd", "fwd_tc_kernel<gated>", 1, 4),
+    ("delta_bf16_1x16x32768x64_bwd", "fwd_tc_kernel<delta>", 5, 4),            # forward: the time split
+    ("delta_bf16_8x40x4096x32", "serial_fwd_kernel<bf16, delta>", 1, 4),       # narrow heads, 320 units
     ("delta_bf16_8x16x4096x128", "serial_fwd_kernel<bf16, delta>", 1, 6),      # 4 slabs: + sums of db, dc, dg, dbeta
-    ("delta_bf16_decode_512x16x1x64", "decode_kernel", 1, 2),
+    ("delta_bf16_decode_512x16x1x64", "decode_kernel", 1, 4),
 ])
 def test_launch_bookkeeping(name, kernel, fwd, bwd):
     w = I.WORKLOADS[name]
@@ -30,8 +30,10 @@ def test_launch_bookkeeping(name, kernel, fwd, bwd):
 
 
 def test_split_backward_launches_follow_the_runs():
-    """The split backward sums G_p over runs of 512 tokens: one run per 512-token segment needs no partial sum."""
-    w = I.custom(name="two_seg", mode="delta", dtype="bf16", B=1, H=64, T=1024, dk=64, dv=64, backward=True)
+    """The split (token-serial) backward sums G_p over runs of 512 tokens: one run per 512-token segment needs no
+    partial sum."""
+    w = I.custom(name="two_seg", mode="delta", dtype="bf16", B=1, H=64, T=1024, dk=64, dv=64, backward=True,
+                 gate_logits=True)
     assert bench.tsplit_factor(w, True) == 2
     assert bench.bwd_launches(w) == 4 + 1 + 1 + 2        # states, G_p, reverse scan, backward + dA_log sum
 
