@@ -1,12 +1,14 @@
 // chunk_common.cuh -- pieces shared by the chunk-parallel kernels of the chunked
 // backward (gdn_chunk_bwd.cu): general tcgen05 products over shared-memory tiles
-// in either major order, 16-column tile rows, and the per-chunk decay tables.
+// in either major order, and 16-column tile rows in bf16, fp16 and hi/lo pairs.
 //
 // Tiles are [rows][64] 16-bit elements with 128-byte swizzling (tc_ptx.cuh).  A
 // tile read "K-major" has its rows along M (or N) and K contiguous; read
 // "MN-major" it has its rows along K and M (or N) contiguous, so the same bytes
 // serve as a matrix or as its transpose.
 #pragma once
+
+#include <cuda_fp16.h>
 
 #include "fwd_tc_common.cuh"
 
@@ -51,6 +53,20 @@ __device__ __forceinline__ void st16_f16(unsigned char* t, int row, int g, const
     st_row8_f16(t, row, 2 * g + 1, b);
 }
 
+// fp16 hi = f16(v) and lo = f16(v - hi): together ~22 significant bits
+__device__ __forceinline__ void st16_f16_split(unsigned char* thi, unsigned char* tlo, int row, int g,
+                                               const float (&v)[16])
+{
+    float h[16], l[16];
+#pragma unroll
+    for (int k = 0; k < 16; k++) {
+        h[k] = __half2float(__float2half_rn(v[k]));
+        l[k] = v[k] - h[k];
+    }
+    st16_f16(thi, row, g, h);
+    st16_f16(tlo, row, g, l);
+}
+
 __device__ __forceinline__ void st16_split(unsigned char* thi, unsigned char* tlo, int row, int g,
                                            const float (&v)[16])
 {
@@ -75,52 +91,6 @@ __device__ __forceinline__ void ld16_bf16(const unsigned char* t, int row, int g
     ld_row8(t, row, 2 * g + 1, b);
 #pragma unroll
     for (int k = 0; k < 8; k++) { v[k] = a[k]; v[8 + k] = b[k]; }
-}
-
-// one element (row, col) of a tile, 16-bit store
-__device__ __forceinline__ void st1_bf16(unsigned char* t, int row, int col, float x)
-{
-    *reinterpret_cast<__nv_bfloat16*>(t + sw128(row, col)) = __float2bfloat16_rn(x);
-}
-
-__device__ __forceinline__ void st1_split(unsigned char* thi, unsigned char* tlo, int row, int col, float x)
-{
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    const uint32_t off = sw128(row, col);
-    *reinterpret_cast<__nv_bfloat16*>(thi + off) = h;
-    *reinterpret_cast<__nv_bfloat16*>(tlo + off) = __float2bfloat16_rn(x - __bfloat162float(h));
-}
-
-// The chunk's decay tables.  With G_t the inclusive sum of g within the chunk, A2 = A log2(e) and the anchor
-// token r(k8) = 8 k8 + 3 of each 8-block, every decay factor the kernels use is an anchor
-// alpha_t = 2^(A2 (G_t - G_r(t))) (or its inverse) times one of these per-(8-block, channel) constants, all <= 1:
-//   KA1[k8]    = 2^(A2 (G_r(k8) - G_{16 I - 1})),  I = k8 / 2 >= 1   (row factor of the 16-block level)
-//   K0[k8]     = 2^(A2 G_r(k8))                                     (exp(A G_t) = alpha_t K0)
-//   KB1[I][k8] = 2^(A2 (G_{16 I - 1} - G_r(k8))),  k8 < 2 I          (column factor towards row block I)
-//   KBH[k8]    = 2^(A2 (G_63 - G_r(k8)))                            (exp(A (G_63 - G_t)) = KBH / alpha_t)
-//   KAP[J]     = 2^(A2 (G_{16 J + 11} - G_{16 J + 3}))              (upper vs lower 8-half of 16-block J)
-//   EC         = 2^(A2 G_63)                                        (the chunk's decay)
-struct Tables {
-    float KA1[8][64];
-    float K0[8][64];
-    float KB1[3][8][64];
-    float KBH[8][64];
-    float KAP[4][64];
-    float EC[64];
-};
-
-// entry e (0 .. 8 * 64 - 1) of every [8][64] table, and the [4][64] and [64] ones for the first 4 * 64 entries
-__device__ __forceinline__ void table_entries(Tables& K, const float* G, const float* A2, int e)
-{
-    const int k8 = e >> 6, i = e & 63, I = k8 >> 1;
-    const float a2 = A2[i], Gr = G[8 * k8 + 3];
-    K.KA1[k8][i] = I >= 1 ? fast_exp2(a2 * (Gr - G[16 * I - 1])) : 0.f;
-    K.K0[k8][i] = fast_exp2(a2 * Gr);
-#pragma unroll
-    for (int J = 1; J <= 3; J++) K.KB1[J - 1][k8][i] = k8 < 2 * J ? fast_exp2(a2 * (G[16 * J - 1] - Gr)) : 0.f;
-    K.KBH[k8][i] = fast_exp2(a2 * (G[63] - Gr));
-    if (k8 < 4) K.KAP[k8][i] = fast_exp2(a2 * (G[16 * k8 + 11] - G[16 * k8 + 3]));
-    if (k8 == 0) K.EC[i] = fast_exp2(a2 * G[63]);
 }
 
 // Row of the 16-block level's column operand for row block I (1..3) and token s < 16 I: the three blocks'

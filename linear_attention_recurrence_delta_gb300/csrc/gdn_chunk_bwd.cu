@@ -49,6 +49,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stdio.h>
 #include <string.h>
 
 #include "chunk_common.cuh"
@@ -133,7 +134,7 @@ constexpr uint32_t NA = 0, X0 = 28672;
 constexpr uint32_t NW = 16384, U = 28672, DSN = 61440;              // U_hi | S_hi | U_lo | S_lo
 constexpr uint32_t BHH = 16384, BHL = 103424;
 constexpr uint32_t DU = 78848, Z = 0, DOR = 78848, ZR = 118784;
-constexpr uint32_t AD = 28672, NEARD = 61440, SEG = 28672;
+constexpr uint32_t AD = 28672, NEARD = 61440, SEG = 28672, A1L = 78848, B1L = 95232;
 constexpr uint32_t DC = 78848, DB = 95232, DG = 111616;
 }  // namespace gl
 
@@ -183,10 +184,12 @@ __device__ __forceinline__ void smem_to_tc()
     tc_fence_after();
 }
 
-// one warp polls the MMA barrier, the others wait at the named barrier
-__device__ __forceinline__ bool mma_wait(Ctx& c, const CbParams& p)
+// one warp polls the MMA barrier, the others wait at the named barrier; an expired wait leaves `where` in
+// status word 2
+__device__ __forceinline__ bool mma_wait(Ctx& c, const CbParams& p, uint32_t where = 0)
 {
-    if (c.warp == 0) wait_or_abort(&c.S->mma, c.mma_phase, &c.S->abort, p.status, p.wait_ns);
+    if (c.warp == 0 && !wait_or_abort(&c.S->mma, c.mma_phase, &c.S->abort, p.status, p.wait_ns) && c.lane == 0)
+        atomicExch(p.status + 2, 100u + where);
     bar_all();
     c.mma_phase ^= 1;
     tc_fence_after();
@@ -230,8 +233,11 @@ __device__ __forceinline__ void front_scan(Ctx& c)
 }
 
 // (2) anchors of token t = r & 63 over channels 16 cq .. 16 cq + 15 (cq = r >> 6): ALPHA, YB; the 16-block level
-// operands A1 = [c f1 ; b f1] (rows t >= 16) and B1 (the column operands of row blocks 1..3), fp16.
-__device__ __forceinline__ void front_operands(Ctx& c, unsigned char* A1, unsigned char* B1, bool with_b_rows)
+// operands A1 = [c f1 ; b f1] (rows t >= 16) and B1 (the column operands of row blocks 1..3), fp16, and with
+// A1lo, B1lo given their fp16 remainders (the backward's level products need the pairs: a pair (t, s) enters
+// dGam_t through A1 and dGam_s through B1, and both must carry the same value)
+__device__ __forceinline__ void front_operands(Ctx& c, unsigned char* A1, unsigned char* B1, bool with_b_rows,
+                                               unsigned char* A1lo = nullptr, unsigned char* B1lo = nullptr)
 {
     Small& S = *c.S;
     const int t = c.r & 63, cq = c.r >> 6, k8 = t >> 3, I = t >> 4;
@@ -269,8 +275,13 @@ __device__ __forceinline__ void front_operands(Ctx& c, unsigned char* A1, unsign
 #pragma unroll
         for (int e = 0; e < 16; e++) y[e] = z[e] = 0.f;
     }
-    st16_f16(A1, t, cq, y);
-    if (with_b_rows) st16_f16(A1, 64 + t, cq, z);
+    if (A1lo) {
+        st16_f16_split(A1, A1lo, t, cq, y);
+        if (with_b_rows) st16_f16_split(A1, A1lo, 64 + t, cq, z);
+    } else {
+        st16_f16(A1, t, cq, y);
+        if (with_b_rows) st16_f16(A1, 64 + t, cq, z);
+    }
     // column factors towards row blocks J > I: exp(A (G_{16 J - 1} - G_t)) <= 1
 #pragma unroll
     for (int J = 1; J <= 3; J++) {
@@ -278,7 +289,8 @@ __device__ __forceinline__ void front_operands(Ctx& c, unsigned char* A1, unsign
             const float Gref = S.G[16 * J - 1];
 #pragma unroll
             for (int e = 0; e < 16; e++) y[e] = bv[e] * fast_exp2(S.A2[16 * cq + e] * (Gref - Gt));
-            st16_f16(B1, seg_base(J) + t, cq, y);
+            if (B1lo) st16_f16_split(B1, B1lo, seg_base(J) + t, cq, y);
+            else st16_f16(B1, seg_base(J) + t, cq, y);
         }
     }
 }
@@ -554,7 +566,7 @@ __device__ bool front_solve(Ctx& c, const CbParams& p, unsigned char* NEARb, uns
                   idesc_bf16(128, 128, false, true), true);
         mma_commit(&S.mma);
     }
-    if (!mma_wait(c, p)) return false;
+    if (!mma_wait(c, p, 1)) return false;
     // -N -> [-N ; -N] (K-major A); X0 -> hi/lo MN-major B blocks.  Twelve 16-column groups of token t:
     // groups 0..5 from lanes 0..63, 6..11 from their copy in lanes 64..127.
     {
@@ -584,7 +596,7 @@ __device__ bool front_solve(Ctx& c, const CbParams& p, unsigned char* NEARb, uns
         mma_tiles(c.tbase + TM_UT, smem_u32(NA), false, 0, 0, smem_u32(X0 + 16384), true, 8192, 0, 4, id, true);
         mma_commit(&S.mma);
     }
-    return mma_wait(c, p);
+    return mma_wait(c, p, 2);
 }
 
 // the operand step's R = [beta V | beta Btil] rows (thread t = r & 63, channels / columns 16 cq ..): hi in LR
@@ -707,7 +719,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
         const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
         load_small(c, p, bb, h, 64 * k);
         if (c.r == 0 && q + (int)gridDim.x < p.nq) prefetch_tma(p, q + gridDim.x);
-        if (c.warp == 0) wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns);
+        if (c.warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && c.lane == 0)
+            atomicExch(p.status + 2, 1u);
         bar_all();
         if (*(volatile uint32_t*)&S.abort) break;
         full_phase ^= 1;
@@ -738,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                 mma_tiles(c.tbase, smem_u32(X + pl::GA + 16384), true, 8192, 0, vd, true, 8192, 0, 4, id, true);
                 mma_commit(&S.mma);
             }
-            if (!mma_wait(c, p)) break;
+            if (!mma_wait(c, p, 3)) break;
             // Delta = rows 0..63, columns 0..63; Y = rows 64..127, columns 64..127
             {
                 const int i = c.trow & 63;
@@ -774,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             }
             front_near(c, fptr(X, pl::NEAR), true);
             bar_all();
-            if (!mma_wait(c, p)) break;
+            if (!mma_wait(c, p, 4)) break;
             if (!front_solve<true>(c, p, X + pl::NEAR, X + pl::P, X + pl::LR, X + pl::LRL, X + pl::MS, X + pl::DINV,
                                    X + pl::NA, X + pl::X0, nullptr))
                 break;
@@ -806,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                 mma_tiles(c.tbase + 416, pp + 8192, false, 0, 0, wu, true, 8192, 0, 4, idB, true);
                 mma_commit(&S.mma);
             }
-            if (!mma_wait(c, p)) break;
+            if (!mma_wait(c, p, 5)) break;
             // lanes 0..63: Phi = diag(E) - Bhat^T W and Delta out; lanes 64..127: Qc = Ctil - P W (hi/lo, natural)
             if (c.trow < 64) {
                 const int i = c.trow;
@@ -859,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                 mma_tiles(c.tbase + 96, qc + 8192, true, 8192, 0, dO, true, 8192, 0, 4, id, true);
                 mma_commit(&S.mma);
             }
-            if (!mma_wait(c, p)) break;
+            if (!mma_wait(c, p, 6)) break;
             if (c.trow < 64) {
                 const int i = c.trow;
                 float* dy = p.ych + ((size_t)q * 64 + i) * 64;
@@ -1043,7 +1056,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         const int t0 = 64 * k, L = min(64, p.T - t0);
         load_small(c, p, bb, h, t0);
         if (c.r == 0 && q + (int)gridDim.x < p.nq) prefetch_tma(p, q + gridDim.x);
-        if (c.warp == 0) wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns);
+        if (c.warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && c.lane == 0)
+            atomicExch(p.status + 2, 2u);
         bar_all();
         if (*(volatile uint32_t*)&S.abort) break;
         full_phase ^= 1;
@@ -1062,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         }
         front_near(c, fptr(X, gl::NEAR), DELTA);
         bar_all();
-        if (!mma_wait(c, p)) break;
+        if (!mma_wait(c, p, 7)) break;
         if (!front_solve<DELTA>(c, p, X + gl::NEAR, X + gl::P, X + gl::LR, X + gl::LRL, X + gl::MS, X + gl::DINV,
                                 X + gl::NA, X + gl::X0, DELTA ? fptr(X, gl::KP) : nullptr))
             break;
@@ -1116,7 +1130,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 mma_tiles(c.tbase + TM_UT, nw, false, 0, 0, sh + 16384, true, 8192, 0, 4, id, true);
                 mma_commit(&S.mma);
             }
-            if (!mma_wait(c, p)) break;
+            if (!mma_wait(c, p, 8)) break;
             // U -> hi/lo [s][j]
             if (!isK) {
 #pragma unroll
@@ -1151,11 +1165,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             mma_tiles(c.tbase + 288, bl, false, 0, 0, dsn, true, 8192, 0, 4, idB, true);
             mma_commit(&S.mma);
         }
-        if (!mma_wait(c, p)) break;
+        if (!mma_wait(c, p, 9)) break;
         const size_t tokrow = ((size_t)bb * p.T + t0 + tt) * p.H + h;   // (b, t0 + tt, h) row of the token tensors
         if (!DELTA) {
-            // dv = dU
-            if (!isK && tt < L) {
+            // dv = dU (the TMEM loads are warp-uniform; only the stores depend on the row)
+            if (!isK) {
 #pragma unroll
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int c0 = 32 * wh + 16 * h2;
@@ -1165,7 +1179,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     __nv_bfloat16* dst = p.dv + tokrow * p.dv_ + c0;
 #pragma unroll
                     for (int e = 0; e < 16; e += 8) {
-                        if (c0 + e < p.dv_) {
+                        if (tt < L && c0 + e < p.dv_) {
                             uint4 w;
                             w.x = pack_bf16(v[e], v[e + 1]); w.y = pack_bf16(v[e + 2], v[e + 3]);
                             w.z = pack_bf16(v[e + 4], v[e + 5]); w.w = pack_bf16(v[e + 6], v[e + 7]);
@@ -1195,7 +1209,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 mma_tiles(c.tbase + 288, na, true, 8192, 0, du + 8192, true, 8192, 0, 4, id, true);
                 mma_commit(&S.mma);
             }
-            if (!mma_wait(c, p)) break;
+            if (!mma_wait(c, p, 10)) break;
             if (!isK) {
 #pragma unroll
                 for (int h2 = 0; h2 < 2; h2++) {
@@ -1215,7 +1229,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 mma_tiles(c.tbase + 352, di, true, 8192, 0, z + 8192, true, 8192, 0, 4, id, true);
                 mma_commit(&S.mma);
             }
-            if (!mma_wait(c, p)) break;
+            if (!mma_wait(c, p, 11)) break;
             // dR: lanes 0..63 -> dv = beta dR (global) and dR hi/lo rows of the A operands [dO ; dR_hi] and
             // [0 ; dR_lo]; lanes 64..127 -> the dO copy and zero rows, and sum_j dR[t][j] V[t][j]
             {
@@ -1272,7 +1286,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             if (DELTA) mma_tiles(c.tbase + 128, ul, false, 0, 0, dsn, false, 0, 0, 4, id9, true);
             mma_commit(&S.mma);
         }
-        if (!mma_wait(c, p)) break;
+        if (!mma_wait(c, p, 12)) break;
         // ---- dQ (lanes 0..63) and dK = -beta (dR U^T) below the diagonal (lanes 64..127): the 16-block level's
         // operand A_d = [dQ | dK] by segments (fp16, K-major [t][seg], two 64-wide K blocks), the near entries in
         // fp32; (delta) the rest of dbeta
@@ -1335,16 +1349,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     nd[e] = I == 0 ? row[e] : (I == 1 ? row[16 + e] : (I == 2 ? row[32 + e] : row[48 + e]));
             }
         }
-        // the 16-block level's operands again (their space was reused)
-        front_operands(c, X + gl::A1, X + gl::B1, true);
+        // the 16-block level's operands again as fp16 hi/lo pairs (their space was reused)
+        front_operands(c, X + gl::A1, X + gl::B1, true, X + gl::A1L, X + gl::B1L);
         smem_to_tc();
         if (c.r == 0) {
             // dA1 = A_d B1 (TMEM 192..255): rows 0..63 -> dc, 64..127 -> db (row side)
-            mma_tiles(c.tbase + 192, smem_u32(X + gl::AD), false, 0, 16384, smem_u32(X + gl::B1), true, 8192, 0, 6,
-                      idesc_f16(128, 64, false, true), false);
+            const uint32_t ad = smem_u32(X + gl::AD), id10 = idesc_f16(128, 64, false, true);
+            mma_tiles(c.tbase + 192, ad, false, 0, 16384, smem_u32(X + gl::B1), true, 8192, 0, 6, id10, false);
+            mma_tiles(c.tbase + 192, ad, false, 0, 16384, smem_u32(X + gl::B1L), true, 8192, 0, 6, id10, true);
             // dB1 = A_d^T A1 (TMEM 256..319): rows = segments (column side)
-            mma_tiles(c.tbase + 256, smem_u32(X + gl::AD), true, 16384, 0, smem_u32(X + gl::A1), true, 8192, 0, 8,
-                      idesc_f16(128, 64, true, true), false);
+            const uint32_t id11 = idesc_f16(128, 64, true, true);
+            mma_tiles(c.tbase + 256, ad, true, 16384, 0, smem_u32(X + gl::A1), true, 8192, 0, 8, id11, false);
+            mma_tiles(c.tbase + 256, ad, true, 16384, 0, smem_u32(X + gl::A1L), true, 8192, 0, 8, id11, true);
             mma_commit(&S.mma);
         }
         // ---- near pairs, reverse (fp32), thread = (token t, channels 16 cq ..): row side (P, K) and column side
@@ -1432,7 +1448,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             }
         }
         bar_all();
-        if (!mma_wait(c, p)) break;
+        if (!mma_wait(c, p, 13)) break;
         // ---- epilogue: dense terms (lanes 0..63), the b-side rows (lanes 64..127), the segments' column side
         float* DC = fptr(X, gl::DC);
         float* DB = fptr(X, gl::DB);
@@ -1671,17 +1687,26 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
     const int grid = p.nq < sms ? p.nq : sms;
+#ifdef GDN_CHUNK_DEBUG
+#define CB_MARK(what) fprintf(stderr, "[chunk bwd] %s: %s\n", what, cudaGetErrorString(cudaStreamSynchronize(st)))
+#else
+#define CB_MARK(what)
+#endif
+    CB_MARK("start");
     if (delta) chunk_prep_kernel<true><<<grid, kThreads, prep_bytes, st>>>(p);
     else chunk_prep_kernel<false><<<grid, kThreads, prep_bytes, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    CB_MARK("prep");
     const int units = a.B * a.H;
     if (delta) chunk_chain_kernel<true><<<units * 4, 256, 0, st>>>(p);
     else chunk_chain_kernel<false><<<units * 4, 256, 0, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    CB_MARK("chain");
     if (delta) chunk_grad_kernel<true><<<grid, kThreads, grad_bytes, st>>>(p);
     else chunk_grad_kernel<false><<<grid, kThreads, grad_bytes, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    CB_MARK("grad");
     chunk_dalog_kernel<<<a.H, 64, 0, st>>>(p.dA_part, a.A_log, a.dA_log, a.B, a.H, a.dk, p.nchunks);
     return cudaGetLastError();
 }
