@@ -92,7 +92,7 @@ constexpr uint32_t OFF_STAGE = 0;                        // b, c, v, dO tiles (T
 constexpr uint32_t ST_B = 0, ST_C = 8192, ST_V = 16384, ST_DO = 24576;
 constexpr uint32_t OFF_ALPHA = 32768;                    // fp32 [64][64] anchors alpha_t[i]
 constexpr uint32_t OFF_YB = 49152;                       // fp32 [64][64] b_t[i] / alpha_t[i]
-constexpr uint32_t OFF_TAB = 65536;                      // KAP [4][64], EC [64] (fp32)
+constexpr uint32_t OFF_TAB = 65536;                      // KU, KL [4][64], EC [64] (fp32)
 constexpr uint32_t OFF_SMALL = 67584;
 constexpr uint32_t OFF_X = 81920;                        // phase region
 
@@ -111,8 +111,12 @@ struct Small {
 };
 static_assert(sizeof(Small) <= OFF_X - OFF_SMALL, "small block");
 
+// per 16-block J and channel: KU = 2^(A2 (G_{16J+11} - G_{16J+7})) and KL = 2^(A2 (G_{16J+7} - G_{16J+3})), both
+// <= 1 and spanning 4 tokens; a pair (t in the upper 8-half, s in the lower one) has exp(A (G_t - G_s)) =
+// (alpha_t KU) (KL / alpha_s) with both brackets <= 1 (an underflow in either means a negligible pair)
 struct Tab {
-    float KAP[4][64];
+    float KU[4][64];
+    float KL[4][64];
     float EC[64];
 };
 static_assert(sizeof(Tab) <= OFF_SMALL - OFF_TAB, "tables");
@@ -201,7 +205,7 @@ __device__ __forceinline__ void front_scan(Ctx& c)
 {
     Small& S = *c.S;
     if (c.warp == 0) {
-        const float ga = S.g[2 * c.lane], gb = S.g[2 * c.lane + 1];
+        const float ga = S.g[2 * c.lane], gb = S.g[2 * c.lane + 1];   // lane l scans tokens 2l, 2l + 1
         float x = ga + gb;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -215,10 +219,12 @@ __device__ __forceinline__ void front_scan(Ctx& c)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         __syncwarp();
+        // the 4-token spans of the anchors (first to 4th, 4th to 8th token of an 8-block) and of KU
         float span = 0.f;
         if (c.lane < 8) {
             const float g0 = S.G[8 * c.lane], g3 = S.G[8 * c.lane + 3], g7 = S.G[8 * c.lane + 7];
             span = fmaxf(g3 - g0, g7 - g3);
+            if (c.lane & 1) span = fmaxf(span, g3 - S.G[8 * c.lane - 1]);
         }
         const bool bad = __any_sync(0xffffffffu, span * m > kSafeLog2);
         if (c.lane == 0) S.unsafe = bad ? 1u : 0u;
@@ -227,7 +233,8 @@ __device__ __forceinline__ void front_scan(Ctx& c)
     {
         const int J = c.r >> 6, i = c.r & 63;
         const float a2 = S.A2[i];
-        c.KT->KAP[J][i] = fast_exp2(a2 * (S.G[16 * J + 11] - S.G[16 * J + 3]));
+        c.KT->KU[J][i] = fast_exp2(a2 * (S.G[16 * J + 11] - S.G[16 * J + 7]));
+        c.KT->KL[J][i] = fast_exp2(a2 * (S.G[16 * J + 7] - S.G[16 * J + 3]));
         if (J == 0) c.KT->EC[i] = fast_exp2(a2 * S.G[63]);
     }
 }
@@ -323,20 +330,25 @@ __device__ __forceinline__ void front_near(Ctx& c, float* NEAR, bool want_k)
             for (int e = 0; e < 8; e++) x[8 * q + e] = v8[e] * c.ALPHA[t * 64 + 32 * hh + 8 * q + e];
         }
         const bool upper = tl16 >= 8;
+        float kl[32];
 #pragma unroll
-        for (int e = 0; e < 32; e++) xe[e] = upper ? x[e] * c.KT->KAP[J][32 * hh + e] : x[e];
+        for (int e = 0; e < 32; e++) {
+            xe[e] = upper ? x[e] * c.KT->KU[J][32 * hh + e] : x[e];
+            kl[e] = upper ? c.KT->KL[J][32 * hh + e] : 1.f;
+        }
 #pragma unroll 1
         for (int sl = 0; sl < 16; sl++) {
             const float* yr = c.YB + (16 * J + sl) * 64 + 32 * hh;
             float acc0 = 0.f, acc1 = 0.f;
             if (sl < 8) {
+                // column in the lower 8-half: (x KU) (y KL) for an upper row, x y for a lower one
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
                     const float4 yv = *reinterpret_cast<const float4*>(yr + e);
-                    acc0 = fmaf(xe[e], yv.x, acc0);
-                    acc1 = fmaf(xe[e + 1], yv.y, acc1);
-                    acc0 = fmaf(xe[e + 2], yv.z, acc0);
-                    acc1 = fmaf(xe[e + 3], yv.w, acc1);
+                    acc0 = fmaf(xe[e], yv.x * kl[e], acc0);
+                    acc1 = fmaf(xe[e + 1], yv.y * kl[e + 1], acc1);
+                    acc0 = fmaf(xe[e + 2], yv.z * kl[e + 2], acc0);
+                    acc1 = fmaf(xe[e + 3], yv.w * kl[e + 3], acc1);
                 }
             } else {
 #pragma unroll
@@ -1377,10 +1389,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 al[e] = c.ALPHA[t * 64 + 16 * cq + e];
                 ai[e] = fast_exp2(-S.A2[16 * cq + e] * dGa);
             }
-            float rP[16], rK[16], cP[16], cK[16];
+            // same-8-half pairs: row side alpha_t sum dM[t][s] (b_s / alpha_s), column side (1 / alpha_t) sum dM[s][t]
+            // left_s alpha_s; pairs across the 8-halves of the block carry KU on the upper token's side and KL on
+            // the lower one's, kept in their own sums (r*x, c*x) so that no factor leaves fp32's range
+            float rP[16], rK[16], cP[16], cK[16], rPx[16], rKx[16], cX[16];
 #pragma unroll
-            for (int e = 0; e < 16; e++) rP[e] = rK[e] = cP[e] = cK[e] = 0.f;
+            for (int e = 0; e < 16; e++) rP[e] = rK[e] = cP[e] = cK[e] = rPx[e] = rKx[e] = cX[e] = 0.f;
             const bool unsafe = S.unsafe != 0;
+            const bool upper = tl16 >= 8;
 #pragma unroll 1
             for (int sl = 0; sl < 16; sl++) {
                 const int s = 16 * J + sl;
@@ -1389,14 +1405,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     const float wq = ND[((0 * 4 + J) * 16 + tl16) * 17 + sl];
                     const float wk = DELTA ? ND[((1 * 4 + J) * 16 + tl16) * 17 + sl] : 0.f;
                     if (!unsafe) {
-                        const bool cross = tl16 >= 8 && sl < 8;
                         const float* yr = c.YB + s * 64 + 16 * cq;
+                        if (upper && sl < 8) {
 #pragma unroll
-                        for (int e = 0; e < 16; e++) {
-                            const float kap = cross ? c.KT->KAP[J][16 * cq + e] : 1.f;
-                            const float y = yr[e] * kap;
-                            rP[e] = fmaf(wq, y, rP[e]);
-                            rK[e] = fmaf(wk, y, rK[e]);
+                            for (int e = 0; e < 16; e++) {
+                                const float y = yr[e] * c.KT->KL[J][16 * cq + e];
+                                rPx[e] = fmaf(wq, y, rPx[e]);
+                                rKx[e] = fmaf(wk, y, rKx[e]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; e++) {
+                                rP[e] = fmaf(wq, yr[e], rP[e]);
+                                rK[e] = fmaf(wk, yr[e], rK[e]);
+                            }
                         }
                     } else {
                         float b8[16];
@@ -1418,14 +1440,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     ld16_bf16(sC, s, cq, cs);
                     ld16_bf16(sB, s, cq, bs);
                     if (!unsafe) {
-                        const bool cross = sl >= 8 && tl16 < 8;
                         const float* as = c.ALPHA + s * 64 + 16 * cq;
+                        if (sl >= 8 && tl16 < 8) {
+                            // row s upper, column t lower: (alpha_s KU) on the row side, (KL / alpha_t) here
 #pragma unroll
-                        for (int e = 0; e < 16; e++) {
-                            const float kap = cross ? c.KT->KAP[J][16 * cq + e] : 1.f;
-                            const float x = as[e] * kap;
-                            cP[e] = fmaf(wq, cs[e] * x, cP[e]);
-                            cK[e] = fmaf(wk, bs[e] * x, cK[e]);
+                            for (int e = 0; e < 16; e++) {
+                                const float x = as[e] * c.KT->KU[J][16 * cq + e];
+                                cX[e] = fmaf(wq * cs[e] + wk * bs[e], x, cX[e]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; e++) {
+                                cP[e] = fmaf(wq, cs[e] * as[e], cP[e]);
+                                cK[e] = fmaf(wk, bs[e] * as[e], cK[e]);
+                            }
                         }
                     } else {
                         const float dG = S.G[s] - Gt;
@@ -1440,8 +1468,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             }
 #pragma unroll
             for (int e = 0; e < 16; e++) {
-                const float ra = unsafe ? 1.f : al[e], ca = unsafe ? 1.f : ai[e];
-                const float dl_c = ra * rP[e], dl_b = ra * rK[e], dr = ca * (cP[e] + cK[e]);
+                float dl_c, dl_b, dr;
+                if (!unsafe) {
+                    const float ku = c.KT->KU[J][16 * cq + e], klv = c.KT->KL[J][16 * cq + e];
+                    const float ax = upper ? al[e] * ku : 0.f;          // alpha_t KU (upper rows' cross pairs)
+                    const float cx = upper ? 0.f : ai[e] * klv;         // KL / alpha_t (lower columns' cross pairs)
+                    dl_c = al[e] * rP[e] + ax * rPx[e];
+                    dl_b = al[e] * rK[e] + ax * rKx[e];
+                    dr = ai[e] * (cP[e] + cK[e]) + cx * cX[e];
+                } else {
+                    dl_c = rP[e];
+                    dl_b = rK[e];
+                    dr = cP[e] + cK[e];
+                }
                 nc[e] = dl_c;
                 nb[e] = dl_b + dr;
                 ng[e] = cv[e] * dl_c + bv[e] * dl_b - bv[e] * dr;
