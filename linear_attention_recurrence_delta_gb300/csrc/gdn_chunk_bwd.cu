@@ -93,7 +93,7 @@ constexpr uint32_t ST_B = 0, ST_C = 8192, ST_V = 16384, ST_DO = 24576;
 constexpr uint32_t OFF_ALPHA = 32768;                    // fp32 [64][64] anchors alpha_t[i]
 constexpr uint32_t OFF_YB = 49152;                       // fp32 [64][64] b_t[i] / alpha_t[i]
 constexpr uint32_t OFF_TAB = 65536;                      // KU, KL [4][64], EC [64] (fp32)
-constexpr uint32_t OFF_SMALL = 67584;
+constexpr uint32_t OFF_SMALL = 68608;
 constexpr uint32_t OFF_X = 81920;                        // phase region
 
 struct Small {
