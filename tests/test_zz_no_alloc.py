@@ -5,10 +5,11 @@ synchronisation, plugins inside a framework that owns all device memory,
 processes that forbid allocations after start-up) get a backward whose
 workspace is a fixed array inside the library, shared by every call on the
 device.  These tests call it through the C ABI: first on another shape so the
-array holds other data, then twice in a row on a shape that runs in one
-segment and on one the library splits in time, each result bit for bit equal
-to gdn_bwd with a caller-allocated workspace (the same kernels run) and within
-the bf16 tolerance of the fp64 oracle.  They also check its error codes and
+array holds other data, then twice in a row on a shape the chunked tensor-core
+backward takes and on one the token-serial backward splits in time (logit
+gates), each result bit for bit equal to gdn_bwd with a caller-allocated
+workspace (the same kernels run) and within the bf16 tolerance of the fp64
+oracle.  They also check its error codes and
 the status query that reads the array's status word.  The file is collected
 last, so a run that stops at the first failure has run every other test.
 """
@@ -44,7 +45,7 @@ def _grads(w):
 
 def _case(w):
     x = I.make_inputs(w)
-    s = gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.mode, w.dtype)
+    s = gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.mode, w.dtype, gate_logits=w.gate_logits)
     t = {k: dev(x[k], "bf16") for k in ("v", "b", "c", "g", "beta", "dO")}
     A_log, h0 = dev32(x["A_log"]), dev32(x["h0"])
     dhT_np = I.round_to(0.3 * I.normal(w.seed + 5, 1, w.B * w.H * w.dk * w.dv).reshape(w.B, w.H, w.dk, w.dv),
@@ -58,9 +59,10 @@ def _noalloc(s, t, A_log, h0, dhT, got):
 
 
 def _split_shape(mode):
-    """A shape whose backward the library splits in time and whose workspace fits the fixed array."""
+    """A shape (with logit gates, so the token-serial backward runs) that the library splits in time and whose
+    workspace fits the fixed array."""
     for B, H, T in ((1, 4, 2048), (1, 2, 2048), (1, 2, 1024), (1, 1, 2048)):
-        s = gdn.make_shape(B, H, T, 64, 64, mode, "bf16")
+        s = gdn.make_shape(B, H, T, 64, 64, mode, "bf16", gate_logits=True)
         if gdn.gdn_plan(s, 1).segments > 1 and gdn.gdn_workspace_bytes(s, 1) <= NOALLOC_BYTES:
             return B, H, T
     return None
@@ -75,23 +77,23 @@ def test_bwd_noalloc_matches_bwd_and_oracle(mode):
     gdn.check(_noalloc(sd, td, Ad, hd, dev32(dhd), _grads(wd)), "gdn_bwd_noalloc (other shape)")
     torch.cuda.synchronize()
 
-    shapes = [(2, 4, 300)]
     split = _split_shape(mode)
     assert split is not None, "no split shape fits the fixed array"
-    shapes.append(split)
-    for B, H, T in shapes:
+    for (B, H, T), logits in (((2, 4, 300), False), (split, True)):
         w = I.custom(name=f"noalloc_{mode}_{B}x{H}x{T}", mode=mode, dtype="bf16", B=B, H=H, T=T, dk=64, dv=64,
-                     seed=31 + T, h0_std=0.2, backward=True)
+                     seed=31 + T, h0_std=0.2, backward=True, gate_logits=logits)
         x, s, t, A_log, h0, dhT_np = _case(w)
         assert gdn.gdn_workspace_bytes(s, 1) <= NOALLOC_BYTES
+        want_kernel = gdn.GDN_BWD_SERIAL if logits else gdn.GDN_BWD_TENSOR_CORE
+        assert gdn.gdn_plan(s, 1).bwd_kernel == want_kernel
         dhT = dev32(dhT_np)
         ref = _grads(w)
         ws = torch.empty(gdn.gdn_workspace_bytes(s, 1), dtype=torch.uint8, device="cuda")
         gdn.check(gdn.gdn_bwd(s, t["v"], t["b"], t["c"], t["g"], t["beta"], A_log, h0, t["dO"], dhT,
                               *ref.values(), ws), "gdn_bwd")
         torch.cuda.synchronize()
-        want = oracle.gdn_bwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], x["dO"], dhT_np,
-                              mode=mode)
+        want = oracle.gdn_bwd_opts(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], x["dO"], dhT_np,
+                                   mode=mode, gate_logits=logits)
         for call in range(2):
             got = _grads(w)
             gdn.check(_noalloc(s, t, A_log, h0, dhT, got), "gdn_bwd_noalloc")
