@@ -90,10 +90,11 @@ struct CbParams {
 // ---------------------------------------------------------------- shared memory
 constexpr uint32_t OFF_STAGE = 0;                        // b, c, v, dO tiles (TMA)
 constexpr uint32_t ST_B = 0, ST_C = 8192, ST_V = 16384, ST_DO = 24576;
-constexpr uint32_t OFF_ALPHA = 32768;                    // fp32 [64][64] anchors alpha_t[i]
-constexpr uint32_t OFF_YB = 49152;                       // fp32 [64][64] b_t[i] / alpha_t[i]
-constexpr uint32_t OFF_TAB = 65536;                      // KU, KL [4][64], EC [64] (fp32)
-constexpr uint32_t OFF_SMALL = 68608;
+constexpr int kAS = 68;                                  // padded row stride of ALPHA, YB (float4 rows, 2-way banks)
+constexpr uint32_t OFF_ALPHA = 32768;                    // fp32 [64][kAS] anchors alpha_t[i]
+constexpr uint32_t OFF_YB = OFF_ALPHA + 64 * kAS * 4;    // fp32 [64][kAS] b_t[i] / alpha_t[i]
+constexpr uint32_t OFF_TAB = OFF_YB + 64 * kAS * 4;      // KU, KL [4][64], EC [64] (fp32)
+constexpr uint32_t OFF_SMALL = OFF_TAB + 2560;
 constexpr uint32_t OFF_X = 81920;                        // phase region
 
 struct Small {
@@ -139,7 +140,8 @@ constexpr uint32_t NW = 16384, U = 28672, DSN = 61440;              // U_hi | S_
 constexpr uint32_t BHH = 16384, BHL = 103424;
 constexpr uint32_t DU = 78848, Z = 0, DOR = 78848, ZR = 118784;
 constexpr uint32_t AD = 28672, NEARD = 61440, SEG = 28672, A1L = 78848, B1L = 95232;
-constexpr uint32_t DC = 78848, DB = 95232, DG = 111616;
+constexpr int kES = 65;                                  // row stride of the epilogue's fp32 arrays (conflict-free)
+constexpr uint32_t DC = 78848, DB = DC + 64 * kES * 4, DG = DB + 64 * kES * 4, PB = 53760;
 }  // namespace gl
 
 // fp32 sub-blocks inside MS: the diagonal 16-blocks of M, the 16-blocks below them inside each 32-block,
@@ -153,6 +155,32 @@ constexpr uint32_t TM_D1 = 0;       // 16-block level [P ; K] (96 columns)
 constexpr uint32_t TM_NX = 96;      // [N | X0V | X0W] -> [N | Util | W]
 constexpr uint32_t TM_UT = TM_NX + 64, TM_W = TM_NX + 128;
 constexpr uint32_t TM_COLS = 512;
+
+#ifdef GDN_CHUNK_DEBUG
+// debug builds only: cycles spent between the phase stamps of CTA 0, per kernel (0 prep, 1 grad), and its chunks
+__device__ unsigned long long g_cb_stamps[2][32];
+__device__ unsigned long long g_cb_last;
+#define CB_STAMP(kid, k)                                                                  \
+    do {                                                                                  \
+        if (threadIdx.x == 0 && blockIdx.x == 0) {                                        \
+            const unsigned long long now_ = clock64();                                    \
+            g_cb_stamps[kid][k] += now_ - g_cb_last;                                      \
+            g_cb_last = now_;                                                             \
+        }                                                                                 \
+    } while (0)
+#define CB_STAMP_INIT                                                                     \
+    do {                                                                                  \
+        if (threadIdx.x == 0 && blockIdx.x == 0) g_cb_last = clock64();                   \
+    } while (0)
+#else
+#define CB_STAMP(kid, k) do {} while (0)
+#define CB_STAMP_INIT do {} while (0)
+#endif
+
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ float* fptr(unsigned char* base, uint32_t off) { return reinterpret_cast<float*>(base + off); }
 
@@ -244,7 +272,8 @@ __device__ __forceinline__ void front_scan(Ctx& c)
 // A1lo, B1lo given their fp16 remainders (the backward's level products need the pairs: a pair (t, s) enters
 // dGam_t through A1 and dGam_s through B1, and both must carry the same value)
 __device__ __forceinline__ void front_operands(Ctx& c, unsigned char* A1, unsigned char* B1, bool with_b_rows,
-                                               unsigned char* A1lo = nullptr, unsigned char* B1lo = nullptr)
+                                               unsigned char* A1lo = nullptr, unsigned char* B1lo = nullptr,
+                                               bool anchors = true)
 {
     Small& S = *c.S;
     const int t = c.r & 63, cq = c.r >> 6, k8 = t >> 3, I = t >> 4;
@@ -254,19 +283,21 @@ __device__ __forceinline__ void front_operands(Ctx& c, unsigned char* A1, unsign
     float bv[16], cv[16];
     ld16_bf16(sB, t, cq, bv);
     ld16_bf16(sC, t, cq, cv);
-    float al[16], yb[16];
+    if (anchors) {
+        float al[16], yb[16];
 #pragma unroll
-    for (int e = 0; e < 16; e++) {
-        const float a2 = S.A2[16 * cq + e];
-        al[e] = fast_exp2(a2 * dG);
-        yb[e] = bv[e] * fast_exp2(-a2 * dG);
-    }
-    float* arow = c.ALPHA + t * 64 + 16 * cq;
-    float* yrow = c.YB + t * 64 + 16 * cq;
+        for (int e = 0; e < 16; e++) {
+            const float a2 = S.A2[16 * cq + e];
+            al[e] = fast_exp2(a2 * dG);
+            yb[e] = bv[e] * fast_exp2(-a2 * dG);
+        }
+        float* arow = c.ALPHA + t * kAS + 16 * cq;
+        float* yrow = c.YB + t * kAS + 16 * cq;
 #pragma unroll
-    for (int e = 0; e < 16; e += 4) {
-        *reinterpret_cast<float4*>(arow + e) = make_float4(al[e], al[e + 1], al[e + 2], al[e + 3]);
-        *reinterpret_cast<float4*>(yrow + e) = make_float4(yb[e], yb[e + 1], yb[e + 2], yb[e + 3]);
+        for (int e = 0; e < 16; e += 4) {
+            *reinterpret_cast<float4*>(arow + e) = make_float4(al[e], al[e + 1], al[e + 2], al[e + 3]);
+            *reinterpret_cast<float4*>(yrow + e) = make_float4(yb[e], yb[e + 1], yb[e + 2], yb[e + 3]);
+        }
     }
     // row factor of the 16-block level: exp(A (G_t - G_{16 I - 1})) <= 1
     float y[16], z[16];
@@ -309,92 +340,97 @@ __device__ __forceinline__ void issue_level(uint32_t tbase, const unsigned char*
               idesc_f16(128, 96, false, false), false);
 }
 
-// (4) near pairs (same 16-block), fp32: warp w takes 16-block J = w & 3 of P (w < 4, c side) or K (b side).
-// Lane = (token tl16 of the block, channel half hh).  Writes NEAR[mat][J][t][s] (s <= t for P, s < t for K,
-// zero elsewhere), kBS-free layout [2][4][16][17].
+// (4) near pairs (same 16-block), fp32, register-blocked.  Per matrix (P: left = c, K: left = b) and 16-block J
+// the pairs s <= t form three 8 x 8 quadrants: lower rows x lower columns, upper x upper (both same 8-half:
+// x_t y_s with x = left alpha, y = b / alpha) and upper x lower (across: (x_t KU)(y_s KL)).  Task = (matrix,
+// block, quadrant, 4-row block, 4-column block, channel half): 96 tasks per matrix, one per thread; the two
+// channel halves of a 4 x 4 block sit in adjacent lanes and are added by one shuffle.  NEAR[mat][J][t][s]
+// ([2][4][16][17]) receives every entry with s <= t (P) or s < t (K); entries above the diagonal are left
+// unwritten and must not be read.
 __device__ __forceinline__ void front_near(Ctx& c, float* NEAR, bool want_k)
 {
     Small& S = *c.S;
-    const int J = c.warp & 3, mat = c.warp >> 2;
-    if (mat == 1 && !want_k) return;
-    const int tl16 = c.lane & 15, hh = c.lane >> 4, t = 16 * J + tl16;
+    const int ntask = want_k ? 192 : 96;
+    if (c.r >= ntask) return;   // whole warps (96, 192 are multiples of 32)
+    const int mat = c.r / 96, rem = c.r % 96, J = rem / 24, rem2 = rem % 24, quad = rem2 >> 3, sub = rem2 & 7;
+    const int tb = sub >> 2, sb = (sub >> 1) & 1, hh = sub & 1;
+    const int t0 = (quad >= 1 ? 8 : 0) + 4 * tb, s0 = (quad == 1 ? 8 : 0) + 4 * sb;   // within the block
+    const bool cross = quad == 2;
     const unsigned char* sL = c.sm + OFF_STAGE + (mat ? ST_B : ST_C);
-    float* out = NEAR + ((mat * 4 + J) * 16 + tl16) * 17;
+    float acc[4][4];
+#pragma unroll
+    for (int ti = 0; ti < 4; ti++)
+#pragma unroll
+        for (int si = 0; si < 4; si++) acc[ti][si] = 0.f;
     if (!S.unsafe) {
-        float x[32], xe[32];
 #pragma unroll
         for (int q = 0; q < 4; q++) {
-            float v8[8];
-            ld_row8(sL, t, 4 * hh + q, v8);
+            const int ch0 = 32 * hh + 8 * q;
+            float ku[8], kl[8];
 #pragma unroll
-            for (int e = 0; e < 8; e++) x[8 * q + e] = v8[e] * c.ALPHA[t * 64 + 32 * hh + 8 * q + e];
-        }
-        const bool upper = tl16 >= 8;
-        float kl[32];
-#pragma unroll
-        for (int e = 0; e < 32; e++) {
-            xe[e] = upper ? x[e] * c.KT->KU[J][32 * hh + e] : x[e];
-            kl[e] = upper ? c.KT->KL[J][32 * hh + e] : 1.f;
-        }
-#pragma unroll 1
-        for (int sl = 0; sl < 16; sl++) {
-            const float* yr = c.YB + (16 * J + sl) * 64 + 32 * hh;
-            float acc0 = 0.f, acc1 = 0.f;
-            if (sl < 8) {
-                // column in the lower 8-half: (x KU) (y KL) for an upper row, x y for a lower one
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 yv = *reinterpret_cast<const float4*>(yr + e);
-                    acc0 = fmaf(xe[e], yv.x * kl[e], acc0);
-                    acc1 = fmaf(xe[e + 1], yv.y * kl[e + 1], acc1);
-                    acc0 = fmaf(xe[e + 2], yv.z * kl[e + 2], acc0);
-                    acc1 = fmaf(xe[e + 3], yv.w * kl[e + 3], acc1);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 yv = *reinterpret_cast<const float4*>(yr + e);
-                    acc0 = fmaf(x[e], yv.x, acc0);
-                    acc1 = fmaf(x[e + 1], yv.y, acc1);
-                    acc0 = fmaf(x[e + 2], yv.z, acc0);
-                    acc1 = fmaf(x[e + 3], yv.w, acc1);
-                }
+            for (int e = 0; e < 8; e++) {
+                ku[e] = cross ? c.KT->KU[J][ch0 + e] : 1.f;
+                kl[e] = cross ? c.KT->KL[J][ch0 + e] : 1.f;
             }
-            float d = acc0 + acc1;
-            d += __shfl_xor_sync(0xffffffffu, d, 16);
-            const bool keep = mat ? (sl < tl16) : (sl <= tl16);
-            if (hh == 0) out[sl] = keep ? d : 0.f;
+            float x[4][8], y[4][8];
+#pragma unroll
+            for (int ti = 0; ti < 4; ti++) {
+                const int t = 16 * J + t0 + ti;
+                float v8[8], a8[8];
+                ld_row8(sL, t, ch0 >> 3, v8);
+                ld_f8(c.ALPHA + t * kAS + ch0, a8);
+#pragma unroll
+                for (int e = 0; e < 8; e++) x[ti][e] = v8[e] * a8[e] * ku[e];
+            }
+#pragma unroll
+            for (int si = 0; si < 4; si++) {
+                const int s = 16 * J + s0 + si;
+                float y8[8];
+                ld_f8(c.YB + s * kAS + ch0, y8);
+#pragma unroll
+                for (int e = 0; e < 8; e++) y[si][e] = y8[e] * kl[e];
+            }
+#pragma unroll
+            for (int ti = 0; ti < 4; ti++)
+#pragma unroll
+                for (int si = 0; si < 4; si++)
+#pragma unroll
+                    for (int e = 0; e < 8; e++) acc[ti][si] = fmaf(x[ti][e], y[si][e], acc[ti][si]);
         }
     } else {
-        // every factor evaluated directly (the anchors could overflow)
-        float x[32];
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            float v8[8];
-            ld_row8(sL, t, 4 * hh + q, v8);
-#pragma unroll
-            for (int e = 0; e < 8; e++) x[8 * q + e] = v8[e];
-        }
+        // every factor evaluated directly (the anchors could overflow); the exponent is clamped at 0 for the
+        // entries above the diagonal, which are discarded
         const unsigned char* sB = c.sm + OFF_STAGE + ST_B;
-        const float Gt = S.G[t];
 #pragma unroll 1
-        for (int sl = 0; sl < 16; sl++) {
-            const int s = 16 * J + sl;
-            const float dG = Gt - S.G[s];
-            float acc = 0.f;
-            if (s <= t) {
+        for (int q = 0; q < 4; q++) {
+            const int ch0 = 32 * hh + 8 * q;
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
+            for (int ti = 0; ti < 4; ti++) {
+                const int t = 16 * J + t0 + ti;
+                float v8[8];
+                ld_row8(sL, t, ch0 >> 3, v8);
+#pragma unroll
+                for (int si = 0; si < 4; si++) {
+                    const int s = 16 * J + s0 + si;
                     float b8[8];
-                    ld_row8(sB, s, 4 * hh + q, b8);
+                    ld_row8(sB, s, ch0 >> 3, b8);
+                    const float dG = fmaxf(S.G[t] - S.G[s], 0.f);
 #pragma unroll
-                    for (int e = 0; e < 8; e++)
-                        acc = fmaf(x[8 * q + e] * b8[e], exp2f(S.A2[32 * hh + 8 * q + e] * dG), acc);
+                    for (int e = 0; e < 8; e++) acc[ti][si] = fmaf(v8[e] * b8[e], exp2f(S.A2[ch0 + e] * dG), acc[ti][si]);
                 }
             }
-            acc += __shfl_xor_sync(0xffffffffu, acc, 16);
-            const bool keep = mat ? (sl < tl16) : (sl <= tl16);
-            if (hh == 0) out[sl] = keep ? acc : 0.f;
+        }
+    }
+#pragma unroll
+    for (int ti = 0; ti < 4; ti++)
+#pragma unroll
+        for (int si = 0; si < 4; si++) acc[ti][si] += __shfl_xor_sync(0xffffffffu, acc[ti][si], 1);
+    if (hh == 0) {
+#pragma unroll
+        for (int ti = 0; ti < 4; ti++) {
+            float* out = NEAR + ((mat * 4 + J) * 16 + t0 + ti) * 17 + s0;
+#pragma unroll
+            for (int si = 0; si < 4; si++) out[si] = acc[ti][si];
         }
     }
 }
@@ -419,7 +455,7 @@ __device__ __forceinline__ void assemble_row(Ctx& c, const float* NEAR, float (&
             const int s = 16 * cg + e;
             float val = 0.f;
             if ((s >> 4) < I) val = (I == Ia) ? da[e] : db[e];
-            else if ((s >> 4) == I) val = NEAR[((isK * 4 + I) * 16 + (t & 15)) * 17 + (s & 15)];
+            else if ((s >> 4) == I && (isK ? s < t : s <= t)) val = NEAR[((isK * 4 + I) * 16 + (t & 15)) * 17 + (s & 15)];
             v[16 * h2 + e] = val;
         }
     }
@@ -519,7 +555,7 @@ __device__ __forceinline__ void write_dinv(Ctx& c, unsigned char* MS, unsigned c
 template <bool DELTA>
 __device__ bool front_solve(Ctx& c, const CbParams& p, unsigned char* NEARb, unsigned char* Pt, unsigned char* LR,
                             unsigned char* LRL, unsigned char* MS, unsigned char* DINV, unsigned char* NA,
-                            unsigned char* X0, float* KP)
+                            unsigned char* X0, float* KP, int kid = 1)
 {
     Small& S = *c.S;
     const int t = c.trow & 63, isK = c.trow >> 6, I = t >> 4;
@@ -566,10 +602,13 @@ __device__ bool front_solve(Ctx& c, const CbParams& p, unsigned char* NEARb, uns
     }
     if (!DELTA) return true;
     bar_all();
+    CB_STAMP(kid, 20);
     solve_blocks(c, MS);
     bar_all();
+    CB_STAMP(kid, 21);
     write_dinv(c, MS, DINV);
     smem_to_tc();
+    CB_STAMP(kid, 22);
     if (c.r == 0) {
         const uint32_t dinv = smem_u32(DINV);
         mma_tiles(c.tbase + TM_NX, dinv, false, 0, 0, smem_u32(LR), true, 8192, 0, 4,
@@ -579,6 +618,7 @@ __device__ bool front_solve(Ctx& c, const CbParams& p, unsigned char* NEARb, uns
         mma_commit(&S.mma);
     }
     if (!mma_wait(c, p, 1)) return false;
+    CB_STAMP(kid, 23);
     // -N -> [-N ; -N] (K-major A); X0 -> hi/lo MN-major B blocks.  Twelve 16-column groups of token t:
     // groups 0..5 from lanes 0..63, 6..11 from their copy in lanes 64..127.
     {
@@ -602,6 +642,7 @@ __device__ bool front_solve(Ctx& c, const CbParams& p, unsigned char* NEARb, uns
         }
     }
     smem_to_tc();
+    CB_STAMP(kid, 24);
     if (c.r == 0) {
         const uint32_t id = idesc_bf16(128, 128, false, true);
         mma_tiles(c.tbase + TM_UT, smem_u32(NA), false, 0, 0, smem_u32(X0), true, 8192, 0, 4, id, true);
@@ -727,7 +768,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
     int q = blockIdx.x;
     int pending = -1;   // chunk whose loads are in flight
     if (c.r == 0 && q < p.nq) { issue_tma(p, S, c.sm, q); pending = q; }
+    CB_STAMP_INIT;
     for (; q < p.nq; q += gridDim.x) {
+        CB_STAMP(0, 0);
         const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
         load_small(c, p, bb, h, 64 * k);
         if (c.r == 0 && q + (int)gridDim.x < p.nq) prefetch_tma(p, q + gridDim.x);
@@ -737,6 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
         if (*(volatile uint32_t*)&S.abort) break;
         full_phase ^= 1;
         pending = -1;
+        CB_STAMP(0, 1);
         front_scan(c);
         bar_all();
         const int t = c.r & 63, cq = c.r >> 6;
@@ -801,8 +845,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             bar_all();
             if (!mma_wait(c, p, 4)) break;
             if (!front_solve<true>(c, p, X + pl::NEAR, X + pl::P, X + pl::LR, X + pl::LRL, X + pl::MS, X + pl::DINV,
-                                   X + pl::NA, X + pl::X0, nullptr))
+                                   X + pl::NA, X + pl::X0, nullptr, 0))
                 break;
+            CB_STAMP(0, 4);
             // [Util | W] -> [W | Util] hi/lo MN-major B blocks (W block 0, Util block 1)
             {
                 const bool isW = c.trow < 64;
@@ -832,6 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                 mma_commit(&S.mma);
             }
             if (!mma_wait(c, p, 5)) break;
+            CB_STAMP(0, 5);
             // lanes 0..63: Phi = diag(E) - Bhat^T W and Delta out; lanes 64..127: Qc = Ctil - P W (hi/lo, natural)
             if (c.trow < 64) {
                 const int i = c.trow;
@@ -885,6 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                 mma_commit(&S.mma);
             }
             if (!mma_wait(c, p, 6)) break;
+            CB_STAMP(0, 6);
             if (c.trow < 64) {
                 const int i = c.trow;
                 float* dy = p.ych + ((size_t)q * 64 + i) * 64;
@@ -900,6 +947,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                 }
             }
         }
+        CB_STAMP(0, 7);
+#ifdef GDN_CHUNK_DEBUG
+        if (c.r == 0 && blockIdx.x == 0) g_cb_stamps[0][31] += 1;
+#endif
         // the stage is free: the next chunk's loads
         tc_fence_before();
         bar_all();
@@ -913,134 +964,181 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
 }
 
 // ================================================================= pass 2: chain
-// One CTA per (unit, 16-column slab of the state), 256 threads: thread = (row i = r >> 2, columns
-// 16 slab + 4 (r & 3) .. + 3).  Forward: S_0 = h0, st[k] = S_k, S_{k+1} = Phi_k S_k + Delta_k.  Reverse:
-// dS = dhT, dst[k] = dS, dS <- Phi_k^T dS + Y_k; dh0 = dS.  The next chunk's records are loaded into registers
-// while the current step computes; Phi and the slab of S alternate between two shared-memory buffers, so one
-// barrier per step suffices.
+// One CTA per (batch, head) unit, 256 threads: thread = (rows 2 ip, 2 ip + 1 with ip = r >> 3, value columns
+// 8 (r & 7) .. + 7), 16 outputs in packed fp32x2 accumulators.  Forward: S_0 = h0, st[k] = S_k,
+// S_{k+1} = Phi_k S_k + Delta_k.  Reverse: dS = dhT, dst[k] = dS, dS <- Phi_k^T dS + Y_k; dh0 = dS.  The next
+// chunk's Phi (four float4 per thread) and Delta / Y rows are loaded into registers while the current step
+// computes, then stored into the other of two shared-memory buffers whose rows are padded to kAS floats (both
+// Phi S and Phi^T dS read them without bank conflicts).  Gated mode: Phi = diag(E), elementwise.
+constexpr uint32_t CHAIN_SMEM = 4 * 64 * kAS * 4;
+
 template <bool DELTA>
 __global__ void __launch_bounds__(256) chunk_chain_kernel(const __grid_constant__ CbParams p)
 {
-    __shared__ __align__(16) float Ph[2][64][68];
-    __shared__ __align__(16) float Sv[2][64][20];
-    const int u = blockIdx.x >> 2, slab = blockIdx.x & 3;
-    const int r = threadIdx.x, i = r >> 2, jq = r & 3, j0 = 16 * slab + 4 * jq;
+    extern __shared__ __align__(16) unsigned char chain_smem[];
+    typedef float Mat[64][kAS];
+    Mat* Ph = reinterpret_cast<Mat*>(chain_smem);                     // [2]
+    Mat* Sv = reinterpret_cast<Mat*>(chain_smem + 2 * 64 * kAS * 4);  // [2]
+    const int u = blockIdx.x, r = threadIdx.x, i0 = 2 * (r >> 3), j0 = 8 * (r & 7);
     const int dk = p.dk, dv = p.dv_, nk = p.nchunks;
     const size_t qb = (size_t)u * nk;
-    float4 pf[4];
-    auto load_phi = [&](int k) {
+    // Phi of the next step (pn) and of the one after (pn2), in registers; pn is stored into the next step's
+    // shared buffer once the current step has computed, then pn2 moves up and the following Phi is loaded
+    float4 pn[4], pn2[4];
+    auto load_phi = [&](int k, float4 (&dst)[4]) {
         const float4* src = reinterpret_cast<const float4*>(p.phi + (qb + k) * 4096);
 #pragma unroll
-        for (int m = 0; m < 4; m++) pf[m] = src[r + 256 * m];
+        for (int m = 0; m < 4; m++) dst[m] = src[r + 256 * m];
     };
-    auto store_phi = [&](int buf) {
+    auto store_phi = [&](int buf, const float4 (&src)[4]) {
 #pragma unroll
         for (int m = 0; m < 4; m++) {
             const int e = r + 256 * m, row = e >> 4, c4 = (e & 15) * 4;
-            *reinterpret_cast<float4*>(&Ph[buf][row][c4]) = pf[m];
+            *reinterpret_cast<float4*>(&Ph[buf][row][c4]) = src[m];
         }
     };
-    auto rec4 = [&](const float* base, int k) {
-        return *reinterpret_cast<const float4*>(base + (qb + k) * 4096 + i * 64 + j0);
-    };
-    float s[4];
+    auto shift = [&]() {
 #pragma unroll
-    for (int e = 0; e < 4; e++) {
-        const int j = j0 + e;
-        s[e] = (p.h0 && i < dk && j < dv) ? p.h0[((size_t)u * dk + i) * dv + j] : 0.f;
+        for (int m = 0; m < 4; m++) pn[m] = pn2[m];
+    };
+    // the thread's 2 x 8 block of a record: rows i0, i0 + 1, columns j0 .. j0 + 7
+    auto rec = [&](const float* base, int k, float4 (&v)[4]) {
+        const float* src = base + (qb + k) * 4096 + i0 * 64 + j0;
+        v[0] = *reinterpret_cast<const float4*>(src);
+        v[1] = *reinterpret_cast<const float4*>(src + 4);
+        v[2] = *reinterpret_cast<const float4*>(src + 64);
+        v[3] = *reinterpret_cast<const float4*>(src + 68);
+    };
+    auto put = [&](float* base, int k, const float2 (&x)[8]) {
+        float* dst = base + (qb + k) * 4096 + i0 * 64 + j0;
+        *reinterpret_cast<float4*>(dst) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
+        *reinterpret_cast<float4*>(dst + 64) = make_float4(x[4].x, x[4].y, x[5].x, x[5].y);
+        *reinterpret_cast<float4*>(dst + 68) = make_float4(x[6].x, x[6].y, x[7].x, x[7].y);
+    };
+    auto to2 = [](const float4 (&v)[4], float2 (&x)[8]) {
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            x[2 * e] = make_float2(v[e].x, v[e].y);
+            x[2 * e + 1] = make_float2(v[e].z, v[e].w);
+        }
+    };
+    auto put_sv = [&](int buf, const float2 (&x)[8]) {
+        *reinterpret_cast<float4*>(&Sv[buf][i0][j0]) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
+        *reinterpret_cast<float4*>(&Sv[buf][i0][j0 + 4]) = make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
+        *reinterpret_cast<float4*>(&Sv[buf][i0 + 1][j0]) = make_float4(x[4].x, x[4].y, x[5].x, x[5].y);
+        *reinterpret_cast<float4*>(&Sv[buf][i0 + 1][j0 + 4]) = make_float4(x[6].x, x[6].y, x[7].x, x[7].y);
+    };
+    // a (+)= P S over the step's buffers; P read as Phi (forward) or Phi^T (reverse)
+    auto step = [&](int buf, bool transpose, float2 (&a)[8]) {
+#pragma unroll 4
+        for (int m = 0; m < 64; m++) {
+            const float p0 = transpose ? Ph[buf][m][i0] : Ph[buf][i0][m];
+            const float p1 = transpose ? Ph[buf][m][i0 + 1] : Ph[buf][i0 + 1][m];
+            const float4 s0 = *reinterpret_cast<const float4*>(&Sv[buf][m][j0]);
+            const float4 s1 = *reinterpret_cast<const float4*>(&Sv[buf][m][j0 + 4]);
+            const float2 q0 = make_float2(p0, p0), q1 = make_float2(p1, p1);
+            const float2 sa = make_float2(s0.x, s0.y), sb = make_float2(s0.z, s0.w);
+            const float2 sc = make_float2(s1.x, s1.y), sd = make_float2(s1.z, s1.w);
+            a[0] = __ffma2_rn(q0, sa, a[0]); a[1] = __ffma2_rn(q0, sb, a[1]);
+            a[2] = __ffma2_rn(q0, sc, a[2]); a[3] = __ffma2_rn(q0, sd, a[3]);
+            a[4] = __ffma2_rn(q1, sa, a[4]); a[5] = __ffma2_rn(q1, sb, a[5]);
+            a[6] = __ffma2_rn(q1, sc, a[6]); a[7] = __ffma2_rn(q1, sd, a[7]);
+        }
+    };
+    float2 s[8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+        const int i = i0 + (e >> 2), j = j0 + 2 * (e & 3);
+        const bool in = p.h0 && i < dk;
+        s[e] = make_float2(in && j < dv ? p.h0[((size_t)u * dk + i) * dv + j] : 0.f,
+                           in && j + 1 < dv ? p.h0[((size_t)u * dk + i) * dv + j + 1] : 0.f);
     }
-    // ---- forward
-    if (DELTA) { load_phi(0); store_phi(0); }
-    float4 d = rec4(p.dlt, 0);
-    float ecv = DELTA ? 0.f : p.ec[qb * 64 + i];
+    // ---- forward (records of step k + 1 and Phi of step k + 2 in flight while step k computes)
+    float4 d[4], dn[4];
+    rec(p.dlt, 0, d);
+    if (DELTA) {
+        load_phi(0, pn);
+        store_phi(0, pn);
+        if (nk > 1) load_phi(1, pn);
+        if (nk > 2) load_phi(2, pn2);
+    }
     for (int k = 0; k < nk; k++) {
-        *reinterpret_cast<float4*>(p.st + (qb + k) * 4096 + i * 64 + j0) = make_float4(s[0], s[1], s[2], s[3]);
-        const bool more = k + 1 < nk;
-        float4 dn = d;
-        float ecn = ecv;
-        if (more) {
-            dn = rec4(p.dlt, k + 1);
-            if (!DELTA) ecn = p.ec[(qb + k + 1) * 64 + i];
-        }
+        const int b = k & 1;
+        put(p.st, k, s);
+        if (k + 1 < nk) rec(p.dlt, k + 1, dn);
         if (DELTA) {
-            *reinterpret_cast<float4*>(&Sv[k & 1][i][4 * jq]) = make_float4(s[0], s[1], s[2], s[3]);
-            if (more) load_phi(k + 1);
-            __syncthreads();
-            float a[4] = {d.x, d.y, d.z, d.w};
-            const float* prow = Ph[k & 1][i];
-#pragma unroll 8
-            for (int m = 0; m < 64; m++) {
-                const float ph = prow[m];
-                const float4 sv = *reinterpret_cast<const float4*>(&Sv[k & 1][m][4 * jq]);
-                a[0] = fmaf(ph, sv.x, a[0]);
-                a[1] = fmaf(ph, sv.y, a[1]);
-                a[2] = fmaf(ph, sv.z, a[2]);
-                a[3] = fmaf(ph, sv.w, a[3]);
-            }
-            if (more) store_phi((k + 1) & 1);
+            put_sv(b, s);
+            __syncthreads();   // Ph[b], Sv[b] complete; step k - 1's reads of the other buffers are done
+            float2 a[8];
+            to2(d, a);
+            step(b, false, a);
+            if (k + 1 < nk) store_phi(b ^ 1, pn);
+            shift();
+            if (k + 3 < nk) load_phi(k + 3, pn2);
 #pragma unroll
-            for (int e = 0; e < 4; e++) s[e] = a[e];
+            for (int e = 0; e < 8; e++) s[e] = a[e];
         } else {
-            s[0] = fmaf(ecv, s[0], d.x);
-            s[1] = fmaf(ecv, s[1], d.y);
-            s[2] = fmaf(ecv, s[2], d.z);
-            s[3] = fmaf(ecv, s[3], d.w);
+            float2 a[8];
+            to2(d, a);
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const float ec = p.ec[(qb + k) * 64 + i0 + (e >> 2)];
+                s[e] = __ffma2_rn(make_float2(ec, ec), s[e], a[e]);
+            }
         }
-        d = dn;
-        ecv = ecn;
+#pragma unroll
+        for (int e = 0; e < 4; e++) d[e] = dn[e];
     }
     // ---- reverse
 #pragma unroll
-    for (int e = 0; e < 4; e++) {
-        const int j = j0 + e;
-        s[e] = (p.dhT && i < dk && j < dv) ? p.dhT[((size_t)u * dk + i) * dv + j] : 0.f;
+    for (int e = 0; e < 8; e++) {
+        const int i = i0 + (e >> 2), j = j0 + 2 * (e & 3);
+        const bool in = p.dhT && i < dk;
+        s[e] = make_float2(in && j < dv ? p.dhT[((size_t)u * dk + i) * dv + j] : 0.f,
+                           in && j + 1 < dv ? p.dhT[((size_t)u * dk + i) * dv + j + 1] : 0.f);
     }
     __syncthreads();
-    if (DELTA) { load_phi(nk - 1); store_phi((nk - 1) & 1); }
-    float4 y = rec4(p.ych, nk - 1);
-    ecv = DELTA ? 0.f : p.ec[(qb + nk - 1) * 64 + i];
-    for (int k = nk - 1; k >= 0; k--) {
-        *reinterpret_cast<float4*>(p.dst + (qb + k) * 4096 + i * 64 + j0) = make_float4(s[0], s[1], s[2], s[3]);
-        const bool more = k > 0;
-        float4 yn = y;
-        float ecn = ecv;
-        if (more) {
-            yn = rec4(p.ych, k - 1);
-            if (!DELTA) ecn = p.ec[(qb + k - 1) * 64 + i];
-        }
-        if (DELTA) {
-            // buffers indexed by k & 1 as in the forward (k descends: the next step uses the other buffer)
-            *reinterpret_cast<float4*>(&Sv[k & 1][i][4 * jq]) = make_float4(s[0], s[1], s[2], s[3]);
-            if (more) load_phi(k - 1);
-            __syncthreads();
-            // (Phi^T dS)[i][j] = sum_m Phi[m][i] dS[m][j]
-            float a[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll 8
-            for (int m = 0; m < 64; m++) {
-                const float pv = Ph[k & 1][m][i];
-                const float4 sv = *reinterpret_cast<const float4*>(&Sv[k & 1][m][4 * jq]);
-                a[0] = fmaf(pv, sv.x, a[0]);
-                a[1] = fmaf(pv, sv.y, a[1]);
-                a[2] = fmaf(pv, sv.z, a[2]);
-                a[3] = fmaf(pv, sv.w, a[3]);
-            }
-            if (more) store_phi((k - 1) & 1);
-#pragma unroll
-            for (int e = 0; e < 4; e++) s[e] = a[e];
-        } else {
-            s[0] = fmaf(ecv, s[0], y.x);
-            s[1] = fmaf(ecv, s[1], y.y);
-            s[2] = fmaf(ecv, s[2], y.z);
-            s[3] = fmaf(ecv, s[3], y.w);
-        }
-        y = yn;
-        ecv = ecn;
+    rec(p.ych, nk - 1, d);
+    if (DELTA) {
+        load_phi(nk - 1, pn);
+        store_phi((nk - 1) & 1, pn);
+        if (nk > 1) load_phi(nk - 2, pn);
+        if (nk > 2) load_phi(nk - 3, pn2);
     }
-    if (p.dh0 && i < dk) {
+    for (int k = nk - 1; k >= 0; k--) {
+        const int b = k & 1;
+        put(p.dst, k, s);
+        if (k > 0) rec(p.ych, k - 1, dn);
+        if (DELTA) {
+            put_sv(b, s);
+            __syncthreads();
+            float2 a[8];
+            to2(d, a);
+            step(b, true, a);
+            if (k > 0) store_phi(b ^ 1, pn);
+            shift();
+            if (k > 2) load_phi(k - 3, pn2);
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
-            const int j = j0 + e;
-            if (j < dv) p.dh0[((size_t)u * dk + i) * dv + j] = s[e];
+            for (int e = 0; e < 8; e++) s[e] = a[e];
+        } else {
+            float2 a[8];
+            to2(d, a);
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const float ec = p.ec[(qb + k) * 64 + i0 + (e >> 2)];
+                s[e] = __ffma2_rn(make_float2(ec, ec), s[e], a[e]);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; e++) d[e] = dn[e];
+    }
+    if (p.dh0) {
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const int i = i0 + (e >> 2), j = j0 + 2 * (e & 3);
+            if (i < dk && j < dv) p.dh0[((size_t)u * dk + i) * dv + j] = s[e].x;
+            if (i < dk && j + 1 < dv) p.dh0[((size_t)u * dk + i) * dv + j + 1] = s[e].y;
         }
     }
 }
@@ -1063,36 +1161,51 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
     if (c.r == 0 && q < p.nq) issue_tma(p, S, c.sm, q);
     if (q < p.nq) pending = q;
     const int trow = c.trow, tt = trow & 63, isK = trow >> 6, wh = c.wh;
+    CB_STAMP_INIT;
     for (; q < p.nq; q += gridDim.x) {
         const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
         const int t0 = 64 * k, L = min(64, p.T - t0);
+        CB_STAMP(1, 0);
         load_small(c, p, bb, h, t0);
-        if (c.r == 0 && q + (int)gridDim.x < p.nq) prefetch_tma(p, q + gridDim.x);
+        if (c.r == 0) {
+            // this chunk's S, dS' records (read after the front) and the next chunk's tiles towards L2
+            prefetch_l2_bulk(p.st + (size_t)q * 4096, 16384);
+            prefetch_l2_bulk(p.dst + (size_t)q * 4096, 16384);
+            if (q + (int)gridDim.x < p.nq) prefetch_tma(p, q + gridDim.x);
+        }
         if (c.warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && c.lane == 0)
             atomicExch(p.status + 2, 2u);
         bar_all();
         if (*(volatile uint32_t*)&S.abort) break;
         full_phase ^= 1;
         pending = -1;
+        CB_STAMP(1, 1);
         front_scan(c);
         bar_all();
         const int t = c.r & 63, cq = c.r >> 6;
+        CB_STAMP(1, 2);
 
         // ---- front: level operands, R, the level product, near pairs, P (and M, the solve)
         front_operands(c, X + gl::A1, X + gl::B1, true);
+        CB_STAMP(1, 16);
         if (DELTA) write_R(c, X + gl::LR, X + gl::LRL);
+        CB_STAMP(1, 17);
         smem_to_tc();
         if (c.r == 0) {
             issue_level(c.tbase, X + gl::A1, X + gl::B1);
             mma_commit(&S.mma);
         }
+        CB_STAMP(1, 18);
         front_near(c, fptr(X, gl::NEAR), DELTA);
+        CB_STAMP(1, 19);
         bar_all();
         if (!mma_wait(c, p, 7)) break;
+        CB_STAMP(1, 3);
         if (!front_solve<DELTA>(c, p, X + gl::NEAR, X + gl::P, X + gl::LR, X + gl::LRL, X + gl::MS, X + gl::DINV,
                                 X + gl::NA, X + gl::X0, DELTA ? fptr(X, gl::KP) : nullptr))
             break;
         if (!DELTA) bar_all();
+        CB_STAMP(1, 4);
 
         // ---- S, dS' of the chunk (fp32 from the chain) -> hi/lo tiles [i][j]; sum_j dS'[i][j] S[i][j]
         {
@@ -1156,6 +1269,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             }
         }
         // Bhat natural [t][i] hi/lo (K-major A of B^ dS')
+        CB_STAMP(1, 5);
         {
             float bv[16], y[16];
             ld16_bf16(sB, t, cq, bv);
@@ -1178,6 +1292,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             mma_commit(&S.mma);
         }
         if (!mma_wait(c, p, 9)) break;
+        CB_STAMP(1, 6);
         const size_t tokrow = ((size_t)bb * p.T + t0 + tt) * p.H + h;   // (b, t0 + tt, h) row of the token tensors
         if (!DELTA) {
             // dv = dU (the TMEM loads are warp-uniform; only the stores depend on the row)
@@ -1286,6 +1401,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         }
         smem_to_tc();
         // ---- [dO ; dR] [U | S]^T (TMEM 0..127) and dBhat = U dS'^T (TMEM 128..191)
+        CB_STAMP(1, 7);
         if (c.r == 0) {
             const uint32_t id8 = idesc_bf16(128, 128, false, false), id9 = idesc_bf16(128, 64, false, false);
             const uint32_t uh = smem_u32(X + gl::U), ul = uh + 16384, dsn = smem_u32(X + gl::DSN);
@@ -1299,6 +1415,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             mma_commit(&S.mma);
         }
         if (!mma_wait(c, p, 12)) break;
+        CB_STAMP(1, 8);
         // ---- dQ (lanes 0..63) and dK = -beta (dR U^T) below the diagonal (lanes 64..127): the 16-block level's
         // operand A_d = [dQ | dK] by segments (fp16, K-major [t][seg], two 64-wide K blocks), the near entries in
         // fp32; (delta) the rest of dbeta
@@ -1353,16 +1470,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 }
                 st16_f16(X + gl::AD + (uint32_t)wh * 16384u, trow, g4, v);
             }
-            // near entries (same 16-block), by one of the row's two threads
+            // near entries (same 16-block), by one of the row's two threads ([2][4][16][20]: float4 rows)
             if (wh == (I >> 1)) {
-                float* nd = fptr(X, gl::NEARD) + ((isK * 4 + I) * 16 + (tt & 15)) * 17;
+                float* nd = fptr(X, gl::NEARD) + ((isK * 4 + I) * 16 + (tt & 15)) * 20;
 #pragma unroll
                 for (int e = 0; e < 16; e++)
                     nd[e] = I == 0 ? row[e] : (I == 1 ? row[16 + e] : (I == 2 ? row[32 + e] : row[48 + e]));
             }
         }
         // the 16-block level's operands again as fp16 hi/lo pairs (their space was reused)
-        front_operands(c, X + gl::A1, X + gl::B1, true, X + gl::A1L, X + gl::B1L);
+        CB_STAMP(1, 9);
+        front_operands(c, X + gl::A1, X + gl::B1, true, X + gl::A1L, X + gl::B1L, false);
         smem_to_tc();
         if (c.r == 0) {
             // dA1 = A_d B1 (TMEM 192..255): rows 0..63 -> dc, 64..127 -> db (row side)
@@ -1375,125 +1493,203 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             mma_tiles(c.tbase + 256, ad, true, 16384, 0, smem_u32(X + gl::A1L), true, 8192, 0, 8, id11, true);
             mma_commit(&S.mma);
         }
-        // ---- near pairs, reverse (fp32), thread = (token t, channels 16 cq ..): row side (P, K) and column side
-        float nc[16], nb[16], ng[16];
+        CB_STAMP(1, 10);
+        // ---- near pairs, reverse (fp32), register-blocked.  Thread = (16-block J, tokens 4 tq .. 4 tq + 3 of the
+        // block, channels 4 cg .. 4 cg + 3); a warp's tokens share an 8-half (tq < 2: lower), so every branch is
+        // warp-uniform.  Row side (t as row): sums over s of dM[t][s] y_s, column side (t as column): sums over s of
+        // dM[s][t] x_s, with y = b / alpha, x = left alpha within an 8-half and the KL / KU factors across the
+        // halves, kept in their own sums so that no factor leaves fp32's range.  The near dQ, dK are zero above
+        // the diagonal, so no mask is needed.
+        const int nJ = c.r >> 6, ntq = (c.r >> 4) & 3, ncg = c.r & 15;
+        const int nt0 = 16 * nJ + 4 * ntq, nch = 4 * ncg;
+        float nc[16], nb[16], ng[16];   // [token ti][channel e] at 4 ti + e
         {
             const float* ND = fptr(X, gl::NEARD);
-            const int J = t >> 4, tl16 = t & 15;
-            float cv[16], bv[16], al[16], ai[16];
-            ld16_bf16(sC, t, cq, cv);
-            ld16_bf16(sB, t, cq, bv);
-            const float Gt = S.G[t], dGa = Gt - S.G[8 * (t >> 3) + 3];
+            const float* NQ = ND + (0 * 4 + nJ) * 16 * 20;
+            const float* NK = ND + (1 * 4 + nJ) * 16 * 20;
+            const bool up = ntq >= 2;
+            const int tl0 = 4 * ntq;
+            float al[16], ai[16], cv[16], bv[16], ku[4], kl[4];
 #pragma unroll
-            for (int e = 0; e < 16; e++) {
-                al[e] = c.ALPHA[t * 64 + 16 * cq + e];
-                ai[e] = fast_exp2(-S.A2[16 * cq + e] * dGa);
+            for (int e = 0; e < 4; e++) {
+                ku[e] = c.KT->KU[nJ][nch + e];
+                kl[e] = c.KT->KL[nJ][nch + e];
             }
-            // same-8-half pairs: row side alpha_t sum dM[t][s] (b_s / alpha_s), column side (1 / alpha_t) sum dM[s][t]
-            // left_s alpha_s; pairs across the 8-halves of the block carry KU on the upper token's side and KL on
-            // the lower one's, kept in their own sums (r*x, c*x) so that no factor leaves fp32's range
-            float rP[16], rK[16], cP[16], cK[16], rPx[16], rKx[16], cX[16];
 #pragma unroll
-            for (int e = 0; e < 16; e++) rP[e] = rK[e] = cP[e] = cK[e] = rPx[e] = rKx[e] = cX[e] = 0.f;
-            const bool unsafe = S.unsafe != 0;
-            const bool upper = tl16 >= 8;
+            for (int ti = 0; ti < 4; ti++) {
+                const int t = nt0 + ti;
+                const float dGa = S.G[t] - S.G[8 * (t >> 3) + 3];
+                const float4 a4 = *reinterpret_cast<const float4*>(c.ALPHA + t * kAS + nch);
+                al[4 * ti] = a4.x; al[4 * ti + 1] = a4.y; al[4 * ti + 2] = a4.z; al[4 * ti + 3] = a4.w;
+#pragma unroll
+                for (int e = 0; e < 4; e++) ai[4 * ti + e] = fast_exp2(-S.A2[nch + e] * dGa);
+                float v8[8];
+                ld_row8(sC, t, nch >> 3, v8);
+#pragma unroll
+                for (int e = 0; e < 4; e++) cv[4 * ti + e] = ((nch & 4) ? v8[4 + e] : v8[e]);
+                ld_row8(sB, t, nch >> 3, v8);
+#pragma unroll
+                for (int e = 0; e < 4; e++) bv[4 * ti + e] = ((nch & 4) ? v8[4 + e] : v8[e]);
+            }
+            if (!S.unsafe) {
+                // row side: s over the block, 4 at a time; same half (s in tokens of my half) or across (my half
+                // upper, s lower)
+                float rP[16], rK[16], rPx[16], rKx[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) rP[e] = rK[e] = rPx[e] = rKx[e] = 0.f;
+#pragma unroll
+                for (int sg = 0; sg < 4; sg++) {
+                    // lower rows: s < 8 only (entries above the diagonal are zero)
+                    if (!up && sg >= 2) continue;
+                    const bool xs = up && sg < 2;   // columns in the lower half of an upper row
+                    float dq[4][4], dkk[4][4];
+#pragma unroll
+                    for (int ti = 0; ti < 4; ti++) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(NQ + (tl0 + ti) * 20 + 4 * sg);
+                        dq[ti][0] = q4.x; dq[ti][1] = q4.y; dq[ti][2] = q4.z; dq[ti][3] = q4.w;
+                        if (DELTA) {
+                            const float4 k4 = *reinterpret_cast<const float4*>(NK + (tl0 + ti) * 20 + 4 * sg);
+                            dkk[ti][0] = k4.x; dkk[ti][1] = k4.y; dkk[ti][2] = k4.z; dkk[ti][3] = k4.w;
+                        } else {
+                            dkk[ti][0] = dkk[ti][1] = dkk[ti][2] = dkk[ti][3] = 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int si = 0; si < 4; si++) {
+                        const int s = 16 * nJ + 4 * sg + si;
+                        const float4 y4 = *reinterpret_cast<const float4*>(c.YB + s * kAS + nch);
+                        float y[4] = {y4.x, y4.y, y4.z, y4.w};
+                        if (xs) {
+#pragma unroll
+                            for (int e = 0; e < 4; e++) y[e] *= kl[e];
+                        }
+#pragma unroll
+                        for (int ti = 0; ti < 4; ti++)
+#pragma unroll
+                            for (int e = 0; e < 4; e++) {
+                                if (xs) {
+                                    rPx[4 * ti + e] = fmaf(dq[ti][si], y[e], rPx[4 * ti + e]);
+                                    rKx[4 * ti + e] = fmaf(dkk[ti][si], y[e], rKx[4 * ti + e]);
+                                } else {
+                                    rP[4 * ti + e] = fmaf(dq[ti][si], y[e], rP[4 * ti + e]);
+                                    rK[4 * ti + e] = fmaf(dkk[ti][si], y[e], rK[4 * ti + e]);
+                                }
+                            }
+                    }
+                }
+#pragma unroll
+                for (int ti = 0; ti < 4; ti++)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int k = 4 * ti + e;
+                        const float ax = up ? al[k] * ku[e] : 0.f;   // alpha_t KU
+                        nc[k] = al[k] * rP[k] + ax * rPx[k];
+                        nb[k] = al[k] * rK[k] + ax * rKx[k];
+                    }
+                // column side: s >= t over the block; same half, or across (my half lower, s upper)
+                float cP[16], cK[16], cX[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) cP[e] = cK[e] = cX[e] = 0.f;
+#pragma unroll
+                for (int sg = 0; sg < 4; sg++) {
+                    if (up && sg < 2) continue;   // upper columns: s >= 8 only
+                    const bool xs = !up && sg >= 2;
+                    float dq[4][4], dkk[4][4];   // [si][ti] = dM[s][t]
+#pragma unroll
+                    for (int si = 0; si < 4; si++) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(NQ + (4 * sg + si) * 20 + tl0);
+                        dq[si][0] = q4.x; dq[si][1] = q4.y; dq[si][2] = q4.z; dq[si][3] = q4.w;
+                        if (DELTA) {
+                            const float4 k4 = *reinterpret_cast<const float4*>(NK + (4 * sg + si) * 20 + tl0);
+                            dkk[si][0] = k4.x; dkk[si][1] = k4.y; dkk[si][2] = k4.z; dkk[si][3] = k4.w;
+                        } else {
+                            dkk[si][0] = dkk[si][1] = dkk[si][2] = dkk[si][3] = 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int si = 0; si < 4; si++) {
+                        const int s = 16 * nJ + 4 * sg + si;
+                        const float4 a4 = *reinterpret_cast<const float4*>(c.ALPHA + s * kAS + nch);
+                        float x[4] = {a4.x, a4.y, a4.z, a4.w};
+                        if (xs) {
+#pragma unroll
+                            for (int e = 0; e < 4; e++) x[e] *= ku[e];
+                        }
+                        float c8[8], b8[8];
+                        ld_row8(sC, s, nch >> 3, c8);
+                        ld_row8(sB, s, nch >> 3, b8);
+#pragma unroll
+                        for (int ti = 0; ti < 4; ti++)
+#pragma unroll
+                            for (int e = 0; e < 4; e++) {
+                                const float xc = ((nch & 4) ? c8[4 + e] : c8[e]) * x[e], xb = ((nch & 4) ? b8[4 + e] : b8[e]) * x[e];
+                                if (xs) {
+                                    cX[4 * ti + e] = fmaf(dq[si][ti], xc, fmaf(dkk[si][ti], xb, cX[4 * ti + e]));
+                                } else {
+                                    cP[4 * ti + e] = fmaf(dq[si][ti], xc, cP[4 * ti + e]);
+                                    cK[4 * ti + e] = fmaf(dkk[si][ti], xb, cK[4 * ti + e]);
+                                }
+                            }
+                    }
+                }
+#pragma unroll
+                for (int ti = 0; ti < 4; ti++)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int k = 4 * ti + e;
+                        const float cx = up ? 0.f : ai[k] * kl[e];   // KL / alpha_t
+                        const float dr = ai[k] * (cP[k] + cK[k]) + cx * cX[k];
+                        ng[k] = cv[k] * nc[k] + bv[k] * nb[k] - bv[k] * dr;
+                        nb[k] += dr;
+                    }
+            } else {
+                // every factor evaluated directly (the anchors could overflow); exponents clamped at 0 where the
+                // weight is zero anyway
+                float rP[16], rK[16], cP[16], cK[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) rP[e] = rK[e] = cP[e] = cK[e] = 0.f;
 #pragma unroll 1
-            for (int sl = 0; sl < 16; sl++) {
-                const int s = 16 * J + sl;
-                if (sl <= tl16) {
-                    // row side: P[t][s], K[t][s] with column s
-                    const float wq = ND[((0 * 4 + J) * 16 + tl16) * 17 + sl];
-                    const float wk = DELTA ? ND[((1 * 4 + J) * 16 + tl16) * 17 + sl] : 0.f;
-                    if (!unsafe) {
-                        const float* yr = c.YB + s * 64 + 16 * cq;
-                        if (upper && sl < 8) {
+                for (int sl = 0; sl < 16; sl++) {
+                    const int s = 16 * nJ + sl;
+                    float c8[8], b8[8];
+                    ld_row8(sC, s, nch >> 3, c8);
+                    ld_row8(sB, s, nch >> 3, b8);
 #pragma unroll
-                            for (int e = 0; e < 16; e++) {
-                                const float y = yr[e] * c.KT->KL[J][16 * cq + e];
-                                rPx[e] = fmaf(wq, y, rPx[e]);
-                                rKx[e] = fmaf(wk, y, rKx[e]);
-                            }
-                        } else {
+                    for (int ti = 0; ti < 4; ti++) {
+                        const int t = nt0 + ti;
+                        const float wq = NQ[(tl0 + ti) * 20 + sl], wk = DELTA ? NK[(tl0 + ti) * 20 + sl] : 0.f;
+                        const float vq = NQ[sl * 20 + tl0 + ti], vk = DELTA ? NK[sl * 20 + tl0 + ti] : 0.f;
+                        const float dGr = fmaxf(S.G[t] - S.G[s], 0.f), dGc = fmaxf(S.G[s] - S.G[t], 0.f);
 #pragma unroll
-                            for (int e = 0; e < 16; e++) {
-                                rP[e] = fmaf(wq, yr[e], rP[e]);
-                                rK[e] = fmaf(wk, yr[e], rK[e]);
-                            }
-                        }
-                    } else {
-                        float b8[16];
-                        ld16_bf16(sB, s, cq, b8);
-                        const float dG = Gt - S.G[s];
-#pragma unroll
-                        for (int e = 0; e < 16; e++) {
-                            const float y = b8[e] * exp2f(S.A2[16 * cq + e] * dG);
-                            rP[e] = fmaf(wq, y, rP[e]);
-                            rK[e] = fmaf(wk, y, rK[e]);
+                        for (int e = 0; e < 4; e++) {
+                            const float a2 = S.A2[nch + e];
+                            const float y = ((nch & 4) ? b8[4 + e] : b8[e]) * exp2f(a2 * dGr), x = exp2f(a2 * dGc);
+                            rP[4 * ti + e] = fmaf(wq, y, rP[4 * ti + e]);
+                            rK[4 * ti + e] = fmaf(wk, y, rK[4 * ti + e]);
+                            cP[4 * ti + e] = fmaf(vq, ((nch & 4) ? c8[4 + e] : c8[e]) * x, cP[4 * ti + e]);
+                            cK[4 * ti + e] = fmaf(vk, ((nch & 4) ? b8[4 + e] : b8[e]) * x, cK[4 * ti + e]);
                         }
                     }
                 }
-                if (sl >= tl16) {
-                    // column side: P[s][t], K[s][t] with row s
-                    const float wq = ND[((0 * 4 + J) * 16 + sl) * 17 + tl16];
-                    const float wk = DELTA ? ND[((1 * 4 + J) * 16 + sl) * 17 + tl16] : 0.f;
-                    float cs[16], bs[16];
-                    ld16_bf16(sC, s, cq, cs);
-                    ld16_bf16(sB, s, cq, bs);
-                    if (!unsafe) {
-                        const float* as = c.ALPHA + s * 64 + 16 * cq;
-                        if (sl >= 8 && tl16 < 8) {
-                            // row s upper, column t lower: (alpha_s KU) on the row side, (KL / alpha_t) here
 #pragma unroll
-                            for (int e = 0; e < 16; e++) {
-                                const float x = as[e] * c.KT->KU[J][16 * cq + e];
-                                cX[e] = fmaf(wq * cs[e] + wk * bs[e], x, cX[e]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; e++) {
-                                cP[e] = fmaf(wq, cs[e] * as[e], cP[e]);
-                                cK[e] = fmaf(wk, bs[e] * as[e], cK[e]);
-                            }
-                        }
-                    } else {
-                        const float dG = S.G[s] - Gt;
-#pragma unroll
-                        for (int e = 0; e < 16; e++) {
-                            const float x = exp2f(S.A2[16 * cq + e] * dG);
-                            cP[e] = fmaf(wq, cs[e] * x, cP[e]);
-                            cK[e] = fmaf(wk, bs[e] * x, cK[e]);
-                        }
-                    }
+                for (int k = 0; k < 16; k++) {
+                    const float dr = cP[k] + cK[k];
+                    nc[k] = rP[k];
+                    nb[k] = rK[k] + dr;
+                    ng[k] = cv[k] * rP[k] + bv[k] * rK[k] - bv[k] * dr;
                 }
-            }
-#pragma unroll
-            for (int e = 0; e < 16; e++) {
-                float dl_c, dl_b, dr;
-                if (!unsafe) {
-                    const float ku = c.KT->KU[J][16 * cq + e], klv = c.KT->KL[J][16 * cq + e];
-                    const float ax = upper ? al[e] * ku : 0.f;          // alpha_t KU (upper rows' cross pairs)
-                    const float cx = upper ? 0.f : ai[e] * klv;         // KL / alpha_t (lower columns' cross pairs)
-                    dl_c = al[e] * rP[e] + ax * rPx[e];
-                    dl_b = al[e] * rK[e] + ax * rKx[e];
-                    dr = ai[e] * (cP[e] + cK[e]) + cx * cX[e];
-                } else {
-                    dl_c = rP[e];
-                    dl_b = rK[e];
-                    dr = cP[e] + cK[e];
-                }
-                nc[e] = dl_c;
-                nb[e] = dl_b + dr;
-                ng[e] = cv[e] * dl_c + bv[e] * dl_b - bv[e] * dr;
             }
         }
         bar_all();
+        CB_STAMP(1, 15);
         if (!mma_wait(c, p, 13)) break;
+        CB_STAMP(1, 11);
         // ---- epilogue: dense terms (lanes 0..63), the b-side rows (lanes 64..127), the segments' column side
         float* DC = fptr(X, gl::DC);
         float* DB = fptr(X, gl::DB);
         float* DG = fptr(X, gl::DG);
-        float* PB = fptr(X, gl::SEG + 24576);   // [64][64] dBhat Bhat, then G_t dGam
-        float* SEGv = fptr(X, gl::SEG);          // [96][64] dB1 h1
+        float* PB = fptr(X, gl::PB);             // [64][gl::kES] dBhat Bhat, then G_t dGam
+        float* SEGv = fptr(X, gl::SEG);          // [96][gl::kES] dB1 h1
         if (!isK) {
             const int I = tt >> 4;
             const float Gt = S.G[tt], G63 = S.G[63], Gref = I >= 1 ? S.G[16 * I - 1] : 0.f;
@@ -1513,10 +1709,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     const float Et = fast_exp2(a2 * Gt), Eh = fast_exp2(a2 * (G63 - Gt));
                     const float f1 = I >= 1 ? fast_exp2(a2 * (Gt - Gref)) : 0.f;
                     const float dcv = dct[e] * Et + da1[e] * f1;
-                    DC[tt * 64 + c0 + e] = dcv;
-                    DB[tt * 64 + c0 + e] = dbh[e] * Eh;
-                    DG[tt * 64 + c0 + e] = dct[e] * cv[e] * Et - dbh[e] * bv[e] * Eh + da1[e] * f1 * cv[e];
-                    PB[tt * 64 + c0 + e] = dbh[e] * bv[e] * Eh;
+                    DC[tt * gl::kES + c0 + e] = dcv;
+                    DB[tt * gl::kES + c0 + e] = dbh[e] * Eh;
+                    DG[tt * gl::kES + c0 + e] = dct[e] * cv[e] * Et - dbh[e] * bv[e] * Eh + da1[e] * f1 * cv[e];
+                    PB[tt * gl::kES + c0 + e] = dbh[e] * bv[e] * Eh;
                 }
             }
         }
@@ -1531,7 +1727,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 tmem_ld16(c.tl + 256 + c0, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; e++) SEGv[trow * 64 + c0 + e] = v[e] * fast_exp2(S.A2[c0 + e] * (Gref - Gs));
+                for (int e = 0; e < 16; e++) SEGv[trow * gl::kES + c0 + e] = v[e] * fast_exp2(S.A2[c0 + e] * (Gref - Gs));
             }
         }
         bar_all();
@@ -1552,14 +1748,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     const float Et = fast_exp2(a2 * Gt);
                     const float f1 = I >= 1 ? fast_exp2(a2 * (Gt - Gref)) : 0.f;
                     const float dbt = -bet * drs[e];   // dBtil
-                    DB[tt * 64 + c0 + e] += dbt * Et + da1[e] * f1;
-                    DG[tt * 64 + c0 + e] += dbt * bv[e] * Et + da1[e] * f1 * bv[e];
+                    DB[tt * gl::kES + c0 + e] += dbt * Et + da1[e] * f1;
+                    DG[tt * gl::kES + c0 + e] += dbt * bv[e] * Et + da1[e] * f1 * bv[e];
                 }
             }
         } else if (c.r < 64) {
             // column sums over tokens of dBhat Bhat (fixed order)
             float acc = 0.f;
-            for (int s = 0; s < 64; s++) acc += PB[s * 64 + c.r];
+            for (int s = 0; s < 64; s++) acc += PB[s * gl::kES + c.r];
             S.colsum[0][c.r] = acc;
         }
         if (DELTA && c.r >= 128 && c.r < 192) {
@@ -1571,50 +1767,47 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             }
         }
         bar_all();
-        // ---- gather, thread = (token t, channels 16 cq ..): dc, db out; dGam -> dg, dA
+        CB_STAMP(1, 12);
+        // ---- gather, thread = (tokens nt0 .. nt0 + 3, channels nch .. nch + 3) as in the near pass: dc, db out;
+        // dGam -> dG (summed over the sixteen channel groups of a token by shuffles in the half-warp), dA
         {
-            float gsum = 0.f;
-            float bv[16];
-            ld16_bf16(sB, t, cq, bv);
-            float dcv[16], dbv[16], dgv[16];
 #pragma unroll
-            for (int e = 0; e < 16; e++) {
-                const int i = 16 * cq + e;
-                float seg = 0.f;
+            for (int ti = 0; ti < 4; ti++) {
+                const int t = nt0 + ti;
+                float bv8[8];
+                ld_row8(sB, t, nch >> 3, bv8);
+                float dcv[4], dbv[4], gsum = 0.f;
 #pragma unroll
-                for (int I = 1; I <= 3; I++)
-                    if (t < 16 * I) seg += SEGv[(seg_base(I) + t) * 64 + i];
-                dcv[e] = DC[t * 64 + i] + nc[e];
-                dbv[e] = DB[t * 64 + i] + seg + nb[e];
-                float gam = DG[t * 64 + i] - bv[e] * seg + ng[e];
-                if (t == 63) {
-                    const float sdi = S.sd[0][i] + S.sd[1][i] + S.sd[2][i] + S.sd[3][i];
-                    gam += S.colsum[0][i] + sdi * c.KT->EC[i];
-                }
-                dgv[e] = gam;
-                gsum = fmaf(S.A2[i], gam, gsum);
-            }
-            if (t < L) {
-                const size_t base = ((size_t)bb * p.T + t0 + t) * p.H + h;
-                __nv_bfloat16* pc = p.dc + base * p.dk + 16 * cq;
-                __nv_bfloat16* pb = p.db + base * p.dk + 16 * cq;
+                for (int e = 0; e < 4; e++) {
+                    const int i = nch + e, k = 4 * ti + e;
+                    float seg = 0.f;
 #pragma unroll
-                for (int e = 0; e < 16; e += 8) {
-                    if (16 * cq + e < p.dk) {
-                        uint4 w;
-                        w.x = pack_bf16(dcv[e], dcv[e + 1]); w.y = pack_bf16(dcv[e + 2], dcv[e + 3]);
-                        w.z = pack_bf16(dcv[e + 4], dcv[e + 5]); w.w = pack_bf16(dcv[e + 6], dcv[e + 7]);
-                        *reinterpret_cast<uint4*>(pc + e) = w;
-                        w.x = pack_bf16(dbv[e], dbv[e + 1]); w.y = pack_bf16(dbv[e + 2], dbv[e + 3]);
-                        w.z = pack_bf16(dbv[e + 4], dbv[e + 5]); w.w = pack_bf16(dbv[e + 6], dbv[e + 7]);
-                        *reinterpret_cast<uint4*>(pb + e) = w;
+                    for (int I = 1; I <= 3; I++)
+                        if (t < 16 * I) seg += SEGv[(seg_base(I) + t) * gl::kES + i];
+                    dcv[e] = DC[t * gl::kES + i] + nc[k];
+                    dbv[e] = DB[t * gl::kES + i] + seg + nb[k];
+                    float gam = DG[t * gl::kES + i] - ((nch & 4) ? bv8[4 + e] : bv8[e]) * seg + ng[k];
+                    if (t == 63) {
+                        const float sdi = S.sd[0][i] + S.sd[1][i] + S.sd[2][i] + S.sd[3][i];
+                        gam += S.colsum[0][i] + sdi * c.KT->EC[i];
                     }
+                    PB[t * gl::kES + i] = S.G[t] * gam;
+                    gsum = fmaf(S.A2[i], gam, gsum);
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
+                if (ncg == 0) S.dgp[0][t] = gsum / kLog2e;   // dG_t (A = A2 / log2 e)
+                if (t < L && nch < p.dk) {
+                    const size_t base = ((size_t)bb * p.T + t0 + t) * p.H + h;
+                    uint2 w;
+                    w.x = pack_bf16(dcv[0], dcv[1]);
+                    w.y = pack_bf16(dcv[2], dcv[3]);
+                    *reinterpret_cast<uint2*>(p.dc + base * p.dk + nch) = w;
+                    w.x = pack_bf16(dbv[0], dbv[1]);
+                    w.y = pack_bf16(dbv[2], dbv[3]);
+                    *reinterpret_cast<uint2*>(p.db + base * p.dk + nch) = w;
                 }
             }
-            const float Gt = S.G[t];
-#pragma unroll
-            for (int e = 0; e < 16; e++) PB[t * 64 + 16 * cq + e] = Gt * dgv[e];
-            S.dgp[cq][t] = gsum / kLog2e;   // dG_t partial (A = A2 / log2 e)
         }
         bar_all();
         if (c.warp == 0) {
@@ -1622,7 +1815,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             float a = 0.f, b = 0.f;
             const int t2 = 2 * c.lane;
 #pragma unroll
-            for (int cq2 = 0; cq2 < 4; cq2++) { a += S.dgp[cq2][t2]; b += S.dgp[cq2][t2 + 1]; }
+            a = S.dgp[0][t2];
+            b = S.dgp[0][t2 + 1];
             // suffix sums: x = a + b per lane, scan from the top
             float x = a + b;
 #pragma unroll
@@ -1639,9 +1833,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             // dA partial: sum_t G_t dGam_t[i] (fixed order)
             const int i = c.r - 64;
             float acc = 0.f;
-            for (int s = 0; s < 64; s++) acc += PB[s * 64 + i];
+            for (int s = 0; s < 64; s++) acc += PB[s * gl::kES + i];
             p.dA_part[(size_t)q * 64 + i] = acc;
         }
+        CB_STAMP(1, 13);
         // the stage is free: the next chunk's loads
         tc_fence_before();
         bar_all();
@@ -1650,6 +1845,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             if (c.r == 0) issue_tma(p, S, c.sm, q + gridDim.x);
             pending = q + gridDim.x;
         }
+        CB_STAMP(1, 14);
+#ifdef GDN_CHUNK_DEBUG
+        if (c.r == 0 && blockIdx.x == 0) g_cb_stamps[1][31] += 1;
+#endif
     }
     teardown(c, p, pending, full_phase);
 }
@@ -1718,6 +1917,7 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
         if ((e = set_smem(chunk_prep_kernel<false>, prep_bytes)) != cudaSuccess) return e;
         if ((e = set_smem(chunk_grad_kernel<true>, grad_bytes)) != cudaSuccess) return e;
         if ((e = set_smem(chunk_grad_kernel<false>, grad_bytes)) != cudaSuccess) return e;
+        if ((e = set_smem(chunk_chain_kernel<true>, CHAIN_SMEM)) != cudaSuccess) return e;
         attr = true;
     }
     int sms = 152;
@@ -1738,8 +1938,8 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     if (e != cudaSuccess) return e;
     CB_MARK("prep");
     const int units = a.B * a.H;
-    if (delta) chunk_chain_kernel<true><<<units * 4, 256, 0, st>>>(p);
-    else chunk_chain_kernel<false><<<units * 4, 256, 0, st>>>(p);
+    if (delta) chunk_chain_kernel<true><<<units, 256, CHAIN_SMEM, st>>>(p);
+    else chunk_chain_kernel<false><<<units, 256, 0, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     CB_MARK("chain");
     if (delta) chunk_grad_kernel<true><<<grid, kThreads, grad_bytes, st>>>(p);
@@ -1751,3 +1951,15 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
 }
 
 }  // namespace gdn
+
+#ifdef GDN_CHUNK_DEBUG
+extern "C" int gdn_chunk_debug_stamps(unsigned long long* out, int clear)
+{
+    if (cudaMemcpyFromSymbol(out, gdn::g_cb_stamps, sizeof(gdn::g_cb_stamps)) != cudaSuccess) return 1;
+    if (clear) {
+        static const unsigned long long zero[2][32] = {};
+        if (cudaMemcpyToSymbol(gdn::g_cb_stamps, zero, sizeof(zero)) != cudaSuccess) return 1;
+    }
+    return 0;
+}
+#endif
