@@ -100,6 +100,8 @@ static size_t place_chunk_bwd(const gdn_shape_t& s, WsLayout& L, size_t off)
     if (s.mode == GDN_DELTA) {
         L.cb_phi_off = off;
         off = round_up(off + rec, 256);
+        L.cb_sv_off = off;
+        off = round_up(off + nq * 65536, 256);
     }
     L.cb_dlt_off = off;
     off = round_up(off + rec, 256);

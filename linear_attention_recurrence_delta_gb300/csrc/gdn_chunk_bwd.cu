@@ -17,9 +17,11 @@
 // The backward is therefore:
 //   1. chunk_prep_kernel, one chunk at a time over every chunk of every head
 //      (no chunk waits for another): Phi (delta), Delta and Y of each chunk;
-//   2. chunk_chain_kernel, per head and 16-column slab of the state: the
-//      states entering the chunks (S_{k+1} = Phi_k S_k + Delta_k from h0) and the
-//      adjoints leaving them (dS_k = Phi_k^T dS_{k+1} + Y_k from dh_T), fp32;
+//   2. the chain, one CTA per head: the states entering the chunks
+//      (S_{k+1} = Phi_k S_k + Delta_k from h0) and the adjoints leaving them
+//      (dS_k = Phi_k^T dS_{k+1} + Y_k from dh_T), fp32 records; in delta mode each
+//      step is one tcgen05 product on Phi's tiles (chunk_chain_tc_kernel), in
+//      gated mode an elementwise update (chunk_chain_gated_kernel);
 //   3. chunk_grad_kernel, again one chunk at a time: with S and dS' of the
 //      chunk known, every token gradient of the chunk by the reverse mode of its
 //      closed form (the transposed contractions of the forward, on tcgen05).
@@ -69,8 +71,12 @@ struct CbParams {
     const __nv_bfloat16* g;
     const __nv_bfloat16* beta;
     const float* A_log;
+    // delta: Phi of chunk q (S' = Phi S + Delta) as two bf16 tiles, hi then lo, each [64][64] (rows i, columns m)
+    // in the 128-byte-swizzled layout of the MMA operands: 16 KB per chunk
+    unsigned char* phi;
+    // delta: the front's results that the gradient pass reuses (layout in namespace sv), 64 KB per chunk
+    unsigned char* sv;
     // per chunk q = unit * nchunks + k, each [64][64] fp32 (rows = key channel i, columns = value column j)
-    float* phi;     // delta: Phi of the chunk (S' = Phi S + Delta)
     float* dlt;     // Delta
     float* ych;     // Y = Qc^T dO
     float* ec;      // gated: [q][64] exp(A G_63)
@@ -106,7 +112,7 @@ struct Small {
     float rs[2][2][64];  // grad: per (kind, column half) row partial sums
     float colsum[4][64];
     float dgp[4][64];    // grad: per channel quarter partial sums of dG_t
-    uint64_t full, mma;
+    uint64_t full, mma, full2;   // full2: the saved front (gradient pass, delta)
     uint32_t tmem_base, abort, unsafe;
     float a2max;
 };
@@ -144,6 +150,13 @@ constexpr int kES = 65;                                  // row stride of the ep
 constexpr uint32_t DC = 78848, DB = DC + 64 * kES * 4, DG = DB + 64 * kES * 4, PB = 53760;
 }  // namespace gl
 
+// The delta front's results, saved by the prep pass for the gradient pass (per chunk, byte offsets): P as hi, lo
+// tiles; -N and Dinv, one half each of the stacked [-N ; -N] and [Dinv ; Dinv] operands; K strictly below the
+// diagonal, packed by rows, fp32; -W, a bf16 tile [t][i]; Util, fp32 [t][j].
+namespace sv {
+constexpr uint32_t P = 0, NA = 16384, DINV = 24576, KP = 32768, NW = 40960, UT = 49152, BYTES = 65536;
+}  // namespace sv
+
 // fp32 sub-blocks inside MS: the diagonal 16-blocks of M, the 16-blocks below them inside each 32-block,
 // the diagonal blocks' inverses and the 32-blocks' coupling blocks
 constexpr uint32_t MS_M32 = 0, MS_C32 = 4 * 16 * kBS * 4, MS_DI32 = MS_C32 + 2 * 16 * kBS * 4,
@@ -180,6 +193,14 @@ __device__ unsigned long long g_cb_last;
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 __device__ __forceinline__ float* fptr(unsigned char* base, uint32_t off) { return reinterpret_cast<float*>(base + off); }
@@ -699,6 +720,22 @@ __device__ __forceinline__ void issue_tma(const CbParams& p, Small& S, unsigned 
     tma_load_4d(st + ST_DO, &p.tm_do, &S.full, 0, h, 64 * k, bb);
 }
 
+// the saved front of chunk q into the gradient pass's phase region (the stacked operands' halves twice)
+__device__ __forceinline__ void issue_saved(const CbParams& p, Small& S, unsigned char* sm, int q)
+{
+    if (q == p.starve) return;
+    unsigned char* X = sm + OFF_X;
+    const unsigned char* src = p.sv + (size_t)q * sv::BYTES;
+    mbar_arrive_expect_tx(&S.full2, 16384 + 6 * 8192);
+    bulk_g2s(X + gl::P, src + sv::P, 16384, &S.full2);
+    bulk_g2s(X + gl::NA, src + sv::NA, 8192, &S.full2);
+    bulk_g2s(X + gl::NA + 8192, src + sv::NA, 8192, &S.full2);
+    bulk_g2s(X + gl::DINV, src + sv::DINV, 8192, &S.full2);
+    bulk_g2s(X + gl::DINV + 8192, src + sv::DINV, 8192, &S.full2);
+    bulk_g2s(X + gl::KP, src + sv::KP, 8192, &S.full2);
+    bulk_g2s(X + gl::NW, src + sv::NW, 8192, &S.full2);
+}
+
 __device__ __forceinline__ void prefetch_tma(const CbParams& p, int q)
 {
     const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
@@ -729,6 +766,7 @@ __device__ __forceinline__ Ctx setup(unsigned char* smem_raw, const CbParams& p)
     if (c.r == 0) {
         mbar_init(&S.full, 1);
         mbar_init(&S.mma, 1);
+        mbar_init(&S.full2, 1);
         S.abort = 0;
         fence_mbar_init();
     }
@@ -745,11 +783,14 @@ __device__ __forceinline__ Ctx setup(unsigned char* smem_raw, const CbParams& p)
     return c;
 }
 
-__device__ __forceinline__ void teardown(Ctx& c, const CbParams& p, int issued_q, uint32_t full_phase)
+__device__ __forceinline__ void teardown(Ctx& c, const CbParams& p, int issued_q, uint32_t full_phase,
+                                         int issued_q2 = -1, uint32_t full2_phase = 0)
 {
-    // after an abort, let the copy still in flight land before exiting
+    // after an abort, let the copies still in flight land before exiting
     if (c.r == 0 && *(volatile uint32_t*)&c.S->abort && issued_q >= 0 && issued_q != p.starve)
         mbar_wait(&c.S->full, full_phase, nullptr, p.wait_ns);
+    if (c.r == 0 && *(volatile uint32_t*)&c.S->abort && issued_q2 >= 0 && issued_q2 != p.starve)
+        mbar_wait(&c.S->full2, full2_phase, nullptr, p.wait_ns);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -844,13 +885,32 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             front_near(c, fptr(X, pl::NEAR), true);
             bar_all();
             if (!mma_wait(c, p, 4)) break;
+            unsigned char* svq = p.sv + (size_t)q * sv::BYTES;
             if (!front_solve<true>(c, p, X + pl::NEAR, X + pl::P, X + pl::LR, X + pl::LRL, X + pl::MS, X + pl::DINV,
-                                   X + pl::NA, X + pl::X0, nullptr, 0))
+                                   X + pl::NA, X + pl::X0, reinterpret_cast<float*>(svq + sv::KP), 0))
                 break;
             CB_STAMP(0, 4);
-            // [Util | W] -> [W | Util] hi/lo MN-major B blocks (W block 0, Util block 1)
+            // saved for the gradient pass: the P tiles and one half each of [-N ; -N] and [Dinv ; Dinv]
+            {
+                const uint4* sp = reinterpret_cast<const uint4*>(X + pl::P);
+                const uint4* sn = reinterpret_cast<const uint4*>(X + pl::NA);
+                const uint4* sd = reinterpret_cast<const uint4*>(X + pl::DINV);
+                uint4* dp = reinterpret_cast<uint4*>(svq + sv::P);
+                uint4* dn = reinterpret_cast<uint4*>(svq + sv::NA);
+                uint4* dd = reinterpret_cast<uint4*>(svq + sv::DINV);
+#pragma unroll
+                for (int m = 0; m < 4; m++) dp[c.r + 256 * m] = sp[c.r + 256 * m];
+#pragma unroll
+                for (int m = 0; m < 2; m++) {
+                    dn[c.r + 256 * m] = sn[c.r + 256 * m];
+                    dd[c.r + 256 * m] = sd[c.r + 256 * m];
+                }
+            }
+            // [Util | W] -> [W | Util] hi/lo MN-major B blocks (W block 0, Util block 1); saved: -W (bf16 tile)
+            // and Util (fp32)
             {
                 const bool isW = c.trow < 64;
+                const int tt = c.trow & 63;
 #pragma unroll
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * c.wh + h2;
@@ -858,7 +918,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                     tmem_ld16(c.tl + (isW ? TM_W : TM_UT) + 16 * cg, v);
                     tmem_wait_ld();
                     const uint32_t blk = isW ? 0u : 8192u;
-                    st16_split(X + pl::WU + blk, X + pl::WU + 16384 + blk, c.trow & 63, cg, v);
+                    st16_split(X + pl::WU + blk, X + pl::WU + 16384 + blk, tt, cg, v);
+                    if (isW) {
+                        float nw[16];
+#pragma unroll
+                        for (int e = 0; e < 16; e++) nw[e] = -v[e];
+                        st16_bf16(svq + sv::NW, tt, cg, nw);
+                    } else {
+                        float4* du = reinterpret_cast<float4*>(svq + sv::UT) + tt * 16 + 4 * cg;
+#pragma unroll
+                        for (int e = 0; e < 4; e++)
+                            du[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                    }
                 }
             }
             smem_to_tc();
@@ -881,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             // lanes 0..63: Phi = diag(E) - Bhat^T W and Delta out; lanes 64..127: Qc = Ctil - P W (hi/lo, natural)
             if (c.trow < 64) {
                 const int i = c.trow;
-                float* dphi = p.phi + ((size_t)q * 64 + i) * 64;
+                unsigned char* phq = p.phi + (size_t)q * 16384;
                 float* ddl = p.dlt + ((size_t)q * 64 + i) * 64;
                 const float eci = c.KT->EC[i];
 #pragma unroll
@@ -893,11 +964,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; e++) a[e] = (c0 + e == i ? eci : 0.f) - a[e];
+                    st16_split(phq, phq + 8192, i, c0 >> 4, a);
 #pragma unroll
-                    for (int e = 0; e < 16; e += 4) {
-                        *reinterpret_cast<float4*>(dphi + c0 + e) = make_float4(a[e], a[e + 1], a[e + 2], a[e + 3]);
+                    for (int e = 0; e < 16; e += 4)
                         *reinterpret_cast<float4*>(ddl + c0 + e) = make_float4(b[e], b[e + 1], b[e + 2], b[e + 3]);
-                    }
                 }
             } else {
                 // the P W rows sit in lanes 0..63; the lanes 64..127 threads read them through the copy below
@@ -964,44 +1034,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
 }
 
 // ================================================================= pass 2: chain
-// One CTA per (batch, head) unit, 256 threads: thread = (rows 2 ip, 2 ip + 1 with ip = r >> 3, value columns
-// 8 (r & 7) .. + 7), 16 outputs in packed fp32x2 accumulators.  Forward: S_0 = h0, st[k] = S_k,
-// S_{k+1} = Phi_k S_k + Delta_k.  Reverse: dS = dhT, dst[k] = dS, dS <- Phi_k^T dS + Y_k; dh0 = dS.  The next
-// chunk's Phi (four float4 per thread) and Delta / Y rows are loaded into registers while the current step
-// computes, then stored into the other of two shared-memory buffers whose rows are padded to kAS floats (both
-// Phi S and Phi^T dS read them without bank conflicts).  Gated mode: Phi = diag(E), elementwise.
-constexpr uint32_t CHAIN_SMEM = 4 * 64 * kAS * 4;
-
-template <bool DELTA>
-__global__ void __launch_bounds__(256) chunk_chain_kernel(const __grid_constant__ CbParams p)
+// Gated mode: Phi = diag(E) and the chain is elementwise.  One CTA per (batch, head) unit, 256 threads, thread =
+// rows 2 ip, 2 ip + 1 (ip = r >> 3) x value columns 8 (r & 7) .. + 7.  Forward: S_0 = h0, st[k] = S_k,
+// S_{k+1} = E_k (.) S_k + Delta_k.  Reverse: dS = dhT, dst[k] = dS, dS <- E_k (.) dS + Y_k; dh0 = dS.
+__global__ void __launch_bounds__(256) chunk_chain_gated_kernel(const __grid_constant__ CbParams p)
 {
-    extern __shared__ __align__(16) unsigned char chain_smem[];
-    typedef float Mat[64][kAS];
-    Mat* Ph = reinterpret_cast<Mat*>(chain_smem);                     // [2]
-    Mat* Sv = reinterpret_cast<Mat*>(chain_smem + 2 * 64 * kAS * 4);  // [2]
     const int u = blockIdx.x, r = threadIdx.x, i0 = 2 * (r >> 3), j0 = 8 * (r & 7);
     const int dk = p.dk, dv = p.dv_, nk = p.nchunks;
     const size_t qb = (size_t)u * nk;
-    // Phi of the next step (pn) and of the one after (pn2), in registers; pn is stored into the next step's
-    // shared buffer once the current step has computed, then pn2 moves up and the following Phi is loaded
-    float4 pn[4], pn2[4];
-    auto load_phi = [&](int k, float4 (&dst)[4]) {
-        const float4* src = reinterpret_cast<const float4*>(p.phi + (qb + k) * 4096);
-#pragma unroll
-        for (int m = 0; m < 4; m++) dst[m] = src[r + 256 * m];
-    };
-    auto store_phi = [&](int buf, const float4 (&src)[4]) {
-#pragma unroll
-        for (int m = 0; m < 4; m++) {
-            const int e = r + 256 * m, row = e >> 4, c4 = (e & 15) * 4;
-            *reinterpret_cast<float4*>(&Ph[buf][row][c4]) = src[m];
-        }
-    };
-    auto shift = [&]() {
-#pragma unroll
-        for (int m = 0; m < 4; m++) pn[m] = pn2[m];
-    };
-    // the thread's 2 x 8 block of a record: rows i0, i0 + 1, columns j0 .. j0 + 7
     auto rec = [&](const float* base, int k, float4 (&v)[4]) {
         const float* src = base + (qb + k) * 4096 + i0 * 64 + j0;
         v[0] = *reinterpret_cast<const float4*>(src);
@@ -1016,120 +1056,43 @@ __global__ void __launch_bounds__(256) chunk_chain_kernel(const __grid_constant_
         *reinterpret_cast<float4*>(dst + 64) = make_float4(x[4].x, x[4].y, x[5].x, x[5].y);
         *reinterpret_cast<float4*>(dst + 68) = make_float4(x[6].x, x[6].y, x[7].x, x[7].y);
     };
-    auto to2 = [](const float4 (&v)[4], float2 (&x)[8]) {
+    auto load_in = [&](const float* src, float2 (&s)[8]) {
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
-            x[2 * e] = make_float2(v[e].x, v[e].y);
-            x[2 * e + 1] = make_float2(v[e].z, v[e].w);
+        for (int e = 0; e < 8; e++) {
+            const int i = i0 + (e >> 2), j = j0 + 2 * (e & 3);
+            const bool in = src && i < dk;
+            s[e] = make_float2(in && j < dv ? src[((size_t)u * dk + i) * dv + j] : 0.f,
+                               in && j + 1 < dv ? src[((size_t)u * dk + i) * dv + j + 1] : 0.f);
         }
     };
-    auto put_sv = [&](int buf, const float2 (&x)[8]) {
-        *reinterpret_cast<float4*>(&Sv[buf][i0][j0]) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
-        *reinterpret_cast<float4*>(&Sv[buf][i0][j0 + 4]) = make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
-        *reinterpret_cast<float4*>(&Sv[buf][i0 + 1][j0]) = make_float4(x[4].x, x[4].y, x[5].x, x[5].y);
-        *reinterpret_cast<float4*>(&Sv[buf][i0 + 1][j0 + 4]) = make_float4(x[6].x, x[6].y, x[7].x, x[7].y);
-    };
-    // a (+)= P S over the step's buffers; P read as Phi (forward) or Phi^T (reverse)
-    auto step = [&](int buf, bool transpose, float2 (&a)[8]) {
-#pragma unroll 4
-        for (int m = 0; m < 64; m++) {
-            const float p0 = transpose ? Ph[buf][m][i0] : Ph[buf][i0][m];
-            const float p1 = transpose ? Ph[buf][m][i0 + 1] : Ph[buf][i0 + 1][m];
-            const float4 s0 = *reinterpret_cast<const float4*>(&Sv[buf][m][j0]);
-            const float4 s1 = *reinterpret_cast<const float4*>(&Sv[buf][m][j0 + 4]);
-            const float2 q0 = make_float2(p0, p0), q1 = make_float2(p1, p1);
-            const float2 sa = make_float2(s0.x, s0.y), sb = make_float2(s0.z, s0.w);
-            const float2 sc = make_float2(s1.x, s1.y), sd = make_float2(s1.z, s1.w);
-            a[0] = __ffma2_rn(q0, sa, a[0]); a[1] = __ffma2_rn(q0, sb, a[1]);
-            a[2] = __ffma2_rn(q0, sc, a[2]); a[3] = __ffma2_rn(q0, sd, a[3]);
-            a[4] = __ffma2_rn(q1, sa, a[4]); a[5] = __ffma2_rn(q1, sb, a[5]);
-            a[6] = __ffma2_rn(q1, sc, a[6]); a[7] = __ffma2_rn(q1, sd, a[7]);
+    // s <- E (.) s + d, E of the chunk's rows i0, i0 + 1
+    auto advance = [&](int k, const float4 (&d)[4], float2 (&s)[8]) {
+        const float e0 = p.ec[(qb + k) * 64 + i0], e1 = p.ec[(qb + k) * 64 + i0 + 1];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float ec = e < 2 ? e0 : e1;
+            const float4 dd = d[e];
+            s[2 * e] = __ffma2_rn(make_float2(ec, ec), s[2 * e], make_float2(dd.x, dd.y));
+            s[2 * e + 1] = __ffma2_rn(make_float2(ec, ec), s[2 * e + 1], make_float2(dd.z, dd.w));
         }
     };
     float2 s[8];
-#pragma unroll
-    for (int e = 0; e < 8; e++) {
-        const int i = i0 + (e >> 2), j = j0 + 2 * (e & 3);
-        const bool in = p.h0 && i < dk;
-        s[e] = make_float2(in && j < dv ? p.h0[((size_t)u * dk + i) * dv + j] : 0.f,
-                           in && j + 1 < dv ? p.h0[((size_t)u * dk + i) * dv + j + 1] : 0.f);
-    }
-    // ---- forward (records of step k + 1 and Phi of step k + 2 in flight while step k computes)
     float4 d[4], dn[4];
+    load_in(p.h0, s);
     rec(p.dlt, 0, d);
-    if (DELTA) {
-        load_phi(0, pn);
-        store_phi(0, pn);
-        if (nk > 1) load_phi(1, pn);
-        if (nk > 2) load_phi(2, pn2);
-    }
     for (int k = 0; k < nk; k++) {
-        const int b = k & 1;
         put(p.st, k, s);
         if (k + 1 < nk) rec(p.dlt, k + 1, dn);
-        if (DELTA) {
-            put_sv(b, s);
-            __syncthreads();   // Ph[b], Sv[b] complete; step k - 1's reads of the other buffers are done
-            float2 a[8];
-            to2(d, a);
-            step(b, false, a);
-            if (k + 1 < nk) store_phi(b ^ 1, pn);
-            shift();
-            if (k + 3 < nk) load_phi(k + 3, pn2);
-#pragma unroll
-            for (int e = 0; e < 8; e++) s[e] = a[e];
-        } else {
-            float2 a[8];
-            to2(d, a);
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const float ec = p.ec[(qb + k) * 64 + i0 + (e >> 2)];
-                s[e] = __ffma2_rn(make_float2(ec, ec), s[e], a[e]);
-            }
-        }
+        advance(k, d, s);
 #pragma unroll
         for (int e = 0; e < 4; e++) d[e] = dn[e];
     }
-    // ---- reverse
-#pragma unroll
-    for (int e = 0; e < 8; e++) {
-        const int i = i0 + (e >> 2), j = j0 + 2 * (e & 3);
-        const bool in = p.dhT && i < dk;
-        s[e] = make_float2(in && j < dv ? p.dhT[((size_t)u * dk + i) * dv + j] : 0.f,
-                           in && j + 1 < dv ? p.dhT[((size_t)u * dk + i) * dv + j + 1] : 0.f);
-    }
-    __syncthreads();
+    load_in(p.dhT, s);
     rec(p.ych, nk - 1, d);
-    if (DELTA) {
-        load_phi(nk - 1, pn);
-        store_phi((nk - 1) & 1, pn);
-        if (nk > 1) load_phi(nk - 2, pn);
-        if (nk > 2) load_phi(nk - 3, pn2);
-    }
     for (int k = nk - 1; k >= 0; k--) {
-        const int b = k & 1;
         put(p.dst, k, s);
         if (k > 0) rec(p.ych, k - 1, dn);
-        if (DELTA) {
-            put_sv(b, s);
-            __syncthreads();
-            float2 a[8];
-            to2(d, a);
-            step(b, true, a);
-            if (k > 0) store_phi(b ^ 1, pn);
-            shift();
-            if (k > 2) load_phi(k - 3, pn2);
-#pragma unroll
-            for (int e = 0; e < 8; e++) s[e] = a[e];
-        } else {
-            float2 a[8];
-            to2(d, a);
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const float ec = p.ec[(qb + k) * 64 + i0 + (e >> 2)];
-                s[e] = __ffma2_rn(make_float2(ec, ec), s[e], a[e]);
-            }
-        }
+        advance(k, d, s);
 #pragma unroll
         for (int e = 0; e < 4; e++) d[e] = dn[e];
     }
@@ -1141,6 +1104,191 @@ __global__ void __launch_bounds__(256) chunk_chain_kernel(const __grid_constant_
             if (i < dk && j + 1 < dv) p.dh0[((size_t)u * dk + i) * dv + j + 1] = s[e].y;
         }
     }
+}
+
+// Delta mode: the chain on the tensor cores.  One CTA per (batch, head) unit.  The prep writes each chunk's Phi as
+// two bf16 tiles, hi and lo (Phi ~ hi + lo to about 16 significant bits), in the 128-byte-swizzled [64][64] layout
+// the MMA reads, 16 KB per chunk; one bulk copy moves them into a ring of CT_NS stages, in the order the two sweeps
+// use them (chunks 0 .. nk - 1, then nk - 1 .. 0), CT_NS steps ahead.  The state (forward) or the adjoint
+// (reverse), X, sits in two bf16 tiles (hi, lo; rows = state row m, read MN-major as the B operand).  A step is
+//   D[:, 0:64 | 64:128] = Phi_hi [X_hi | X_lo]   (N = 128)    D[:, 0:64] += Phi_lo X_hi   (N = 64)
+//   X' = D[:, 0:64] + D[:, 64:128] + R           (R = Delta_k forward, Y_k reverse, fp32 records)
+// with Phi read K-major (Phi X) or MN-major (Phi^T X) from the same tiles; M = 128, rows 64 .. 127 are not used.
+// Warps 0, 1, 4, 5 hold TMEM lanes 0 .. 63 (the state rows): thread = row i = 32 (warp & 1) + lane, columns
+// 32 (warp >> 2) .. + 31.  Each reads its part of D, adds R (loaded a step ahead), writes the fp32 record
+// (st forward, dst reverse) and rebuilds its part of the tiles; thread 0 issues the MMAs and the copies.  Warps 2
+// and 3 exist only so that warps 4 and 5 map to TMEM lanes 0 .. 63; they leave after the set-up.
+constexpr int CT_NS = 4;
+constexpr uint32_t CT_STAGE = 16384;
+constexpr uint32_t CT_X = CT_NS * CT_STAGE;       // X hi tile, then X lo tile
+constexpr uint32_t CT_BAR = CT_X + 16384;          // full[CT_NS], mma, tmem base, abort
+constexpr uint32_t CHAIN_TC_SMEM = CT_BAR + 128 + 1024;
+constexpr int CT_THREADS = 192;
+
+__global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_tc_kernel(const __grid_constant__ CbParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + CT_BAR);
+    uint64_t* mmab = full + CT_NS;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(mmab + 1);   // [0] TMEM base, [1] abort
+    unsigned char* Xhi = sm + CT_X;
+    unsigned char* Xlo = Xhi + 8192;
+    const int u = blockIdx.x, r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const int dk = p.dk, dv = p.dv_, nk = p.nchunks, nseq = 2 * nk;
+    const size_t qb = (size_t)u * nk;
+    const unsigned char* phi = p.phi;
+    // sweep position n -> chunk: 0 .. nk - 1 forward, then nk - 1 .. 0
+    auto chunk_of = [&](int n) { return n < nk ? n : nseq - 1 - n; };
+    auto issue_copy = [&](int n) {
+        const int s = n % CT_NS;
+        mbar_arrive_expect_tx(&full[s], CT_STAGE);
+        bulk_g2s(sm + s * CT_STAGE, phi + (qb + chunk_of(n)) * CT_STAGE, CT_STAGE, &full[s]);
+    };
+    if (r == 0) {
+        for (int s = 0; s < CT_NS; s++) mbar_init(&full[s], 1);
+        mbar_init(mmab, 1);
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&misc[0], 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2 || warp == 3) return;
+    const uint32_t tb = misc[0];
+    int issued = nseq < CT_NS ? nseq : CT_NS;
+    if (r == 0) {
+        for (int n = 0; n < issued; n++) issue_copy(n);
+        for (int n = 1; n < 3 && n < nseq; n++)
+            prefetch_l2_bulk((n < nk ? p.dlt : p.ych) + (qb + chunk_of(n)) * 4096, 16384);
+    }
+    const int i = 32 * (warp & 1) + lane, j0 = 32 * (warp >> 2);
+    const uint32_t tl = tb + ((uint32_t)(32 * (warp & 1)) << 16);
+    uint32_t* abortf = &misc[1];
+
+    auto rec = [&](const float* base, int k, float (&v)[32]) {
+        const float4* src = reinterpret_cast<const float4*>(base + (qb + k) * 4096 + i * 64 + j0);
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const float4 t = src[e];
+            v[4 * e] = t.x; v[4 * e + 1] = t.y; v[4 * e + 2] = t.z; v[4 * e + 3] = t.w;
+        }
+    };
+    auto put = [&](float* base, int k, const float (&v)[32]) {
+        float4* dst = reinterpret_cast<float4*>(base + (qb + k) * 4096 + i * 64 + j0);
+#pragma unroll
+        for (int e = 0; e < 8; e++) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+    };
+    auto load_in = [&](const float* src, float (&v)[32]) {
+#pragma unroll
+        for (int e = 0; e < 32; e++) {
+            const int j = j0 + e;
+            v[e] = src && i < dk && j < dv ? src[((size_t)u * dk + i) * dv + j] : 0.f;
+        }
+    };
+    auto tiles = [&](const float (&v)[32]) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            float a[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) a[e] = v[8 * q + e];
+            st_row8_split(Xhi, Xlo, i, (j0 >> 3) + q, a);
+        }
+    };
+    // one step of either sweep: x <- P x + R with P = Phi (forward) or Phi^T (reverse); false after an abort
+    auto step = [&](int n, float (&x)[32], const float (&R)[32]) -> bool {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(1, 128);
+        tc_fence_after();
+        const bool transpose = n >= nk;
+        const int s = n % CT_NS;
+        if (r == 0) {
+            if (wait_or_abort(&full[s], (uint32_t)(n / CT_NS) & 1u, abortf, p.status, p.wait_ns)) {
+                tc_fence_after();
+                const uint32_t a = smem_u32(sm + s * CT_STAGE), xb = smem_u32(Xhi);
+                mma_tiles(tb, a, transpose, 8192, 0, xb, true, 8192, 0, 4, idesc_bf16(128, 128, transpose, true),
+                          false);
+                mma_tiles(tb, a + 8192, transpose, 8192, 0, xb, true, 8192, 0, 4,
+                          idesc_bf16(128, 64, transpose, true), true);
+                mma_commit(mmab);
+            } else {
+                atomicExch(p.status + 2, 300u + (uint32_t)n);
+            }
+        }
+        if (r == 0 && n + 3 < nseq) {
+            // the fp32 record of step n + 3 into L2, so that its register loads (issued a step ahead) hit there
+            const int m = n + 3;
+            prefetch_l2_bulk((m < nk ? p.dlt : p.ych) + (qb + chunk_of(m)) * 4096, 16384);
+        }
+        if (!wait_or_abort(mmab, (uint32_t)n & 1u, abortf, p.status, p.wait_ns)) return false;
+        tc_fence_after();
+        if (r == 0 && issued < nseq) issue_copy(issued++);   // the stage just read is free
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            float a[16], b[16];
+            tmem_ld16(tl + j0 + 16 * h, a);         // Phi_hi X_hi + Phi_lo X_hi
+            tmem_ld16(tl + 64 + j0 + 16 * h, b);    // Phi_hi X_lo
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; e++) x[16 * h + e] = (a[e] + b[e]) + R[16 * h + e];
+        }
+        return true;
+    };
+
+    float x[32], R[32], Rn[32];
+    bool ok = true;
+    // ---- forward: st[k] = S_k, S_{k+1} = Phi_k S_k + Delta_k
+    load_in(p.h0, x);
+    rec(p.dlt, 0, R);
+    put(p.st, 0, x);
+    tiles(x);
+    for (int k = 0; k < nk && ok; k++) {
+        if (k + 1 < nk) rec(p.dlt, k + 1, Rn);
+        ok = step(k, x, R);
+        if (!ok) break;
+        if (k + 1 < nk) {
+            put(p.st, k + 1, x);
+            tiles(x);   // the step's MMAs have completed: the tiles are free
+#pragma unroll
+            for (int e = 0; e < 32; e++) R[e] = Rn[e];
+        }
+    }
+    // ---- reverse: dst[k] = dS_{k+1}, dS_k = Phi_k^T dS_{k+1} + Y_k, dh0 = dS_0
+    if (ok) {
+        load_in(p.dhT, x);
+        rec(p.ych, nk - 1, R);
+        put(p.dst, nk - 1, x);
+        tiles(x);
+        for (int k = nk - 1; k >= 0; k--) {
+            if (k > 0) rec(p.ych, k - 1, Rn);
+            ok = step(nseq - 1 - k, x, R);
+            if (!ok) break;
+            if (k > 0) {
+                put(p.dst, k - 1, x);
+                tiles(x);
+#pragma unroll
+                for (int e = 0; e < 32; e++) R[e] = Rn[e];
+            }
+        }
+        if (ok && p.dh0) {
+#pragma unroll
+            for (int e = 0; e < 32; e++) {
+                const int j = j0 + e;
+                if (i < dk && j < dv) p.dh0[((size_t)u * dk + i) * dv + j] = x[e];
+            }
+        }
+    }
+    // wind down: after an abort, let the copies still in flight land before the CTA leaves
+    if (r == 0 && *(volatile uint32_t*)abortf) {
+        for (int n = issued - CT_NS < 0 ? 0 : issued - CT_NS; n < issued; n++)
+            mbar_wait(&full[n % CT_NS], (uint32_t)(n / CT_NS) & 1u, nullptr, p.wait_ns);
+    }
+    tc_fence_before();
+    named_bar_sync(1, 128);
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tb, 128);
 }
 
 // ================================================================= pass 3: gradients
@@ -1155,11 +1303,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
     const unsigned char* sC = c.sm + OFF_STAGE + ST_C;
     const unsigned char* sV = c.sm + OFF_STAGE + ST_V;
     const unsigned char* sDO = c.sm + OFF_STAGE + ST_DO;
-    uint32_t full_phase = 0;
+    uint32_t full_phase = 0, full2_phase = 0;
     int q = blockIdx.x;
-    int pending = -1;
-    if (c.r == 0 && q < p.nq) issue_tma(p, S, c.sm, q);
-    if (q < p.nq) pending = q;
+    int pending = -1, pending2 = -1;   // chunks whose loads (stage, saved front) are in flight
+    if (c.r == 0 && q < p.nq) {
+        issue_tma(p, S, c.sm, q);
+        if (DELTA) issue_saved(p, S, c.sm, q);
+    }
+    if (q < p.nq) {
+        pending = q;
+        if (DELTA) pending2 = q;
+    }
     const int trow = c.trow, tt = trow & 63, isK = trow >> 6, wh = c.wh;
     CB_STAMP_INIT;
     for (; q < p.nq; q += gridDim.x) {
@@ -1168,43 +1322,47 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         CB_STAMP(1, 0);
         load_small(c, p, bb, h, t0);
         if (c.r == 0) {
-            // this chunk's S, dS' records (read after the front) and the next chunk's tiles towards L2
+            // this chunk's S, dS' (and Util) records and the next chunk's tiles towards L2
             prefetch_l2_bulk(p.st + (size_t)q * 4096, 16384);
             prefetch_l2_bulk(p.dst + (size_t)q * 4096, 16384);
+            if (DELTA) prefetch_l2_bulk(p.sv + (size_t)q * sv::BYTES + sv::UT, 16384);
             if (q + (int)gridDim.x < p.nq) prefetch_tma(p, q + gridDim.x);
         }
         if (c.warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && c.lane == 0)
             atomicExch(p.status + 2, 2u);
+        if (DELTA && c.warp == 1 && !wait_or_abort(&S.full2, full2_phase, &S.abort, p.status, p.wait_ns) &&
+            c.lane == 0)
+            atomicExch(p.status + 2, 3u);
         bar_all();
         if (*(volatile uint32_t*)&S.abort) break;
         full_phase ^= 1;
         pending = -1;
+        if (DELTA) {
+            full2_phase ^= 1;
+            pending2 = -1;
+        }
         CB_STAMP(1, 1);
         front_scan(c);
         bar_all();
         const int t = c.r & 63, cq = c.r >> 6;
         CB_STAMP(1, 2);
 
-        // ---- front: level operands, R, the level product, near pairs, P (and M, the solve)
-        front_operands(c, X + gl::A1, X + gl::B1, true);
-        CB_STAMP(1, 16);
-        if (DELTA) write_R(c, X + gl::LR, X + gl::LRL);
-        CB_STAMP(1, 17);
-        smem_to_tc();
-        if (c.r == 0) {
-            issue_level(c.tbase, X + gl::A1, X + gl::B1);
-            mma_commit(&S.mma);
+        // ---- front.  Delta: P, -N, Dinv, K and -W arrived with the saved front (the prep pass computed them);
+        // gated: the level operands, the level product, the near pairs and P
+        if (!DELTA) {
+            front_operands(c, X + gl::A1, X + gl::B1, true);
+            smem_to_tc();
+            if (c.r == 0) {
+                issue_level(c.tbase, X + gl::A1, X + gl::B1);
+                mma_commit(&S.mma);
+            }
+            front_near(c, fptr(X, gl::NEAR), false);
+            bar_all();
+            if (!mma_wait(c, p, 7)) break;
+            front_solve<false>(c, p, X + gl::NEAR, X + gl::P, X + gl::LR, X + gl::LRL, X + gl::MS, X + gl::DINV,
+                               X + gl::NA, X + gl::X0, nullptr);
+            bar_all();
         }
-        CB_STAMP(1, 18);
-        front_near(c, fptr(X, gl::NEAR), DELTA);
-        CB_STAMP(1, 19);
-        bar_all();
-        if (!mma_wait(c, p, 7)) break;
-        CB_STAMP(1, 3);
-        if (!front_solve<DELTA>(c, p, X + gl::NEAR, X + gl::P, X + gl::LR, X + gl::LRL, X + gl::MS, X + gl::DINV,
-                                X + gl::NA, X + gl::X0, DELTA ? fptr(X, gl::KP) : nullptr))
-            break;
-        if (!DELTA) bar_all();
         CB_STAMP(1, 4);
 
         // ---- S, dS' of the chunk (fp32 from the chain) -> hi/lo tiles [i][j]; sum_j dS'[i][j] S[i][j]
@@ -1234,18 +1392,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             }
         }
         if (DELTA) {
-            // -W (plain bf16, K-major [t][i]) for U = Util - W S
+            // Util (saved fp32) into TMEM as the start of U = Util - W S; -W came with the saved front
             if (!isK) {
+                const float4* urow =
+                    reinterpret_cast<const float4*>(p.sv + (size_t)q * sv::BYTES + sv::UT) + tt * 16;
 #pragma unroll
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
                     float v[16];
-                    tmem_ld16(c.tl + TM_W + 16 * cg, v);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; e++) v[e] = -v[e];
-                    st16_bf16(X + gl::NW, tt, cg, v);
+                    for (int e = 0; e < 4; e++) {
+                        const float4 x = urow[4 * cg + e];
+                        v[4 * e] = x.x; v[4 * e + 1] = x.y; v[4 * e + 2] = x.z; v[4 * e + 3] = x.w;
+                    }
+                    tmem_st16(c.tl + TM_UT + 16 * cg, v);
                 }
+                tmem_wait_st();
             }
             smem_to_tc();
             if (c.r == 0) {
@@ -1480,7 +1642,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         }
         // the 16-block level's operands again as fp16 hi/lo pairs (their space was reused)
         CB_STAMP(1, 9);
-        front_operands(c, X + gl::A1, X + gl::B1, true, X + gl::A1L, X + gl::B1L, false);
+        front_operands(c, X + gl::A1, X + gl::B1, true, X + gl::A1L, X + gl::B1L, DELTA);
         smem_to_tc();
         if (c.r == 0) {
             // dA1 = A_d B1 (TMEM 192..255): rows 0..63 -> dc, 64..127 -> db (row side)
@@ -1814,7 +1976,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             // dg = reverse cumulative sum of dG over the chunk's tokens
             float a = 0.f, b = 0.f;
             const int t2 = 2 * c.lane;
-#pragma unroll
             a = S.dgp[0][t2];
             b = S.dgp[0][t2 + 1];
             // suffix sums: x = a + b per lane, scan from the top
@@ -1842,15 +2003,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         bar_all();
         tc_fence_after();
         if (q + (int)gridDim.x < p.nq) {
-            if (c.r == 0) issue_tma(p, S, c.sm, q + gridDim.x);
+            if (c.r == 0) {
+                issue_tma(p, S, c.sm, q + gridDim.x);
+                if (DELTA) issue_saved(p, S, c.sm, q + gridDim.x);
+            }
             pending = q + gridDim.x;
+            if (DELTA) pending2 = q + gridDim.x;
         }
         CB_STAMP(1, 14);
 #ifdef GDN_CHUNK_DEBUG
         if (c.r == 0 && blockIdx.x == 0) g_cb_stamps[1][31] += 1;
 #endif
     }
-    teardown(c, p, pending, full_phase);
+    teardown(c, p, pending, full_phase, pending2, full2_phase);
 }
 
 // dA_log[h][i] = A[h][i] sum over batch rows and chunks of the chunk partials (fixed order)
@@ -1887,7 +2052,8 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     p.g = (const __nv_bfloat16*)a.g;
     p.beta = (const __nv_bfloat16*)a.beta;
     p.A_log = a.A_log;
-    p.phi = (float*)(ws + Lw.cb_phi_off);
+    p.phi = ws + Lw.cb_phi_off;
+    p.sv = ws + Lw.cb_sv_off;
     p.dlt = (float*)(ws + Lw.cb_dlt_off);
     p.ych = (float*)(ws + Lw.cb_y_off);
     p.ec = (float*)(ws + Lw.cb_ec_off);
@@ -1917,7 +2083,7 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
         if ((e = set_smem(chunk_prep_kernel<false>, prep_bytes)) != cudaSuccess) return e;
         if ((e = set_smem(chunk_grad_kernel<true>, grad_bytes)) != cudaSuccess) return e;
         if ((e = set_smem(chunk_grad_kernel<false>, grad_bytes)) != cudaSuccess) return e;
-        if ((e = set_smem(chunk_chain_kernel<true>, CHAIN_SMEM)) != cudaSuccess) return e;
+        if ((e = set_smem(chunk_chain_tc_kernel, CHAIN_TC_SMEM)) != cudaSuccess) return e;
         attr = true;
     }
     int sms = 152;
@@ -1938,8 +2104,8 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     if (e != cudaSuccess) return e;
     CB_MARK("prep");
     const int units = a.B * a.H;
-    if (delta) chunk_chain_kernel<true><<<units, 256, CHAIN_SMEM, st>>>(p);
-    else chunk_chain_kernel<false><<<units, 256, 0, st>>>(p);
+    if (delta) chunk_chain_tc_kernel<<<units, CT_THREADS, CHAIN_TC_SMEM, st>>>(p);
+    else chunk_chain_gated_kernel<<<units, 256, 0, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     CB_MARK("chain");
     if (delta) chunk_grad_kernel<true><<<grid, kThreads, grad_bytes, st>>>(p);

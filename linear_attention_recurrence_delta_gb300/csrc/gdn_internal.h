@@ -53,6 +53,7 @@ struct WsLayout {
     size_t ts_e_off = 0;          // end gradients of the segments       [B*P, H, d_k, d_v]
     // chunked backward (gdn_chunk_bwd.cu): per chunk of 64 tokens, [B*H*chunks][64][64] fp32 records
     size_t cb_phi_off = 0;        // delta: the chunk's state transition Phi
+    size_t cb_sv_off = 0;         // delta: the front's results saved for the gradient pass (64 KB per chunk)
     size_t cb_dlt_off = 0;        // the state the chunk leaves from a zero start
     size_t cb_y_off = 0;          // the chunk's share of the entering state's adjoint
     size_t cb_st_off = 0;         // the state entering the chunk

@@ -157,14 +157,15 @@ def test_time_split_backward_workspace():
 
 
 def test_chunked_backward_workspace():
-    """The chunked backward (bf16, heads up to 64 wide, no option bits) keeps per chunk of 64 tokens five fp32
-    64 x 64 records in delta mode (transition, zero-start state, adjoint share, entering state, leaving adjoint),
-    four in gated mode, and two rows of 64 floats (decay, dA partial), after the 256-byte status word."""
-    for mode, nrec in (("delta", 5), ("gated", 4)):
+    """The chunked backward (bf16, heads up to 64 wide, no option bits) keeps per chunk of 64 tokens five 16 KB
+    64 x 64 records in delta mode (transition as bf16 hi/lo tiles, zero-start state, adjoint share, entering state,
+    leaving adjoint) plus the 64 KB of the front's results that the gradient pass reuses, four fp32 records in
+    gated mode, and two rows of 64 floats (decay, dA partial), after the 256-byte status word."""
+    for mode, per_chunk in (("delta", 5 * 16384 + 65536), ("gated", 4 * 16384)):
         for B, H, T, d in ((8, 16, 4096, 64), (1, 16, 32768, 64), (2, 3, 100, 56), (1, 1, 1, 8)):
             s = gdn.make_shape(B, H, T, d, d, mode, "bf16")
             nq = B * H * -(-T // 64)
-            want = 256 + nrec * nq * 16384 + 2 * -(-(nq * 256) // 256) * 256
+            want = 256 + per_chunk * nq + 2 * -(-(nq * 256) // 256) * 256
             assert gdn.gdn_workspace_bytes(s, 1) == want, (mode, B, H, T, d)
             p = gdn.gdn_plan(s, 1)
             assert (p.segments, p.fwd_kernel, p.bwd_kernel) == (1, gdn.GDN_KERNEL_NONE, gdn.GDN_BWD_TENSOR_CORE)
