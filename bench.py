@@ -5,7 +5,8 @@
 A step is one forward pass (gdn_fwd, every forward row of the chunked
 recurrence) over one batch of the named workload, inputs already resident in
 device memory; the line also carries the forward+backward throughput of the
-same shape (gdn_fwd followed by gdn_bwd), the end-to-end throughput through
+same shape (gdn_fwd_save followed by gdn_bwd_saved where the shape has the
+residual hand-off, else gdn_fwd followed by gdn_bwd), the end-to-end throughput through
 the C ABI with host buffers (host->device copies of the inputs and the
 device->host read of the outputs inside the timed region), the roofline of
 the dominant kernel, the clocks seen during the timed region and the fp64
@@ -550,9 +551,23 @@ def main():
 
     fwdbwd = None
     if not args.no_bwd:
-        def fb():
-            fwd()
-            bwd()
+        # training step: the forward keeps the chunked backward's residuals where the shape has them
+        n_saved = gdn.gdn_saved_bytes(s)
+        if n_saved:
+            saved = torch.empty(n_saved, dtype=torch.uint8, device="cuda")
+            ws2 = torch.empty(gdn.gdn_workspace_bytes(s, 2), dtype=torch.uint8, device="cuda")
+
+            def fb():
+                gdn.check(gdn.gdn_fwd_save(s, t["v"], t["b"], t["c"], t["g"], t["beta"], A_log, h0, o, hT, saved,
+                                           ws, stream=stream), "gdn_fwd_save")
+                gdn.check(gdn.gdn_bwd_saved(s, t["v"], t["b"], t["c"], t["g"], t["beta"], A_log, saved, t["dO"],
+                                            None, grads["dv"], grads["db"], grads["dc"], grads["dg"],
+                                            grads["dbeta"], grads["dA_log"], grads["dh0"], ws2, stream=stream),
+                          "gdn_bwd_saved")
+        else:
+            def fb():
+                fwd()
+                bwd()
         kb = max(3, args.steps // 4)
         fb_total, fb_launch = timed(fb, kb, 3)
         fb_ms = fb_total / kb
@@ -560,6 +575,8 @@ def main():
         fb_flops = chunk_flops(w) + chunk_flops(w, backward=True)
         fwdbwd = {"value": replicas.whole_job_tokens_per_s(tokens, world, fb_ms), "unit": "tokens/s",
                   "ms_per_step": fb_ms, "bwd_bytes": io_bytes(w, backward=True),
+                  "calls": "gdn_fwd_save + gdn_bwd_saved" if n_saved else "gdn_fwd + gdn_bwd",
+                  "saved_bytes": n_saved,
                   "roofline": roofline_of(fb_bytes, fb_flops, fb_ms, peaks, peak_kind)}
         gpu_launches += (fwd_launches(w) + bwd_launches(w)) * kb
 

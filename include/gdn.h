@@ -122,9 +122,10 @@ typedef struct {
     int io;          /* gdn_dtype_t of v, b, c, g, beta, o and the grads   */
 } gdn_shape_t;
 
-/* Bytes of workspace gdn_fwd (backward = 0) or gdn_bwd (backward = 1) needs
- * for this shape; 0 if the shape is invalid.  Always a multiple of 256 and
- * at least 256 (the device status word lives in the first bytes). */
+/* Bytes of workspace gdn_fwd (backward = 0), gdn_bwd (backward = 1) or
+ * gdn_bwd_saved (backward = 2) needs for this shape; 0 if the shape is invalid
+ * (for backward = 2: if gdn_saved_bytes(shape) is 0).  Always a multiple of
+ * 256 and at least 256 (the device status word lives in the first bytes). */
 size_t gdn_workspace_bytes(const gdn_shape_t* shape, int backward);
 
 /* How the library runs a shape.  Host only: it touches no device and is
@@ -198,6 +199,47 @@ gdn_status_t gdn_bwd(const gdn_shape_t* shape,
                      void* dv, void* db, void* dc, void* dg, void* dbeta,
                      float* dA_log, float* dh0,
                      void* ws, size_t ws_bytes, gdn_stream_t stream);
+
+/* Forward pass that also keeps what the chunked backward would otherwise
+ * recompute ("GDN & MLA Mechanism Deep-Dive", Step 5: each chunk's closed form
+ * is a function of its inputs and the state entering it).  Per chunk of 64
+ * tokens `saved` receives the entering state (fp32 64 x 64, 16 KB) and the
+ * results of the chunk's delta solve that the backward reuses (72 KB: the
+ * decay-weighted scores P, K, the block inverse D^-1 and N, W, Util; layout
+ * private to the library).  gdn_bwd_saved then takes them instead of running
+ * the forward sweep again.  Arguments and results are those of gdn_fwd, plus
+ * `saved`: device memory of at least gdn_saved_bytes(shape) bytes, 256-byte
+ * aligned, written completely by the call.  o and hT equal gdn_fwd's within
+ * the bf16 tolerance (the level products form K without beta, M = beta K
+ * after them, so the rounding differs).  Shapes: delta mode, bf16, d_k and
+ * d_v <= 64, no option bits but GDN_CHECK_FINITE, and a forward that runs as
+ * one tensor-core pass (gdn_plan(shape, 0): segments 1, GDN_KERNEL_TENSOR_CORE);
+ * gdn_saved_bytes is 0 for any other shape, and both calls return
+ * GDN_ERR_MODE for it.  GDN_ERR_NULL if saved is NULL, GDN_ERR_ALIGN if it is
+ * misaligned, GDN_ERR_WORKSPACE if saved_bytes is too small. */
+size_t gdn_saved_bytes(const gdn_shape_t* shape);
+
+gdn_status_t gdn_fwd_save(const gdn_shape_t* shape,
+                          const void* v, const void* b, const void* c,
+                          const void* g, const void* beta, const float* A_log,
+                          const float* h0, void* o, float* hT,
+                          void* saved, size_t saved_bytes,
+                          void* ws, size_t ws_bytes, gdn_stream_t stream);
+
+/* Backward pass from gdn_fwd_save's residuals: gdn_bwd's gradients, for the
+ * same shape and the same v, b, c, g, beta, A_log (h0 is not needed: the
+ * residuals hold the entering states).  `saved` is read only.  ws must hold at
+ * least gdn_workspace_bytes(shape, 2) bytes (smaller than the plain backward's:
+ * the states and solve results live in `saved`).  Errors as gdn_bwd, plus
+ * those of gdn_fwd_save for `saved`. */
+gdn_status_t gdn_bwd_saved(const gdn_shape_t* shape,
+                           const void* v, const void* b, const void* c,
+                           const void* g, const void* beta, const float* A_log,
+                           const void* saved, size_t saved_bytes,
+                           const void* dO, const float* dhT,
+                           void* dv, void* db, void* dc, void* dg, void* dbeta,
+                           float* dA_log, float* dh0,
+                           void* ws, size_t ws_bytes, gdn_stream_t stream);
 
 /* Backward pass that allocates nothing and needs no workspace argument.  The
  * pages describe no counterpart; this is a convenience of the library.  It is

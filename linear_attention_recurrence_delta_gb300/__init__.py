@@ -106,6 +106,12 @@ def load(path: str | None = None):
             lib.gdn_fwd.restype = ctypes.c_int
             lib.gdn_bwd.argtypes = [sp] + [vp] * 16 + [vp, sz, vp]
             lib.gdn_bwd.restype = ctypes.c_int
+            lib.gdn_saved_bytes.argtypes = [sp]
+            lib.gdn_saved_bytes.restype = sz
+            lib.gdn_fwd_save.argtypes = [sp] + [vp] * 9 + [vp, sz, vp, sz, vp]
+            lib.gdn_fwd_save.restype = ctypes.c_int
+            lib.gdn_bwd_saved.argtypes = [sp] + [vp] * 6 + [vp, sz] + [vp] * 9 + [vp, sz, vp]
+            lib.gdn_bwd_saved.restype = ctypes.c_int
             lib.gdn_bwd_noalloc.argtypes = [sp] + [vp] * 16 + [vp]
             lib.gdn_bwd_noalloc.restype = ctypes.c_int
             lib.gdn_bwd_noalloc_status.argtypes = [vp]
@@ -164,6 +170,32 @@ def gdn_bwd(shape, v, b, c, g, beta, A_log, h0, dO, dhT, dv, db, dc, dg, dbeta, 
     return int(load().gdn_bwd(ctypes.byref(shape), _ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(beta), _ptr(A_log),
                               _ptr(h0), _ptr(dO), _ptr(dhT), _ptr(dv), _ptr(db), _ptr(dc), _ptr(dg), _ptr(dbeta),
                               _ptr(dA_log), _ptr(dh0), _ptr(ws), wsb, _stream(stream)))
+
+
+def gdn_saved_bytes(shape: gdn_shape_t) -> int:
+    """Bytes of the residuals gdn_fwd_save keeps for gdn_bwd_saved (0: the shape has none)."""
+    return int(load().gdn_saved_bytes(ctypes.byref(shape)))
+
+
+def gdn_fwd_save(shape, v, b, c, g, beta, A_log, h0, o, hT, saved, ws, saved_bytes=None, ws_bytes=None,
+                 stream=None) -> int:
+    """gdn_fwd that also writes the chunked backward's residuals into `saved`; returns the status code."""
+    svb = _nbytes(saved) if saved_bytes is None and saved is not None else (saved_bytes or 0)
+    wsb = _nbytes(ws) if ws_bytes is None and ws is not None else (ws_bytes or 0)
+    return int(load().gdn_fwd_save(ctypes.byref(shape), _ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(beta),
+                                   _ptr(A_log), _ptr(h0), _ptr(o), _ptr(hT), _ptr(saved), svb, _ptr(ws), wsb,
+                                   _stream(stream)))
+
+
+def gdn_bwd_saved(shape, v, b, c, g, beta, A_log, saved, dO, dhT, dv, db, dc, dg, dbeta, dA_log, dh0, ws,
+                  saved_bytes=None, ws_bytes=None, stream=None) -> int:
+    """The backward from gdn_fwd_save's residuals; returns the status code."""
+    svb = _nbytes(saved) if saved_bytes is None and saved is not None else (saved_bytes or 0)
+    wsb = _nbytes(ws) if ws_bytes is None and ws is not None else (ws_bytes or 0)
+    return int(load().gdn_bwd_saved(ctypes.byref(shape), _ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(beta),
+                                    _ptr(A_log), _ptr(saved), svb, _ptr(dO), _ptr(dhT), _ptr(dv), _ptr(db),
+                                    _ptr(dc), _ptr(dg), _ptr(dbeta), _ptr(dA_log), _ptr(dh0), _ptr(ws), wsb,
+                                    _stream(stream)))
 
 
 def gdn_bwd_noalloc(shape, v, b, c, g, beta, A_log, h0, dO, dhT, dv, db, dc, dg, dbeta, dA_log, dh0,

@@ -35,6 +35,8 @@ struct TcParams {
     int logits;   // g, beta arrive before their sigmoid
     int starve_chunk;        // failure-path test hook: the loads of this chunk are never issued (-1: none)
     uint64_t wait_ns;        // limit of every bounded wait
+    float* st;               // saving forward: the states entering the chunks
+    unsigned char* sv;       // saving forward: the solve's results per chunk
 };
 
 // Limit of a bounded wait: a chunk's loads or products take microseconds, so two

@@ -92,23 +92,30 @@ int bwd_split(const gdn_shape_t& s, int logits, int norm)
     return tsplit_factor(s, 1);
 }
 
-// the chunked backward's per-chunk records, placed from `off`
-static size_t place_chunk_bwd(const gdn_shape_t& s, WsLayout& L, size_t off)
+// the chunked backward's per-chunk records, placed from `off`; with the residuals of a saving forward
+// (`from_saved`) the entering states and the solve's results are the caller's, not the workspace's
+static size_t place_chunk_bwd(const gdn_shape_t& s, WsLayout& L, size_t off, bool from_saved)
 {
     const size_t nq = (size_t)s.B * s.H * (size_t)((s.T + 63) / 64);
     const size_t rec = nq * 64 * 64 * sizeof(float);
     if (s.mode == GDN_DELTA) {
         L.cb_phi_off = off;
         off = round_up(off + rec, 256);
-        L.cb_sv_off = off;
-        off = round_up(off + nq * 65536, 256);
+        if (!from_saved) {
+            L.cb_sv_off = off;
+            off = round_up(off + nq * kSavedSolveBytes, 256);
+        }
     }
-    L.cb_dlt_off = off;
-    off = round_up(off + rec, 256);
+    if (!from_saved) {
+        L.cb_dlt_off = off;
+        off = round_up(off + rec, 256);
+    }
     L.cb_y_off = off;
     off = round_up(off + rec, 256);
-    L.cb_st_off = off;
-    off = round_up(off + rec, 256);
+    if (!from_saved) {
+        L.cb_st_off = off;
+        off = round_up(off + rec, 256);
+    }
     L.cb_dst_off = off;
     off = round_up(off + rec, 256);
     L.cb_ec_off = off;
@@ -123,7 +130,7 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm, int logits)
     WsLayout L;
     size_t off = 256;  // status word
     if (backward && chunk_bwd_applies(s, logits, norm)) {
-        L.total = place_chunk_bwd(s, L, off);
+        L.total = place_chunk_bwd(s, L, off, backward == 2);
         return L;
     }
     const int P = s.T > 0 ? (backward ? bwd_split(s, logits, norm) : tsplit_factor(s, 0)) : 1;
@@ -247,6 +254,19 @@ static cudaError_t fwd_core(const Args& a, cudaStream_t st)
     }
 }
 
+// Shapes whose forward can keep the chunked backward's residuals: delta mode on the chunked backward, and a
+// forward that runs as one tcgen05 pass (no time split, neither the decode nor the token-serial kernel).
+static bool saved_applies(const gdn_shape_t& s, int logits, int norm)
+{
+    if (s.mode != GDN_DELTA || !chunk_bwd_applies(s, logits, norm) || tsplit_factor(s, 0) != 1) return false;
+    return fwd_kernel_of(make_args(&s)) == GDN_KERNEL_TENSOR_CORE;
+}
+
+static size_t saved_bytes_of(const gdn_shape_t& s)
+{
+    return (size_t)s.B * s.H * (size_t)((s.T + 63) / 64) * (kSavedStateBytes + kSavedSolveBytes);
+}
+
 }  // namespace gdn
 
 using namespace gdn;
@@ -280,12 +300,23 @@ extern "C" size_t gdn_workspace_bytes(const gdn_shape_t* shape_in, int backward)
     if (!shape_ok(*shape)) return 0;
     if ((shape->mode != GDN_GATED && shape->mode != GDN_DELTA) || (shape->io != GDN_F32 && shape->io != GDN_BF16))
         return 0;
-    return ws_layout(*shape, backward ? 1 : 0, norm, logits).total;
+    if (backward == 2 && !saved_applies(sh, logits, norm)) return 0;
+    return ws_layout(*shape, backward == 2 ? 2 : (backward ? 1 : 0), norm, logits).total;
 }
 
-extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, const void* b, const void* c,
-                                const void* g, const void* beta, const float* A_log, const float* h0,
-                                void* o, float* hT, void* ws, size_t ws_bytes, gdn_stream_t stream)
+extern "C" size_t gdn_saved_bytes(const gdn_shape_t* shape_in)
+{
+    gdn_shape_t sh;
+    int logits = 0, norm = 0;
+    if (!shape_in || !split_mode(shape_in, &sh, &logits, &norm)) return 0;
+    if (!shape_ok(sh) || sh.io != GDN_BF16 || !saved_applies(sh, logits, norm)) return 0;
+    return saved_bytes_of(sh);
+}
+
+static gdn_status_t fwd_impl(const gdn_shape_t* shape_in, const void* v, const void* b, const void* c,
+                             const void* g, const void* beta, const float* A_log, const float* h0, void* o,
+                             float* hT, void* saved, size_t saved_bytes, bool saving, void* ws, size_t ws_bytes,
+                             gdn_stream_t stream)
 {
     gdn_shape_t sh;
     int logits = 0, norm = 0, check = 0;
@@ -297,6 +328,12 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, cons
     if (!o && shape->T > 0) return GDN_ERR_NULL;
     const size_t ioa = shape->io == GDN_BF16 ? 16 : 4;
     if (!aligned(o, ioa) || (hT && !aligned(hT, 16))) return GDN_ERR_ALIGN;
+    if (saving) {
+        if (!saved) return GDN_ERR_NULL;
+        if (!saved_applies(sh, logits, norm)) return GDN_ERR_MODE;
+        if (!aligned(saved, 256)) return GDN_ERR_ALIGN;
+        if (saved_bytes < saved_bytes_of(sh)) return GDN_ERR_WORKSPACE;
+    }
     if ((r = check_device()) != GDN_OK) return r;
 
     cudaStream_t st = (cudaStream_t)stream;
@@ -304,6 +341,7 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, cons
     Args a = make_args(shape);
     a.v = v; a.b = b; a.c = c; a.g = g; a.beta = beta; a.A_log = A_log; a.h0 = h0; a.o = o; a.hT = hT;
     a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits; a.norm = norm;
+    a.saved = saving ? saved : nullptr;
     const size_t state_bytes = (size_t)a.B * a.H * a.dk * a.dv * sizeof(float);
     if (a.T == 0) {
         if (hT && hT != h0) {
@@ -322,18 +360,41 @@ extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape_in, const void* v, cons
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape_in, const void* v, const void* b, const void* c,
+extern "C" gdn_status_t gdn_fwd(const gdn_shape_t* shape, const void* v, const void* b, const void* c,
                                 const void* g, const void* beta, const float* A_log, const float* h0,
-                                const void* dO, const float* dhT, void* dv, void* db, void* dc, void* dg,
-                                void* dbeta, float* dA_log, float* dh0, void* ws, size_t ws_bytes,
-                                gdn_stream_t stream)
+                                void* o, float* hT, void* ws, size_t ws_bytes, gdn_stream_t stream)
+{
+    return fwd_impl(shape, v, b, c, g, beta, A_log, h0, o, hT, nullptr, 0, false, ws, ws_bytes, stream);
+}
+
+extern "C" gdn_status_t gdn_fwd_save(const gdn_shape_t* shape, const void* v, const void* b, const void* c,
+                                     const void* g, const void* beta, const float* A_log, const float* h0,
+                                     void* o, float* hT, void* saved, size_t saved_bytes, void* ws,
+                                     size_t ws_bytes, gdn_stream_t stream)
+{
+    return fwd_impl(shape, v, b, c, g, beta, A_log, h0, o, hT, saved, saved_bytes, true, ws, ws_bytes, stream);
+}
+
+static gdn_status_t bwd_impl(const gdn_shape_t* shape_in, const void* v, const void* b, const void* c,
+                             const void* g, const void* beta, const float* A_log, const float* h0,
+                             const void* saved, size_t saved_bytes, bool from_saved, const void* dO,
+                             const float* dhT, void* dv, void* db, void* dc, void* dg, void* dbeta, float* dA_log,
+                             float* dh0, void* ws, size_t ws_bytes, gdn_stream_t stream)
 {
     gdn_shape_t sh;
     int logits = 0, norm = 0, check = 0;
     if (!shape_in) return GDN_ERR_NULL;
     if (!split_mode(shape_in, &sh, &logits, &norm, &check)) return GDN_ERR_MODE;
     const gdn_shape_t* shape = &sh;
-    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, 1, norm, logits);
+    if (from_saved) {
+        if (!saved) return GDN_ERR_NULL;
+        if (!shape_ok(sh)) return GDN_ERR_SHAPE;
+        if (!saved_applies(sh, logits, norm)) return GDN_ERR_MODE;
+        if (!aligned(saved, 256)) return GDN_ERR_ALIGN;
+        if (saved_bytes < saved_bytes_of(sh)) return GDN_ERR_WORKSPACE;
+    }
+    gdn_status_t r = check_common(shape, v, b, c, g, beta, A_log, h0, ws, ws_bytes, from_saved ? 2 : 1, norm,
+                                  logits);
     if (r != GDN_OK) return r;
     const bool tok = shape->T > 0;
     if ((tok && (!dO || !dv || !db || !dc || !dg)) || !dA_log) return GDN_ERR_NULL;
@@ -353,9 +414,10 @@ extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape_in, const void* v, cons
     a.v = v; a.b = b; a.c = c; a.g = g; a.beta = beta; a.A_log = A_log; a.h0 = h0;
     a.dO = dO; a.dhT = dhT; a.dv_ = dv; a.db = db; a.dc = dc; a.dg = dg; a.dbeta = dbeta;
     a.dA_log = dA_log; a.dh0 = dh0; a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits; a.norm = norm;
+    a.saved = from_saved ? const_cast<void*>(saved) : nullptr;
     cudaError_t e;
     if (a.T > 0 && chunk_bwd_applies(*shape, logits, norm)) {
-        e = launch_chunk_bwd(a, ws_layout(*shape, 1, norm, logits), st);
+        e = launch_chunk_bwd(a, ws_layout(*shape, from_saved ? 2 : 1, norm, logits), st);
     } else {
         const int P = bwd_split(*shape, logits, norm);
         e = P > 1 ? launch_bwd_tsplit(a, ws_layout(*shape, 1, norm, logits), P, st, fwd_core)
@@ -370,6 +432,26 @@ extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape_in, const void* v, cons
             if (e == cudaSuccess && x.p && x.n) e = launch_check_finite(x.p, x.n, x.io, ws, st);
     }
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status_t gdn_bwd(const gdn_shape_t* shape, const void* v, const void* b, const void* c,
+                                const void* g, const void* beta, const float* A_log, const float* h0,
+                                const void* dO, const float* dhT, void* dv, void* db, void* dc, void* dg,
+                                void* dbeta, float* dA_log, float* dh0, void* ws, size_t ws_bytes,
+                                gdn_stream_t stream)
+{
+    return bwd_impl(shape, v, b, c, g, beta, A_log, h0, nullptr, 0, false, dO, dhT, dv, db, dc, dg, dbeta, dA_log,
+                    dh0, ws, ws_bytes, stream);
+}
+
+extern "C" gdn_status_t gdn_bwd_saved(const gdn_shape_t* shape, const void* v, const void* b, const void* c,
+                                      const void* g, const void* beta, const float* A_log, const void* saved,
+                                      size_t saved_bytes, const void* dO, const float* dhT, void* dv, void* db,
+                                      void* dc, void* dg, void* dbeta, float* dA_log, float* dh0, void* ws,
+                                      size_t ws_bytes, gdn_stream_t stream)
+{
+    return bwd_impl(shape, v, b, c, g, beta, A_log, nullptr, saved, saved_bytes, true, dO, dhT, dv, db, dc, dg,
+                    dbeta, dA_log, dh0, ws, ws_bytes, stream);
 }
 
 extern "C" gdn_status_t gdn_last_device_status(const void* ws, gdn_stream_t stream)

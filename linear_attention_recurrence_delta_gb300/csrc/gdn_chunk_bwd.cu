@@ -91,6 +91,7 @@ struct CbParams {
     int B, H, T, dk, dv_, nchunks, nq;
     uint64_t wait_ns;
     int starve;       // failure-path test hook: the chunk q whose loads are never issued (-1: none)
+    int rev_only;     // the entering states came from the forward: the chain runs its reverse sweep only
 };
 
 // ---------------------------------------------------------------- shared memory
@@ -150,11 +151,12 @@ constexpr int kES = 65;                                  // row stride of the ep
 constexpr uint32_t DC = 78848, DB = DC + 64 * kES * 4, DG = DB + 64 * kES * 4, PB = 53760;
 }  // namespace gl
 
-// The delta front's results, saved by the prep pass for the gradient pass (per chunk, byte offsets): P as hi, lo
-// tiles; -N and Dinv, one half each of the stacked [-N ; -N] and [Dinv ; Dinv] operands; K strictly below the
-// diagonal, packed by rows, fp32; -W, a bf16 tile [t][i]; Util, fp32 [t][j].
+// The delta front's results that the gradient pass reuses, per chunk (byte offsets), written by the prep pass or
+// by a saving forward (gdn_fwd_tc.cu, the same layout): P as hi, lo tiles; -N and Dinv, one half each of the
+// stacked [-N ; -N] and [Dinv ; Dinv] operands; K strictly below the diagonal, packed by rows, fp32; -W, a bf16
+// tile [t][i] (its lo part after it: written by the saving forward only); Util, fp32 [t][j].
 namespace sv {
-constexpr uint32_t P = 0, NA = 16384, DINV = 24576, KP = 32768, NW = 40960, UT = 49152, BYTES = 65536;
+constexpr uint32_t P = 0, NA = 16384, DINV = 24576, KP = 32768, NW = 40960, NWL = 49152, UT = 57344, BYTES = 73728;
 }  // namespace sv
 
 // fp32 sub-blocks inside MS: the diagonal 16-blocks of M, the 16-blocks below them inside each 32-block,
@@ -170,8 +172,9 @@ constexpr uint32_t TM_UT = TM_NX + 64, TM_W = TM_NX + 128;
 constexpr uint32_t TM_COLS = 512;
 
 #ifdef GDN_CHUNK_DEBUG
-// debug builds only: cycles spent between the phase stamps of CTA 0, per kernel (0 prep, 1 grad), and its chunks
-__device__ unsigned long long g_cb_stamps[2][32];
+// debug builds only: cycles spent between the phase stamps of CTA 0, per kernel (0 prep, 1 grad, 2 delta chain),
+// and its chunks (steps for the chain)
+__device__ unsigned long long g_cb_stamps[3][32];
 __device__ unsigned long long g_cb_last;
 #define CB_STAMP(kid, k)                                                                  \
     do {                                                                                  \
@@ -1033,6 +1036,192 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
     teardown(c, p, pending, full_phase);
 }
 
+// ================================================================= pass 1 from a saving forward's residuals (delta)
+// With P and W of every chunk kept by the forward, the chain's inputs take three products per chunk:
+//   Phi - diag(E) = Bhat^T (-W),   Qc - Ctil = P (-W),   Y = Qc^T dO,
+// on hi/lo operands (hi*hi + hi*lo + lo*hi; dO exact).  Bhat and Ctil come from b, c and the chunk's decay (every
+// factor <= 1).  About 100 KB of shared memory and 256 TMEM columns, so two CTAs share an SM.
+namespace ps {
+constexpr uint32_t STB = 0, STC = 8192, STDO = 16384;   // b, c, dO tiles (TMA)
+constexpr uint32_t P = 24576;                            // P hi, lo (residuals)
+constexpr uint32_t NW = 40960;                           // -W hi, lo (residuals)
+constexpr uint32_t BH = 57344;                           // Bhat hi, lo, natural [t][i]
+constexpr uint32_t QC = 73728;                           // Qc hi, lo, natural [t][i]
+constexpr uint32_t SMALL = 98304;                        // after 8 KB that the unused M rows of Qc lo's reads see
+constexpr uint32_t SMEM = SMALL + 1024 + 1024;
+}  // namespace ps
+
+struct PsSmall {
+    float G[64];
+    float A2[64];
+    float g[64];
+    uint64_t full, mma;
+    uint32_t tmem_base, abort;
+};
+static_assert(sizeof(PsSmall) <= 1024, "small block");
+
+__global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_constant__ CbParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    PsSmall& S = *reinterpret_cast<PsSmall*>(sm + ps::SMALL);
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31, q4 = warp & 3, wh = warp >> 2, trow = r & 127;
+    if (r == 0) {
+        mbar_init(&S.full, 1);
+        mbar_init(&S.mma, 1);
+        S.abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&p.tm_b); tma_prefetch_desc(&p.tm_c); tma_prefetch_desc(&p.tm_do);
+    }
+    if (warp == 0) tmem_alloc(&S.tmem_base, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = S.tmem_base, tl = tb + ((uint32_t)(q4 * 32) << 16);
+    uint32_t full_phase = 0, mma_phase = 0;
+    auto issue = [&](int q) {
+        if (q == p.starve) return;   // failure-path test hook
+        const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
+        mbar_arrive_expect_tx(&S.full, 3 * 8192 + 32768);
+        tma_load_4d(sm + ps::STB, &p.tm_b, &S.full, 0, h, 64 * k, bb);
+        tma_load_4d(sm + ps::STC, &p.tm_c, &S.full, 0, h, 64 * k, bb);
+        tma_load_4d(sm + ps::STDO, &p.tm_do, &S.full, 0, h, 64 * k, bb);
+        const unsigned char* rq = p.sv + (size_t)q * sv::BYTES;
+        bulk_g2s(sm + ps::P, rq + sv::P, 16384, &S.full);
+        bulk_g2s(sm + ps::NW, rq + sv::NW, 16384, &S.full);   // -W hi, then lo
+    };
+    auto sync_all = [&]() {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(1, 256);
+        tc_fence_after();
+    };
+    auto wait_mma = [&](uint32_t where) -> bool {
+        if (warp == 0 && !wait_or_abort(&S.mma, mma_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
+            atomicExch(p.status + 2, 400u + where);
+        named_bar_sync(1, 256);
+        mma_phase ^= 1;
+        tc_fence_after();
+        return *(volatile uint32_t*)&S.abort == 0;
+    };
+    int q = blockIdx.x, pending = -1;
+    if (r == 0 && q < p.nq) issue(q);
+    if (q < p.nq) pending = q;
+    for (; q < p.nq; q += gridDim.x) {
+        const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H, t0 = 64 * k;
+        if (r < 64) {
+            const int t = t0 + r;
+            S.g[r] = t < p.T ? __bfloat162float(p.g[((size_t)bb * p.T + t) * p.H + h]) : 0.f;
+        } else if (r < 128) {
+            const int i = r - 64;
+            S.A2[i] = i < p.dk ? -expf(p.A_log[h * p.dk + i]) * kLog2e : 0.f;
+        }
+        if (warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
+            atomicExch(p.status + 2, 5u);
+        named_bar_sync(1, 256);
+        if (*(volatile uint32_t*)&S.abort) break;
+        full_phase ^= 1;
+        pending = -1;
+        if (warp == 0) {
+            // inclusive scan of g, two tokens per lane
+            const float ga = S.g[2 * lane], gb = S.g[2 * lane + 1];
+            float x = ga + gb;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            S.G[2 * lane] = x - gb;
+            S.G[2 * lane + 1] = x;
+        }
+        named_bar_sync(1, 256);
+        {
+            // Bhat = b (.) exp(A (G_63 - G_t)), thread = (token t, 16 channels)
+            const int t = r & 63, cq = r >> 6;
+            float bv[16], y[16];
+            ld16_bf16(sm + ps::STB, t, cq, bv);
+            const float Gt = S.G[t], G63 = S.G[63];
+#pragma unroll
+            for (int e = 0; e < 16; e++) y[e] = bv[e] * fast_exp2(S.A2[16 * cq + e] * (G63 - Gt));
+            st16_split(sm + ps::BH, sm + ps::BH + 8192, t, cq, y);
+        }
+        sync_all();
+        if (r == 0) {
+            const uint32_t bh = smem_u32(sm + ps::BH), pp = smem_u32(sm + ps::P), nw = smem_u32(sm + ps::NW);
+            const uint32_t idA = idesc_bf16(128, 64, true, true), idB = idesc_bf16(128, 64, false, true);
+            // Bhat^T (-W): TMEM columns 0..63, rows i
+            mma_tiles(tb, bh, true, 8192, 0, nw, true, 8192, 0, 4, idA, false);
+            mma_tiles(tb, bh, true, 8192, 0, nw + 8192, true, 8192, 0, 4, idA, true);
+            mma_tiles(tb, bh + 8192, true, 8192, 0, nw, true, 8192, 0, 4, idA, true);
+            // P (-W): columns 64..127, rows t
+            mma_tiles(tb + 64, pp, false, 0, 0, nw, true, 8192, 0, 4, idB, false);
+            mma_tiles(tb + 64, pp, false, 0, 0, nw + 8192, true, 8192, 0, 4, idB, true);
+            mma_tiles(tb + 64, pp + 8192, false, 0, 0, nw, true, 8192, 0, 4, idB, true);
+            mma_commit(&S.mma);
+        }
+        if (!wait_mma(0)) break;
+        if (q4 < 2) {
+            // lanes 0..63: Phi row i out (hi/lo tiles), Qc row t = i = Ctil + P (-W) into its tiles
+            const int i = trow;
+            unsigned char* phq = p.phi + (size_t)q * 16384;
+            const float ec = fast_exp2(S.A2[i] * S.G[63]), Gt = S.G[i];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; h2++) {
+                const int cg = 2 * wh + h2;
+                float a[16], b[16], cv[16];
+                tmem_ld16(tl + 16 * cg, a);
+                tmem_ld16(tl + 64 + 16 * cg, b);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; e++) a[e] += (16 * cg + e == i) ? ec : 0.f;
+                st16_split(phq, phq + 8192, i, cg, a);
+                ld16_bf16(sm + ps::STC, i, cg, cv);
+#pragma unroll
+                for (int e = 0; e < 16; e++) b[e] += cv[e] * fast_exp2(S.A2[16 * cg + e] * Gt);
+                st16_split(sm + ps::QC, sm + ps::QC + 8192, i, cg, b);
+            }
+        }
+        sync_all();
+        if (r == 0) {
+            // Y = Qc^T dO: columns 128..191, rows i
+            const uint32_t qc = smem_u32(sm + ps::QC), dO = smem_u32(sm + ps::STDO);
+            const uint32_t id = idesc_bf16(128, 64, true, true);
+            mma_tiles(tb + 128, qc, true, 8192, 0, dO, true, 8192, 0, 4, id, false);
+            mma_tiles(tb + 128, qc + 8192, true, 8192, 0, dO, true, 8192, 0, 4, id, true);
+            mma_commit(&S.mma);
+        }
+        if (!wait_mma(1)) break;
+        if (q4 < 2) {
+            float* dy = p.ych + ((size_t)q * 64 + trow) * 64;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; h2++) {
+                const int c0 = 32 * wh + 16 * h2;
+                float v[16];
+                tmem_ld16(tl + 128 + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; e += 4)
+                    *reinterpret_cast<float4*>(dy + c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            }
+        }
+        // the tiles are free: the next chunk's loads
+        tc_fence_before();
+        named_bar_sync(1, 256);
+        tc_fence_after();
+        if (q + (int)gridDim.x < p.nq) {
+            if (r == 0) issue(q + gridDim.x);
+            pending = q + gridDim.x;
+        }
+    }
+    // after an abort, let the loads in flight land before the CTA leaves
+    if (r == 0 && *(volatile uint32_t*)&S.abort && pending >= 0 && pending != p.starve)
+        mbar_wait(&S.full, full_phase, nullptr, p.wait_ns);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tb, 256);
+}
+
 // ================================================================= pass 2: chain
 // Gated mode: Phi = diag(E) and the chain is elementwise.  One CTA per (batch, head) unit, 256 threads, thread =
 // rows 2 ip, 2 ip + 1 (ip = r >> 3) x value columns 8 (r & 7) .. + 7.  Forward: S_0 = h0, st[k] = S_k,
@@ -1136,12 +1325,13 @@ __global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_tc_kernel(const __g
     unsigned char* Xlo = Xhi + 8192;
     const int u = blockIdx.x, r = threadIdx.x, warp = r >> 5, lane = r & 31;
     const int dk = p.dk, dv = p.dv_, nk = p.nchunks, nseq = 2 * nk;
+    const int n0 = p.rev_only ? nk : 0;   // first sweep position (the forward sweep is skipped when states are given)
     const size_t qb = (size_t)u * nk;
     const unsigned char* phi = p.phi;
-    // sweep position n -> chunk: 0 .. nk - 1 forward, then nk - 1 .. 0
+    // sweep position n -> chunk: 0 .. nk - 1 forward, then nk - 1 .. 0; the ring counts positions from n0
     auto chunk_of = [&](int n) { return n < nk ? n : nseq - 1 - n; };
     auto issue_copy = [&](int n) {
-        const int s = n % CT_NS;
+        const int s = (n - n0) % CT_NS;
         mbar_arrive_expect_tx(&full[s], CT_STAGE);
         bulk_g2s(sm + s * CT_STAGE, phi + (qb + chunk_of(n)) * CT_STAGE, CT_STAGE, &full[s]);
     };
@@ -1157,10 +1347,10 @@ __global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_tc_kernel(const __g
     tc_fence_after();
     if (warp == 2 || warp == 3) return;
     const uint32_t tb = misc[0];
-    int issued = nseq < CT_NS ? nseq : CT_NS;
+    int issued = n0 + (nseq - n0 < CT_NS ? nseq - n0 : CT_NS);
     if (r == 0) {
-        for (int n = 0; n < issued; n++) issue_copy(n);
-        for (int n = 1; n < 3 && n < nseq; n++)
+        for (int n = n0; n < issued; n++) issue_copy(n);
+        for (int n = n0 + 1; n < n0 + 3 && n < nseq; n++)
             prefetch_l2_bulk((n < nk ? p.dlt : p.ych) + (qb + chunk_of(n)) * 4096, 16384);
     }
     const int i = 32 * (warp & 1) + lane, j0 = 32 * (warp >> 2);
@@ -1198,14 +1388,16 @@ __global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_tc_kernel(const __g
     };
     // one step of either sweep: x <- P x + R with P = Phi (forward) or Phi^T (reverse); false after an abort
     auto step = [&](int n, float (&x)[32], const float (&R)[32]) -> bool {
+        CB_STAMP(2, 0);
         fence_proxy_async_smem();
         tc_fence_before();
         named_bar_sync(1, 128);
         tc_fence_after();
+        CB_STAMP(2, 1);
         const bool transpose = n >= nk;
-        const int s = n % CT_NS;
+        const int s = (n - n0) % CT_NS;
         if (r == 0) {
-            if (wait_or_abort(&full[s], (uint32_t)(n / CT_NS) & 1u, abortf, p.status, p.wait_ns)) {
+            if (wait_or_abort(&full[s], (uint32_t)((n - n0) / CT_NS) & 1u, abortf, p.status, p.wait_ns)) {
                 tc_fence_after();
                 const uint32_t a = smem_u32(sm + s * CT_STAGE), xb = smem_u32(Xhi);
                 mma_tiles(tb, a, transpose, 8192, 0, xb, true, 8192, 0, 4, idesc_bf16(128, 128, transpose, true),
@@ -1217,13 +1409,16 @@ __global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_tc_kernel(const __g
                 atomicExch(p.status + 2, 300u + (uint32_t)n);
             }
         }
+        CB_STAMP(2, 2);
         if (r == 0 && n + 3 < nseq) {
             // the fp32 record of step n + 3 into L2, so that its register loads (issued a step ahead) hit there
             const int m = n + 3;
             prefetch_l2_bulk((m < nk ? p.dlt : p.ych) + (qb + chunk_of(m)) * 4096, 16384);
         }
-        if (!wait_or_abort(mmab, (uint32_t)n & 1u, abortf, p.status, p.wait_ns)) return false;
+        CB_STAMP(2, 3);
+        if (!wait_or_abort(mmab, (uint32_t)(n - n0) & 1u, abortf, p.status, p.wait_ns)) return false;
         tc_fence_after();
+        CB_STAMP(2, 4);
         if (r == 0 && issued < nseq) issue_copy(issued++);   // the stage just read is free
 #pragma unroll
         for (int h = 0; h < 2; h++) {
@@ -1234,26 +1429,36 @@ __global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_tc_kernel(const __g
 #pragma unroll
             for (int e = 0; e < 16; e++) x[16 * h + e] = (a[e] + b[e]) + R[16 * h + e];
         }
+        CB_STAMP(2, 5);
         return true;
     };
 
     float x[32], R[32], Rn[32];
     bool ok = true;
+    CB_STAMP_INIT;
     // ---- forward: st[k] = S_k, S_{k+1} = Phi_k S_k + Delta_k
-    load_in(p.h0, x);
-    rec(p.dlt, 0, R);
-    put(p.st, 0, x);
-    tiles(x);
-    for (int k = 0; k < nk && ok; k++) {
+    if (!p.rev_only) {
+        load_in(p.h0, x);
+        rec(p.dlt, 0, R);
+        put(p.st, 0, x);
+        tiles(x);
+    }
+    for (int k = 0; k < nk && ok && !p.rev_only; k++) {
         if (k + 1 < nk) rec(p.dlt, k + 1, Rn);
         ok = step(k, x, R);
         if (!ok) break;
         if (k + 1 < nk) {
             put(p.st, k + 1, x);
+            CB_STAMP(2, 6);
             tiles(x);   // the step's MMAs have completed: the tiles are free
+            CB_STAMP(2, 7);
 #pragma unroll
             for (int e = 0; e < 32; e++) R[e] = Rn[e];
+            CB_STAMP(2, 8);
         }
+#ifdef GDN_CHUNK_DEBUG
+        if (r == 0 && blockIdx.x == 0) g_cb_stamps[2][31] += 1;
+#endif
     }
     // ---- reverse: dst[k] = dS_{k+1}, dS_k = Phi_k^T dS_{k+1} + Y_k, dh0 = dS_0
     if (ok) {
@@ -1282,8 +1487,8 @@ __global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_tc_kernel(const __g
     }
     // wind down: after an abort, let the copies still in flight land before the CTA leaves
     if (r == 0 && *(volatile uint32_t*)abortf) {
-        for (int n = issued - CT_NS < 0 ? 0 : issued - CT_NS; n < issued; n++)
-            mbar_wait(&full[n % CT_NS], (uint32_t)(n / CT_NS) & 1u, nullptr, p.wait_ns);
+        for (int n = issued - CT_NS < n0 ? n0 : issued - CT_NS; n < issued; n++)
+            mbar_wait(&full[(n - n0) % CT_NS], (uint32_t)((n - n0) / CT_NS) & 1u, nullptr, p.wait_ns);
     }
     tc_fence_before();
     named_bar_sync(1, 128);
@@ -2072,6 +2277,12 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv_ = a.dv;
     p.nchunks = (a.T + 63) / 64;
     p.nq = a.B * a.H * p.nchunks;
+    if (a.saved) {
+        // residuals of a saving forward (delta): the entering states, then the solve's results
+        p.st = (float*)a.saved;
+        p.sv = (unsigned char*)a.saved + (size_t)p.nq * 16384;
+        p.rev_only = 1;
+    }
     p.starve = test_starve_chunk();
     p.wait_ns = p.starve >= 0 ? kTestWaitNs : kWaitNs;
     const bool delta = a.mode == GDN_DELTA;
@@ -2084,6 +2295,7 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
         if ((e = set_smem(chunk_grad_kernel<true>, grad_bytes)) != cudaSuccess) return e;
         if ((e = set_smem(chunk_grad_kernel<false>, grad_bytes)) != cudaSuccess) return e;
         if ((e = set_smem(chunk_chain_tc_kernel, CHAIN_TC_SMEM)) != cudaSuccess) return e;
+        if ((e = set_smem(chunk_prep_saved_kernel, ps::SMEM)) != cudaSuccess) return e;
         attr = true;
     }
     int sms = 152;
@@ -2098,7 +2310,8 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
 #define CB_MARK(what)
 #endif
     CB_MARK("start");
-    if (delta) chunk_prep_kernel<true><<<grid, kThreads, prep_bytes, st>>>(p);
+    if (a.saved) chunk_prep_saved_kernel<<<p.nq < 2 * sms ? p.nq : 2 * sms, 256, ps::SMEM, st>>>(p);
+    else if (delta) chunk_prep_kernel<true><<<grid, kThreads, prep_bytes, st>>>(p);
     else chunk_prep_kernel<false><<<grid, kThreads, prep_bytes, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -2123,7 +2336,7 @@ extern "C" int gdn_chunk_debug_stamps(unsigned long long* out, int clear)
 {
     if (cudaMemcpyFromSymbol(out, gdn::g_cb_stamps, sizeof(gdn::g_cb_stamps)) != cudaSuccess) return 1;
     if (clear) {
-        static const unsigned long long zero[2][32] = {};
+        static const unsigned long long zero[3][32] = {};
         if (cudaMemcpyToSymbol(gdn::g_cb_stamps, zero, sizeof(zero)) != cudaSuccess) return 1;
     }
     return 0;

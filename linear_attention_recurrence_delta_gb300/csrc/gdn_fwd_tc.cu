@@ -154,6 +154,27 @@ __device__ __forceinline__ void zero_chunk(unsigned char* tile, int row, int q)
     *reinterpret_cast<uint4*>(tile + sw128(row, 8 * q)) = make_uint4(0, 0, 0, 0);
 }
 
+// The residuals a saving forward writes for the chunked backward (gdn_chunk_bwd.cu reads them with the same
+// layout), per chunk q = unit * nchunks + k.  p.st: the state entering the chunk, fp32 [64][64] (rows = key channel,
+// columns = value column).  p.sv, byte offsets in a chunk's record: P as hi, lo tiles; -N and Dinv (bf16 tiles,
+// the upper halves of the stacked solve operands); K strictly below the diagonal, fp32, packed by rows; -W as
+// hi, lo tiles ([t][i]); Util, fp32 [t][j].  Tiles are [64][64] 16-bit with the 128-byte swizzle of the MMA
+// operands.
+namespace svr {
+constexpr uint32_t P = 0, NA = 16384, DINV = 24576, KP = 32768, NW = 40960, NWL = 49152, UT = 57344, BYTES = 73728;
+__device__ __forceinline__ unsigned char* rec(const TcParams& p, int u, int k)
+{
+    return p.sv + ((size_t)u * p.nchunks + k) * BYTES;
+}
+// state row `row`, columns 32 wh .. 32 wh + 31
+__device__ __forceinline__ void put_state(const TcParams& p, int u, int k, int row, int wh, const float (&v)[32])
+{
+    float4* d = reinterpret_cast<float4*>(p.st + (((size_t)u * p.nchunks + k) * 64 + row) * 64 + 32 * wh);
+#pragma unroll
+    for (int e = 0; e < 8; e++) d[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+}
+}  // namespace svr
+
 // D[d] (+)= A x B over K = 64 (four K = 16 steps); A K-major, B K- or MN-major
 __device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a, uint32_t b, bool b_mn, uint32_t idesc, bool acc)
 {
@@ -168,8 +189,12 @@ __device__ __forceinline__ const float* ktab(const unsigned char* sm, int tab, i
     return reinterpret_cast<const float*>(sm + OFF_K) + (tab * 8 + k8) * 64;
 }
 
-// NORM: b and c arrive before their L2 normalisation (a template flag, so the plain kernel carries no trace of it)
-template <bool DELTA, bool NORM>
+// NORM: b and c arrive before their L2 normalisation (a template flag, so the plain kernel carries no trace of it).
+// SAVE (delta, one 64-column slab): the residuals of the chunked backward are written as well, per chunk q of the
+// unit: the entering state (p.st, fp32 [64][64]) and the solve's results (p.sv, the layout of namespace svr).  The
+// b-side level operands then leave beta out, so that the level products give K itself (M = beta K is formed
+// when it is assembled).
+template <bool DELTA, bool NORM, bool SAVE>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -248,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
                 st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
             }
+            if (SAVE) svr::put_state(p, u, 0, trow, wh, Sreg);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, kMath);
@@ -273,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
                     st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
                 }
+                if (SAVE && kk + 1 < p.nchunks) svr::put_state(p, u, kk + 1, trow, wh, Sreg);
             } else {
                 const int tg = kk * kC + (trow - 64);
                 const size_t orow_at = (((size_t)bb * T + tg) * H + h) * dv + jc0;
@@ -461,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             const float an = fast_exp2(a2[e] * dG), ai = fast_exp2(-a2[e] * dG);
                             ax[e] = cv[e] * an;
                             bxp[e] = bv[e] * ai;
-                            bbx[e] = bet * bv[e] * an;
+                            bbx[e] = (SAVE ? 1.f : bet) * bv[e] * an;
                         }
                         float kk[8];
                         if (I > 0) {
@@ -507,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         st_row8_split(X + X_B3, X + X_B3L, t, q, bxp);
                         ld_f8(ktab(sm, K_0, k8) + 8 * q, kk);
 #pragma unroll
-                        for (int e = 0; e < 8; e++) keep[8 * qq + e] = (DELTA ? bbx[e] : ax[e]) * kk[e];
+                        for (int e = 0; e < 8; e++) keep[8 * qq + e] = (DELTA ? (SAVE ? bet : 1.f) * bbx[e] : ax[e]) * kk[e];
                     }
                 } else {
                     // fallback: every factor evaluated directly (all exponents <= 0 except L3's,
@@ -523,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         for (int e = 0; e < 8; e++) {
                             cv[e] *= nct;
                             bv[e] *= nbt;
-                            bbv[e] = bet * bv[e];
+                            bbv[e] = (SAVE ? 1.f : bet) * bv[e];
                         }
                         if (I > 0) {
                             scale8(cv, S.A2, q, Gt - GI, y); st_row8_f16(X + X_A1, t, q, y);
@@ -541,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (!upper) { scale8(bv, S.A2, q, GJ7 - Gt, y); st_row8_f16(X + X_B2, t, q, y); }
                         scale8(DELTA ? bbv : cv, S.A2, q, Gt, y);
 #pragma unroll
-                        for (int e = 0; e < 8; e++) keep[8 * qq + e] = y[e];
+                        for (int e = 0; e < 8; e++) keep[8 * qq + e] = (SAVE ? bet : 1.f) * y[e];
                     }
                 }
             }
@@ -625,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                 }
                                 if (NORM) acc *= (isM ? S.nb[t] : S.nc[t]) * S.nb[sc];
                             }
-                            ew[e] = isM ? bet * acc : acc;
+                            ew[e] = (isM && !SAVE) ? bet * acc : acc;
                         }
                     }
                     const int Ia = 2 * wl, Ib = 2 * wl + 1;
@@ -660,8 +687,23 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                 out[c] = val;
                             }
                         }
+                        if (SAVE && isM) {
+                            // the level products gave K: its strictly lower part is a residual, M = beta K
+                            float* kp = reinterpret_cast<float*>(svr::rec(p, u, k) + svr::KP);
+                            const float bet = S.beta[s][t];
+#pragma unroll
+                            for (int c = 0; c < 16; c++) {
+                                const int sc = 16 * cg + c;
+                                if (sc < t) kp[t * (t - 1) / 2 + sc] = out[c];
+                                out[c] *= bet;
+                            }
+                        }
                         if (!isM) {
                             st_split16(sm + OFF_CH0, sm + OFF_CH0L, 64 + t, cg, out);
+                            if (SAVE) {
+                                unsigned char* pr = svr::rec(p, u, k) + svr::P;
+                                st_split16(pr, pr + 8192, t, cg, out);
+                            }
                         } else {
                             // L: the column blocks left of the row's 32-block; the diagonal 16-block (M32) and,
                             // in the upper 16-block of a 32-block, the one below the diagonal (C32) in fp32
@@ -823,6 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             v16[c] = x.x; v16[c + 1] = x.y; v16[c + 2] = x.z; v16[c + 3] = x.w;
                         }
                         st_plain16(X + X_DINV, trow, cg, v16);
+                        if (SAVE && trow < 64) st_plain16(svr::rec(p, u, k) + svr::DINV, trow, cg, v16);
                     }
                 }
                 smem_to_tc();
@@ -854,6 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                             for (int c = 0; c < 16; c++) v[c] = -v[c];
                             st_plain16(X + X_NA, t, g, v);
+                            if (SAVE) st_plain16(svr::rec(p, u, k) + svr::NA, t, g, v);
                         } else {
                             const int xg = g - 4;
                             const uint32_t blk = (uint32_t)(xg >> 2) * 8192u;
@@ -917,6 +961,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                         for (int c = 0; c < 16; c++) v[c] = -v[c];
                         st_plain16(X + X_CW, trow, cg, v);
+                        if (SAVE) {
+                            unsigned char* rq = svr::rec(p, u, k);
+                            st_split16(rq + svr::NW, rq + svr::NWL, trow, cg, v);
+                            tmem_ld16(tl + TM_U + 16 * cg, v);   // Util, before S is folded in
+                            tmem_wait_ld();
+                            float4* du = reinterpret_cast<float4*>(rq + svr::UT) + trow * 16 + 4 * cg;
+#pragma unroll
+                            for (int e = 0; e < 4; e++) du[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                        }
                     }
                 }
                 smem_to_tc();
@@ -990,17 +1043,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (warp == 0) tmem_dealloc(tbase, TM_COLS);
 }
 
-template <bool DELTA, bool NORM>
+template <bool DELTA, bool NORM, bool SAVE = false>
 cudaError_t launch_t(const TcParams& p, dim3 grid, cudaStream_t st)
 {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<DELTA, NORM>,
+        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<DELTA, NORM, SAVE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    fwd_tc_kernel<DELTA, NORM><<<grid, kThreads, SMEM_BYTES, st>>>(p);
+    fwd_tc_kernel<DELTA, NORM, SAVE><<<grid, kThreads, SMEM_BYTES, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -1032,6 +1085,14 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     p.wait_ns = p.starve_chunk >= 0 ? kTestWaitNs : kWaitNs;
     *handled = true;
     const dim3 grid(a.B * a.H, (a.dv + 63) / 64);
+    if (a.saved) {
+        // the residuals of the chunked backward: delta, one slab, no option bits, no fp32 output (the host checks)
+        if (a.mode != GDN_DELTA || a.dv > 64 || a.norm || a.logits || a.o32) return cudaErrorInvalidValue;
+        const size_t nq = (size_t)a.B * a.H * p.nchunks;
+        p.st = (float*)a.saved;
+        p.sv = (unsigned char*)a.saved + nq * 16384;
+        return launch_t<true, false, true>(p, grid, st);
+    }
     if (a.norm)
         return a.mode == GDN_DELTA ? launch_t<true, true>(p, grid, st) : launch_t<false, true>(p, grid, st);
     return a.mode == GDN_DELTA ? launch_t<true, false>(p, grid, st) : launch_t<false, false>(p, grid, st);

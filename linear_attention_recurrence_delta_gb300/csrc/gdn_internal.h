@@ -27,6 +27,8 @@ struct Args {
     void *dv_, *db, *dc, *dg, *dbeta;
     float* dA_log;
     float* dh0;
+    // residuals of the chunked backward (delta): a saving forward writes them, the backward reads them
+    void* saved;
     // workspace
     void* ws;
     size_t ws_bytes;
@@ -75,11 +77,15 @@ constexpr size_t kStateSlot = 16 * 256 * 4;    // one state snapshot (256 thread
 inline int bwd_cols(int dk) { return dk <= 64 ? 64 : 32; }
 inline int bwd_slabs(int dk, int dv) { return (dv + bwd_cols(dk) - 1) / bwd_cols(dk); }
 
-// `norm`: GDN_NORM_BC is set (the backward then routes db, dc through fp32 partials); `logits`: GDN_GATE_LOGITS
+// `norm`: GDN_NORM_BC is set (the backward then routes db, dc through fp32 partials); `logits`: GDN_GATE_LOGITS.
+// backward: 0 forward, 1 backward, 2 backward from a saving forward's residuals (no state or solve records)
 WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm = 0, int logits = 0);
 
 // The chunked tensor-core backward takes bf16 heads up to 64 wide without the option bits; other backward
 // calls take the token-serial one (with its time split for long sequences over few heads).
+// Residuals a saving forward keeps for it, per chunk of 64 tokens: the entering state (fp32 64 x 64) and the
+// delta solve's results (layout in gdn_chunk_bwd.cu, namespace sv).
+constexpr size_t kSavedStateBytes = 16384, kSavedSolveBytes = 73728;
 inline bool chunk_bwd_applies(const gdn_shape_t& s, int logits, int norm)
 {
     return s.io == GDN_BF16 && s.T > 0 && s.dk <= 64 && s.dv <= 64 && !logits && !norm;

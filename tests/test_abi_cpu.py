@@ -159,9 +159,9 @@ def test_time_split_backward_workspace():
 def test_chunked_backward_workspace():
     """The chunked backward (bf16, heads up to 64 wide, no option bits) keeps per chunk of 64 tokens five 16 KB
     64 x 64 records in delta mode (transition as bf16 hi/lo tiles, zero-start state, adjoint share, entering state,
-    leaving adjoint) plus the 64 KB of the front's results that the gradient pass reuses, four fp32 records in
+    leaving adjoint) plus the 72 KB of the front's results that the gradient pass reuses, four fp32 records in
     gated mode, and two rows of 64 floats (decay, dA partial), after the 256-byte status word."""
-    for mode, per_chunk in (("delta", 5 * 16384 + 65536), ("gated", 4 * 16384)):
+    for mode, per_chunk in (("delta", 5 * 16384 + 73728), ("gated", 4 * 16384)):
         for B, H, T, d in ((8, 16, 4096, 64), (1, 16, 32768, 64), (2, 3, 100, 56), (1, 1, 1, 8)):
             s = gdn.make_shape(B, H, T, d, d, mode, "bf16")
             nq = B * H * -(-T // 64)
@@ -296,3 +296,47 @@ def test_plan_and_workspace_agree_on_random_shapes():
                     assert p.fwd_kernel == gdn.GDN_KERNEL_DECODE
                 if p.fwd_kernel == gdn.GDN_KERNEL_TENSOR_CORE:
                     assert io == "bf16" and dk <= 64
+
+
+def test_saved_residuals_sizes_and_argument_errors(lib):
+    """gdn_saved_bytes: per chunk of 64 tokens a 16 KB state and 72 KB of solve results, for delta-mode bf16 shapes
+    whose forward is one tensor-core pass and whose backward is the chunked one; 0 for every other shape.  The
+    backward from the residuals needs a smaller workspace (backward = 2).  gdn_fwd_save and gdn_bwd_saved reject
+    bad arguments before any device work."""
+    for B, H, T, d in ((8, 16, 4096, 64), (2, 3, 100, 56), (1, 1, 9, 8)):
+        s = gdn.make_shape(B, H, T, d, d, "delta", "bf16")
+        nq = B * H * -(-T // 64)
+        assert gdn.gdn_saved_bytes(s) == nq * (16384 + 73728)
+        assert 0 < gdn.gdn_workspace_bytes(s, 2) < gdn.gdn_workspace_bytes(s, 1)
+    none = [gdn.make_shape(8, 16, 4096, 64, 64, "gated", "bf16"),            # gated mode
+            gdn.make_shape(2, 2, 256, 64, 64, "delta", "f32"),               # fp32 I/O
+            gdn.make_shape(2, 2, 256, 128, 128, "delta", "bf16"),            # wider than 64
+            gdn.make_shape(2, 2, 256, 64, 64, "delta", "bf16", gate_logits=True),
+            gdn.make_shape(2, 2, 256, 64, 64, "delta", "bf16", norm_bc=True),
+            gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"),           # the forward splits in time
+            gdn.make_shape(2, 2, 4, 64, 64, "delta", "bf16"),                # the decode kernel's length
+            gdn.make_shape(2, 2, 0, 64, 64, "delta", "bf16")]
+    for s in none:
+        assert gdn.gdn_saved_bytes(s) == 0
+        assert gdn.gdn_workspace_bytes(s, 2) == 0
+    s = gdn.make_shape(2, 2, 256, 64, 64, "delta", "bf16")
+    need = gdn.gdn_saved_bytes(s)
+
+    def fwd_save(shape, saved=FAKE, saved_bytes=need):
+        return gdn.gdn_fwd_save(shape, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, saved, FAKE,
+                                saved_bytes=saved_bytes, ws_bytes=1 << 30, stream=0)
+
+    def bwd_saved(shape, saved=FAKE, saved_bytes=need, beta=FAKE):
+        return gdn.gdn_bwd_saved(shape, FAKE, FAKE, FAKE, FAKE, beta, FAKE, saved, FAKE, None, FAKE, FAKE, FAKE,
+                                 FAKE, beta, FAKE, None, FAKE, saved_bytes=saved_bytes, ws_bytes=1 << 30, stream=0)
+
+    assert fwd_save(s, saved=None) == 1
+    assert fwd_save(s, saved_bytes=need - 1) == 5
+    assert fwd_save(s, saved=FAKE + 16) == 3
+    assert fwd_save(gdn.make_shape(2, 2, 256, 64, 64, "delta", "f32")) == 4
+    assert fwd_save(gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16")) == 4
+    assert bwd_saved(s, saved=None) == 1
+    assert bwd_saved(s, saved_bytes=need - 1) == 5
+    assert bwd_saved(s, saved=FAKE + 16) == 3
+    assert bwd_saved(gdn.make_shape(2, 2, 256, 128, 128, "delta", "bf16")) == 4
+    assert bwd_saved(s, beta=None) == 4   # delta mode needs beta (and dbeta)
