@@ -345,7 +345,7 @@ __device__ __forceinline__ void front_operands(Ctx& c, unsigned char* A1, unsign
         if (with_b_rows) st16_f16(A1, 64 + t, cq, z);
     }
     // column factors towards row blocks J > I: exp(A (G_{16 J - 1} - G_t)) <= 1
-#pragma unroll
+#pragma unroll 1
     for (int J = 1; J <= 3; J++) {
         if (t < 16 * J) {
             const float Gref = S.G[16 * J - 1];
@@ -557,7 +557,7 @@ __device__ __forceinline__ void write_dinv(Ctx& c, unsigned char* MS, unsigned c
     const int t = c.trow & 63, J = t >> 4;
     const float* DI32 = fptr(MS, MS_DI32) + (J * 16 + (t & 15)) * kBS;
     const float* E32 = fptr(MS, MS_E32) + ((J >> 1) * 16 + (t & 15)) * kBS;
-#pragma unroll
+#pragma unroll 1
     for (int h2 = 0; h2 < 2; h2++) {
         const int cg = 2 * c.wh + h2;
         const float* src = (cg == J) ? DI32 : ((J & 1) && cg == J - 1) ? E32 : nullptr;
@@ -647,7 +647,7 @@ __device__ bool front_solve(Ctx& c, const CbParams& p, unsigned char* NEARb, uns
     // groups 0..5 from lanes 0..63, 6..11 from their copy in lanes 64..127.
     {
         const int gb = (isK ? 6 : 0) + 3 * c.wh;
-#pragma unroll
+#pragma unroll 1
         for (int gg = 0; gg < 3; gg++) {
             const int g = gb + gg;
             float v[16];
@@ -857,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                 const int i = c.trow & 63;
                 float* dst = (c.trow < 64 ? p.dlt : p.ych) + ((size_t)q * 64 + i) * 64;
                 const uint32_t col0 = c.trow < 64 ? 0u : 64u;
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     float v[16];
                     tmem_ld16(c.tl + col0 + 32 * c.wh + 16 * h2, v);
@@ -914,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             {
                 const bool isW = c.trow < 64;
                 const int tt = c.trow & 63;
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * c.wh + h2;
                     float v[16];
@@ -958,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                 unsigned char* phq = p.phi + (size_t)q * 16384;
                 float* ddl = p.dlt + ((size_t)q * 64 + i) * 64;
                 const float eci = c.KT->EC[i];
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int c0 = 32 * c.wh + 16 * h2;
                     float a[16], b[16];
@@ -981,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                 const int tt = c.trow;
                 float cv[16];
                 const float Gt = S.G[tt];
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * c.wh + h2;
                     float pw[16];
@@ -1008,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             if (c.trow < 64) {
                 const int i = c.trow;
                 float* dy = p.ych + ((size_t)q * 64 + i) * 64;
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int c0 = 32 * c.wh + 16 * h2;
                     float v[16];
@@ -1165,7 +1165,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
             const int i = trow;
             unsigned char* phq = p.phi + (size_t)q * 16384;
             const float ec = fast_exp2(S.A2[i] * S.G[63]), Gt = S.G[i];
-#pragma unroll
+#pragma unroll 1
             for (int h2 = 0; h2 < 2; h2++) {
                 const int cg = 2 * wh + h2;
                 float a[16], b[16], cv[16];
@@ -1193,7 +1193,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
         if (!wait_mma(1)) break;
         if (q4 < 2) {
             float* dy = p.ych + ((size_t)q * 64 + trow) * 64;
-#pragma unroll
+#pragma unroll 1
             for (int h2 = 0; h2 < 2; h2++) {
                 const int c0 = 32 * wh + 16 * h2;
                 float v[16];
@@ -1601,7 +1601,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             if (!isK) {
                 const float4* urow =
                     reinterpret_cast<const float4*>(p.sv + (size_t)q * sv::BYTES + sv::UT) + tt * 16;
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
                     float v[16];
@@ -1625,7 +1625,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             if (!mma_wait(c, p, 8)) break;
             // U -> hi/lo [s][j]
             if (!isK) {
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
                     float v[16];
@@ -1664,7 +1664,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         if (!DELTA) {
             // dv = dU (the TMEM loads are warp-uniform; only the stores depend on the row)
             if (!isK) {
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int c0 = 32 * wh + 16 * h2;
                     float v[16];
@@ -1685,7 +1685,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         } else {
             // dU -> hi/lo [s][j] (MN-major B)
             if (!isK) {
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
                     float v[16];
@@ -1705,7 +1705,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             }
             if (!mma_wait(c, p, 10)) break;
             if (!isK) {
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
                     float v[16];
@@ -1729,7 +1729,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             {
                 const float bet = S.beta[tt];
                 float part = 0.f;
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2, c0 = 16 * cg;
                     float v[16];
@@ -1806,7 +1806,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 float part = 0.f;
                 const float Gt = S.G[tt];
                 const float* KP = fptr(X, gl::KP);
-#pragma unroll
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
                     float drs[16], dru[16], bv[16];
@@ -1825,7 +1825,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             }
             // A_d row trow: segment I's columns (lo .. lo + 16 I) hold the row's values for s < 16 I
             const int lo16 = seg_base(I) >> 4;
-#pragma unroll
+#pragma unroll 1
             for (int g4 = 0; g4 < 4; g4++) {
                 const int sgrp = 4 * wh + g4 - lo16;   // 16-column group of s this segment group holds
                 const bool valid = sgrp >= 0 && sgrp < I;
@@ -1904,7 +1904,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 float rP[16], rK[16], rPx[16], rKx[16];
 #pragma unroll
                 for (int e = 0; e < 16; e++) rP[e] = rK[e] = rPx[e] = rKx[e] = 0.f;
-#pragma unroll
+#pragma unroll 1
                 for (int sg = 0; sg < 4; sg++) {
                     // lower rows: s < 8 only (entries above the diagonal are zero)
                     if (!up && sg >= 2) continue;
@@ -1957,7 +1957,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 float cP[16], cK[16], cX[16];
 #pragma unroll
                 for (int e = 0; e < 16; e++) cP[e] = cK[e] = cX[e] = 0.f;
-#pragma unroll
+#pragma unroll 1
                 for (int sg = 0; sg < 4; sg++) {
                     if (up && sg < 2) continue;   // upper columns: s >= 8 only
                     const bool xs = !up && sg >= 2;
@@ -2060,7 +2060,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         if (!isK) {
             const int I = tt >> 4;
             const float Gt = S.G[tt], G63 = S.G[63], Gref = I >= 1 ? S.G[16 * I - 1] : 0.f;
-#pragma unroll
+#pragma unroll 1
             for (int h2 = 0; h2 < 2; h2++) {
                 const int cg = 2 * wh + h2, c0 = 16 * cg;
                 float dct[16], dbh[16], da1[16], cv[16], bv[16];
@@ -2087,7 +2087,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         if (trow < 96) {
             const int I = trow < 16 ? 1 : (trow < 48 ? 2 : 3), s = trow - seg_base(I);
             const float Gref = S.G[16 * I - 1], Gs = S.G[s];
-#pragma unroll
+#pragma unroll 1
             for (int h2 = 0; h2 < 2; h2++) {
                 const int c0 = 32 * wh + 16 * h2;
                 float v[16];
@@ -2101,7 +2101,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         if (DELTA && isK) {
             const int I = tt >> 4;
             const float Gt = S.G[tt], Gref = I >= 1 ? S.G[16 * I - 1] : 0.f, bet = S.beta[tt];
-#pragma unroll
+#pragma unroll 1
             for (int h2 = 0; h2 < 2; h2++) {
                 const int cg = 2 * wh + h2, c0 = 16 * cg;
                 float drs[16], da1[16], bv[16];
