@@ -376,6 +376,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-bwd", action="store_true", help="skip the forward+backward measurement")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch B (profiling captures)")
+    ap.add_argument("--tokens", type=int, default=None, help="override the workload's length T (profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -400,6 +402,9 @@ def main():
     gdn.load()
 
     base = I.WORKLOADS[args.workload]
+    if args.batch or args.tokens:
+        B, T = args.batch or base.B, args.tokens or base.T
+        base = base.with_(name=f"{base.name}@B{B}T{T}", B=B, T=T)
     w = replicas.rank_workload(base, rank, world)
     wb = w.with_(backward=True)
     x = I.make_inputs(wb)
