@@ -76,7 +76,8 @@ struct CbParams {
     unsigned char* phi;
     // delta: the front's results that the gradient pass reuses (layout in namespace sv), 64 KB per chunk
     unsigned char* sv;
-    // per chunk q = unit * nchunks + k, each [64][64] fp32 (rows = key channel i, columns = value column j)
+    // per chunk q = unit * nchunks + k, each 64 x 64 fp32 (rows = key channel i, columns = value column j), stored
+    // column-group major (rec4)
     float* dlt;     // Delta
     float* ych;     // Y = Qc^T dO
     float* ec;      // gated: [q][64] exp(A G_63)
@@ -207,6 +208,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 __device__ __forceinline__ float* fptr(unsigned char* base, uint32_t off) { return reinterpret_cast<float*>(base + off); }
+
+// The fp32 records (Delta, Y, S, dS') are stored column-group major: the float4 of row `row`, columns col .. col + 3
+// (col a multiple of 4) sits at index (col / 4) * 64 + row of the chunk's record, so the 32 rows of a warp read or
+// write 512 contiguous bytes.
+__device__ __forceinline__ float4* rec4(float* base, size_t q, int row, int col)
+{
+    return reinterpret_cast<float4*>(base + q * 4096) + ((col >> 2) * 64 + row);
+}
+__device__ __forceinline__ const float4* rec4(const float* base, size_t q, int row, int col)
+{
+    return reinterpret_cast<const float4*>(base + q * 4096) + ((col >> 2) * 64 + row);
+}
 
 __device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int c0, int c1, int c2, int c3)
 {
@@ -855,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             // Delta = rows 0..63, columns 0..63; Y = rows 64..127, columns 64..127
             {
                 const int i = c.trow & 63;
-                float* dst = (c.trow < 64 ? p.dlt : p.ych) + ((size_t)q * 64 + i) * 64;
+                float* dst = c.trow < 64 ? p.dlt : p.ych;
                 const uint32_t col0 = c.trow < 64 ? 0u : 64u;
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
@@ -864,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; e += 4)
-                        *reinterpret_cast<float4*>(dst + 32 * c.wh + 16 * h2 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                        *rec4(dst, q, i, 32 * c.wh + 16 * h2 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
                 }
                 if (c.r < 64) p.ec[(size_t)q * 64 + c.r] = c.KT->EC[c.r];
             }
@@ -956,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             if (c.trow < 64) {
                 const int i = c.trow;
                 unsigned char* phq = p.phi + (size_t)q * 16384;
-                float* ddl = p.dlt + ((size_t)q * 64 + i) * 64;
+
                 const float eci = c.KT->EC[i];
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
@@ -970,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                     st16_split(phq, phq + 8192, i, c0 >> 4, a);
 #pragma unroll
                     for (int e = 0; e < 16; e += 4)
-                        *reinterpret_cast<float4*>(ddl + c0 + e) = make_float4(b[e], b[e + 1], b[e + 2], b[e + 3]);
+                        *rec4(p.dlt, q, i, c0 + e) = make_float4(b[e], b[e + 1], b[e + 2], b[e + 3]);
                 }
             } else {
                 // the P W rows sit in lanes 0..63; the lanes 64..127 threads read them through the copy below
@@ -1007,7 +1020,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             CB_STAMP(0, 6);
             if (c.trow < 64) {
                 const int i = c.trow;
-                float* dy = p.ych + ((size_t)q * 64 + i) * 64;
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int c0 = 32 * c.wh + 16 * h2;
@@ -1016,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; e += 4)
-                        *reinterpret_cast<float4*>(dy + c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                        *rec4(p.ych, q, i, c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
                 }
             }
         }
@@ -1192,7 +1204,6 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
         }
         if (!wait_mma(1)) break;
         if (q4 < 2) {
-            float* dy = p.ych + ((size_t)q * 64 + trow) * 64;
 #pragma unroll 1
             for (int h2 = 0; h2 < 2; h2++) {
                 const int c0 = 32 * wh + 16 * h2;
@@ -1201,7 +1212,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; e += 4)
-                    *reinterpret_cast<float4*>(dy + c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                    *rec4(p.ych, q, trow, c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
             }
         }
         // the tiles are free: the next chunk's loads
@@ -1232,18 +1243,16 @@ __global__ void __launch_bounds__(256) chunk_chain_gated_kernel(const __grid_con
     const int dk = p.dk, dv = p.dv_, nk = p.nchunks;
     const size_t qb = (size_t)u * nk;
     auto rec = [&](const float* base, int k, float4 (&v)[4]) {
-        const float* src = base + (qb + k) * 4096 + i0 * 64 + j0;
-        v[0] = *reinterpret_cast<const float4*>(src);
-        v[1] = *reinterpret_cast<const float4*>(src + 4);
-        v[2] = *reinterpret_cast<const float4*>(src + 64);
-        v[3] = *reinterpret_cast<const float4*>(src + 68);
+        v[0] = *rec4(base, qb + k, i0, j0);
+        v[1] = *rec4(base, qb + k, i0, j0 + 4);
+        v[2] = *rec4(base, qb + k, i0 + 1, j0);
+        v[3] = *rec4(base, qb + k, i0 + 1, j0 + 4);
     };
     auto put = [&](float* base, int k, const float2 (&x)[8]) {
-        float* dst = base + (qb + k) * 4096 + i0 * 64 + j0;
-        *reinterpret_cast<float4*>(dst) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
-        *reinterpret_cast<float4*>(dst + 4) = make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
-        *reinterpret_cast<float4*>(dst + 64) = make_float4(x[4].x, x[4].y, x[5].x, x[5].y);
-        *reinterpret_cast<float4*>(dst + 68) = make_float4(x[6].x, x[6].y, x[7].x, x[7].y);
+        *rec4(base, qb + k, i0, j0) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
+        *rec4(base, qb + k, i0, j0 + 4) = make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
+        *rec4(base, qb + k, i0 + 1, j0) = make_float4(x[4].x, x[4].y, x[5].x, x[5].y);
+        *rec4(base, qb + k, i0 + 1, j0 + 4) = make_float4(x[6].x, x[6].y, x[7].x, x[7].y);
     };
     auto load_in = [&](const float* src, float2 (&s)[8]) {
 #pragma unroll
@@ -1358,17 +1367,17 @@ __global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_tc_kernel(const __g
     uint32_t* abortf = &misc[1];
 
     auto rec = [&](const float* base, int k, float (&v)[32]) {
-        const float4* src = reinterpret_cast<const float4*>(base + (qb + k) * 4096 + i * 64 + j0);
+        const float4* src = rec4(base, qb + k, i, j0);
 #pragma unroll
         for (int e = 0; e < 8; e++) {
-            const float4 t = src[e];
+            const float4 t = src[64 * e];
             v[4 * e] = t.x; v[4 * e + 1] = t.y; v[4 * e + 2] = t.z; v[4 * e + 3] = t.w;
         }
     };
     auto put = [&](float* base, int k, const float (&v)[32]) {
-        float4* dst = reinterpret_cast<float4*>(base + (qb + k) * 4096 + i * 64 + j0);
+        float4* dst = rec4(base, qb + k, i, j0);
 #pragma unroll
-        for (int e = 0; e < 8; e++) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        for (int e = 0; e < 8; e++) dst[64 * e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
     };
     auto load_in = [&](const float* src, float (&v)[32]) {
 #pragma unroll
@@ -1572,13 +1581,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
 
         // ---- S, dS' of the chunk (fp32 from the chain) -> hi/lo tiles [i][j]; sum_j dS'[i][j] S[i][j]
         {
-            const float* srow = p.st + ((size_t)q * 64 + t) * 64 + 16 * cq;
-            const float* drow = p.dst + ((size_t)q * 64 + t) * 64 + 16 * cq;
             float sv[16], dv16[16];
 #pragma unroll
             for (int e = 0; e < 16; e += 4) {
-                const float4 a = *reinterpret_cast<const float4*>(srow + e);
-                const float4 b = *reinterpret_cast<const float4*>(drow + e);
+                const float4 a = *rec4(p.st, q, t, 16 * cq + e);
+                const float4 b = *rec4(p.dst, q, t, 16 * cq + e);
                 sv[e] = a.x; sv[e + 1] = a.y; sv[e + 2] = a.z; sv[e + 3] = a.w;
                 dv16[e] = b.x; dv16[e + 1] = b.y; dv16[e + 2] = b.z; dv16[e + 3] = b.w;
             }

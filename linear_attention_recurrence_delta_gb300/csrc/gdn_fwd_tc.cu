@@ -155,8 +155,8 @@ __device__ __forceinline__ void zero_chunk(unsigned char* tile, int row, int q)
 }
 
 // The residuals a saving forward writes for the chunked backward (gdn_chunk_bwd.cu reads them with the same
-// layout), per chunk q = unit * nchunks + k.  p.st: the state entering the chunk, fp32 [64][64] (rows = key channel,
-// columns = value column).  p.sv, byte offsets in a chunk's record: P as hi, lo tiles; -N and Dinv (bf16 tiles,
+// layout), per chunk q = unit * nchunks + k.  p.st: the state entering the chunk, fp32 64 x 64 (rows = key channel,
+// columns = value column), column-group major.  p.sv, byte offsets in a chunk's record: P as hi, lo tiles; -N and Dinv (bf16 tiles,
 // the upper halves of the stacked solve operands); K strictly below the diagonal, fp32, packed by rows; -W as
 // hi, lo tiles ([t][i]); Util, fp32 [t][j].  Tiles are [64][64] 16-bit with the 128-byte swizzle of the MMA
 // operands.
@@ -166,12 +166,13 @@ __device__ __forceinline__ unsigned char* rec(const TcParams& p, int u, int k)
 {
     return p.sv + ((size_t)u * p.nchunks + k) * BYTES;
 }
-// state row `row`, columns 32 wh .. 32 wh + 31
+// state row `row`, columns 32 wh .. 32 wh + 31; the record is column-group major (the float4 of row r, columns
+// 4 g .. 4 g + 3 at index 64 g + r), so a warp's 32 rows write 512 contiguous bytes
 __device__ __forceinline__ void put_state(const TcParams& p, int u, int k, int row, int wh, const float (&v)[32])
 {
-    float4* d = reinterpret_cast<float4*>(p.st + (((size_t)u * p.nchunks + k) * 64 + row) * 64 + 32 * wh);
+    float4* d = reinterpret_cast<float4*>(p.st + ((size_t)u * p.nchunks + k) * 4096) + (8 * wh) * 64 + row;
 #pragma unroll
-    for (int e = 0; e < 8; e++) d[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+    for (int e = 0; e < 8; e++) d[64 * e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
 }
 }  // namespace svr
 
@@ -191,7 +192,7 @@ __device__ __forceinline__ const float* ktab(const unsigned char* sm, int tab, i
 
 // NORM: b and c arrive before their L2 normalisation (a template flag, so the plain kernel carries no trace of it).
 // SAVE (delta, one 64-column slab): the residuals of the chunked backward are written as well, per chunk q of the
-// unit: the entering state (p.st, fp32 [64][64]) and the solve's results (p.sv, the layout of namespace svr).  The
+// unit: the entering state (p.st, fp32 64 x 64, column-group major) and the solve's results (p.sv, the layout of namespace svr).  The
 // b-side level operands then leave beta out, so that the level products give K itself (M = beta K is formed
 // when it is assembled).
 template <bool DELTA, bool NORM, bool SAVE>
