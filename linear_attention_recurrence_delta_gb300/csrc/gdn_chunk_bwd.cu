@@ -148,8 +148,12 @@ constexpr uint32_t NW = 16384, U = 28672, DSN = 61440;              // U_hi | S_
 constexpr uint32_t BHH = 16384, BHL = 103424;
 constexpr uint32_t DU = 78848, Z = 0, DOR = 78848, ZR = 118784;
 constexpr uint32_t AD = 28672, NEARD = 61440, SEG = 28672, A1L = 78848, B1L = 95232;
-constexpr int kES = 65;                                  // row stride of the epilogue's fp32 arrays (conflict-free)
-constexpr uint32_t DC = 78848, DB = DC + 64 * kES * 4, DG = DB + 64 * kES * 4, PB = 53760;
+// row stride of the epilogue's fp32 arrays: float4 rows, and a warp's 32 rows at one column map 8 rows of a
+// quarter-warp onto disjoint bank groups (float4 access) or 32 consecutive banks (one row, 32 columns)
+constexpr int kES = 68;
+constexpr uint32_t SEG_END = SEG + 96 * kES * 4;
+constexpr uint32_t DC = 78848, DB = DC + 64 * kES * 4, DG = DB + 64 * kES * 4, PB = SEG_END;
+static_assert(PB + 64 * kES * 4 <= DC && DG + 64 * kES * 4 <= BYTES, "epilogue arrays");
 }  // namespace gl
 
 // The delta front's results that the gradient pass reuses, per chunk (byte offsets), written by the prep pass or
@@ -2078,15 +2082,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 ld16_bf16(sC, tt, cg, cv);
                 ld16_bf16(sB, tt, cg, bv);
 #pragma unroll
-                for (int e = 0; e < 16; e++) {
-                    const float a2 = S.A2[c0 + e];
-                    const float Et = fast_exp2(a2 * Gt), Eh = fast_exp2(a2 * (G63 - Gt));
-                    const float f1 = I >= 1 ? fast_exp2(a2 * (Gt - Gref)) : 0.f;
-                    const float dcv = dct[e] * Et + da1[e] * f1;
-                    DC[tt * gl::kES + c0 + e] = dcv;
-                    DB[tt * gl::kES + c0 + e] = dbh[e] * Eh;
-                    DG[tt * gl::kES + c0 + e] = dct[e] * cv[e] * Et - dbh[e] * bv[e] * Eh + da1[e] * f1 * cv[e];
-                    PB[tt * gl::kES + c0 + e] = dbh[e] * bv[e] * Eh;
+                for (int e4 = 0; e4 < 16; e4 += 4) {
+                    float o1[4], o2[4], o3[4], o4[4];
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        const int e = e4 + k;
+                        const float a2 = S.A2[c0 + e];
+                        const float Et = fast_exp2(a2 * Gt), Eh = fast_exp2(a2 * (G63 - Gt));
+                        const float f1 = I >= 1 ? fast_exp2(a2 * (Gt - Gref)) : 0.f;
+                        o1[k] = dct[e] * Et + da1[e] * f1;
+                        o2[k] = dbh[e] * Eh;
+                        o3[k] = dct[e] * cv[e] * Et - dbh[e] * bv[e] * Eh + da1[e] * f1 * cv[e];
+                        o4[k] = dbh[e] * bv[e] * Eh;
+                    }
+                    const int at = tt * gl::kES + c0 + e4;
+                    *reinterpret_cast<float4*>(DC + at) = make_float4(o1[0], o1[1], o1[2], o1[3]);
+                    *reinterpret_cast<float4*>(DB + at) = make_float4(o2[0], o2[1], o2[2], o2[3]);
+                    *reinterpret_cast<float4*>(DG + at) = make_float4(o3[0], o3[1], o3[2], o3[3]);
+                    *reinterpret_cast<float4*>(PB + at) = make_float4(o4[0], o4[1], o4[2], o4[3]);
                 }
             }
         }
@@ -2101,7 +2114,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 tmem_ld16(c.tl + 256 + c0, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; e++) SEGv[trow * gl::kES + c0 + e] = v[e] * fast_exp2(S.A2[c0 + e] * (Gref - Gs));
+                for (int e4 = 0; e4 < 16; e4 += 4) {
+                    float o[4];
+#pragma unroll
+                    for (int k = 0; k < 4; k++) o[k] = v[e4 + k] * fast_exp2(S.A2[c0 + e4 + k] * (Gref - Gs));
+                    *reinterpret_cast<float4*>(SEGv + trow * gl::kES + c0 + e4) = make_float4(o[0], o[1], o[2], o[3]);
+                }
             }
         }
         bar_all();
@@ -2117,13 +2135,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 tmem_wait_ld();
                 ld16_bf16(sB, tt, cg, bv);
 #pragma unroll
-                for (int e = 0; e < 16; e++) {
-                    const float a2 = S.A2[c0 + e];
-                    const float Et = fast_exp2(a2 * Gt);
-                    const float f1 = I >= 1 ? fast_exp2(a2 * (Gt - Gref)) : 0.f;
-                    const float dbt = -bet * drs[e];   // dBtil
-                    DB[tt * gl::kES + c0 + e] += dbt * Et + da1[e] * f1;
-                    DG[tt * gl::kES + c0 + e] += dbt * bv[e] * Et + da1[e] * f1 * bv[e];
+                for (int e4 = 0; e4 < 16; e4 += 4) {
+                    const int at = tt * gl::kES + c0 + e4;
+                    float4 xb = *reinterpret_cast<const float4*>(DB + at);
+                    float4 xg = *reinterpret_cast<const float4*>(DG + at);
+                    float ob[4] = {xb.x, xb.y, xb.z, xb.w}, og[4] = {xg.x, xg.y, xg.z, xg.w};
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        const int e = e4 + k;
+                        const float a2 = S.A2[c0 + e];
+                        const float Et = fast_exp2(a2 * Gt);
+                        const float f1 = I >= 1 ? fast_exp2(a2 * (Gt - Gref)) : 0.f;
+                        const float dbt = -bet * drs[e];   // dBtil
+                        ob[k] += dbt * Et + da1[e] * f1;
+                        og[k] += dbt * bv[e] * Et + da1[e] * f1 * bv[e];
+                    }
+                    *reinterpret_cast<float4*>(DB + at) = make_float4(ob[0], ob[1], ob[2], ob[3]);
+                    *reinterpret_cast<float4*>(DG + at) = make_float4(og[0], og[1], og[2], og[3]);
                 }
             }
         } else if (c.r < 64) {
@@ -2150,24 +2178,35 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 const int t = nt0 + ti;
                 float bv8[8];
                 ld_row8(sB, t, nch >> 3, bv8);
-                float dcv[4], dbv[4], gsum = 0.f;
+                float dcv[4], dbv[4], pbv[4], gsum = 0.f;
+                // this thread's four channels of the row's arrays (float4), the segments' shares summed in I order
+                float sg[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int I = 1; I <= 3; I++)
+                    if (t < 16 * I) {
+                        const float4 x = *reinterpret_cast<const float4*>(SEGv + (seg_base(I) + t) * gl::kES + nch);
+                        sg[0] += x.x; sg[1] += x.y; sg[2] += x.z; sg[3] += x.w;
+                    }
+                const float4 c4 = *reinterpret_cast<const float4*>(DC + t * gl::kES + nch);
+                const float4 b4 = *reinterpret_cast<const float4*>(DB + t * gl::kES + nch);
+                const float4 g4 = *reinterpret_cast<const float4*>(DG + t * gl::kES + nch);
+                const float dcr[4] = {c4.x, c4.y, c4.z, c4.w}, dbr[4] = {b4.x, b4.y, b4.z, b4.w};
+                const float dgr[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
                     const int i = nch + e, k = 4 * ti + e;
-                    float seg = 0.f;
-#pragma unroll
-                    for (int I = 1; I <= 3; I++)
-                        if (t < 16 * I) seg += SEGv[(seg_base(I) + t) * gl::kES + i];
-                    dcv[e] = DC[t * gl::kES + i] + nc[k];
-                    dbv[e] = DB[t * gl::kES + i] + seg + nb[k];
-                    float gam = DG[t * gl::kES + i] - ((nch & 4) ? bv8[4 + e] : bv8[e]) * seg + ng[k];
+                    const float seg = sg[e];
+                    dcv[e] = dcr[e] + nc[k];
+                    dbv[e] = dbr[e] + seg + nb[k];
+                    float gam = dgr[e] - ((nch & 4) ? bv8[4 + e] : bv8[e]) * seg + ng[k];
                     if (t == 63) {
                         const float sdi = S.sd[0][i] + S.sd[1][i] + S.sd[2][i] + S.sd[3][i];
                         gam += S.colsum[0][i] + sdi * c.KT->EC[i];
                     }
-                    PB[t * gl::kES + i] = S.G[t] * gam;
+                    pbv[e] = S.G[t] * gam;
                     gsum = fmaf(S.A2[i], gam, gsum);
                 }
+                *reinterpret_cast<float4*>(PB + t * gl::kES + nch) = make_float4(pbv[0], pbv[1], pbv[2], pbv[3]);
 #pragma unroll
                 for (int o = 1; o < 16; o <<= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
                 if (ncg == 0) S.dgp[0][t] = gsum / kLog2e;   // dG_t (A = A2 / log2 e)
