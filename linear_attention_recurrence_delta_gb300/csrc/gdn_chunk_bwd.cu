@@ -2269,18 +2269,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
     teardown(c, p, pending, full_phase, pending2, full2_phase);
 }
 
-// dA_log[h][i] = A[h][i] sum over batch rows and chunks of the chunk partials (fixed order)
-__global__ void chunk_dalog_kernel(const float* __restrict__ part, const float* __restrict__ A_log,
-                                   float* __restrict__ dA_log, int B, int H, int dk, int nchunks)
+// dA_log[h][i] = A[h][i] sum over batch rows and chunks of the chunk partials, in a fixed order: 256 threads per
+// head, thread (lane group g = threadIdx.x >> 6, channel i) sums the (batch, chunk) pairs n with n mod 4 = g in
+// order, then the four group sums are added in group order
+__global__ void __launch_bounds__(256) chunk_dalog_kernel(const float* __restrict__ part, const float* __restrict__ A_log,
+                                                          float* __restrict__ dA_log, int B, int H, int dk, int nchunks)
 {
-    const int h = blockIdx.x, i = threadIdx.x;
-    if (i >= dk) return;
+    __shared__ float grp[4][64];
+    const int h = blockIdx.x, i = threadIdx.x & 63, g = threadIdx.x >> 6;
+    const int n_all = B * nchunks;
     float acc = 0.f;
-    for (int bb = 0; bb < B; bb++) {
-        const size_t qb = ((size_t)bb * H + h) * nchunks;
-        for (int k = 0; k < nchunks; k++) acc += part[(qb + k) * 64 + i];
+    for (int n = g; n < n_all; n += 4) {
+        const int bb = n / nchunks, k = n - bb * nchunks;
+        acc += part[(((size_t)bb * H + h) * nchunks + k) * 64 + i];
     }
-    dA_log[h * dk + i] = -expf(A_log[h * dk + i]) * acc;
+    grp[g][i] = acc;
+    __syncthreads();
+    if (g == 0 && i < dk)
+        dA_log[h * dk + i] = -expf(A_log[h * dk + i]) * (((grp[0][i] + grp[1][i]) + grp[2][i]) + grp[3][i]);
 }
 
 template <typename K>
@@ -2371,7 +2377,7 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     else chunk_grad_kernel<false><<<grid, kThreads, grad_bytes, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     CB_MARK("grad");
-    chunk_dalog_kernel<<<a.H, 64, 0, st>>>(p.dA_part, a.A_log, a.dA_log, a.B, a.H, a.dk, p.nchunks);
+    chunk_dalog_kernel<<<a.H, 256, 0, st>>>(p.dA_part, a.A_log, a.dA_log, a.B, a.H, a.dk, p.nchunks);
     return cudaGetLastError();
 }
 
