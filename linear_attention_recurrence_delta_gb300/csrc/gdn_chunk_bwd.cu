@@ -158,11 +158,16 @@ static_assert(PB + 64 * kES * 4 <= DC && DG + 64 * kES * 4 <= BYTES, "epilogue a
 
 // The delta front's results that the gradient pass reuses, per chunk (byte offsets), written by the prep pass or
 // by a saving forward (gdn_fwd_tc.cu, the same layout): P as hi, lo tiles; -N and Dinv, one half each of the
-// stacked [-N ; -N] and [Dinv ; Dinv] operands; K strictly below the diagonal, packed by rows, fp32; -W, a bf16
-// tile [t][i] (its lo part after it: written by the saving forward only); Util, fp32 [t][j].
+// stacked [-N ; -N] and [Dinv ; Dinv] operands; K strictly below the diagonal, packed by columns (kp_index), fp32; -W, a bf16
+// tile [t][i] (its lo part after it: written by the saving forward only); Util, fp32, column-group major like the
+// records (rec4).
 namespace sv {
 constexpr uint32_t P = 0, NA = 16384, DINV = 24576, KP = 32768, NW = 40960, NWL = 49152, UT = 57344, BYTES = 73728;
 }  // namespace sv
+
+// K strictly below the diagonal, packed by columns: entry (t, s), s < t, at index s * 63 - s (s - 1) / 2 + t - s - 1
+// (2016 entries).  A warp's consecutive rows t at one column s are consecutive floats.
+__host__ __device__ __forceinline__ int kp_index(int t, int s) { return s * 63 - s * (s - 1) / 2 + (t - s - 1); }
 
 // fp32 sub-blocks inside MS: the diagonal 16-blocks of M, the 16-blocks below them inside each 32-block,
 // the diagonal blocks' inverses and the 32-blocks' coupling blocks
@@ -635,7 +640,7 @@ __device__ bool front_solve(Ctx& c, const CbParams& p, unsigned char* NEARb, uns
 #pragma unroll
                     for (int e = 0; e < 16; e++) {
                         const int s = 16 * cg + e;
-                        if (s < t) KP[t * (t - 1) / 2 + s] = v[16 * h2 + e];
+                        if (s < t) KP[kp_index(t, s)] = v[16 * h2 + e];
                     }
                 }
             }
@@ -945,10 +950,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
                         for (int e = 0; e < 16; e++) nw[e] = -v[e];
                         st16_bf16(svq + sv::NW, tt, cg, nw);
                     } else {
-                        float4* du = reinterpret_cast<float4*>(svq + sv::UT) + tt * 16 + 4 * cg;
+                        float4* du = reinterpret_cast<float4*>(svq + sv::UT) + (4 * cg) * 64 + tt;
 #pragma unroll
                         for (int e = 0; e < 4; e++)
-                            du[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                            du[64 * e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                     }
                 }
             }
@@ -1610,15 +1615,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         if (DELTA) {
             // Util (saved fp32) into TMEM as the start of U = Util - W S; -W came with the saved front
             if (!isK) {
-                const float4* urow =
-                    reinterpret_cast<const float4*>(p.sv + (size_t)q * sv::BYTES + sv::UT) + tt * 16;
+                const float4* urow = reinterpret_cast<const float4*>(p.sv + (size_t)q * sv::BYTES + sv::UT) + tt;
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
                     float v[16];
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
-                        const float4 x = urow[4 * cg + e];
+                        const float4 x = urow[(4 * cg + e) * 64];
                         v[4 * e] = x.x; v[4 * e + 1] = x.y; v[4 * e + 2] = x.z; v[4 * e + 3] = x.w;
                     }
                     tmem_st16(c.tl + TM_UT + 16 * cg, v);
@@ -1829,7 +1833,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     for (int e = 0; e < 16; e++) {
                         const int s = 16 * cg + e;
                         part -= bv[e] * fast_exp2(S.A2[s] * Gt) * drs[e];
-                        if (s < tt) part -= dru[e] * KP[tt * (tt - 1) / 2 + s];
+                        if (s < tt) part -= dru[e] * KP[kp_index(tt, s)];
                     }
                 }
                 S.rs[1][wh][tt] = part;

@@ -155,13 +155,15 @@ __device__ __forceinline__ void zero_chunk(unsigned char* tile, int row, int q)
 }
 
 // The residuals a saving forward writes for the chunked backward (gdn_chunk_bwd.cu reads them with the same
-// layout), per chunk q = unit * nchunks + k.  p.st: the state entering the chunk, fp32 64 x 64 (rows = key channel,
-// columns = value column), column-group major.  p.sv, byte offsets in a chunk's record: P as hi, lo tiles; -N and Dinv (bf16 tiles,
-// the upper halves of the stacked solve operands); K strictly below the diagonal, fp32, packed by rows; -W as
-// hi, lo tiles ([t][i]); Util, fp32 [t][j].  Tiles are [64][64] 16-bit with the 128-byte swizzle of the MMA
-// operands.
+// layout), per chunk q = unit * nchunks + k.  p.st: the state entering the chunk, fp32 64 x 64 (rows = key
+// channel, columns = value column), column-group major (row r, columns 4 g .. 4 g + 3 at float4 64 g + r).
+// p.sv, byte offsets in a chunk's record: P as hi, lo tiles; -N and Dinv (bf16 tiles, the upper halves of the
+// stacked solve operands); K strictly below the diagonal, fp32, packed by columns (kp_index: a warp's rows at one
+// column are consecutive); -W as hi, lo tiles ([t][i]); Util, fp32, column-group major.  Tiles are [64][64]
+// 16-bit with the 128-byte swizzle of the MMA operands.
 namespace svr {
 constexpr uint32_t P = 0, NA = 16384, DINV = 24576, KP = 32768, NW = 40960, NWL = 49152, UT = 57344, BYTES = 73728;
+__device__ __forceinline__ int kp_index(int t, int s) { return s * 63 - s * (s - 1) / 2 + (t - s - 1); }
 __device__ __forceinline__ unsigned char* rec(const TcParams& p, int u, int k)
 {
     return p.sv + ((size_t)u * p.nchunks + k) * BYTES;
@@ -695,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                             for (int c = 0; c < 16; c++) {
                                 const int sc = 16 * cg + c;
-                                if (sc < t) kp[t * (t - 1) / 2 + sc] = out[c];
+                                if (sc < t) kp[svr::kp_index(t, sc)] = out[c];
                                 out[c] *= bet;
                             }
                         }
@@ -967,9 +969,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             st_split16(rq + svr::NW, rq + svr::NWL, trow, cg, v);
                             tmem_ld16(tl + TM_U + 16 * cg, v);   // Util, before S is folded in
                             tmem_wait_ld();
-                            float4* du = reinterpret_cast<float4*>(rq + svr::UT) + trow * 16 + 4 * cg;
+                            float4* du = reinterpret_cast<float4*>(rq + svr::UT) + (4 * cg) * 64 + trow;
 #pragma unroll
-                            for (int e = 0; e < 4; e++) du[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                            for (int e = 0; e < 4; e++)
+                                du[64 * e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                         }
                     }
                 }
