@@ -147,11 +147,13 @@ constexpr uint32_t NA = 0, X0 = 28672;
 constexpr uint32_t NW = 16384, U = 28672, DSN = 61440;              // U_hi | S_hi | U_lo | S_lo
 constexpr uint32_t BHH = 16384, BHL = 103424;
 constexpr uint32_t DU = 78848, Z = 0, DOR = 78848, ZR = 118784;
-constexpr uint32_t AD = 28672, NEARD = 61440, SEG = 28672, A1L = 78848, B1L = 95232;
+constexpr uint32_t AD = 28672, NEARD = 61440, SEG = 28672, A1L = 78848, B1L = 118784;
 // row stride of the epilogue's fp32 arrays: float4 rows, and a warp's 32 rows at one column map 8 rows of a
 // quarter-warp onto disjoint bank groups (float4 access) or 32 consecutive banks (one row, 32 columns)
 constexpr int kES = 68;
 constexpr uint32_t SEG_END = SEG + 96 * kES * 4;
+// the dQ block reads K (KP) while other warps may already write the next level operands: they must not meet
+static_assert(A1L + 16384 <= KP && B1L >= KP + 8192 && B1L + 96 * 128 <= BYTES, "level operands clear of K");
 constexpr uint32_t DC = 78848, DB = DC + 64 * kES * 4, DG = DB + 64 * kES * 4, PB = SEG_END;
 static_assert(PB + 64 * kES * 4 <= DC && DG + 64 * kES * 4 <= BYTES, "epilogue arrays");
 }  // namespace gl
@@ -1860,7 +1862,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     nd[e] = I == 0 ? row[e] : (I == 1 ? row[16 + e] : (I == 2 ? row[32 + e] : row[48 + e]));
             }
         }
-        // the 16-block level's operands again as fp16 hi/lo pairs (their space was reused)
+        // the 16-block level's operands again as fp16 hi/lo pairs (their space was reused; none of them covers K's
+        // packed rows, which the dbeta part above may still be reading in other warps)
         CB_STAMP(1, 9);
         front_operands(c, X + gl::A1, X + gl::B1, true, X + gl::A1L, X + gl::B1L, DELTA);
         smem_to_tc();
