@@ -204,9 +204,9 @@ gdn_status_t gdn_bwd(const gdn_shape_t* shape,
  * recompute ("GDN & MLA Mechanism Deep-Dive", Step 5: each chunk's closed form
  * is a function of its inputs and the state entering it).  Per chunk of 64
  * tokens `saved` receives the entering state (fp32 64 x 64, 16 KB) and the
- * results of the chunk's delta solve that the backward reuses (72 KB: the
- * decay-weighted scores P, K, the block inverse D^-1 and N, W, Util; layout
- * private to the library).  gdn_bwd_saved then takes them instead of running
+ * results of the chunk's delta solve that the backward reuses (80 KB: the
+ * decay-weighted scores P, K, the block inverse D^-1 and N, W and
+ * U = Util - W S; layout private to the library).  gdn_bwd_saved then takes them instead of running
  * the forward sweep again.  Arguments and results are those of gdn_fwd, plus
  * `saved`: device memory of at least gdn_saved_bytes(shape) bytes, 256-byte
  * aligned, written completely by the call.  o and hT equal gdn_fwd's within

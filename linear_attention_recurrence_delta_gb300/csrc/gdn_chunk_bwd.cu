@@ -141,7 +141,7 @@ constexpr uint32_t GA = 0;
 
 // grad layout
 namespace gl {
-constexpr uint32_t A1 = 0, B1 = 16384, LR = 28672, LRL = 53248, NEAR = 69632, P = 78848, KP = 95232,
+constexpr uint32_t A1 = 0, B1 = 16384, LR = 28672, LRL = 53248, NEAR = 69632, P = 78848,
                    MS = 103424, DINV = 118784, BYTES = 135168;
 constexpr uint32_t NA = 0, X0 = 28672;
 constexpr uint32_t NW = 16384, U = 28672, DSN = 61440;              // U_hi | S_hi | U_lo | S_lo
@@ -152,24 +152,18 @@ constexpr uint32_t AD = 28672, NEARD = 61440, SEG = 28672, A1L = 78848, B1L = 11
 // quarter-warp onto disjoint bank groups (float4 access) or 32 consecutive banks (one row, 32 columns)
 constexpr int kES = 68;
 constexpr uint32_t SEG_END = SEG + 96 * kES * 4;
-// the dQ block reads K (KP) while other warps may already write the next level operands: they must not meet
-static_assert(A1L + 16384 <= KP && B1L >= KP + 8192 && B1L + 96 * 128 <= BYTES, "level operands clear of K");
 constexpr uint32_t DC = 78848, DB = DC + 64 * kES * 4, DG = DB + 64 * kES * 4, PB = SEG_END;
 static_assert(PB + 64 * kES * 4 <= DC && DG + 64 * kES * 4 <= BYTES, "epilogue arrays");
 }  // namespace gl
 
 // The delta front's results that the gradient pass reuses, per chunk (byte offsets), written by the prep pass or
 // by a saving forward (gdn_fwd_tc.cu, the same layout): P as hi, lo tiles; -N and Dinv, one half each of the
-// stacked [-N ; -N] and [Dinv ; Dinv] operands; K strictly below the diagonal, packed by columns (kp_index), fp32; -W, a bf16
-// tile [t][i] (its lo part after it: written by the saving forward only); Util, fp32, column-group major like the
-// records (rec4).
+// stacked [-N ; -N] and [Dinv ; Dinv] operands; K (zero on and above the diagonal), fp32 64 x 64; -W, a bf16 tile
+// [t][i] (its lo part after it: written by the saving forward only); at UT, fp32 [t][j], Util from the prep pass
+// or U = Util - W S from the saving forward.  The fp32 matrices are column-group major like the records (rec4).
 namespace sv {
-constexpr uint32_t P = 0, NA = 16384, DINV = 24576, KP = 32768, NW = 40960, NWL = 49152, UT = 57344, BYTES = 73728;
+constexpr uint32_t P = 0, NA = 16384, DINV = 24576, K = 32768, NW = 49152, NWL = 57344, UT = 65536, BYTES = 81920;
 }  // namespace sv
-
-// K strictly below the diagonal, packed by columns: entry (t, s), s < t, at index s * 63 - s (s - 1) / 2 + t - s - 1
-// (2016 entries).  A warp's consecutive rows t at one column s are consecutive floats.
-__host__ __device__ __forceinline__ int kp_index(int t, int s) { return s * 63 - s * (s - 1) / 2 + (t - s - 1); }
 
 // fp32 sub-blocks inside MS: the diagonal 16-blocks of M, the 16-blocks below them inside each 32-block,
 // the diagonal blocks' inverses and the 32-blocks' coupling blocks
@@ -596,8 +590,8 @@ __device__ __forceinline__ void write_dinv(Ctx& c, unsigned char* MS, unsigned c
 }
 
 // The delta front after the level product: assemble P (into the hi/lo tile Pt) and M = diag(beta) K
-// (L part into LR block 0, diagonal and coupling 16-blocks into MS, optionally K strictly below the diagonal,
-// packed, into KP), invert the 32-blocks, write [Dinv ; Dinv], run [N | X0] = Dinv [L | R] and
+// (L part into LR block 0, diagonal and coupling 16-blocks into MS, optionally K, fp32 column-group major, into
+// KP), invert the 32-blocks, write [Dinv ; Dinv], run [N | X0] = Dinv [L | R] and
 // [Util | W] = X0 - N X0 (both copies in TMEM lanes 0..63 and 64..127).  R was written by the operand step.
 // Returns false on an abort.
 template <bool DELTA>
@@ -639,11 +633,12 @@ __device__ bool front_solve(Ctx& c, const CbParams& p, unsigned char* NEARb, uns
                         *reinterpret_cast<float4*>(f32 + e) = make_float4(m16[e], m16[e + 1], m16[e + 2], m16[e + 3]);
                 }
                 if (KP) {
+                    // K's row (zero on and above the diagonal), column-group major
+                    float4* kr = reinterpret_cast<float4*>(KP) + (4 * cg) * 64 + t;
 #pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        const int s = 16 * cg + e;
-                        if (s < t) KP[kp_index(t, s)] = v[16 * h2 + e];
-                    }
+                    for (int e = 0; e < 4; e++)
+                        kr[64 * e] = make_float4(v[16 * h2 + 4 * e], v[16 * h2 + 4 * e + 1], v[16 * h2 + 4 * e + 2],
+                                                 v[16 * h2 + 4 * e + 3]);
                 }
             }
         }
@@ -753,14 +748,14 @@ __device__ __forceinline__ void issue_saved(const CbParams& p, Small& S, unsigne
     if (q == p.starve) return;
     unsigned char* X = sm + OFF_X;
     const unsigned char* src = p.sv + (size_t)q * sv::BYTES;
-    mbar_arrive_expect_tx(&S.full2, 16384 + 6 * 8192);
+    // -W only where U is still to be formed (a saving forward's record holds U itself)
+    mbar_arrive_expect_tx(&S.full2, 16384 + 4 * 8192 + (p.rev_only ? 0 : 8192));
     bulk_g2s(X + gl::P, src + sv::P, 16384, &S.full2);
     bulk_g2s(X + gl::NA, src + sv::NA, 8192, &S.full2);
     bulk_g2s(X + gl::NA + 8192, src + sv::NA, 8192, &S.full2);
     bulk_g2s(X + gl::DINV, src + sv::DINV, 8192, &S.full2);
     bulk_g2s(X + gl::DINV + 8192, src + sv::DINV, 8192, &S.full2);
-    bulk_g2s(X + gl::KP, src + sv::KP, 8192, &S.full2);
-    bulk_g2s(X + gl::NW, src + sv::NW, 8192, &S.full2);
+    if (!p.rev_only) bulk_g2s(X + gl::NW, src + sv::NW, 8192, &S.full2);
 }
 
 __device__ __forceinline__ void prefetch_tma(const CbParams& p, int q)
@@ -914,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             if (!mma_wait(c, p, 4)) break;
             unsigned char* svq = p.sv + (size_t)q * sv::BYTES;
             if (!front_solve<true>(c, p, X + pl::NEAR, X + pl::P, X + pl::LR, X + pl::LRL, X + pl::MS, X + pl::DINV,
-                                   X + pl::NA, X + pl::X0, reinterpret_cast<float*>(svq + sv::KP), 0))
+                                   X + pl::NA, X + pl::X0, reinterpret_cast<float*>(svq + sv::K), 0))
                 break;
             CB_STAMP(0, 4);
             // saved for the gradient pass: the P tiles and one half each of [-N ; -N] and [Dinv ; Dinv]
@@ -1550,7 +1545,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             // this chunk's S, dS' (and Util) records and the next chunk's tiles towards L2
             prefetch_l2_bulk(p.st + (size_t)q * 4096, 16384);
             prefetch_l2_bulk(p.dst + (size_t)q * 4096, 16384);
-            if (DELTA) prefetch_l2_bulk(p.sv + (size_t)q * sv::BYTES + sv::UT, 16384);
+            if (DELTA) {
+                prefetch_l2_bulk(p.sv + (size_t)q * sv::BYTES + sv::UT, 16384);
+                prefetch_l2_bulk(p.sv + (size_t)q * sv::BYTES + sv::K, 16384);
+            }
             if (q + (int)gridDim.x < p.nq) prefetch_tma(p, q + gridDim.x);
         }
         if (c.warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && c.lane == 0)
@@ -1614,7 +1612,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 zero16(X + gl::U + 16384, t, cq);
             }
         }
-        if (DELTA) {
+        if (DELTA && p.rev_only) {
+            // a saving forward kept U itself: straight into its hi/lo tiles
+            if (!isK) {
+                const float4* urow = reinterpret_cast<const float4*>(p.sv + (size_t)q * sv::BYTES + sv::UT) + tt;
+#pragma unroll 1
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int cg = 2 * wh + h2;
+                    float v[16];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const float4 x = urow[(4 * cg + e) * 64];
+                        v[4 * e] = x.x; v[4 * e + 1] = x.y; v[4 * e + 2] = x.z; v[4 * e + 3] = x.w;
+                    }
+                    st16_split(X + gl::U, X + gl::U + 16384, tt, cg, v);
+                }
+            }
+        } else if (DELTA) {
             // Util (saved fp32) into TMEM as the start of U = Util - W S; -W came with the saved front
             if (!isK) {
                 const float4* urow = reinterpret_cast<const float4*>(p.sv + (size_t)q * sv::BYTES + sv::UT) + tt;
@@ -1822,11 +1836,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 // dbeta_t = sum_j dR V - sum_i Btil (dR S^T) - sum_{s<t} (dR U^T) K   (dMm = -dR U^T)
                 float part = 0.f;
                 const float Gt = S.G[tt];
-                const float* KP = fptr(X, gl::KP);
+                // K's row tt from the saved front (L2), column-group major
+                const float4* kr = reinterpret_cast<const float4*>(p.sv + (size_t)q * sv::BYTES + sv::K) + tt;
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
-                    float drs[16], dru[16], bv[16];
+                    float drs[16], dru[16], bv[16], kv[16];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const float4 x = kr[(4 * cg + e) * 64];
+                        kv[4 * e] = x.x; kv[4 * e + 1] = x.y; kv[4 * e + 2] = x.z; kv[4 * e + 3] = x.w;
+                    }
                     tmem_ld16(c.tl + 64 + 16 * cg, drs);
                     tmem_ld16(c.tl + 16 * cg, dru);
                     tmem_wait_ld();
@@ -1835,7 +1855,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     for (int e = 0; e < 16; e++) {
                         const int s = 16 * cg + e;
                         part -= bv[e] * fast_exp2(S.A2[s] * Gt) * drs[e];
-                        if (s < tt) part -= dru[e] * KP[kp_index(tt, s)];
+                        if (s < tt) part -= dru[e] * kv[e];
                     }
                 }
                 S.rs[1][wh][tt] = part;

@@ -155,15 +155,14 @@ __device__ __forceinline__ void zero_chunk(unsigned char* tile, int row, int q)
 }
 
 // The residuals a saving forward writes for the chunked backward (gdn_chunk_bwd.cu reads them with the same
-// layout), per chunk q = unit * nchunks + k.  p.st: the state entering the chunk, fp32 64 x 64 (rows = key
-// channel, columns = value column), column-group major (row r, columns 4 g .. 4 g + 3 at float4 64 g + r).
-// p.sv, byte offsets in a chunk's record: P as hi, lo tiles; -N and Dinv (bf16 tiles, the upper halves of the
-// stacked solve operands); K strictly below the diagonal, fp32, packed by columns (kp_index: a warp's rows at one
-// column are consecutive); -W as hi, lo tiles ([t][i]); Util, fp32, column-group major.  Tiles are [64][64]
-// 16-bit with the 128-byte swizzle of the MMA operands.
+// layout), per chunk q = unit * nchunks + k.  p.st: the state S entering the chunk, fp32 64 x 64 (rows = key
+// channel, columns = value column).  p.sv, byte offsets in a chunk's record: P as hi, lo tiles; -N and Dinv (bf16
+// tiles, the upper halves of the stacked solve operands); K (zero on and above the diagonal), fp32 64 x 64; -W as
+// hi, lo tiles ([t][i]); U = Util - W S, fp32 [t][j].  Tiles are [64][64] 16-bit with the 128-byte swizzle of the
+// MMA operands; the fp32 matrices are column-group major (row r, columns 4 g .. 4 g + 3 at float4 64 g + r), so a
+// warp's 32 rows store 512 contiguous bytes.
 namespace svr {
-constexpr uint32_t P = 0, NA = 16384, DINV = 24576, KP = 32768, NW = 40960, NWL = 49152, UT = 57344, BYTES = 73728;
-__device__ __forceinline__ int kp_index(int t, int s) { return s * 63 - s * (s - 1) / 2 + (t - s - 1); }
+constexpr uint32_t P = 0, NA = 16384, DINV = 24576, K = 32768, NW = 49152, NWL = 57344, U = 65536, BYTES = 81920;
 __device__ __forceinline__ unsigned char* rec(const TcParams& p, int u, int k)
 {
     return p.sv + ((size_t)u * p.nchunks + k) * BYTES;
@@ -691,15 +690,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             }
                         }
                         if (SAVE && isM) {
-                            // the level products gave K: its strictly lower part is a residual, M = beta K
-                            float* kp = reinterpret_cast<float*>(svr::rec(p, u, k) + svr::KP);
+                            // the level products gave K (zero on and above the diagonal): a residual; M = beta K
+                            float4* kr = reinterpret_cast<float4*>(svr::rec(p, u, k) + svr::K) + (4 * cg) * 64 + t;
                             const float bet = S.beta[s][t];
 #pragma unroll
-                            for (int c = 0; c < 16; c++) {
-                                const int sc = 16 * cg + c;
-                                if (sc < t) kp[svr::kp_index(t, sc)] = out[c];
-                                out[c] *= bet;
-                            }
+                            for (int e = 0; e < 4; e++)
+                                kr[64 * e] = make_float4(out[4 * e], out[4 * e + 1], out[4 * e + 2], out[4 * e + 3]);
+#pragma unroll
+                            for (int c = 0; c < 16; c++) out[c] *= bet;
                         }
                         if (!isM) {
                             st_split16(sm + OFF_CH0, sm + OFF_CH0L, 64 + t, cg, out);
@@ -967,12 +965,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (SAVE) {
                             unsigned char* rq = svr::rec(p, u, k);
                             st_split16(rq + svr::NW, rq + svr::NWL, trow, cg, v);
-                            tmem_ld16(tl + TM_U + 16 * cg, v);   // Util, before S is folded in
-                            tmem_wait_ld();
-                            float4* du = reinterpret_cast<float4*>(rq + svr::UT) + (4 * cg) * 64 + trow;
-#pragma unroll
-                            for (int e = 0; e < 4; e++)
-                                du[64 * e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                         }
                     }
                 }
@@ -997,6 +989,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         tmem_ld16(tl + TM_U + 16 * cg, v);
                         tmem_wait_ld();
                         st_split16(X + X_UH, X + X_UL, trow, cg, v);
+                        if (SAVE) {
+                            // U itself (the state already folded in) is a residual
+                            float4* du = reinterpret_cast<float4*>(svr::rec(p, u, k) + svr::U) + (4 * cg) * 64 + trow;
+#pragma unroll
+                            for (int e = 0; e < 4; e++)
+                                du[64 * e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                        }
                     }
                 }
                 smem_to_tc();

@@ -85,7 +85,7 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm = 0, int logits 
 // calls take the token-serial one (with its time split for long sequences over few heads).
 // Residuals a saving forward keeps for it, per chunk of 64 tokens: the entering state (fp32 64 x 64) and the
 // delta solve's results (layout in gdn_chunk_bwd.cu, namespace sv).
-constexpr size_t kSavedStateBytes = 16384, kSavedSolveBytes = 73728;
+constexpr size_t kSavedStateBytes = 16384, kSavedSolveBytes = 81920;
 inline bool chunk_bwd_applies(const gdn_shape_t& s, int logits, int norm)
 {
     return s.io == GDN_BF16 && s.T > 0 && s.dk <= 64 && s.dv <= 64 && !logits && !norm;

@@ -117,7 +117,8 @@ def test_wide_head_workspace(lib):
     of db, dc [slabs, B, T, H, d_k] and dg, dbeta [slabs, B, T, H]."""
     B, H, T = 2, 4, 256
     assert gdn.gdn_workspace_bytes(gdn.make_shape(B, H, T, 128, 128, "delta", "bf16"), 0) == 256
-    one = gdn.gdn_workspace_bytes(gdn.make_shape(B, H, T, 64, 64, "delta", "bf16"), 1)
+    # (logit gates keep the 64-wide head on the token-serial backward, whose buffers this compares)
+    one = gdn.gdn_workspace_bytes(gdn.make_shape(B, H, T, 64, 64, "delta", "bf16", gate_logits=True), 1)
     two = gdn.gdn_workspace_bytes(gdn.make_shape(B, H, T, 64, 128, "delta", "bf16"), 1)
     four = gdn.gdn_workspace_bytes(gdn.make_shape(B, H, T, 128, 128, "delta", "bf16"), 1)
     ntok = B * T * H
@@ -159,9 +160,9 @@ def test_time_split_backward_workspace():
 def test_chunked_backward_workspace():
     """The chunked backward (bf16, heads up to 64 wide, no option bits) keeps per chunk of 64 tokens five 16 KB
     64 x 64 records in delta mode (transition as bf16 hi/lo tiles, zero-start state, adjoint share, entering state,
-    leaving adjoint) plus the 72 KB of the front's results that the gradient pass reuses, four fp32 records in
+    leaving adjoint) plus the 80 KB of the front's results that the gradient pass reuses, four fp32 records in
     gated mode, and two rows of 64 floats (decay, dA partial), after the 256-byte status word."""
-    for mode, per_chunk in (("delta", 5 * 16384 + 73728), ("gated", 4 * 16384)):
+    for mode, per_chunk in (("delta", 5 * 16384 + 81920), ("gated", 4 * 16384)):
         for B, H, T, d in ((8, 16, 4096, 64), (1, 16, 32768, 64), (2, 3, 100, 56), (1, 1, 1, 8)):
             s = gdn.make_shape(B, H, T, d, d, mode, "bf16")
             nq = B * H * -(-T // 64)
@@ -299,14 +300,14 @@ def test_plan_and_workspace_agree_on_random_shapes():
 
 
 def test_saved_residuals_sizes_and_argument_errors(lib):
-    """gdn_saved_bytes: per chunk of 64 tokens a 16 KB state and 72 KB of solve results, for delta-mode bf16 shapes
+    """gdn_saved_bytes: per chunk of 64 tokens a 16 KB state and 80 KB of solve results, for delta-mode bf16 shapes
     whose forward is one tensor-core pass and whose backward is the chunked one; 0 for every other shape.  The
     backward from the residuals needs a smaller workspace (backward = 2).  gdn_fwd_save and gdn_bwd_saved reject
     bad arguments before any device work."""
     for B, H, T, d in ((8, 16, 4096, 64), (2, 3, 100, 56), (1, 1, 9, 8)):
         s = gdn.make_shape(B, H, T, d, d, "delta", "bf16")
         nq = B * H * -(-T // 64)
-        assert gdn.gdn_saved_bytes(s) == nq * (16384 + 73728)
+        assert gdn.gdn_saved_bytes(s) == nq * (16384 + 81920)
         assert 0 < gdn.gdn_workspace_bytes(s, 2) < gdn.gdn_workspace_bytes(s, 1)
     none = [gdn.make_shape(8, 16, 4096, 64, 64, "gated", "bf16"),            # gated mode
             gdn.make_shape(2, 2, 256, 64, 64, "delta", "f32"),               # fp32 I/O

@@ -28,7 +28,7 @@ def run_saved(w, x, dhT):
     o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
     hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
     nbytes = gdn.gdn_saved_bytes(s)
-    assert nbytes == B * H * -(-T // 64) * (16384 + 73728)
+    assert nbytes == B * H * -(-T // 64) * (16384 + 81920)
     saved = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN patterns: all must be written
     ws0 = torch.empty(gdn.gdn_workspace_bytes(s, 0), dtype=torch.uint8, device="cuda")
     gdn.check(gdn.gdn_fwd_save(s, t["v"], t["b"], t["c"], t["g"], t["beta"], A_log, h0, o, hT, saved, ws0),
