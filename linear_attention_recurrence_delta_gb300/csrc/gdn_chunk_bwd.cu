@@ -1133,6 +1133,16 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
         } else if (r < 128) {
             const int i = r - 64;
             S.A2[i] = i < p.dk ? -expf(p.A_log[h * p.dk + i]) * kLog2e : 0.f;
+        } else if (r == 128 && q + (int)gridDim.x < p.nq) {
+            // the next chunk's tiles and residuals towards L2 (its loads go out when this chunk is done)
+            const int qn = q + gridDim.x, un = qn / p.nchunks, kn = qn - un * p.nchunks, bn = un / p.H,
+                      hn = un - bn * p.H;
+            tma_prefetch_l2(&p.tm_b, 0, hn, 64 * kn, bn);
+            tma_prefetch_l2(&p.tm_c, 0, hn, 64 * kn, bn);
+            tma_prefetch_l2(&p.tm_do, 0, hn, 64 * kn, bn);
+            const unsigned char* rq = p.sv + (size_t)qn * sv::BYTES;
+            prefetch_l2_bulk(rq + sv::P, 16384);
+            prefetch_l2_bulk(rq + sv::NW, 16384);
         }
         if (warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
             atomicExch(p.status + 2, 5u);
@@ -1549,7 +1559,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 prefetch_l2_bulk(p.sv + (size_t)q * sv::BYTES + sv::UT, 16384);
                 prefetch_l2_bulk(p.sv + (size_t)q * sv::BYTES + sv::K, 16384);
             }
-            if (q + (int)gridDim.x < p.nq) prefetch_tma(p, q + gridDim.x);
+            if (q + (int)gridDim.x < p.nq) {
+                prefetch_tma(p, q + gridDim.x);
+                // the next chunk's saved front (P, -N, Dinv, -W: the bulk copies at this chunk's end)
+                if (DELTA) prefetch_l2_bulk(p.sv + (size_t)(q + gridDim.x) * sv::BYTES, sv::K);
+                if (DELTA && !p.rev_only) prefetch_l2_bulk(p.sv + (size_t)(q + gridDim.x) * sv::BYTES + sv::NW, 8192);
+            }
         }
         if (c.warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && c.lane == 0)
             atomicExch(p.status + 2, 2u);
@@ -2306,6 +2321,7 @@ __global__ void __launch_bounds__(256) chunk_dalog_kernel(const float* __restric
     const int h = blockIdx.x, i = threadIdx.x & 63, g = threadIdx.x >> 6;
     const int n_all = B * nchunks;
     float acc = 0.f;
+#pragma unroll 8
     for (int n = g; n < n_all; n += 4) {
         const int bb = n / nchunks, k = n - bb * nchunks;
         acc += part[(((size_t)bb * H + h) * nchunks + k) * 64 + i];
