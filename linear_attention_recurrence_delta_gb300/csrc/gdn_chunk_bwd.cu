@@ -142,12 +142,16 @@ constexpr uint32_t GA = 0;
 // grad layout
 namespace gl {
 constexpr uint32_t A1 = 0, B1 = 16384, LR = 28672, LRL = 53248, NEAR = 69632, P = 78848,
-                   MS = 103424, DINV = 118784, BYTES = 135168;
+                   MS = 103424, DINV = 118784, BYTES = 140288;
 constexpr uint32_t NA = 0, X0 = 28672;
 constexpr uint32_t NW = 16384, U = 28672, DSN = 61440;              // U_hi | S_hi | U_lo | S_lo
 constexpr uint32_t BHH = 16384, BHL = 103424;
-constexpr uint32_t DU = 78848, Z = 0, DOR = 78848, ZR = 118784;
-constexpr uint32_t AD = 28672, NEARD = 61440, SEG = 28672, A1L = 78848, B1L = 118784;
+constexpr uint32_t DU = 78848, Z = 0, DOR = 78848, ZR = 0;
+// the level operands of the reverse pass (A1H, A1L hi/lo; B1, B1L hi/lo) are written while [dO ; dR] [U | S]^T and
+// U dS'^T run: clear of DOR, ZR, U and DSN, which those products read
+constexpr uint32_t AD = 28672, NEARD = 61440, SEG = 28672, A1H = 95232, A1L = 111616, B1L = 128000;
+static_assert(B1 >= ZR + 16384 && B1 + 96 * 128 <= U && A1H >= DOR + 16384 && B1L + 96 * 128 <= BYTES,
+              "reverse-pass level operands clear of the products in flight");
 // row stride of the epilogue's fp32 arrays: float4 rows, and a warp's 32 rows at one column map 8 rows of a
 // quarter-warp onto disjoint bank groups (float4 access) or 32 consecutive banks (one row, 32 columns)
 constexpr int kES = 68;
@@ -1827,6 +1831,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             if (DELTA) mma_tiles(c.tbase + 128, ul, false, 0, 0, dsn, false, 0, 0, 4, id9, true);
             mma_commit(&S.mma);
         }
+        // while they run: the 16-block level's operands again, as fp16 hi/lo pairs (and, delta, the anchors); they
+        // depend on b, c and the decay only
+        front_operands(c, X + gl::A1H, X + gl::B1, true, X + gl::A1L, X + gl::B1L, DELTA);
         if (!mma_wait(c, p, 12)) break;
         CB_STAMP(1, 8);
         // ---- dQ (lanes 0..63) and dK = -beta (dR U^T) below the diagonal (lanes 64..127): the 16-block level's
@@ -1897,10 +1904,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     nd[e] = I == 0 ? row[e] : (I == 1 ? row[16 + e] : (I == 2 ? row[32 + e] : row[48 + e]));
             }
         }
-        // the 16-block level's operands again as fp16 hi/lo pairs (their space was reused; none of them covers K's
-        // packed rows, which the dbeta part above may still be reading in other warps)
         CB_STAMP(1, 9);
-        front_operands(c, X + gl::A1, X + gl::B1, true, X + gl::A1L, X + gl::B1L, DELTA);
         smem_to_tc();
         if (c.r == 0) {
             // dA1 = A_d B1 (TMEM 192..255): rows 0..63 -> dc, 64..127 -> db (row side)
@@ -1909,7 +1913,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             mma_tiles(c.tbase + 192, ad, false, 0, 16384, smem_u32(X + gl::B1L), true, 8192, 0, 6, id10, true);
             // dB1 = A_d^T A1 (TMEM 256..319): rows = segments (column side)
             const uint32_t id11 = idesc_f16(128, 64, true, true);
-            mma_tiles(c.tbase + 256, ad, true, 16384, 0, smem_u32(X + gl::A1), true, 8192, 0, 8, id11, false);
+            mma_tiles(c.tbase + 256, ad, true, 16384, 0, smem_u32(X + gl::A1H), true, 8192, 0, 8, id11, false);
             mma_tiles(c.tbase + 256, ad, true, 16384, 0, smem_u32(X + gl::A1L), true, 8192, 0, 8, id11, true);
             mma_commit(&S.mma);
         }
