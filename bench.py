@@ -56,7 +56,11 @@ def load_peaks():
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one forward launch from an ncu capture, with the
 # SHA-256 of the kernel's source files at the time of the capture.  When a source no longer matches, the counters
 # describe another kernel and the line reports traffic = null until the capture is retaken.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    # profiles/fwd_tc_delta_8x16x4096x64.md: dram__bytes_read.sum 203621120 + dram__bytes_write.sum 43716352
+    "delta_bf16_8x16x4096x64": {"bytes": 247337472, "files": ["gdn_fwd_tc.cu", "fwd_tc_common.cuh", "tc_ptx.cuh"],
+                                "sha256": "a93d039c0eb6ba1a98048d0bbece796729c9dc04d4feebf7bd1084e5eb9edb73"},
+}
 
 
 def source_digest(files):
