@@ -218,6 +218,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 __device__ __forceinline__ float* fptr(unsigned char* base, uint32_t off) { return reinterpret_cast<float*>(base + off); }
 
+// 4 bf16 of row `row`, columns col .. col + 3 (col a multiple of 4) of a swizzled tile, as fp32: one 8-byte load
+__device__ __forceinline__ void ld4_bf16(const unsigned char* tile, int row, int col, float (&v)[4])
+{
+    const uint2 w = *reinterpret_cast<const uint2*>(tile + sw128(row, col));
+    v[0] = __uint_as_float(w.x << 16); v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(w.y << 16); v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+}
+
 // The fp32 records (Delta, Y, S, dS') are stored column-group major: the float4 of row `row`, columns col .. col + 3
 // (col a multiple of 4) sits at index (col / 4) * 64 + row of the chunk's record, so the 32 rows of a warp read or
 // write 512 contiguous bytes.
@@ -1947,13 +1955,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 al[4 * ti] = a4.x; al[4 * ti + 1] = a4.y; al[4 * ti + 2] = a4.z; al[4 * ti + 3] = a4.w;
 #pragma unroll
                 for (int e = 0; e < 4; e++) ai[4 * ti + e] = fast_exp2(-S.A2[nch + e] * dGa);
-                float v8[8];
-                ld_row8(sC, t, nch >> 3, v8);
+                float v4[4];
+                ld4_bf16(sC, t, nch, v4);
 #pragma unroll
-                for (int e = 0; e < 4; e++) cv[4 * ti + e] = ((nch & 4) ? v8[4 + e] : v8[e]);
-                ld_row8(sB, t, nch >> 3, v8);
+                for (int e = 0; e < 4; e++) cv[4 * ti + e] = v4[e];
+                ld4_bf16(sB, t, nch, v4);
 #pragma unroll
-                for (int e = 0; e < 4; e++) bv[4 * ti + e] = ((nch & 4) ? v8[4 + e] : v8[e]);
+                for (int e = 0; e < 4; e++) bv[4 * ti + e] = v4[e];
             }
             if (!S.unsafe) {
                 // row side: s over the block, 4 at a time; same half (s in tokens of my half) or across (my half
@@ -2039,14 +2047,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
 #pragma unroll
                             for (int e = 0; e < 4; e++) x[e] *= ku[e];
                         }
-                        float c8[8], b8[8];
-                        ld_row8(sC, s, nch >> 3, c8);
-                        ld_row8(sB, s, nch >> 3, b8);
+                        float c4[4], b4[4];
+                        ld4_bf16(sC, s, nch, c4);
+                        ld4_bf16(sB, s, nch, b4);
 #pragma unroll
                         for (int ti = 0; ti < 4; ti++)
 #pragma unroll
                             for (int e = 0; e < 4; e++) {
-                                const float xc = ((nch & 4) ? c8[4 + e] : c8[e]) * x[e], xb = ((nch & 4) ? b8[4 + e] : b8[e]) * x[e];
+                                const float xc = c4[e] * x[e], xb = b4[e] * x[e];
                                 if (xs) {
                                     cX[4 * ti + e] = fmaf(dq[si][ti], xc, fmaf(dkk[si][ti], xb, cX[4 * ti + e]));
                                 } else {
@@ -2075,9 +2083,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
 #pragma unroll 1
                 for (int sl = 0; sl < 16; sl++) {
                     const int s = 16 * nJ + sl;
-                    float c8[8], b8[8];
-                    ld_row8(sC, s, nch >> 3, c8);
-                    ld_row8(sB, s, nch >> 3, b8);
+                    float c4[4], b4[4];
+                    ld4_bf16(sC, s, nch, c4);
+                    ld4_bf16(sB, s, nch, b4);
 #pragma unroll
                     for (int ti = 0; ti < 4; ti++) {
                         const int t = nt0 + ti;
@@ -2087,11 +2095,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
 #pragma unroll
                         for (int e = 0; e < 4; e++) {
                             const float a2 = S.A2[nch + e];
-                            const float y = ((nch & 4) ? b8[4 + e] : b8[e]) * exp2f(a2 * dGr), x = exp2f(a2 * dGc);
+                            const float y = b4[e] * exp2f(a2 * dGr), x = exp2f(a2 * dGc);
                             rP[4 * ti + e] = fmaf(wq, y, rP[4 * ti + e]);
                             rK[4 * ti + e] = fmaf(wk, y, rK[4 * ti + e]);
-                            cP[4 * ti + e] = fmaf(vq, ((nch & 4) ? c8[4 + e] : c8[e]) * x, cP[4 * ti + e]);
-                            cK[4 * ti + e] = fmaf(vk, ((nch & 4) ? b8[4 + e] : b8[e]) * x, cK[4 * ti + e]);
+                            cP[4 * ti + e] = fmaf(vq, c4[e] * x, cP[4 * ti + e]);
+                            cK[4 * ti + e] = fmaf(vk, b4[e] * x, cK[4 * ti + e]);
                         }
                     }
                 }
@@ -2222,8 +2230,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
 #pragma unroll
             for (int ti = 0; ti < 4; ti++) {
                 const int t = nt0 + ti;
-                float bv8[8];
-                ld_row8(sB, t, nch >> 3, bv8);
+                float bv4[4];
+                ld4_bf16(sB, t, nch, bv4);
                 float dcv[4], dbv[4], pbv[4], gsum = 0.f;
                 // this thread's four channels of the row's arrays (float4), the segments' shares summed in I order
                 float sg[4] = {0.f, 0.f, 0.f, 0.f};
@@ -2244,7 +2252,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     const float seg = sg[e];
                     dcv[e] = dcr[e] + nc[k];
                     dbv[e] = dbr[e] + seg + nb[k];
-                    float gam = dgr[e] - ((nch & 4) ? bv8[4 + e] : bv8[e]) * seg + ng[k];
+                    float gam = dgr[e] - bv4[e] * seg + ng[k];
                     if (t == 63) {
                         const float sdi = S.sd[0][i] + S.sd[1][i] + S.sd[2][i] + S.sd[3][i];
                         gam += S.colsum[0][i] + sdi * c.KT->EC[i];
