@@ -206,13 +206,14 @@ gdn_status_t gdn_bwd(const gdn_shape_t* shape,
  * tokens `saved` receives the entering state (fp32 64 x 64, 16 KB) and the
  * results of the chunk's delta solve that the backward reuses (80 KB: the
  * decay-weighted scores P, K, the block inverse D^-1 and N, W and
- * U = Util - W S; layout private to the library).  gdn_bwd_saved then takes them instead of running
+ * U = Util - W S; in gated mode the scores P, 16 KB; layout private to the
+ * library).  gdn_bwd_saved then takes them instead of running
  * the forward sweep again.  Arguments and results are those of gdn_fwd, plus
  * `saved`: device memory of at least gdn_saved_bytes(shape) bytes, 256-byte
  * aligned, written completely by the call.  o and hT equal gdn_fwd's within
  * the bf16 tolerance (the level products form K without beta, M = beta K
- * after them, so the rounding differs).  Shapes: delta mode, bf16, d_k and
- * d_v <= 64, no option bits but GDN_CHECK_FINITE, and a forward that runs as
+ * after them, so the rounding differs).  Shapes: bf16, d_k and d_v <= 64, no
+ * option bits but GDN_CHECK_FINITE, and a forward that runs as
  * one tensor-core pass (gdn_plan(shape, 0): segments 1, GDN_KERNEL_TENSOR_CORE);
  * gdn_saved_bytes is 0 for any other shape, and both calls return
  * GDN_ERR_MODE for it.  GDN_ERR_NULL if saved is NULL, GDN_ERR_ALIGN if it is

@@ -37,6 +37,7 @@ struct TcParams {
     uint64_t wait_ns;        // limit of every bounded wait
     float* st;               // saving forward: the states entering the chunks
     unsigned char* sv;       // saving forward: the solve's results per chunk
+    uint32_t sv_stride;      // saving forward: bytes per chunk of sv
 };
 
 // Limit of a bounded wait: a chunk's loads or products take microseconds, so two

@@ -106,7 +106,7 @@ static size_t place_chunk_bwd(const gdn_shape_t& s, WsLayout& L, size_t off, boo
             off = round_up(off + nq * kSavedSolveBytes, 256);
         }
     }
-    if (!from_saved) {
+    if (!from_saved || s.mode != GDN_DELTA) {   // (the gated prep writes Delta either way)
         L.cb_dlt_off = off;
         off = round_up(off + rec, 256);
     }
@@ -254,17 +254,17 @@ static cudaError_t fwd_core(const Args& a, cudaStream_t st)
     }
 }
 
-// Shapes whose forward can keep the chunked backward's residuals: delta mode on the chunked backward, and a
-// forward that runs as one tcgen05 pass (no time split, neither the decode nor the token-serial kernel).
+// Shapes whose forward can keep the chunked backward's residuals: the chunked backward's shapes whose forward runs
+// as one tcgen05 pass (no time split, neither the decode nor the token-serial kernel).
 static bool saved_applies(const gdn_shape_t& s, int logits, int norm)
 {
-    if (s.mode != GDN_DELTA || !chunk_bwd_applies(s, logits, norm) || tsplit_factor(s, 0) != 1) return false;
+    if (!chunk_bwd_applies(s, logits, norm) || tsplit_factor(s, 0) != 1) return false;
     return fwd_kernel_of(make_args(&s)) == GDN_KERNEL_TENSOR_CORE;
 }
 
 static size_t saved_bytes_of(const gdn_shape_t& s)
 {
-    return (size_t)s.B * s.H * (size_t)((s.T + 63) / 64) * (kSavedStateBytes + kSavedSolveBytes);
+    return (size_t)s.B * s.H * (size_t)((s.T + 63) / 64) * (kSavedStateBytes + saved_solve_bytes(s.mode));
 }
 
 }  // namespace gdn

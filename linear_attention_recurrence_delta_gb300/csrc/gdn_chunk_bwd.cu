@@ -93,6 +93,7 @@ struct CbParams {
     uint64_t wait_ns;
     int starve;       // failure-path test hook: the chunk q whose loads are never issued (-1: none)
     int rev_only;     // the entering states came from the forward: the chain runs its reverse sweep only
+    uint32_t sv_stride;   // bytes per chunk of the saved front (delta: sv::BYTES; gated residuals: P only, 16 KB)
 };
 
 // ---------------------------------------------------------------- shared memory
@@ -167,6 +168,7 @@ static_assert(PB + 64 * kES * 4 <= DC && DG + 64 * kES * 4 <= BYTES, "epilogue a
 // or U = Util - W S from the saving forward.  The fp32 matrices are column-group major like the records (rec4).
 namespace sv {
 constexpr uint32_t P = 0, NA = 16384, DINV = 24576, K = 32768, NW = 49152, NWL = 57344, UT = 65536, BYTES = 81920;
+constexpr uint32_t GATED_BYTES = 16384;   // a gated saving forward keeps P only
 }  // namespace sv
 
 // fp32 sub-blocks inside MS: the diagonal 16-blocks of M, the 16-blocks below them inside each 32-block,
@@ -754,12 +756,18 @@ __device__ __forceinline__ void issue_tma(const CbParams& p, Small& S, unsigned 
     tma_load_4d(st + ST_DO, &p.tm_do, &S.full, 0, h, 64 * k, bb);
 }
 
-// the saved front of chunk q into the gradient pass's phase region (the stacked operands' halves twice)
+// the saved front of chunk q into the gradient pass's phase region (the stacked operands' halves twice; gated: P)
+template <bool DELTA>
 __device__ __forceinline__ void issue_saved(const CbParams& p, Small& S, unsigned char* sm, int q)
 {
     if (q == p.starve) return;
     unsigned char* X = sm + OFF_X;
-    const unsigned char* src = p.sv + (size_t)q * sv::BYTES;
+    const unsigned char* src = p.sv + (size_t)q * p.sv_stride;
+    if (!DELTA) {
+        mbar_arrive_expect_tx(&S.full2, 16384);
+        bulk_g2s(X + gl::P, src + sv::P, 16384, &S.full2);
+        return;
+    }
     // -W only where U is still to be formed (a saving forward's record holds U itself)
     mbar_arrive_expect_tx(&S.full2, 16384 + 4 * 8192 + (p.rev_only ? 0 : 8192));
     bulk_g2s(X + gl::P, src + sv::P, 16384, &S.full2);
@@ -919,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             front_near(c, fptr(X, pl::NEAR), true);
             bar_all();
             if (!mma_wait(c, p, 4)) break;
-            unsigned char* svq = p.sv + (size_t)q * sv::BYTES;
+            unsigned char* svq = p.sv + (size_t)q * p.sv_stride;
             if (!front_solve<true>(c, p, X + pl::NEAR, X + pl::P, X + pl::LR, X + pl::LRL, X + pl::MS, X + pl::DINV,
                                    X + pl::NA, X + pl::X0, reinterpret_cast<float*>(svq + sv::K), 0))
                 break;
@@ -1116,7 +1124,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
         tma_load_4d(sm + ps::STB, &p.tm_b, &S.full, 0, h, 64 * k, bb);
         tma_load_4d(sm + ps::STC, &p.tm_c, &S.full, 0, h, 64 * k, bb);
         tma_load_4d(sm + ps::STDO, &p.tm_do, &S.full, 0, h, 64 * k, bb);
-        const unsigned char* rq = p.sv + (size_t)q * sv::BYTES;
+        const unsigned char* rq = p.sv + (size_t)q * p.sv_stride;
         bulk_g2s(sm + ps::P, rq + sv::P, 16384, &S.full);
         bulk_g2s(sm + ps::NW, rq + sv::NW, 16384, &S.full);   // -W hi, then lo
     };
@@ -1152,7 +1160,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
             tma_prefetch_l2(&p.tm_b, 0, hn, 64 * kn, bn);
             tma_prefetch_l2(&p.tm_c, 0, hn, 64 * kn, bn);
             tma_prefetch_l2(&p.tm_do, 0, hn, 64 * kn, bn);
-            const unsigned char* rq = p.sv + (size_t)qn * sv::BYTES;
+            const unsigned char* rq = p.sv + (size_t)qn * p.sv_stride;
             prefetch_l2_bulk(rq + sv::P, 16384);
             prefetch_l2_bulk(rq + sv::NW, 16384);
         }
@@ -1304,14 +1312,16 @@ __global__ void __launch_bounds__(256) chunk_chain_gated_kernel(const __grid_con
     };
     float2 s[8];
     float4 d[4], dn[4];
-    load_in(p.h0, s);
-    rec(p.dlt, 0, d);
-    for (int k = 0; k < nk; k++) {
-        put(p.st, k, s);
-        if (k + 1 < nk) rec(p.dlt, k + 1, dn);
-        advance(k, d, s);
+    if (!p.rev_only) {   // (with a saving forward's states only the reverse sweep runs)
+        load_in(p.h0, s);
+        rec(p.dlt, 0, d);
+        for (int k = 0; k < nk; k++) {
+            put(p.st, k, s);
+            if (k + 1 < nk) rec(p.dlt, k + 1, dn);
+            advance(k, d, s);
 #pragma unroll
-        for (int e = 0; e < 4; e++) d[e] = dn[e];
+            for (int e = 0; e < 4; e++) d[e] = dn[e];
+        }
     }
     load_in(p.dhT, s);
     rec(p.ych, nk - 1, d);
@@ -1548,13 +1558,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
     uint32_t full_phase = 0, full2_phase = 0;
     int q = blockIdx.x;
     int pending = -1, pending2 = -1;   // chunks whose loads (stage, saved front) are in flight
+    // the saved front: delta always (from prep or a saving forward); gated only from a saving forward (P)
+    const bool use_sv = DELTA || p.rev_only;
     if (c.r == 0 && q < p.nq) {
         issue_tma(p, S, c.sm, q);
-        if (DELTA) issue_saved(p, S, c.sm, q);
+        if (use_sv) issue_saved<DELTA>(p, S, c.sm, q);
     }
     if (q < p.nq) {
         pending = q;
-        if (DELTA) pending2 = q;
+        if (use_sv) pending2 = q;
     }
     const int trow = c.trow, tt = trow & 63, isK = trow >> 6, wh = c.wh;
     CB_STAMP_INIT;
@@ -1568,26 +1580,26 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             prefetch_l2_bulk(p.st + (size_t)q * 4096, 16384);
             prefetch_l2_bulk(p.dst + (size_t)q * 4096, 16384);
             if (DELTA) {
-                prefetch_l2_bulk(p.sv + (size_t)q * sv::BYTES + sv::UT, 16384);
-                prefetch_l2_bulk(p.sv + (size_t)q * sv::BYTES + sv::K, 16384);
+                prefetch_l2_bulk(p.sv + (size_t)q * p.sv_stride + sv::UT, 16384);
+                prefetch_l2_bulk(p.sv + (size_t)q * p.sv_stride + sv::K, 16384);
             }
             if (q + (int)gridDim.x < p.nq) {
                 prefetch_tma(p, q + gridDim.x);
                 // the next chunk's saved front (P, -N, Dinv, -W: the bulk copies at this chunk's end)
-                if (DELTA) prefetch_l2_bulk(p.sv + (size_t)(q + gridDim.x) * sv::BYTES, sv::K);
-                if (DELTA && !p.rev_only) prefetch_l2_bulk(p.sv + (size_t)(q + gridDim.x) * sv::BYTES + sv::NW, 8192);
+                if (use_sv) prefetch_l2_bulk(p.sv + (size_t)(q + gridDim.x) * p.sv_stride, DELTA ? sv::K : 16384);
+                if (DELTA && !p.rev_only) prefetch_l2_bulk(p.sv + (size_t)(q + gridDim.x) * p.sv_stride + sv::NW, 8192);
             }
         }
         if (c.warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && c.lane == 0)
             atomicExch(p.status + 2, 2u);
-        if (DELTA && c.warp == 1 && !wait_or_abort(&S.full2, full2_phase, &S.abort, p.status, p.wait_ns) &&
+        if (use_sv && c.warp == 1 && !wait_or_abort(&S.full2, full2_phase, &S.abort, p.status, p.wait_ns) &&
             c.lane == 0)
             atomicExch(p.status + 2, 3u);
         bar_all();
         if (*(volatile uint32_t*)&S.abort) break;
         full_phase ^= 1;
         pending = -1;
-        if (DELTA) {
+        if (use_sv) {
             full2_phase ^= 1;
             pending2 = -1;
         }
@@ -1597,9 +1609,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         const int t = c.r & 63, cq = c.r >> 6;
         CB_STAMP(1, 2);
 
-        // ---- front.  Delta: P, -N, Dinv, K and -W arrived with the saved front (the prep pass computed them);
-        // gated: the level operands, the level product, the near pairs and P
-        if (!DELTA) {
+        // ---- front.  Delta: P, -N, Dinv, K and -W arrived with the saved front (the prep pass or the forward
+        // computed them); gated: P from a saving forward, else the level operands, the level product, the near
+        // pairs and P here
+        if (!DELTA && !p.rev_only) {
             front_operands(c, X + gl::A1, X + gl::B1, true);
             smem_to_tc();
             if (c.r == 0) {
@@ -1642,7 +1655,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         if (DELTA && p.rev_only) {
             // a saving forward kept U itself: straight into its hi/lo tiles
             if (!isK) {
-                const float4* urow = reinterpret_cast<const float4*>(p.sv + (size_t)q * sv::BYTES + sv::UT) + tt;
+                const float4* urow = reinterpret_cast<const float4*>(p.sv + (size_t)q * p.sv_stride + sv::UT) + tt;
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
@@ -1658,7 +1671,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         } else if (DELTA) {
             // Util (saved fp32) into TMEM as the start of U = Util - W S; -W came with the saved front
             if (!isK) {
-                const float4* urow = reinterpret_cast<const float4*>(p.sv + (size_t)q * sv::BYTES + sv::UT) + tt;
+                const float4* urow = reinterpret_cast<const float4*>(p.sv + (size_t)q * p.sv_stride + sv::UT) + tt;
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
@@ -1841,7 +1854,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         }
         // while they run: the 16-block level's operands again, as fp16 hi/lo pairs (and, delta, the anchors); they
         // depend on b, c and the decay only
-        front_operands(c, X + gl::A1H, X + gl::B1, true, X + gl::A1L, X + gl::B1L, DELTA);
+        front_operands(c, X + gl::A1H, X + gl::B1, true, X + gl::A1L, X + gl::B1L, use_sv);
         if (!mma_wait(c, p, 12)) break;
         CB_STAMP(1, 8);
         // ---- dQ (lanes 0..63) and dK = -beta (dR U^T) below the diagonal (lanes 64..127): the 16-block level's
@@ -1867,7 +1880,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 float part = 0.f;
                 const float Gt = S.G[tt];
                 // K's row tt from the saved front (L2), column-group major
-                const float4* kr = reinterpret_cast<const float4*>(p.sv + (size_t)q * sv::BYTES + sv::K) + tt;
+                const float4* kr = reinterpret_cast<const float4*>(p.sv + (size_t)q * p.sv_stride + sv::K) + tt;
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
@@ -2310,10 +2323,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         if (q + (int)gridDim.x < p.nq) {
             if (c.r == 0) {
                 issue_tma(p, S, c.sm, q + gridDim.x);
-                if (DELTA) issue_saved(p, S, c.sm, q + gridDim.x);
+                if (use_sv) issue_saved<DELTA>(p, S, c.sm, q + gridDim.x);
             }
             pending = q + gridDim.x;
-            if (DELTA) pending2 = q + gridDim.x;
+            if (use_sv) pending2 = q + gridDim.x;
         }
         CB_STAMP(1, 14);
 #ifdef GDN_CHUNK_DEBUG
@@ -2384,8 +2397,9 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv_ = a.dv;
     p.nchunks = (a.T + 63) / 64;
     p.nq = a.B * a.H * p.nchunks;
+    p.sv_stride = a.mode == GDN_DELTA ? sv::BYTES : sv::GATED_BYTES;
     if (a.saved) {
-        // residuals of a saving forward (delta): the entering states, then the solve's results
+        // residuals of a saving forward: the entering states, then the solve's results (gated: P)
         p.st = (float*)a.saved;
         p.sv = (unsigned char*)a.saved + (size_t)p.nq * 16384;
         p.rev_only = 1;
@@ -2417,7 +2431,7 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
 #define CB_MARK(what)
 #endif
     CB_MARK("start");
-    if (a.saved) chunk_prep_saved_kernel<<<p.nq < 2 * sms ? p.nq : 2 * sms, 256, ps::SMEM, st>>>(p);
+    if (a.saved && delta) chunk_prep_saved_kernel<<<p.nq < 2 * sms ? p.nq : 2 * sms, 256, ps::SMEM, st>>>(p);
     else if (delta) chunk_prep_kernel<true><<<grid, kThreads, prep_bytes, st>>>(p);
     else chunk_prep_kernel<false><<<grid, kThreads, prep_bytes, st>>>(p);
     cudaError_t e = cudaGetLastError();

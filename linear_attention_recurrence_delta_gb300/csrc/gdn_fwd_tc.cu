@@ -160,12 +160,13 @@ __device__ __forceinline__ void zero_chunk(unsigned char* tile, int row, int q)
 // tiles, the upper halves of the stacked solve operands); K (zero on and above the diagonal), fp32 64 x 64; -W as
 // hi, lo tiles ([t][i]); U = Util - W S, fp32 [t][j].  Tiles are [64][64] 16-bit with the 128-byte swizzle of the
 // MMA operands; the fp32 matrices are column-group major (row r, columns 4 g .. 4 g + 3 at float4 64 g + r), so a
-// warp's 32 rows store 512 contiguous bytes.
+// warp's 32 rows store 512 contiguous bytes.  Gated mode keeps the state and P only (a 16 KB record).
 namespace svr {
 constexpr uint32_t P = 0, NA = 16384, DINV = 24576, K = 32768, NW = 49152, NWL = 57344, U = 65536, BYTES = 81920;
+constexpr uint32_t GATED_BYTES = 16384;   // gated: P only
 __device__ __forceinline__ unsigned char* rec(const TcParams& p, int u, int k)
 {
-    return p.sv + ((size_t)u * p.nchunks + k) * BYTES;
+    return p.sv + ((size_t)u * p.nchunks + k) * p.sv_stride;
 }
 // state row `row`, columns 32 wh .. 32 wh + 31; the record is column-group major (the float4 of row r, columns
 // 4 g .. 4 g + 3 at index 64 g + r), so a warp's 32 rows write 512 contiguous bytes
@@ -192,10 +193,10 @@ __device__ __forceinline__ const float* ktab(const unsigned char* sm, int tab, i
 }
 
 // NORM: b and c arrive before their L2 normalisation (a template flag, so the plain kernel carries no trace of it).
-// SAVE (delta, one 64-column slab): the residuals of the chunked backward are written as well, per chunk q of the
-// unit: the entering state (p.st, fp32 64 x 64, column-group major) and the solve's results (p.sv, the layout of namespace svr).  The
-// b-side level operands then leave beta out, so that the level products give K itself (M = beta K is formed
-// when it is assembled).
+// SAVE (one 64-column slab): the residuals of the chunked backward are written as well, per chunk q of the unit:
+// the entering state (p.st, fp32 64 x 64, column-group major) and, in the layout of namespace svr, the delta
+// solve's results (gated: P).  In delta mode the b-side level operands then leave beta out, so that the level
+// products give K itself (M = beta K is formed when it is assembled).
 template <bool DELTA, bool NORM, bool SAVE>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcParams p)
 {
@@ -570,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (!upper) { scale8(bv, S.A2, q, GJ7 - Gt, y); st_row8_f16(X + X_B2, t, q, y); }
                         scale8(DELTA ? bbv : cv, S.A2, q, Gt, y);
 #pragma unroll
-                        for (int e = 0; e < 8; e++) keep[8 * qq + e] = (SAVE ? bet : 1.f) * y[e];
+                        for (int e = 0; e < 8; e++) keep[8 * qq + e] = (DELTA && SAVE ? bet : 1.f) * y[e];
                     }
                 }
             }
@@ -1089,12 +1090,13 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     *handled = true;
     const dim3 grid(a.B * a.H, (a.dv + 63) / 64);
     if (a.saved) {
-        // the residuals of the chunked backward: delta, one slab, no option bits, no fp32 output (the host checks)
-        if (a.mode != GDN_DELTA || a.dv > 64 || a.norm || a.logits || a.o32) return cudaErrorInvalidValue;
+        // the residuals of the chunked backward: one slab, no option bits, no fp32 output (the host checks)
+        if (a.dv > 64 || a.norm || a.logits || a.o32) return cudaErrorInvalidValue;
         const size_t nq = (size_t)a.B * a.H * p.nchunks;
         p.st = (float*)a.saved;
         p.sv = (unsigned char*)a.saved + nq * 16384;
-        return launch_t<true, false, true>(p, grid, st);
+        p.sv_stride = a.mode == GDN_DELTA ? svr::BYTES : svr::GATED_BYTES;
+        return a.mode == GDN_DELTA ? launch_t<true, false, true>(p, grid, st) : launch_t<false, false, true>(p, grid, st);
     }
     if (a.norm)
         return a.mode == GDN_DELTA ? launch_t<true, true>(p, grid, st) : launch_t<false, true>(p, grid, st);

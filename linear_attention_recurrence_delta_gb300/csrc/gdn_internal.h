@@ -84,8 +84,9 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm = 0, int logits 
 // The chunked tensor-core backward takes bf16 heads up to 64 wide without the option bits; other backward
 // calls take the token-serial one (with its time split for long sequences over few heads).
 // Residuals a saving forward keeps for it, per chunk of 64 tokens: the entering state (fp32 64 x 64) and the
-// delta solve's results (layout in gdn_chunk_bwd.cu, namespace sv).
-constexpr size_t kSavedStateBytes = 16384, kSavedSolveBytes = 81920;
+// delta solve's results (layout in gdn_chunk_bwd.cu, namespace sv), or in gated mode the scores P.
+constexpr size_t kSavedStateBytes = 16384, kSavedSolveBytes = 81920, kSavedGatedBytes = 16384;
+inline size_t saved_solve_bytes(int mode) { return mode == GDN_DELTA ? kSavedSolveBytes : kSavedGatedBytes; }
 inline bool chunk_bwd_applies(const gdn_shape_t& s, int logits, int norm)
 {
     return s.io == GDN_BF16 && s.T > 0 && s.dk <= 64 && s.dv <= 64 && !logits && !norm;

@@ -300,8 +300,9 @@ def test_plan_and_workspace_agree_on_random_shapes():
 
 
 def test_saved_residuals_sizes_and_argument_errors(lib):
-    """gdn_saved_bytes: per chunk of 64 tokens a 16 KB state and 80 KB of solve results, for delta-mode bf16 shapes
-    whose forward is one tensor-core pass and whose backward is the chunked one; 0 for every other shape.  The
+    """gdn_saved_bytes: per chunk of 64 tokens a 16 KB state and 80 KB of solve results (gated mode: the 16 KB
+    scores P), for bf16 shapes whose forward is one tensor-core pass and whose backward is the chunked one; 0 for
+    every other shape.  The
     backward from the residuals needs a smaller workspace (backward = 2).  gdn_fwd_save and gdn_bwd_saved reject
     bad arguments before any device work."""
     for B, H, T, d in ((8, 16, 4096, 64), (2, 3, 100, 56), (1, 1, 9, 8)):
@@ -309,8 +310,10 @@ def test_saved_residuals_sizes_and_argument_errors(lib):
         nq = B * H * -(-T // 64)
         assert gdn.gdn_saved_bytes(s) == nq * (16384 + 81920)
         assert 0 < gdn.gdn_workspace_bytes(s, 2) < gdn.gdn_workspace_bytes(s, 1)
-    none = [gdn.make_shape(8, 16, 4096, 64, 64, "gated", "bf16"),            # gated mode
-            gdn.make_shape(2, 2, 256, 64, 64, "delta", "f32"),               # fp32 I/O
+        sg = gdn.make_shape(B, H, T, d, d, "gated", "bf16")
+        assert gdn.gdn_saved_bytes(sg) == nq * (16384 + 16384)
+        assert 0 < gdn.gdn_workspace_bytes(sg, 2) < gdn.gdn_workspace_bytes(sg, 1)
+    none = [gdn.make_shape(2, 2, 256, 64, 64, "delta", "f32"),               # fp32 I/O
             gdn.make_shape(2, 2, 256, 128, 128, "delta", "bf16"),            # wider than 64
             gdn.make_shape(2, 2, 256, 64, 64, "delta", "bf16", gate_logits=True),
             gdn.make_shape(2, 2, 256, 64, 64, "delta", "bf16", norm_bc=True),
@@ -335,6 +338,7 @@ def test_saved_residuals_sizes_and_argument_errors(lib):
     assert fwd_save(s, saved_bytes=need - 1) == 5
     assert fwd_save(s, saved=FAKE + 16) == 3
     assert fwd_save(gdn.make_shape(2, 2, 256, 64, 64, "delta", "f32")) == 4
+    assert fwd_save(gdn.make_shape(2, 2, 256, 64, 64, "gated", "bf16")) == 4   # beta given in gated mode
     assert fwd_save(gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16")) == 4
     assert bwd_saved(s, saved=None) == 1
     assert bwd_saved(s, saved_bytes=need - 1) == 5
