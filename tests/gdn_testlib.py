@@ -68,6 +68,41 @@ def run_bwd(w, x, dhT=None, want_dh0=True):
     return {k: (None if v is None else v.double().cpu().numpy()) for k, v in out.items()}
 
 
+def run_saved(w, x, dhT):
+    """gdn_fwd_save then gdn_bwd_saved (bf16): o, h_T and the gradients as float64 arrays."""
+    s = shape_of(w)
+    B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
+    delta = w.mode == "delta"
+    t = {k: dev(x[k], "bf16") for k in ("v", "b", "c", "g", "beta", "dO")}
+    A_log, h0 = dev32(x["A_log"]), dev32(x["h0"])
+    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
+    hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
+    nbytes = gdn.gdn_saved_bytes(s)
+    assert nbytes == B * H * -(-T // 64) * (16384 + (81920 if delta else 16384))
+    saved = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN patterns: all must be written
+    ws0 = torch.empty(gdn.gdn_workspace_bytes(s, 0), dtype=torch.uint8, device="cuda")
+    gdn.check(gdn.gdn_fwd_save(s, t["v"], t["b"], t["c"], t["g"], t["beta"], A_log, h0, o, hT, saved, ws0),
+              "gdn_fwd_save")
+    gdn.check(gdn.gdn_last_device_status(ws0), "forward device status")
+    dt = torch.bfloat16
+    out = {
+        "dv": torch.empty((B, T, H, dv), dtype=dt, device="cuda"),
+        "db": torch.empty((B, T, H, dk), dtype=dt, device="cuda"),
+        "dc": torch.empty((B, T, H, dk), dtype=dt, device="cuda"),
+        "dg": torch.empty((B, T, H), dtype=dt, device="cuda"),
+        "dbeta": torch.empty((B, T, H), dtype=dt, device="cuda") if delta else None,
+        "dA_log": torch.empty((H, dk), dtype=torch.float32, device="cuda"),
+        "dh0": torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda"),
+    }
+    ws = torch.empty(gdn.gdn_workspace_bytes(s, 2), dtype=torch.uint8, device="cuda")
+    assert 0 < ws.numel() < gdn.gdn_workspace_bytes(s, 1)
+    gdn.check(gdn.gdn_bwd_saved(s, t["v"], t["b"], t["c"], t["g"], t["beta"], A_log, saved, t["dO"], dev32(dhT),
+                                *out.values(), ws), "gdn_bwd_saved")
+    gdn.check(gdn.gdn_last_device_status(ws), "backward device status")
+    got = {k: (None if v is None else v.double().cpu().numpy()) for k, v in out.items()}
+    return o.double().cpu().numpy(), hT.double().cpu().numpy(), got
+
+
 def rel_err(got, ref):
     den = np.abs(ref).max()
     num = np.abs(got - ref).max()

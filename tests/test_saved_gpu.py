@@ -1,57 +1,20 @@
 """gdn_fwd_save / gdn_bwd_saved through the C ABI: the forward keeps what the chunked backward would recompute
 (the state entering every chunk of 64 tokens and the results of the chunk's delta solve, or in gated mode the
-scores P), and the backward reads it.  Output, final state and every gradient against the fp64 oracle, on shapes with several chunks, ragged last
-chunks and the widths the tensor-core path takes, with and without h0 and dh_T, and on chunks whose decay factors
-would overflow (the exact elementwise path).  The gradients are also compared with gdn_bwd's, which recomputes
+scores P), and the backward reads it.  Output, final state and every gradient against the fp64 oracle, on shapes
+with several chunks, ragged last chunks and the widths the tensor-core path takes, with and without h0 and dh_T,
+and on chunks whose decay factors would overflow (the exact elementwise path).  The gradients are also compared with gdn_bwd's, which recomputes
 everything: the two must agree to within the bf16 tolerance of each other."""
 import math
 
-import numpy as np
 import pytest
-import torch
 
-import linear_attention_recurrence_delta_gb300 as gdn
 import oracle
 from linear_attention_recurrence_delta_gb300 import inputs as I
-from tests.gdn_testlib import TOL, assert_close, dev, dev32, run_bwd, shape_of
+from tests.gdn_testlib import TOL, assert_close, run_bwd, run_saved
 
 pytestmark = pytest.mark.gpu
 
 KEYS = ("dv", "db", "dc", "dg", "dbeta", "dA_log", "dh0")
-
-
-def run_saved(w, x, dhT):
-    s = shape_of(w)
-    B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
-    delta = w.mode == "delta"
-    t = {k: dev(x[k], "bf16") for k in ("v", "b", "c", "g", "beta", "dO")}
-    A_log, h0 = dev32(x["A_log"]), dev32(x["h0"])
-    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
-    hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
-    nbytes = gdn.gdn_saved_bytes(s)
-    assert nbytes == B * H * -(-T // 64) * (16384 + (81920 if delta else 16384))
-    saved = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN patterns: all must be written
-    ws0 = torch.empty(gdn.gdn_workspace_bytes(s, 0), dtype=torch.uint8, device="cuda")
-    gdn.check(gdn.gdn_fwd_save(s, t["v"], t["b"], t["c"], t["g"], t["beta"], A_log, h0, o, hT, saved, ws0),
-              "gdn_fwd_save")
-    gdn.check(gdn.gdn_last_device_status(ws0), "forward device status")
-    dt = torch.bfloat16
-    out = {
-        "dv": torch.empty((B, T, H, dv), dtype=dt, device="cuda"),
-        "db": torch.empty((B, T, H, dk), dtype=dt, device="cuda"),
-        "dc": torch.empty((B, T, H, dk), dtype=dt, device="cuda"),
-        "dg": torch.empty((B, T, H), dtype=dt, device="cuda"),
-        "dbeta": torch.empty((B, T, H), dtype=dt, device="cuda") if delta else None,
-        "dA_log": torch.empty((H, dk), dtype=torch.float32, device="cuda"),
-        "dh0": torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda"),
-    }
-    ws = torch.empty(gdn.gdn_workspace_bytes(s, 2), dtype=torch.uint8, device="cuda")
-    assert 0 < ws.numel() < gdn.gdn_workspace_bytes(s, 1)
-    gdn.check(gdn.gdn_bwd_saved(s, t["v"], t["b"], t["c"], t["g"], t["beta"], A_log, saved, t["dO"], dev32(dhT),
-                                *out.values(), ws), "gdn_bwd_saved")
-    gdn.check(gdn.gdn_last_device_status(ws), "backward device status")
-    got = {k: (None if v is None else v.double().cpu().numpy()) for k, v in out.items()}
-    return o.double().cpu().numpy(), hT.double().cpu().numpy(), got
 
 
 def check_saved(w, with_dhT=True):
