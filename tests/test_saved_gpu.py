@@ -59,20 +59,22 @@ def test_saved_steep_decay(mode, g_mu):
 
 @pytest.mark.parametrize("name", ["delta_bf16_8x16x4096x64", "gated_bf16_8x16x4096x56_bwd"])
 def test_saved_full_size(name):
-    """The bench's shape (8 x 16 x 4096 x 64, delta) and the gated 8 x 16 x 4096 x 56 workload: forward and
-    backward from the residuals on every unit, against gdn_fwd and gdn_bwd (which the full-size oracle tests pin)
-    within the bf16 tolerance."""
+    """The bench's training step (8 x 16 x 4096 x 64, delta) and the gated 8 x 16 x 4096 x 56 workload at full size,
+    every unit: o, h_T and every gradient from the residuals against the fp64 oracle, and the gradients against
+    gdn_bwd's, within the bf16 tolerance."""
     w = I.WORKLOADS[name].with_(backward=True)
     x = I.make_inputs(w)
     o, hT, got = run_saved(w, x, None)
-    from tests.gdn_testlib import run_fwd
-    ro, rhT = run_fwd(w, x)
     tol = TOL["bf16"]
-    assert_close(o, ro, tol, "o vs gdn_fwd")
-    assert_close(hT, rhT, tol, "hT vs gdn_fwd")
+    ro, rhT = oracle.gdn_fwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], mode=w.mode)
+    assert_close(o, ro, tol, "o vs oracle")
+    assert_close(hT, rhT, tol, "hT vs oracle")
+    ref = oracle.gdn_bwd(x["v"], x["b"], x["c"], x["g"], x["beta"], x["A_log"], x["h0"], x["dO"], None, mode=w.mode)
     plain = run_bwd(w, x, dhT=None)
     for k in KEYS:
-        if plain[k] is None:
-            assert got[k] is None
+        if ref[k] is None:
+            assert got[k] is None and plain[k] is None
             continue
-        assert_close(got[k], plain[k], tol, f"{k} vs gdn_bwd")
+        assert_close(got[k], ref[k], tol, f"{k} from residuals vs oracle")
+        assert_close(plain[k], ref[k], tol, f"{k} (gdn_bwd) vs oracle")
+        assert_close(got[k], plain[k], tol, f"{k} from residuals vs gdn_bwd")
