@@ -143,10 +143,13 @@ def bwd_slabs(w):
     return -(-w.dv // cols)
 
 
-def bwd_launches(w):
-    """Kernels one gdn_bwd call launches."""
-    if plan(w, True).bwd_kernel == 2:
-        return 4   # chunked backward: prep, chain, gradients, dA_log sum
+def bwd_launches(w, saved=False):
+    """Kernels one gdn_bwd call (gdn_bwd_saved if saved) launches."""
+    p = plan(w, True)
+    if p.bwd_kernel == 2:
+        # chunked backward: prep, chain, gradients, dA_log sum; a chain split in time runs as first walks over the
+        # segments, a scan and second walks
+        return 4 if plan(w, 2 if saved else 1).segments == 1 else 6
     if tsplit_factor(w, True) == 1:
         # backward, the slabs' partial sums of db, dc, dg (, dbeta) if several, dA_log reduction
         sums = (4 if w.mode == "delta" else 3) if bwd_slabs(w) > 1 else 0
@@ -587,7 +590,7 @@ def main():
                   "calls": "gdn_fwd_save + gdn_bwd_saved" if n_saved else "gdn_fwd + gdn_bwd",
                   "saved_bytes": n_saved,
                   "roofline": roofline_of(fb_bytes, fb_flops, fb_ms, peaks, peak_kind)}
-        gpu_launches += (fwd_launches(w) + bwd_launches(w)) * kb
+        gpu_launches += (fwd_launches(w) + bwd_launches(w, saved=bool(n_saved))) * kb
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -130,17 +130,23 @@ size_t gdn_workspace_bytes(const gdn_shape_t* shape, int backward);
 
 /* How the library runs a shape.  Host only: it touches no device and is
  * answered from the shape alone, by the rules the calls themselves follow.
- *   segments    gdn_fwd (backward = 0) or gdn_bwd (backward = 1) cuts the
- *               sequence into this many equal segments that run side by side
- *               (the state a segment passes on is an affine map of the state
- *               it receives, "GDN & MLA Mechanism Deep-Dive", Step 5: chunked
- *               recurrence; a scan over the segments joins them); 1 = no
- *               split.  Long sequences over few heads are split.
+ *   segments    gdn_fwd (backward = 0), gdn_bwd (backward = 1) or
+ *               gdn_bwd_saved (backward = 2) cuts the sequence into this many
+ *               equal segments that run side by side (the state a segment
+ *               passes on is an affine map of the state it receives, "GDN &
+ *               MLA Mechanism Deep-Dive", Step 5: chunked recurrence; a scan
+ *               over the segments joins them); 1 = no split.  Long sequences
+ *               over few heads are split.  With the chunked backward only its
+ *               chain over the chunk boundaries is, in delta mode: its sweeps
+ *               (two, or the reverse one alone from the forward's residuals)
+ *               times heads x batch rows times segments stay within 152
+ *               walks, each segment at least 16 chunks of 64 tokens (the last
+ *               one may be shorter).
  *   fwd_kernel  the kernel of the forward runs the call makes (gdn_kernel_t):
  *               gdn_fwd's own runs; gdn_bwd's forward runs over the segments
  *               under a split, GDN_KERNEL_NONE otherwise (both backward
  *               kernels recompute the forward themselves).  NONE for T = 0.
- *   bwd_kernel  (backward = 1) the backward kernel (gdn_bwd_kernel_t):
+ *   bwd_kernel  (backward = 1 or 2) the backward kernel (gdn_bwd_kernel_t):
  *               GDN_BWD_TENSOR_CORE, the chunked reverse recurrence on tcgen05
  *               (bf16, d_k and d_v <= 64, no option bits: three passes over
  *               the chunks, a chain over the chunk boundaries between them);

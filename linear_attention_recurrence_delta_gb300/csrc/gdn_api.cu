@@ -122,6 +122,13 @@ static size_t place_chunk_bwd(const gdn_shape_t& s, WsLayout& L, size_t off, boo
     off = round_up(off + nq * 64 * sizeof(float), 256);
     L.cb_da_off = off;
     off = round_up(off + nq * 64 * sizeof(float), 256);
+    int seg_len = 0;
+    const int dirs = from_saved ? 1 : 2;
+    const int nseg = chain_segments(s.mode, (long)s.B * s.H, (s.T + 63) / 64, dirs, &seg_len);
+    if (nseg > 1) {
+        L.cb_seg_off = off;
+        off = round_up(off + (size_t)dirs * s.B * s.H * nseg * 3 * 64 * 64 * sizeof(float), 256);
+    }
     return off;
 }
 
@@ -288,6 +295,9 @@ extern "C" gdn_status_t gdn_plan(const gdn_shape_t* shape_in, int backward, gdn_
     plan->fwd_kernel = (backward && P == 1) ? GDN_KERNEL_NONE : fwd_kernel_of(a);
     plan->bwd_kernel = !backward || sh.T <= 0 ? GDN_BWD_NONE
                        : chunk_bwd_applies(sh, logits, norm) ? GDN_BWD_TENSOR_CORE : GDN_BWD_SERIAL;
+    if (plan->bwd_kernel == GDN_BWD_TENSOR_CORE)   // the chunked backward's chain, split in time for few heads
+        plan->segments = chain_segments(sh.mode, (long)sh.B * sh.H, (sh.T + 63) / 64, backward == 2 ? 1 : 2,
+                                        nullptr);
     return GDN_OK;
 }
 

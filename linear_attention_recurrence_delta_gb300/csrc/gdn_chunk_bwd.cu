@@ -94,6 +94,9 @@ struct CbParams {
     int starve;       // failure-path test hook: the chunk q whose loads are never issued (-1: none)
     int rev_only;     // the entering states came from the forward: the chain runs its reverse sweep only
     uint32_t sv_stride;   // bytes per chunk of the saved front (delta: sv::BYTES; gated residuals: P only, 16 KB)
+    // delta, the chain as walks (few heads): nseg segments of seg_len chunks per unit (nseg = 1: no split)
+    int nseg, seg_len;
+    float* segrec;        // nseg > 1: per (direction, unit, segment) final X, final Pi, true start
 };
 
 // ---------------------------------------------------------------- shared memory
@@ -1543,6 +1546,286 @@ __global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_tc_kernel(const __g
     if (warp == 0) tmem_dealloc(tb, 128);
 }
 
+// ---------------------------------------------------------------- the chain as walks over segments (delta)
+// With few heads over many chunks the chain above keeps few SMs busy.  Two changes spread it out.  (1) The two
+// sweeps are independent (the reverse one reads Y and Phi only), so they run side by side: blockIdx.z = direction
+// (0 forward, 1 reverse; with the forward's states given, the reverse one alone).  (2) The chunk map is affine
+// ("GDN & MLA Mechanism Deep-Dive", Step 5: chunked recurrence), so a head's chunks are cut into nseg segments
+// [k0, k1) of seg_len chunks: a first walk (TRANS) takes each segment once from zero, carrying beside the local
+// state X the segment's transition Pi (from the identity),
+//   forward: X <- Phi_k X + Delta_k,   Pi <- Phi_k Pi      (k = k0 .. k1 - 1)
+//   reverse: X <- Phi_k^T X + Y_k,     Pi <- Phi_k^T Pi    (k = k1 - 1 .. k0)
+// and leaves X and Pi in the segment records; chunk_walk_scan_kernel joins the segments (the true state entering
+// segment s + 1 is Pi_s S_s + X_s, and the same for the adjoints backwards); a second walk (!TRANS) then takes each
+// segment from its true start and writes the per-chunk records (st forward, dst reverse) as the chain above does,
+// and in the reverse direction dh0 at the sequence's start.  The first walk skips the segment whose result nothing
+// uses (the last one forward, the first one reverse).  A TRANS step is one product for both matrices:
+//   D = Phi_hi [X_hi | Pi_hi | X_lo | Pi_lo] (N = 256),   D[:, 0:128] += Phi_lo [X_hi | Pi_hi]
+//   X' = D[:, 0:64] + D[:, 128:192] + R,   Pi' = D[:, 64:128] + D[:, 192:256]
+// and a !TRANS step is the chain's own (N = 128 then 64).  Thread roles and the copy ring are the chain's.
+__host__ __device__ constexpr uint32_t walk_tiles_bytes(bool trans) { return trans ? 32768u : 16384u; }
+constexpr uint32_t walk_smem(bool trans) { return CT_NS * CT_STAGE + walk_tiles_bytes(trans) + 128 + 1024; }
+
+// segment records of direction slot d, unit u, segment sg: [0] the final X, [1] the final Pi, [2] the true state
+// entering the segment (forward) or the true adjoint leaving it (reverse); each 64 x 64 fp32, column-group major
+__device__ __forceinline__ float* seg_rec(const CbParams& p, int d, int u, int sg, int which)
+{
+    const size_t units = (size_t)(p.nq / p.nchunks);
+    return p.segrec + ((((size_t)d * units + u) * p.nseg + sg) * 3 + which) * 4096;
+}
+
+template <bool TRANS>
+__global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_walk_kernel(const __grid_constant__ CbParams p)
+{
+    constexpr uint32_t XB = walk_tiles_bytes(TRANS);
+    constexpr uint32_t LO = XB / 2;                    // offset of the lo tiles
+    constexpr uint32_t XLO_COL = TRANS ? 128 : 64;     // TMEM column of Phi_hi X_lo
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char* Xt = sm + CT_NS * CT_STAGE;
+    uint64_t* full = reinterpret_cast<uint64_t*>(Xt + XB);
+    uint64_t* mmab = full + CT_NS;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(mmab + 1);   // [0] TMEM base, [1] abort
+    const bool rev = p.rev_only || blockIdx.z == 1;
+    const int dslot = p.rev_only ? 0 : (int)blockIdx.z;
+    const int u = blockIdx.x, sg = TRANS && rev ? (int)blockIdx.y + 1 : (int)blockIdx.y;
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const int dk = p.dk, dv = p.dv_, nk = p.nchunks;
+    const int k0 = sg * p.seg_len, k1 = min(k0 + p.seg_len, nk), ns = k1 - k0;
+    const size_t qb = (size_t)u * nk;
+    const unsigned char* phi = p.phi;
+    auto chunk_of = [&](int n) { return rev ? k1 - 1 - n : k0 + n; };
+    auto issue_copy = [&](int n) {
+        const int s = n % CT_NS;
+        mbar_arrive_expect_tx(&full[s], CT_STAGE);
+        bulk_g2s(sm + s * CT_STAGE, phi + (qb + chunk_of(n)) * CT_STAGE, CT_STAGE, &full[s]);
+    };
+    if (r == 0) {
+        for (int s = 0; s < CT_NS; s++) mbar_init(&full[s], 1);
+        mbar_init(mmab, 1);
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&misc[0], TRANS ? 256 : 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2 || warp == 3) return;
+    const uint32_t tb = misc[0];
+    int issued = ns < CT_NS ? ns : CT_NS;
+    const float* rec_in = rev ? p.ych : p.dlt;
+    float* rec_out = rev ? p.dst : p.st;
+    if (r == 0) {
+        for (int n = 0; n < issued; n++) issue_copy(n);
+        for (int n = 1; n < 3 && n < ns; n++) prefetch_l2_bulk(rec_in + (qb + chunk_of(n)) * 4096, 16384);
+    }
+    const int i = 32 * (warp & 1) + lane, j0 = 32 * (warp >> 2);
+    const uint32_t tl = tb + ((uint32_t)(32 * (warp & 1)) << 16);
+    uint32_t* abortf = &misc[1];
+
+    auto rec = [&](const float* base, size_t q, float (&v)[32]) {
+        const float4* src = rec4(base, q, i, j0);
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const float4 t = src[64 * e];
+            v[4 * e] = t.x; v[4 * e + 1] = t.y; v[4 * e + 2] = t.z; v[4 * e + 3] = t.w;
+        }
+    };
+    auto put = [&](float* base, size_t q, const float (&v)[32]) {
+        float4* dst = rec4(base, q, i, j0);
+#pragma unroll
+        for (int e = 0; e < 8; e++) dst[64 * e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+    };
+    auto tiles = [&](const float (&v)[32], uint32_t off) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            float a[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) a[e] = v[8 * q + e];
+            st_row8_split(Xt + off, Xt + off + LO, i, (j0 >> 3) + q, a);
+        }
+    };
+    float x[32], pi[TRANS ? 32 : 1], R[32], Rn[32];
+    // one step: x <- P x + R (and pi <- P pi) with P = Phi (forward) or Phi^T (reverse); false after an abort
+    auto step = [&](int n) -> bool {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(1, 128);
+        tc_fence_after();
+        const int s = n % CT_NS;
+        if (r == 0) {
+            if (wait_or_abort(&full[s], (uint32_t)(n / CT_NS) & 1u, abortf, p.status, p.wait_ns)) {
+                tc_fence_after();
+                const uint32_t a = smem_u32(sm + s * CT_STAGE), xb = smem_u32(Xt);
+                mma_tiles(tb, a, rev, 8192, 0, xb, true, 8192, 0, 4, idesc_bf16(128, TRANS ? 256 : 128, rev, true),
+                          false);
+                mma_tiles(tb, a + 8192, rev, 8192, 0, xb, true, 8192, 0, 4,
+                          idesc_bf16(128, TRANS ? 128 : 64, rev, true), true);
+                mma_commit(mmab);
+            } else {
+                atomicExch(p.status + 2, (TRANS ? 500u : 600u) + (uint32_t)n);
+            }
+        }
+        if (r == 0 && n + 3 < ns) prefetch_l2_bulk(rec_in + (qb + chunk_of(n + 3)) * 4096, 16384);
+        if (!wait_or_abort(mmab, (uint32_t)n & 1u, abortf, p.status, p.wait_ns)) return false;
+        tc_fence_after();
+        if (r == 0 && issued < ns) issue_copy(issued++);   // the stage just read is free
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            float a[16], b[16];
+            tmem_ld16(tl + j0 + 16 * h, a);                 // Phi_hi X_hi + Phi_lo X_hi
+            tmem_ld16(tl + XLO_COL + j0 + 16 * h, b);       // Phi_hi X_lo
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; e++) x[16 * h + e] = (a[e] + b[e]) + R[16 * h + e];
+            if constexpr (TRANS) {
+                tmem_ld16(tl + 64 + j0 + 16 * h, a);        // Phi_hi Pi_hi + Phi_lo Pi_hi
+                tmem_ld16(tl + 192 + j0 + 16 * h, b);       // Phi_hi Pi_lo
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; e++) pi[16 * h + e] = a[e] + b[e];
+            }
+        }
+        return true;
+    };
+
+    // the start: the sequence's own (h0 forward, dh_T reverse) at its end segment; zero elsewhere in the first
+    // walk; the scan's true start elsewhere in the second
+    const bool seq_start = rev ? sg == p.nseg - 1 : sg == 0;
+    if (seq_start || TRANS) {
+        const float* src0 = seq_start ? (rev ? p.dhT : p.h0) : nullptr;
+#pragma unroll
+        for (int e = 0; e < 32; e++) {
+            const int j = j0 + e;
+            x[e] = src0 && i < dk && j < dv ? src0[((size_t)u * dk + i) * dv + j] : 0.f;
+        }
+    } else {
+        rec(seg_rec(p, dslot, u, sg, 2), 0, x);
+    }
+    if constexpr (TRANS) {
+#pragma unroll
+        for (int e = 0; e < 32; e++) pi[e] = i == j0 + e ? 1.f : 0.f;
+    }
+    rec(rec_in, qb + chunk_of(0), R);
+    bool ok = true;
+    for (int n = 0; n < ns; n++) {
+        if constexpr (!TRANS) put(rec_out, qb + chunk_of(n), x);
+        tiles(x, 0);
+        if constexpr (TRANS) tiles(pi, 8192);
+        if (n + 1 < ns) rec(rec_in, qb + chunk_of(n + 1), Rn);
+        ok = step(n);
+        if (!ok) break;
+#pragma unroll
+        for (int e = 0; e < 32; e++) R[e] = Rn[e];
+    }
+    if (ok) {
+        if constexpr (TRANS) {
+            put(seg_rec(p, dslot, u, sg, 0), 0, x);
+            put(seg_rec(p, dslot, u, sg, 1), 0, pi);
+        } else if (rev && sg == 0 && p.dh0) {
+#pragma unroll
+            for (int e = 0; e < 32; e++) {
+                const int j = j0 + e;
+                if (i < dk && j < dv) p.dh0[((size_t)u * dk + i) * dv + j] = x[e];
+            }
+        }
+    }
+    // wind down: after an abort, let the copies still in flight land before the CTA leaves
+    if (r == 0 && *(volatile uint32_t*)abortf)
+        for (int n = issued - CT_NS < 0 ? 0 : issued - CT_NS; n < issued; n++)
+            mbar_wait(&full[n % CT_NS], (uint32_t)(n / CT_NS) & 1u, nullptr, p.wait_ns);
+    tc_fence_before();
+    named_bar_sync(1, 128);
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tb, TRANS ? 256 : 128);
+}
+
+// The scan over a unit's segments, one CTA (256 threads) per (unit, direction); fp32 on the CUDA cores, thread =
+// rows 2 (r >> 3), + 1 x columns 8 (r & 7) .. + 7.  Forward: the first segment started from h0, so its X is the true
+// state entering the second; then S_{s+1} = Pi_s S_s + X_s.  Reverse: the last segment started from dh_T, so its X
+// is the true adjoint leaving the one before; then E_{s-1} = Pi_s E_s + X_s.  Each value goes to record [2] of the
+// segment it starts; the fold past the sequence's far end is not needed.  The next fold's Pi and X are loaded while
+// the current one is computed.
+__global__ void __launch_bounds__(256) chunk_walk_scan_kernel(const __grid_constant__ CbParams p)
+{
+    __shared__ __align__(16) float Pm[64][kAS];
+    __shared__ __align__(16) float Cm[64][kAS];
+    const bool rev = p.rev_only || blockIdx.y == 1;
+    const int dslot = p.rev_only ? 0 : (int)blockIdx.y;
+    const int u = blockIdx.x, r = threadIdx.x, i0 = 2 * (r >> 3), j0 = 8 * (r & 7);
+    const int P = p.nseg;
+    auto seg_of = [&](int t) { return rev ? P - 1 - t : t; };   // the t-th segment along the walk
+    float cur[2][8];
+    auto load_own = [&](const float* src, float (&dst)[2][8]) {
+#pragma unroll
+        for (int a = 0; a < 2; a++)
+#pragma unroll
+            for (int b = 0; b < 2; b++) {
+                const float4 t = *rec4(src, 0, i0 + a, j0 + 4 * b);
+                dst[a][4 * b] = t.x; dst[a][4 * b + 1] = t.y; dst[a][4 * b + 2] = t.z; dst[a][4 * b + 3] = t.w;
+            }
+    };
+    float4 pn[4];      // the next fold's Pi: float4 e of this thread's share of the shared tile
+    float xn[2][8];    // and its X at this thread's outputs
+    auto fetch = [&](int sg) {
+        const float* pim = seg_rec(p, dslot, u, sg, 1);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const int f = r + 256 * e;
+            pn[e] = *rec4(pim, 0, f & 63, 4 * (f >> 6));
+        }
+        load_own(seg_rec(p, dslot, u, sg, 0), xn);
+    };
+    load_own(seg_rec(p, dslot, u, seg_of(0), 0), cur);
+    if (P > 2) fetch(seg_of(1));
+    for (int t = 1; t < P; t++) {
+        const int sg = seg_of(t);   // cur is this segment's true start
+        float* dst = seg_rec(p, dslot, u, sg, 2);
+#pragma unroll
+        for (int a = 0; a < 2; a++)
+#pragma unroll
+            for (int b = 0; b < 2; b++)
+                *rec4(dst, 0, i0 + a, j0 + 4 * b) = make_float4(cur[a][4 * b], cur[a][4 * b + 1], cur[a][4 * b + 2],
+                                                                cur[a][4 * b + 3]);
+        if (t == P - 1) break;
+        // cur <- Pi_sg cur + X_sg
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const int f = r + 256 * e;
+            *reinterpret_cast<float4*>(&Pm[f & 63][4 * (f >> 6)]) = pn[e];
+        }
+#pragma unroll
+        for (int a = 0; a < 2; a++) {
+            *reinterpret_cast<float4*>(&Cm[i0 + a][j0]) = make_float4(cur[a][0], cur[a][1], cur[a][2], cur[a][3]);
+            *reinterpret_cast<float4*>(&Cm[i0 + a][j0 + 4]) = make_float4(cur[a][4], cur[a][5], cur[a][6], cur[a][7]);
+        }
+        __syncthreads();
+        float nx[2][8];
+#pragma unroll
+        for (int a = 0; a < 2; a++)
+#pragma unroll
+            for (int e = 0; e < 8; e++) nx[a][e] = xn[a][e];
+        if (t + 1 < P - 1) fetch(seg_of(t + 1));
+#pragma unroll 4
+        for (int m = 0; m < 64; m++) {
+            const float p0 = Pm[i0][m], p1 = Pm[i0 + 1][m];
+            const float4 c0 = *reinterpret_cast<const float4*>(&Cm[m][j0]);
+            const float4 c1 = *reinterpret_cast<const float4*>(&Cm[m][j0 + 4]);
+            const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                nx[0][e] = fmaf(p0, cv[e], nx[0][e]);
+                nx[1][e] = fmaf(p1, cv[e], nx[1][e]);
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 2; a++)
+#pragma unroll
+            for (int e = 0; e < 8; e++) cur[a][e] = nx[a][e];
+    }
+}
+
 // ================================================================= pass 3: gradients
 template <bool DELTA>
 __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_constant__ CbParams p)
@@ -2398,6 +2681,8 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     p.nchunks = (a.T + 63) / 64;
     p.nq = a.B * a.H * p.nchunks;
     p.sv_stride = a.mode == GDN_DELTA ? sv::BYTES : sv::GATED_BYTES;
+    p.nseg = chain_segments(a.mode, a.B * a.H, p.nchunks, a.saved ? 1 : 2, &p.seg_len);
+    p.segrec = (float*)(ws + Lw.cb_seg_off);
     if (a.saved) {
         // residuals of a saving forward: the entering states, then the solve's results (gated: P)
         p.st = (float*)a.saved;
@@ -2417,6 +2702,8 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
         if ((e = set_smem(chunk_grad_kernel<false>, grad_bytes)) != cudaSuccess) return e;
         if ((e = set_smem(chunk_chain_tc_kernel, CHAIN_TC_SMEM)) != cudaSuccess) return e;
         if ((e = set_smem(chunk_prep_saved_kernel, ps::SMEM)) != cudaSuccess) return e;
+        if ((e = set_smem(chunk_chain_walk_kernel<false>, walk_smem(false))) != cudaSuccess) return e;
+        if ((e = set_smem(chunk_chain_walk_kernel<true>, walk_smem(true))) != cudaSuccess) return e;
         attr = true;
     }
     int sms = 152;
@@ -2438,8 +2725,19 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     if (e != cudaSuccess) return e;
     CB_MARK("prep");
     const int units = a.B * a.H;
-    if (delta) chunk_chain_tc_kernel<<<units, CT_THREADS, CHAIN_TC_SMEM, st>>>(p);
-    else chunk_chain_gated_kernel<<<units, 256, 0, st>>>(p);
+    const int dirs = p.rev_only ? 1 : 2;
+    if (delta && (p.nseg > 1 || dirs * units <= sms)) {
+        // the chain as walks: the two sweeps side by side; split in time, a first walk per segment and a scan
+        if (p.nseg > 1) {
+            chunk_chain_walk_kernel<true><<<dim3(units, p.nseg - 1, dirs), CT_THREADS, walk_smem(true), st>>>(p);
+            chunk_walk_scan_kernel<<<dim3(units, dirs), 256, 0, st>>>(p);
+        }
+        chunk_chain_walk_kernel<false><<<dim3(units, p.nseg, dirs), CT_THREADS, walk_smem(false), st>>>(p);
+    } else if (delta) {
+        chunk_chain_tc_kernel<<<units, CT_THREADS, CHAIN_TC_SMEM, st>>>(p);
+    } else {
+        chunk_chain_gated_kernel<<<units, 256, 0, st>>>(p);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     CB_MARK("chain");
     if (delta) chunk_grad_kernel<true><<<grid, kThreads, grad_bytes, st>>>(p);

@@ -62,6 +62,7 @@ struct WsLayout {
     size_t cb_dst_off = 0;        // the adjoint of the state leaving the chunk
     size_t cb_ec_off = 0;         // gated: the chunk's decay [B*H*chunks][64]
     size_t cb_da_off = 0;         // per-chunk dA partials [B*H*chunks][64]
+    size_t cb_seg_off = 0;        // delta, chain split in time: per (direction, unit, segment) three 64 x 64 fp32 records
     size_t total = 0;
 };
 
@@ -91,6 +92,23 @@ inline bool chunk_bwd_applies(const gdn_shape_t& s, int logits, int norm)
 {
     return s.io == GDN_BF16 && s.T > 0 && s.dk <= 64 && s.dv <= 64 && !logits && !norm;
 }
+// The chunked backward's chain split in time (delta only; gated chains are elementwise and cheap): its `dirs`
+// sweeps (2, or 1 from the forward's residuals) over `units` (batch, head) units run as dirs * units * nseg walks
+// side by side, one per SM (at most 152), each over a segment of *seg_len chunks (at least 16).  Splits when that
+// gives at least 2 segments of a sequence of at least 32 chunks.  Returns nseg (1 = no split).
+inline int chain_segments(int mode, long units, int nchunks, int dirs, int* seg_len)
+{
+    int P = 1;
+    if (mode == GDN_DELTA && units > 0 && nchunks >= 32) {
+        const long fit = kSplitSMs / (dirs * units);
+        P = fit < nchunks / 16 ? (int)fit : nchunks / 16;
+        if (P < 2) P = 1;
+    }
+    const int L = (nchunks + P - 1) / P;
+    if (seg_len) *seg_len = L;
+    return L > 0 ? (nchunks + L - 1) / L : 1;
+}
+
 // segments of the backward's time split (1 = none; never with the chunked backward)
 int bwd_split(const gdn_shape_t& s, int logits, int norm);
 WsLayout ws_layout_bwd_core(const gdn_shape_t& s, int norm = 0);   // the serial backward's own buffers only

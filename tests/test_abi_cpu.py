@@ -163,13 +163,25 @@ def test_chunked_backward_workspace():
     leaving adjoint) plus the 80 KB of the front's results that the gradient pass reuses, four fp32 records in
     gated mode, and two rows of 64 floats (decay, dA partial), after the 256-byte status word."""
     for mode, per_chunk in (("delta", 5 * 16384 + 81920), ("gated", 4 * 16384)):
-        for B, H, T, d in ((8, 16, 4096, 64), (1, 16, 32768, 64), (2, 3, 100, 56), (1, 1, 1, 8)):
+        for B, H, T, d in ((8, 16, 4096, 64), (1, 16, 32768, 64), (2, 3, 100, 56), (1, 1, 1, 8), (1, 3, 2500, 64)):
             s = gdn.make_shape(B, H, T, d, d, mode, "bf16")
-            nq = B * H * -(-T // 64)
+            nk = -(-T // 64)
+            nq = B * H * nk
+            # delta chains over few heads split in time: segments of >= 16 chunks, 2 sweeps x heads x segments
+            # <= 152; each (sweep, head, segment) then keeps three 16 KB records
+            units, nseg = B * H, 1
+            P = min(152 // (2 * units), nk // 16)
+            if mode == "delta" and nk >= 32 and P >= 2:
+                L = -(-nk // P)
+                nseg = -(-nk // L)
             want = 256 + per_chunk * nq + 2 * -(-(nq * 256) // 256) * 256
+            if nseg > 1:
+                want += 2 * units * nseg * 3 * 16384
             assert gdn.gdn_workspace_bytes(s, 1) == want, (mode, B, H, T, d)
             p = gdn.gdn_plan(s, 1)
-            assert (p.segments, p.fwd_kernel, p.bwd_kernel) == (1, gdn.GDN_KERNEL_NONE, gdn.GDN_BWD_TENSOR_CORE)
+            assert (p.segments, p.fwd_kernel, p.bwd_kernel) == (nseg, gdn.GDN_KERNEL_NONE, gdn.GDN_BWD_TENSOR_CORE)
+            if (mode, B, H, T) == ("delta", 1, 16, 32768):
+                assert nseg == 4
 
 
 def test_gate_logits_option_bit():
@@ -216,7 +228,8 @@ def test_check_finite_option_bit():
 
 def test_plan_reports_split_and_kernel():
     """gdn_plan answers from the shape alone, by the rules the calls dispatch with: the time split for long
-    sequences over few heads (forward at least 4 segments in delta mode, 3 in gated mode, backward at least 2),
+    sequences over few heads (forward at least 4 segments in delta mode, 3 in gated mode, token-serial backward at
+    least 2, the chunked backward's chain in delta mode segments of at least 16 chunks),
     the decode kernel up to 8 tokens, the tensor-core forward for bf16 keys up to 64 wide except delta heads up to
     32 wide over more than 304 units, the token-serial forward otherwise."""
     K = gdn
@@ -226,7 +239,12 @@ def test_plan_reports_split_and_kernel():
         return p.segments, p.fwd_kernel
 
     assert plan(1, 16, 32768, 64, 64, "delta", "bf16") == (8, K.GDN_KERNEL_TENSOR_CORE)
-    assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=1) == (1, K.GDN_KERNEL_NONE)   # chunked backward
+    # chunked backward: its chain over the 512 chunk boundaries split into 4 segments of 128 chunks (2 sweeps x 16
+    # heads x 4 <= 152), from the forward's residuals (the reverse sweep alone) into 9 of 57 (16 x 9 <= 152)
+    assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=1) == (4, K.GDN_KERNEL_NONE)
+    assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=2) == (9, K.GDN_KERNEL_NONE)
+    assert plan(1, 16, 32768, 64, 64, "gated", "bf16", bw=1) == (1, K.GDN_KERNEL_NONE)   # gated chain: not split
+    assert plan(1, 16, 1024, 64, 64, "delta", "bf16", bw=1) == (1, K.GDN_KERNEL_NONE)    # 16 chunks: too short
     assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=1, gate_logits=True) == (8, K.GDN_KERNEL_TENSOR_CORE)
     assert plan(8, 16, 4096, 64, 64, "delta", "bf16") == (1, K.GDN_KERNEL_TENSOR_CORE)
     assert plan(8, 16, 4096, 64, 64, "delta", "bf16", bw=1) == (1, K.GDN_KERNEL_NONE)
@@ -256,7 +274,8 @@ def test_plan_reports_split_and_kernel():
 def test_plan_and_workspace_agree_on_random_shapes():
     """Over random shapes, valid or not: gdn_plan succeeds exactly when both workspace sizes are non-zero; a split
     has T divisible by its segments, at least 512 tokens per segment, heads at most 64 wide and at most 152
-    (batch, head, segment) units (forward: at least 4 segments in delta mode, 3 in gated mode); a forward splits
+    (batch, head, segment) units (forward: at least 4 segments in delta mode, 3 in gated mode; the chunked
+    backward's chain: delta mode, segments of at least 16 chunks); a forward splits
     exactly when its workspace holds more than the status word; the forward kernel is NONE only without tokens."""
     rng = np.random.default_rng(7)
     for _ in range(3000):
@@ -277,17 +296,25 @@ def test_plan_and_workspace_agree_on_random_shapes():
                 continue
             assert w0 > 0 and w1 > 0
             P = p.segments
-            assert P >= 1 and (T % P == 0 if T else P == 1)
-            if P > 1:
-                assert T // P >= 512 and dk <= 64 and dv <= 64 and B * H * P <= 152
-                if not bw:
-                    assert P >= (4 if mode == "delta" else 3)
             chunked = io == "bf16" and dk <= 64 and dv <= 64 and T > 0
+            assert P >= 1
+            if bw and chunked:
+                # the chunked backward splits only its chain, in delta mode, into segments of >= 16 whole chunks
+                # (the last one may be shorter), at most 152 (sweep, unit, segment) walks
+                nk = -(-T // 64)
+                assert P == 1 or (mode == "delta" and 2 * B * H * P <= 152 and -(-nk // P) >= 16
+                                  and (P - 1) * -(-nk // P) < nk), (B, H, T, P)
+            else:
+                assert T % P == 0 if T else P == 1
+                if P > 1:
+                    assert T // P >= 512 and dk <= 64 and dv <= 64 and B * H * P <= 152
+                    if not bw:
+                        assert P >= (4 if mode == "delta" else 3)
             if bw:
                 want = gdn.GDN_BWD_NONE if T == 0 else (gdn.GDN_BWD_TENSOR_CORE if chunked else gdn.GDN_BWD_SERIAL)
                 assert p.bwd_kernel == want
                 if chunked:
-                    assert P == 1 and p.fwd_kernel == gdn.GDN_KERNEL_NONE
+                    assert p.fwd_kernel == gdn.GDN_KERNEL_NONE
             else:
                 assert p.bwd_kernel == gdn.GDN_BWD_NONE
             if not bw:
