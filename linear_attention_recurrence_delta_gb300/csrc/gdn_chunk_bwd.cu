@@ -1562,7 +1562,8 @@ __global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_tc_kernel(const __g
 // uses (the last one forward, the first one reverse).  A TRANS step is one product for both matrices:
 //   D = Phi_hi [X_hi | Pi_hi | X_lo | Pi_lo] (N = 256),   D[:, 0:128] += Phi_lo [X_hi | Pi_hi]
 //   X' = D[:, 0:64] + D[:, 128:192] + R,   Pi' = D[:, 64:128] + D[:, 192:256]
-// and a !TRANS step is the chain's own (N = 128 then 64).  Thread roles and the copy ring are the chain's.
+// and a !TRANS step is the chain's own (N = 128 then 64).  Thread roles and the copy ring are the chain's.  Two
+// !TRANS walks fit an SM (83 KB of shared memory, 128 TMEM columns, at most 168 registers a thread).
 __host__ __device__ constexpr uint32_t walk_tiles_bytes(bool trans) { return trans ? 32768u : 16384u; }
 constexpr uint32_t walk_smem(bool trans) { return CT_NS * CT_STAGE + walk_tiles_bytes(trans) + 128 + 1024; }
 
@@ -1575,7 +1576,7 @@ __device__ __forceinline__ float* seg_rec(const CbParams& p, int d, int u, int s
 }
 
 template <bool TRANS>
-__global__ void __launch_bounds__(CT_THREADS, 1) chunk_chain_walk_kernel(const __grid_constant__ CbParams p)
+__global__ void __launch_bounds__(CT_THREADS, TRANS ? 1 : 2) chunk_chain_walk_kernel(const __grid_constant__ CbParams p)
 {
     constexpr uint32_t XB = walk_tiles_bytes(TRANS);
     constexpr uint32_t LO = XB / 2;                    // offset of the lo tiles
@@ -1911,7 +1912,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         }
         CB_STAMP(1, 4);
 
-        // ---- S, dS' of the chunk (fp32 from the chain) -> hi/lo tiles [i][j]; sum_j dS'[i][j] S[i][j]
+        // ---- S, dS' of the chunk (fp32 from the chain) -> hi/lo tiles [i][j]; sum_j dS'[i][j] S[i][j].  (Delta from
+        // residuals: U, kept by the saving forward, is loaded here too, so that the loads share one wait.)
+        float4 ures[8];
+        if (DELTA && p.rev_only && !isK) {
+            const float4* urow = reinterpret_cast<const float4*>(p.sv + (size_t)q * p.sv_stride + sv::UT) + tt;
+#pragma unroll
+            for (int e = 0; e < 8; e++) ures[e] = urow[(4 * (2 * wh + (e >> 2)) + (e & 3)) * 64];
+        }
         {
             float sv[16], dv16[16];
 #pragma unroll
@@ -1938,17 +1946,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         if (DELTA && p.rev_only) {
             // a saving forward kept U itself: straight into its hi/lo tiles
             if (!isK) {
-                const float4* urow = reinterpret_cast<const float4*>(p.sv + (size_t)q * p.sv_stride + sv::UT) + tt;
-#pragma unroll 1
+#pragma unroll
                 for (int h2 = 0; h2 < 2; h2++) {
-                    const int cg = 2 * wh + h2;
                     float v[16];
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
-                        const float4 x = urow[(4 * cg + e) * 64];
+                        const float4 x = ures[4 * h2 + e];
                         v[4 * e] = x.x; v[4 * e + 1] = x.y; v[4 * e + 2] = x.z; v[4 * e + 3] = x.w;
                     }
-                    st16_split(X + gl::U, X + gl::U + 16384, tt, cg, v);
+                    st16_split(X + gl::U, X + gl::U + 16384, tt, 2 * wh + h2, v);
                 }
             }
         } else if (DELTA) {
@@ -2162,15 +2168,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 // dbeta_t = sum_j dR V - sum_i Btil (dR S^T) - sum_{s<t} (dR U^T) K   (dMm = -dR U^T)
                 float part = 0.f;
                 const float Gt = S.G[tt];
-                // K's row tt from the saved front (L2), column-group major
-                const float4* kr = reinterpret_cast<const float4*>(p.sv + (size_t)q * p.sv_stride + sv::K) + tt;
+                // K's row tt from the saved front (L2), column-group major: both halves' loads under one wait
+                float4 krow[8];
+                {
+                    const float4* kr = reinterpret_cast<const float4*>(p.sv + (size_t)q * p.sv_stride + sv::K) + tt;
+#pragma unroll
+                    for (int e = 0; e < 8; e++) krow[e] = kr[(4 * (2 * wh + (e >> 2)) + (e & 3)) * 64];
+                }
 #pragma unroll 1
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2;
                     float drs[16], dru[16], bv[16], kv[16];
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
-                        const float4 x = kr[(4 * cg + e) * 64];
+                        const float4 x = h2 ? krow[4 + e] : krow[e];
                         kv[4 * e] = x.x; kv[4 * e + 1] = x.y; kv[4 * e + 2] = x.z; kv[4 * e + 3] = x.w;
                     }
                     tmem_ld16(c.tl + 64 + 16 * cg, drs);
@@ -2726,7 +2737,7 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     CB_MARK("prep");
     const int units = a.B * a.H;
     const int dirs = p.rev_only ? 1 : 2;
-    if (delta && (p.nseg > 1 || dirs * units <= sms)) {
+    if (delta && (p.nseg > 1 || dirs * units <= 2 * sms)) {
         // the chain as walks: the two sweeps side by side; split in time, a first walk per segment and a scan
         if (p.nseg > 1) {
             chunk_chain_walk_kernel<true><<<dim3(units, p.nseg - 1, dirs), CT_THREADS, walk_smem(true), st>>>(p);
