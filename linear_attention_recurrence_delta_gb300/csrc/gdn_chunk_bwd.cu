@@ -1081,15 +1081,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
 // With P and W of every chunk kept by the forward, the chain's inputs take three products per chunk:
 //   Phi - diag(E) = Bhat^T (-W),   Qc - Ctil = P (-W),   Y = Qc^T dO,
 // on hi/lo operands (hi*hi + hi*lo + lo*hi; dO exact).  Bhat and Ctil come from b, c and the chunk's decay (every
-// factor <= 1).  About 100 KB of shared memory and 256 TMEM columns, so two CTAs share an SM.
+// factor <= 1).  74 KB of shared memory and 128 TMEM columns, so three CTAs share an SM.  The products have M = 128;
+// the rows past 64 of an A operand read the next 8 KB (the lo tile, or the region after it), which hold other data
+// and give TMEM rows that nobody reads.  Qc takes P's place once the first products are done, and Y takes their
+// TMEM columns once Phi and Qc have been read out.
 namespace ps {
 constexpr uint32_t STB = 0, STC = 8192, STDO = 16384;   // b, c, dO tiles (TMA)
-constexpr uint32_t P = 24576;                            // P hi, lo (residuals)
-constexpr uint32_t NW = 40960;                           // -W hi, lo (residuals)
-constexpr uint32_t BH = 57344;                           // Bhat hi, lo, natural [t][i]
-constexpr uint32_t QC = 73728;                           // Qc hi, lo, natural [t][i]
-constexpr uint32_t SMALL = 98304;                        // after 8 KB that the unused M rows of Qc lo's reads see
+constexpr uint32_t BH = 24576;                           // Bhat hi, lo, natural [t][i]
+constexpr uint32_t P = 40960;                            // P hi, lo (residuals)
+constexpr uint32_t NW = 57344;                           // -W hi, lo (residuals)
+constexpr uint32_t QC = P;                               // Qc hi, lo, natural [t][i] (after the first products)
+constexpr uint32_t SMALL = 73728;
 constexpr uint32_t SMEM = SMALL + 1024 + 1024;
+constexpr uint32_t TM_COLS = 128;
+static_assert(BH + 24576 <= SMALL && QC + 24576 <= SMALL && P + 24576 <= SMALL, "M = 128 reads stay inside");
 }  // namespace ps
 
 struct PsSmall {
@@ -1101,7 +1106,7 @@ struct PsSmall {
 };
 static_assert(sizeof(PsSmall) <= 1024, "small block");
 
-__global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_constant__ CbParams p)
+__global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_constant__ CbParams p)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -1114,7 +1119,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_b); tma_prefetch_desc(&p.tm_c); tma_prefetch_desc(&p.tm_do);
     }
-    if (warp == 0) tmem_alloc(&S.tmem_base, 256);
+    if (warp == 0) tmem_alloc(&S.tmem_base, ps::TM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1234,11 +1239,11 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
         }
         sync_all();
         if (r == 0) {
-            // Y = Qc^T dO: columns 128..191, rows i
+            // Y = Qc^T dO: columns 0..63 (Phi's, read out), rows i
             const uint32_t qc = smem_u32(sm + ps::QC), dO = smem_u32(sm + ps::STDO);
             const uint32_t id = idesc_bf16(128, 64, true, true);
-            mma_tiles(tb + 128, qc, true, 8192, 0, dO, true, 8192, 0, 4, id, false);
-            mma_tiles(tb + 128, qc + 8192, true, 8192, 0, dO, true, 8192, 0, 4, id, true);
+            mma_tiles(tb, qc, true, 8192, 0, dO, true, 8192, 0, 4, id, false);
+            mma_tiles(tb, qc + 8192, true, 8192, 0, dO, true, 8192, 0, 4, id, true);
             mma_commit(&S.mma);
         }
         if (!wait_mma(1)) break;
@@ -1247,7 +1252,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
             for (int h2 = 0; h2 < 2; h2++) {
                 const int c0 = 32 * wh + 16 * h2;
                 float v[16];
-                tmem_ld16(tl + 128 + c0, v);
+                tmem_ld16(tl + c0, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; e += 4)
@@ -1269,7 +1274,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_saved_kernel(const __grid_c
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tb, 256);
+    if (warp == 0) tmem_dealloc(tb, ps::TM_COLS);
 }
 
 // ================================================================= pass 2: chain
@@ -2630,25 +2635,32 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
     teardown(c, p, pending, full_phase, pending2, full2_phase);
 }
 
-// dA_log[h][i] = A[h][i] sum over batch rows and chunks of the chunk partials, in a fixed order: 256 threads per
-// head, thread (lane group g = threadIdx.x >> 6, channel i) sums the (batch, chunk) pairs n with n mod 4 = g in
-// order, then the four group sums are added in group order
-__global__ void __launch_bounds__(256) chunk_dalog_kernel(const float* __restrict__ part, const float* __restrict__ A_log,
-                                                          float* __restrict__ dA_log, int B, int H, int dk, int nchunks)
+// dA_log[h][i] = A[h][i] sum over batch rows and chunks of the chunk partials, in a fixed order: 1024 threads per
+// head, thread (lane group g = threadIdx.x >> 6, channel i) sums the (batch, chunk) pairs n with n mod 16 = g in
+// order, then the sixteen group sums are added in group order
+constexpr int kDalogGroups = 16;
+__global__ void __launch_bounds__(64 * kDalogGroups) chunk_dalog_kernel(const float* __restrict__ part,
+                                                                        const float* __restrict__ A_log,
+                                                                        float* __restrict__ dA_log, int B, int H,
+                                                                        int dk, int nchunks)
 {
-    __shared__ float grp[4][64];
+    __shared__ float grp[kDalogGroups][64];
     const int h = blockIdx.x, i = threadIdx.x & 63, g = threadIdx.x >> 6;
     const int n_all = B * nchunks;
     float acc = 0.f;
-#pragma unroll 8
-    for (int n = g; n < n_all; n += 4) {
+#pragma unroll 4
+    for (int n = g; n < n_all; n += kDalogGroups) {
         const int bb = n / nchunks, k = n - bb * nchunks;
         acc += part[(((size_t)bb * H + h) * nchunks + k) * 64 + i];
     }
     grp[g][i] = acc;
     __syncthreads();
-    if (g == 0 && i < dk)
-        dA_log[h * dk + i] = -expf(A_log[h * dk + i]) * (((grp[0][i] + grp[1][i]) + grp[2][i]) + grp[3][i]);
+    if (g == 0 && i < dk) {
+        float sum = grp[0][i];
+#pragma unroll
+        for (int e = 1; e < kDalogGroups; e++) sum += grp[e][i];
+        dA_log[h * dk + i] = -expf(A_log[h * dk + i]) * sum;
+    }
 }
 
 template <typename K>
@@ -2729,7 +2741,7 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
 #define CB_MARK(what)
 #endif
     CB_MARK("start");
-    if (a.saved && delta) chunk_prep_saved_kernel<<<p.nq < 2 * sms ? p.nq : 2 * sms, 256, ps::SMEM, st>>>(p);
+    if (a.saved && delta) chunk_prep_saved_kernel<<<p.nq < 3 * sms ? p.nq : 3 * sms, 256, ps::SMEM, st>>>(p);
     else if (delta) chunk_prep_kernel<true><<<grid, kThreads, prep_bytes, st>>>(p);
     else chunk_prep_kernel<false><<<grid, kThreads, prep_bytes, st>>>(p);
     cudaError_t e = cudaGetLastError();
@@ -2755,7 +2767,7 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     else chunk_grad_kernel<false><<<grid, kThreads, grad_bytes, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     CB_MARK("grad");
-    chunk_dalog_kernel<<<a.H, 256, 0, st>>>(p.dA_part, a.A_log, a.dA_log, a.B, a.H, a.dk, p.nchunks);
+    chunk_dalog_kernel<<<a.H, 64 * kDalogGroups, 0, st>>>(p.dA_part, a.A_log, a.dA_log, a.B, a.H, a.dk, p.nchunks);
     return cudaGetLastError();
 }
 
