@@ -79,6 +79,25 @@ static size_t place_tsplit(const gdn_shape_t& s, int P, bool backward, WsLayout&
     return off;
 }
 
+// buffers of the delta forward split in time by walks (see launch_fwd_walks), placed from `off`
+static size_t place_fwd_walks(const gdn_shape_t& s, int P, WsLayout& L, size_t off)
+{
+    const size_t units = (size_t)s.B * s.H, nq = units * (size_t)(s.T / 64);
+    L.ts_h_off = off;
+    off = round_up(off + units * P * s.dk * s.dv * sizeof(float), 256);
+    L.ts_o_off = off;
+    off = round_up(off + (size_t)s.B * s.T * s.H * s.dv * sizeof(float), 256);
+    L.fw_res_off = off;
+    off = round_up(off + nq * (kSavedStateBytes + kSavedSolveBytes), 256);
+    L.cb_phi_off = off;
+    off = round_up(off + nq * 16384, 256);
+    L.fw_d_off = off;
+    off = round_up(off + nq * 16384, 256);
+    L.cb_seg_off = off;
+    off = round_up(off + units * P * 3 * 16384, 256);
+    return off;
+}
+
 WsLayout ws_layout_bwd_core(const gdn_shape_t& s, int norm)
 {
     WsLayout L;
@@ -149,7 +168,10 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm, int logits)
         }
         off = place_bwd_core(core, L, off, norm);
     }
-    if (P > 1) off = place_tsplit(s, P, backward != 0, L, off);
+    if (P > 1 && !backward && fwd_walks_apply(s, P, logits, norm))
+        off = place_fwd_walks(s, P, L, off);
+    else if (P > 1)
+        off = place_tsplit(s, P, backward != 0, L, off);
     L.total = off;
     return L;
 }
@@ -263,9 +285,12 @@ static cudaError_t fwd_core(const Args& a, cudaStream_t st)
 
 // Shapes whose forward can keep the chunked backward's residuals: the chunked backward's shapes whose forward runs
 // as one tcgen05 pass (no time split, neither the decode nor the token-serial kernel).
+// gdn_fwd_save applies: the chunked backward's shapes whose forward is one tcgen05 pass, or a split by walks
 static bool saved_applies(const gdn_shape_t& s, int logits, int norm)
 {
-    if (!chunk_bwd_applies(s, logits, norm) || tsplit_factor(s, 0) != 1) return false;
+    if (!chunk_bwd_applies(s, logits, norm)) return false;
+    const int P = tsplit_factor(s, 0);
+    if (P > 1) return fwd_walks_apply(s, P, logits, norm);
     return fwd_kernel_of(make_args(&s)) == GDN_KERNEL_TENSOR_CORE;
 }
 
@@ -362,7 +387,13 @@ static gdn_status_t fwd_impl(const gdn_shape_t* shape_in, const void* v, const v
         return GDN_OK;
     }
     const int P = tsplit_factor(*shape, 0);
-    cudaError_t e = P > 1 ? launch_fwd_tsplit(a, ws_layout(*shape, 0, norm), P, st, fwd_core) : fwd_core(a, st);
+    cudaError_t e;
+    if (P > 1 && fwd_walks_apply(*shape, P, logits, norm))
+        e = launch_fwd_walks(a, ws_layout(*shape, 0, norm, logits), P, st);
+    else if (P > 1)
+        e = launch_fwd_tsplit(a, ws_layout(*shape, 0, norm, logits), P, st, fwd_core);
+    else
+        e = fwd_core(a, st);
     if (e == cudaSuccess && check) {
         e = launch_check_finite(o, (size_t)a.B * a.T * a.H * a.dv, a.io, ws, st);
         if (e == cudaSuccess && hT) e = launch_check_finite(hT, state_bytes / sizeof(float), GDN_F32, ws, st);

@@ -97,6 +97,12 @@ struct CbParams {
     // delta, the chain as walks (few heads): nseg segments of seg_len chunks per unit (nseg = 1: no split)
     int nseg, seg_len;
     float* segrec;        // nseg > 1: per (direction, unit, segment) final X, final Pi, true start
+    // the forward split in time by walks (delta): prep builds Phi only, the walks carry no records R, the second
+    // walk starts every segment from its record [2] and writes D = T_k S_s to st; then the fix-up pass
+    int fwd_walks;
+    const float* fw_o32;  // the zero-start run's outputs, fp32 [B, T, H, d_v]
+    __nv_bfloat16* fw_o;  // the outputs
+    float* fw_st;         // saving: the residual states, made true by adding D (null: not saving)
 };
 
 // ---------------------------------------------------------------- shared memory
@@ -1128,12 +1134,12 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
     auto issue = [&](int q) {
         if (q == p.starve) return;   // failure-path test hook
         const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
-        mbar_arrive_expect_tx(&S.full, 3 * 8192 + 32768);
+        mbar_arrive_expect_tx(&S.full, p.fwd_walks ? 2 * 8192 + 16384 : 3 * 8192 + 32768);
         tma_load_4d(sm + ps::STB, &p.tm_b, &S.full, 0, h, 64 * k, bb);
         tma_load_4d(sm + ps::STC, &p.tm_c, &S.full, 0, h, 64 * k, bb);
-        tma_load_4d(sm + ps::STDO, &p.tm_do, &S.full, 0, h, 64 * k, bb);
+        if (!p.fwd_walks) tma_load_4d(sm + ps::STDO, &p.tm_do, &S.full, 0, h, 64 * k, bb);
         const unsigned char* rq = p.sv + (size_t)q * p.sv_stride;
-        bulk_g2s(sm + ps::P, rq + sv::P, 16384, &S.full);
+        if (!p.fwd_walks) bulk_g2s(sm + ps::P, rq + sv::P, 16384, &S.full);   // (Phi alone needs no P)
         bulk_g2s(sm + ps::NW, rq + sv::NW, 16384, &S.full);   // -W hi, then lo
     };
     auto sync_all = [&]() {
@@ -1167,9 +1173,9 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
                       hn = un - bn * p.H;
             tma_prefetch_l2(&p.tm_b, 0, hn, 64 * kn, bn);
             tma_prefetch_l2(&p.tm_c, 0, hn, 64 * kn, bn);
-            tma_prefetch_l2(&p.tm_do, 0, hn, 64 * kn, bn);
+            if (!p.fwd_walks) tma_prefetch_l2(&p.tm_do, 0, hn, 64 * kn, bn);
             const unsigned char* rq = p.sv + (size_t)qn * p.sv_stride;
-            prefetch_l2_bulk(rq + sv::P, 16384);
+            if (!p.fwd_walks) prefetch_l2_bulk(rq + sv::P, 16384);
             prefetch_l2_bulk(rq + sv::NW, 16384);
         }
         if (warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
@@ -1209,10 +1215,12 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             mma_tiles(tb, bh, true, 8192, 0, nw, true, 8192, 0, 4, idA, false);
             mma_tiles(tb, bh, true, 8192, 0, nw + 8192, true, 8192, 0, 4, idA, true);
             mma_tiles(tb, bh + 8192, true, 8192, 0, nw, true, 8192, 0, 4, idA, true);
-            // P (-W): columns 64..127, rows t
-            mma_tiles(tb + 64, pp, false, 0, 0, nw, true, 8192, 0, 4, idB, false);
-            mma_tiles(tb + 64, pp, false, 0, 0, nw + 8192, true, 8192, 0, 4, idB, true);
-            mma_tiles(tb + 64, pp + 8192, false, 0, 0, nw, true, 8192, 0, 4, idB, true);
+            if (!p.fwd_walks) {
+                // P (-W): columns 64..127, rows t
+                mma_tiles(tb + 64, pp, false, 0, 0, nw, true, 8192, 0, 4, idB, false);
+                mma_tiles(tb + 64, pp, false, 0, 0, nw + 8192, true, 8192, 0, 4, idB, true);
+                mma_tiles(tb + 64, pp + 8192, false, 0, 0, nw, true, 8192, 0, 4, idB, true);
+            }
             mma_commit(&S.mma);
         }
         if (!wait_mma(0)) break;
@@ -1226,37 +1234,41 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
                 const int cg = 2 * wh + h2;
                 float a[16], b[16], cv[16];
                 tmem_ld16(tl + 16 * cg, a);
-                tmem_ld16(tl + 64 + 16 * cg, b);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; e++) a[e] += (16 * cg + e == i) ? ec : 0.f;
                 st16_split(phq, phq + 8192, i, cg, a);
+                if (p.fwd_walks) continue;   // the forward's walks need Phi only
+                tmem_ld16(tl + 64 + 16 * cg, b);
+                tmem_wait_ld();
                 ld16_bf16(sm + ps::STC, i, cg, cv);
 #pragma unroll
                 for (int e = 0; e < 16; e++) b[e] += cv[e] * fast_exp2(S.A2[16 * cg + e] * Gt);
                 st16_split(sm + ps::QC, sm + ps::QC + 8192, i, cg, b);
             }
         }
-        sync_all();
-        if (r == 0) {
-            // Y = Qc^T dO: columns 0..63 (Phi's, read out), rows i
-            const uint32_t qc = smem_u32(sm + ps::QC), dO = smem_u32(sm + ps::STDO);
-            const uint32_t id = idesc_bf16(128, 64, true, true);
-            mma_tiles(tb, qc, true, 8192, 0, dO, true, 8192, 0, 4, id, false);
-            mma_tiles(tb, qc + 8192, true, 8192, 0, dO, true, 8192, 0, 4, id, true);
-            mma_commit(&S.mma);
-        }
-        if (!wait_mma(1)) break;
-        if (q4 < 2) {
+        if (!p.fwd_walks) {   // Y = Qc^T dO
+            sync_all();
+            if (r == 0) {
+                // Y = Qc^T dO: columns 0..63 (Phi's, read out), rows i
+                const uint32_t qc = smem_u32(sm + ps::QC), dO = smem_u32(sm + ps::STDO);
+                const uint32_t id = idesc_bf16(128, 64, true, true);
+                mma_tiles(tb, qc, true, 8192, 0, dO, true, 8192, 0, 4, id, false);
+                mma_tiles(tb, qc + 8192, true, 8192, 0, dO, true, 8192, 0, 4, id, true);
+                mma_commit(&S.mma);
+            }
+            if (!wait_mma(1)) break;
+            if (q4 < 2) {
 #pragma unroll 1
-            for (int h2 = 0; h2 < 2; h2++) {
-                const int c0 = 32 * wh + 16 * h2;
-                float v[16];
-                tmem_ld16(tl + c0, v);
-                tmem_wait_ld();
+                for (int h2 = 0; h2 < 2; h2++) {
+                    const int c0 = 32 * wh + 16 * h2;
+                    float v[16];
+                    tmem_ld16(tl + c0, v);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; e += 4)
-                    *rec4(p.ych, q, trow, c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                    for (int e = 0; e < 16; e += 4)
+                        *rec4(p.ych, q, trow, c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                }
             }
         }
         // the tiles are free: the next chunk's loads
@@ -1619,17 +1631,24 @@ __global__ void __launch_bounds__(CT_THREADS, TRANS ? 1 : 2) chunk_chain_walk_ke
     if (warp == 2 || warp == 3) return;
     const uint32_t tb = misc[0];
     int issued = ns < CT_NS ? ns : CT_NS;
-    const float* rec_in = rev ? p.ych : p.dlt;
+    // the records R (none in the forward's walks, whose maps are linear) and the per-chunk records written
+    const float* rec_in = p.fwd_walks ? nullptr : (rev ? p.ych : p.dlt);
     float* rec_out = rev ? p.dst : p.st;
     if (r == 0) {
         for (int n = 0; n < issued; n++) issue_copy(n);
-        for (int n = 1; n < 3 && n < ns; n++) prefetch_l2_bulk(rec_in + (qb + chunk_of(n)) * 4096, 16384);
+        for (int n = 1; n < 3 && n < ns && rec_in; n++)
+            prefetch_l2_bulk(rec_in + (qb + chunk_of(n)) * 4096, 16384);
     }
     const int i = 32 * (warp & 1) + lane, j0 = 32 * (warp >> 2);
     const uint32_t tl = tb + ((uint32_t)(32 * (warp & 1)) << 16);
     uint32_t* abortf = &misc[1];
 
     auto rec = [&](const float* base, size_t q, float (&v)[32]) {
+        if (!base) {
+#pragma unroll
+            for (int e = 0; e < 32; e++) v[e] = 0.f;
+            return;
+        }
         const float4* src = rec4(base, q, i, j0);
 #pragma unroll
         for (int e = 0; e < 8; e++) {
@@ -1672,7 +1691,7 @@ __global__ void __launch_bounds__(CT_THREADS, TRANS ? 1 : 2) chunk_chain_walk_ke
                 atomicExch(p.status + 2, (TRANS ? 500u : 600u) + (uint32_t)n);
             }
         }
-        if (r == 0 && n + 3 < ns) prefetch_l2_bulk(rec_in + (qb + chunk_of(n + 3)) * 4096, 16384);
+        if (r == 0 && n + 3 < ns && rec_in) prefetch_l2_bulk(rec_in + (qb + chunk_of(n + 3)) * 4096, 16384);
         if (!wait_or_abort(mmab, (uint32_t)n & 1u, abortf, p.status, p.wait_ns)) return false;
         tc_fence_after();
         if (r == 0 && issued < ns) issue_copy(issued++);   // the stage just read is free
@@ -1696,9 +1715,9 @@ __global__ void __launch_bounds__(CT_THREADS, TRANS ? 1 : 2) chunk_chain_walk_ke
     };
 
     // the start: the sequence's own (h0 forward, dh_T reverse) at its end segment; zero elsewhere in the first
-    // walk; the scan's true start elsewhere in the second
+    // walk; the scan's true start elsewhere in the second, and in every segment of the forward's second walk
     const bool seq_start = rev ? sg == p.nseg - 1 : sg == 0;
-    if (seq_start || TRANS) {
+    if (TRANS || (seq_start && !p.fwd_walks)) {
         const float* src0 = seq_start ? (rev ? p.dhT : p.h0) : nullptr;
 #pragma unroll
         for (int e = 0; e < 32; e++) {
@@ -1830,6 +1849,334 @@ __global__ void __launch_bounds__(256) chunk_walk_scan_kernel(const __grid_const
 #pragma unroll
             for (int e = 0; e < 8; e++) cur[a][e] = nx[a][e];
     }
+}
+
+// ---------------------------------------------------------------- the forward split in time by walks (delta)
+// A long sequence over few heads is cut into P segments of seg_len chunks.  The tcgen05 forward runs every segment
+// from a zero state (the segments as batch rows) and keeps its residuals, so that the per-chunk maps are at hand:
+// Phi_k = diag(E_k) + Bhat_k^T (-W_k) (prep in its Phi-only mode).  The chunk map is affine ("GDN & MLA Mechanism
+// Deep-Dive", Step 5: chunked recurrence): with T_k = Phi_{k-1} ... Phi_{k0} the transition from the segment's start
+// to chunk k, the true state entering chunk k is S_k = S_local,k + T_k S_s.  So: a first walk per segment carries
+// T from the identity (its product Pi_s = T_{k1}); fwd_walk_scan_kernel joins the segments (S_0 = h0,
+// S_{s+1} = Pi_s S_s + X_s with X_s the zero-start run's final state) and writes h_T; a second walk per segment
+// carries D_k = T_k S_s from S_s and records it; fwd_walk_fix_kernel adds the outputs' share, o_k += Qc_k D_k with
+// Qc = Ctil + P (-W) (the part of o that the entering state drives), and, for a saving forward, makes the residuals
+// true: S_k += D_k, U_k += (-W_k) D_k.
+
+// The scan over a unit's segments, one CTA (256 threads) per unit, fp32 on the CUDA cores: thread = rows 2 (r >> 3),
+// + 1 x columns 8 (r & 7) .. + 7.  Xb: the zero-start run's final states [B * P, H, d_k, d_v] (segment view).
+__global__ void __launch_bounds__(256) fwd_walk_scan_kernel(const __grid_constant__ CbParams p, const float* Xb,
+                                                            const float* h0, float* hT)
+{
+    __shared__ __align__(16) float Pm[64][kAS];
+    __shared__ __align__(16) float Cm[64][kAS];
+    const int u = blockIdx.x, r = threadIdx.x, i0 = 2 * (r >> 3), j0 = 8 * (r & 7);
+    const int P = p.nseg, dk = p.dk, dv = p.dv_, b = u / p.H, h = u - b * p.H;
+    float cur[2][8];
+#pragma unroll
+    for (int a = 0; a < 2; a++)
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const int i = i0 + a, j = j0 + e;
+            cur[a][e] = h0 && i < dk && j < dv ? h0[((size_t)u * dk + i) * dv + j] : 0.f;
+        }
+    // fold s's Pi (this thread's four float4 of the shared tile) and X (its outputs), loaded a fold ahead
+    float4 pn[4];
+    float xn[2][8];
+    auto fetch = [&](int s) {
+        const float* pim = seg_rec(p, 0, u, s, 1);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const int f = r + 256 * e;
+            pn[e] = *rec4(pim, 0, f & 63, 4 * (f >> 6));
+        }
+        const float* xs = Xb + ((size_t)(b * P + s) * p.H + h) * dk * dv;
+#pragma unroll
+        for (int a = 0; a < 2; a++)
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const int i = i0 + a, j = j0 + e;
+                xn[a][e] = i < dk && j < dv ? xs[i * dv + j] : 0.f;
+            }
+    };
+    const int folds = hT ? P : P - 1;   // the last fold only gives h_T
+    if (folds > 0) fetch(0);
+    for (int s = 0; s < P; s++) {
+        float* dst = seg_rec(p, 0, u, s, 2);   // segment s starts from cur
+#pragma unroll
+        for (int a = 0; a < 2; a++)
+#pragma unroll
+            for (int c = 0; c < 2; c++)
+                *rec4(dst, 0, i0 + a, j0 + 4 * c) = make_float4(cur[a][4 * c], cur[a][4 * c + 1], cur[a][4 * c + 2],
+                                                                cur[a][4 * c + 3]);
+        if (s >= folds) break;
+        // cur <- Pi_s cur + X_s
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const int f = r + 256 * e;
+            *reinterpret_cast<float4*>(&Pm[f & 63][4 * (f >> 6)]) = pn[e];
+        }
+#pragma unroll
+        for (int a = 0; a < 2; a++) {
+            *reinterpret_cast<float4*>(&Cm[i0 + a][j0]) = make_float4(cur[a][0], cur[a][1], cur[a][2], cur[a][3]);
+            *reinterpret_cast<float4*>(&Cm[i0 + a][j0 + 4]) = make_float4(cur[a][4], cur[a][5], cur[a][6], cur[a][7]);
+        }
+        __syncthreads();
+        float nx[2][8];
+#pragma unroll
+        for (int a = 0; a < 2; a++)
+#pragma unroll
+            for (int e = 0; e < 8; e++) nx[a][e] = xn[a][e];
+        if (s + 1 < folds) fetch(s + 1);
+#pragma unroll 4
+        for (int m = 0; m < 64; m++) {
+            const float p0 = Pm[i0][m], p1 = Pm[i0 + 1][m];
+            const float4 c0 = *reinterpret_cast<const float4*>(&Cm[m][j0]);
+            const float4 c1 = *reinterpret_cast<const float4*>(&Cm[m][j0 + 4]);
+            const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                nx[0][e] = fmaf(p0, cv[e], nx[0][e]);
+                nx[1][e] = fmaf(p1, cv[e], nx[1][e]);
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 2; a++)
+#pragma unroll
+            for (int e = 0; e < 8; e++) cur[a][e] = nx[a][e];
+    }
+    if (hT) {
+#pragma unroll
+        for (int a = 0; a < 2; a++)
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const int i = i0 + a, j = j0 + e;
+                if (i < dk && j < dv) hT[((size_t)u * dk + i) * dv + j] = cur[a][e];
+            }
+    }
+}
+
+// The fix-up, chunk-parallel (persistent, three CTAs of 256 threads per SM).  Per chunk: Qc = Ctil + P (-W) from
+// the residuals (Ctil = c (.) exp(A Gam_t)), then one product of the stacked A operand [Qc ; -W] (M = 128, hi/lo)
+// with D (hi/lo tiles): TMEM rows 0..63 hold Qc D (tokens t), rows 64..127 (-W) D.  Lanes 0..63 write
+// o = o_zero-start + Qc D (bf16); lanes 64..127 add (-W) D to the residual U; every thread adds its share of D to
+// the residual state.  The products have M = 128; the rows past 64 of P's lo tile read the next 8 KB (Qc hi).
+namespace fx {
+constexpr uint32_t C = 0;          // c tile (TMA)
+constexpr uint32_t P = 8192;       // P hi, lo (residuals)
+constexpr uint32_t QCH = 24576;    // Qc hi, then -W hi: the stacked hi operand
+constexpr uint32_t NWH = 32768;
+constexpr uint32_t QCL = 40960;    // Qc lo, then -W lo: the stacked lo operand
+constexpr uint32_t NWL = 49152;
+constexpr uint32_t DH = 57344, DL = 65536;   // D hi, lo [i][j] (MN-major B)
+constexpr uint32_t SMALL = 73728;
+constexpr uint32_t SMEM = SMALL + 1024 + 1024;
+constexpr uint32_t TM_COLS = 128;
+static_assert(NWH == QCH + 8192 && NWL == QCL + 8192 && DL == DH + 8192 && P + 24576 <= NWH, "stacked operands");
+}  // namespace fx
+
+__global__ void __launch_bounds__(256, 3) fwd_walk_fix_kernel(const __grid_constant__ CbParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    PsSmall& S = *reinterpret_cast<PsSmall*>(sm + fx::SMALL);
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31, q4 = warp & 3, wh = warp >> 2, trow = r & 127;
+    if (r == 0) {
+        mbar_init(&S.full, 1);
+        mbar_init(&S.mma, 1);
+        S.abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&p.tm_c);
+    }
+    if (warp == 0) tmem_alloc(&S.tmem_base, fx::TM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = S.tmem_base, tl = tb + ((uint32_t)(q4 * 32) << 16);
+    uint32_t full_phase = 0, mma_phase = 0;
+    auto issue = [&](int q) {
+        const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
+        mbar_arrive_expect_tx(&S.full, 8192 + 16384 + 16384);
+        tma_load_4d(sm + fx::C, &p.tm_c, &S.full, 0, h, 64 * k, bb);
+        const unsigned char* rq = p.sv + (size_t)q * p.sv_stride;
+        bulk_g2s(sm + fx::P, rq + sv::P, 16384, &S.full);
+        bulk_g2s(sm + fx::NWH, rq + sv::NW, 8192, &S.full);
+        bulk_g2s(sm + fx::NWL, rq + sv::NWL, 8192, &S.full);
+    };
+    auto sync_all = [&]() {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(1, 256);
+        tc_fence_after();
+    };
+    auto wait_mma = [&](uint32_t where) -> bool {
+        if (warp == 0 && !wait_or_abort(&S.mma, mma_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
+            atomicExch(p.status + 2, 700u + where);
+        named_bar_sync(1, 256);
+        mma_phase ^= 1;
+        tc_fence_after();
+        return *(volatile uint32_t*)&S.abort == 0;
+    };
+    int q = blockIdx.x, pending = -1;
+    if (r == 0 && q < p.nq) issue(q);
+    if (q < p.nq) pending = q;
+    for (; q < p.nq; q += gridDim.x) {
+        const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H, t0 = 64 * k;
+        if (r < 64) {
+            const int t = t0 + r;
+            S.g[r] = t < p.T ? __bfloat162float(p.g[((size_t)bb * p.T + t) * p.H + h]) : 0.f;
+        } else if (r < 128) {
+            const int i = r - 64;
+            S.A2[i] = i < p.dk ? -expf(p.A_log[h * p.dk + i]) * kLog2e : 0.f;
+        } else if (r == 128 && q + (int)gridDim.x < p.nq) {
+            // the next chunk's tile, residuals and records towards L2 (its loads go out when this chunk is done)
+            const int qn = q + gridDim.x, un = qn / p.nchunks, kn = qn - un * p.nchunks, bn = un / p.H,
+                      hn = un - bn * p.H;
+            tma_prefetch_l2(&p.tm_c, 0, hn, 64 * kn, bn);
+            const unsigned char* rq = p.sv + (size_t)qn * p.sv_stride;
+            prefetch_l2_bulk(rq + sv::P, 16384);
+            prefetch_l2_bulk(rq + sv::NW, 16384);
+            prefetch_l2_bulk(p.st + (size_t)qn * 4096, 16384);
+        }
+        if (r >= 192 && q + (int)gridDim.x < p.nq) {
+            // the next chunk's zero-start output rows (one per thread) towards L2
+            const int qn = q + gridDim.x, un = qn / p.nchunks, kn = qn - un * p.nchunks, bn = un / p.H,
+                      hn = un - bn * p.H, tok = 64 * kn + (r - 192);
+            if (tok < p.T)
+                prefetch_l2_bulk(p.fw_o32 + (((size_t)bn * p.T + tok) * p.H + hn) * p.dv_, (uint32_t)p.dv_ * 4u);
+        }
+        // D of this chunk -> hi/lo tiles (thread = row i, 16 columns); the residual state S += D
+        {
+            const int i = r & 63, cq = r >> 6;
+            float dv16[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 d4 = *rec4(p.st, q, i, 16 * cq + e);
+                dv16[e] = d4.x; dv16[e + 1] = d4.y; dv16[e + 2] = d4.z; dv16[e + 3] = d4.w;
+            }
+            st16_split(sm + fx::DH, sm + fx::DL, i, cq, dv16);
+            if (p.fw_st) {
+#pragma unroll
+                for (int e = 0; e < 16; e += 4) {
+                    float4* s4 = rec4(p.fw_st, q, i, 16 * cq + e);
+                    const float4 o = *s4;
+                    *s4 = make_float4(o.x + dv16[e], o.y + dv16[e + 1], o.z + dv16[e + 2], o.w + dv16[e + 3]);
+                }
+            }
+        }
+        if (warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
+            atomicExch(p.status + 2, 6u);
+        named_bar_sync(1, 256);
+        if (*(volatile uint32_t*)&S.abort) break;
+        full_phase ^= 1;
+        pending = -1;
+        if (warp == 0) {
+            // inclusive scan of g, two tokens per lane
+            const float ga = S.g[2 * lane], gb = S.g[2 * lane + 1];
+            float x = ga + gb;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            S.G[2 * lane] = x - gb;
+            S.G[2 * lane + 1] = x;
+        }
+        sync_all();
+        if (r == 0) {
+            // P (-W): TMEM columns 0..63, rows t
+            const uint32_t pp = smem_u32(sm + fx::P), nwh = smem_u32(sm + fx::NWH), nwl = smem_u32(sm + fx::NWL);
+            const uint32_t id = idesc_bf16(128, 64, false, true);
+            mma_tiles(tb, pp, false, 0, 0, nwh, true, 8192, 0, 4, id, false);
+            mma_tiles(tb, pp, false, 0, 0, nwl, true, 8192, 0, 4, id, true);
+            mma_tiles(tb, pp + 8192, false, 0, 0, nwh, true, 8192, 0, 4, id, true);
+            mma_commit(&S.mma);
+        }
+        if (!wait_mma(0)) break;
+        if (q4 < 2) {
+            // Qc row t = Ctil + P (-W) into its hi/lo tiles
+            const int t = trow;
+            const float Gt = S.G[t];
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; h2++) {
+                const int cg = 2 * wh + h2;
+                float a[16], cv[16];
+                tmem_ld16(tl + 16 * cg, a);
+                tmem_wait_ld();
+                ld16_bf16(sm + fx::C, t, cg, cv);
+#pragma unroll
+                for (int e = 0; e < 16; e++) a[e] += cv[e] * fast_exp2(S.A2[16 * cg + e] * Gt);
+                st16_split(sm + fx::QCH, sm + fx::QCL, t, cg, a);
+            }
+        }
+        sync_all();
+        if (r == 0) {
+            // [Qc ; -W] D: rows 0..63 Qc D, rows 64..127 (-W) D; columns 0..63 (hi D_hi + lo D_hi), 64..127 (hi D_lo)
+            const uint32_t ah = smem_u32(sm + fx::QCH), al = smem_u32(sm + fx::QCL), dh = smem_u32(sm + fx::DH);
+            mma_tiles(tb, ah, false, 0, 0, dh, true, 8192, 0, 4, idesc_bf16(128, 128, false, true), false);
+            mma_tiles(tb, al, false, 0, 0, dh, true, 8192, 0, 4, idesc_bf16(128, 64, false, true), true);
+            mma_commit(&S.mma);
+        }
+        if (!wait_mma(1)) break;
+        {
+            const int t = trow & 63, tok = t0 + t;
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; h2++) {
+                const int c0 = 32 * wh + 16 * h2;
+                float a[16], b[16];
+                tmem_ld16(tl + c0, a);
+                tmem_ld16(tl + 64 + c0, b);
+                tmem_wait_ld();
+                if (q4 < 2) {
+                    // o = o_zero-start + Qc D
+                    if (tok < p.T) {
+                        const size_t row = ((size_t)bb * p.T + tok) * p.H + h;
+                        const float* o0 = p.fw_o32 + row * p.dv_ + c0;
+                        __nv_bfloat16* o = p.fw_o + row * p.dv_ + c0;
+#pragma unroll
+                        for (int e = 0; e < 16; e += 8) {
+                            if (c0 + e < p.dv_) {
+                                const float4 x0 = *reinterpret_cast<const float4*>(o0 + e);
+                                const float4 x1 = *reinterpret_cast<const float4*>(o0 + e + 4);
+                                uint4 w;
+                                w.x = pack_bf16(x0.x + a[e] + b[e], x0.y + a[e + 1] + b[e + 1]);
+                                w.y = pack_bf16(x0.z + a[e + 2] + b[e + 2], x0.w + a[e + 3] + b[e + 3]);
+                                w.z = pack_bf16(x1.x + a[e + 4] + b[e + 4], x1.y + a[e + 5] + b[e + 5]);
+                                w.w = pack_bf16(x1.z + a[e + 6] + b[e + 6], x1.w + a[e + 7] + b[e + 7]);
+                                *reinterpret_cast<uint4*>(o + e) = w;
+                            }
+                        }
+                    }
+                } else if (p.fw_st) {
+                    // the residual U += (-W) D
+                    float4* ur = reinterpret_cast<float4*>(p.sv + (size_t)q * p.sv_stride + sv::UT);
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4) {
+                        float4* u4 = ur + ((c0 + e) >> 2) * 64 + t;
+                        const float4 x = *u4;
+                        *u4 = make_float4(x.x + a[e] + b[e], x.y + a[e + 1] + b[e + 1], x.z + a[e + 2] + b[e + 2],
+                                          x.w + a[e + 3] + b[e + 3]);
+                    }
+                }
+            }
+        }
+        // the tiles are free: the next chunk's loads
+        tc_fence_before();
+        named_bar_sync(1, 256);
+        tc_fence_after();
+        if (q + (int)gridDim.x < p.nq) {
+            if (r == 0) issue(q + gridDim.x);
+            pending = q + gridDim.x;
+        }
+    }
+    // after an abort, let the loads in flight land before the CTA leaves
+    if (r == 0 && *(volatile uint32_t*)&S.abort && pending >= 0)
+        mbar_wait(&S.full, full_phase, nullptr, p.wait_ns);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tb, fx::TM_COLS);
 }
 
 // ================================================================= pass 3: gradients
@@ -2768,6 +3115,82 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     CB_MARK("grad");
     chunk_dalog_kernel<<<a.H, 64 * kDalogGroups, 0, st>>>(p.dA_part, a.A_log, a.dA_log, a.B, a.H, a.dk, p.nchunks);
+    return cudaGetLastError();
+}
+
+// The forward split in time by walks (fwd_walks_apply): the zero-start saving run over the segment view, Phi per
+// chunk, the transition walks, the scan over segments (with h_T), the walks of D = T_k S_s, the fix-up.  The
+// residuals go to a.saved (a saving forward, made true by the fix-up) or to the workspace.
+cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, int P, cudaStream_t st)
+{
+    unsigned char* ws = (unsigned char*)a.ws;
+    unsigned char* res = a.saved ? (unsigned char*)a.saved : ws + Lw.fw_res_off;
+    float* Xb = (float*)(ws + Lw.ts_h_off);
+    float* o32 = (float*)(ws + Lw.ts_o_off);
+    const int nk = a.T / 64, units = a.B * a.H;
+    if (a.T % (64 * P) != 0 || P < 2) return cudaErrorInvalidValue;
+    // 1. every segment from a zero state, keeping the residuals (states entering the chunks, from zero)
+    Args r = a;
+    r.B = a.B * P;
+    r.T = a.T / P;
+    r.h0 = nullptr;
+    r.hT = Xb;
+    r.o32 = o32;
+    r.saved = res;
+    r.seg = P;
+    bool handled = false;
+    cudaError_t e = launch_fwd_tc(r, st, &handled);
+    if (e != cudaSuccess) return e;
+    if (!handled) return cudaErrorInvalidValue;
+
+    CbParams p;
+    memset(&p, 0, sizeof(p));
+    if (!make_map(&p.tm_b, a.b, a.B, a.T, a.H, a.dk) || !make_map(&p.tm_c, a.c, a.B, a.T, a.H, a.dk))
+        return cudaErrorInvalidValue;
+    p.g = (const __nv_bfloat16*)a.g;
+    p.beta = (const __nv_bfloat16*)a.beta;
+    p.A_log = a.A_log;
+    p.phi = ws + Lw.cb_phi_off;
+    p.sv = res + (size_t)units * nk * kSavedStateBytes;
+    p.st = (float*)(ws + Lw.fw_d_off);   // the second walk's records D
+    p.status = (uint32_t*)a.ws;
+    p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv_ = a.dv;
+    p.nchunks = nk;
+    p.nq = units * nk;
+    p.sv_stride = sv::BYTES;
+    p.nseg = P;
+    p.seg_len = nk / P;
+    p.segrec = (float*)(ws + Lw.cb_seg_off);
+    p.fwd_walks = 1;
+    p.fw_o32 = o32;
+    p.fw_o = (__nv_bfloat16*)a.o;
+    p.fw_st = a.saved ? (float*)a.saved : nullptr;
+    p.starve = -1;
+    p.wait_ns = kWaitNs;
+    static bool attr = false;
+    if (!attr) {
+        if ((e = set_smem(chunk_prep_saved_kernel, ps::SMEM)) != cudaSuccess) return e;
+        if ((e = set_smem(chunk_chain_walk_kernel<false>, walk_smem(false))) != cudaSuccess) return e;
+        if ((e = set_smem(chunk_chain_walk_kernel<true>, walk_smem(true))) != cudaSuccess) return e;
+        if ((e = set_smem(fwd_walk_fix_kernel, fx::SMEM)) != cudaSuccess) return e;
+        attr = true;
+    }
+    int sms = 152;
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const int grid3 = p.nq < 3 * sms ? p.nq : 3 * sms;
+    // 2. Phi of every chunk
+    chunk_prep_saved_kernel<<<grid3, 256, ps::SMEM, st>>>(p);
+    // 3. each segment's transition
+    chunk_chain_walk_kernel<true><<<dim3(units, P, 1), CT_THREADS, walk_smem(true), st>>>(p);
+    // 4. the segments' true starting states, and h_T
+    fwd_walk_scan_kernel<<<units, 256, 0, st>>>(p, Xb, a.h0, a.hT);
+    // 5. D = T_k S_s through every segment
+    chunk_chain_walk_kernel<false><<<dim3(units, P, 1), CT_THREADS, walk_smem(false), st>>>(p);
+    // 6. outputs (and residuals) from the zero-start run's plus the state's share
+    fwd_walk_fix_kernel<<<grid3, 256, fx::SMEM, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -164,15 +164,23 @@ __device__ __forceinline__ void zero_chunk(unsigned char* tile, int row, int q)
 namespace svr {
 constexpr uint32_t P = 0, NA = 16384, DINV = 24576, K = 32768, NW = 49152, NWL = 57344, U = 65536, BYTES = 81920;
 constexpr uint32_t GATED_BYTES = 16384;   // gated: P only
+// the record index of chunk k of unit u: u * nchunks + k, or, on the segment view of a time split (p.seg
+// segments of a sequence as batch rows b' = b * seg + s), the index of that chunk in the whole sequence
+__device__ __forceinline__ size_t rec_index(const TcParams& p, int u, int k)
+{
+    if (p.seg <= 1) return (size_t)u * p.nchunks + k;
+    const int bs = u / p.H, h = u - bs * p.H, b = bs / p.seg, s = bs - b * p.seg;
+    return (((size_t)b * p.H + h) * p.seg + s) * p.nchunks + k;
+}
 __device__ __forceinline__ unsigned char* rec(const TcParams& p, int u, int k)
 {
-    return p.sv + ((size_t)u * p.nchunks + k) * p.sv_stride;
+    return p.sv + rec_index(p, u, k) * p.sv_stride;
 }
 // state row `row`, columns 32 wh .. 32 wh + 31; the record is column-group major (the float4 of row r, columns
 // 4 g .. 4 g + 3 at index 64 g + r), so a warp's 32 rows write 512 contiguous bytes
 __device__ __forceinline__ void put_state(const TcParams& p, int u, int k, int row, int wh, const float (&v)[32])
 {
-    float4* d = reinterpret_cast<float4*>(p.st + ((size_t)u * p.nchunks + k) * 4096) + (8 * wh) * 64 + row;
+    float4* d = reinterpret_cast<float4*>(p.st + rec_index(p, u, k) * 4096) + (8 * wh) * 64 + row;
 #pragma unroll
     for (int e = 0; e < 8; e++) d[64 * e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
 }
@@ -1090,9 +1098,11 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     *handled = true;
     const dim3 grid(a.B * a.H, (a.dv + 63) / 64);
     if (a.saved) {
-        // the residuals of the chunked backward: one slab, no option bits, no fp32 output (the host checks)
-        if (a.dv > 64 || a.norm || a.logits || a.o32) return cudaErrorInvalidValue;
+        // the residuals of the chunked backward: one slab, no option bits (the host checks); on a time split's
+        // segment view (a.seg segments per sequence) they are laid out by the chunks of the whole sequence
+        if (a.dv > 64 || a.norm || a.logits) return cudaErrorInvalidValue;
         const size_t nq = (size_t)a.B * a.H * p.nchunks;
+        p.seg = a.seg > 1 ? a.seg : 1;
         p.st = (float*)a.saved;
         p.sv = (unsigned char*)a.saved + nq * 16384;
         p.sv_stride = a.mode == GDN_DELTA ? svr::BYTES : svr::GATED_BYTES;

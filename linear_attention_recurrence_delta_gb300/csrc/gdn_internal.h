@@ -29,6 +29,7 @@ struct Args {
     float* dh0;
     // residuals of the chunked backward (delta): a saving forward writes them, the backward reads them
     void* saved;
+    int seg;               // a saving run over a time split's segment view: segments per sequence (else 0 or 1)
     // workspace
     void* ws;
     size_t ws_bytes;
@@ -63,6 +64,10 @@ struct WsLayout {
     size_t cb_ec_off = 0;         // gated: the chunk's decay [B*H*chunks][64]
     size_t cb_da_off = 0;         // per-chunk dA partials [B*H*chunks][64]
     size_t cb_seg_off = 0;        // delta, chain split in time: per (direction, unit, segment) three 64 x 64 fp32 records
+    // forward split in time by walks (delta, bf16): also ts_h_off (the zero-start run's final states), ts_o_off
+    // (its fp32 outputs), cb_phi_off (Phi per chunk) and cb_seg_off (per segment X, Pi, true start)
+    size_t fw_res_off = 0;        // the residuals when the caller keeps none (states, then the solve's results)
+    size_t fw_d_off = 0;          // D = T_k S_s per chunk, fp32 [B*H*chunks][64][64]
     size_t total = 0;
 };
 
@@ -91,6 +96,12 @@ inline size_t saved_solve_bytes(int mode) { return mode == GDN_DELTA ? kSavedSol
 inline bool chunk_bwd_applies(const gdn_shape_t& s, int logits, int norm)
 {
     return s.io == GDN_BF16 && s.T > 0 && s.dk <= 64 && s.dv <= 64 && !logits && !norm;
+}
+// The delta forward split in time into P segments runs as walks (launch_fwd_walks) when its segments are whole
+// chunks and the tcgen05 forward with residuals applies (bf16, heads up to 64 wide, no option bits).
+inline bool fwd_walks_apply(const gdn_shape_t& s, int P, int logits, int norm)
+{
+    return P > 1 && s.mode == GDN_DELTA && chunk_bwd_applies(s, logits, norm) && s.T % (64 * P) == 0;
 }
 // The chunked backward's chain split in time (delta only; gated chains are elementwise and cheap): its `dirs`
 // sweeps (2, or 1 from the forward's residuals) over `units` (batch, head) units run as dirs * units * nseg walks
@@ -123,6 +134,7 @@ cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled);
 cudaError_t launch_decode(const Args& a, cudaStream_t st);   // 1 <= T <= decode_max_tokens()
 cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& L, cudaStream_t st);   // chunk_bwd_applies()
+cudaError_t launch_fwd_walks(const Args& a, const WsLayout& L, int P, cudaStream_t st);   // fwd_walks_apply()
 int tsplit_factor(const gdn_shape_t& s, int backward);   // segments P of a time split, 1 = no split
 cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
                               cudaError_t (*fwd_core)(const Args&, cudaStream_t));

@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 from linear_attention_recurrence_delta_gb300 import inputs as I
-from tests.gdn_testlib import TOL, assert_close, run_bwd, run_saved
+import linear_attention_recurrence_delta_gb300 as gdn
+from tests.gdn_testlib import TOL, assert_close, run_bwd, run_saved, shape_of
 
 pytestmark = pytest.mark.gpu
 
@@ -57,10 +58,22 @@ def test_saved_steep_decay(mode, g_mu):
     check_saved(w)
 
 
-@pytest.mark.parametrize("name", ["delta_bf16_8x16x4096x64", "gated_bf16_8x16x4096x56_bwd"])
+@pytest.mark.parametrize("B,H,T,d", [(1, 4, 2048, 64), (2, 3, 3072, 56), (1, 2, 4096, 32)])
+def test_saved_split_forward(B, H, T, d):
+    """Long sequences over few heads: the delta forward splits in time into whole-chunk segments and runs them by
+    walks (zero-start runs keeping their residuals, the segments' transitions, a scan, the walks of T_k S_s and a
+    fix-up that makes outputs and residuals true); gdn_bwd_saved then reads those residuals."""
+    w = I.custom(name=f"saved_split_{B}x{H}x{T}x{d}", mode="delta", dtype="bf16", B=B, H=H, T=T, dk=d, dv=d,
+                 seed=5 + T + d, h0_std=0.3, backward=True)
+    assert gdn.gdn_plan(shape_of(w), 0).segments > 1 and gdn.gdn_saved_bytes(shape_of(w)) > 0
+    check_saved(w)
+
+
+@pytest.mark.parametrize("name", ["delta_bf16_8x16x4096x64", "gated_bf16_8x16x4096x56_bwd",
+                                  "delta_bf16_1x16x32768x64_bwd"])
 def test_saved_full_size(name):
-    """The bench's training step (8 x 16 x 4096 x 64, delta) and the gated 8 x 16 x 4096 x 56 workload at full size,
-    every unit: o, h_T and every gradient from the residuals against the fp64 oracle, and the gradients against
+    """The bench's training step (8 x 16 x 4096 x 64, delta), the gated 8 x 16 x 4096 x 56 workload and the
+    long-context 1 x 16 x 32768 x 64 one (forward split in time by walks) at full size, every unit: o, h_T and every gradient from the residuals against the fp64 oracle, and the gradients against
     gdn_bwd's, within the bf16 tolerance."""
     w = I.WORKLOADS[name].with_(backward=True)
     x = I.make_inputs(w)
