@@ -3138,6 +3138,7 @@ cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, int P, cudaStrea
     r.o32 = o32;
     r.saved = res;
     r.seg = P;
+    r.save_lite = a.saved ? 0 : 1;   // without a caller's residuals the walks need P and -W alone
     bool handled = false;
     cudaError_t e = launch_fwd_tc(r, st, &handled);
     if (e != cudaSuccess) return e;

@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
                 st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
             }
-            if (SAVE) svr::put_state(p, u, 0, trow, wh, Sreg);
+            if (SAVE && !p.sv_lite) svr::put_state(p, u, 0, trow, wh, Sreg);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, kMath);
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
                     st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
                 }
-                if (SAVE && kk + 1 < p.nchunks) svr::put_state(p, u, kk + 1, trow, wh, Sreg);
+                if (SAVE && !p.sv_lite && kk + 1 < p.nchunks) svr::put_state(p, u, kk + 1, trow, wh, Sreg);
             } else {
                 const int tg = kk * kC + (trow - 64);
                 const size_t orow_at = (((size_t)bb * T + tg) * H + h) * dv + jc0;
@@ -702,9 +702,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             // the level products gave K (zero on and above the diagonal): a residual; M = beta K
                             float4* kr = reinterpret_cast<float4*>(svr::rec(p, u, k) + svr::K) + (4 * cg) * 64 + t;
                             const float bet = S.beta[s][t];
+                            if (!p.sv_lite) {
 #pragma unroll
-                            for (int e = 0; e < 4; e++)
-                                kr[64 * e] = make_float4(out[4 * e], out[4 * e + 1], out[4 * e + 2], out[4 * e + 3]);
+                                for (int e = 0; e < 4; e++)
+                                    kr[64 * e] = make_float4(out[4 * e], out[4 * e + 1], out[4 * e + 2], out[4 * e + 3]);
+                            }
 #pragma unroll
                             for (int c = 0; c < 16; c++) out[c] *= bet;
                         }
@@ -875,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             v16[c] = x.x; v16[c + 1] = x.y; v16[c + 2] = x.z; v16[c + 3] = x.w;
                         }
                         st_plain16(X + X_DINV, trow, cg, v16);
-                        if (SAVE && trow < 64) st_plain16(svr::rec(p, u, k) + svr::DINV, trow, cg, v16);
+                        if (SAVE && !p.sv_lite && trow < 64) st_plain16(svr::rec(p, u, k) + svr::DINV, trow, cg, v16);
                     }
                 }
                 smem_to_tc();
@@ -907,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                             for (int c = 0; c < 16; c++) v[c] = -v[c];
                             st_plain16(X + X_NA, t, g, v);
-                            if (SAVE) st_plain16(svr::rec(p, u, k) + svr::NA, t, g, v);
+                            if (SAVE && !p.sv_lite) st_plain16(svr::rec(p, u, k) + svr::NA, t, g, v);
                         } else {
                             const int xg = g - 4;
                             const uint32_t blk = (uint32_t)(xg >> 2) * 8192u;
@@ -998,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         tmem_ld16(tl + TM_U + 16 * cg, v);
                         tmem_wait_ld();
                         st_split16(X + X_UH, X + X_UL, trow, cg, v);
-                        if (SAVE) {
+                        if (SAVE && !p.sv_lite) {
                             // U itself (the state already folded in) is a residual
                             float4* du = reinterpret_cast<float4*>(svr::rec(p, u, k) + svr::U) + (4 * cg) * 64 + trow;
 #pragma unroll
@@ -1103,6 +1105,7 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
         if (a.dv > 64 || a.norm || a.logits) return cudaErrorInvalidValue;
         const size_t nq = (size_t)a.B * a.H * p.nchunks;
         p.seg = a.seg > 1 ? a.seg : 1;
+        p.sv_lite = a.save_lite;
         p.st = (float*)a.saved;
         p.sv = (unsigned char*)a.saved + nq * 16384;
         p.sv_stride = a.mode == GDN_DELTA ? svr::BYTES : svr::GATED_BYTES;

@@ -30,6 +30,7 @@ struct Args {
     // residuals of the chunked backward (delta): a saving forward writes them, the backward reads them
     void* saved;
     int seg;               // a saving run over a time split's segment view: segments per sequence (else 0 or 1)
+    int save_lite;         // a saving run for the time split's walks alone: P and -W only
     // workspace
     void* ws;
     size_t ws_bytes;
