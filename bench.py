@@ -134,7 +134,17 @@ def fwd_launches(w):
     """Kernels one gdn_fwd call launches."""
     if tsplit_factor(w, False) == 1:
         return 1
+    if w.mode == "delta" and saved_bytes(w) > 0:
+        # the split by walks: zero-start run, Phi, transition walks, scan, walks of T_k S_s, fix-up
+        return 6
     return 5 if w.mode == "delta" else 3   # zero-start run, (identity, transition run), scan, output kernel
+
+
+def saved_bytes(w):
+    """gdn_saved_bytes of workload w: the residuals a saving forward keeps (0: it keeps none)."""
+    import linear_attention_recurrence_delta_gb300 as gdn
+    s = gdn.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.mode, w.dtype, gate_logits=w.gate_logits, norm_bc=w.norm_bc)
+    return gdn.gdn_saved_bytes(s)
 
 
 def bwd_slabs(w):

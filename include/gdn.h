@@ -220,9 +220,13 @@ gdn_status_t gdn_bwd(const gdn_shape_t* shape,
  * the bf16 tolerance (the level products form K without beta, M = beta K
  * after them, so the rounding differs).  Shapes: bf16, d_k and d_v <= 64, no
  * option bits but GDN_CHECK_FINITE, and a forward that runs as
- * one tensor-core pass (gdn_plan(shape, 0): segments 1, GDN_KERNEL_TENSOR_CORE);
- * gdn_saved_bytes is 0 for any other shape, and both calls return
- * GDN_ERR_MODE for it.  GDN_ERR_NULL if saved is NULL, GDN_ERR_ALIGN if it is
+ * one tensor-core pass (gdn_plan(shape, 0): segments 1, GDN_KERNEL_TENSOR_CORE)
+ * or, in delta mode, a split in time whose segments are whole chunks of 64
+ * tokens (T a multiple of 64 x segments); that split runs every segment from
+ * a zero state, keeping the residuals, then walks the segments' transitions
+ * on the tensor cores and corrects outputs and residuals by the true entering
+ * states (the saving call writes the true ones).  gdn_saved_bytes is 0 for
+ * any other shape, and both calls return GDN_ERR_MODE for it.  GDN_ERR_NULL if saved is NULL, GDN_ERR_ALIGN if it is
  * misaligned, GDN_ERR_WORKSPACE if saved_bytes is too small. */
 size_t gdn_saved_bytes(const gdn_shape_t* shape);
 
