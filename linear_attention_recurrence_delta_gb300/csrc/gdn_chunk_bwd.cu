@@ -97,8 +97,8 @@ struct CbParams {
     // delta, the chain as walks (few heads): nseg segments of seg_len chunks per unit (nseg = 1: no split)
     int nseg, seg_len;
     float* segrec;        // nseg > 1: per (direction, unit, segment) final X, final Pi, true start
-    // the forward split in time by walks (delta): prep builds Phi only, the walks carry no records R, the second
-    // walk starts every segment from its record [2] and writes D = T_k S_s to st; then the fix-up pass
+    // the forward split in time by walks (delta): prep writes [Phi_hi | Qc_hi | Phi_lo | Qc_lo] per chunk to phi
+    // and no Y; a saving forward's second walk writes D = T_k S_s to st for the residual fix-up
     int fwd_walks;
     const float* fw_o32;  // the zero-start run's outputs, fp32 [B, T, H, d_v]
     __nv_bfloat16* fw_o;  // the outputs
@@ -1134,12 +1134,12 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
     auto issue = [&](int q) {
         if (q == p.starve) return;   // failure-path test hook
         const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
-        mbar_arrive_expect_tx(&S.full, p.fwd_walks ? 2 * 8192 + 16384 : 3 * 8192 + 32768);
+        mbar_arrive_expect_tx(&S.full, (p.fwd_walks ? 2 : 3) * 8192 + 32768);
         tma_load_4d(sm + ps::STB, &p.tm_b, &S.full, 0, h, 64 * k, bb);
         tma_load_4d(sm + ps::STC, &p.tm_c, &S.full, 0, h, 64 * k, bb);
         if (!p.fwd_walks) tma_load_4d(sm + ps::STDO, &p.tm_do, &S.full, 0, h, 64 * k, bb);
         const unsigned char* rq = p.sv + (size_t)q * p.sv_stride;
-        if (!p.fwd_walks) bulk_g2s(sm + ps::P, rq + sv::P, 16384, &S.full);   // (Phi alone needs no P)
+        bulk_g2s(sm + ps::P, rq + sv::P, 16384, &S.full);
         bulk_g2s(sm + ps::NW, rq + sv::NW, 16384, &S.full);   // -W hi, then lo
     };
     auto sync_all = [&]() {
@@ -1175,7 +1175,7 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             tma_prefetch_l2(&p.tm_c, 0, hn, 64 * kn, bn);
             if (!p.fwd_walks) tma_prefetch_l2(&p.tm_do, 0, hn, 64 * kn, bn);
             const unsigned char* rq = p.sv + (size_t)qn * p.sv_stride;
-            if (!p.fwd_walks) prefetch_l2_bulk(rq + sv::P, 16384);
+            prefetch_l2_bulk(rq + sv::P, 16384);
             prefetch_l2_bulk(rq + sv::NW, 16384);
         }
         if (warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
@@ -1215,36 +1215,36 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             mma_tiles(tb, bh, true, 8192, 0, nw, true, 8192, 0, 4, idA, false);
             mma_tiles(tb, bh, true, 8192, 0, nw + 8192, true, 8192, 0, 4, idA, true);
             mma_tiles(tb, bh + 8192, true, 8192, 0, nw, true, 8192, 0, 4, idA, true);
-            if (!p.fwd_walks) {
-                // P (-W): columns 64..127, rows t
-                mma_tiles(tb + 64, pp, false, 0, 0, nw, true, 8192, 0, 4, idB, false);
-                mma_tiles(tb + 64, pp, false, 0, 0, nw + 8192, true, 8192, 0, 4, idB, true);
-                mma_tiles(tb + 64, pp + 8192, false, 0, 0, nw, true, 8192, 0, 4, idB, true);
-            }
+            // P (-W): columns 64..127, rows t
+            mma_tiles(tb + 64, pp, false, 0, 0, nw, true, 8192, 0, 4, idB, false);
+            mma_tiles(tb + 64, pp, false, 0, 0, nw + 8192, true, 8192, 0, 4, idB, true);
+            mma_tiles(tb + 64, pp + 8192, false, 0, 0, nw, true, 8192, 0, 4, idB, true);
             mma_commit(&S.mma);
         }
         if (!wait_mma(0)) break;
         if (q4 < 2) {
             // lanes 0..63: Phi row i out (hi/lo tiles), Qc row t = i = Ctil + P (-W) into its tiles
             const int i = trow;
-            unsigned char* phq = p.phi + (size_t)q * 16384;
+            // the forward's walks take [Phi_hi | Qc_hi | Phi_lo | Qc_lo] (32 KB a chunk): the stacked A operand
+            // [Phi ; Qc] gives the next state and the outputs' share in one product
+            const uint32_t rb = p.fwd_walks ? 32768u : 16384u, lo = p.fwd_walks ? 16384u : 8192u;
+            unsigned char* phq = p.phi + (size_t)q * rb;
             const float ec = fast_exp2(S.A2[i] * S.G[63]), Gt = S.G[i];
 #pragma unroll 1
             for (int h2 = 0; h2 < 2; h2++) {
                 const int cg = 2 * wh + h2;
                 float a[16], b[16], cv[16];
                 tmem_ld16(tl + 16 * cg, a);
+                tmem_ld16(tl + 64 + 16 * cg, b);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; e++) a[e] += (16 * cg + e == i) ? ec : 0.f;
-                st16_split(phq, phq + 8192, i, cg, a);
-                if (p.fwd_walks) continue;   // the forward's walks need Phi only
-                tmem_ld16(tl + 64 + 16 * cg, b);
-                tmem_wait_ld();
+                st16_split(phq, phq + lo, i, cg, a);
                 ld16_bf16(sm + ps::STC, i, cg, cv);
 #pragma unroll
                 for (int e = 0; e < 16; e++) b[e] += cv[e] * fast_exp2(S.A2[16 * cg + e] * Gt);
-                st16_split(sm + ps::QC, sm + ps::QC + 8192, i, cg, b);
+                if (p.fwd_walks) st16_split(phq + 8192, phq + 8192 + lo, i, cg, b);
+                else st16_split(sm + ps::QC, sm + ps::QC + 8192, i, cg, b);
             }
         }
         if (!p.fwd_walks) {   // Y = Qc^T dO
@@ -1631,24 +1631,17 @@ __global__ void __launch_bounds__(CT_THREADS, TRANS ? 1 : 2) chunk_chain_walk_ke
     if (warp == 2 || warp == 3) return;
     const uint32_t tb = misc[0];
     int issued = ns < CT_NS ? ns : CT_NS;
-    // the records R (none in the forward's walks, whose maps are linear) and the per-chunk records written
-    const float* rec_in = p.fwd_walks ? nullptr : (rev ? p.ych : p.dlt);
+    const float* rec_in = rev ? p.ych : p.dlt;
     float* rec_out = rev ? p.dst : p.st;
     if (r == 0) {
         for (int n = 0; n < issued; n++) issue_copy(n);
-        for (int n = 1; n < 3 && n < ns && rec_in; n++)
-            prefetch_l2_bulk(rec_in + (qb + chunk_of(n)) * 4096, 16384);
+        for (int n = 1; n < 3 && n < ns; n++) prefetch_l2_bulk(rec_in + (qb + chunk_of(n)) * 4096, 16384);
     }
     const int i = 32 * (warp & 1) + lane, j0 = 32 * (warp >> 2);
     const uint32_t tl = tb + ((uint32_t)(32 * (warp & 1)) << 16);
     uint32_t* abortf = &misc[1];
 
     auto rec = [&](const float* base, size_t q, float (&v)[32]) {
-        if (!base) {
-#pragma unroll
-            for (int e = 0; e < 32; e++) v[e] = 0.f;
-            return;
-        }
         const float4* src = rec4(base, q, i, j0);
 #pragma unroll
         for (int e = 0; e < 8; e++) {
@@ -1691,7 +1684,7 @@ __global__ void __launch_bounds__(CT_THREADS, TRANS ? 1 : 2) chunk_chain_walk_ke
                 atomicExch(p.status + 2, (TRANS ? 500u : 600u) + (uint32_t)n);
             }
         }
-        if (r == 0 && n + 3 < ns && rec_in) prefetch_l2_bulk(rec_in + (qb + chunk_of(n + 3)) * 4096, 16384);
+        if (r == 0 && n + 3 < ns) prefetch_l2_bulk(rec_in + (qb + chunk_of(n + 3)) * 4096, 16384);
         if (!wait_or_abort(mmab, (uint32_t)n & 1u, abortf, p.status, p.wait_ns)) return false;
         tc_fence_after();
         if (r == 0 && issued < ns) issue_copy(issued++);   // the stage just read is free
@@ -1715,9 +1708,9 @@ __global__ void __launch_bounds__(CT_THREADS, TRANS ? 1 : 2) chunk_chain_walk_ke
     };
 
     // the start: the sequence's own (h0 forward, dh_T reverse) at its end segment; zero elsewhere in the first
-    // walk; the scan's true start elsewhere in the second, and in every segment of the forward's second walk
+    // walk; the scan's true start elsewhere in the second
     const bool seq_start = rev ? sg == p.nseg - 1 : sg == 0;
-    if (TRANS || (seq_start && !p.fwd_walks)) {
+    if (seq_start || TRANS) {
         const float* src0 = seq_start ? (rev ? p.dhT : p.h0) : nullptr;
 #pragma unroll
         for (int e = 0; e < 32; e++) {
@@ -1854,14 +1847,14 @@ __global__ void __launch_bounds__(256) chunk_walk_scan_kernel(const __grid_const
 // ---------------------------------------------------------------- the forward split in time by walks (delta)
 // A long sequence over few heads is cut into P segments of seg_len chunks.  The tcgen05 forward runs every segment
 // from a zero state (the segments as batch rows) and keeps its residuals, so that the per-chunk maps are at hand:
-// Phi_k = diag(E_k) + Bhat_k^T (-W_k) (prep in its Phi-only mode).  The chunk map is affine ("GDN & MLA Mechanism
-// Deep-Dive", Step 5: chunked recurrence): with T_k = Phi_{k-1} ... Phi_{k0} the transition from the segment's start
-// to chunk k, the true state entering chunk k is S_k = S_local,k + T_k S_s.  So: a first walk per segment carries
-// T from the identity (its product Pi_s = T_{k1}); fwd_walk_scan_kernel joins the segments (S_0 = h0,
-// S_{s+1} = Pi_s S_s + X_s with X_s the zero-start run's final state) and writes h_T; a second walk per segment
-// carries D_k = T_k S_s from S_s and records it; fwd_walk_fix_kernel adds the outputs' share, o_k += Qc_k D_k with
-// Qc = Ctil + P (-W) (the part of o that the entering state drives), and, for a saving forward, makes the residuals
-// true: S_k += D_k, U_k += (-W_k) D_k.
+// Phi_k = diag(E_k) + Bhat_k^T (-W_k) and Qc_k = Ctil_k + P_k (-W_k) (prep in its forward mode).  The chunk map is
+// affine ("GDN & MLA Mechanism Deep-Dive", Step 5: chunked recurrence): with T_k = Phi_{k-1} ... Phi_{k0} the
+// transition from the segment's start to chunk k, the true state entering chunk k is S_local,k + T_k S_s, and the
+// chunk's outputs gain Qc_k T_k S_s.  So: a walk per segment carries T from the identity to the segment's
+// transition Pi_s; fwd_walk_scan_kernel joins the segments (S_0 = h0, S_{s+1} = Pi_s S_s + X_s with X_s the
+// zero-start run's final state) and writes h_T; a second walk per segment carries D_k = T_k S_s from S_s and writes
+// o = o_zero-start + Qc_k D_k; for a saving forward, fwd_walk_res_kernel then makes the residuals true:
+// S_k += D_k, U_k += (-W_k) D_k.
 
 // The scan over a unit's segments, one CTA (256 threads) per unit, fp32 on the CUDA cores: thread = rows 2 (r >> 3),
 // + 1 x columns 8 (r & 7) .. + 7.  Xb: the zero-start run's final states [B * P, H, d_k, d_v] (segment view).
@@ -1957,37 +1950,208 @@ __global__ void __launch_bounds__(256) fwd_walk_scan_kernel(const __grid_constan
     }
 }
 
-// The fix-up, chunk-parallel (persistent, three CTAs of 256 threads per SM).  Per chunk: Qc = Ctil + P (-W) from
-// the residuals (Ctil = c (.) exp(A Gam_t)), then one product of the stacked A operand [Qc ; -W] (M = 128, hi/lo)
-// with D (hi/lo tiles): TMEM rows 0..63 hold Qc D (tokens t), rows 64..127 (-W) D.  Lanes 0..63 write
-// o = o_zero-start + Qc D (bf16); lanes 64..127 add (-W) D to the residual U; every thread adds its share of D to
-// the residual state.  The products have M = 128; the rows past 64 of P's lo tile read the next 8 KB (Qc hi).
-namespace fx {
-constexpr uint32_t C = 0;          // c tile (TMA)
-constexpr uint32_t P = 8192;       // P hi, lo (residuals)
-constexpr uint32_t QCH = 24576;    // Qc hi, then -W hi: the stacked hi operand
-constexpr uint32_t NWH = 32768;
-constexpr uint32_t QCL = 40960;    // Qc lo, then -W lo: the stacked lo operand
-constexpr uint32_t NWL = 49152;
-constexpr uint32_t DH = 57344, DL = 65536;   // D hi, lo [i][j] (MN-major B)
-constexpr uint32_t SMALL = 73728;
-constexpr uint32_t SMEM = SMALL + 1024 + 1024;
-constexpr uint32_t TM_COLS = 128;
-static_assert(NWH == QCH + 8192 && NWL == QCL + 8192 && DL == DH + 8192 && P + 24576 <= NWH, "stacked operands");
-}  // namespace fx
+// The forward's walks over one segment each (blockIdx.x = unit, blockIdx.y = segment), on the records that prep
+// writes in its forward mode, [Phi_hi | Qc_hi | Phi_lo | Qc_lo] (32 KB a chunk, one bulk copy into a ring of CT_NS
+// stages).  A step is the chain's product with the stacked A operand [Phi ; Qc] (M = 128, rows 64..127 are Qc):
+//   D[:, 0:64 | 64:128] = [Phi ; Qc]_hi [X_hi | X_lo] (N = 128),   D[:, 0:64] += [Phi ; Qc]_lo X_hi (N = 64)
+// so TMEM lanes 0..63 hold Phi X (the next X) and lanes 64..127 Qc X.  OUT = false: X starts at the identity and
+// the segment's transition Pi is left in its record [1].  OUT = true: X starts at the segment's true state S_s
+// (record [2]) and is D_k = T_k S_s before chunk k's step; warps 2 and 3 (lanes 64..127, token t of the chunk,
+// 64 columns each) write o = o_zero-start + Qc D, and a saving forward's D goes to its records for the residual
+// fix-up.  Warps 0, 1, 4, 5 hold X as in the chain (row i, 32 columns); thread 0 issues the copies and products.
+constexpr uint32_t FW_STAGE = 32768;
+constexpr uint32_t FW_X = CT_NS * FW_STAGE;                  // X hi, X lo tiles
+constexpr uint32_t FW_BAR = FW_X + 16384;
+constexpr uint32_t FW_SMEM = FW_BAR + 128 + 1024;
 
-__global__ void __launch_bounds__(256, 3) fwd_walk_fix_kernel(const __grid_constant__ CbParams p)
+template <bool OUT>
+__global__ void __launch_bounds__(CT_THREADS, 1) fwd_walk_kernel(const __grid_constant__ CbParams p)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    PsSmall& S = *reinterpret_cast<PsSmall*>(sm + fx::SMALL);
+    unsigned char* Xt = sm + FW_X;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + FW_BAR);
+    uint64_t* mmab = full + CT_NS;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(mmab + 1);   // [0] TMEM base, [1] abort
+    const int u = blockIdx.x, sg = blockIdx.y, r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const int nk = p.nchunks, k0 = sg * p.seg_len, k1 = min(k0 + p.seg_len, nk), ns = k1 - k0;
+    const int bb = u / p.H, h = u - bb * p.H;
+    const size_t qb = (size_t)u * nk;
+    // active threads: the X rows (warps 0, 1, 4, 5) and, with OUT, the output rows (warps 2, 3)
+    const int nact = OUT ? 192 : 128;
+    const bool orow = OUT && (warp == 2 || warp == 3);
+    auto issue_copy = [&](int n) {
+        const int s = n % CT_NS;
+        mbar_arrive_expect_tx(&full[s], FW_STAGE);
+        bulk_g2s(sm + s * FW_STAGE, p.phi + (qb + k0 + n) * FW_STAGE, FW_STAGE, &full[s]);
+    };
+    if (r == 0) {
+        for (int s = 0; s < CT_NS; s++) mbar_init(&full[s], 1);
+        mbar_init(mmab, 1);
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&misc[0], 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (!OUT && (warp == 2 || warp == 3)) return;
+    const uint32_t tb = misc[0];
+    int issued = ns < CT_NS ? ns : CT_NS;
+    if (r == 0)
+        for (int n = 0; n < issued; n++) issue_copy(n);
+    const int i = 32 * (warp & 1) + lane, j0 = 32 * (warp >> 2);
+    const uint32_t tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+    uint32_t* abortf = &misc[1];
+    const int t = 32 * (warp & 1) + lane;   // output rows: the chunk's token
+    auto o_row = [&](int k) { return ((size_t)bb * p.T + 64 * k + t) * p.H + h; };
+    if (orow)
+        for (int n = 0; n < 2 && n < ns; n++)
+            if (64 * (k0 + n) + t < p.T) prefetch_l2_bulk(p.fw_o32 + o_row(k0 + n) * p.dv_, (uint32_t)p.dv_ * 4u);
+    float x[32];
+    if (!orow) {
+        if (OUT) {
+            const float4* src = rec4(seg_rec(p, 0, u, sg, 2), 0, i, j0);
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const float4 v = src[64 * e];
+                x[4 * e] = v.x; x[4 * e + 1] = v.y; x[4 * e + 2] = v.z; x[4 * e + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; e++) x[e] = i == j0 + e ? 1.f : 0.f;
+        }
+    }
+    bool ok = true;
+    float4 o0v[16];   // output rows: the zero-start outputs of token t, loaded before the step's product
+    for (int n = 0; n < ns; n++) {
+        const int k = k0 + n;
+        if (orow) {
+            const bool in = 64 * k + t < p.T;
+            const float* o0 = p.fw_o32 + o_row(in ? k : k0) * p.dv_;
+#pragma unroll
+            for (int e = 0; e < 16; e++)
+                o0v[e] = 4 * e < p.dv_ ? *reinterpret_cast<const float4*>(o0 + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (!orow) {
+            if (OUT && p.fw_st) {   // D_k for the residual fix-up
+                float4* dst = rec4(p.st, qb + k, i, j0);
+#pragma unroll
+                for (int e = 0; e < 8; e++) dst[64 * e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                float a8[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) a8[e] = x[8 * q + e];
+                st_row8_split(Xt, Xt + 8192, i, (j0 >> 3) + q, a8);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(1, nact);
+        tc_fence_after();
+        const int s = n % CT_NS;
+        if (r == 0) {
+            if (wait_or_abort(&full[s], (uint32_t)(n / CT_NS) & 1u, abortf, p.status, p.wait_ns)) {
+                tc_fence_after();
+                const uint32_t a = smem_u32(sm + s * FW_STAGE), xb = smem_u32(Xt);
+                mma_tiles(tb, a, false, 0, 0, xb, true, 8192, 0, 4, idesc_bf16(128, 128, false, true), false);
+                mma_tiles(tb, a + 16384, false, 0, 0, xb, true, 8192, 0, 4, idesc_bf16(128, 64, false, true), true);
+                mma_commit(mmab);
+            } else {
+                atomicExch(p.status + 2, (OUT ? 820u : 810u) + (uint32_t)n);
+            }
+        }
+        if (orow && n + 2 < ns && 64 * (k + 2) + t < p.T)
+            prefetch_l2_bulk(p.fw_o32 + o_row(k + 2) * p.dv_, (uint32_t)p.dv_ * 4u);
+        if (!wait_or_abort(mmab, (uint32_t)n & 1u, abortf, p.status, p.wait_ns)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        if (r == 0 && issued < ns) issue_copy(issued++);   // the stage just read is free
+        if (!orow) {
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                float a[16], b[16];
+                tmem_ld16(tl + j0 + 16 * hh, a);        // [Phi ; Qc]_hi X_hi + [Phi ; Qc]_lo X_hi
+                tmem_ld16(tl + 64 + j0 + 16 * hh, b);   // [Phi ; Qc]_hi X_lo
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; e++) x[16 * hh + e] = a[e] + b[e];
+            }
+        } else {
+            // o = o_zero-start + Qc D, token t of chunk k (the TMEM loads are warp-uniform; the row may be past T)
+            const bool in = 64 * k + t < p.T;
+            __nv_bfloat16* o = p.fw_o + o_row(k) * p.dv_;
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                float a[16], b[16];
+                tmem_ld16(tl + c0, a);
+                tmem_ld16(tl + 64 + c0, b);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; e += 8) {
+                    if (in && c0 + e < p.dv_) {
+                        const float4 x0 = o0v[(c0 + e) >> 2];
+                        const float4 x1 = o0v[((c0 + e) >> 2) + 1];
+                        uint4 w;
+                        w.x = pack_bf16(x0.x + a[e] + b[e], x0.y + a[e + 1] + b[e + 1]);
+                        w.y = pack_bf16(x0.z + a[e + 2] + b[e + 2], x0.w + a[e + 3] + b[e + 3]);
+                        w.z = pack_bf16(x1.x + a[e + 4] + b[e + 4], x1.y + a[e + 5] + b[e + 5]);
+                        w.w = pack_bf16(x1.z + a[e + 6] + b[e + 6], x1.w + a[e + 7] + b[e + 7]);
+                        *reinterpret_cast<uint4*>(o + c0 + e) = w;
+                    }
+                }
+            }
+        }
+    }
+    if (ok && !OUT && !orow) {   // the segment's transition
+        float4* dst = rec4(seg_rec(p, 0, u, sg, 1), 0, i, j0);
+#pragma unroll
+        for (int e = 0; e < 8; e++) dst[64 * e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+    }
+    // wind down: after an abort, let the copies still in flight land before the CTA leaves
+    if (r == 0 && *(volatile uint32_t*)abortf)
+        for (int n = issued - CT_NS < 0 ? 0 : issued - CT_NS; n < issued; n++)
+            mbar_wait(&full[n % CT_NS], (uint32_t)(n / CT_NS) & 1u, nullptr, p.wait_ns);
+    tc_fence_before();
+    named_bar_sync(1, nact);
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tb, 128);
+}
+
+// A saving forward's residual fix-up, chunk-parallel (persistent, three CTAs of 256 threads per SM): with D_k from
+// the output walk, the residual state S_k += D_k and U_k += (-W_k) D_k, the latter one product on hi/lo operands:
+// TMEM[:, 0:64 | 64:128] = (-W)_hi [D_hi | D_lo] (N = 128), TMEM[:, 0:64] += (-W)_lo D_hi; lanes 0..63 (tokens t)
+// add it to U.  The products have M = 128; the rows past 64 of the A operands read the next 8 KB (the lo tile, and
+// for the lo tile the D tiles), which give TMEM rows nobody reads.
+namespace fx {
+constexpr uint32_t NWH = 0, NWL = 8192;           // -W hi, lo (residuals, one bulk copy)
+constexpr uint32_t DH = 16384, DL = 24576;        // D hi, lo [i][j] (MN-major B)
+constexpr uint32_t SMALL = 32768;
+constexpr uint32_t SMEM = SMALL + 1024 + 1024;
+constexpr uint32_t TM_COLS = 128;
+static_assert(NWL == NWH + 8192 && DH == NWL + 8192 && DL == DH + 8192, "stacked operands");
+}  // namespace fx
+
+struct FxSmall {
+    uint64_t full, mma;
+    uint32_t tmem_base, abort;
+};
+
+__global__ void __launch_bounds__(256, 3) fwd_walk_res_kernel(const __grid_constant__ CbParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    FxSmall& S = *reinterpret_cast<FxSmall*>(sm + fx::SMALL);
     const int r = threadIdx.x, warp = r >> 5, lane = r & 31, q4 = warp & 3, wh = warp >> 2, trow = r & 127;
     if (r == 0) {
         mbar_init(&S.full, 1);
         mbar_init(&S.mma, 1);
         S.abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&p.tm_c);
     }
     if (warp == 0) tmem_alloc(&S.tmem_base, fx::TM_COLS);
     tc_fence_before();
@@ -1996,57 +2160,21 @@ __global__ void __launch_bounds__(256, 3) fwd_walk_fix_kernel(const __grid_const
     const uint32_t tb = S.tmem_base, tl = tb + ((uint32_t)(q4 * 32) << 16);
     uint32_t full_phase = 0, mma_phase = 0;
     auto issue = [&](int q) {
-        const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
-        mbar_arrive_expect_tx(&S.full, 8192 + 16384 + 16384);
-        tma_load_4d(sm + fx::C, &p.tm_c, &S.full, 0, h, 64 * k, bb);
-        const unsigned char* rq = p.sv + (size_t)q * p.sv_stride;
-        bulk_g2s(sm + fx::P, rq + sv::P, 16384, &S.full);
-        bulk_g2s(sm + fx::NWH, rq + sv::NW, 8192, &S.full);
-        bulk_g2s(sm + fx::NWL, rq + sv::NWL, 8192, &S.full);
-    };
-    auto sync_all = [&]() {
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(1, 256);
-        tc_fence_after();
-    };
-    auto wait_mma = [&](uint32_t where) -> bool {
-        if (warp == 0 && !wait_or_abort(&S.mma, mma_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
-            atomicExch(p.status + 2, 700u + where);
-        named_bar_sync(1, 256);
-        mma_phase ^= 1;
-        tc_fence_after();
-        return *(volatile uint32_t*)&S.abort == 0;
+        mbar_arrive_expect_tx(&S.full, 16384);
+        bulk_g2s(sm + fx::NWH, p.sv + (size_t)q * p.sv_stride + sv::NW, 16384, &S.full);   // -W hi, then lo
     };
     int q = blockIdx.x, pending = -1;
     if (r == 0 && q < p.nq) issue(q);
     if (q < p.nq) pending = q;
     for (; q < p.nq; q += gridDim.x) {
-        const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H, t0 = 64 * k;
-        if (r < 64) {
-            const int t = t0 + r;
-            S.g[r] = t < p.T ? __bfloat162float(p.g[((size_t)bb * p.T + t) * p.H + h]) : 0.f;
-        } else if (r < 128) {
-            const int i = r - 64;
-            S.A2[i] = i < p.dk ? -expf(p.A_log[h * p.dk + i]) * kLog2e : 0.f;
-        } else if (r == 128 && q + (int)gridDim.x < p.nq) {
-            // the next chunk's tile, residuals and records towards L2 (its loads go out when this chunk is done)
-            const int qn = q + gridDim.x, un = qn / p.nchunks, kn = qn - un * p.nchunks, bn = un / p.H,
-                      hn = un - bn * p.H;
-            tma_prefetch_l2(&p.tm_c, 0, hn, 64 * kn, bn);
-            const unsigned char* rq = p.sv + (size_t)qn * p.sv_stride;
-            prefetch_l2_bulk(rq + sv::P, 16384);
-            prefetch_l2_bulk(rq + sv::NW, 16384);
+        if (r == 0 && q + (int)gridDim.x < p.nq) {
+            const int qn = q + gridDim.x;
+            prefetch_l2_bulk(p.sv + (size_t)qn * p.sv_stride + sv::NW, 16384);
+            prefetch_l2_bulk(p.sv + (size_t)qn * p.sv_stride + sv::UT, 16384);
             prefetch_l2_bulk(p.st + (size_t)qn * 4096, 16384);
+            prefetch_l2_bulk(p.fw_st + (size_t)qn * 4096, 16384);
         }
-        if (r >= 192 && q + (int)gridDim.x < p.nq) {
-            // the next chunk's zero-start output rows (one per thread) towards L2
-            const int qn = q + gridDim.x, un = qn / p.nchunks, kn = qn - un * p.nchunks, bn = un / p.H,
-                      hn = un - bn * p.H, tok = 64 * kn + (r - 192);
-            if (tok < p.T)
-                prefetch_l2_bulk(p.fw_o32 + (((size_t)bn * p.T + tok) * p.H + hn) * p.dv_, (uint32_t)p.dv_ * 4u);
-        }
-        // D of this chunk -> hi/lo tiles (thread = row i, 16 columns); the residual state S += D
+        // D -> hi/lo tiles (thread = row i, 16 columns); the residual state S += D
         {
             const int i = r & 63, cq = r >> 6;
             float dv16[16];
@@ -2056,71 +2184,37 @@ __global__ void __launch_bounds__(256, 3) fwd_walk_fix_kernel(const __grid_const
                 dv16[e] = d4.x; dv16[e + 1] = d4.y; dv16[e + 2] = d4.z; dv16[e + 3] = d4.w;
             }
             st16_split(sm + fx::DH, sm + fx::DL, i, cq, dv16);
-            if (p.fw_st) {
 #pragma unroll
-                for (int e = 0; e < 16; e += 4) {
-                    float4* s4 = rec4(p.fw_st, q, i, 16 * cq + e);
-                    const float4 o = *s4;
-                    *s4 = make_float4(o.x + dv16[e], o.y + dv16[e + 1], o.z + dv16[e + 2], o.w + dv16[e + 3]);
-                }
+            for (int e = 0; e < 16; e += 4) {
+                float4* s4 = rec4(p.fw_st, q, i, 16 * cq + e);
+                const float4 o = *s4;
+                *s4 = make_float4(o.x + dv16[e], o.y + dv16[e + 1], o.z + dv16[e + 2], o.w + dv16[e + 3]);
             }
         }
         if (warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
             atomicExch(p.status + 2, 6u);
+        fence_proxy_async_smem();
+        tc_fence_before();
         named_bar_sync(1, 256);
+        tc_fence_after();
         if (*(volatile uint32_t*)&S.abort) break;
         full_phase ^= 1;
         pending = -1;
-        if (warp == 0) {
-            // inclusive scan of g, two tokens per lane
-            const float ga = S.g[2 * lane], gb = S.g[2 * lane + 1];
-            float x = ga + gb;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            S.G[2 * lane] = x - gb;
-            S.G[2 * lane + 1] = x;
-        }
-        sync_all();
         if (r == 0) {
-            // P (-W): TMEM columns 0..63, rows t
-            const uint32_t pp = smem_u32(sm + fx::P), nwh = smem_u32(sm + fx::NWH), nwl = smem_u32(sm + fx::NWL);
-            const uint32_t id = idesc_bf16(128, 64, false, true);
-            mma_tiles(tb, pp, false, 0, 0, nwh, true, 8192, 0, 4, id, false);
-            mma_tiles(tb, pp, false, 0, 0, nwl, true, 8192, 0, 4, id, true);
-            mma_tiles(tb, pp + 8192, false, 0, 0, nwh, true, 8192, 0, 4, id, true);
+            const uint32_t nwh = smem_u32(sm + fx::NWH), nwl = smem_u32(sm + fx::NWL), dh = smem_u32(sm + fx::DH);
+            mma_tiles(tb, nwh, false, 0, 0, dh, true, 8192, 0, 4, idesc_bf16(128, 128, false, true), false);
+            mma_tiles(tb, nwl, false, 0, 0, dh, true, 8192, 0, 4, idesc_bf16(128, 64, false, true), true);
             mma_commit(&S.mma);
         }
-        if (!wait_mma(0)) break;
+        if (warp == 0 && !wait_or_abort(&S.mma, mma_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
+            atomicExch(p.status + 2, 710u);
+        named_bar_sync(1, 256);
+        mma_phase ^= 1;
+        tc_fence_after();
+        if (*(volatile uint32_t*)&S.abort) break;
         if (q4 < 2) {
-            // Qc row t = Ctil + P (-W) into its hi/lo tiles
-            const int t = trow;
-            const float Gt = S.G[t];
-#pragma unroll 1
-            for (int h2 = 0; h2 < 2; h2++) {
-                const int cg = 2 * wh + h2;
-                float a[16], cv[16];
-                tmem_ld16(tl + 16 * cg, a);
-                tmem_wait_ld();
-                ld16_bf16(sm + fx::C, t, cg, cv);
-#pragma unroll
-                for (int e = 0; e < 16; e++) a[e] += cv[e] * fast_exp2(S.A2[16 * cg + e] * Gt);
-                st16_split(sm + fx::QCH, sm + fx::QCL, t, cg, a);
-            }
-        }
-        sync_all();
-        if (r == 0) {
-            // [Qc ; -W] D: rows 0..63 Qc D, rows 64..127 (-W) D; columns 0..63 (hi D_hi + lo D_hi), 64..127 (hi D_lo)
-            const uint32_t ah = smem_u32(sm + fx::QCH), al = smem_u32(sm + fx::QCL), dh = smem_u32(sm + fx::DH);
-            mma_tiles(tb, ah, false, 0, 0, dh, true, 8192, 0, 4, idesc_bf16(128, 128, false, true), false);
-            mma_tiles(tb, al, false, 0, 0, dh, true, 8192, 0, 4, idesc_bf16(128, 64, false, true), true);
-            mma_commit(&S.mma);
-        }
-        if (!wait_mma(1)) break;
-        {
-            const int t = trow & 63, tok = t0 + t;
+            // the residual U += (-W) D, token trow
+            float4* ur = reinterpret_cast<float4*>(p.sv + (size_t)q * p.sv_stride + sv::UT);
 #pragma unroll 1
             for (int h2 = 0; h2 < 2; h2++) {
                 const int c0 = 32 * wh + 16 * h2;
@@ -2128,40 +2222,16 @@ __global__ void __launch_bounds__(256, 3) fwd_walk_fix_kernel(const __grid_const
                 tmem_ld16(tl + c0, a);
                 tmem_ld16(tl + 64 + c0, b);
                 tmem_wait_ld();
-                if (q4 < 2) {
-                    // o = o_zero-start + Qc D
-                    if (tok < p.T) {
-                        const size_t row = ((size_t)bb * p.T + tok) * p.H + h;
-                        const float* o0 = p.fw_o32 + row * p.dv_ + c0;
-                        __nv_bfloat16* o = p.fw_o + row * p.dv_ + c0;
 #pragma unroll
-                        for (int e = 0; e < 16; e += 8) {
-                            if (c0 + e < p.dv_) {
-                                const float4 x0 = *reinterpret_cast<const float4*>(o0 + e);
-                                const float4 x1 = *reinterpret_cast<const float4*>(o0 + e + 4);
-                                uint4 w;
-                                w.x = pack_bf16(x0.x + a[e] + b[e], x0.y + a[e + 1] + b[e + 1]);
-                                w.y = pack_bf16(x0.z + a[e + 2] + b[e + 2], x0.w + a[e + 3] + b[e + 3]);
-                                w.z = pack_bf16(x1.x + a[e + 4] + b[e + 4], x1.y + a[e + 5] + b[e + 5]);
-                                w.w = pack_bf16(x1.z + a[e + 6] + b[e + 6], x1.w + a[e + 7] + b[e + 7]);
-                                *reinterpret_cast<uint4*>(o + e) = w;
-                            }
-                        }
-                    }
-                } else if (p.fw_st) {
-                    // the residual U += (-W) D
-                    float4* ur = reinterpret_cast<float4*>(p.sv + (size_t)q * p.sv_stride + sv::UT);
-#pragma unroll
-                    for (int e = 0; e < 16; e += 4) {
-                        float4* u4 = ur + ((c0 + e) >> 2) * 64 + t;
-                        const float4 x = *u4;
-                        *u4 = make_float4(x.x + a[e] + b[e], x.y + a[e + 1] + b[e + 1], x.z + a[e + 2] + b[e + 2],
-                                          x.w + a[e + 3] + b[e + 3]);
-                    }
+                for (int e = 0; e < 16; e += 4) {
+                    float4* u4 = ur + ((c0 + e) >> 2) * 64 + trow;
+                    const float4 x = *u4;
+                    *u4 = make_float4(x.x + a[e] + b[e], x.y + a[e + 1] + b[e + 1], x.z + a[e + 2] + b[e + 2],
+                                      x.w + a[e + 3] + b[e + 3]);
                 }
             }
         }
-        // the tiles are free: the next chunk's loads
+        // the tiles are free: the next chunk's -W
         tc_fence_before();
         named_bar_sync(1, 256);
         tc_fence_after();
@@ -2170,9 +2240,7 @@ __global__ void __launch_bounds__(256, 3) fwd_walk_fix_kernel(const __grid_const
             pending = q + gridDim.x;
         }
     }
-    // after an abort, let the loads in flight land before the CTA leaves
-    if (r == 0 && *(volatile uint32_t*)&S.abort && pending >= 0)
-        mbar_wait(&S.full, full_phase, nullptr, p.wait_ns);
+    if (r == 0 && *(volatile uint32_t*)&S.abort && pending >= 0) mbar_wait(&S.full, full_phase, nullptr, p.wait_ns);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -3171,9 +3239,9 @@ cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, int P, cudaStrea
     static bool attr = false;
     if (!attr) {
         if ((e = set_smem(chunk_prep_saved_kernel, ps::SMEM)) != cudaSuccess) return e;
-        if ((e = set_smem(chunk_chain_walk_kernel<false>, walk_smem(false))) != cudaSuccess) return e;
-        if ((e = set_smem(chunk_chain_walk_kernel<true>, walk_smem(true))) != cudaSuccess) return e;
-        if ((e = set_smem(fwd_walk_fix_kernel, fx::SMEM)) != cudaSuccess) return e;
+        if ((e = set_smem(fwd_walk_kernel<false>, FW_SMEM)) != cudaSuccess) return e;
+        if ((e = set_smem(fwd_walk_kernel<true>, FW_SMEM)) != cudaSuccess) return e;
+        if ((e = set_smem(fwd_walk_res_kernel, fx::SMEM)) != cudaSuccess) return e;
         attr = true;
     }
     int sms = 152;
@@ -3182,16 +3250,16 @@ cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, int P, cudaStrea
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
     const int grid3 = p.nq < 3 * sms ? p.nq : 3 * sms;
-    // 2. Phi of every chunk
+    // 2. Phi and Qc of every chunk
     chunk_prep_saved_kernel<<<grid3, 256, ps::SMEM, st>>>(p);
     // 3. each segment's transition
-    chunk_chain_walk_kernel<true><<<dim3(units, P, 1), CT_THREADS, walk_smem(true), st>>>(p);
+    fwd_walk_kernel<false><<<dim3(units, P), CT_THREADS, FW_SMEM, st>>>(p);
     // 4. the segments' true starting states, and h_T
     fwd_walk_scan_kernel<<<units, 256, 0, st>>>(p, Xb, a.h0, a.hT);
-    // 5. D = T_k S_s through every segment
-    chunk_chain_walk_kernel<false><<<dim3(units, P, 1), CT_THREADS, walk_smem(false), st>>>(p);
-    // 6. outputs (and residuals) from the zero-start run's plus the state's share
-    fwd_walk_fix_kernel<<<grid3, 256, fx::SMEM, st>>>(p);
+    // 5. D = T_k S_s through every segment, and the outputs o = o_zero-start + Qc D
+    fwd_walk_kernel<true><<<dim3(units, P), CT_THREADS, FW_SMEM, st>>>(p);
+    // 6. a saving forward's residuals made true
+    if (a.saved) fwd_walk_res_kernel<<<grid3, 256, fx::SMEM, st>>>(p);
     return cudaGetLastError();
 }
 

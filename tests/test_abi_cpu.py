@@ -134,8 +134,8 @@ def test_time_split_workspace():
     """Long sequences over few heads take the time-split forward, whose workspace holds per-segment states; many
     heads or short sequences need none.  Delta bf16 heads up to 64 wide whose segments are whole chunks run the split
     by walks: the zero-start run's final states and fp32 outputs, its residuals (a 16 KB state and 80 KB of solve
-    results per chunk of 64 tokens), Phi and D = T_k S_s per chunk (16 KB each), three 16 KB records per (head,
-    segment).  Other splits (gated, option bits, fp32, ragged segments) keep the transition run's buffers (delta:
+    results per chunk of 64 tokens), Phi with Qc (32 KB) and D = T_k S_s (16 KB) per chunk, three 16 KB records per
+    (head, segment).  Other splits (gated, option bits, fp32, ragged segments) keep the transition run's buffers (delta:
     transitions, a zero-value tensor and the transition run's fp32 outputs)."""
     lib = gdn
     few = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0)
@@ -146,7 +146,7 @@ def test_time_split_workspace():
     assert many == 256 and short == 256
     nq, P = 16 * 512, 8
     assert lib.gdn_plan(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0).segments == P
-    assert few == 256 + 16 * P * 16384 + 32768 * 16 * 64 * 4 + nq * (16384 + 81920) + 2 * nq * 16384 \
+    assert few == 256 + 16 * P * 16384 + 32768 * 16 * 64 * 4 + nq * (16384 + 81920) + nq * (32768 + 16384) \
         + 16 * P * 3 * 16384
     # the transition run's buffers: 2 x 128 states (16 KB) + 2 x 128 transitions + zero values (bf16) and the fp32
     # outputs of the zero-start and transition runs
