@@ -1758,90 +1758,89 @@ __global__ void __launch_bounds__(CT_THREADS, TRANS ? 1 : 2) chunk_chain_walk_ke
     if (warp == 0) tmem_dealloc(tb, TRANS ? 256 : 128);
 }
 
-// The scan over a unit's segments, one CTA (256 threads) per (unit, direction); fp32 on the CUDA cores, thread =
-// rows 2 (r >> 3), + 1 x columns 8 (r & 7) .. + 7.  Forward: the first segment started from h0, so its X is the true
-// state entering the second; then S_{s+1} = Pi_s S_s + X_s.  Reverse: the last segment started from dh_T, so its X
-// is the true adjoint leaving the one before; then E_{s-1} = Pi_s E_s + X_s.  Each value goes to record [2] of the
-// segment it starts; the fold past the sequence's far end is not needed.  The next fold's Pi and X are loaded while
-// the current one is computed.
-__global__ void __launch_bounds__(256) chunk_walk_scan_kernel(const __grid_constant__ CbParams p)
+// One element (row i, column j) of a 64 x 64 column-group-major record (rec4)
+__device__ __forceinline__ float& rec_at(float* base, int i, int j) { return base[(64 * (j >> 2) + i) * 4 + (j & 3)]; }
+__device__ __forceinline__ float rec_at(const float* base, int i, int j)
+{
+    return base[(64 * (j >> 2) + i) * 4 + (j & 3)];
+}
+
+// The folds of a scan over segments, S <- Pi S + X, for one unit and the eight columns 8 blockIdx.y .. + 7 (the
+// columns of a state never mix): 256 threads, thread = row i = r >> 2, columns j, j + 1 (j = 8 blockIdx.y +
+// 2 (r & 3)), fp32 on the CUDA cores.  The next fold's Pi (this thread's four float4 of the shared tile) and X are
+// loaded while the current one is computed.  fold(s) gives fold s's Pi and X; emit(s, c0, c1) takes the value
+// entering step s (before its fold).
+template <typename PiOf, typename XOf, typename Emit>
+__device__ __forceinline__ void scan_columns(int nfold, int nemit, float& c0, float& c1, PiOf pi_of, XOf x_of,
+                                             Emit emit)
 {
     __shared__ __align__(16) float Pm[64][kAS];
-    __shared__ __align__(16) float Cm[64][kAS];
-    const bool rev = p.rev_only || blockIdx.y == 1;
-    const int dslot = p.rev_only ? 0 : (int)blockIdx.y;
-    const int u = blockIdx.x, r = threadIdx.x, i0 = 2 * (r >> 3), j0 = 8 * (r & 7);
-    const int P = p.nseg;
-    auto seg_of = [&](int t) { return rev ? P - 1 - t : t; };   // the t-th segment along the walk
-    float cur[2][8];
-    auto load_own = [&](const float* src, float (&dst)[2][8]) {
-#pragma unroll
-        for (int a = 0; a < 2; a++)
-#pragma unroll
-            for (int b = 0; b < 2; b++) {
-                const float4 t = *rec4(src, 0, i0 + a, j0 + 4 * b);
-                dst[a][4 * b] = t.x; dst[a][4 * b + 1] = t.y; dst[a][4 * b + 2] = t.z; dst[a][4 * b + 3] = t.w;
-            }
-    };
-    float4 pn[4];      // the next fold's Pi: float4 e of this thread's share of the shared tile
-    float xn[2][8];    // and its X at this thread's outputs
-    auto fetch = [&](int sg) {
-        const float* pim = seg_rec(p, dslot, u, sg, 1);
+    __shared__ float Cm[64][8];
+    const int r = threadIdx.x, i = r >> 2, jj = 2 * (r & 3);
+    float4 pn[4];
+    float xn0 = 0.f, xn1 = 0.f;
+    auto fetch = [&](int s) {
+        const float* pim = pi_of(s);
 #pragma unroll
         for (int e = 0; e < 4; e++) {
             const int f = r + 256 * e;
             pn[e] = *rec4(pim, 0, f & 63, 4 * (f >> 6));
         }
-        load_own(seg_rec(p, dslot, u, sg, 0), xn);
+        x_of(s, xn0, xn1);
     };
-    load_own(seg_rec(p, dslot, u, seg_of(0), 0), cur);
-    if (P > 2) fetch(seg_of(1));
-    for (int t = 1; t < P; t++) {
-        const int sg = seg_of(t);   // cur is this segment's true start
-        float* dst = seg_rec(p, dslot, u, sg, 2);
-#pragma unroll
-        for (int a = 0; a < 2; a++)
-#pragma unroll
-            for (int b = 0; b < 2; b++)
-                *rec4(dst, 0, i0 + a, j0 + 4 * b) = make_float4(cur[a][4 * b], cur[a][4 * b + 1], cur[a][4 * b + 2],
-                                                                cur[a][4 * b + 3]);
-        if (t == P - 1) break;
-        // cur <- Pi_sg cur + X_sg
+    if (nfold > 0) fetch(0);
+    for (int s = 0; s < nemit; s++) {
+        emit(s, c0, c1);
+        if (s >= nfold) break;
         __syncthreads();
 #pragma unroll
         for (int e = 0; e < 4; e++) {
             const int f = r + 256 * e;
             *reinterpret_cast<float4*>(&Pm[f & 63][4 * (f >> 6)]) = pn[e];
         }
-#pragma unroll
-        for (int a = 0; a < 2; a++) {
-            *reinterpret_cast<float4*>(&Cm[i0 + a][j0]) = make_float4(cur[a][0], cur[a][1], cur[a][2], cur[a][3]);
-            *reinterpret_cast<float4*>(&Cm[i0 + a][j0 + 4]) = make_float4(cur[a][4], cur[a][5], cur[a][6], cur[a][7]);
-        }
+        Cm[i][jj] = c0;
+        Cm[i][jj + 1] = c1;
         __syncthreads();
-        float nx[2][8];
-#pragma unroll
-        for (int a = 0; a < 2; a++)
-#pragma unroll
-            for (int e = 0; e < 8; e++) nx[a][e] = xn[a][e];
-        if (t + 1 < P - 1) fetch(seg_of(t + 1));
-#pragma unroll 4
+        float n0 = xn0, n1 = xn1;
+        if (s + 1 < nfold) fetch(s + 1);
+#pragma unroll 8
         for (int m = 0; m < 64; m++) {
-            const float p0 = Pm[i0][m], p1 = Pm[i0 + 1][m];
-            const float4 c0 = *reinterpret_cast<const float4*>(&Cm[m][j0]);
-            const float4 c1 = *reinterpret_cast<const float4*>(&Cm[m][j0 + 4]);
-            const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                nx[0][e] = fmaf(p0, cv[e], nx[0][e]);
-                nx[1][e] = fmaf(p1, cv[e], nx[1][e]);
-            }
+            const float pv = Pm[i][m];
+            n0 = fmaf(pv, Cm[m][jj], n0);
+            n1 = fmaf(pv, Cm[m][jj + 1], n1);
         }
-#pragma unroll
-        for (int a = 0; a < 2; a++)
-#pragma unroll
-            for (int e = 0; e < 8; e++) cur[a][e] = nx[a][e];
+        c0 = n0;
+        c1 = n1;
     }
+}
+
+// The scan over a unit's segments, one CTA of 256 threads per (unit, 8 columns, direction).  Forward: the first
+// segment started from h0, so its X is the true state entering the second; then S_{s+1} = Pi_s S_s + X_s.
+// Reverse: the last segment started from dh_T, so its X is the true adjoint leaving the one before; then
+// E_{s-1} = Pi_s E_s + X_s.  Each value goes to record [2] of the segment it starts; the fold past the sequence's
+// far end is not needed.
+__global__ void __launch_bounds__(256) chunk_walk_scan_kernel(const __grid_constant__ CbParams p)
+{
+    const bool rev = p.rev_only || blockIdx.z == 1;
+    const int dslot = p.rev_only ? 0 : (int)blockIdx.z;
+    const int u = blockIdx.x, r = threadIdx.x, i = r >> 2, j = 8 * blockIdx.y + 2 * (r & 3);
+    const int P = p.nseg;
+    auto seg_of = [&](int t) { return rev ? P - 1 - t : t; };   // the t-th segment along the walk
+    const float* x0 = seg_rec(p, dslot, u, seg_of(0), 0);
+    float c0 = rec_at(x0, i, j), c1 = rec_at(x0, i, j + 1);
+    // step t (1 .. P - 1) emits the start of segment seg_of(t); fold t - 1 + 1 = t uses segment seg_of(t)
+    scan_columns(
+        P - 2, P - 1, c0, c1, [&](int s) -> const float* { return seg_rec(p, dslot, u, seg_of(s + 1), 1); },
+        [&](int s, float& a, float& b) {
+            const float* xs = seg_rec(p, dslot, u, seg_of(s + 1), 0);
+            a = rec_at(xs, i, j);
+            b = rec_at(xs, i, j + 1);
+        },
+        [&](int s, float a, float b) {
+            float* dst = seg_rec(p, dslot, u, seg_of(s + 1), 2);
+            rec_at(dst, i, j) = a;
+            rec_at(dst, i, j + 1) = b;
+        });
 }
 
 // ---------------------------------------------------------------- the forward split in time by walks (delta)
@@ -1856,97 +1855,31 @@ __global__ void __launch_bounds__(256) chunk_walk_scan_kernel(const __grid_const
 // o = o_zero-start + Qc_k D_k; for a saving forward, fwd_walk_res_kernel then makes the residuals true:
 // S_k += D_k, U_k += (-W_k) D_k.
 
-// The scan over a unit's segments, one CTA (256 threads) per unit, fp32 on the CUDA cores: thread = rows 2 (r >> 3),
-// + 1 x columns 8 (r & 7) .. + 7.  Xb: the zero-start run's final states [B * P, H, d_k, d_v] (segment view).
+// The forward's scan over a unit's segments, one CTA of 256 threads per (unit, 8 columns): S_0 = h0,
+// S_{s+1} = Pi_s S_s + X_s (X_s from Xb, the zero-start run's final states [B * P, H, d_k, d_v], segment view); each
+// S_s goes to record [2] of segment s, and S_P is h_T.
 __global__ void __launch_bounds__(256) fwd_walk_scan_kernel(const __grid_constant__ CbParams p, const float* Xb,
                                                             const float* h0, float* hT)
 {
-    __shared__ __align__(16) float Pm[64][kAS];
-    __shared__ __align__(16) float Cm[64][kAS];
-    const int u = blockIdx.x, r = threadIdx.x, i0 = 2 * (r >> 3), j0 = 8 * (r & 7);
+    const int u = blockIdx.x, r = threadIdx.x, i = r >> 2, j = 8 * blockIdx.y + 2 * (r & 3);
     const int P = p.nseg, dk = p.dk, dv = p.dv_, b = u / p.H, h = u - b * p.H;
-    float cur[2][8];
-#pragma unroll
-    for (int a = 0; a < 2; a++)
-#pragma unroll
-        for (int e = 0; e < 8; e++) {
-            const int i = i0 + a, j = j0 + e;
-            cur[a][e] = h0 && i < dk && j < dv ? h0[((size_t)u * dk + i) * dv + j] : 0.f;
-        }
-    // fold s's Pi (this thread's four float4 of the shared tile) and X (its outputs), loaded a fold ahead
-    float4 pn[4];
-    float xn[2][8];
-    auto fetch = [&](int s) {
-        const float* pim = seg_rec(p, 0, u, s, 1);
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            const int f = r + 256 * e;
-            pn[e] = *rec4(pim, 0, f & 63, 4 * (f >> 6));
-        }
-        const float* xs = Xb + ((size_t)(b * P + s) * p.H + h) * dk * dv;
-#pragma unroll
-        for (int a = 0; a < 2; a++)
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const int i = i0 + a, j = j0 + e;
-                xn[a][e] = i < dk && j < dv ? xs[i * dv + j] : 0.f;
-            }
-    };
-    const int folds = hT ? P : P - 1;   // the last fold only gives h_T
-    if (folds > 0) fetch(0);
-    for (int s = 0; s < P; s++) {
-        float* dst = seg_rec(p, 0, u, s, 2);   // segment s starts from cur
-#pragma unroll
-        for (int a = 0; a < 2; a++)
-#pragma unroll
-            for (int c = 0; c < 2; c++)
-                *rec4(dst, 0, i0 + a, j0 + 4 * c) = make_float4(cur[a][4 * c], cur[a][4 * c + 1], cur[a][4 * c + 2],
-                                                                cur[a][4 * c + 3]);
-        if (s >= folds) break;
-        // cur <- Pi_s cur + X_s
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            const int f = r + 256 * e;
-            *reinterpret_cast<float4*>(&Pm[f & 63][4 * (f >> 6)]) = pn[e];
-        }
-#pragma unroll
-        for (int a = 0; a < 2; a++) {
-            *reinterpret_cast<float4*>(&Cm[i0 + a][j0]) = make_float4(cur[a][0], cur[a][1], cur[a][2], cur[a][3]);
-            *reinterpret_cast<float4*>(&Cm[i0 + a][j0 + 4]) = make_float4(cur[a][4], cur[a][5], cur[a][6], cur[a][7]);
-        }
-        __syncthreads();
-        float nx[2][8];
-#pragma unroll
-        for (int a = 0; a < 2; a++)
-#pragma unroll
-            for (int e = 0; e < 8; e++) nx[a][e] = xn[a][e];
-        if (s + 1 < folds) fetch(s + 1);
-#pragma unroll 4
-        for (int m = 0; m < 64; m++) {
-            const float p0 = Pm[i0][m], p1 = Pm[i0 + 1][m];
-            const float4 c0 = *reinterpret_cast<const float4*>(&Cm[m][j0]);
-            const float4 c1 = *reinterpret_cast<const float4*>(&Cm[m][j0 + 4]);
-            const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                nx[0][e] = fmaf(p0, cv[e], nx[0][e]);
-                nx[1][e] = fmaf(p1, cv[e], nx[1][e]);
-            }
-        }
-#pragma unroll
-        for (int a = 0; a < 2; a++)
-#pragma unroll
-            for (int e = 0; e < 8; e++) cur[a][e] = nx[a][e];
-    }
+    auto at = [&](const float* m, int jj) { return i < dk && jj < dv ? m[((size_t)u * dk + i) * dv + jj] : 0.f; };
+    float c0 = h0 ? at(h0, j) : 0.f, c1 = h0 ? at(h0, j + 1) : 0.f;
+    scan_columns(
+        hT ? P : P - 1, P, c0, c1, [&](int s) -> const float* { return seg_rec(p, 0, u, s, 1); },
+        [&](int s, float& a, float& bv) {
+            const float* xs = Xb + ((size_t)(b * P + s) * p.H + h) * dk * dv;
+            a = i < dk && j < dv ? xs[i * dv + j] : 0.f;
+            bv = i < dk && j + 1 < dv ? xs[i * dv + j + 1] : 0.f;
+        },
+        [&](int s, float a, float bv) {
+            float* dst = seg_rec(p, 0, u, s, 2);
+            rec_at(dst, i, j) = a;
+            rec_at(dst, i, j + 1) = bv;
+        });
     if (hT) {
-#pragma unroll
-        for (int a = 0; a < 2; a++)
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const int i = i0 + a, j = j0 + e;
-                if (i < dk && j < dv) hT[((size_t)u * dk + i) * dv + j] = cur[a][e];
-            }
+        if (i < dk && j < dv) hT[((size_t)u * dk + i) * dv + j] = c0;
+        if (i < dk && j + 1 < dv) hT[((size_t)u * dk + i) * dv + j + 1] = c1;
     }
 }
 
@@ -3168,7 +3101,7 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
         // the chain as walks: the two sweeps side by side; split in time, a first walk per segment and a scan
         if (p.nseg > 1) {
             chunk_chain_walk_kernel<true><<<dim3(units, p.nseg - 1, dirs), CT_THREADS, walk_smem(true), st>>>(p);
-            chunk_walk_scan_kernel<<<dim3(units, dirs), 256, 0, st>>>(p);
+            chunk_walk_scan_kernel<<<dim3(units, 8, dirs), 256, 0, st>>>(p);
         }
         chunk_chain_walk_kernel<false><<<dim3(units, p.nseg, dirs), CT_THREADS, walk_smem(false), st>>>(p);
     } else if (delta) {
@@ -3255,7 +3188,7 @@ cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, int P, cudaStrea
     // 3. each segment's transition
     fwd_walk_kernel<false><<<dim3(units, P), CT_THREADS, FW_SMEM, st>>>(p);
     // 4. the segments' true starting states, and h_T
-    fwd_walk_scan_kernel<<<units, 256, 0, st>>>(p, Xb, a.h0, a.hT);
+    fwd_walk_scan_kernel<<<dim3(units, 8), 256, 0, st>>>(p, Xb, a.h0, a.hT);
     // 5. D = T_k S_s through every segment, and the outputs o = o_zero-start + Qc D
     fwd_walk_kernel<true><<<dim3(units, P), CT_THREADS, FW_SMEM, st>>>(p);
     // 6. a saving forward's residuals made true
