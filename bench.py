@@ -130,13 +130,14 @@ def tsplit_factor(w, backward):
     return plan(w, backward).segments
 
 
-def fwd_launches(w):
-    """Kernels one gdn_fwd call launches."""
+def fwd_launches(w, saving=False):
+    """Kernels one gdn_fwd call (gdn_fwd_save if saving) launches."""
     if tsplit_factor(w, False) == 1:
         return 1
     if w.mode == "delta" and saved_bytes(w) > 0:
-        # the split by walks: zero-start run, Phi, transition walks, scan, walks of T_k S_s, fix-up
-        return 6
+        # the split by walks: zero-start run, Phi and Qc, transition walks, scan, output walks (and, saving, the
+        # residuals' fix-up)
+        return 6 if saving else 5
     return 5 if w.mode == "delta" else 3   # zero-start run, (identity, transition run), scan, output kernel
 
 
@@ -600,7 +601,7 @@ def main():
                   "calls": "gdn_fwd_save + gdn_bwd_saved" if n_saved else "gdn_fwd + gdn_bwd",
                   "saved_bytes": n_saved,
                   "roofline": roofline_of(fb_bytes, fb_flops, fb_ms, peaks, peak_kind)}
-        gpu_launches += (fwd_launches(w) + bwd_launches(w, saved=bool(n_saved))) * kb
+        gpu_launches += (fwd_launches(w, saving=bool(n_saved)) + bwd_launches(w, saved=bool(n_saved))) * kb
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

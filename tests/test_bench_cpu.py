@@ -18,7 +18,7 @@ from linear_attention_recurrence_delta_gb300 import inputs as I  # noqa: E402
     ("delta_bf16_8x16x4096x64", "fwd_tc_kernel<delta>", 1, 4),    # chunked backward: prep, chain, grads, dA_log
     ("gated_bf16_8x16x4096x56_bwd", "fwd_tc_kernel<gated>", 1, 4),
     # forward: the time split by walks; backward: the chain in 4 segments (first walks, scan, second walks)
-    ("delta_bf16_1x16x32768x64_bwd", "fwd_tc_kernel<delta>", 6, 6),
+    ("delta_bf16_1x16x32768x64_bwd", "fwd_tc_kernel<delta>", 5, 6),
     ("delta_bf16_8x40x4096x32", "serial_fwd_kernel<bf16, delta>", 1, 4),       # narrow heads, 320 units
     ("delta_bf16_8x16x4096x128", "serial_fwd_kernel<bf16, delta>", 1, 6),      # 4 slabs: + sums of db, dc, dg, dbeta
     ("delta_bf16_decode_512x16x1x64", "decode_kernel", 1, 4),
@@ -36,6 +36,7 @@ def test_split_chain_launches_from_residuals():
     w = I.WORKLOADS["delta_bf16_1x16x32768x64_bwd"]
     assert bench.plan(w, True).segments == 4 and bench.plan(w, 2).segments == 9
     assert bench.bwd_launches(w, saved=True) == 6
+    assert bench.fwd_launches(w, saving=True) == 6   # the saving forward adds the residuals' fix-up
     assert bench.bwd_launches(I.WORKLOADS["delta_bf16_8x16x4096x64"], saved=True) == 4
 
 
