@@ -39,8 +39,6 @@ struct TcParams {
     unsigned char* sv;       // saving forward: the solve's results per chunk
     uint32_t sv_stride;      // saving forward: bytes per chunk of sv
     int seg;                 // saving forward on a time split's segment view: segments per sequence (else 1)
-    int sv_lite;             // saving forward: P and -W only (what the time split's walks need), no states,
-                             // K, Dinv, -N or U
 };
 
 // Limit of a bounded wait: a chunk's loads or products take microseconds, so two

@@ -229,6 +229,20 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 __device__ __forceinline__ float* fptr(unsigned char* base, uint32_t off) { return reinterpret_cast<float*>(base + off); }
 
+// The sum of 64 values x[s * stride] in a fixed order: four chains over s = 4 m + c, then (c0 + c1) + (c2 + c3)
+__device__ __forceinline__ float sum64_fixed(const float* x, int stride)
+{
+    float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll 4
+    for (int m = 0; m < 16; m++) {
+        c0 += x[(4 * m) * stride];
+        c1 += x[(4 * m + 1) * stride];
+        c2 += x[(4 * m + 2) * stride];
+        c3 += x[(4 * m + 3) * stride];
+    }
+    return (c0 + c1) + (c2 + c3);
+}
+
 // 4 bf16 of row `row`, columns col .. col + 3 (col a multiple of 4) of a swizzled tile, as fp32: one 8-byte load
 __device__ __forceinline__ void ld4_bf16(const unsigned char* tile, int row, int col, float (&v)[4])
 {
@@ -2506,16 +2520,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             const int I = tt >> 4;
             const float bet = DELTA ? S.beta[tt] : 0.f;
             float row[64];
+            {
+                // the row's 64 columns in one TMEM round trip
+                float v[4][16];
 #pragma unroll
-            for (int g4 = 0; g4 < 4; g4++) {
-                float v[16];
-                tmem_ld16(c.tl + 16 * g4, v);
+                for (int g4 = 0; g4 < 4; g4++) tmem_ld16(c.tl + 16 * g4, v[g4]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; e++) {
-                    const int s = 16 * g4 + e;
-                    row[s] = isK ? ((DELTA && s < tt) ? -bet * v[e] : 0.f) : (s <= tt ? v[e] : 0.f);
-                }
+                for (int g4 = 0; g4 < 4; g4++)
+#pragma unroll
+                    for (int e = 0; e < 16; e++) {
+                        const int s = 16 * g4 + e;
+                        row[s] = isK ? ((DELTA && s < tt) ? -bet * v[g4][e] : 0.f) : (s <= tt ? v[g4][e] : 0.f);
+                    }
             }
             if (DELTA && isK) {
                 // dbeta_t = sum_j dR V - sum_i Btil (dR S^T) - sum_{s<t} (dR U^T) K   (dMm = -dR U^T)
@@ -2869,10 +2886,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 }
             }
         } else if (c.r < 64) {
-            // column sums over tokens of dBhat Bhat (fixed order)
-            float acc = 0.f;
-            for (int s = 0; s < 64; s++) acc += PB[s * gl::kES + c.r];
-            S.colsum[0][c.r] = acc;
+            // column sums over tokens of dBhat Bhat (fixed order: four interleaved chains, then their sum)
+            S.colsum[0][c.r] = sum64_fixed(PB + c.r, gl::kES);
         }
         if (DELTA && c.r >= 128 && c.r < 192) {
             // dbeta of the chunk's tokens (both column halves of every part)
@@ -2956,11 +2971,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             if (t2 < L) p.dg[((size_t)bb * p.T + t0 + t2) * p.H + h] = __float2bfloat16_rn(dg0);
             if (t2 + 1 < L) p.dg[((size_t)bb * p.T + t0 + t2 + 1) * p.H + h] = __float2bfloat16_rn(dg1);
         } else if (c.r >= 64 && c.r < 128) {
-            // dA partial: sum_t G_t dGam_t[i] (fixed order)
+            // dA partial: sum_t G_t dGam_t[i] (fixed order: four interleaved chains, then their sum)
             const int i = c.r - 64;
-            float acc = 0.f;
-            for (int s = 0; s < 64; s++) acc += PB[s * gl::kES + i];
-            p.dA_part[(size_t)q * 64 + i] = acc;
+            p.dA_part[(size_t)q * 64 + i] = sum64_fixed(PB + i, gl::kES);
         }
         CB_STAMP(1, 13);
         // the stage is free: the next chunk's loads

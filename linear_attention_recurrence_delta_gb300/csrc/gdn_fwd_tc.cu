@@ -164,23 +164,26 @@ __device__ __forceinline__ void zero_chunk(unsigned char* tile, int row, int q)
 namespace svr {
 constexpr uint32_t P = 0, NA = 16384, DINV = 24576, K = 32768, NW = 49152, NWL = 57344, U = 65536, BYTES = 81920;
 constexpr uint32_t GATED_BYTES = 16384;   // gated: P only
-// the record index of chunk k of unit u: u * nchunks + k, or, on the segment view of a time split (p.seg
+// the record index of chunk k of unit u: u * nchunks + k, or, on the segment view of a time split (SEG: p.seg
 // segments of a sequence as batch rows b' = b * seg + s), the index of that chunk in the whole sequence
+template <bool SEG>
 __device__ __forceinline__ size_t rec_index(const TcParams& p, int u, int k)
 {
-    if (p.seg <= 1) return (size_t)u * p.nchunks + k;
+    if (!SEG) return (size_t)u * p.nchunks + k;
     const int bs = u / p.H, h = u - bs * p.H, b = bs / p.seg, s = bs - b * p.seg;
     return (((size_t)b * p.H + h) * p.seg + s) * p.nchunks + k;
 }
+template <bool SEG>
 __device__ __forceinline__ unsigned char* rec(const TcParams& p, int u, int k)
 {
-    return p.sv + rec_index(p, u, k) * p.sv_stride;
+    return p.sv + rec_index<SEG>(p, u, k) * p.sv_stride;
 }
 // state row `row`, columns 32 wh .. 32 wh + 31; the record is column-group major (the float4 of row r, columns
 // 4 g .. 4 g + 3 at index 64 g + r), so a warp's 32 rows write 512 contiguous bytes
+template <bool SEG>
 __device__ __forceinline__ void put_state(const TcParams& p, int u, int k, int row, int wh, const float (&v)[32])
 {
-    float4* d = reinterpret_cast<float4*>(p.st + rec_index(p, u, k) * 4096) + (8 * wh) * 64 + row;
+    float4* d = reinterpret_cast<float4*>(p.st + rec_index<SEG>(p, u, k) * 4096) + (8 * wh) * 64 + row;
 #pragma unroll
     for (int e = 0; e < 8; e++) d[64 * e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
 }
@@ -200,14 +203,22 @@ __device__ __forceinline__ const float* ktab(const unsigned char* sm, int tab, i
     return reinterpret_cast<const float*>(sm + OFF_K) + (tab * 8 + k8) * 64;
 }
 
+// What a forward keeps for the chunked backward: nothing; the residuals of one pass; those of a time split's
+// segment view (laid out by the chunks of the whole sequence); or only P and -W of them (what the split's walks read)
+enum SaveMode { SAVE_NONE = 0, SAVE_FULL = 1, SAVE_SPLIT = 2, SAVE_SPLIT_LITE = 3 };
+
 // NORM: b and c arrive before their L2 normalisation (a template flag, so the plain kernel carries no trace of it).
-// SAVE (one 64-column slab): the residuals of the chunked backward are written as well, per chunk q of the unit:
+// SAVE (one 64-column slab; a SaveMode): the residuals of the chunked backward are written as well, per chunk q of
+// the unit:
 // the entering state (p.st, fp32 64 x 64, column-group major) and, in the layout of namespace svr, the delta
 // solve's results (gated: P).  In delta mode the b-side level operands then leave beta out, so that the level
 // products give K itself (M = beta K is formed when it is assembled).
-template <bool DELTA, bool NORM, bool SAVE>
+template <bool DELTA, bool NORM, int SAVEM>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ TcParams p)
 {
+    constexpr bool SAVE = SAVEM != SAVE_NONE;
+    constexpr bool LITE = SAVEM == SAVE_SPLIT_LITE;                        // P and -W only
+    constexpr bool SEG = SAVEM == SAVE_SPLIT || SAVEM == SAVE_SPLIT_LITE;  // records of the whole sequence
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char* X = sm + OFF_X;
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
                 st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
             }
-            if (SAVE && !p.sv_lite) svr::put_state(p, u, 0, trow, wh, Sreg);
+            if (SAVE && !LITE) svr::put_state<SEG>(p, u, 0, trow, wh, Sreg);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, kMath);
@@ -310,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
                     st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
                 }
-                if (SAVE && !p.sv_lite && kk + 1 < p.nchunks) svr::put_state(p, u, kk + 1, trow, wh, Sreg);
+                if (SAVE && !LITE && kk + 1 < p.nchunks) svr::put_state<SEG>(p, u, kk + 1, trow, wh, Sreg);
             } else {
                 const int tg = kk * kC + (trow - 64);
                 const size_t orow_at = (((size_t)bb * T + tg) * H + h) * dv + jc0;
@@ -700,9 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         }
                         if (SAVE && isM) {
                             // the level products gave K (zero on and above the diagonal): a residual; M = beta K
-                            float4* kr = reinterpret_cast<float4*>(svr::rec(p, u, k) + svr::K) + (4 * cg) * 64 + t;
+                            float4* kr = reinterpret_cast<float4*>(svr::rec<SEG>(p, u, k) + svr::K) + (4 * cg) * 64 + t;
                             const float bet = S.beta[s][t];
-                            if (!p.sv_lite) {
+                            if (!LITE) {
 #pragma unroll
                                 for (int e = 0; e < 4; e++)
                                     kr[64 * e] = make_float4(out[4 * e], out[4 * e + 1], out[4 * e + 2], out[4 * e + 3]);
@@ -713,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (!isM) {
                             st_split16(sm + OFF_CH0, sm + OFF_CH0L, 64 + t, cg, out);
                             if (SAVE) {
-                                unsigned char* pr = svr::rec(p, u, k) + svr::P;
+                                unsigned char* pr = svr::rec<SEG>(p, u, k) + svr::P;
                                 st_split16(pr, pr + 8192, t, cg, out);
                             }
                         } else {
@@ -877,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             v16[c] = x.x; v16[c + 1] = x.y; v16[c + 2] = x.z; v16[c + 3] = x.w;
                         }
                         st_plain16(X + X_DINV, trow, cg, v16);
-                        if (SAVE && !p.sv_lite && trow < 64) st_plain16(svr::rec(p, u, k) + svr::DINV, trow, cg, v16);
+                        if (SAVE && !LITE && trow < 64) st_plain16(svr::rec<SEG>(p, u, k) + svr::DINV, trow, cg, v16);
                     }
                 }
                 smem_to_tc();
@@ -909,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                             for (int c = 0; c < 16; c++) v[c] = -v[c];
                             st_plain16(X + X_NA, t, g, v);
-                            if (SAVE && !p.sv_lite) st_plain16(svr::rec(p, u, k) + svr::NA, t, g, v);
+                            if (SAVE && !LITE) st_plain16(svr::rec<SEG>(p, u, k) + svr::NA, t, g, v);
                         } else {
                             const int xg = g - 4;
                             const uint32_t blk = (uint32_t)(xg >> 2) * 8192u;
@@ -974,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         for (int c = 0; c < 16; c++) v[c] = -v[c];
                         st_plain16(X + X_CW, trow, cg, v);
                         if (SAVE) {
-                            unsigned char* rq = svr::rec(p, u, k);
+                            unsigned char* rq = svr::rec<SEG>(p, u, k);
                             st_split16(rq + svr::NW, rq + svr::NWL, trow, cg, v);
                         }
                     }
@@ -1000,9 +1011,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         tmem_ld16(tl + TM_U + 16 * cg, v);
                         tmem_wait_ld();
                         st_split16(X + X_UH, X + X_UL, trow, cg, v);
-                        if (SAVE && !p.sv_lite) {
+                        if (SAVE && !LITE) {
                             // U itself (the state already folded in) is a residual
-                            float4* du = reinterpret_cast<float4*>(svr::rec(p, u, k) + svr::U) + (4 * cg) * 64 + trow;
+                            float4* du = reinterpret_cast<float4*>(svr::rec<SEG>(p, u, k) + svr::U) + (4 * cg) * 64 + trow;
 #pragma unroll
                             for (int e = 0; e < 4; e++)
                                 du[64 * e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
@@ -1057,17 +1068,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (warp == 0) tmem_dealloc(tbase, TM_COLS);
 }
 
-template <bool DELTA, bool NORM, bool SAVE = false>
+template <bool DELTA, bool NORM, int SAVEM = SAVE_NONE>
 cudaError_t launch_t(const TcParams& p, dim3 grid, cudaStream_t st)
 {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<DELTA, NORM, SAVE>,
+        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<DELTA, NORM, SAVEM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    fwd_tc_kernel<DELTA, NORM, SAVE><<<grid, kThreads, SMEM_BYTES, st>>>(p);
+    fwd_tc_kernel<DELTA, NORM, SAVEM><<<grid, kThreads, SMEM_BYTES, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -1105,11 +1116,13 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
         if (a.dv > 64 || a.norm || a.logits) return cudaErrorInvalidValue;
         const size_t nq = (size_t)a.B * a.H * p.nchunks;
         p.seg = a.seg > 1 ? a.seg : 1;
-        p.sv_lite = a.save_lite;
         p.st = (float*)a.saved;
         p.sv = (unsigned char*)a.saved + nq * 16384;
         p.sv_stride = a.mode == GDN_DELTA ? svr::BYTES : svr::GATED_BYTES;
-        return a.mode == GDN_DELTA ? launch_t<true, false, true>(p, grid, st) : launch_t<false, false, true>(p, grid, st);
+        if (a.mode != GDN_DELTA) return p.seg > 1 ? cudaErrorInvalidValue : launch_t<false, false, SAVE_FULL>(p, grid, st);
+        if (p.seg <= 1) return launch_t<true, false, SAVE_FULL>(p, grid, st);
+        return a.save_lite ? launch_t<true, false, SAVE_SPLIT_LITE>(p, grid, st)
+                           : launch_t<true, false, SAVE_SPLIT>(p, grid, st);
     }
     if (a.norm)
         return a.mode == GDN_DELTA ? launch_t<true, true>(p, grid, st) : launch_t<false, true>(p, grid, st);
