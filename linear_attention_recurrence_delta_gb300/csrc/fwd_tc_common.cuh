@@ -38,7 +38,7 @@ struct TcParams {
     float* st;               // saving forward: the states entering the chunks
     unsigned char* sv;       // saving forward: the solve's results per chunk
     uint32_t sv_stride;      // saving forward: bytes per chunk of sv
-    int seg;                 // saving forward on a time split's segment view: segments per sequence (else 1)
+    int seg, seg_len;        // saving forward over a time split: segments per sequence (else 1), chunks each
 };
 
 // Limit of a bounded wait: a chunk's loads or products take microseconds, so two

@@ -82,7 +82,7 @@ static size_t place_tsplit(const gdn_shape_t& s, int P, bool backward, WsLayout&
 // buffers of the delta forward split in time by walks (see launch_fwd_walks), placed from `off`
 static size_t place_fwd_walks(const gdn_shape_t& s, int P, WsLayout& L, size_t off)
 {
-    const size_t units = (size_t)s.B * s.H, nq = units * (size_t)(s.T / 64);
+    const size_t units = (size_t)s.B * s.H, nq = units * (size_t)((s.T + 63) / 64);
     L.ts_h_off = off;
     off = round_up(off + units * P * s.dk * s.dv * sizeof(float), 256);
     L.ts_o_off = off;
@@ -159,7 +159,8 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm, int logits)
         L.total = place_chunk_bwd(s, L, off, backward == 2);
         return L;
     }
-    const int P = s.T > 0 ? (backward ? bwd_split(s, logits, norm) : tsplit_factor(s, 0)) : 1;
+    const int walks = backward || s.T <= 0 ? 1 : fwd_walk_split(s, logits, norm, nullptr);
+    const int P = s.T > 0 ? (backward ? bwd_split(s, logits, norm) : (walks > 1 ? walks : tsplit_factor(s, 0))) : 1;
     if (backward) {
         gdn_shape_t core = s;
         if (P > 1) {
@@ -168,7 +169,7 @@ WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm, int logits)
         }
         off = place_bwd_core(core, L, off, norm);
     }
-    if (P > 1 && !backward && fwd_walks_apply(s, P, logits, norm))
+    if (walks > 1)
         off = place_fwd_walks(s, P, L, off);
     else if (P > 1)
         off = place_tsplit(s, P, backward != 0, L, off);
@@ -289,8 +290,8 @@ static cudaError_t fwd_core(const Args& a, cudaStream_t st)
 static bool saved_applies(const gdn_shape_t& s, int logits, int norm)
 {
     if (!chunk_bwd_applies(s, logits, norm)) return false;
-    const int P = tsplit_factor(s, 0);
-    if (P > 1) return fwd_walks_apply(s, P, logits, norm);
+    if (fwd_walk_split(s, logits, norm, nullptr) > 1) return true;
+    if (tsplit_factor(s, 0) > 1) return false;
     return fwd_kernel_of(make_args(&s)) == GDN_KERNEL_TENSOR_CORE;
 }
 
@@ -312,12 +313,15 @@ extern "C" gdn_status_t gdn_plan(const gdn_shape_t* shape_in, int backward, gdn_
     if ((sh.mode != GDN_GATED && sh.mode != GDN_DELTA) || (sh.io != GDN_F32 && sh.io != GDN_BF16))
         return GDN_ERR_MODE;
     if (!shape_ok(sh)) return GDN_ERR_SHAPE;
-    const int P = sh.T > 0 ? (backward ? bwd_split(sh, logits, norm) : tsplit_factor(sh, 0)) : 1;
+    const int walks = backward || sh.T <= 0 ? 1 : fwd_walk_split(sh, logits, norm, nullptr);
+    const int P = sh.T > 0 ? (backward ? bwd_split(sh, logits, norm) : (walks > 1 ? walks : tsplit_factor(sh, 0))) : 1;
     Args a = make_args(&sh);   // the runs' view: P segments of one sequence are P batch rows
     a.B = sh.B * P;
     a.T = sh.T / P;
     plan->segments = P;
-    plan->fwd_kernel = (backward && P == 1) ? GDN_KERNEL_NONE : fwd_kernel_of(a);
+    plan->fwd_kernel = (backward && P == 1) ? GDN_KERNEL_NONE
+                       : walks > 1 ? GDN_KERNEL_TENSOR_CORE   // the split by walks runs the tcgen05 forward
+                                   : fwd_kernel_of(a);
     plan->bwd_kernel = !backward || sh.T <= 0 ? GDN_BWD_NONE
                        : chunk_bwd_applies(sh, logits, norm) ? GDN_BWD_TENSOR_CORE : GDN_BWD_SERIAL;
     if (plan->bwd_kernel == GDN_BWD_TENSOR_CORE)   // the chunked backward's chain, split in time for few heads
@@ -388,8 +392,8 @@ static gdn_status_t fwd_impl(const gdn_shape_t* shape_in, const void* v, const v
     }
     const int P = tsplit_factor(*shape, 0);
     cudaError_t e;
-    if (P > 1 && fwd_walks_apply(*shape, P, logits, norm))
-        e = launch_fwd_walks(a, ws_layout(*shape, 0, norm, logits), P, st);
+    if (fwd_walk_split(*shape, logits, norm, nullptr) > 1)
+        e = launch_fwd_walks(a, ws_layout(*shape, 0, norm, logits), st);
     else if (P > 1)
         e = launch_fwd_tsplit(a, ws_layout(*shape, 0, norm, logits), P, st, fwd_core);
     else

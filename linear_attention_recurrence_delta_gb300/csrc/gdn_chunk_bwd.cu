@@ -3135,23 +3135,25 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
 // The forward split in time by walks (fwd_walks_apply): the zero-start saving run over the segment view, Phi per
 // chunk, the transition walks, the scan over segments (with h_T), the walks of D = T_k S_s, the fix-up.  The
 // residuals go to a.saved (a saving forward, made true by the fix-up) or to the workspace.
-cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, int P, cudaStream_t st)
+cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, cudaStream_t st)
 {
     unsigned char* ws = (unsigned char*)a.ws;
     unsigned char* res = a.saved ? (unsigned char*)a.saved : ws + Lw.fw_res_off;
     float* Xb = (float*)(ws + Lw.ts_h_off);
     float* o32 = (float*)(ws + Lw.ts_o_off);
-    const int nk = a.T / 64, units = a.B * a.H;
-    if (a.T % (64 * P) != 0 || P < 2) return cudaErrorInvalidValue;
+    gdn_shape_t sh = {a.B, a.H, a.T, a.dk, a.dv, a.mode, a.io};
+    int L = 0;
+    const int P = fwd_walk_split(sh, a.logits, a.norm, &L);
+    const int nk = (a.T + 63) / 64, units = a.B * a.H;
+    if (P < 2) return cudaErrorInvalidValue;
     // 1. every segment from a zero state, keeping the residuals (states entering the chunks, from zero)
     Args r = a;
-    r.B = a.B * P;
-    r.T = a.T / P;
     r.h0 = nullptr;
     r.hT = Xb;
     r.o32 = o32;
     r.saved = res;
     r.seg = P;
+    r.seg_len = L;
     r.save_lite = a.saved ? 0 : 1;   // without a caller's residuals the walks need P and -W alone
     bool handled = false;
     cudaError_t e = launch_fwd_tc(r, st, &handled);
@@ -3174,7 +3176,7 @@ cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, int P, cudaStrea
     p.nq = units * nk;
     p.sv_stride = sv::BYTES;
     p.nseg = P;
-    p.seg_len = nk / P;
+    p.seg_len = L;
     p.segrec = (float*)(ws + Lw.cb_seg_off);
     p.fwd_walks = 1;
     p.fw_o32 = o32;

@@ -164,14 +164,14 @@ __device__ __forceinline__ void zero_chunk(unsigned char* tile, int row, int q)
 namespace svr {
 constexpr uint32_t P = 0, NA = 16384, DINV = 24576, K = 32768, NW = 49152, NWL = 57344, U = 65536, BYTES = 81920;
 constexpr uint32_t GATED_BYTES = 16384;   // gated: P only
-// the record index of chunk k of unit u: u * nchunks + k, or, on the segment view of a time split (SEG: p.seg
-// segments of a sequence as batch rows b' = b * seg + s), the index of that chunk in the whole sequence
+// the record index of chunk k of unit u: u * nchunks + k, or, for the segments of a time split (SEG: unit
+// u = (b * seg + s) * H + h runs chunks s * seg_len .. of (b, h)), the index of that chunk in the whole sequence
 template <bool SEG>
 __device__ __forceinline__ size_t rec_index(const TcParams& p, int u, int k)
 {
     if (!SEG) return (size_t)u * p.nchunks + k;
     const int bs = u / p.H, h = u - bs * p.H, b = bs / p.seg, s = bs - b * p.seg;
-    return (((size_t)b * p.H + h) * p.seg + s) * p.nchunks + k;
+    return ((size_t)b * p.H + h) * p.nchunks + (size_t)s * p.seg_len + k;
 }
 template <bool SEG>
 __device__ __forceinline__ unsigned char* rec(const TcParams& p, int u, int k)
@@ -224,7 +224,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     unsigned char* X = sm + OFF_X;
     Small& S = *reinterpret_cast<Small*>(sm + OFF_SMALL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int u = blockIdx.x, bb = u / p.H, h = u % p.H;
+    const int u = blockIdx.x;
+    // the unit's (batch, head) and its chunks: all of them, or (SEG) segment s of a time split, chunks
+    // kbase .. kbase + nck - 1 of the sequence (the last segment may be shorter, its last chunk ragged)
+    int bb, h, kbase = 0, nck = p.nchunks;
+    if constexpr (SEG) {
+        const int bs = u / p.H, sgi = bs % p.seg;
+        h = u - bs * p.H;
+        bb = bs / p.seg;
+        kbase = sgi * p.seg_len;
+        nck = min(p.seg_len, p.nchunks - kbase);
+    } else {
+        bb = u / p.H;
+        h = u % p.H;
+    }
     const int T = p.T, H = p.H, dk = p.dk, dv = p.dv;
     // value columns jc0 .. jc0 + nv - 1 of the unit (columns of the state never mix, so wider values are
     // split in 64-column slabs over blockIdx.y; the slabs repeat the decay and solve work of the keys)
@@ -247,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     // g (and beta) of the first chunks
     for (int k = 0; k < kStages; k++)
         if (tid < kC) {
-            const int t = k * kC + tid;
+            const int t = (kbase + k) * kC + tid;
             const size_t row = ((size_t)bb * T + t) * H + h;
             S.g[k][tid] = t < T ? gate_in(__bfloat162float(p.g[row]), p.logits) : 0.f;
             if (DELTA) S.beta[k][tid] = t < T ? gate_in(__bfloat162float(p.beta[row]), p.logits) : 0.f;
@@ -266,13 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const int s = k % kStages;
         unsigned char* st = sm + OFF_RING + s * STAGE_BYTES;
         mbar_arrive_expect_tx(&S.full[s], STAGE_BYTES);
-        tma_load_4d(st, &p.tm_v, &S.full[s], jc0, h, k * kC, bb);
-        tma_load_4d(st + 8192, &p.tm_b, &S.full[s], 0, h, k * kC, bb);
-        tma_load_4d(st + 16384, &p.tm_c, &S.full[s], 0, h, k * kC, bb);
+        tma_load_4d(st, &p.tm_v, &S.full[s], jc0, h, (kbase + k) * kC, bb);
+        tma_load_4d(st + 8192, &p.tm_b, &S.full[s], 0, h, (kbase + k) * kC, bb);
+        tma_load_4d(st + 16384, &p.tm_c, &S.full[s], 0, h, (kbase + k) * kC, bb);
     };
     int issued = 0;
     if (tid == 0)
-        for (; issued < kStages && issued < p.nchunks; issued++) issue_load(issued);
+        for (; issued < kStages && issued < nck; issued++) issue_load(issued);
 
     {
         // ---------------------------------------------------------- math
@@ -321,9 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     for (int e = 0; e < 8; e++) v8[e] = Sreg[8 * q + e];
                     st_row8_split(sm + OFF_S, sm + OFF_SL, trow, 4 * wh + q, v8);
                 }
-                if (SAVE && !LITE && kk + 1 < p.nchunks) svr::put_state<SEG>(p, u, kk + 1, trow, wh, Sreg);
+                if (SAVE && !LITE && kk + 1 < nck) svr::put_state<SEG>(p, u, kk + 1, trow, wh, Sreg);
             } else {
-                const int tg = kk * kC + (trow - 64);
+                const int tg = (kbase + kk) * kC + (trow - 64);
                 const size_t orow_at = (((size_t)bb * T + tg) * H + h) * dv + jc0;
                 __nv_bfloat16* orow = p.o + orow_at;
 #pragma unroll
@@ -440,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         // (delta) or output product (gated)
         prep_all(0);
         named_bar_sync(1, kMath);
-        for (int k = 0; k < p.nchunks; k++) {
+        for (int k = 0; k < nck; k++) {
             const int s = k % kStages;
             if (warp == 0) wait_or_abort(&S.full[s], (k / kStages) & 1, &S.abort, p.status, p.wait_ns);
             named_bar_sync(1, kMath);
@@ -451,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // g, beta of chunk k + kStages (threads 0..63), kept as raw bf16 until they are stored so that
             // nothing waits on the loads inside the chunk
             __nv_bfloat16 g_next = __float2bfloat16(0.f), beta_next = __float2bfloat16(0.f);
-            if (r < kC && k + kStages < p.nchunks) {
-                const int t = (k + kStages) * kC + r;
+            if (r < kC && k + kStages < nck) {
+                const int t = (kbase + k + kStages) * kC + r;
                 const size_t row = ((size_t)bb * T + t) * H + h;
                 if (t < T) {
                     g_next = p.g[row];
@@ -794,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 // meanwhile warps 2, 3, 6, 7: the next chunk's scan and constants (G and the tables are the
                 // current chunk's no longer: both were last read before this product)
-                if ((warp & 2) && k + 1 < p.nchunks) prep_idle(k + 1);
+                if ((warp & 2) && k + 1 < nck) prep_idle(k + 1);
                 if (!mma_wait_all()) break;
             } else {
                 named_bar_sync(1, kMath);
@@ -867,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             Eb[(q0 + kq) * kBS + c] = -x;
                         }
                     }
-                } else if ((warp & 2) && k + 1 < p.nchunks) {
+                } else if ((warp & 2) && k + 1 < nck) {
                     prep_idle(k + 1);   // meanwhile warps 2, 3, 6, 7: the next chunk's scan and constants
                 }
                 named_bar_sync(1, kMath);
@@ -1038,12 +1051,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             pending = k;   // its state update and outputs run under the next chunk's level products
             smem_to_tc();
             // stage s is free again (every read of it, and the last MMA, are done)
-            if (k + kStages < p.nchunks) {
+            if (k + kStages < nck) {
                 if (r < kC) {
                     // (the sigmoid of a logit is taken here, where the loaded value is first used,
                     // so the load's latency stays hidden behind the chunk)
                     // tokens past T keep g = beta = 0 (an identity step)
-                    const bool tok = (k + kStages) * kC + r < T;
+                    const bool tok = (kbase + k + kStages) * kC + r < T;
                     S.g[s][r] = tok ? gate_in(__bfloat162float(g_next), p.logits) : 0.f;
                     if (DELTA) S.beta[s][r] = tok ? gate_in(__bfloat162float(beta_next), p.logits) : 0.f;
                 }
@@ -1109,13 +1122,15 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
     p.starve_chunk = test_starve_chunk();
     p.wait_ns = p.starve_chunk >= 0 ? kTestWaitNs : kWaitNs;
     *handled = true;
-    const dim3 grid(a.B * a.H, (a.dv + 63) / 64);
+    const int nseg = a.saved && a.seg > 1 ? a.seg : 1;
+    const dim3 grid(a.B * a.H * nseg, (a.dv + 63) / 64);
     if (a.saved) {
         // the residuals of the chunked backward: one slab, no option bits (the host checks); on a time split's
         // segment view (a.seg segments per sequence) they are laid out by the chunks of the whole sequence
         if (a.dv > 64 || a.norm || a.logits) return cudaErrorInvalidValue;
         const size_t nq = (size_t)a.B * a.H * p.nchunks;
-        p.seg = a.seg > 1 ? a.seg : 1;
+        p.seg = nseg;
+        p.seg_len = a.seg_len;
         p.st = (float*)a.saved;
         p.sv = (unsigned char*)a.saved + nq * 16384;
         p.sv_stride = a.mode == GDN_DELTA ? svr::BYTES : svr::GATED_BYTES;

@@ -29,7 +29,7 @@ struct Args {
     float* dh0;
     // residuals of the chunked backward (delta): a saving forward writes them, the backward reads them
     void* saved;
-    int seg;               // a saving run over a time split's segment view: segments per sequence (else 0 or 1)
+    int seg, seg_len;      // a saving run over a time split: segments per sequence (else 0 or 1), chunks each
     int save_lite;         // a saving run for the time split's walks alone: P and -W only
     // workspace
     void* ws;
@@ -98,11 +98,20 @@ inline bool chunk_bwd_applies(const gdn_shape_t& s, int logits, int norm)
 {
     return s.io == GDN_BF16 && s.T > 0 && s.dk <= 64 && s.dv <= 64 && !logits && !norm;
 }
-// The delta forward split in time into P segments runs as walks (launch_fwd_walks) when its segments are whole
-// chunks and the tcgen05 forward with residuals applies (bf16, heads up to 64 wide, no option bits).
-inline bool fwd_walks_apply(const gdn_shape_t& s, int P, int logits, int norm)
+// The delta forward split in time by walks (launch_fwd_walks): bf16, heads up to 64 wide, no option bits, few
+// heads.  P segments of *seg_len chunks of 64 tokens (the last one may be shorter, its last chunk ragged), sized like
+// the other time split (B * H * P <= 152, P >= 4, at least 512 tokens each) but for any length.  Returns P (1: no
+// split by walks).
+inline int fwd_walk_split(const gdn_shape_t& s, int logits, int norm, int* seg_len)
 {
-    return P > 1 && s.mode == GDN_DELTA && chunk_bwd_applies(s, logits, norm) && s.T % (64 * P) == 0;
+    if (s.mode != GDN_DELTA || !chunk_bwd_applies(s, logits, norm)) return 1;
+    const long units = (long)s.B * s.H, nk = (s.T + 63) / 64;
+    long P = kSplitSMs / units;
+    if (P > nk / 8) P = nk / 8;
+    if (P < 4) return 1;
+    const long L = (nk + P - 1) / P;
+    if (seg_len) *seg_len = (int)L;
+    return (int)((nk + L - 1) / L);
 }
 // The chunked backward's chain split in time (delta only; gated chains are elementwise and cheap): its `dirs`
 // sweeps (2, or 1 from the forward's residuals) over `units` (batch, head) units run as dirs * units * nseg walks
@@ -135,7 +144,7 @@ cudaError_t launch_serial_bwd(const Args& a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled);
 cudaError_t launch_decode(const Args& a, cudaStream_t st);   // 1 <= T <= decode_max_tokens()
 cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& L, cudaStream_t st);   // chunk_bwd_applies()
-cudaError_t launch_fwd_walks(const Args& a, const WsLayout& L, int P, cudaStream_t st);   // fwd_walks_apply()
+cudaError_t launch_fwd_walks(const Args& a, const WsLayout& L, cudaStream_t st);   // fwd_walk_split() > 1
 int tsplit_factor(const gdn_shape_t& s, int backward);   // segments P of a time split, 1 = no split
 cudaError_t launch_fwd_tsplit(const Args& a, const WsLayout& L, int P, cudaStream_t st,
                               cudaError_t (*fwd_core)(const Args&, cudaStream_t));

@@ -132,11 +132,11 @@ def test_wide_head_workspace(lib):
 
 def test_time_split_workspace():
     """Long sequences over few heads take the time-split forward, whose workspace holds per-segment states; many
-    heads or short sequences need none.  Delta bf16 heads up to 64 wide whose segments are whole chunks run the split
-    by walks: the zero-start run's final states and fp32 outputs, its residuals (a 16 KB state and 80 KB of solve
+    heads or short sequences need none.  Delta bf16 heads up to 64 wide without option bits run the split by walks
+    (segments of whole chunks, of any length): the zero-start run's final states and fp32 outputs, its residuals (a 16 KB state and 80 KB of solve
     results per chunk of 64 tokens), Phi with Qc (32 KB) and D = T_k S_s (16 KB) per chunk, three 16 KB records per
     (head, segment).  Other splits (gated, option bits, fp32, ragged segments) keep the transition run's buffers (delta:
-    transitions, a zero-value tensor and the transition run's fp32 outputs)."""
+    transitions, a zero-value tensor and the transition run's fp32 outputs); those need T divisible by P."""
     lib = gdn
     few = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0)
     many = lib.gdn_workspace_bytes(lib.make_shape(8, 16, 4096, 64, 64, "delta", "bf16"), 0)
@@ -144,7 +144,7 @@ def test_time_split_workspace():
     short = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 1000, 64, 64, "delta", "bf16"), 0)
     logits = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16", gate_logits=True), 0)
     assert many == 256 and short == 256
-    nq, P = 16 * 512, 8
+    nq, P = 16 * 512, 9   # segments of 57 chunks (the last 56): 16 x 9 <= 152
     assert lib.gdn_plan(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0).segments == P
     assert few == 256 + 16 * P * 16384 + 32768 * 16 * 64 * 4 + nq * (16384 + 81920) + nq * (32768 + 16384) \
         + 16 * P * 3 * 16384
@@ -237,7 +237,9 @@ def test_check_finite_option_bit():
 
 def test_plan_reports_split_and_kernel():
     """gdn_plan answers from the shape alone, by the rules the calls dispatch with: the time split for long
-    sequences over few heads (forward at least 4 segments in delta mode, 3 in gated mode, token-serial backward at
+    sequences over few heads (forward at least 4 segments in delta mode, 3 in gated mode; the delta bf16 split by
+    walks into segments of at least 8 whole chunks for any length, the others into equal segments; token-serial
+    backward at
     least 2, the chunked backward's chain in delta mode segments of at least 16 chunks),
     the decode kernel up to 8 tokens, the tensor-core forward for bf16 keys up to 64 wide except delta heads up to
     32 wide over more than 304 units, the token-serial forward otherwise."""
@@ -247,7 +249,9 @@ def test_plan_reports_split_and_kernel():
         p = gdn.gdn_plan(gdn.make_shape(*a, **kw), bw)
         return p.segments, p.fwd_kernel
 
-    assert plan(1, 16, 32768, 64, 64, "delta", "bf16") == (8, K.GDN_KERNEL_TENSOR_CORE)
+    assert plan(1, 16, 32768, 64, 64, "delta", "bf16") == (9, K.GDN_KERNEL_TENSOR_CORE)   # split by walks
+    assert plan(1, 16, 32749, 64, 64, "delta", "bf16") == (9, K.GDN_KERNEL_TENSOR_CORE)   # any length
+    assert plan(1, 16, 32768, 64, 64, "delta", "bf16", gate_logits=True) == (8, K.GDN_KERNEL_TENSOR_CORE)
     # chunked backward: its chain over the 512 chunk boundaries split into 4 segments of 128 chunks (2 sweeps x 16
     # heads x 4 <= 152), from the forward's residuals (the reverse sweep alone) into 9 of 57 (16 x 9 <= 152)
     assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=1) == (4, K.GDN_KERNEL_NONE)
@@ -313,6 +317,11 @@ def test_plan_and_workspace_agree_on_random_shapes():
                 nk = -(-T // 64)
                 assert P == 1 or (mode == "delta" and 2 * B * H * P <= 152 and -(-nk // P) >= 16
                                   and (P - 1) * -(-nk // P) < nk), (B, H, T, P)
+            elif not bw and chunked and mode == "delta":
+                # the split by walks: segments of at least 8 whole chunks (the last may be shorter), any length
+                nk = -(-T // 64)
+                assert P == 1 or (P >= 4 and B * H * P <= 152 and -(-nk // P) >= 8
+                                  and (P - 1) * -(-nk // P) < nk), (B, H, T, P)
             else:
                 assert T % P == 0 if T else P == 1
                 if P > 1:
@@ -341,12 +350,12 @@ def test_saved_residuals_sizes_and_argument_errors(lib):
     delta mode, a split in time into whole-chunk segments run by walks; 0 for every other shape.  The
     backward from the residuals needs a smaller workspace (backward = 2).  gdn_fwd_save and gdn_bwd_saved reject
     bad arguments before any device work."""
-    for B, H, T, d in ((8, 16, 4096, 64), (2, 3, 100, 56), (1, 1, 9, 8), (1, 16, 32768, 64)):
+    for B, H, T, d in ((8, 16, 4096, 64), (2, 3, 100, 56), (1, 1, 9, 8), (1, 16, 32768, 64), (1, 3, 2496, 64)):
         s = gdn.make_shape(B, H, T, d, d, "delta", "bf16")
         nq = B * H * -(-T // 64)
         assert gdn.gdn_saved_bytes(s) == nq * (16384 + 81920)
         assert 0 < gdn.gdn_workspace_bytes(s, 2) < gdn.gdn_workspace_bytes(s, 1)
-        if T == 32768:
+        if T >= 2496:
             continue   # the gated split in time keeps no residuals
         sg = gdn.make_shape(B, H, T, d, d, "gated", "bf16")
         assert gdn.gdn_saved_bytes(sg) == nq * (16384 + 16384)
@@ -356,7 +365,7 @@ def test_saved_residuals_sizes_and_argument_errors(lib):
             gdn.make_shape(2, 2, 256, 64, 64, "delta", "bf16", gate_logits=True),
             gdn.make_shape(2, 2, 256, 64, 64, "delta", "bf16", norm_bc=True),
             gdn.make_shape(1, 16, 32768, 64, 64, "gated", "bf16"),           # gated split in time
-            gdn.make_shape(1, 3, 2496, 64, 64, "delta", "bf16"),             # segments of 624 tokens
+            gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16", gate_logits=True),   # option bits
             gdn.make_shape(2, 2, 4, 64, 64, "delta", "bf16"),                # the decode kernel's length
             gdn.make_shape(2, 2, 0, 64, 64, "delta", "bf16")]
     for s in none:
