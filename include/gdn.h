@@ -132,11 +132,15 @@ size_t gdn_workspace_bytes(const gdn_shape_t* shape, int backward);
  * answered from the shape alone, by the rules the calls themselves follow.
  *   segments    gdn_fwd (backward = 0), gdn_bwd (backward = 1) or
  *               gdn_bwd_saved (backward = 2) cuts the sequence into this many
- *               equal segments that run side by side (the state a segment
- *               passes on is an affine map of the state it receives, "GDN &
- *               MLA Mechanism Deep-Dive", Step 5: chunked recurrence; a scan
- *               over the segments joins them); 1 = no split.  Long sequences
- *               over few heads are split.  With the chunked backward only its
+ *               segments that run side by side (the state a segment passes on
+ *               is an affine map of the state it receives, "GDN & MLA
+ *               Mechanism Deep-Dive", Step 5: chunked recurrence; a scan over
+ *               the segments joins them); 1 = no split.  Long sequences over
+ *               few heads are split: the delta bf16 forward (heads up to 64
+ *               wide, no option bits) into segments of whole chunks of 64
+ *               tokens for any T (the last segment may be shorter), other
+ *               forwards into equal segments (T divisible by them).  With the
+ *               chunked backward only its
  *               chain over the chunk boundaries is, in delta mode: its sweeps
  *               (two, or the reverse one alone from the forward's residuals)
  *               times heads x batch rows times segments stay within 152
@@ -221,11 +225,11 @@ gdn_status_t gdn_bwd(const gdn_shape_t* shape,
  * after them, so the rounding differs).  Shapes: bf16, d_k and d_v <= 64, no
  * option bits but GDN_CHECK_FINITE, and a forward that runs as
  * one tensor-core pass (gdn_plan(shape, 0): segments 1, GDN_KERNEL_TENSOR_CORE)
- * or, in delta mode, a split in time whose segments are whole chunks of 64
- * tokens (T a multiple of 64 x segments); that split runs every segment from
- * a zero state, keeping the residuals, then walks the segments' transitions
- * on the tensor cores and corrects outputs and residuals by the true entering
- * states (the saving call writes the true ones).  gdn_saved_bytes is 0 for
+ * or, in delta mode, a split in time (gdn_plan(shape, 0): segments > 1); that
+ * split runs every segment from a zero state, keeping the residuals, then
+ * walks the segments' transitions on the tensor cores and corrects outputs
+ * and residuals by the true entering states (the saving call writes the true
+ * ones).  gdn_saved_bytes is 0 for
  * any other shape, and both calls return GDN_ERR_MODE for it.  GDN_ERR_NULL if saved is NULL, GDN_ERR_ALIGN if it is
  * misaligned, GDN_ERR_WORKSPACE if saved_bytes is too small. */
 size_t gdn_saved_bytes(const gdn_shape_t* shape);
