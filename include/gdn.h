@@ -223,8 +223,9 @@ gdn_status_t gdn_bwd(const gdn_shape_t* shape,
  * aligned, written completely by the call.  o and hT equal gdn_fwd's within
  * the bf16 tolerance (the level products form K without beta, M = beta K
  * after them, so the rounding differs).  Shapes: bf16, d_k and d_v <= 64, no
- * option bits but GDN_CHECK_FINITE, and a forward that runs as
- * one tensor-core pass (gdn_plan(shape, 0): segments 1, GDN_KERNEL_TENSOR_CORE)
+ * option bits but GDN_CHECK_FINITE, and a forward that runs unsplit over
+ * more than 8 tokens (the saving call always takes the tensor-core kernel,
+ * also where gdn_plan reports the token-serial one for gdn_fwd)
  * or, in delta mode, a split in time (gdn_plan(shape, 0): segments > 1); that
  * split runs every segment from a zero state, keeping the residuals, then
  * walks the segments' transitions on the tensor cores and corrects outputs

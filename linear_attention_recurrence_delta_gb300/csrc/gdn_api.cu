@@ -284,15 +284,16 @@ static cudaError_t fwd_core(const Args& a, cudaStream_t st)
     }
 }
 
-// Shapes whose forward can keep the chunked backward's residuals: the chunked backward's shapes whose forward runs
-// as one tcgen05 pass (no time split, neither the decode nor the token-serial kernel).
-// gdn_fwd_save applies: the chunked backward's shapes whose forward is one tcgen05 pass, or a split by walks
+// Shapes whose forward can keep the chunked backward's residuals (gdn_fwd_save): the chunked backward's shapes whose
+// forward is a split by walks, or unsplit and longer than the decode kernel's reach.  The saving forward always runs
+// the tcgen05 kernel, also where gdn_fwd prefers the token-serial one (narrow delta heads over many units): the
+// residuals spare the backward far more than that costs.
 static bool saved_applies(const gdn_shape_t& s, int logits, int norm)
 {
     if (!chunk_bwd_applies(s, logits, norm)) return false;
     if (fwd_walk_split(s, logits, norm, nullptr) > 1) return true;
     if (tsplit_factor(s, 0) > 1) return false;
-    return fwd_kernel_of(make_args(&s)) == GDN_KERNEL_TENSOR_CORE;
+    return s.T > decode_max_tokens();
 }
 
 static size_t saved_bytes_of(const gdn_shape_t& s)
@@ -392,12 +393,17 @@ static gdn_status_t fwd_impl(const gdn_shape_t* shape_in, const void* v, const v
     }
     const int P = tsplit_factor(*shape, 0);
     cudaError_t e;
-    if (fwd_walk_split(*shape, logits, norm, nullptr) > 1)
+    if (fwd_walk_split(*shape, logits, norm, nullptr) > 1) {
         e = launch_fwd_walks(a, ws_layout(*shape, 0, norm, logits), st);
-    else if (P > 1)
+    } else if (P > 1) {
         e = launch_fwd_tsplit(a, ws_layout(*shape, 0, norm, logits), P, st, fwd_core);
-    else
+    } else if (saving) {
+        bool handled = false;   // the tcgen05 kernel keeps the residuals (saved_applies)
+        e = launch_fwd_tc(a, st, &handled);
+        if (e == cudaSuccess && !handled) e = cudaErrorInvalidValue;
+    } else {
         e = fwd_core(a, st);
+    }
     if (e == cudaSuccess && check) {
         e = launch_check_finite(o, (size_t)a.B * a.T * a.H * a.dv, a.io, ws, st);
         if (e == cudaSuccess && hT) e = launch_check_finite(hT, state_bytes / sizeof(float), GDN_F32, ws, st);

@@ -49,6 +49,16 @@ def test_saved_matches_oracle(mode, B, H, T, d, h0_std):
     check_saved(w, with_dhT=h0_std > 0)
 
 
+def test_saved_narrow_heads_many_units():
+    """320 narrow delta heads (d = 32, the 40-head production shape at 8 batch rows): gdn_fwd takes the token-serial
+    kernel there, but the saving forward runs the tensor-core one and keeps the residuals."""
+    w = I.custom(name="saved_narrow_8x40x512x32", mode="delta", dtype="bf16", B=8, H=40, T=512, dk=32, dv=32, seed=41,
+                 h0_std=0.2, backward=True)
+    assert gdn.gdn_plan(shape_of(w), 0).fwd_kernel == gdn.GDN_KERNEL_SERIAL
+    assert gdn.gdn_saved_bytes(shape_of(w)) > 0
+    check_saved(w)
+
+
 @pytest.mark.parametrize("mode", ["delta", "gated"])
 @pytest.mark.parametrize("g_mu", [0.0, 3.0])
 def test_saved_steep_decay(mode, g_mu):
