@@ -151,11 +151,33 @@ static size_t place_chunk_bwd(const gdn_shape_t& s, WsLayout& L, size_t off, boo
     return off;
 }
 
+// The plain backward of the chunked backward's unsplit shapes runs the saving forward into its workspace and then
+// the backward from those residuals when the heads fill most of their waves of one CTA per SM: per chunk the
+// forward (one CTA per head, the front and the state chain together) takes about 12 us of its CTA, the chunk-parallel
+// prep (the front, Phi, Delta and Y) about 18 us of an SM, and the prep route adds the chain's forward sweep.
+static bool bwd_via_forward(const gdn_shape_t& s, int logits, int norm)
+{
+    if (s.T <= decode_max_tokens() || !chunk_bwd_applies(s, logits, norm)) return false;
+    if (fwd_walk_split(s, logits, norm, nullptr) > 1 || tsplit_factor(s, 0) > 1) return false;
+    const long units = (long)s.B * s.H, waves = (units + kSplitSMs - 1) / kSplitSMs;
+    return 3 * units > 2 * waves * kSplitSMs;
+}
+
 WsLayout ws_layout(const gdn_shape_t& s, int backward, int norm, int logits)
 {
     WsLayout L;
     size_t off = 256;  // status word
     if (backward && chunk_bwd_applies(s, logits, norm)) {
+        if (backward == 1 && bwd_via_forward(s, logits, norm)) {
+            // the saving forward's residuals and (unused) outputs, then the backward from the residuals
+            const size_t nq = (size_t)s.B * s.H * (size_t)((s.T + 63) / 64);
+            L.bf_res_off = off;
+            off = round_up(off + nq * (kSavedStateBytes + saved_solve_bytes(s.mode)), 256);
+            L.bf_o_off = off;
+            off = round_up(off + (size_t)s.B * s.T * s.H * s.dv * 2, 256);
+            L.total = place_chunk_bwd(s, L, off, true);
+            return L;
+        }
         L.total = place_chunk_bwd(s, L, off, backward == 2);
         return L;
     }
@@ -467,7 +489,21 @@ static gdn_status_t bwd_impl(const gdn_shape_t* shape_in, const void* v, const v
     a.dA_log = dA_log; a.dh0 = dh0; a.ws = ws; a.ws_bytes = ws_bytes; a.logits = logits; a.norm = norm;
     a.saved = from_saved ? const_cast<void*>(saved) : nullptr;
     cudaError_t e;
-    if (a.T > 0 && chunk_bwd_applies(*shape, logits, norm)) {
+    if (a.T > 0 && chunk_bwd_applies(*shape, logits, norm) && !from_saved && bwd_via_forward(*shape, logits, norm)) {
+        // the saving forward recomputes the residuals (outputs to the workspace), then the backward from them
+        const WsLayout L = ws_layout(*shape, 1, norm, logits);
+        Args f = a;
+        f.o = (unsigned char*)ws + L.bf_o_off;
+        f.hT = nullptr;
+        f.saved = (unsigned char*)ws + L.bf_res_off;
+        bool handled = false;
+        e = launch_fwd_tc(f, st, &handled);
+        if (e == cudaSuccess && !handled) e = cudaErrorInvalidValue;
+        if (e == cudaSuccess) {
+            a.saved = f.saved;
+            e = launch_chunk_bwd(a, L, st);
+        }
+    } else if (a.T > 0 && chunk_bwd_applies(*shape, logits, norm)) {
         e = launch_chunk_bwd(a, ws_layout(*shape, from_saved ? 2 : 1, norm, logits), st);
     } else {
         const int P = bwd_split(*shape, logits, norm);

@@ -69,6 +69,9 @@ struct WsLayout {
     // (its fp32 outputs), cb_phi_off (Phi per chunk) and cb_seg_off (per segment X, Pi, true start)
     size_t fw_res_off = 0;        // the residuals when the caller keeps none (states, then the solve's results)
     size_t fw_d_off = 0;          // D = T_k S_s per chunk, fp32 [B*H*chunks][64][64]
+    // chunked backward through the saving forward (bwd_via_forward in gdn_api.cu)
+    size_t bf_res_off = 0;        // the residuals (states, then the solve's results)
+    size_t bf_o_off = 0;          // the forward's outputs, bf16 [B, T, H, d_v] (not used)
     size_t total = 0;
 };
 

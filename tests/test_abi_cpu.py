@@ -170,7 +170,9 @@ def test_chunked_backward_workspace():
     """The chunked backward (bf16, heads up to 64 wide, no option bits) keeps per chunk of 64 tokens five 16 KB
     64 x 64 records in delta mode (transition as bf16 hi/lo tiles, zero-start state, adjoint share, entering state,
     leaving adjoint) plus the 80 KB of the front's results that the gradient pass reuses, four fp32 records in
-    gated mode, and two rows of 64 floats (decay, dA partial), after the 256-byte status word."""
+    gated mode, and two rows of 64 floats (decay, dA partial), after the 256-byte status word.  Where the heads fill
+    most of a wave of one CTA per SM, gdn_bwd runs the saving forward instead of the prep front: its workspace is
+    the backward-from-residuals one plus the residuals and the forward's outputs."""
     for mode, per_chunk in (("delta", 5 * 16384 + 81920), ("gated", 4 * 16384)):
         for B, H, T, d in ((8, 16, 4096, 64), (1, 16, 32768, 64), (2, 3, 100, 56), (1, 1, 1, 8), (1, 3, 2500, 64)):
             s = gdn.make_shape(B, H, T, d, d, mode, "bf16")
@@ -186,6 +188,11 @@ def test_chunked_backward_workspace():
             want = 256 + per_chunk * nq + 2 * -(-(nq * 256) // 256) * 256
             if nseg > 1:
                 want += 2 * units * nseg * 3 * 16384
+            if units == 128 and T == 4096:
+                # heads filling most of a wave: the saving forward recomputes the residuals (a 16 KB state and the
+                # solve's 80 KB, gated the 16 KB scores) and outputs into the workspace, then the backward from them
+                res = nq * (16384 + (81920 if mode == "delta" else 16384))
+                want = gdn.gdn_workspace_bytes(s, 2) + res + B * T * H * d * 2
             assert gdn.gdn_workspace_bytes(s, 1) == want, (mode, B, H, T, d)
             p = gdn.gdn_plan(s, 1)
             assert (p.segments, p.fwd_kernel, p.bwd_kernel) == (nseg, gdn.GDN_KERNEL_NONE, gdn.GDN_BWD_TENSOR_CORE)
