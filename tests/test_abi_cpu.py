@@ -141,7 +141,7 @@ def test_time_split_workspace():
     few = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0)
     many = lib.gdn_workspace_bytes(lib.make_shape(8, 16, 4096, 64, 64, "delta", "bf16"), 0)
     gated = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "gated", "bf16"), 0)
-    short = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 1000, 64, 64, "delta", "bf16"), 0)
+    short = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 500, 64, 64, "delta", "bf16"), 0)   # 8 chunks
     logits = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16", gate_logits=True), 0)
     assert many == 256 and short == 256
     nq, P = 16 * 512, 9   # segments of 57 chunks (the last 56): 16 x 9 <= 152
@@ -244,8 +244,8 @@ def test_check_finite_option_bit():
 
 def test_plan_reports_split_and_kernel():
     """gdn_plan answers from the shape alone, by the rules the calls dispatch with: the time split for long
-    sequences over few heads (forward at least 4 segments in delta mode, 3 in gated mode; the delta bf16 split by
-    walks into segments of at least 8 whole chunks for any length, the others into equal segments; token-serial
+    sequences over few heads (the delta bf16 forward split by walks into at least 2 segments of at least 8 whole
+    chunks for any length; other forwards into at least 4 equal segments in delta mode, 3 in gated mode; token-serial
     backward at
     least 2, the chunked backward's chain in delta mode segments of at least 16 chunks),
     the decode kernel up to 8 tokens, the tensor-core forward for bf16 keys up to 64 wide except delta heads up to
@@ -327,7 +327,7 @@ def test_plan_and_workspace_agree_on_random_shapes():
             elif not bw and chunked and mode == "delta":
                 # the split by walks: segments of at least 8 whole chunks (the last may be shorter), any length
                 nk = -(-T // 64)
-                assert P == 1 or (P >= 4 and B * H * P <= 152 and -(-nk // P) >= 8
+                assert P == 1 or (P >= 2 and B * H * P <= 152 and -(-nk // P) >= 8
                                   and (P - 1) * -(-nk // P) < nk), (B, H, T, P)
             else:
                 assert T % P == 0 if T else P == 1
