@@ -1903,16 +1903,19 @@ __global__ void __launch_bounds__(256) fwd_walk_scan_kernel(const __grid_constan
 //   D[:, 0:64 | 64:128] = [Phi ; Qc]_hi [X_hi | X_lo] (N = 128),   D[:, 0:64] += [Phi ; Qc]_lo X_hi (N = 64)
 // so TMEM lanes 0..63 hold Phi X (the next X) and lanes 64..127 Qc X.  OUT = false: X starts at the identity and
 // the segment's transition Pi is left in its record [1].  OUT = true: X starts at the segment's true state S_s
-// (record [2]) and is D_k = T_k S_s before chunk k's step; warps 2 and 3 (lanes 64..127, token t of the chunk,
-// 64 columns each) write o = o_zero-start + Qc D, and a saving forward's D goes to its records for the residual
+// (record [2]) and is D_k = T_k S_s before chunk k's step; warps 2, 3, 6, 7 (lanes 64..127: token t of the chunk,
+// 32 columns each) write o = o_zero-start + Qc D, and a saving forward's D goes to its records for the residual
 // fix-up.  Warps 0, 1, 4, 5 hold X as in the chain (row i, 32 columns); thread 0 issues the copies and products.
+// OUT = false launches 192 threads (warps 2 and 3 leave after the set-up), OUT = true 256.
 constexpr uint32_t FW_STAGE = 32768;
 constexpr uint32_t FW_X = CT_NS * FW_STAGE;                  // X hi, X lo tiles
 constexpr uint32_t FW_BAR = FW_X + 16384;
 constexpr uint32_t FW_SMEM = FW_BAR + 128 + 1024;
 
+constexpr int fw_threads(bool out) { return out ? 256 : CT_THREADS; }
+
 template <bool OUT>
-__global__ void __launch_bounds__(CT_THREADS, 1) fwd_walk_kernel(const __grid_constant__ CbParams p)
+__global__ void __launch_bounds__(fw_threads(OUT), 1) fwd_walk_kernel(const __grid_constant__ CbParams p)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -1924,9 +1927,9 @@ __global__ void __launch_bounds__(CT_THREADS, 1) fwd_walk_kernel(const __grid_co
     const int nk = p.nchunks, k0 = sg * p.seg_len, k1 = min(k0 + p.seg_len, nk), ns = k1 - k0;
     const int bb = u / p.H, h = u - bb * p.H;
     const size_t qb = (size_t)u * nk;
-    // active threads: the X rows (warps 0, 1, 4, 5) and, with OUT, the output rows (warps 2, 3)
-    const int nact = OUT ? 192 : 128;
-    const bool orow = OUT && (warp == 2 || warp == 3);
+    // active threads: the X rows (warps 0, 1, 4, 5) and, with OUT, the output rows (warps 2, 3, 6, 7)
+    const int nact = OUT ? 256 : 128;
+    const bool orow = OUT && (warp & 2);
     auto issue_copy = [&](int n) {
         const int s = n % CT_NS;
         mbar_arrive_expect_tx(&full[s], FW_STAGE);
@@ -1950,9 +1953,10 @@ __global__ void __launch_bounds__(CT_THREADS, 1) fwd_walk_kernel(const __grid_co
     const int i = 32 * (warp & 1) + lane, j0 = 32 * (warp >> 2);
     const uint32_t tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
     uint32_t* abortf = &misc[1];
-    const int t = 32 * (warp & 1) + lane;   // output rows: the chunk's token
+    const int t = 32 * (warp & 1) + lane;   // output rows: the chunk's token, columns oc0 .. oc0 + 31
+    const int oc0 = 32 * (warp >> 2);
     auto o_row = [&](int k) { return ((size_t)bb * p.T + 64 * k + t) * p.H + h; };
-    if (orow)
+    if (orow && oc0 == 0)   // one prefetch per token row
         for (int n = 0; n < 2 && n < ns; n++)
             if (64 * (k0 + n) + t < p.T) prefetch_l2_bulk(p.fw_o32 + o_row(k0 + n) * p.dv_, (uint32_t)p.dv_ * 4u);
     float x[32];
@@ -1970,15 +1974,16 @@ __global__ void __launch_bounds__(CT_THREADS, 1) fwd_walk_kernel(const __grid_co
         }
     }
     bool ok = true;
-    float4 o0v[16];   // output rows: the zero-start outputs of token t, loaded before the step's product
+    float4 o0v[8];   // output rows: the zero-start outputs of token t, loaded before the step's product
     for (int n = 0; n < ns; n++) {
         const int k = k0 + n;
         if (orow) {
             const bool in = 64 * k + t < p.T;
-            const float* o0 = p.fw_o32 + o_row(in ? k : k0) * p.dv_;
+            const float* o0 = p.fw_o32 + o_row(in ? k : k0) * p.dv_ + oc0;
 #pragma unroll
-            for (int e = 0; e < 16; e++)
-                o0v[e] = 4 * e < p.dv_ ? *reinterpret_cast<const float4*>(o0 + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = 0; e < 8; e++)
+                o0v[e] = oc0 + 4 * e < p.dv_ ? *reinterpret_cast<const float4*>(o0 + 4 * e)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         if (!orow) {
             if (OUT && p.fw_st) {   // D_k for the residual fix-up
@@ -2010,7 +2015,7 @@ __global__ void __launch_bounds__(CT_THREADS, 1) fwd_walk_kernel(const __grid_co
                 atomicExch(p.status + 2, (OUT ? 820u : 810u) + (uint32_t)n);
             }
         }
-        if (orow && n + 2 < ns && 64 * (k + 2) + t < p.T)
+        if (orow && oc0 == 0 && n + 2 < ns && 64 * (k + 2) + t < p.T)
             prefetch_l2_bulk(p.fw_o32 + o_row(k + 2) * p.dv_, (uint32_t)p.dv_ * 4u);
         if (!wait_or_abort(mmab, (uint32_t)n & 1u, abortf, p.status, p.wait_ns)) {
             ok = false;
@@ -2031,16 +2036,16 @@ __global__ void __launch_bounds__(CT_THREADS, 1) fwd_walk_kernel(const __grid_co
         } else {
             // o = o_zero-start + Qc D, token t of chunk k (the TMEM loads are warp-uniform; the row may be past T)
             const bool in = 64 * k + t < p.T;
-            __nv_bfloat16* o = p.fw_o + o_row(k) * p.dv_;
+            __nv_bfloat16* o = p.fw_o + o_row(k) * p.dv_ + oc0;
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16) {
+            for (int c0 = 0; c0 < 32; c0 += 16) {
                 float a[16], b[16];
-                tmem_ld16(tl + c0, a);
-                tmem_ld16(tl + 64 + c0, b);
+                tmem_ld16(tl + oc0 + c0, a);
+                tmem_ld16(tl + 64 + oc0 + c0, b);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; e += 8) {
-                    if (in && c0 + e < p.dv_) {
+                    if (in && oc0 + c0 + e < p.dv_) {
                         const float4 x0 = o0v[(c0 + e) >> 2];
                         const float4 x1 = o0v[((c0 + e) >> 2) + 1];
                         uint4 w;
@@ -3201,11 +3206,11 @@ cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, cudaStream_t st)
     // 2. Phi and Qc of every chunk
     chunk_prep_saved_kernel<<<grid3, 256, ps::SMEM, st>>>(p);
     // 3. each segment's transition
-    fwd_walk_kernel<false><<<dim3(units, P), CT_THREADS, FW_SMEM, st>>>(p);
+    fwd_walk_kernel<false><<<dim3(units, P), fw_threads(false), FW_SMEM, st>>>(p);
     // 4. the segments' true starting states, and h_T
     fwd_walk_scan_kernel<<<dim3(units, 8), 256, 0, st>>>(p, Xb, a.h0, a.hT);
     // 5. D = T_k S_s through every segment, and the outputs o = o_zero-start + Qc D
-    fwd_walk_kernel<true><<<dim3(units, P), CT_THREADS, FW_SMEM, st>>>(p);
+    fwd_walk_kernel<true><<<dim3(units, P), fw_threads(true), FW_SMEM, st>>>(p);
     // 6. a saving forward's residuals made true
     if (a.saved) fwd_walk_res_kernel<<<grid3, 256, fx::SMEM, st>>>(p);
     return cudaGetLastError();
