@@ -88,7 +88,7 @@ static size_t place_fwd_walks(const gdn_shape_t& s, int P, WsLayout& L, size_t o
     L.ts_o_off = off;
     off = round_up(off + (size_t)s.B * s.T * s.H * s.dv * sizeof(float), 256);
     L.fw_res_off = off;
-    off = round_up(off + nq * (kSavedStateBytes + kSavedSolveBytes), 256);
+    off = round_up(off + nq * (kSavedStateBytes + saved_solve_bytes(s.mode)), 256);
     L.cb_phi_off = off;
     off = round_up(off + nq * 32768, 256);   // [Phi_hi | Qc_hi | Phi_lo | Qc_lo]
     L.fw_d_off = off;

@@ -100,6 +100,7 @@ struct CbParams {
     // the forward split in time by walks (delta): prep writes [Phi_hi | Qc_hi | Phi_lo | Qc_lo] per chunk to phi
     // and no Y; a saving forward's second walk writes D = T_k S_s to st for the residual fix-up
     int fwd_walks;
+    int fw_gated;         // gated mode: Phi = diag(E) and Qc = Ctil come from g and c alone (no residuals read)
     const float* fw_o32;  // the zero-start run's outputs, fp32 [B, T, H, d_v]
     __nv_bfloat16* fw_o;  // the outputs
     float* fw_st;         // saving: the residual states, made true by adding D (null: not saving)
@@ -1148,6 +1149,11 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
     auto issue = [&](int q) {
         if (q == p.starve) return;   // failure-path test hook
         const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
+        if (p.fw_gated) {   // Phi and Qc of a gated chunk need its c tile alone
+            mbar_arrive_expect_tx(&S.full, 8192);
+            tma_load_4d(sm + ps::STC, &p.tm_c, &S.full, 0, h, 64 * k, bb);
+            return;
+        }
         mbar_arrive_expect_tx(&S.full, (p.fwd_walks ? 2 : 3) * 8192 + 32768);
         tma_load_4d(sm + ps::STB, &p.tm_b, &S.full, 0, h, 64 * k, bb);
         tma_load_4d(sm + ps::STC, &p.tm_c, &S.full, 0, h, 64 * k, bb);
@@ -1185,12 +1191,14 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             // the next chunk's tiles and residuals towards L2 (its loads go out when this chunk is done)
             const int qn = q + gridDim.x, un = qn / p.nchunks, kn = qn - un * p.nchunks, bn = un / p.H,
                       hn = un - bn * p.H;
-            tma_prefetch_l2(&p.tm_b, 0, hn, 64 * kn, bn);
             tma_prefetch_l2(&p.tm_c, 0, hn, 64 * kn, bn);
-            if (!p.fwd_walks) tma_prefetch_l2(&p.tm_do, 0, hn, 64 * kn, bn);
-            const unsigned char* rq = p.sv + (size_t)qn * p.sv_stride;
-            prefetch_l2_bulk(rq + sv::P, 16384);
-            prefetch_l2_bulk(rq + sv::NW, 16384);
+            if (!p.fw_gated) {
+                tma_prefetch_l2(&p.tm_b, 0, hn, 64 * kn, bn);
+                if (!p.fwd_walks) tma_prefetch_l2(&p.tm_do, 0, hn, 64 * kn, bn);
+                const unsigned char* rq = p.sv + (size_t)qn * p.sv_stride;
+                prefetch_l2_bulk(rq + sv::P, 16384);
+                prefetch_l2_bulk(rq + sv::NW, 16384);
+            }
         }
         if (warp == 0 && !wait_or_abort(&S.full, full_phase, &S.abort, p.status, p.wait_ns) && lane == 0)
             atomicExch(p.status + 2, 5u);
@@ -1211,7 +1219,7 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             S.G[2 * lane + 1] = x;
         }
         named_bar_sync(1, 256);
-        {
+        if (!p.fw_gated) {
             // Bhat = b (.) exp(A (G_63 - G_t)), thread = (token t, 16 channels)
             const int t = r & 63, cq = r >> 6;
             float bv[16], y[16];
@@ -1222,7 +1230,7 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             st16_split(sm + ps::BH, sm + ps::BH + 8192, t, cq, y);
         }
         sync_all();
-        if (r == 0) {
+        if (r == 0 && !p.fw_gated) {
             const uint32_t bh = smem_u32(sm + ps::BH), pp = smem_u32(sm + ps::P), nw = smem_u32(sm + ps::NW);
             const uint32_t idA = idesc_bf16(128, 64, true, true), idB = idesc_bf16(128, 64, false, true);
             // Bhat^T (-W): TMEM columns 0..63, rows i
@@ -1235,9 +1243,9 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             mma_tiles(tb + 64, pp + 8192, false, 0, 0, nw, true, 8192, 0, 4, idB, true);
             mma_commit(&S.mma);
         }
-        if (!wait_mma(0)) break;
+        if (!p.fw_gated && !wait_mma(0)) break;
         if (q4 < 2) {
-            // lanes 0..63: Phi row i out (hi/lo tiles), Qc row t = i = Ctil + P (-W) into its tiles
+            // lanes 0..63: Phi row i out (hi/lo tiles), Qc row t = i = Ctil + P (-W) into its tiles (gated: W = 0)
             const int i = trow;
             // the forward's walks take [Phi_hi | Qc_hi | Phi_lo | Qc_lo] (32 KB a chunk): the stacked A operand
             // [Phi ; Qc] gives the next state and the outputs' share in one product
@@ -1248,9 +1256,14 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             for (int h2 = 0; h2 < 2; h2++) {
                 const int cg = 2 * wh + h2;
                 float a[16], b[16], cv[16];
-                tmem_ld16(tl + 16 * cg, a);
-                tmem_ld16(tl + 64 + 16 * cg, b);
-                tmem_wait_ld();
+                if (p.fw_gated) {
+#pragma unroll
+                    for (int e = 0; e < 16; e++) a[e] = b[e] = 0.f;
+                } else {
+                    tmem_ld16(tl + 16 * cg, a);
+                    tmem_ld16(tl + 64 + 16 * cg, b);
+                    tmem_wait_ld();
+                }
 #pragma unroll
                 for (int e = 0; e < 16; e++) a[e] += (16 * cg + e == i) ? ec : 0.f;
                 st16_split(phq, phq + lo, i, cg, a);
@@ -2095,6 +2108,19 @@ struct FxSmall {
 
 __global__ void __launch_bounds__(256, 3) fwd_walk_res_kernel(const __grid_constant__ CbParams p)
 {
+    if (p.fw_gated) {
+        // gated residuals keep no U: the state alone, S += D (thread = row i, 16 columns)
+        const int i = threadIdx.x & 63, cq = threadIdx.x >> 6;
+        for (int q = blockIdx.x; q < p.nq; q += gridDim.x)
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 d4 = *rec4(p.st, q, i, 16 * cq + e);
+                float4* s4 = rec4(p.fw_st, q, i, 16 * cq + e);
+                const float4 o = *s4;
+                *s4 = make_float4(o.x + d4.x, o.y + d4.y, o.z + d4.z, o.w + d4.w);
+            }
+        return;
+    }
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     FxSmall& S = *reinterpret_cast<FxSmall*>(sm + fx::SMALL);
@@ -3175,11 +3201,12 @@ cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, cudaStream_t st)
     p.phi = ws + Lw.cb_phi_off;
     p.sv = res + (size_t)units * nk * kSavedStateBytes;
     p.st = (float*)(ws + Lw.fw_d_off);   // the second walk's records D
+    p.fw_gated = a.mode == GDN_GATED;
     p.status = (uint32_t*)a.ws;
     p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv_ = a.dv;
     p.nchunks = nk;
     p.nq = units * nk;
-    p.sv_stride = sv::BYTES;
+    p.sv_stride = (uint32_t)saved_solve_bytes(a.mode);
     p.nseg = P;
     p.seg_len = L;
     p.segrec = (float*)(ws + Lw.cb_seg_off);

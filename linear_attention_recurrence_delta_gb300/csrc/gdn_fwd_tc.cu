@@ -1134,7 +1134,11 @@ cudaError_t launch_fwd_tc(const Args& a, cudaStream_t st, bool* handled)
         p.st = (float*)a.saved;
         p.sv = (unsigned char*)a.saved + nq * 16384;
         p.sv_stride = a.mode == GDN_DELTA ? svr::BYTES : svr::GATED_BYTES;
-        if (a.mode != GDN_DELTA) return p.seg > 1 ? cudaErrorInvalidValue : launch_t<false, false, SAVE_FULL>(p, grid, st);
+        if (a.mode != GDN_DELTA) {
+            if (p.seg <= 1) return launch_t<false, false, SAVE_FULL>(p, grid, st);
+            return a.save_lite ? launch_t<false, false, SAVE_SPLIT_LITE>(p, grid, st)
+                               : launch_t<false, false, SAVE_SPLIT>(p, grid, st);
+        }
         if (p.seg <= 1) return launch_t<true, false, SAVE_FULL>(p, grid, st);
         return a.save_lite ? launch_t<true, false, SAVE_SPLIT_LITE>(p, grid, st)
                            : launch_t<true, false, SAVE_SPLIT>(p, grid, st);

@@ -101,12 +101,12 @@ inline bool chunk_bwd_applies(const gdn_shape_t& s, int logits, int norm)
 {
     return s.io == GDN_BF16 && s.T > 0 && s.dk <= 64 && s.dv <= 64 && !logits && !norm;
 }
-// The delta forward split in time by walks (launch_fwd_walks): bf16, heads up to 64 wide, no option bits, at most
-// 76 (batch, head) units.  P segments of *seg_len chunks of 64 tokens (the last one may be shorter, its last chunk
+// The forward split in time by walks (launch_fwd_walks): bf16, heads up to 64 wide, no option bits, at most 76
+// (batch, head) units.  P segments of *seg_len chunks of 64 tokens (the last one may be shorter, its last chunk
 // ragged) for any length: B * H * P <= 152, at least 8 chunks each, P >= 2.  Returns P (1: no split by walks).
 inline int fwd_walk_split(const gdn_shape_t& s, int logits, int norm, int* seg_len)
 {
-    if (s.mode != GDN_DELTA || !chunk_bwd_applies(s, logits, norm)) return 1;
+    if (!chunk_bwd_applies(s, logits, norm)) return 1;
     const long units = (long)s.B * s.H, nk = (s.T + 63) / 64;
     long P = kSplitSMs / units;
     if (P > nk / 8) P = nk / 8;

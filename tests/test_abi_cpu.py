@@ -132,26 +132,30 @@ def test_wide_head_workspace(lib):
 
 def test_time_split_workspace():
     """Long sequences over few heads take the time-split forward, whose workspace holds per-segment states; many
-    heads or short sequences need none.  Delta bf16 heads up to 64 wide without option bits run the split by walks
-    (segments of whole chunks, of any length): the zero-start run's final states and fp32 outputs, its residuals (a 16 KB state and 80 KB of solve
-    results per chunk of 64 tokens), Phi with Qc (32 KB) and D = T_k S_s (16 KB) per chunk, three 16 KB records per
-    (head, segment).  Other splits (gated, option bits, fp32, ragged segments) keep the transition run's buffers (delta:
-    transitions, a zero-value tensor and the transition run's fp32 outputs); those need T divisible by P."""
+    heads or short sequences need none.  bf16 heads up to 64 wide without option bits run the split by walks
+    (segments of whole chunks, of any length): the zero-start run's final states and fp32 outputs, its residuals (a
+    16 KB state and 80 KB of solve results per chunk of 64 tokens, gated the 16 KB scores), Phi with Qc (32 KB) and
+    D = T_k S_s (16 KB) per chunk, three 16 KB records per (head, segment).  Other splits (option bits, fp32) keep
+    the transition run's buffers (delta: transitions, a zero-value tensor and the transition run's fp32 outputs);
+    those need T divisible by P."""
     lib = gdn
     few = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0)
     many = lib.gdn_workspace_bytes(lib.make_shape(8, 16, 4096, 64, 64, "delta", "bf16"), 0)
     gated = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "gated", "bf16"), 0)
     short = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 500, 64, 64, "delta", "bf16"), 0)   # 8 chunks
     logits = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16", gate_logits=True), 0)
+    glogits = lib.gdn_workspace_bytes(lib.make_shape(1, 16, 32768, 64, 64, "gated", "bf16", gate_logits=True), 0)
     assert many == 256 and short == 256
     nq, P = 16 * 512, 9   # segments of 57 chunks (the last 56): 16 x 9 <= 152
     assert lib.gdn_plan(lib.make_shape(1, 16, 32768, 64, 64, "delta", "bf16"), 0).segments == P
-    assert few == 256 + 16 * P * 16384 + 32768 * 16 * 64 * 4 + nq * (16384 + 81920) + nq * (32768 + 16384) \
-        + 16 * P * 3 * 16384
+    assert lib.gdn_plan(lib.make_shape(1, 16, 32768, 64, 64, "gated", "bf16"), 0).segments == P
+    walks = 256 + 16 * P * 16384 + 32768 * 16 * 64 * 4 + nq * (32768 + 16384) + 16 * P * 3 * 16384
+    assert few == walks + nq * (16384 + 81920)
+    assert gated == walks + nq * (16384 + 16384)
     # the transition run's buffers: 2 x 128 states (16 KB) + 2 x 128 transitions + zero values (bf16) and the fp32
-    # outputs of the zero-start and transition runs
+    # outputs of the zero-start and transition runs; gated without the transitions
     assert logits >= 256 + 4 * 128 * 16384 + 32768 * 16 * 64 * 2 + 2 * 32768 * 16 * 64 * 4
-    assert 256 + 2 * 128 * 16384 <= gated < logits
+    assert 256 + 2 * 128 * 16384 <= glogits < logits
 
 
 def test_time_split_backward_workspace():
@@ -324,7 +328,7 @@ def test_plan_and_workspace_agree_on_random_shapes():
                 nk = -(-T // 64)
                 assert P == 1 or (mode == "delta" and 2 * B * H * P <= 152 and -(-nk // P) >= 16
                                   and (P - 1) * -(-nk // P) < nk), (B, H, T, P)
-            elif not bw and chunked and mode == "delta":
+            elif not bw and chunked:
                 # the split by walks: segments of at least 8 whole chunks (the last may be shorter), any length
                 nk = -(-T // 64)
                 assert P == 1 or (P >= 2 and B * H * P <= 152 and -(-nk // P) >= 8
@@ -353,8 +357,8 @@ def test_plan_and_workspace_agree_on_random_shapes():
 
 def test_saved_residuals_sizes_and_argument_errors(lib):
     """gdn_saved_bytes: per chunk of 64 tokens a 16 KB state and 80 KB of solve results (gated mode: the 16 KB
-    scores P), for bf16 shapes whose backward is the chunked one and whose forward is one tensor-core pass or, in
-    delta mode, a split in time into whole-chunk segments run by walks; 0 for every other shape.  The
+    scores P), for bf16 shapes whose backward is the chunked one and whose forward is one tensor-core pass or a
+    split in time into whole-chunk segments run by walks; 0 for every other shape.  The
     backward from the residuals needs a smaller workspace (backward = 2).  gdn_fwd_save and gdn_bwd_saved reject
     bad arguments before any device work."""
     for B, H, T, d in ((8, 16, 4096, 64), (2, 3, 100, 56), (1, 1, 9, 8), (1, 16, 32768, 64), (1, 3, 2496, 64)):
@@ -362,8 +366,6 @@ def test_saved_residuals_sizes_and_argument_errors(lib):
         nq = B * H * -(-T // 64)
         assert gdn.gdn_saved_bytes(s) == nq * (16384 + 81920)
         assert 0 < gdn.gdn_workspace_bytes(s, 2) < gdn.gdn_workspace_bytes(s, 1)
-        if T >= 2496:
-            continue   # the gated split in time keeps no residuals
         sg = gdn.make_shape(B, H, T, d, d, "gated", "bf16")
         assert gdn.gdn_saved_bytes(sg) == nq * (16384 + 16384)
         assert 0 < gdn.gdn_workspace_bytes(sg, 2) < gdn.gdn_workspace_bytes(sg, 1)
@@ -371,7 +373,6 @@ def test_saved_residuals_sizes_and_argument_errors(lib):
             gdn.make_shape(2, 2, 256, 128, 128, "delta", "bf16"),            # wider than 64
             gdn.make_shape(2, 2, 256, 64, 64, "delta", "bf16", gate_logits=True),
             gdn.make_shape(2, 2, 256, 64, 64, "delta", "bf16", norm_bc=True),
-            gdn.make_shape(1, 16, 32768, 64, 64, "gated", "bf16"),           # gated split in time
             gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16", gate_logits=True),   # option bits
             gdn.make_shape(2, 2, 4, 64, 64, "delta", "bf16"),                # the decode kernel's length
             gdn.make_shape(2, 2, 0, 64, 64, "delta", "bf16")]
@@ -394,7 +395,7 @@ def test_saved_residuals_sizes_and_argument_errors(lib):
     assert fwd_save(s, saved=FAKE + 16) == 3
     assert fwd_save(gdn.make_shape(2, 2, 256, 64, 64, "delta", "f32")) == 4
     assert fwd_save(gdn.make_shape(2, 2, 256, 64, 64, "gated", "bf16")) == 4   # beta given in gated mode
-    assert fwd_save(gdn.make_shape(1, 16, 32768, 64, 64, "gated", "bf16"), saved_bytes=1 << 40) == 4
+    assert fwd_save(gdn.make_shape(1, 16, 32768, 64, 64, "delta", "bf16", gate_logits=True), saved_bytes=1 << 40) == 4
     assert bwd_saved(s, saved=None) == 1
     assert bwd_saved(s, saved_bytes=need - 1) == 5
     assert bwd_saved(s, saved=FAKE + 16) == 3

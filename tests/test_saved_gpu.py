@@ -68,15 +68,16 @@ def test_saved_steep_decay(mode, g_mu):
     check_saved(w)
 
 
+@pytest.mark.parametrize("mode", ["delta", "gated"])
 @pytest.mark.parametrize("B,H,T,d", [(1, 4, 2048, 64), (2, 3, 3072, 56), (1, 2, 4096, 32),
                                      (1, 3, 2496, 64),     # 39 chunks: segments of 10, the last of 9
                                      (2, 5, 3001, 48)])    # 47 chunks, the last of 57 tokens: 10, 10, 10, 10, 7
-def test_saved_split_forward(B, H, T, d):
-    """Long sequences over few heads: the delta forward splits in time into segments of whole chunks (any length:
-    the last segment may be shorter and its last chunk ragged) and runs them by walks (zero-start runs keeping their
+def test_saved_split_forward(mode, B, H, T, d):
+    """Long sequences over few heads: the forward splits in time into segments of whole chunks (any length: the
+    last segment may be shorter and its last chunk ragged) and runs them by walks (zero-start runs keeping their
     residuals, the segments' transitions, a scan, the walks of T_k S_s writing the outputs, and a fix-up that makes
-    the residuals true); gdn_bwd_saved then reads those residuals."""
-    w = I.custom(name=f"saved_split_{B}x{H}x{T}x{d}", mode="delta", dtype="bf16", B=B, H=H, T=T, dk=d, dv=d,
+    the residuals true; gated heads' transitions are diagonal); gdn_bwd_saved then reads those residuals."""
+    w = I.custom(name=f"saved_split_{mode}_{B}x{H}x{T}x{d}", mode=mode, dtype="bf16", B=B, H=H, T=T, dk=d, dv=d,
                  seed=5 + T + d, h0_std=0.3, backward=True)
     assert gdn.gdn_plan(shape_of(w), 0).segments > 1 and gdn.gdn_saved_bytes(shape_of(w)) > 0
     check_saved(w)
