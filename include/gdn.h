@@ -141,7 +141,7 @@ size_t gdn_workspace_bytes(const gdn_shape_t* shape, int backward);
  *               tokens for any T (the last segment may be shorter), other
  *               forwards into equal segments (T divisible by them).  With the
  *               chunked backward only its
- *               chain over the chunk boundaries is, in delta mode: its sweeps
+ *               chain over the chunk boundaries is (both modes): its sweeps
  *               (two, or the reverse one alone from the forward's residuals)
  *               times heads x batch rows times segments stay within 152
  *               walks, each segment at least 16 chunks of 64 tokens (the last

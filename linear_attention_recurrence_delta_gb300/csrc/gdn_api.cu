@@ -147,6 +147,10 @@ static size_t place_chunk_bwd(const gdn_shape_t& s, WsLayout& L, size_t off, boo
     if (nseg > 1) {
         L.cb_seg_off = off;
         off = round_up(off + (size_t)dirs * s.B * s.H * nseg * 3 * 64 * 64 * sizeof(float), 256);
+        if (s.mode == GDN_GATED) {
+            L.cb_tvec_off = off;
+            off = round_up(off + (size_t)dirs * nq * 64 * sizeof(float), 256);
+        }
     }
     return off;
 }

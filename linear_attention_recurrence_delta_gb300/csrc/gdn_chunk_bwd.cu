@@ -97,6 +97,7 @@ struct CbParams {
     // delta, the chain as walks (few heads): nseg segments of seg_len chunks per unit (nseg = 1: no split)
     int nseg, seg_len;
     float* segrec;        // nseg > 1: per (direction, unit, segment) final X, final Pi, true start
+    float* tvec;          // gated, nseg > 1: per (direction, chunk) the rows' decay product from the segment's start
     // the forward split in time by walks (delta): prep writes [Phi_hi | Qc_hi | Phi_lo | Qc_lo] per chunk to phi
     // and no Y; a saving forward's second walk writes D = T_k S_s to st for the residual fix-up
     int fwd_walks;
@@ -1870,6 +1871,169 @@ __global__ void __launch_bounds__(256) chunk_walk_scan_kernel(const __grid_const
         });
 }
 
+// Gated mode, the chain split in time (few heads over many chunks): Phi = diag(E) acts on the rows, so a segment's
+// transition is the vector of its decays' products and everything stays elementwise.  A walk per (unit, segment,
+// sweep) from zero (the sequence's own start at its end segment) writes the local records and, per chunk, the
+// product T_k of the decays walked so far (the rows' factor from the segment's start to the chunk); the scan
+// joins the segments (S_{s+1} = Pi_s (.) S_s + X_s, likewise for the adjoints, and dh0 after the last fold); the
+// fix-up adds T_k (.) S_s to every record of a segment that did not start from the sequence's own start.  Thread
+// mapping as in chunk_chain_gated_kernel: rows 2 (r >> 3), + 1 x columns 8 (r & 7) .. + 7.
+__device__ __forceinline__ float* gated_tvec(const CbParams& p, int d, size_t q)
+{
+    return p.tvec + ((size_t)d * p.nq + q) * 64;
+}
+
+__global__ void __launch_bounds__(256) chunk_chain_gated_seg_kernel(const __grid_constant__ CbParams p)
+{
+    const bool rev = p.rev_only || blockIdx.z == 1;
+    const int dslot = p.rev_only ? 0 : (int)blockIdx.z;
+    const int u = blockIdx.x, sg = blockIdx.y, r = threadIdx.x, i0 = 2 * (r >> 3), j0 = 8 * (r & 7);
+    const int dk = p.dk, dv = p.dv_, nk = p.nchunks;
+    const int k0 = sg * p.seg_len, k1 = min(k0 + p.seg_len, nk), ns = k1 - k0;
+    const size_t qb = (size_t)u * nk;
+    const float* rec_in = rev ? p.ych : p.dlt;
+    float* rec_out = rev ? p.dst : p.st;
+    auto chunk_of = [&](int n) { return rev ? k1 - 1 - n : k0 + n; };
+    auto rec = [&](int k, float4 (&v)[4]) {
+        v[0] = *rec4(rec_in, qb + k, i0, j0);
+        v[1] = *rec4(rec_in, qb + k, i0, j0 + 4);
+        v[2] = *rec4(rec_in, qb + k, i0 + 1, j0);
+        v[3] = *rec4(rec_in, qb + k, i0 + 1, j0 + 4);
+    };
+    auto put = [&](float* base, size_t q, const float2 (&x)[8]) {
+        *rec4(base, q, i0, j0) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
+        *rec4(base, q, i0, j0 + 4) = make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
+        *rec4(base, q, i0 + 1, j0) = make_float4(x[4].x, x[4].y, x[5].x, x[5].y);
+        *rec4(base, q, i0 + 1, j0 + 4) = make_float4(x[6].x, x[6].y, x[7].x, x[7].y);
+    };
+    // the local start: the sequence's own (h0 forward, dh_T reverse) at its end segment, zero elsewhere
+    const float* src0 = rev ? (sg == p.nseg - 1 ? p.dhT : nullptr) : (sg == 0 ? p.h0 : nullptr);
+    float2 s[8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+        const int i = i0 + (e >> 2), j = j0 + 2 * (e & 3);
+        const bool in = src0 && i < dk;
+        s[e] = make_float2(in && j < dv ? src0[((size_t)u * dk + i) * dv + j] : 0.f,
+                           in && j + 1 < dv ? src0[((size_t)u * dk + i) * dv + j + 1] : 0.f);
+    }
+    float t0 = 1.f, t1 = 1.f;   // T of rows i0, i0 + 1
+    float4 d[4], dn[4];
+    float e0 = 0.f, e1 = 0.f, en0 = 0.f, en1 = 0.f;
+    rec(chunk_of(0), d);
+    e0 = p.ec[(qb + chunk_of(0)) * 64 + i0];
+    e1 = p.ec[(qb + chunk_of(0)) * 64 + i0 + 1];
+    for (int n = 0; n < ns; n++) {
+        const int k = chunk_of(n);
+        put(rec_out, qb + k, s);
+        if ((r & 7) == 0) {
+            float* tv = gated_tvec(p, dslot, qb + k);
+            tv[i0] = t0;
+            tv[i0 + 1] = t1;
+        }
+        if (n + 1 < ns) {   // the next chunk's record and decays, a step ahead
+            rec(chunk_of(n + 1), dn);
+            en0 = p.ec[(qb + chunk_of(n + 1)) * 64 + i0];
+            en1 = p.ec[(qb + chunk_of(n + 1)) * 64 + i0 + 1];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float ec = e < 2 ? e0 : e1;
+            s[2 * e] = __ffma2_rn(make_float2(ec, ec), s[2 * e], make_float2(d[e].x, d[e].y));
+            s[2 * e + 1] = __ffma2_rn(make_float2(ec, ec), s[2 * e + 1], make_float2(d[e].z, d[e].w));
+        }
+        t0 *= e0;
+        t1 *= e1;
+#pragma unroll
+        for (int e = 0; e < 4; e++) d[e] = dn[e];
+        e0 = en0;
+        e1 = en1;
+    }
+    // the segment's final X and its transition Pi (record [1], its first 64 floats)
+    put(seg_rec(p, dslot, u, sg, 0), 0, s);
+    if ((r & 7) == 0) {
+        float* pi = seg_rec(p, dslot, u, sg, 1);
+        pi[i0] = t0;
+        pi[i0 + 1] = t1;
+    }
+}
+
+// The scan over a unit's segments, one CTA of 256 threads per (unit, sweep), elementwise: forward S_1 = X_0,
+// S_{s+1} = Pi_s (.) S_s + X_s; reverse E_{P-2} = X_{P-1}, E_{s-1} = Pi_s (.) E_s + X_s, and dh0 = Pi_0 (.) E_0 + X_0.
+// Each segment's start goes to its record [2].
+__global__ void __launch_bounds__(256) chunk_gated_scan_kernel(const __grid_constant__ CbParams p)
+{
+    const bool rev = p.rev_only || blockIdx.y == 1;
+    const int dslot = p.rev_only ? 0 : (int)blockIdx.y;
+    const int u = blockIdx.x, r = threadIdx.x, i0 = 2 * (r >> 3), j0 = 8 * (r & 7);
+    const int P = p.nseg;
+    auto seg_of = [&](int t) { return rev ? P - 1 - t : t; };
+    auto load = [&](const float* base, float4 (&v)[4]) {
+        v[0] = *rec4(base, 0, i0, j0);
+        v[1] = *rec4(base, 0, i0, j0 + 4);
+        v[2] = *rec4(base, 0, i0 + 1, j0);
+        v[3] = *rec4(base, 0, i0 + 1, j0 + 4);
+    };
+    float4 cur[4];
+    load(seg_rec(p, dslot, u, seg_of(0), 0), cur);
+    auto fold = [&](int sg) {   // cur <- Pi_sg (.) cur + X_sg
+        const float* pi = seg_rec(p, dslot, u, sg, 1);
+        const float p0 = pi[i0], p1 = pi[i0 + 1];
+        float4 x[4];
+        load(seg_rec(p, dslot, u, sg, 0), x);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float pv = e < 2 ? p0 : p1;
+            cur[e] = make_float4(fmaf(pv, cur[e].x, x[e].x), fmaf(pv, cur[e].y, x[e].y), fmaf(pv, cur[e].z, x[e].z),
+                                 fmaf(pv, cur[e].w, x[e].w));
+        }
+    };
+    for (int t = 1; t < P; t++) {
+        float* dst = seg_rec(p, dslot, u, seg_of(t), 2);   // cur is this segment's true start
+        *rec4(dst, 0, i0, j0) = cur[0];
+        *rec4(dst, 0, i0, j0 + 4) = cur[1];
+        *rec4(dst, 0, i0 + 1, j0) = cur[2];
+        *rec4(dst, 0, i0 + 1, j0 + 4) = cur[3];
+        if (t + 1 < P || rev) fold(seg_of(t));
+    }
+    if (rev && p.dh0) {
+        // cur is the adjoint at the sequence's start
+        const float v[2][8] = {{cur[0].x, cur[0].y, cur[0].z, cur[0].w, cur[1].x, cur[1].y, cur[1].z, cur[1].w},
+                               {cur[2].x, cur[2].y, cur[2].z, cur[2].w, cur[3].x, cur[3].y, cur[3].z, cur[3].w}};
+#pragma unroll
+        for (int a = 0; a < 2; a++)
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const int i = i0 + a, j = j0 + e;
+                if (i < p.dk && j < p.dv_) p.dh0[((size_t)u * p.dk + i) * p.dv_ + j] = v[a][e];
+            }
+    }
+}
+
+// The fix-up, one CTA of 256 threads per (chunk, sweep): record += T_k (.) S_s for the chunks of every segment
+// that did not start from the sequence's own start.
+__global__ void __launch_bounds__(256) chunk_gated_fix_kernel(const __grid_constant__ CbParams p)
+{
+    const bool rev = p.rev_only || blockIdx.y == 1;
+    const int dslot = p.rev_only ? 0 : (int)blockIdx.y;
+    const int q = blockIdx.x, u = q / p.nchunks, k = q - u * p.nchunks, sg = k / p.seg_len;
+    if (rev ? sg == p.nseg - 1 : sg == 0) return;   // those records are true already
+    const int r = threadIdx.x, i0 = 2 * (r >> 3), j0 = 8 * (r & 7);
+    const float* S = seg_rec(p, dslot, u, sg, 2);
+    const float* tv = gated_tvec(p, dslot, (size_t)q);
+    float* out = rev ? p.dst : p.st;
+    const float ta = tv[i0], tb = tv[i0 + 1];
+#pragma unroll
+    for (int a = 0; a < 2; a++)
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+            const float t = a ? tb : ta;
+            float4* o = rec4(out, (size_t)q, i0 + a, j0 + 4 * c);
+            const float4 sv = *rec4(S, 0, i0 + a, j0 + 4 * c);
+            const float4 x = *o;
+            *o = make_float4(fmaf(t, sv.x, x.x), fmaf(t, sv.y, x.y), fmaf(t, sv.z, x.z), fmaf(t, sv.w, x.w));
+        }
+}
+
 // ---------------------------------------------------------------- the forward split in time by walks (delta)
 // A long sequence over few heads is cut into P segments of seg_len chunks.  The tcgen05 forward runs every segment
 // from a zero state (the segments as batch rows) and keeps its residuals, so that the per-chunk maps are at hand:
@@ -3098,6 +3262,7 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
     p.sv_stride = a.mode == GDN_DELTA ? sv::BYTES : sv::GATED_BYTES;
     p.nseg = chain_segments(a.mode, a.B * a.H, p.nchunks, a.saved ? 1 : 2, &p.seg_len);
     p.segrec = (float*)(ws + Lw.cb_seg_off);
+    p.tvec = (float*)(ws + Lw.cb_tvec_off);
     if (a.saved) {
         // residuals of a saving forward: the entering states, then the solve's results (gated: P)
         p.st = (float*)a.saved;
@@ -3150,6 +3315,11 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
         chunk_chain_walk_kernel<false><<<dim3(units, p.nseg, dirs), CT_THREADS, walk_smem(false), st>>>(p);
     } else if (delta) {
         chunk_chain_tc_kernel<<<units, CT_THREADS, CHAIN_TC_SMEM, st>>>(p);
+    } else if (p.nseg > 1) {
+        // gated, split in time: local walks per segment, an elementwise scan, the records' fix-up
+        chunk_chain_gated_seg_kernel<<<dim3(units, p.nseg, dirs), 256, 0, st>>>(p);
+        chunk_gated_scan_kernel<<<dim3(units, dirs), 256, 0, st>>>(p);
+        chunk_gated_fix_kernel<<<dim3(p.nq, dirs), 256, 0, st>>>(p);
     } else {
         chunk_chain_gated_kernel<<<units, 256, 0, st>>>(p);
     }

@@ -64,7 +64,8 @@ struct WsLayout {
     size_t cb_dst_off = 0;        // the adjoint of the state leaving the chunk
     size_t cb_ec_off = 0;         // gated: the chunk's decay [B*H*chunks][64]
     size_t cb_da_off = 0;         // per-chunk dA partials [B*H*chunks][64]
-    size_t cb_seg_off = 0;        // delta, chain split in time: per (direction, unit, segment) three 64 x 64 fp32 records
+    size_t cb_seg_off = 0;        // chain split in time: per (direction, unit, segment) three 64 x 64 fp32 records
+    size_t cb_tvec_off = 0;       // gated chain split in time: per (direction, chunk) 64 decay products
     // forward split in time by walks (delta, bf16): also ts_h_off (the zero-start run's final states), ts_o_off
     // (its fp32 outputs), cb_phi_off (Phi per chunk) and cb_seg_off (per segment X, Pi, true start)
     size_t fw_res_off = 0;        // the residuals when the caller keeps none (states, then the solve's results)
@@ -115,14 +116,15 @@ inline int fwd_walk_split(const gdn_shape_t& s, int logits, int norm, int* seg_l
     if (seg_len) *seg_len = (int)L;
     return (int)((nk + L - 1) / L);
 }
-// The chunked backward's chain split in time (delta only; gated chains are elementwise and cheap): its `dirs`
-// sweeps (2, or 1 from the forward's residuals) over `units` (batch, head) units run as dirs * units * nseg walks
-// side by side, one per SM (at most 152), each over a segment of *seg_len chunks (at least 16).  Splits when that
-// gives at least 2 segments of a sequence of at least 32 chunks.  Returns nseg (1 = no split).
+// The chunked backward's chain split in time: its `dirs` sweeps (2, or 1 from the forward's residuals) over `units`
+// (batch, head) units run as dirs * units * nseg walks side by side (at most 152), each over a segment of *seg_len
+// chunks (at least 16).  Splits when that gives at least 2 segments of a sequence of at least 32 chunks.  Returns
+// nseg (1 = no split).
 inline int chain_segments(int mode, long units, int nchunks, int dirs, int* seg_len)
 {
     int P = 1;
-    if (mode == GDN_DELTA && units > 0 && nchunks >= 32) {
+    (void)mode;
+    if (units > 0 && nchunks >= 32) {
         const long fit = kSplitSMs / (dirs * units);
         P = fit < nchunks / 16 ? (int)fit : nchunks / 16;
         if (P < 2) P = 1;

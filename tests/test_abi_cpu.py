@@ -182,16 +182,19 @@ def test_chunked_backward_workspace():
             s = gdn.make_shape(B, H, T, d, d, mode, "bf16")
             nk = -(-T // 64)
             nq = B * H * nk
-            # delta chains over few heads split in time: segments of >= 16 chunks, 2 sweeps x heads x segments
-            # <= 152; each (sweep, head, segment) then keeps three 16 KB records
+            # chains over few heads split in time: segments of >= 16 chunks, 2 sweeps x heads x segments <= 152;
+            # each (sweep, head, segment) then keeps three 16 KB records, and gated each (sweep, chunk) the rows'
+            # 64 decay products
             units, nseg = B * H, 1
             P = min(152 // (2 * units), nk // 16)
-            if mode == "delta" and nk >= 32 and P >= 2:
+            if nk >= 32 and P >= 2:
                 L = -(-nk // P)
                 nseg = -(-nk // L)
             want = 256 + per_chunk * nq + 2 * -(-(nq * 256) // 256) * 256
             if nseg > 1:
                 want += 2 * units * nseg * 3 * 16384
+                if mode == "gated":
+                    want += 2 * nq * 256
             if units == 128 and T == 4096:
                 # heads filling most of a wave: the saving forward recomputes the residuals (a 16 KB state and the
                 # solve's 80 KB, gated the 16 KB scores) and outputs into the workspace, then the backward from them
@@ -267,7 +270,7 @@ def test_plan_reports_split_and_kernel():
     # heads x 4 <= 152), from the forward's residuals (the reverse sweep alone) into 9 of 57 (16 x 9 <= 152)
     assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=1) == (4, K.GDN_KERNEL_NONE)
     assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=2) == (9, K.GDN_KERNEL_NONE)
-    assert plan(1, 16, 32768, 64, 64, "gated", "bf16", bw=1) == (1, K.GDN_KERNEL_NONE)   # gated chain: not split
+    assert plan(1, 16, 32768, 64, 64, "gated", "bf16", bw=1) == (4, K.GDN_KERNEL_NONE)   # gated chain split too
     assert plan(1, 16, 1024, 64, 64, "delta", "bf16", bw=1) == (1, K.GDN_KERNEL_NONE)    # 16 chunks: too short
     assert plan(1, 16, 32768, 64, 64, "delta", "bf16", bw=1, gate_logits=True) == (8, K.GDN_KERNEL_TENSOR_CORE)
     assert plan(8, 16, 4096, 64, 64, "delta", "bf16") == (1, K.GDN_KERNEL_TENSOR_CORE)
@@ -323,10 +326,10 @@ def test_plan_and_workspace_agree_on_random_shapes():
             chunked = io == "bf16" and dk <= 64 and dv <= 64 and T > 0
             assert P >= 1
             if bw and chunked:
-                # the chunked backward splits only its chain, in delta mode, into segments of >= 16 whole chunks
+                # the chunked backward splits only its chain, into segments of >= 16 whole chunks
                 # (the last one may be shorter), at most 152 (sweep, unit, segment) walks
                 nk = -(-T // 64)
-                assert P == 1 or (mode == "delta" and 2 * B * H * P <= 152 and -(-nk // P) >= 16
+                assert P == 1 or (2 * B * H * P <= 152 and -(-nk // P) >= 16
                                   and (P - 1) * -(-nk // P) < nk), (B, H, T, P)
             elif not bw and chunked:
                 # the split by walks: segments of at least 8 whole chunks (the last may be shorter), any length
