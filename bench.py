@@ -134,7 +134,7 @@ def fwd_launches(w, saving=False):
     """Kernels one gdn_fwd call (gdn_fwd_save if saving) launches."""
     if tsplit_factor(w, False) == 1:
         return 1
-    if w.mode == "delta" and saved_bytes(w) > 0:
+    if saved_bytes(w) > 0:
         # the split by walks: zero-start run, Phi and Qc, transition walks, scan, output walks (and, saving, the
         # residuals' fix-up)
         return 6 if saving else 5
