@@ -125,7 +125,7 @@ static size_t place_chunk_bwd(const gdn_shape_t& s, WsLayout& L, size_t off, boo
             off = round_up(off + nq * kSavedSolveBytes, 256);
         }
     }
-    if (!from_saved || s.mode != GDN_DELTA) {   // (the gated prep writes Delta either way)
+    if (!from_saved) {
         L.cb_dlt_off = off;
         off = round_up(off + rec, 256);
     }

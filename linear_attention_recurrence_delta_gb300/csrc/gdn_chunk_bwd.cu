@@ -101,7 +101,7 @@ struct CbParams {
     // the forward split in time by walks (delta): prep writes [Phi_hi | Qc_hi | Phi_lo | Qc_lo] per chunk to phi
     // and no Y; a saving forward's second walk writes D = T_k S_s to st for the residual fix-up
     int fwd_walks;
-    int fw_gated;         // gated mode: Phi = diag(E) and Qc = Ctil come from g and c alone (no residuals read)
+    int gated;            // prep from residuals, gated mode: Phi = diag(E) and Qc = Ctil come from g and c alone
     const float* fw_o32;  // the zero-start run's outputs, fp32 [B, T, H, d_v]
     __nv_bfloat16* fw_o;  // the outputs
     float* fw_st;         // saving: the residual states, made true by adding D (null: not saving)
@@ -1150,9 +1150,10 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
     auto issue = [&](int q) {
         if (q == p.starve) return;   // failure-path test hook
         const int u = q / p.nchunks, k = q - u * p.nchunks, bb = u / p.H, h = u - bb * p.H;
-        if (p.fw_gated) {   // Phi and Qc of a gated chunk need its c tile alone
-            mbar_arrive_expect_tx(&S.full, 8192);
+        if (p.gated) {   // a gated chunk needs its c tile alone (and dO for Y)
+            mbar_arrive_expect_tx(&S.full, p.fwd_walks ? 8192 : 16384);
             tma_load_4d(sm + ps::STC, &p.tm_c, &S.full, 0, h, 64 * k, bb);
+            if (!p.fwd_walks) tma_load_4d(sm + ps::STDO, &p.tm_do, &S.full, 0, h, 64 * k, bb);
             return;
         }
         mbar_arrive_expect_tx(&S.full, (p.fwd_walks ? 2 : 3) * 8192 + 32768);
@@ -1193,9 +1194,9 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             const int qn = q + gridDim.x, un = qn / p.nchunks, kn = qn - un * p.nchunks, bn = un / p.H,
                       hn = un - bn * p.H;
             tma_prefetch_l2(&p.tm_c, 0, hn, 64 * kn, bn);
-            if (!p.fw_gated) {
+            if (!p.fwd_walks) tma_prefetch_l2(&p.tm_do, 0, hn, 64 * kn, bn);
+            if (!p.gated) {
                 tma_prefetch_l2(&p.tm_b, 0, hn, 64 * kn, bn);
-                if (!p.fwd_walks) tma_prefetch_l2(&p.tm_do, 0, hn, 64 * kn, bn);
                 const unsigned char* rq = p.sv + (size_t)qn * p.sv_stride;
                 prefetch_l2_bulk(rq + sv::P, 16384);
                 prefetch_l2_bulk(rq + sv::NW, 16384);
@@ -1220,7 +1221,7 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             S.G[2 * lane + 1] = x;
         }
         named_bar_sync(1, 256);
-        if (!p.fw_gated) {
+        if (!p.gated) {
             // Bhat = b (.) exp(A (G_63 - G_t)), thread = (token t, 16 channels)
             const int t = r & 63, cq = r >> 6;
             float bv[16], y[16];
@@ -1231,7 +1232,7 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             st16_split(sm + ps::BH, sm + ps::BH + 8192, t, cq, y);
         }
         sync_all();
-        if (r == 0 && !p.fw_gated) {
+        if (r == 0 && !p.gated) {
             const uint32_t bh = smem_u32(sm + ps::BH), pp = smem_u32(sm + ps::P), nw = smem_u32(sm + ps::NW);
             const uint32_t idA = idesc_bf16(128, 64, true, true), idB = idesc_bf16(128, 64, false, true);
             // Bhat^T (-W): TMEM columns 0..63, rows i
@@ -1244,7 +1245,7 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             mma_tiles(tb + 64, pp + 8192, false, 0, 0, nw, true, 8192, 0, 4, idB, true);
             mma_commit(&S.mma);
         }
-        if (!p.fw_gated && !wait_mma(0)) break;
+        if (!p.gated && !wait_mma(0)) break;
         if (q4 < 2) {
             // lanes 0..63: Phi row i out (hi/lo tiles), Qc row t = i = Ctil + P (-W) into its tiles (gated: W = 0)
             const int i = trow;
@@ -1257,7 +1258,7 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
             for (int h2 = 0; h2 < 2; h2++) {
                 const int cg = 2 * wh + h2;
                 float a[16], b[16], cv[16];
-                if (p.fw_gated) {
+                if (p.gated) {
 #pragma unroll
                     for (int e = 0; e < 16; e++) a[e] = b[e] = 0.f;
                 } else {
@@ -1267,7 +1268,8 @@ __global__ void __launch_bounds__(256, 3) chunk_prep_saved_kernel(const __grid_c
                 }
 #pragma unroll
                 for (int e = 0; e < 16; e++) a[e] += (16 * cg + e == i) ? ec : 0.f;
-                st16_split(phq, phq + lo, i, cg, a);
+                if (p.fwd_walks || !p.gated) st16_split(phq, phq + lo, i, cg, a);   // (the gated chain takes E)
+                else if (h2 == 0 && wh == 0) p.ec[(size_t)q * 64 + i] = ec;
                 ld16_bf16(sm + ps::STC, i, cg, cv);
 #pragma unroll
                 for (int e = 0; e < 16; e++) b[e] += cv[e] * fast_exp2(S.A2[16 * cg + e] * Gt);
@@ -2272,7 +2274,7 @@ struct FxSmall {
 
 __global__ void __launch_bounds__(256, 3) fwd_walk_res_kernel(const __grid_constant__ CbParams p)
 {
-    if (p.fw_gated) {
+    if (p.gated) {
         // gated residuals keep no U: the state alone, S += D (thread = row i, 16 columns)
         const int i = threadIdx.x & 63, cq = threadIdx.x >> 6;
         for (int q = blockIdx.x; q < p.nq; q += gridDim.x)
@@ -3298,8 +3300,12 @@ cudaError_t launch_chunk_bwd(const Args& a, const WsLayout& Lw, cudaStream_t st)
 #define CB_MARK(what)
 #endif
     CB_MARK("start");
-    if (a.saved && delta) chunk_prep_saved_kernel<<<p.nq < 3 * sms ? p.nq : 3 * sms, 256, ps::SMEM, st>>>(p);
-    else if (delta) chunk_prep_kernel<true><<<grid, kThreads, prep_bytes, st>>>(p);
+    if (a.saved) {
+        // from the residuals: delta Phi and Y; gated Y and the chunks' decays E alone
+        CbParams pg = p;
+        pg.gated = !delta;
+        chunk_prep_saved_kernel<<<p.nq < 3 * sms ? p.nq : 3 * sms, 256, ps::SMEM, st>>>(pg);
+    } else if (delta) chunk_prep_kernel<true><<<grid, kThreads, prep_bytes, st>>>(p);
     else chunk_prep_kernel<false><<<grid, kThreads, prep_bytes, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -3371,7 +3377,7 @@ cudaError_t launch_fwd_walks(const Args& a, const WsLayout& Lw, cudaStream_t st)
     p.phi = ws + Lw.cb_phi_off;
     p.sv = res + (size_t)units * nk * kSavedStateBytes;
     p.st = (float*)(ws + Lw.fw_d_off);   // the second walk's records D
-    p.fw_gated = a.mode == GDN_GATED;
+    p.gated = a.mode == GDN_GATED;
     p.status = (uint32_t*)a.ws;
     p.B = a.B; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv_ = a.dv;
     p.nchunks = nk;
