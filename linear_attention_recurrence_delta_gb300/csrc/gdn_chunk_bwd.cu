@@ -1349,9 +1349,8 @@ __global__ void __launch_bounds__(256) chunk_chain_gated_kernel(const __grid_con
                                in && j + 1 < dv ? src[((size_t)u * dk + i) * dv + j + 1] : 0.f);
         }
     };
-    // s <- E (.) s + d, E of the chunk's rows i0, i0 + 1
-    auto advance = [&](int k, const float4 (&d)[4], float2 (&s)[8]) {
-        const float e0 = p.ec[(qb + k) * 64 + i0], e1 = p.ec[(qb + k) * 64 + i0 + 1];
+    // s <- E (.) s + d, E = (e0, e1) of the chunk's rows i0, i0 + 1
+    auto advance = [&](float e0, float e1, const float4 (&d)[4], float2 (&s)[8]) {
 #pragma unroll
         for (int e = 0; e < 4; e++) {
             const float ec = e < 2 ? e0 : e1;
@@ -1360,27 +1359,44 @@ __global__ void __launch_bounds__(256) chunk_chain_gated_kernel(const __grid_con
             s[2 * e + 1] = __ffma2_rn(make_float2(ec, ec), s[2 * e + 1], make_float2(dd.z, dd.w));
         }
     };
+    auto ec_of = [&](int k, float& e0, float& e1) {
+        e0 = p.ec[(qb + k) * 64 + i0];
+        e1 = p.ec[(qb + k) * 64 + i0 + 1];
+    };
     float2 s[8];
     float4 d[4], dn[4];
+    float e0, e1, en0 = 0.f, en1 = 0.f;   // the chunk's decays, and the next chunk's, loaded a step ahead
     if (!p.rev_only) {   // (with a saving forward's states only the reverse sweep runs)
         load_in(p.h0, s);
         rec(p.dlt, 0, d);
+        ec_of(0, e0, e1);
         for (int k = 0; k < nk; k++) {
             put(p.st, k, s);
-            if (k + 1 < nk) rec(p.dlt, k + 1, dn);
-            advance(k, d, s);
+            if (k + 1 < nk) {
+                rec(p.dlt, k + 1, dn);
+                ec_of(k + 1, en0, en1);
+            }
+            advance(e0, e1, d, s);
 #pragma unroll
             for (int e = 0; e < 4; e++) d[e] = dn[e];
+            e0 = en0;
+            e1 = en1;
         }
     }
     load_in(p.dhT, s);
     rec(p.ych, nk - 1, d);
+    ec_of(nk - 1, e0, e1);
     for (int k = nk - 1; k >= 0; k--) {
         put(p.dst, k, s);
-        if (k > 0) rec(p.ych, k - 1, dn);
-        advance(k, d, s);
+        if (k > 0) {
+            rec(p.ych, k - 1, dn);
+            ec_of(k - 1, en0, en1);
+        }
+        advance(e0, e1, d, s);
 #pragma unroll
         for (int e = 0; e < 4; e++) d[e] = dn[e];
+        e0 = en0;
+        e1 = en1;
     }
     if (p.dh0) {
 #pragma unroll
