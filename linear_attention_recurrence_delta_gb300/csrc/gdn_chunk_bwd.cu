@@ -2127,8 +2127,17 @@ __global__ void __launch_bounds__(fw_threads(OUT), 1) fwd_walk_kernel(const __gr
     const bool orow = OUT && (warp & 2);
     auto issue_copy = [&](int n) {
         const int s = n % CT_NS;
-        mbar_arrive_expect_tx(&full[s], FW_STAGE);
-        bulk_g2s(sm + s * FW_STAGE, p.phi + (qb + k0 + n) * FW_STAGE, FW_STAGE, &full[s]);
+        const unsigned char* src = p.phi + (qb + k0 + n) * FW_STAGE;
+        if (OUT) {
+            mbar_arrive_expect_tx(&full[s], FW_STAGE);
+            bulk_g2s(sm + s * FW_STAGE, src, FW_STAGE, &full[s]);
+        } else {
+            // the transitions need Phi alone: its hi and lo tiles (the Qc rows of the stage feed TMEM rows
+            // 64..127, which this walk never reads)
+            mbar_arrive_expect_tx(&full[s], 16384);
+            bulk_g2s(sm + s * FW_STAGE, src, 8192, &full[s]);
+            bulk_g2s(sm + s * FW_STAGE + 16384, src + 16384, 8192, &full[s]);
+        }
     };
     if (r == 0) {
         for (int s = 0; s < CT_NS; s++) mbar_init(&full[s], 1);
