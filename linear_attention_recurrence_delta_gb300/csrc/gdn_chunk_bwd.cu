@@ -2417,6 +2417,90 @@ __global__ void __launch_bounds__(256, 3) fwd_walk_res_kernel(const __grid_const
 }
 
 // ================================================================= pass 3: gradients
+// The near pairs' adjoint, one 4-column group sg of a 16-block at a time (rows tl0 .. tl0 + 3 of the block, channels
+// nch .. nch + 3).  NQ / NK: the block's near dQ / dK entries ([16][20] fp32, zero above the diagonal).  Row side
+// (t as row): aP[4 ti + e] += dQ[t][s] y_s[e] and aK likewise with dK, y = b / alpha (times KL across the halves).
+// Column side (t as column): aP += dQ[s][t] c_s[e] x_s[e], aK += dK[s][t] b_s[e] x_s[e], x = left alpha (times KU
+// across the halves, where both sums go into aP).  Every load of the group is issued before its products, and
+// the accumulator each product feeds is fixed at compile time.
+template <bool DELTA, bool CROSS>
+__device__ __forceinline__ void near_rows_rev(const float* NQ, const float* NK, const float* yb, int tl0, int sg,
+                                              const float* kl, float* aP, float* aK)
+{
+    float dq[4][4], dk[4][4], y[4][4];
+#pragma unroll
+    for (int ti = 0; ti < 4; ti++) {
+        const float4 q4 = *reinterpret_cast<const float4*>(NQ + (tl0 + ti) * 20 + 4 * sg);
+        dq[ti][0] = q4.x; dq[ti][1] = q4.y; dq[ti][2] = q4.z; dq[ti][3] = q4.w;
+        if (DELTA) {
+            const float4 k4 = *reinterpret_cast<const float4*>(NK + (tl0 + ti) * 20 + 4 * sg);
+            dk[ti][0] = k4.x; dk[ti][1] = k4.y; dk[ti][2] = k4.z; dk[ti][3] = k4.w;
+        }
+    }
+#pragma unroll
+    for (int si = 0; si < 4; si++) {
+        const float4 y4 = *reinterpret_cast<const float4*>(yb + (4 * sg + si) * kAS);
+        y[si][0] = y4.x; y[si][1] = y4.y; y[si][2] = y4.z; y[si][3] = y4.w;
+        if (CROSS) {
+#pragma unroll
+            for (int e = 0; e < 4; e++) y[si][e] *= kl[e];
+        }
+    }
+#pragma unroll
+    for (int si = 0; si < 4; si++)
+#pragma unroll
+        for (int ti = 0; ti < 4; ti++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                aP[4 * ti + e] = fmaf(dq[ti][si], y[si][e], aP[4 * ti + e]);
+                if (DELTA) aK[4 * ti + e] = fmaf(dk[ti][si], y[si][e], aK[4 * ti + e]);
+            }
+}
+
+template <bool DELTA, bool CROSS>
+__device__ __forceinline__ void near_cols_rev(const float* NQ, const float* NK, const float* alpha,
+                                              const unsigned char* sC, const unsigned char* sB, int tl0, int sb, int sg,
+                                              int nch, const float* ku, float* aP, float* aK)
+{
+    float dq[4][4], dk[4][4], x[4][4], c4[4][4], b4[4][4];   // dq, dk: [si][ti] = dM[s][t]
+#pragma unroll
+    for (int si = 0; si < 4; si++) {
+        const float4 q4 = *reinterpret_cast<const float4*>(NQ + (4 * sg + si) * 20 + tl0);
+        dq[si][0] = q4.x; dq[si][1] = q4.y; dq[si][2] = q4.z; dq[si][3] = q4.w;
+        if (DELTA) {
+            const float4 k4 = *reinterpret_cast<const float4*>(NK + (4 * sg + si) * 20 + tl0);
+            dk[si][0] = k4.x; dk[si][1] = k4.y; dk[si][2] = k4.z; dk[si][3] = k4.w;
+        }
+    }
+#pragma unroll
+    for (int si = 0; si < 4; si++) {
+        const int s = sb + 4 * sg + si;
+        const float4 a4 = *reinterpret_cast<const float4*>(alpha + s * kAS + nch);
+        x[si][0] = a4.x; x[si][1] = a4.y; x[si][2] = a4.z; x[si][3] = a4.w;
+        if (CROSS) {
+#pragma unroll
+            for (int e = 0; e < 4; e++) x[si][e] *= ku[e];
+        }
+        ld4_bf16(sC, s, nch, c4[si]);
+        ld4_bf16(sB, s, nch, b4[si]);
+    }
+#pragma unroll
+    for (int si = 0; si < 4; si++)
+#pragma unroll
+        for (int ti = 0; ti < 4; ti++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const float xc = c4[si][e] * x[si][e], xb = b4[si][e] * x[si][e];
+                if (CROSS) {
+                    const float in = DELTA ? fmaf(dk[si][ti], xb, aP[4 * ti + e]) : aP[4 * ti + e];
+                    aP[4 * ti + e] = fmaf(dq[si][ti], xc, in);
+                } else {
+                    aP[4 * ti + e] = fmaf(dq[si][ti], xc, aP[4 * ti + e]);
+                    if (DELTA) aK[4 * ti + e] = fmaf(dk[si][ti], xb, aK[4 * ti + e]);
+                }
+            }
+}
+
 template <bool DELTA>
 __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_constant__ CbParams p)
 {
@@ -2830,7 +2914,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         // warp-uniform.  Row side (t as row): sums over s of dM[t][s] y_s, column side (t as column): sums over s of
         // dM[s][t] x_s, with y = b / alpha, x = left alpha within an 8-half and the KL / KU factors across the
         // halves, kept in their own sums so that no factor leaves fp32's range.  The near dQ, dK are zero above
-        // the diagonal, so no mask is needed.
+        // the diagonal, so no mask is needed: each side takes the two 4-column groups of its own 8-half, and the
+        // upper rows (row side) or the lower columns (column side) the two of the other half.
         const int nJ = c.r >> 6, ntq = (c.r >> 4) & 3, ncg = c.r & 15;
         const int nt0 = 16 * nJ + 4 * ntq, nch = 4 * ncg;
         float nc[16], nb[16], ng[16];   // [token ti][channel e] at 4 ti + e
@@ -2839,140 +2924,66 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             const float* NQ = ND + (0 * 4 + nJ) * 16 * 20;
             const float* NK = ND + (1 * 4 + nJ) * 16 * 20;
             const bool up = ntq >= 2;
-            const int tl0 = 4 * ntq;
-            float al[16], ai[16], cv[16], bv[16], ku[4], kl[4];
+            const int tl0 = 4 * ntq, sg0 = up ? 2 : 0;
+            float ku[4], kl[4];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
                 ku[e] = c.KT->KU[nJ][nch + e];
                 kl[e] = c.KT->KL[nJ][nch + e];
             }
-#pragma unroll
-            for (int ti = 0; ti < 4; ti++) {
-                const int t = nt0 + ti;
-                const float dGa = S.G[t] - S.G[8 * (t >> 3) + 3];
-                const float4 a4 = *reinterpret_cast<const float4*>(c.ALPHA + t * kAS + nch);
-                al[4 * ti] = a4.x; al[4 * ti + 1] = a4.y; al[4 * ti + 2] = a4.z; al[4 * ti + 3] = a4.w;
-#pragma unroll
-                for (int e = 0; e < 4; e++) ai[4 * ti + e] = fast_exp2(-S.A2[nch + e] * dGa);
-                float v4[4];
-                ld4_bf16(sC, t, nch, v4);
-#pragma unroll
-                for (int e = 0; e < 4; e++) cv[4 * ti + e] = v4[e];
-                ld4_bf16(sB, t, nch, v4);
-#pragma unroll
-                for (int e = 0; e < 4; e++) bv[4 * ti + e] = v4[e];
-            }
             if (!S.unsafe) {
-                // row side: s over the block, 4 at a time; same half (s in tokens of my half) or across (my half
-                // upper, s lower)
-                float rP[16], rK[16], rPx[16], rKx[16];
+                {
+                    float rP[16], rK[16], rPx[16], rKx[16];
 #pragma unroll
-                for (int e = 0; e < 16; e++) rP[e] = rK[e] = rPx[e] = rKx[e] = 0.f;
+                    for (int e = 0; e < 16; e++) rP[e] = rK[e] = rPx[e] = rKx[e] = 0.f;
+                    const float* yb = c.YB + 16 * nJ * kAS + nch;
 #pragma unroll 1
-                for (int sg = 0; sg < 4; sg++) {
-                    // lower rows: s < 8 only (entries above the diagonal are zero)
-                    if (!up && sg >= 2) continue;
-                    const bool xs = up && sg < 2;   // columns in the lower half of an upper row
-                    float dq[4][4], dkk[4][4];
+                    for (int j = 0; j < 2; j++) near_rows_rev<DELTA, false>(NQ, NK, yb, tl0, sg0 + j, kl, rP, rK);
+                    if (up) {
+#pragma unroll 1
+                        for (int j = 0; j < 2; j++) near_rows_rev<DELTA, true>(NQ, NK, yb, tl0, j, kl, rPx, rKx);
+                    }
 #pragma unroll
                     for (int ti = 0; ti < 4; ti++) {
-                        const float4 q4 = *reinterpret_cast<const float4*>(NQ + (tl0 + ti) * 20 + 4 * sg);
-                        dq[ti][0] = q4.x; dq[ti][1] = q4.y; dq[ti][2] = q4.z; dq[ti][3] = q4.w;
-                        if (DELTA) {
-                            const float4 k4 = *reinterpret_cast<const float4*>(NK + (tl0 + ti) * 20 + 4 * sg);
-                            dkk[ti][0] = k4.x; dkk[ti][1] = k4.y; dkk[ti][2] = k4.z; dkk[ti][3] = k4.w;
-                        } else {
-                            dkk[ti][0] = dkk[ti][1] = dkk[ti][2] = dkk[ti][3] = 0.f;
+                        const float4 a4 = *reinterpret_cast<const float4*>(c.ALPHA + (nt0 + ti) * kAS + nch);
+                        const float al[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const int k = 4 * ti + e;
+                            const float ax = up ? al[e] * ku[e] : 0.f;   // alpha_t KU
+                            nc[k] = al[e] * rP[k] + ax * rPx[k];
+                            nb[k] = al[e] * rK[k] + ax * rKx[k];
                         }
-                    }
-#pragma unroll
-                    for (int si = 0; si < 4; si++) {
-                        const int s = 16 * nJ + 4 * sg + si;
-                        const float4 y4 = *reinterpret_cast<const float4*>(c.YB + s * kAS + nch);
-                        float y[4] = {y4.x, y4.y, y4.z, y4.w};
-                        if (xs) {
-#pragma unroll
-                            for (int e = 0; e < 4; e++) y[e] *= kl[e];
-                        }
-#pragma unroll
-                        for (int ti = 0; ti < 4; ti++)
-#pragma unroll
-                            for (int e = 0; e < 4; e++) {
-                                if (xs) {
-                                    rPx[4 * ti + e] = fmaf(dq[ti][si], y[e], rPx[4 * ti + e]);
-                                    rKx[4 * ti + e] = fmaf(dkk[ti][si], y[e], rKx[4 * ti + e]);
-                                } else {
-                                    rP[4 * ti + e] = fmaf(dq[ti][si], y[e], rP[4 * ti + e]);
-                                    rK[4 * ti + e] = fmaf(dkk[ti][si], y[e], rK[4 * ti + e]);
-                                }
-                            }
                     }
                 }
-#pragma unroll
-                for (int ti = 0; ti < 4; ti++)
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int k = 4 * ti + e;
-                        const float ax = up ? al[k] * ku[e] : 0.f;   // alpha_t KU
-                        nc[k] = al[k] * rP[k] + ax * rPx[k];
-                        nb[k] = al[k] * rK[k] + ax * rKx[k];
-                    }
-                // column side: s >= t over the block; same half, or across (my half lower, s upper)
                 float cP[16], cK[16], cX[16];
 #pragma unroll
                 for (int e = 0; e < 16; e++) cP[e] = cK[e] = cX[e] = 0.f;
 #pragma unroll 1
-                for (int sg = 0; sg < 4; sg++) {
-                    if (up && sg < 2) continue;   // upper columns: s >= 8 only
-                    const bool xs = !up && sg >= 2;
-                    float dq[4][4], dkk[4][4];   // [si][ti] = dM[s][t]
-#pragma unroll
-                    for (int si = 0; si < 4; si++) {
-                        const float4 q4 = *reinterpret_cast<const float4*>(NQ + (4 * sg + si) * 20 + tl0);
-                        dq[si][0] = q4.x; dq[si][1] = q4.y; dq[si][2] = q4.z; dq[si][3] = q4.w;
-                        if (DELTA) {
-                            const float4 k4 = *reinterpret_cast<const float4*>(NK + (4 * sg + si) * 20 + tl0);
-                            dkk[si][0] = k4.x; dkk[si][1] = k4.y; dkk[si][2] = k4.z; dkk[si][3] = k4.w;
-                        } else {
-                            dkk[si][0] = dkk[si][1] = dkk[si][2] = dkk[si][3] = 0.f;
-                        }
-                    }
-#pragma unroll
-                    for (int si = 0; si < 4; si++) {
-                        const int s = 16 * nJ + 4 * sg + si;
-                        const float4 a4 = *reinterpret_cast<const float4*>(c.ALPHA + s * kAS + nch);
-                        float x[4] = {a4.x, a4.y, a4.z, a4.w};
-                        if (xs) {
-#pragma unroll
-                            for (int e = 0; e < 4; e++) x[e] *= ku[e];
-                        }
-                        float c4[4], b4[4];
-                        ld4_bf16(sC, s, nch, c4);
-                        ld4_bf16(sB, s, nch, b4);
-#pragma unroll
-                        for (int ti = 0; ti < 4; ti++)
-#pragma unroll
-                            for (int e = 0; e < 4; e++) {
-                                const float xc = c4[e] * x[e], xb = b4[e] * x[e];
-                                if (xs) {
-                                    cX[4 * ti + e] = fmaf(dq[si][ti], xc, fmaf(dkk[si][ti], xb, cX[4 * ti + e]));
-                                } else {
-                                    cP[4 * ti + e] = fmaf(dq[si][ti], xc, cP[4 * ti + e]);
-                                    cK[4 * ti + e] = fmaf(dkk[si][ti], xb, cK[4 * ti + e]);
-                                }
-                            }
-                    }
+                for (int j = 0; j < 2; j++)
+                    near_cols_rev<DELTA, false>(NQ, NK, c.ALPHA, sC, sB, tl0, 16 * nJ, sg0 + j, nch, ku, cP, cK);
+                if (!up) {
+#pragma unroll 1
+                    for (int j = 0; j < 2; j++)
+                        near_cols_rev<DELTA, true>(NQ, NK, c.ALPHA, sC, sB, tl0, 16 * nJ, 2 + j, nch, ku, cX, nullptr);
                 }
 #pragma unroll
-                for (int ti = 0; ti < 4; ti++)
+                for (int ti = 0; ti < 4; ti++) {
+                    const int t = nt0 + ti;
+                    const float dGa = S.G[t] - S.G[8 * (t >> 3) + 3];
+                    float cv[4], bv[4];
+                    ld4_bf16(sC, t, nch, cv);
+                    ld4_bf16(sB, t, nch, bv);
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
                         const int k = 4 * ti + e;
-                        const float cx = up ? 0.f : ai[k] * kl[e];   // KL / alpha_t
-                        const float dr = ai[k] * (cP[k] + cK[k]) + cx * cX[k];
-                        ng[k] = cv[k] * nc[k] + bv[k] * nb[k] - bv[k] * dr;
+                        const float ai = fast_exp2(-S.A2[nch + e] * dGa);
+                        const float cx = up ? 0.f : ai * kl[e];   // KL / alpha_t
+                        const float dr = ai * (cP[k] + cK[k]) + cx * cX[k];
+                        ng[k] = cv[e] * nc[k] + bv[e] * nb[k] - bv[e] * dr;
                         nb[k] += dr;
                     }
+                }
             } else {
                 // every factor evaluated directly (the anchors could overflow); exponents clamped at 0 where the
                 // weight is zero anyway
@@ -3003,11 +3014,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     }
                 }
 #pragma unroll
-                for (int k = 0; k < 16; k++) {
-                    const float dr = cP[k] + cK[k];
-                    nc[k] = rP[k];
-                    nb[k] = rK[k] + dr;
-                    ng[k] = cv[k] * rP[k] + bv[k] * rK[k] - bv[k] * dr;
+                for (int ti = 0; ti < 4; ti++) {
+                    float cv[4], bv[4];
+                    ld4_bf16(sC, nt0 + ti, nch, cv);
+                    ld4_bf16(sB, nt0 + ti, nch, bv);
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int k = 4 * ti + e;
+                        const float dr = cP[k] + cK[k];
+                        nc[k] = rP[k];
+                        nb[k] = rK[k] + dr;
+                        ng[k] = cv[e] * rP[k] + bv[e] * rK[k] - bv[e] * dr;
+                    }
                 }
             }
         }
