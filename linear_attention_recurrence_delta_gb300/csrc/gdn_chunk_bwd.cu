@@ -2821,7 +2821,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         CB_STAMP(1, 8);
         // ---- dQ (lanes 0..63) and dK = -beta (dR U^T) below the diagonal (lanes 64..127): the 16-block level's
         // operand A_d = [dQ | dK] by segments (fp16, K-major [t][seg], two 64-wide K blocks), the near entries in
-        // fp32; (delta) the rest of dbeta
+        // fp32
         {
             const int I = tt >> 4;
             const float bet = DELTA ? S.beta[tt] : 0.f;
@@ -2839,39 +2839,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                         const int s = 16 * g4 + e;
                         row[s] = isK ? ((DELTA && s < tt) ? -bet * v[g4][e] : 0.f) : (s <= tt ? v[g4][e] : 0.f);
                     }
-            }
-            if (DELTA && isK) {
-                // dbeta_t = sum_j dR V - sum_i Btil (dR S^T) - sum_{s<t} (dR U^T) K   (dMm = -dR U^T)
-                float part = 0.f;
-                const float Gt = S.G[tt];
-                // K's row tt from the saved front (L2), column-group major: both halves' loads under one wait
-                float4 krow[8];
-                {
-                    const float4* kr = reinterpret_cast<const float4*>(p.sv + (size_t)q * p.sv_stride + sv::K) + tt;
-#pragma unroll
-                    for (int e = 0; e < 8; e++) krow[e] = kr[(4 * (2 * wh + (e >> 2)) + (e & 3)) * 64];
-                }
-#pragma unroll 1
-                for (int h2 = 0; h2 < 2; h2++) {
-                    const int cg = 2 * wh + h2;
-                    float drs[16], dru[16], bv[16], kv[16];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const float4 x = h2 ? krow[4 + e] : krow[e];
-                        kv[4 * e] = x.x; kv[4 * e + 1] = x.y; kv[4 * e + 2] = x.z; kv[4 * e + 3] = x.w;
-                    }
-                    tmem_ld16(c.tl + 64 + 16 * cg, drs);
-                    tmem_ld16(c.tl + 16 * cg, dru);
-                    tmem_wait_ld();
-                    ld16_bf16(sB, tt, cg, bv);
-#pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        const int s = 16 * cg + e;
-                        part -= bv[e] * fast_exp2(S.A2[s] * Gt) * drs[e];
-                        if (s < tt) part -= dru[e] * kv[e];
-                    }
-                }
-                S.rs[1][wh][tt] = part;
             }
             // A_d row trow: segment I's columns (lo .. lo + 16 I) hold the row's values for s < 16 I
             const int lo16 = seg_base(I) >> 4;
@@ -3039,6 +3006,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         float* DG = fptr(X, gl::DG);
         float* PB = fptr(X, gl::PB);             // [64][gl::kES] dBhat Bhat, then G_t dGam
         float* SEGv = fptr(X, gl::SEG);          // [96][gl::kES] dB1 h1
+        // (delta, b-side rows) K's row tt from the saved front (L2), column-group major, for dbeta below: the loads
+        // run under the dense terms
+        float4 krow[8];
+        if (DELTA && isK) {
+            const float4* kr = reinterpret_cast<const float4*>(p.sv + (size_t)q * p.sv_stride + sv::K) + tt;
+#pragma unroll
+            for (int e = 0; e < 8; e++) krow[e] = kr[(4 * (2 * wh + (e >> 2)) + (e & 3)) * 64];
+        }
         if (!isK) {
             const int I = tt >> 4;
             const float Gt = S.G[tt], G63 = S.G[63], Gref = I >= 1 ? S.G[16 * I - 1] : 0.f;
@@ -3095,14 +3070,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         }
         bar_all();
         if (DELTA && isK) {
+            // the b-side rows' terms of dc, dg; and the rest of dbeta,
+            // dbeta_t = sum_j dR V - sum_i Btil (dR S^T) - sum_{s<t} (dR U^T) K   (dMm = -dR U^T),
+            // whose factors exp(Gam_t) are the same
             const int I = tt >> 4;
             const float Gt = S.G[tt], Gref = I >= 1 ? S.G[16 * I - 1] : 0.f, bet = S.beta[tt];
+            float part = 0.f;
 #pragma unroll 1
             for (int h2 = 0; h2 < 2; h2++) {
                 const int cg = 2 * wh + h2, c0 = 16 * cg;
-                float drs[16], da1[16], bv[16];
+                float drs[16], da1[16], dru[16], bv[16], kv[16];
                 tmem_ld16(c.tl + 64 + c0, drs);
                 tmem_ld16(c.tl + 192 + c0, da1);
+                tmem_ld16(c.tl + c0, dru);
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const float4 x = h2 ? krow[4 + e] : krow[e];
+                    kv[4 * e] = x.x; kv[4 * e + 1] = x.y; kv[4 * e + 2] = x.z; kv[4 * e + 3] = x.w;
+                }
                 tmem_wait_ld();
                 ld16_bf16(sB, tt, cg, bv);
 #pragma unroll
@@ -3120,22 +3105,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                         const float dbt = -bet * drs[e];   // dBtil
                         ob[k] += dbt * Et + da1[e] * f1;
                         og[k] += dbt * bv[e] * Et + da1[e] * f1 * bv[e];
+                        part -= bv[e] * Et * drs[e];
+                        if (c0 + e < tt) part -= dru[e] * kv[e];
                     }
                     *reinterpret_cast<float4*>(DB + at) = make_float4(ob[0], ob[1], ob[2], ob[3]);
                     *reinterpret_cast<float4*>(DG + at) = make_float4(og[0], og[1], og[2], og[3]);
                 }
             }
+            S.rs[1][wh][tt] = part;
         } else if (c.r < 64) {
             // column sums over tokens of dBhat Bhat (fixed order: four interleaved chains, then their sum)
             S.colsum[0][c.r] = sum64_fixed(PB + c.r, gl::kES);
-        }
-        if (DELTA && c.r >= 128 && c.r < 192) {
-            // dbeta of the chunk's tokens (both column halves of every part)
-            const int tq = c.r - 128;
-            if (tq < L) {
-                const float db_ = S.rs[0][0][tq] + S.rs[0][1][tq] + S.rs[1][0][tq] + S.rs[1][1][tq];
-                p.dbeta[((size_t)bb * p.T + t0 + tq) * p.H + h] = __float2bfloat16_rn(db_);
-            }
         }
         bar_all();
         CB_STAMP(1, 12);
@@ -3214,6 +3194,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             // dA partial: sum_t G_t dGam_t[i] (fixed order: four interleaved chains, then their sum)
             const int i = c.r - 64;
             p.dA_part[(size_t)q * 64 + i] = sum64_fixed(PB + i, gl::kES);
+        } else if (DELTA && c.r >= 128 && c.r < 192) {
+            // dbeta of the chunk's tokens (both column halves of every part)
+            const int tq = c.r - 128;
+            if (tq < L) {
+                const float db_ = S.rs[0][0][tq] + S.rs[0][1][tq] + S.rs[1][0][tq] + S.rs[1][1][tq];
+                p.dbeta[((size_t)bb * p.T + t0 + tq) * p.H + h] = __float2bfloat16_rn(db_);
+            }
         }
         CB_STAMP(1, 13);
         // the stage is free: the next chunk's loads
