@@ -130,6 +130,11 @@ struct Small {
 };
 static_assert(sizeof(Small) <= 4096, "the small-state block has a 4 KB slot");
 
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
 __device__ __forceinline__ void st_split16(unsigned char* thi, unsigned char* tlo, int row, int col16,
                                            const float (&v)[16])
 {
@@ -666,10 +671,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // one 16-column group of its row
             {
                 const bool isM = DELTA && q4 >= 2;
-                {
+                // two instances: the common one without the elementwise L3 entries of a chunk whose anchors could
+                // overflow (their registers and code stay out of it)
+                auto assemble = [&](auto us) {
+                    constexpr bool US = decltype(us)::value;
                     const int t = trow & 63, wl = q4 & 1, tb = t >> 4;
                     float ew[8];
-                    if (unsafe) {
+                    if (US) {
                         const int s0 = 8 * (t >> 3);
                         const float bet = DELTA ? S.beta[s][t] : 0.f;
 #pragma unroll
@@ -718,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                 if (sc > t || (isM && sc == t)) val = 0.f;
                                 else if ((sc >> 4) < tb) val = (tb == Ia) ? v1a[c] : v1b[c];
                                 else if ((sc >> 3) < (t >> 3)) val = v2[c];
-                                else val = unsafe ? ew[c & 7] : v3[c];
+                                else val = US ? ew[c & 7] : v3[c];
                                 out[c] = val;
                             }
                         }
@@ -759,7 +767,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             }
                         }
                     }
-                }
+                };
+                if (unsafe) assemble(BoolTag<true>{});
+                else assemble(BoolTag<false>{});
             }
             {
                 const int t = op_row(r), cq = r >> 6;   // the rows whose keep[] this thread holds
