@@ -169,7 +169,10 @@ static_assert(B1 >= ZR + 16384 && B1 + 96 * 128 <= U && A1H >= DOR + 16384 && B1
 constexpr int kES = 68;
 constexpr uint32_t SEG_END = SEG + 96 * kES * 4;
 constexpr uint32_t DC = 78848, DB = DC + 64 * kES * 4, DG = DB + 64 * kES * 4, PB = SEG_END;
-static_assert(PB + 64 * kES * 4 <= DC && DG + 64 * kES * 4 <= BYTES, "epilogue arrays");
+// (delta) the b-side rows' share of db, kept apart so that those rows run beside the dense terms; it also gives
+// their share of dGam (times b)
+constexpr uint32_t DB2 = 0;
+static_assert(PB + 64 * kES * 4 <= DC && DG + 64 * kES * 4 <= BYTES && DB2 + 64 * kES * 4 <= SEG, "epilogue arrays");
 }  // namespace gl
 
 // The delta front's results that the gradient pass reuses, per chunk (byte offsets), written by the prep pass or
@@ -3049,30 +3052,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 }
             }
         }
-        // segment rows (TMEM lanes 0..95): dB1[seg][i] times the column factor
-        if (trow < 96) {
-            const int I = trow < 16 ? 1 : (trow < 48 ? 2 : 3), s = trow - seg_base(I);
-            const float Gref = S.G[16 * I - 1], Gs = S.G[s];
-#pragma unroll 1
-            for (int h2 = 0; h2 < 2; h2++) {
-                const int c0 = 32 * wh + 16 * h2;
-                float v[16];
-                tmem_ld16(c.tl + 256 + c0, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e4 = 0; e4 < 16; e4 += 4) {
-                    float o[4];
-#pragma unroll
-                    for (int k = 0; k < 4; k++) o[k] = v[e4 + k] * fast_exp2(S.A2[c0 + e4 + k] * (Gref - Gs));
-                    *reinterpret_cast<float4*>(SEGv + trow * gl::kES + c0 + e4) = make_float4(o[0], o[1], o[2], o[3]);
-                }
-            }
-        }
-        bar_all();
         if (DELTA && isK) {
-            // the b-side rows' terms of dc, dg; and the rest of dbeta,
-            // dbeta_t = sum_j dR V - sum_i Btil (dR S^T) - sum_{s<t} (dR U^T) K   (dMm = -dR U^T),
-            // whose factors exp(Gam_t) are the same
+            // the b-side rows' share of db (into DB2; of dGam, b times it), beside the dense terms; and the rest of
+            // dbeta, dbeta_t = sum_j dR V - sum_i Btil (dR S^T) - sum_{s<t} (dR U^T) K   (dMm = -dR U^T), whose
+            // factors exp(Gam_t) are the same
+            float* DB2 = fptr(X, gl::DB2);
             const int I = tt >> 4;
             const float Gt = S.G[tt], Gref = I >= 1 ? S.G[16 * I - 1] : 0.f, bet = S.beta[tt];
             float part = 0.f;
@@ -3092,10 +3076,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 ld16_bf16(sB, tt, cg, bv);
 #pragma unroll
                 for (int e4 = 0; e4 < 16; e4 += 4) {
-                    const int at = tt * gl::kES + c0 + e4;
-                    float4 xb = *reinterpret_cast<const float4*>(DB + at);
-                    float4 xg = *reinterpret_cast<const float4*>(DG + at);
-                    float ob[4] = {xb.x, xb.y, xb.z, xb.w}, og[4] = {xg.x, xg.y, xg.z, xg.w};
+                    float ob[4];
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
                         const int e = e4 + k;
@@ -3103,19 +3084,38 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                         const float Et = fast_exp2(a2 * Gt);
                         const float f1 = I >= 1 ? fast_exp2(a2 * (Gt - Gref)) : 0.f;
                         const float dbt = -bet * drs[e];   // dBtil
-                        ob[k] += dbt * Et + da1[e] * f1;
-                        og[k] += dbt * bv[e] * Et + da1[e] * f1 * bv[e];
+                        ob[k] = dbt * Et + da1[e] * f1;
                         part -= bv[e] * Et * drs[e];
                         if (c0 + e < tt) part -= dru[e] * kv[e];
                     }
-                    *reinterpret_cast<float4*>(DB + at) = make_float4(ob[0], ob[1], ob[2], ob[3]);
-                    *reinterpret_cast<float4*>(DG + at) = make_float4(og[0], og[1], og[2], og[3]);
+                    *reinterpret_cast<float4*>(DB2 + tt * gl::kES + c0 + e4) = make_float4(ob[0], ob[1], ob[2], ob[3]);
                 }
             }
             S.rs[1][wh][tt] = part;
-        } else if (c.r < 64) {
+        }
+        bar_all();
+        if (c.r < 64) {
             // column sums over tokens of dBhat Bhat (fixed order: four interleaved chains, then their sum)
             S.colsum[0][c.r] = sum64_fixed(PB + c.r, gl::kES);
+        }
+        // segment rows (TMEM lanes 0..95): dB1[seg][i] times the column factor
+        if (trow < 96) {
+            const int I = trow < 16 ? 1 : (trow < 48 ? 2 : 3), s = trow - seg_base(I);
+            const float Gref = S.G[16 * I - 1], Gs = S.G[s];
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; h2++) {
+                const int c0 = 32 * wh + 16 * h2;
+                float v[16];
+                tmem_ld16(c.tl + 256 + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e4 = 0; e4 < 16; e4 += 4) {
+                    float o[4];
+#pragma unroll
+                    for (int k = 0; k < 4; k++) o[k] = v[e4 + k] * fast_exp2(S.A2[c0 + e4 + k] * (Gref - Gs));
+                    *reinterpret_cast<float4*>(SEGv + trow * gl::kES + c0 + e4) = make_float4(o[0], o[1], o[2], o[3]);
+                }
+            }
         }
         bar_all();
         CB_STAMP(1, 12);
@@ -3139,15 +3139,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 const float4 c4 = *reinterpret_cast<const float4*>(DC + t * gl::kES + nch);
                 const float4 b4 = *reinterpret_cast<const float4*>(DB + t * gl::kES + nch);
                 const float4 g4 = *reinterpret_cast<const float4*>(DG + t * gl::kES + nch);
+                const float4 k4 = DELTA ? *reinterpret_cast<const float4*>(fptr(X, gl::DB2) + t * gl::kES + nch)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                 const float dcr[4] = {c4.x, c4.y, c4.z, c4.w}, dbr[4] = {b4.x, b4.y, b4.z, b4.w};
-                const float dgr[4] = {g4.x, g4.y, g4.z, g4.w};
+                const float dgr[4] = {g4.x, g4.y, g4.z, g4.w}, dbk[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
                     const int i = nch + e, k = 4 * ti + e;
                     const float seg = sg[e];
                     dcv[e] = dcr[e] + nc[k];
-                    dbv[e] = dbr[e] + seg + nb[k];
-                    float gam = dgr[e] - bv4[e] * seg + ng[k];
+                    dbv[e] = dbr[e] + dbk[e] + seg + nb[k];
+                    float gam = dgr[e] + bv4[e] * dbk[e] - bv4[e] * seg + ng[k];
                     if (t == 63) {
                         const float sdi = S.sd[0][i] + S.sd[1][i] + S.sd[2][i] + S.sd[3][i];
                         gam += S.colsum[0][i] + sdi * c.KT->EC[i];
