@@ -2721,14 +2721,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         } else {
             // dU -> hi/lo [s][j] (MN-major B)
             if (!isK) {
-#pragma unroll 1
-                for (int h2 = 0; h2 < 2; h2++) {
-                    const int cg = 2 * wh + h2;
-                    float v[16];
-                    tmem_ld16(c.tl + 288 + 16 * cg, v);
-                    tmem_wait_ld();
-                    st16_split(X + gl::DU, X + gl::DU + 8192, tt, cg, v);
-                }
+                float v0[16], v1[16];   // both column groups in one TMEM round trip
+                tmem_ld16(c.tl + 288 + 32 * wh, v0);
+                tmem_ld16(c.tl + 288 + 32 * wh + 16, v1);
+                tmem_wait_ld();
+                st16_split(X + gl::DU, X + gl::DU + 8192, tt, 2 * wh, v0);
+                st16_split(X + gl::DU, X + gl::DU + 8192, tt, 2 * wh + 1, v1);
             }
             smem_to_tc();
             // Z = dU - N^T dU (accumulated onto dU)
@@ -2741,14 +2739,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             }
             if (!mma_wait(c, p, 10)) break;
             if (!isK) {
-#pragma unroll 1
-                for (int h2 = 0; h2 < 2; h2++) {
-                    const int cg = 2 * wh + h2;
-                    float v[16];
-                    tmem_ld16(c.tl + 288 + 16 * cg, v);
-                    tmem_wait_ld();
-                    st16_split(X + gl::Z, X + gl::Z + 8192, tt, cg, v);
-                }
+                float v0[16], v1[16];   // both column groups in one TMEM round trip
+                tmem_ld16(c.tl + 288 + 32 * wh, v0);
+                tmem_ld16(c.tl + 288 + 32 * wh + 16, v1);
+                tmem_wait_ld();
+                st16_split(X + gl::Z, X + gl::Z + 8192, tt, 2 * wh, v0);
+                st16_split(X + gl::Z, X + gl::Z + 8192, tt, 2 * wh + 1, v1);
             }
             smem_to_tc();
             // dR = Dinv^T Z (TMEM 352; lanes 64..127 hold a copy)
@@ -2765,12 +2761,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
             {
                 const float bet = S.beta[tt];
                 float part = 0.f;
-#pragma unroll 1
+                float vb[2][16];   // both column groups in one TMEM round trip
+                tmem_ld16(c.tl + 352 + 32 * wh, vb[0]);
+                tmem_ld16(c.tl + 352 + 32 * wh + 16, vb[1]);
+                tmem_wait_ld();
+#pragma unroll
                 for (int h2 = 0; h2 < 2; h2++) {
                     const int cg = 2 * wh + h2, c0 = 16 * cg;
-                    float v[16];
-                    tmem_ld16(c.tl + 352 + c0, v);
-                    tmem_wait_ld();
+                    const float (&v)[16] = vb[h2];
                     if (!isK) {
                         st16_split(X + gl::DOR + 8192, X + gl::ZR + 8192, tt, cg, v);
                         if (tt < L) {
@@ -3102,12 +3100,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
         if (trow < 96) {
             const int I = trow < 16 ? 1 : (trow < 48 ? 2 : 3), s = trow - seg_base(I);
             const float Gref = S.G[16 * I - 1], Gs = S.G[s];
-#pragma unroll 1
+            float vb[2][16];   // both column groups in one TMEM round trip
+            tmem_ld16(c.tl + 256 + 32 * wh, vb[0]);
+            tmem_ld16(c.tl + 256 + 32 * wh + 16, vb[1]);
+            tmem_wait_ld();
+#pragma unroll
             for (int h2 = 0; h2 < 2; h2++) {
                 const int c0 = 32 * wh + 16 * h2;
-                float v[16];
-                tmem_ld16(c.tl + 256 + c0, v);
-                tmem_wait_ld();
+                const float (&v)[16] = vb[h2];
 #pragma unroll
                 for (int e4 = 0; e4 < 16; e4 += 4) {
                     float o[4];
