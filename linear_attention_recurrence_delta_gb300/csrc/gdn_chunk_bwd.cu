@@ -2900,6 +2900,34 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                 kl[e] = c.KT->KL[nJ][nch + e];
             }
             if (!S.unsafe) {
+                // column side first: its three sums fold into dr at once, so that only dr (not nc, nb) is live
+                // through the row side
+                float dr[16];
+                {
+                    float cP[16], cK[16], cX[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e++) cP[e] = cK[e] = cX[e] = 0.f;
+#pragma unroll 1
+                    for (int j = 0; j < 2; j++)
+                        near_cols_rev<DELTA, false>(NQ, NK, c.ALPHA, sC, sB, tl0, 16 * nJ, sg0 + j, nch, ku, cP, cK);
+                    if (!up) {
+#pragma unroll 1
+                        for (int j = 0; j < 2; j++)
+                            near_cols_rev<DELTA, true>(NQ, NK, c.ALPHA, sC, sB, tl0, 16 * nJ, 2 + j, nch, ku, cX, nullptr);
+                    }
+#pragma unroll
+                    for (int ti = 0; ti < 4; ti++) {
+                        const int t = nt0 + ti;
+                        const float dGa = S.G[t] - S.G[8 * (t >> 3) + 3];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const int k = 4 * ti + e;
+                            const float ai = fast_exp2(-S.A2[nch + e] * dGa);
+                            const float cx = up ? 0.f : ai * kl[e];   // KL / alpha_t
+                            dr[k] = ai * (cP[k] + cK[k]) + cx * cX[k];
+                        }
+                    }
+                }
                 {
                     float rP[16], rK[16], rPx[16], rKx[16];
 #pragma unroll
@@ -2915,41 +2943,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_grad_kernel(const __grid_co
                     for (int ti = 0; ti < 4; ti++) {
                         const float4 a4 = *reinterpret_cast<const float4*>(c.ALPHA + (nt0 + ti) * kAS + nch);
                         const float al[4] = {a4.x, a4.y, a4.z, a4.w};
+                        float cv[4], bv[4];
+                        ld4_bf16(sC, nt0 + ti, nch, cv);
+                        ld4_bf16(sB, nt0 + ti, nch, bv);
 #pragma unroll
                         for (int e = 0; e < 4; e++) {
                             const int k = 4 * ti + e;
                             const float ax = up ? al[e] * ku[e] : 0.f;   // alpha_t KU
                             nc[k] = al[e] * rP[k] + ax * rPx[k];
                             nb[k] = al[e] * rK[k] + ax * rKx[k];
+                            ng[k] = cv[e] * nc[k] + bv[e] * nb[k] - bv[e] * dr[k];
+                            nb[k] += dr[k];
                         }
-                    }
-                }
-                float cP[16], cK[16], cX[16];
-#pragma unroll
-                for (int e = 0; e < 16; e++) cP[e] = cK[e] = cX[e] = 0.f;
-#pragma unroll 1
-                for (int j = 0; j < 2; j++)
-                    near_cols_rev<DELTA, false>(NQ, NK, c.ALPHA, sC, sB, tl0, 16 * nJ, sg0 + j, nch, ku, cP, cK);
-                if (!up) {
-#pragma unroll 1
-                    for (int j = 0; j < 2; j++)
-                        near_cols_rev<DELTA, true>(NQ, NK, c.ALPHA, sC, sB, tl0, 16 * nJ, 2 + j, nch, ku, cX, nullptr);
-                }
-#pragma unroll
-                for (int ti = 0; ti < 4; ti++) {
-                    const int t = nt0 + ti;
-                    const float dGa = S.G[t] - S.G[8 * (t >> 3) + 3];
-                    float cv[4], bv[4];
-                    ld4_bf16(sC, t, nch, cv);
-                    ld4_bf16(sB, t, nch, bv);
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int k = 4 * ti + e;
-                        const float ai = fast_exp2(-S.A2[nch + e] * dGa);
-                        const float cx = up ? 0.f : ai * kl[e];   // KL / alpha_t
-                        const float dr = ai * (cP[k] + cK[k]) + cx * cX[k];
-                        ng[k] = cv[e] * nc[k] + bv[e] * nb[k] - bv[e] * dr;
-                        nb[k] += dr;
                     }
                 }
             } else {
